@@ -1,0 +1,137 @@
+"""Byte layout of the packed KIVI cache — oracle side.
+
+Written from the format specification in ``include/kvq.h`` (section "Grouped
+region layout"); it shares no code with the CUDA library. The layout is this
+library's own choice (the pages fix the codes and their meaning, not their
+placement in memory).
+
+Per (batch, kv head, group of 32 tokens) there are four records:
+
+* key codes   : 32 lanes x W words (W = D/16 at 2 bits, D/8 at 4 bits), u32
+* key meta    : (D/16) x 4 records of 16 bytes:
+                {s[d0], s[d0+1], s[d0+8], s[d0+9], z[d0], z[d0+1], z[d0+8], z[d0+9]}
+                (fp16) with d0 = 16*ks + 2*tig, record index ks*4 + tig
+* value codes : 32 lanes x W words, u32
+* value meta  : 4 x 16 bytes of scales then 4 x 16 bytes of zeros; record tig
+                holds tokens {2tig, 2tig+1, 8+2tig, 9+2tig, 16+2tig, 17+2tig,
+                24+2tig, 25+2tig}
+
+Code words. A lane is ``lane = 4*g + tig`` (g in 0..7, tig in 0..3). Each
+32-bit word carries codes for one pair of elements in its two 16-bit halves
+(low half: first element of the pair, high half: second element). For a
+pair ``(ks, r, nt)``:
+
+* keys   : elements are channels ``d0 = 16*ks + 8*r + 2*tig`` and ``d0+1`` of
+           token ``8*nt + g`` (nt in 0..3, ks in 0..D/16-1);
+* values : elements are tokens ``t0 = 16*ks + 8*r + 2*tig`` and ``t0+1`` of
+           channel ``8*nt + g`` (nt in 0..D/8-1, ks in 0..1).
+
+With ``NQ`` = 1 for keys and D/32 for values:
+
+* 2 bits: word ``u = ks*NQ + nt//4``, field ``f = 4*r + nt%4`` at bits
+  ``[2f, 2f+2)`` of each half;
+* 4 bits: word ``u = (2*ks + r)*NQ + nt//4``, field ``f = nt%4`` at bits
+  ``[4f, 4f+4)`` of each half.
+
+Word ``u`` of lane ``lane`` is stored at u32 index ``(u//4)*128 + lane*4 + u%4``.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+GROUP = 32
+
+
+def code_words_per_lane(head_dim: int, bits: int) -> int:
+    return head_dim // 16 if bits == 2 else head_dim // 8
+
+
+def _word_address(lane: int, u: int) -> int:
+    return (u // 4) * 128 + lane * 4 + (u % 4)
+
+
+def _place(words, lane, u, f, bits, lo_code, hi_code):
+    shift = bits * f
+    words[..., _word_address(lane, u)] |= (lo_code.astype(np.uint32) << shift) | (hi_code.astype(np.uint32) << (16 + shift))
+
+
+def pack_key_codes(codes: np.ndarray, bits: int) -> np.ndarray:
+    """codes uint8 ``[..., 32, D]`` (token, channel) -> uint8 ``[..., 32*W*4]``."""
+    *lead, t, d = codes.shape
+    assert t == GROUP
+    w = code_words_per_lane(d, bits)
+    words = np.zeros((*lead, 32 * w), np.uint32)
+    for lane in range(32):
+        g, tig = lane // 4, lane % 4
+        for ks in range(d // 16):
+            for r in range(2):
+                d0 = 16 * ks + 8 * r + 2 * tig
+                for nt in range(4):
+                    tok = 8 * nt + g
+                    if bits == 2:
+                        u, f = ks, 4 * r + nt % 4
+                    else:
+                        u, f = 2 * ks + r, nt % 4
+                    _place(words, lane, u, f, bits, codes[..., tok, d0], codes[..., tok, d0 + 1])
+    return words.view(np.uint8).reshape(*lead, -1)
+
+
+def pack_value_codes(codes: np.ndarray, bits: int) -> np.ndarray:
+    """codes uint8 ``[..., 32, D]`` (token, channel) -> uint8 ``[..., 32*W*4]``."""
+    *lead, t, d = codes.shape
+    assert t == GROUP
+    w = code_words_per_lane(d, bits)
+    nq = d // 32
+    words = np.zeros((*lead, 32 * w), np.uint32)
+    for lane in range(32):
+        g, tig = lane // 4, lane % 4
+        for ks in range(2):
+            for r in range(2):
+                t0 = 16 * ks + 8 * r + 2 * tig
+                for nt in range(d // 8):
+                    ch = 8 * nt + g
+                    if bits == 2:
+                        u, f = ks * nq + nt // 4, 4 * r + nt % 4
+                    else:
+                        u, f = (2 * ks + r) * nq + nt // 4, nt % 4
+                    _place(words, lane, u, f, bits, codes[..., t0, ch], codes[..., t0 + 1, ch])
+    return words.view(np.uint8).reshape(*lead, -1)
+
+
+def pack_key_meta(scale16: np.ndarray, zero16: np.ndarray) -> np.ndarray:
+    """scale/zero fp16 ``[..., D]`` -> uint8 ``[..., 4*D]``."""
+    *lead, d = scale16.shape
+    out = np.zeros((*lead, d // 16, 4, 8), np.uint16)
+    s, z = scale16.view(np.uint16), zero16.view(np.uint16)
+    for ks in range(d // 16):
+        for tig in range(4):
+            d0 = 16 * ks + 2 * tig
+            chans = [d0, d0 + 1, d0 + 8, d0 + 9]
+            for j, c in enumerate(chans):
+                out[..., ks, tig, j] = s[..., c]
+                out[..., ks, tig, 4 + j] = z[..., c]
+    return out.view(np.uint8).reshape(*lead, -1)
+
+
+def pack_value_meta(scale16: np.ndarray, zero16: np.ndarray) -> np.ndarray:
+    """scale/zero fp16 ``[..., 32]`` (per token) -> uint8 ``[..., 128]``."""
+    *lead, t = scale16.shape
+    assert t == GROUP
+    out = np.zeros((*lead, 2, 4, 8), np.uint16)
+    s, z = scale16.view(np.uint16), zero16.view(np.uint16)
+    for tig in range(4):
+        toks = [2 * tig, 2 * tig + 1, 8 + 2 * tig, 9 + 2 * tig, 16 + 2 * tig, 17 + 2 * tig, 24 + 2 * tig, 25 + 2 * tig]
+        for j, tk in enumerate(toks):
+            out[..., 0, tig, j] = s[..., tk]
+            out[..., 1, tig, j] = z[..., tk]
+    return out.view(np.uint8).reshape(*lead, -1)
+
+
+def pack_cache(cache) -> dict:
+    """All four grouped records of an ``oracle.kivi.KiviCache``: uint8 ``[B, H, ng, bytes]``."""
+    return {
+        "k_codes": pack_key_codes(cache.k_codes, cache.k_bits),
+        "k_meta": pack_key_meta(cache.k_scale, cache.k_zero),
+        "v_codes": pack_value_codes(cache.v_codes, cache.v_bits),
+        "v_meta": pack_value_meta(cache.v_scale, cache.v_zero),
+    }
