@@ -1,0 +1,245 @@
+/*
+ * kvq.h — quantized KV cache and decode attention over it, for NVIDIA GB300 (sm_103a).
+ *
+ * C ABI of libkvq.so. Plain pointers and sizes only; every device pointer is
+ * memory the caller allocated (cudaMalloc, a PyTorch tensor, a pool). The
+ * library never allocates, never synchronizes and never prints: each call
+ * validates its arguments on the host, enqueues kernels on `stream` (a
+ * cudaStream_t passed as void*, NULL = the legacy default stream) and returns.
+ * On any validation error nothing is enqueued and the cache descriptor is left
+ * unchanged. Calls that work on one cache must be issued on one stream.
+ *
+ * Sources (the pages this library implements):
+ *  [KIVI]  "4.4 KV Cache 量化：KIVI 2-bit 与 FP8 KV Cache" (aiinfraguide),
+ *          section 3 (grouped + residual structure, per-channel keys,
+ *          per-token values, group 32, residual 128) and section 5 (FP8 E4M3).
+ *  [CSDN]  "大模型量化从0到1（十三）：KV Cache 量化", section 2 (attention),
+ *          section 4 (cache shape [B, H_kv, S, D]), section 5 (GQA), section 10
+ *          (affine and FP8 quantization formulas, per-tensor granularity),
+ *          section 12 (paged cache blocks).
+ *  [YUN]   "LLM推理加速KV Cache量化压缩实战方案" (yunthe), "自定义KV Cache量化的实现
+ *          路径": per-tensor FP8 scale = max|x| / 448.
+ *
+ * Scalar conventions: fp16 tensors are passed as uint16_t* (IEEE binary16 bit
+ * patterns); all tensors are contiguous and row-major in the order given.
+ * Every device buffer must start on a 256-byte boundary (KVQ_ERR_ALIGN).
+ * GQA: query head hq uses kv head hq / (q_heads / kv_heads).
+ */
+#ifndef KVQ_H_
+#define KVQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define KVQ_API __attribute__((visibility("default")))
+#else
+#define KVQ_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  KVQ_OK = 0,
+  KVQ_ERR_NULL = 1,        /* a required pointer is NULL */
+  KVQ_ERR_ARG = 2,         /* an argument is out of its documented range */
+  KVQ_ERR_SHAPE = 3,       /* shapes disagree (e.g. q_heads % kv_heads != 0) */
+  KVQ_ERR_CAPACITY = 4,    /* the cache or the pool cannot hold the tokens */
+  KVQ_ERR_WORKSPACE = 5,   /* workspace NULL or smaller than the size query */
+  KVQ_ERR_UNSUPPORTED = 6, /* a valid but unimplemented combination */
+  KVQ_ERR_CUDA = 7,        /* a kernel launch failed (cudaGetLastError) */
+  KVQ_ERR_TIMEOUT = 8,     /* a device wait gave up (see the workspace status word) */
+  KVQ_ERR_ALIGN = 9        /* a device buffer is not 256-byte aligned */
+} kvq_status;
+
+KVQ_API const char* kvq_status_string(kvq_status s);
+
+/* ------------------------------------------------------------------------ */
+/* KIVI 2/4-bit cache [KIVI section 3]                                       */
+/* ------------------------------------------------------------------------ */
+
+/* Shape and scheme of one layer's cache.
+ *   batch, kv_heads, q_heads : B, H_kv, H_q (H_q % H_kv == 0, H_q / H_kv <= 8)
+ *   head_dim                 : D, 64 or 128
+ *   k_bits, v_bits           : 2 or 4
+ *   group_size               : must be 32 (tokens per quantization group)
+ *   residual_len             : R, 0 or a positive multiple of 32 (the newest R
+ *                              tokens stay fp16; R = 0 keeps at most 31 tokens
+ *                              in a 32-slot fp16 stage between flushes)
+ *   max_tokens               : capacity in tokens per sequence               */
+typedef struct {
+  int32_t batch, kv_heads, q_heads, head_dim;
+  int32_t k_bits, v_bits, group_size, residual_len, max_tokens;
+} kivi_config;
+
+/* Host-side descriptor of a cache whose six device buffers the caller owns.
+ * n_grouped (a multiple of 32) and n_resid are the tokens held in the grouped
+ * region and in the fp16 window; they change only through the calls below. */
+typedef struct {
+  kivi_config cfg;
+  uint8_t* k_codes;  /* [B, H_kv, groups_cap, 32*D*k_bits/8]                 */
+  uint8_t* k_meta;   /* [B, H_kv, groups_cap, 4*D]                           */
+  uint8_t* v_codes;  /* [B, H_kv, groups_cap, 32*D*v_bits/8]                 */
+  uint8_t* v_meta;   /* [B, H_kv, groups_cap, 128]                           */
+  uint16_t* k_res;   /* fp16 [B, H_kv, res_cap, D], oldest token first      */
+  uint16_t* v_res;   /* fp16 [B, H_kv, res_cap, D]                          */
+  int32_t groups_cap; /* ceil(max_tokens / 32)                               */
+  int32_t res_cap;    /* R, or 32 when R = 0                                 */
+  int32_t n_grouped;
+  int32_t n_resid;
+} kivi_cache;
+
+/* Grouped region layout (per batch row, kv head and group g of 32 tokens,
+ * tokens 32g .. 32g+31). Codes, scales and zero points are those of [KIVI]
+ * section 3 with the affine form of [CSDN] section 10, computed in IEEE fp32:
+ *   per group of values x (keys: one channel over the 32 tokens; values: one
+ *   token over its D channels): mn = min x (a zero min is stored as +0),
+ *   mx = max x, s = fp16(fl32(fl32(mx - mn) / (2^b - 1))), z = mn,
+ *   code = clamp(rint_even(fl32(fl32(x - z) / s)), 0, 2^b - 1), 0 if s == 0;
+ *   dequantized value = code * s + z.
+ * Inputs must be finite.
+ *
+ * Key meta (4*D bytes): D/16 x 4 records of 16 bytes, record ks*4 + tig holds
+ *   fp16 {s[d0], s[d0+1], s[d0+8], s[d0+9], z[d0], z[d0+1], z[d0+8], z[d0+9]},
+ *   d0 = 16*ks + 2*tig.
+ * Value meta (128 bytes): 4 records of fp16 scales, then 4 of zero points;
+ *   record tig holds tokens {2tig, 2tig+1, 8+2tig, 9+2tig, 16+2tig, 17+2tig,
+ *   24+2tig, 25+2tig}.
+ * Codes (32*D*b/8 bytes each for keys and values): 32 lanes x W 32-bit words
+ *   (W = D/16 at 2 bits, D/8 at 4 bits); lane = 4*g + tig. Each word holds a
+ *   pair of elements in its 16-bit halves (low half: first element):
+ *     keys  : channels d0 = 16*ks + 8*r + 2*tig and d0+1 of token 8*nt + g
+ *             (nt < 4, ks < D/16);
+ *     values: tokens t0 = 16*ks + 8*r + 2*tig and t0+1 of channel 8*nt + g
+ *             (nt < D/8, ks < 2).
+ *   With NQ = 1 (keys) or D/32 (values):
+ *     2 bits: word u = ks*NQ + nt/4, field f = 4*r + nt%4 at bits [2f, 2f+2);
+ *     4 bits: word u = (2*ks + r)*NQ + nt/4, field f = nt%4 at bits [4f, 4f+4).
+ *   Word u of a lane is stored at 32-bit index (u/4)*128 + lane*4 + u%4.
+ *   (These are the operand fragments of the mma.sync m16n8k16 tensor-core
+ *   instruction, so that the decode kernel loads each lane's codes with
+ *   16-byte shared-memory loads and turns them into operands with shifts and
+ *   masks only.)                                                            */
+
+/* Byte sizes of the six buffers in the order k_codes, k_meta, v_codes,
+ * v_meta, k_res, v_res. */
+KVQ_API kvq_status kivi_cache_sizes(const kivi_config* cfg, size_t bytes_out[6]);
+
+/* Fill a descriptor for caller buffers bufs[6] (order as above, each at least
+ * the size kivi_cache_sizes reports). The cache starts empty. No device work. */
+KVQ_API kvq_status kivi_cache_init(kivi_cache* cache, const kivi_config* cfg, void* const bufs[6]);
+
+/* Prefill [KIVI section 3.2]: start the cache from seq_len tokens.
+ *   k, v : device fp16 [B, H_kv, seq_len, D]
+ * With R > 0 the oldest 32*ceil(max(seq_len - R, 0)/32) tokens are quantized
+ * into groups and the rest (at most R) are copied to the fp16 window; with
+ * R = 0 the oldest 32*floor(seq_len/32) tokens are quantized. Any previous
+ * content is discarded. KVQ_ERR_CAPACITY if seq_len > max_tokens. */
+KVQ_API kvq_status kv_quant_prefill(kivi_cache* cache, const uint16_t* k, const uint16_t* v,
+                            int32_t seq_len, void* stream);
+
+/* Append one decode step's token [KIVI section 3.2]: k_new, v_new device fp16
+ * [B, H_kv, D]. If the window is full (n_resid == res_cap) it is flushed first;
+ * with R = 0 the 32-slot stage is flushed right after the append that fills
+ * it. KVQ_ERR_CAPACITY if the cache already holds max_tokens tokens. */
+KVQ_API kvq_status kv_append_token(kivi_cache* cache, const uint16_t* k_new, const uint16_t* v_new,
+                           void* stream);
+
+/* Flush [KIVI section 3.2]: quantize the oldest 32*floor(n_resid/32) window
+ * tokens into groups and move the remaining n_resid % 32 tokens to the front
+ * of the window. A no-op when n_resid < 32. */
+KVQ_API kvq_status kv_flush_residual(kivi_cache* cache, void* stream);
+
+/* Workspace for kv_decode_attention / fp8_decode_attention with this shape
+ * (split-K partials). Its first 256 bytes hold a status word (uint32 at
+ * offset 0) that kernels OR error bits into: bit 0 = a device wait timed out.
+ * Zero the workspace once after allocating it; the status stays sticky. */
+KVQ_API size_t kv_decode_workspace_bytes(const kivi_config* cfg);
+
+/* Decode attention [CSDN sections 2, 5] for one new token per sequence:
+ *   out[b, hq, :] = softmax(q[b, hq, :] . K_hat^T * softmax_scale) V_hat
+ * over the grouped tokens followed by the window tokens of kv head
+ * hq / (H_q/H_kv), where K_hat, V_hat are the dequantized values.
+ *   q   : device fp16 [B, H_q, D]
+ *   out : device [B, H_q, D], fp32 if out_fp32 != 0, else fp16
+ *   softmax_scale <= 0 selects 1/sqrt(D)
+ *   ws  : workspace of at least kv_decode_workspace_bytes(cfg) bytes
+ * Split-K ("flash-decoding"): token chunks of each (b, kv head) go to
+ * separate thread blocks, each writes (m, l, o) partials, and a log-sum-exp
+ * merge kernel combines them. Dequantization happens in registers.
+ * KVQ_ERR_ARG if the cache is empty. */
+KVQ_API kvq_status kv_decode_attention(const kivi_cache* cache, const uint16_t* q, void* out,
+                               int32_t out_fp32, float softmax_scale, void* ws,
+                               size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* FP8 E4M3 paged cache [KIVI section 5, CSDN section 10, YUN]               */
+/* ------------------------------------------------------------------------ */
+
+/* E4M3: 1 sign, 4 exponent (bias 7), 3 mantissa bits; largest finite 448.
+ * Encoding rounds to nearest even; magnitudes >= 448 (and infinities)
+ * saturate to +-448; NaN encodes as 0x7F.
+ *
+ * Pool layout: pool[num_blocks, H_kv, block_size * D] bytes; logical token t
+ * of sequence b lives in physical block block_table[b * max_blocks + t/bs],
+ * row t % bs ([CSDN] section 12). Within one (block, kv head), block_size must
+ * be 16 and the 16*D bytes are stored in mma.sync fragment order (lane =
+ * 4*g + tig, D/2 bytes per lane; byte p of lane l's stream is stored at byte
+ * ((p/16)*32 + l)*16 + p%16):
+ *   keys   (value_layout = 0): byte pair i = (nt*(D/16) + ks)*2 + r of a lane
+ *          holds channels d0 = 16*ks + 8*r + 2*tig, d0+1 of token 8*nt + g
+ *          (nt < 2);
+ *   values (value_layout = 1): byte pair i = nt*2 + r holds tokens
+ *          t0 = 8*r + 2*tig, t0+1 of channel 8*nt + g (nt < D/8).
+ * Rows of a block past the end of the sequence are written as zero bytes. */
+
+/* Workspace of fp8_kv_quantize: per-block amax partials. */
+KVQ_API size_t fp8_quantize_workspace_bytes(int32_t batch, int32_t kv_heads, int32_t seq_len, int32_t head_dim);
+
+/* Quantize one tensor (K or V) of one layer into the paged pool.
+ *   x           : device fp16 [B, H_kv, seq_len, D]
+ *   block_table : device int32 [B, max_blocks]; entries < num_blocks
+ *   pool        : device uint8 [num_blocks, H_kv, 16*D]
+ *   scale       : device float32 scalar. static_scale == 0: written with
+ *                 fl32(amax/448) (amax = max|x| over the whole tensor, scale 1
+ *                 if amax == 0) [YUN]; static_scale != 0: read as given
+ *                 (e.g. 1.0, the no-calibration route of [KIVI] section 6.1).
+ *   value_layout: 0 for keys, 1 for values (the in-block order above)
+ * byte = E4M3(fl32(x / scale)). Block-table entries outside [0, num_blocks)
+ * are skipped (nothing is written for that block). */
+KVQ_API kvq_status fp8_kv_quantize(const uint16_t* x, int32_t batch, int32_t kv_heads, int32_t seq_len,
+                           int32_t head_dim, const int32_t* block_table, int32_t max_blocks,
+                           int32_t block_size, int32_t num_blocks, uint8_t* pool, float* scale,
+                           int32_t static_scale, int32_t value_layout, void* ws, size_t ws_bytes,
+                           void* stream);
+
+/* Workspace of fp8_decode_attention (split-K partials + status word, as for
+ * kv_decode_workspace_bytes). */
+KVQ_API size_t fp8_decode_workspace_bytes(int32_t batch, int32_t q_heads, int32_t head_dim);
+
+/* Decode attention over the FP8 paged cache:
+ *   out[b, hq] = softmax(q . (k_scale * K)^T * softmax_scale) (v_scale * V)
+ * over tokens 0 .. seq_lens[b]-1 of kv head hq / (H_q/H_kv).
+ *   q        : device fp16 [B, H_q, D];  out: device [B, H_q, D] (fp32 or fp16)
+ *   k_pool, v_pool : pools written by fp8_kv_quantize (value_layout 0 and 1)
+ *   k_scale, v_scale : device float32 scalars
+ *   seq_lens : device int32 [B], each in [1, max_seq_len]
+ * The host passes max_seq_len >= every seq_lens[b] (it sizes the grid) and
+ * max_seq_len <= max_blocks*16. Block-table entries must lie in
+ * [0, num_blocks); the kernels clamp them (and seq_lens) so that a bad table
+ * gives wrong numbers but never an access outside the pool or the table. */
+KVQ_API kvq_status fp8_decode_attention(const uint16_t* q, const uint8_t* k_pool, const uint8_t* v_pool,
+                                const float* k_scale, const float* v_scale,
+                                const int32_t* block_table, const int32_t* seq_lens,
+                                int32_t batch, int32_t q_heads, int32_t kv_heads, int32_t head_dim,
+                                int32_t block_size, int32_t max_blocks, int32_t num_blocks,
+                                int32_t max_seq_len, void* out, int32_t out_fp32,
+                                float softmax_scale, void* ws, size_t ws_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H_ */

@@ -73,7 +73,7 @@ def e4m3_encode(y: np.ndarray) -> np.ndarray:
 
 def amax(x16: np.ndarray) -> np.float32:
     """max |x| over a whole fp16 tensor (exact; NaN if any element is NaN)."""
-    return np.float32(np.max(np.abs(x16.astype(np.float32))))
+    return np.float32(np.max(np.abs(x16)))
 
 
 def dynamic_scale(x16: np.ndarray) -> np.float32:

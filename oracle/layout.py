@@ -135,3 +135,54 @@ def pack_cache(cache) -> dict:
         "v_codes": pack_value_codes(cache.v_codes, cache.v_bits),
         "v_meta": pack_value_meta(cache.v_scale, cache.v_zero),
     }
+
+
+# ---------------------------------------------------------------------------
+# FP8 paged blocks: byte order inside one (block, kv head) of 16 tokens x D
+# ---------------------------------------------------------------------------
+# From the pool specification in ``include/kvq.h``: each lane = 4*g + tig owns
+# D/2 bytes (D/4 byte pairs); byte p of lane l's stream is stored at byte
+# ((p//16)*32 + l)*16 + p%16 of the block.
+#   keys   : pair i = (nt*(D//16) + ks)*2 + r holds channels d0 = 16ks + 8r + 2tig
+#            and d0+1 of token 8nt + g (nt < 2);
+#   values : pair i = nt*2 + r holds tokens t0 = 8r + 2tig and t0+1 of channel
+#            8nt + g (nt < D/8).
+
+def fp8_block_order(head_dim: int, value_layout: int) -> np.ndarray:
+    """perm[storage_byte] = index into the natural row-major [16, D] block."""
+    d = head_dim
+    perm = np.full(16 * d, -1, np.int64)
+    for lane in range(32):
+        g, tig = lane // 4, lane % 4
+        for i in range(d // 4):
+            if value_layout:
+                nt, r = i // 2, i % 2
+                t0 = 8 * r + 2 * tig
+                elems = [(t0, 8 * nt + g), (t0 + 1, 8 * nt + g)]
+            else:
+                nt, rem = i // (d // 8), i % (d // 8)
+                ks, r = rem // 2, rem % 2
+                d0 = 16 * ks + 8 * r + 2 * tig
+                elems = [(8 * nt + g, d0), (8 * nt + g, d0 + 1)]
+            for e, (tok, ch) in enumerate(elems):
+                p = 2 * i + e
+                perm[((p // 16) * 32 + lane) * 16 + p % 16] = tok * d + ch
+    assert np.all(perm >= 0)
+    return perm
+
+
+def fp8_pack_pool(natural_pool: np.ndarray, value_layout: int) -> np.ndarray:
+    """[nb, H, 16, D] natural blocks -> [nb, H, 16*D] in fragment byte order."""
+    nb, h, bs, d = natural_pool.shape
+    assert bs == 16
+    perm = fp8_block_order(d, value_layout)
+    return natural_pool.reshape(nb, h, bs * d)[:, :, perm]
+
+
+def fp8_unpack_pool(packed_pool: np.ndarray, head_dim: int, value_layout: int) -> np.ndarray:
+    """Inverse of ``fp8_pack_pool``."""
+    nb, h, n = packed_pool.shape
+    perm = fp8_block_order(head_dim, value_layout)
+    out = np.empty_like(packed_pool)
+    out[:, :, perm] = packed_pool
+    return out.reshape(nb, h, 16, head_dim)

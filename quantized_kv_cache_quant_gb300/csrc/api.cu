@@ -1,0 +1,452 @@
+// C-ABI host layer of libkvq: argument validation, the streaming state machine
+// of the KIVI cache, split-K sizing, and kernel launches. Declared in kvq.h.
+#include <algorithm>
+#include <climits>
+#include <cmath>
+#include <cstdint>
+
+#include "kvq.h"
+#include "kvq_device.cuh"
+#include "kvq_internal.h"
+
+using kvq::kGroup;
+using kvq::kMaxSplits;
+using kvq::kWsHeader;
+
+namespace {
+
+constexpr int kAmaxBlocksMax = 4096;
+constexpr int kCtasPerSm = 4;       // resident decode blocks per SM the split count aims for
+constexpr int kMinUnitsPerSplit = 8;  // groups (or paged blocks) per split: two per warp
+
+bool aligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
+
+kvq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA; }
+
+int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
+
+kvq_status check_config(const kivi_config* c) {
+  if (c == nullptr) return KVQ_ERR_NULL;
+  if (c->batch <= 0 || c->kv_heads <= 0 || c->q_heads <= 0 || c->max_tokens <= 0) return KVQ_ERR_ARG;
+  if (c->batch > 65535 || c->kv_heads > 65535) return KVQ_ERR_UNSUPPORTED;
+  if (c->head_dim != 64 && c->head_dim != 128) return KVQ_ERR_UNSUPPORTED;
+  if ((c->k_bits != 2 && c->k_bits != 4) || (c->v_bits != 2 && c->v_bits != 4)) return KVQ_ERR_UNSUPPORTED;
+  if (c->group_size != kGroup) return KVQ_ERR_UNSUPPORTED;
+  if (c->residual_len < 0 || c->residual_len % kGroup != 0) return KVQ_ERR_ARG;
+  if (c->q_heads % c->kv_heads != 0) return KVQ_ERR_SHAPE;
+  if (c->q_heads / c->kv_heads > kvq::kMaxGqa) return KVQ_ERR_UNSUPPORTED;
+  return KVQ_OK;
+}
+
+int groups_cap_of(const kivi_config* c) { return ceil_div(c->max_tokens, kGroup); }
+int res_cap_of(const kivi_config* c) { return c->residual_len > 0 ? c->residual_len : kGroup; }
+
+void record_bytes(const kivi_config* c, size_t out[6]) {
+  const size_t bh = static_cast<size_t>(c->batch) * c->kv_heads;
+  const size_t groups = static_cast<size_t>(groups_cap_of(c));
+  const size_t d = static_cast<size_t>(c->head_dim);
+  out[0] = bh * groups * (32 * d * c->k_bits / 8);
+  out[1] = bh * groups * (4 * d);
+  out[2] = bh * groups * (32 * d * c->v_bits / 8);
+  out[3] = bh * groups * 128;
+  out[4] = bh * static_cast<size_t>(res_cap_of(c)) * d * 2;
+  out[5] = out[4];
+}
+
+kvq_status check_cache(const kivi_cache* cache) {
+  if (cache == nullptr) return KVQ_ERR_NULL;
+  const kvq_status st = check_config(&cache->cfg);
+  if (st != KVQ_OK) return st;
+  if (!cache->k_codes || !cache->k_meta || !cache->v_codes || !cache->v_meta || !cache->k_res || !cache->v_res)
+    return KVQ_ERR_NULL;
+  if (cache->groups_cap != groups_cap_of(&cache->cfg) || cache->res_cap != res_cap_of(&cache->cfg)) return KVQ_ERR_ARG;
+  if (cache->n_grouped < 0 || cache->n_grouped % kGroup != 0 || cache->n_resid < 0 || cache->n_resid > cache->res_cap)
+    return KVQ_ERR_ARG;
+  if (cache->n_grouped + cache->n_resid > cache->cfg.max_tokens) return KVQ_ERR_ARG;
+  return KVQ_OK;
+}
+
+// Quantize n whole groups from the head of the fp16 window into the grouped region.
+kvq_status flush_groups(kivi_cache* c, int n_tokens, cudaStream_t s) {
+  kvq::QuantGroupsArgs q{};
+  q.k_src = c->k_res;
+  q.v_src = c->v_res;
+  q.src_bh_stride = static_cast<long long>(c->res_cap) * c->cfg.head_dim;
+  q.src_tok0 = 0;
+  q.n_groups = n_tokens / kGroup;
+  q.dst_group0 = c->n_grouped / kGroup;
+  q.batch = c->cfg.batch;
+  q.kv_heads = c->cfg.kv_heads;
+  q.head_dim = c->cfg.head_dim;
+  q.k_bits = c->cfg.k_bits;
+  q.v_bits = c->cfg.v_bits;
+  q.groups_cap = c->groups_cap;
+  q.k_codes = c->k_codes;
+  q.k_meta = c->k_meta;
+  q.v_codes = c->v_codes;
+  q.v_meta = c->v_meta;
+  kvq_status st = from_cuda(kvq::launch_kivi_quantize(q, s));
+  if (st != KVQ_OK) return st;
+  const int rest = c->n_resid - n_tokens;
+  if (rest > 0) {  // rest < 32 <= n_tokens: source and destination rows do not overlap
+    kvq::CopyTokensArgs m{};
+    m.k_src = c->k_res;
+    m.v_src = c->v_res;
+    m.src_bh_stride = q.src_bh_stride;
+    m.src_tok0 = n_tokens;
+    m.k_dst = c->k_res;
+    m.v_dst = c->v_res;
+    m.dst_bh_stride = q.src_bh_stride;
+    m.dst_tok0 = 0;
+    m.n_tokens = rest;
+    m.bh = c->cfg.batch * c->cfg.kv_heads;
+    m.head_dim = c->cfg.head_dim;
+    st = from_cuda(kvq::launch_copy_tokens(m, s));
+    if (st != KVQ_OK) return st;
+  }
+  c->n_grouped += n_tokens;
+  c->n_resid = rest;
+  return KVQ_OK;
+}
+
+size_t decode_ws_bytes(int batch, int q_heads, int head_dim) {
+  return static_cast<size_t>(kWsHeader) +
+         static_cast<size_t>(batch) * q_heads * kMaxSplits * (static_cast<size_t>(head_dim) + 2) * sizeof(float);
+}
+
+// Number of splits for `units` work items per (b, kv head) and `pairs` pairs.
+int choose_splits(int units, int pairs, int max_splits) {
+  if (units <= 0) return 0;
+  const int target = kCtasPerSm * kvq::device_sm_count();
+  int splits = ceil_div(target, pairs);
+  splits = std::min(splits, std::max(1, ceil_div(units, kMinUnitsPerSplit)));
+  splits = std::max(1, std::min(splits, max_splits));
+  const int per = ceil_div(units, splits);
+  return ceil_div(units, per);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* kvq_status_string(kvq_status s) {
+  switch (s) {
+    case KVQ_OK: return "ok";
+    case KVQ_ERR_NULL: return "a required pointer is NULL";
+    case KVQ_ERR_ARG: return "an argument is out of range";
+    case KVQ_ERR_SHAPE: return "shapes disagree";
+    case KVQ_ERR_CAPACITY: return "capacity exceeded";
+    case KVQ_ERR_WORKSPACE: return "workspace missing or too small";
+    case KVQ_ERR_UNSUPPORTED: return "unsupported combination";
+    case KVQ_ERR_CUDA: return "CUDA launch failed";
+    case KVQ_ERR_TIMEOUT: return "a device wait timed out";
+    case KVQ_ERR_ALIGN: return "a device buffer is not 256-byte aligned";
+  }
+  return "unknown status";
+}
+
+kvq_status kivi_cache_sizes(const kivi_config* cfg, size_t bytes_out[6]) {
+  const kvq_status st = check_config(cfg);
+  if (st != KVQ_OK) return st;
+  if (bytes_out == nullptr) return KVQ_ERR_NULL;
+  record_bytes(cfg, bytes_out);
+  return KVQ_OK;
+}
+
+kvq_status kivi_cache_init(kivi_cache* cache, const kivi_config* cfg, void* const bufs[6]) {
+  if (cache == nullptr || bufs == nullptr) return KVQ_ERR_NULL;
+  const kvq_status st = check_config(cfg);
+  if (st != KVQ_OK) return st;
+  for (int i = 0; i < 6; ++i) {
+    if (bufs[i] == nullptr) return KVQ_ERR_NULL;
+    if (!aligned(bufs[i])) return KVQ_ERR_ALIGN;
+  }
+  kivi_cache c{};
+  c.cfg = *cfg;
+  c.k_codes = static_cast<uint8_t*>(bufs[0]);
+  c.k_meta = static_cast<uint8_t*>(bufs[1]);
+  c.v_codes = static_cast<uint8_t*>(bufs[2]);
+  c.v_meta = static_cast<uint8_t*>(bufs[3]);
+  c.k_res = static_cast<uint16_t*>(bufs[4]);
+  c.v_res = static_cast<uint16_t*>(bufs[5]);
+  c.groups_cap = groups_cap_of(cfg);
+  c.res_cap = res_cap_of(cfg);
+  c.n_grouped = 0;
+  c.n_resid = 0;
+  *cache = c;
+  return KVQ_OK;
+}
+
+kvq_status kv_quant_prefill(kivi_cache* cache, const uint16_t* k, const uint16_t* v, int32_t seq_len, void* stream) {
+  kvq_status st = check_cache(cache);
+  if (st != KVQ_OK) return st;
+  if (seq_len < 0) return KVQ_ERR_ARG;
+  if (seq_len > cache->cfg.max_tokens) return KVQ_ERR_CAPACITY;
+  if (seq_len > 0 && (k == nullptr || v == nullptr)) return KVQ_ERR_NULL;
+  if (seq_len > 0 && (!aligned(k) || !aligned(v))) return KVQ_ERR_ALIGN;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int R = cache->cfg.residual_len;
+  const int grouped = (R > 0) ? kGroup * ceil_div(std::max(seq_len - R, 0), kGroup) : kGroup * (seq_len / kGroup);
+  const int resid = seq_len - grouped;
+  kivi_cache c = *cache;
+  if (grouped > 0) {
+    kvq::QuantGroupsArgs q{};
+    q.k_src = k;
+    q.v_src = v;
+    q.src_bh_stride = static_cast<long long>(seq_len) * c.cfg.head_dim;
+    q.src_tok0 = 0;
+    q.n_groups = grouped / kGroup;
+    q.dst_group0 = 0;
+    q.batch = c.cfg.batch;
+    q.kv_heads = c.cfg.kv_heads;
+    q.head_dim = c.cfg.head_dim;
+    q.k_bits = c.cfg.k_bits;
+    q.v_bits = c.cfg.v_bits;
+    q.groups_cap = c.groups_cap;
+    q.k_codes = c.k_codes;
+    q.k_meta = c.k_meta;
+    q.v_codes = c.v_codes;
+    q.v_meta = c.v_meta;
+    st = from_cuda(kvq::launch_kivi_quantize(q, s));
+    if (st != KVQ_OK) return st;
+  }
+  if (resid > 0) {
+    kvq::CopyTokensArgs m{};
+    m.k_src = k;
+    m.v_src = v;
+    m.src_bh_stride = static_cast<long long>(seq_len) * c.cfg.head_dim;
+    m.src_tok0 = grouped;
+    m.k_dst = c.k_res;
+    m.v_dst = c.v_res;
+    m.dst_bh_stride = static_cast<long long>(c.res_cap) * c.cfg.head_dim;
+    m.dst_tok0 = 0;
+    m.n_tokens = resid;
+    m.bh = c.cfg.batch * c.cfg.kv_heads;
+    m.head_dim = c.cfg.head_dim;
+    st = from_cuda(kvq::launch_copy_tokens(m, s));
+    if (st != KVQ_OK) return st;
+  }
+  cache->n_grouped = grouped;
+  cache->n_resid = resid;
+  return KVQ_OK;
+}
+
+kvq_status kv_append_token(kivi_cache* cache, const uint16_t* k_new, const uint16_t* v_new, void* stream) {
+  kvq_status st = check_cache(cache);
+  if (st != KVQ_OK) return st;
+  if (k_new == nullptr || v_new == nullptr) return KVQ_ERR_NULL;
+  if (!aligned(k_new) || !aligned(v_new)) return KVQ_ERR_ALIGN;
+  if (cache->n_grouped + cache->n_resid + 1 > cache->cfg.max_tokens) return KVQ_ERR_CAPACITY;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  kivi_cache c = *cache;
+  if (c.n_resid == c.res_cap) {
+    st = flush_groups(&c, c.res_cap, s);
+    if (st != KVQ_OK) return st;
+  }
+  kvq::CopyTokensArgs m{};
+  m.k_src = k_new;
+  m.v_src = v_new;
+  m.src_bh_stride = c.cfg.head_dim;
+  m.src_tok0 = 0;
+  m.k_dst = c.k_res;
+  m.v_dst = c.v_res;
+  m.dst_bh_stride = static_cast<long long>(c.res_cap) * c.cfg.head_dim;
+  m.dst_tok0 = c.n_resid;
+  m.n_tokens = 1;
+  m.bh = c.cfg.batch * c.cfg.kv_heads;
+  m.head_dim = c.cfg.head_dim;
+  st = from_cuda(kvq::launch_copy_tokens(m, s));
+  if (st != KVQ_OK) return st;
+  c.n_resid += 1;
+  if (c.cfg.residual_len == 0 && c.n_resid == kGroup) {
+    st = flush_groups(&c, kGroup, s);
+    if (st != KVQ_OK) return st;
+  }
+  *cache = c;
+  return KVQ_OK;
+}
+
+kvq_status kv_flush_residual(kivi_cache* cache, void* stream) {
+  kvq_status st = check_cache(cache);
+  if (st != KVQ_OK) return st;
+  const int n = kGroup * (cache->n_resid / kGroup);
+  if (n == 0) return KVQ_OK;
+  kivi_cache c = *cache;
+  st = flush_groups(&c, n, static_cast<cudaStream_t>(stream));
+  if (st != KVQ_OK) return st;
+  *cache = c;
+  return KVQ_OK;
+}
+
+size_t kv_decode_workspace_bytes(const kivi_config* cfg) {
+  if (check_config(cfg) != KVQ_OK) return 0;
+  return decode_ws_bytes(cfg->batch, cfg->q_heads, cfg->head_dim);
+}
+
+kvq_status kv_decode_attention(const kivi_cache* cache, const uint16_t* q, void* out, int32_t out_fp32,
+                               float softmax_scale, void* ws, size_t ws_bytes, void* stream) {
+  kvq_status st = check_cache(cache);
+  if (st != KVQ_OK) return st;
+  if (q == nullptr || out == nullptr) return KVQ_ERR_NULL;
+  if (!aligned(q) || !aligned(out)) return KVQ_ERR_ALIGN;
+  if (ws == nullptr) return KVQ_ERR_WORKSPACE;
+  if (!aligned(ws)) return KVQ_ERR_ALIGN;
+  const kivi_config& cf = cache->cfg;
+  if (ws_bytes < decode_ws_bytes(cf.batch, cf.q_heads, cf.head_dim)) return KVQ_ERR_WORKSPACE;
+  if (cache->n_grouped + cache->n_resid == 0) return KVQ_ERR_ARG;
+  if (!(softmax_scale == softmax_scale) || std::isinf(softmax_scale)) return KVQ_ERR_ARG;
+  const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(cf.head_dim));
+
+  const int ng = cache->n_grouped / kGroup;
+  const int pairs = cf.batch * cf.kv_heads;
+  const int has_resid = cache->n_resid > 0 ? 1 : 0;
+  const int splits_g = choose_splits(ng, pairs, kMaxSplits - 1);
+  kvq::KiviDecodeArgs a{};
+  a.k_codes = cache->k_codes;
+  a.k_meta = cache->k_meta;
+  a.v_codes = cache->v_codes;
+  a.v_meta = cache->v_meta;
+  a.k_res = cache->k_res;
+  a.v_res = cache->v_res;
+  a.q = q;
+  a.batch = cf.batch;
+  a.kv_heads = cf.kv_heads;
+  a.q_heads = cf.q_heads;
+  a.head_dim = cf.head_dim;
+  a.k_bits = cf.k_bits;
+  a.v_bits = cf.v_bits;
+  a.groups_cap = cache->groups_cap;
+  a.res_cap = cache->res_cap;
+  a.n_groups = ng;
+  a.n_resid = cache->n_resid;
+  a.splits_g = splits_g;
+  a.groups_per_split = splits_g > 0 ? ceil_div(ng, splits_g) : 0;
+  a.splits_total = splits_g + has_resid;
+  a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  a.status = reinterpret_cast<uint32_t*>(base);
+  a.part_o = reinterpret_cast<float*>(base + kWsHeader);
+  a.part_ml = a.part_o + static_cast<size_t>(cf.batch) * cf.q_heads * a.splits_total * cf.head_dim;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = from_cuda(kvq::launch_kivi_decode(a, s));
+  if (st != KVQ_OK) return st;
+  kvq::MergeArgs mg{};
+  mg.part_o = a.part_o;
+  mg.part_ml = a.part_ml;
+  mg.splits_total = a.splits_total;
+  mg.rows = cf.batch * cf.q_heads;
+  mg.head_dim = cf.head_dim;
+  mg.out = out;
+  mg.out_fp32 = out_fp32;
+  return from_cuda(kvq::launch_merge(mg, s));
+}
+
+size_t fp8_quantize_workspace_bytes(int32_t batch, int32_t kv_heads, int32_t seq_len, int32_t head_dim) {
+  (void)batch;
+  (void)kv_heads;
+  (void)seq_len;
+  (void)head_dim;
+  return static_cast<size_t>(kAmaxBlocksMax) * sizeof(uint32_t);
+}
+
+kvq_status fp8_kv_quantize(const uint16_t* x, int32_t batch, int32_t kv_heads, int32_t seq_len, int32_t head_dim,
+                           const int32_t* block_table, int32_t max_blocks, int32_t block_size, int32_t num_blocks,
+                           uint8_t* pool, float* scale, int32_t static_scale, int32_t value_layout, void* ws,
+                           size_t ws_bytes, void* stream) {
+  if (x == nullptr || block_table == nullptr || pool == nullptr || scale == nullptr) return KVQ_ERR_NULL;
+  if (batch <= 0 || kv_heads <= 0 || seq_len <= 0 || num_blocks <= 0 || max_blocks <= 0) return KVQ_ERR_ARG;
+  if (head_dim != 64 && head_dim != 128) return KVQ_ERR_UNSUPPORTED;
+  if (block_size != 16) return KVQ_ERR_UNSUPPORTED;
+  if (value_layout != 0 && value_layout != 1) return KVQ_ERR_ARG;
+  if (ceil_div(seq_len, block_size) > max_blocks) return KVQ_ERR_CAPACITY;
+  if (!aligned(x) || !aligned(block_table) || !aligned(pool) || !aligned(scale)) return KVQ_ERR_ALIGN;
+  if (!static_scale) {
+    if (ws == nullptr) return KVQ_ERR_WORKSPACE;
+    if (!aligned(ws)) return KVQ_ERR_ALIGN;
+    if (ws_bytes < fp8_quantize_workspace_bytes(batch, kv_heads, seq_len, head_dim)) return KVQ_ERR_WORKSPACE;
+  }
+  kvq::Fp8QuantArgs a{};
+  a.x = x;
+  a.batch = batch;
+  a.kv_heads = kv_heads;
+  a.seq_len = seq_len;
+  a.head_dim = head_dim;
+  a.block_table = block_table;
+  a.max_blocks = max_blocks;
+  a.num_blocks = num_blocks;
+  a.pool = pool;
+  a.scale = scale;
+  a.static_scale = static_scale;
+  a.value_layout = value_layout;
+  a.amax_partials = static_cast<uint32_t*>(ws);
+  const long long n_vec = static_cast<long long>(batch) * kv_heads * seq_len * head_dim / 8;
+  a.amax_blocks = static_cast<int>(std::min<long long>(
+      {static_cast<long long>(kAmaxBlocksMax), 8LL * kvq::device_sm_count(), (n_vec + 255) / 256}));
+  return from_cuda(kvq::launch_fp8_quantize(a, static_cast<cudaStream_t>(stream)));
+}
+
+size_t fp8_decode_workspace_bytes(int32_t batch, int32_t q_heads, int32_t head_dim) {
+  if (batch <= 0 || q_heads <= 0 || head_dim <= 0) return 0;
+  return decode_ws_bytes(batch, q_heads, head_dim);
+}
+
+kvq_status fp8_decode_attention(const uint16_t* q, const uint8_t* k_pool, const uint8_t* v_pool, const float* k_scale,
+                                const float* v_scale, const int32_t* block_table, const int32_t* seq_lens,
+                                int32_t batch, int32_t q_heads, int32_t kv_heads, int32_t head_dim, int32_t block_size,
+                                int32_t max_blocks, int32_t num_blocks, int32_t max_seq_len, void* out,
+                                int32_t out_fp32, float softmax_scale, void* ws, size_t ws_bytes, void* stream) {
+  if (!q || !k_pool || !v_pool || !k_scale || !v_scale || !block_table || !seq_lens || !out) return KVQ_ERR_NULL;
+  if (batch <= 0 || q_heads <= 0 || kv_heads <= 0 || max_blocks <= 0 || num_blocks <= 0 || max_seq_len <= 0)
+    return KVQ_ERR_ARG;
+  if (batch > 65535 || kv_heads > 65535) return KVQ_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128) return KVQ_ERR_UNSUPPORTED;
+  if (block_size != 16) return KVQ_ERR_UNSUPPORTED;
+  if (q_heads % kv_heads != 0) return KVQ_ERR_SHAPE;
+  if (q_heads / kv_heads > kvq::kMaxGqa) return KVQ_ERR_UNSUPPORTED;
+  if (max_seq_len > max_blocks * block_size) return KVQ_ERR_CAPACITY;
+  if (!aligned(q) || !aligned(k_pool) || !aligned(v_pool) || !aligned(k_scale) || !aligned(v_scale) ||
+      !aligned(block_table) || !aligned(seq_lens) || !aligned(out))
+    return KVQ_ERR_ALIGN;
+  if (ws == nullptr) return KVQ_ERR_WORKSPACE;
+  if (!aligned(ws)) return KVQ_ERR_ALIGN;
+  if (ws_bytes < decode_ws_bytes(batch, q_heads, head_dim)) return KVQ_ERR_WORKSPACE;
+  if (!(softmax_scale == softmax_scale) || std::isinf(softmax_scale)) return KVQ_ERR_ARG;
+  const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(head_dim));
+  const int nblk = ceil_div(max_seq_len, block_size);
+  const int splits = choose_splits(nblk, batch * kv_heads, kMaxSplits);
+  kvq::Fp8DecodeArgs a{};
+  a.q = q;
+  a.k_pool = k_pool;
+  a.v_pool = v_pool;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  a.block_table = block_table;
+  a.seq_lens = seq_lens;
+  a.batch = batch;
+  a.q_heads = q_heads;
+  a.kv_heads = kv_heads;
+  a.head_dim = head_dim;
+  a.max_blocks = max_blocks;
+  a.num_blocks = num_blocks;
+  a.splits = splits;
+  a.blocks_per_split = ceil_div(nblk, splits);
+  a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  a.status = reinterpret_cast<uint32_t*>(base);
+  a.part_o = reinterpret_cast<float*>(base + kWsHeader);
+  a.part_ml = a.part_o + static_cast<size_t>(batch) * q_heads * splits * head_dim;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  kvq_status st = from_cuda(kvq::launch_fp8_decode(a, s));
+  if (st != KVQ_OK) return st;
+  kvq::MergeArgs mg{};
+  mg.part_o = a.part_o;
+  mg.part_ml = a.part_ml;
+  mg.splits_total = splits;
+  mg.rows = batch * q_heads;
+  mg.head_dim = head_dim;
+  mg.out = out;
+  mg.out_fp32 = out_fp32;
+  return from_cuda(kvq::launch_merge(mg, s));
+}
+
+}  // extern "C"

@@ -1,0 +1,397 @@
+// FP8 E4M3 paged KV cache kernels for sm_103a: per-tensor amax (two passes, no
+// atomics), scale = amax / 448, cast + scatter into paged blocks, and split-K
+// decode attention over the paged cache.
+//
+// Method: "4.4 KV Cache 量化：KIVI 2-bit 与 FP8 KV Cache" (aiinfraguide), section 5
+// (E4M3 = 1 sign, 4 exponent, 3 mantissa bits); "大模型量化从0到1（十三）：KV Cache
+// 量化" (CSDN), section 10 (q = cast_fp8(x / s), x_hat = float(q) * s, per-tensor
+// scale) and section 12 (paged blocks through a block table); "LLM推理加速KV Cache
+// 量化压缩实战方案" (yunthe), custom-cache section (scale = max|x| / 448).
+#include <cmath>
+
+#include "kvq_device.cuh"
+#include "kvq_internal.h"
+
+namespace kvq {
+namespace {
+
+constexpr int kBlock = 16;  // tokens per paged block
+
+// ---------------------------------------------------------------------------
+// amax: max |x| as the maximum of the fp16 magnitude bits (|x| orders like its
+// bits; a NaN's bits exceed every finite value's and infinity's).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) fp8_amax_kernel(const uint4* __restrict__ x, long long n_vec,
+                                                       uint32_t* __restrict__ partials) {
+  uint32_t m = 0;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+  for (; i + 3 * stride < n_vec; i += 4 * stride) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v[u] = __ldcs(x + i + u * stride);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) m = max(m, max(w[k] & 0x7FFFu, (w[k] >> 16) & 0x7FFFu));
+    }
+  }
+  for (; i < n_vec; i += stride) {
+    const uint4 v = __ldcs(x + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) m = max(m, max(w[k] & 0x7FFFu, (w[k] >> 16) & 0x7FFFu));
+  }
+  m = __reduce_max_sync(0xffffffffu, m);
+  __shared__ uint32_t wm[8];
+  if ((threadIdx.x & 31) == 0) wm[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t r = 0;
+    for (int k = 0; k < (blockDim.x >> 5); ++k) r = max(r, wm[k]);
+    partials[blockIdx.x] = r;
+  }
+}
+
+// scale = fl32(amax / 448), or 1 when the tensor is all zeros.
+__global__ void __launch_bounds__(256) fp8_scale_kernel(const uint32_t* __restrict__ partials, int n,
+                                                        float* __restrict__ scale) {
+  uint32_t m = 0;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) m = max(m, partials[i]);
+  m = __reduce_max_sync(0xffffffffu, m);
+  __shared__ uint32_t wm[8];
+  if ((threadIdx.x & 31) == 0) wm[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t r = 0;
+    for (int k = 0; k < (blockDim.x >> 5); ++k) r = max(r, wm[k]);
+    const float amax = __half2float(__ushort_as_half(static_cast<unsigned short>(r)));
+    *scale = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Cast + scatter: one (b, h, logical block) unit at a time per thread block.
+// The 16 x D block is staged in shared memory, then each thread writes one
+// 16-byte chunk of the fragment-ordered block.
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(128) fp8_cast_kernel(Fp8QuantArgs a) {
+  __shared__ __align__(16) __half xs[kBlock * D];
+  const int nb = (a.seq_len + kBlock - 1) / kBlock;
+  const long long units = static_cast<long long>(a.batch) * a.kv_heads * nb;
+  const float scale = *a.scale;
+  const int tid = threadIdx.x;
+  for (long long u = blockIdx.x; u < units; u += gridDim.x) {
+    const int j = static_cast<int>(u % nb);
+    const long long bh = u / nb;
+    const int b = static_cast<int>(bh / a.kv_heads), h = static_cast<int>(bh % a.kv_heads);
+    const int t0 = j * kBlock;
+    const int ntok = min(kBlock, a.seq_len - t0);
+    const uint4* src = reinterpret_cast<const uint4*>(a.x + (bh * a.seq_len + t0) * static_cast<long long>(D));
+    __syncthreads();  // the previous unit's readers are done with xs
+    for (int i = tid; i < kBlock * D / 8; i += 128) {
+      const int tok = i / (D / 8);
+      reinterpret_cast<uint4*>(xs)[i] = (tok < ntok) ? __ldcs(src + i) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    __syncthreads();
+    const int blk = a.block_table[static_cast<long long>(b) * a.max_blocks + j];
+    if (blk < 0 || blk >= a.num_blocks) continue;  // uniform per block: no write outside the pool
+    uint8_t* dst = a.pool + (static_cast<long long>(blk) * a.kv_heads + h) * (kBlock * D);
+    // storage chunk tid: lane l = tid % 32 holds stream bytes 16c .. 16c+15, c = tid / 32
+    for (int chunk = tid; chunk < kBlock * D / 16; chunk += 128) {
+      const int l = chunk % 32, c = chunk / 32;
+      const int gg = l >> 2, tg = l & 3;
+      uint32_t out[4];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int i = 8 * c + k;  // byte pair index in the lane's stream
+        int tok0, ch0, tok1, ch1;
+        if (a.value_layout) {
+          const int nt = i >> 1, r = i & 1;
+          tok0 = 8 * r + 2 * tg;
+          tok1 = tok0 + 1;
+          ch0 = ch1 = 8 * nt + gg;
+        } else {
+          const int nt = i / (D / 8), rem = i % (D / 8), ks = rem >> 1, r = rem & 1;
+          tok0 = tok1 = 8 * nt + gg;
+          ch0 = 16 * ks + 8 * r + 2 * tg;
+          ch1 = ch0 + 1;
+        }
+        const bool v0 = tok0 < ntok, v1 = tok1 < ntok;
+        const float y0 = v0 ? __fdiv_rn(__half2float(xs[tok0 * D + ch0]), scale) : 0.0f;
+        const float y1 = v1 ? __fdiv_rn(__half2float(xs[tok1 * D + ch1]), scale) : 0.0f;
+        uint32_t pair = f32x2_to_e4m3x2(y0, y1);
+        if (!v0) pair &= 0xFF00u;
+        if (!v1) pair &= 0x00FFu;
+        if (k & 1)
+          out[k >> 1] |= pair << 16;
+        else
+          out[k >> 1] = pair;
+      }
+      reinterpret_cast<uint4*>(dst)[chunk] = make_uint4(out[0], out[1], out[2], out[3]);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Split-K decode attention over the paged FP8 cache.
+// Grid (splits, H_kv, B), 4 warps; warp w of block x takes logical blocks
+// x*bps + w, x*bps + w + 4, ... through a ring of STAGES stages (K block and
+// V block of one kv head, 16*D bytes each) filled by bulk copies.
+//   q.k^T : A = q (fp16, exact), B = E4M3 keys converted to fp16 (exact).
+//   p.V   : A = p split into fp16 hi + lo rows, B = E4M3 values as fp16.
+// ---------------------------------------------------------------------------
+template <int D, int STAGES>
+struct Fp8Smem {
+  static constexpr int BAR_BYTES = 128;
+  static constexpr int STAGE = 2 * kBlock * D;
+  static constexpr int RING = 4 * STAGES * STAGE;
+  static constexpr int COMBINE = (4 * 8 * D + 64) * 4;
+  static constexpr int AREA = RING > COMBINE ? RING : COMBINE;
+  static constexpr int BYTES = BAR_BYTES + AREA;
+};
+
+template <int D, int STAGES>
+__global__ void __launch_bounds__(128) fp8_decode_kernel(Fp8DecodeArgs a) {
+  using S = Fp8Smem<D, STAGES>;
+  constexpr int KS = D / 16, NT = D / 8, CH = D / 32;  // CH: 16-byte chunks per lane
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
+  uint8_t* area = smem + S::BAR_BYTES;
+  float* o_s = reinterpret_cast<float*>(area);
+  float* m_s = o_s + 4 * 8 * D;
+  float* l_s = m_s + 32;
+
+  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, tig = lane & 3;
+  const int gq = a.q_heads / a.kv_heads;
+  const int len = min(max(a.seq_lens[b], 0), a.max_blocks * kBlock);
+  const int nblk = (len + kBlock - 1) / kBlock;
+  const int j_begin = split * a.blocks_per_split;
+  const int j_end = min(nblk, j_begin + a.blocks_per_split);
+  const int n_here = j_end - j_begin;
+  const int n_mine = (n_here > warp) ? (n_here - warp + 3) / 4 : 0;
+  uint64_t* bar = bars + warp * STAGES;
+  uint8_t* ring = area + warp * STAGES * S::STAGE;
+  const int32_t* table = a.block_table + static_cast<long long>(b) * a.max_blocks;
+
+  if (lane == 0) {
+#pragma unroll
+    for (int s = 0; s < STAGES; ++s) mbar_init(&bar[s], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  // Physical block of the warp's j-th logical block; out-of-range table
+  // entries are clamped so that a bad table cannot address outside the pool.
+  auto phys = [&](int j) -> long long {
+    const int blk = table[j_begin + warp + 4 * j];
+    return static_cast<long long>(min(max(blk, 0), a.num_blocks - 1));
+  };
+  auto issue = [&](int j, long long blk) {
+    const long long off = (blk * a.kv_heads + h) * (kBlock * D);
+    uint8_t* dst = ring + (j % STAGES) * S::STAGE;
+    uint64_t* bb = &bar[j % STAGES];
+    mbar_arrive_expect_tx(bb, S::STAGE);
+    bulk_g2s(dst, a.k_pool + off, kBlock * D, bb);
+    bulk_g2s(dst + kBlock * D, a.v_pool + off, kBlock * D, bb);
+  };
+  if (lane == 0) {
+    for (int j = 0; j < STAGES && j < n_mine; ++j) issue(j, phys(j));
+  }
+
+  const bool row_ok = g < gq;
+  const __half* qrow = reinterpret_cast<const __half*>(a.q) +
+                       (static_cast<long long>(b) * a.q_heads + h * gq + (row_ok ? g : 0)) * D;
+  uint32_t qa[KS][2];
+#pragma unroll
+  for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj)
+      qa[ks][jj] = row_ok ? *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8 * jj + 2 * tig) : 0u;
+  const float kmul = (*a.k_scale) * a.scale_log2;
+  const float vscale = *a.v_scale;
+
+  float m_run = -INFINITY, l_run = 0.0f;
+  float o_acc[NT][4];
+#pragma unroll
+  for (int i = 0; i < NT; ++i) o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.0f;
+
+  int j = 0;
+  bool timed_out = false;
+  for (; j < n_mine; ++j) {
+    const int s = j % STAGES;
+    // table entry of the block this iteration will prefetch, loaded early
+    const long long next_blk = (lane == 0 && j + STAGES < n_mine) ? phys(j + STAGES) : 0;
+    if (!mbar_wait_bounded(&bar[s], (j / STAGES) & 1)) {
+      timed_out = true;
+      break;
+    }
+    const uint4* kb = reinterpret_cast<const uint4*>(ring + s * S::STAGE);
+    const uint4* vb = reinterpret_cast<const uint4*>(ring + s * S::STAGE + kBlock * D);
+    const int tok_base = (j_begin + warp + 4 * j) * kBlock;
+
+    // keys: lane's stream word wi = nt*KS + ks holds (r = 0, r = 1) byte pairs
+    uint32_t kw[2 * KS];
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      const uint4 x = kb[c * 32 + lane];
+      kw[4 * c] = x.x;
+      kw[4 * c + 1] = x.y;
+      kw[4 * c + 2] = x.z;
+      kw[4 * c + 3] = x.w;
+    }
+    float sacc[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.0f;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        const uint32_t w = kw[nt * KS + ks];
+        mma16816(sacc[nt], qa[ks][0], 0u, qa[ks][1], 0u, e4m3x2_to_f16x2(static_cast<uint16_t>(w & 0xFFFFu)),
+                 e4m3x2_to_f16x2(static_cast<uint16_t>(w >> 16)));
+      }
+    }
+    float sc[4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int tok = tok_base + 8 * nt + 2 * tig + e;
+        sc[2 * nt + e] = (tok < len) ? sacc[nt][e] * kmul : -INFINITY;
+      }
+    float mx = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+    mx = quad_max(mx);
+    const float m_new = fmaxf(m_run, mx);
+    if (m_new != m_run) {
+      const float alpha = fast_exp2(m_run - m_new);
+      l_run *= alpha;
+#pragma unroll
+      for (int i = 0; i < NT; ++i) {
+        o_acc[i][0] *= alpha;
+        o_acc[i][1] *= alpha;
+        o_acc[i][2] *= alpha;
+        o_acc[i][3] *= alpha;
+      }
+      m_run = m_new;
+    }
+    float p[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) p[i] = fast_exp2(sc[i] - m_new);
+    l_run += (p[0] + p[1]) + (p[2] + p[3]);
+    const __half2 h0 = __floats2half2_rn(p[0], p[1]), h1 = __floats2half2_rn(p[2], p[3]);
+    const float2 f0 = __half22float2(h0), f1 = __half22float2(h1);
+    const uint32_t A0 = h2_bits(h0), A1 = pack_rn_f16x2(p[0] - f0.x, p[1] - f0.y);
+    const uint32_t A2 = h2_bits(h1), A3 = pack_rn_f16x2(p[2] - f1.x, p[3] - f1.y);
+
+    // values: lane's stream word nt holds (r = 0, r = 1) byte pairs of channel 8nt + g
+    uint32_t vw[NT];
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      const uint4 x = vb[c * 32 + lane];
+      vw[4 * c] = x.x;
+      vw[4 * c + 1] = x.y;
+      vw[4 * c + 2] = x.z;
+      vw[4 * c + 3] = x.w;
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+      mma16816(o_acc[nt], A0, A1, A2, A3, e4m3x2_to_f16x2(static_cast<uint16_t>(vw[nt] & 0xFFFFu)),
+               e4m3x2_to_f16x2(static_cast<uint16_t>(vw[nt] >> 16)));
+
+    __syncwarp();
+    if (lane == 0 && j + STAGES < n_mine) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      issue(j + STAGES, next_blk);
+    }
+  }
+  if (timed_out) {
+    if (lane == 0) report_timeout(a.status);
+    for (int jj = j; jj < n_mine && jj < j + STAGES; ++jj) (void)mbar_wait_bounded(&bar[jj % STAGES], (jj / STAGES) & 1);
+    m_run = -INFINITY;
+    l_run = 0.0f;
+#pragma unroll
+    for (int i = 0; i < NT; ++i) o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.0f;
+  }
+  l_run = quad_sum(l_run);
+
+  __syncthreads();
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int c = 8 * nt + 2 * tig;
+    o_s[(warp * 8 + g) * D + c] = (o_acc[nt][0] + o_acc[nt][2]) * vscale;
+    o_s[(warp * 8 + g) * D + c + 1] = (o_acc[nt][1] + o_acc[nt][3]) * vscale;
+  }
+  if (tig == 0) {
+    m_s[warp * 8 + g] = m_run;
+    l_s[warp * 8 + g] = l_run;
+  }
+  __syncthreads();
+  for (int i = tid; i < gq * D; i += 128) {
+    const int r = i / D, c = i % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) M = fmaxf(M, m_s[w * 8 + r]);
+    float L = 0.0f, O = 0.0f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const float f = fast_exp2(m_s[w * 8 + r] - M);
+        L = fmaf(l_s[w * 8 + r], f, L);
+        O = fmaf(o_s[(w * 8 + r) * D + c], f, O);
+      }
+    }
+    const long long row = (static_cast<long long>(b) * a.q_heads + h * gq + r) * a.splits + split;
+    a.part_o[row * D + c] = O;
+    if (c == 0) {
+      a.part_ml[row * 2] = M;
+      a.part_ml[row * 2 + 1] = L;
+    }
+  }
+}
+
+constexpr int kFp8Stages = 4;
+
+template <int D>
+cudaError_t fp8_decode_dispatch(const Fp8DecodeArgs& a, cudaStream_t s) {
+  constexpr int smem = Fp8Smem<D, kFp8Stages>::BYTES;
+  auto kern = fp8_decode_kernel<D, kFp8Stages>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(a.splits, a.kv_heads, a.batch);
+  kern<<<grid, 128, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fp8_quantize(const Fp8QuantArgs& a, cudaStream_t s) {
+  if (!a.static_scale) {
+    const long long n_vec = static_cast<long long>(a.batch) * a.kv_heads * a.seq_len * a.head_dim / 8;
+    fp8_amax_kernel<<<a.amax_blocks, 256, 0, s>>>(reinterpret_cast<const uint4*>(a.x), n_vec, a.amax_partials);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    fp8_scale_kernel<<<1, 256, 0, s>>>(a.amax_partials, a.amax_blocks, a.scale);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  const int nb = (a.seq_len + kBlock - 1) / kBlock;
+  const long long units = static_cast<long long>(a.batch) * a.kv_heads * nb;
+  const int grid = static_cast<int>(units < 16LL * device_sm_count() ? units : 16LL * device_sm_count());
+  if (a.head_dim == 128)
+    fp8_cast_kernel<128><<<grid, 128, 0, s>>>(a);
+  else if (a.head_dim == 64)
+    fp8_cast_kernel<64><<<grid, 128, 0, s>>>(a);
+  else
+    return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fp8_decode(const Fp8DecodeArgs& a, cudaStream_t s) {
+  if (a.head_dim == 128) return fp8_decode_dispatch<128>(a, s);
+  if (a.head_dim == 64) return fp8_decode_dispatch<64>(a, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace kvq

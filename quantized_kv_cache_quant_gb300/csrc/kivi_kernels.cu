@@ -1,0 +1,746 @@
+// KIVI 2/4-bit KV cache kernels for sm_103a: group quantize + pack (prefill and
+// residual flush), token copies (window fill, append), split-K decode attention
+// over the packed codes with in-register dequantization, and the log-sum-exp
+// merge of the split partials.
+//
+// Method: "4.4 KV Cache 量化：KIVI 2-bit 与 FP8 KV Cache" (aiinfraguide), section 3
+// (keys per channel, values per token, groups of 32 tokens, fp16 residual
+// window flushed when full); affine form of "大模型量化从0到1（十三）：KV Cache 量化"
+// (CSDN), section 10; attention softmax(q K^T / sqrt(d)) V of the same page,
+// section 2, with grouped-query sharing (section 5).
+#include <cfloat>
+#include <cmath>
+
+#include "kvq_device.cuh"
+#include "kvq_internal.h"
+
+namespace kvq {
+namespace {
+
+template <int D, int KB, int VB>
+struct Kivi {
+  static constexpr int KS = D / 16;                     // k-steps of q . k^T
+  static constexpr int NTV = D / 8;                     // n-tiles of p . V
+  static constexpr int NQ = D / 32;                     // value code words per (k-step[, r])
+  static constexpr int KW = (KB == 2) ? D / 16 : D / 8;  // key code words per lane
+  static constexpr int VW = (VB == 2) ? D / 16 : D / 8;  // value code words per lane
+  static constexpr int KC = 32 * D * KB / 8;            // bytes of one group's records
+  static constexpr int KM = 4 * D;
+  static constexpr int VC = 32 * D * VB / 8;
+  static constexpr int VM = 128;
+  static constexpr int STAGE = KC + KM + VC + VM;
+  static_assert(STAGE % 16 == 0, "bulk copies need 16-byte multiples");
+};
+
+// Masks that keep the code field of each fp16 half after the shift: bits 6-7
+// or 8-9 for 2-bit codes, bits 6-9 for 4-bit codes. The field then reads as
+// the fp16 subnormal code * 2^(P-24), P = 6 or 8; the top mantissa bits keep
+// the tensor-core products at full fp32-accumulation accuracy.
+constexpr uint32_t kMaskP6 = 0x00C000C0u;
+constexpr uint32_t kMaskP8 = 0x03000300u;
+constexpr uint32_t kMask4 = 0x03C003C0u;
+constexpr float kInvP6 = 262144.0f;  // 2^18 = 2^(24-6)
+constexpr float kInvP8 = 65536.0f;   // 2^16 = 2^(24-8)
+
+// ---------------------------------------------------------------------------
+// Group quantization (one thread block per (group, kv head, batch row))
+// ---------------------------------------------------------------------------
+
+// The group formula in IEEE fp32 with round-to-nearest-even everywhere.
+__device__ __forceinline__ void group_scale_zero(float mn, float mx, float levels, __half& s16, __half& z16) {
+  s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), levels));
+  z16 = __float2half_rn(__fadd_rn(mn, 0.0f));  // exact; -0 becomes +0
+}
+
+__device__ __forceinline__ uint32_t group_code(float x, float zf, float sf, float levels) {
+  if (sf == 0.0f) return 0u;
+  const float r = rintf(__fdiv_rn(__fsub_rn(x, zf), sf));
+  return static_cast<uint32_t>(fminf(fmaxf(r, 0.0f), levels));
+}
+
+template <int D, int KB, int VB>
+__global__ void __launch_bounds__(128) kivi_quantize_kernel(QuantGroupsArgs a) {
+  using P = Kivi<D, KB, VB>;
+  __shared__ __align__(16) __half xk[32 * D];
+  __shared__ __align__(16) __half xv[32 * D];
+  __shared__ uint8_t ck[32 * D];
+  __shared__ uint8_t cv[32 * D];
+  __shared__ __half sk[D], zk[D], sv[32], zv[32];
+
+  const int grp = blockIdx.x, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
+  const long long bh = static_cast<long long>(b) * a.kv_heads + h;
+  const long long src_off = bh * a.src_bh_stride + static_cast<long long>(a.src_tok0 + 32 * grp) * D;
+  const uint4* srck = reinterpret_cast<const uint4*>(a.k_src + src_off);
+  const uint4* srcv = reinterpret_cast<const uint4*>(a.v_src + src_off);
+  for (int i = tid; i < 32 * D / 8; i += 128) {
+    reinterpret_cast<uint4*>(xk)[i] = srck[i];
+    reinterpret_cast<uint4*>(xv)[i] = srcv[i];
+  }
+  __syncthreads();
+
+  constexpr float KL = static_cast<float>((1 << KB) - 1);
+  constexpr float VL = static_cast<float>((1 << VB) - 1);
+
+  // Keys: one channel per thread, statistics over the group's 32 tokens.
+  for (int c = tid; c < D; c += 128) {
+    float mn = FLT_MAX, mx = -FLT_MAX;
+#pragma unroll 8
+    for (int t = 0; t < 32; ++t) {
+      const float x = __half2float(xk[t * D + c]);
+      mn = fminf(mn, x);
+      mx = fmaxf(mx, x);
+    }
+    __half s16, z16;
+    group_scale_zero(mn, mx, KL, s16, z16);
+    sk[c] = s16;
+    zk[c] = z16;
+    const float sf = __half2float(s16), zf = __half2float(z16);
+#pragma unroll 8
+    for (int t = 0; t < 32; ++t) ck[t * D + c] = static_cast<uint8_t>(group_code(__half2float(xk[t * D + c]), zf, sf, KL));
+  }
+
+  // Values: one token per warp step, channels across lanes, warp-shuffle min/max.
+  const int warp = tid >> 5, lane = tid & 31;
+  for (int t = warp; t < 32; t += 4) {
+    float xs[D / 32];
+    float mn = FLT_MAX, mx = -FLT_MAX;
+#pragma unroll
+    for (int j = 0; j < D / 32; ++j) {
+      xs[j] = __half2float(xv[t * D + lane + 32 * j]);
+      mn = fminf(mn, xs[j]);
+      mx = fmaxf(mx, xs[j]);
+    }
+    mn = warp_min(mn);
+    mx = warp_max(mx);
+    __half s16, z16;
+    group_scale_zero(mn, mx, VL, s16, z16);
+    if (lane == 0) {
+      sv[t] = s16;
+      zv[t] = z16;
+    }
+    const float sf = __half2float(s16), zf = __half2float(z16);
+#pragma unroll
+    for (int j = 0; j < D / 32; ++j) cv[t * D + lane + 32 * j] = static_cast<uint8_t>(group_code(xs[j], zf, sf, VL));
+  }
+  __syncthreads();
+
+  const long long grp_index = bh * a.groups_cap + a.dst_group0 + grp;
+
+  // Key code words; storage word j belongs to lane (j%128)/4, word u = 4*(j/128) + j%4.
+  uint32_t* kdst = reinterpret_cast<uint32_t*>(a.k_codes + grp_index * P::KC);
+  for (int j = tid; j < 32 * P::KW; j += 128) {
+    const int L = (j % 128) / 4, u = (j / 128) * 4 + (j % 4);
+    const int gg = L >> 2, tg = L & 3;
+    uint32_t w = 0;
+    if constexpr (KB == 2) {
+      const int ks = u;
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int d0 = 16 * ks + 8 * r + 2 * tg;
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+          const int tok = 8 * nt + gg, f = 4 * r + nt;
+          w |= (static_cast<uint32_t>(ck[tok * D + d0]) << (2 * f)) |
+               (static_cast<uint32_t>(ck[tok * D + d0 + 1]) << (16 + 2 * f));
+        }
+      }
+    } else {
+      const int ks = u >> 1, r = u & 1;
+      const int d0 = 16 * ks + 8 * r + 2 * tg;
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        const int tok = 8 * nt + gg;
+        w |= (static_cast<uint32_t>(ck[tok * D + d0]) << (4 * nt)) |
+             (static_cast<uint32_t>(ck[tok * D + d0 + 1]) << (16 + 4 * nt));
+      }
+    }
+    kdst[j] = w;
+  }
+
+  // Value code words.
+  uint32_t* vdst = reinterpret_cast<uint32_t*>(a.v_codes + grp_index * P::VC);
+  for (int j = tid; j < 32 * P::VW; j += 128) {
+    const int L = (j % 128) / 4, u = (j / 128) * 4 + (j % 4);
+    const int gg = L >> 2, tg = L & 3;
+    uint32_t w = 0;
+    if constexpr (VB == 2) {
+      const int ks = u / P::NQ, q = u % P::NQ;
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int t0 = 16 * ks + 8 * r + 2 * tg;
+#pragma unroll
+        for (int n = 0; n < 4; ++n) {
+          const int ch = 8 * (4 * q + n) + gg, f = 4 * r + n;
+          w |= (static_cast<uint32_t>(cv[t0 * D + ch]) << (2 * f)) |
+               (static_cast<uint32_t>(cv[(t0 + 1) * D + ch]) << (16 + 2 * f));
+        }
+      }
+    } else {
+      const int ks = u / (2 * P::NQ), r = (u / P::NQ) % 2, q = u % P::NQ;
+      const int t0 = 16 * ks + 8 * r + 2 * tg;
+#pragma unroll
+      for (int n = 0; n < 4; ++n) {
+        const int ch = 8 * (4 * q + n) + gg;
+        w |= (static_cast<uint32_t>(cv[t0 * D + ch]) << (4 * n)) |
+             (static_cast<uint32_t>(cv[(t0 + 1) * D + ch]) << (16 + 4 * n));
+      }
+    }
+    vdst[j] = w;
+  }
+
+  // Key meta: record ks*4 + tig = {s[d0], s[d0+1], s[d0+8], s[d0+9], z[...]}.
+  if (tid < D / 4) {
+    const int ks = tid >> 2, tg = tid & 3, d0 = 16 * ks + 2 * tg;
+    const int chans[4] = {d0, d0 + 1, d0 + 8, d0 + 9};
+    uint16_t v[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[i] = __half_as_ushort(sk[chans[i]]);
+      v[4 + i] = __half_as_ushort(zk[chans[i]]);
+    }
+    uint4 rec;
+    rec.x = v[0] | (static_cast<uint32_t>(v[1]) << 16);
+    rec.y = v[2] | (static_cast<uint32_t>(v[3]) << 16);
+    rec.z = v[4] | (static_cast<uint32_t>(v[5]) << 16);
+    rec.w = v[6] | (static_cast<uint32_t>(v[7]) << 16);
+    reinterpret_cast<uint4*>(a.k_meta + grp_index * P::KM)[tid] = rec;
+  }
+  // Value meta: 4 records of scales, then 4 of zero points.
+  if (tid < 8) {
+    const int tg = tid & 3;
+    const __half* src = (tid < 4) ? sv : zv;
+    uint16_t v[8];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      v[2 * nt] = __half_as_ushort(src[8 * nt + 2 * tg]);
+      v[2 * nt + 1] = __half_as_ushort(src[8 * nt + 2 * tg + 1]);
+    }
+    uint4 rec;
+    rec.x = v[0] | (static_cast<uint32_t>(v[1]) << 16);
+    rec.y = v[2] | (static_cast<uint32_t>(v[3]) << 16);
+    rec.z = v[4] | (static_cast<uint32_t>(v[5]) << 16);
+    rec.w = v[6] | (static_cast<uint32_t>(v[7]) << 16);
+    reinterpret_cast<uint4*>(a.v_meta + grp_index * P::VM)[tid] = rec;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Token copies (fill the fp16 window, append a decode token, move a remainder)
+// ---------------------------------------------------------------------------
+__global__ void copy_tokens_kernel(CopyTokensArgs a) {
+  const int vec_per_tok = a.head_dim / 8;
+  const long long per_bh = static_cast<long long>(a.n_tokens) * vec_per_tok;
+  const long long total = per_bh * a.bh;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long bh = i / per_bh;
+    const long long rem = i % per_bh;
+    const long long tok = rem / vec_per_tok, v = rem % vec_per_tok;
+    const long long s = (bh * a.src_bh_stride + (a.src_tok0 + tok) * a.head_dim) / 8 + v;
+    const long long d = (bh * a.dst_bh_stride + (a.dst_tok0 + tok) * a.head_dim) / 8 + v;
+    reinterpret_cast<uint4*>(a.k_dst)[d] = reinterpret_cast<const uint4*>(a.k_src)[s];
+    reinterpret_cast<uint4*>(a.v_dst)[d] = reinterpret_cast<const uint4*>(a.v_src)[s];
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Split-K decode attention
+// ---------------------------------------------------------------------------
+// Grid (splits_total, H_kv, B), 4 warps. Thread blocks x < splits_g take a
+// contiguous range of groups; warp w of such a block takes groups
+// begin + w, begin + w + 4, ... through its own ring of STAGES shared-memory
+// stages filled by bulk copies (one mbarrier per stage). The last block
+// (x == splits_g) attends over the fp16 window on CUDA cores. Each block
+// writes unnormalized (m, l, o) partials per query head; m and the scores are
+// in log2 units.
+//
+// Tensor-core mapping per group (m16n8k16, M = 16 rows = 8 query heads x
+// {hi, lo} fp16 parts):
+//   q.k^T : A = q'_{h,d} = q_{h,d} * s_{g,d} split exactly into fp16 hi + lo
+//           (hi = fp16(q*s), lo = fma(q, s, -hi)); B = key codes (fields as
+//           fp16 subnormals); plus q . z_g from one MMA with A = q, B = z.
+//   p.V   : A = p_t * s_t split into fp16 hi + lo; B = value codes; plus
+//           sum_t p_t z_t on CUDA cores.
+template <int D>
+struct CombineSmem {
+  static constexpr int O_FLOATS = 4 * 8 * D;
+  static constexpr int BYTES = (O_FLOATS + 64) * 4;
+};
+
+template <int D, int KB, int VB, int STAGES>
+struct DecodeSmem {
+  static constexpr int BAR_BYTES = 128;
+  static constexpr int STAGE_BYTES = 4 * STAGES * Kivi<D, KB, VB>::STAGE;
+  static constexpr int QF_BYTES = 8 * D * 4;
+  static constexpr int AREA = (STAGE_BYTES > CombineSmem<D>::BYTES + QF_BYTES) ? STAGE_BYTES
+                                                                               : CombineSmem<D>::BYTES + QF_BYTES;
+  static constexpr int BYTES = BAR_BYTES + AREA;
+  static_assert(4 * STAGES * 8 <= BAR_BYTES, "barrier area");
+};
+
+template <int D, int KB, int VB, int STAGES>
+__global__ void __launch_bounds__(128) kivi_decode_kernel(KiviDecodeArgs a) {
+  using P = Kivi<D, KB, VB>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
+  uint8_t* area = smem + DecodeSmem<D, KB, VB, STAGES>::BAR_BYTES;
+  float* o_s = reinterpret_cast<float*>(area);  // [4 warps][8 rows][D]  (after the main loop)
+  float* m_s = o_s + CombineSmem<D>::O_FLOATS;  // [4][8]
+  float* l_s = m_s + 32;                        // [4][8]
+
+  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, tig = lane & 3;
+  const int gq = a.q_heads / a.kv_heads;
+  const long long bh = static_cast<long long>(b) * a.kv_heads + h;
+
+  float m_run = -INFINITY, l_run = 0.0f, vz_run = 0.0f;
+  float o_acc[P::NTV][4];
+#pragma unroll
+  for (int i = 0; i < P::NTV; ++i) o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.0f;
+  // window path results (one value per query row)
+  float rw_m[kMaxGqa], rw_l[kMaxGqa], rw_o[kMaxGqa][D / 32];
+
+  if (split < a.splits_g) {
+    // ------------------------------- grouped region -------------------------------
+    const int g_begin = split * a.groups_per_split;
+    const int g_end = min(a.n_groups, g_begin + a.groups_per_split);
+    const int n_here = g_end - g_begin;
+    const int n_mine = (n_here > warp) ? (n_here - warp + 3) / 4 : 0;
+    uint64_t* bar = bars + warp * STAGES;
+    uint8_t* ring = area + warp * STAGES * P::STAGE;
+    const uint8_t* kc_g = a.k_codes + bh * a.groups_cap * static_cast<long long>(P::KC);
+    const uint8_t* km_g = a.k_meta + bh * a.groups_cap * static_cast<long long>(P::KM);
+    const uint8_t* vc_g = a.v_codes + bh * a.groups_cap * static_cast<long long>(P::VC);
+    const uint8_t* vm_g = a.v_meta + bh * a.groups_cap * static_cast<long long>(P::VM);
+
+    if (lane == 0) {
+#pragma unroll
+      for (int s = 0; s < STAGES; ++s) mbar_init(&bar[s], 1);
+      fence_mbar_init();
+    }
+    __syncwarp();
+
+    auto issue = [&](int j) {
+      const long long grp = g_begin + warp + 4 * j;
+      uint8_t* dst = ring + (j % STAGES) * P::STAGE;
+      uint64_t* bb = &bar[j % STAGES];
+      mbar_arrive_expect_tx(bb, P::STAGE);
+      bulk_g2s(dst, kc_g + grp * P::KC, P::KC, bb);
+      bulk_g2s(dst + P::KC, km_g + grp * P::KM, P::KM, bb);
+      bulk_g2s(dst + P::KC + P::KM, vc_g + grp * P::VC, P::VC, bb);
+      bulk_g2s(dst + P::KC + P::KM + P::VC, vm_g + grp * P::VM, P::VM, bb);
+    };
+    if (lane == 0) {
+      for (int j = 0; j < STAGES && j < n_mine; ++j) issue(j);
+    }
+
+    // Query fragments of row g (query head h*gq + g), scaled by 2^-e so that
+    // |q| < 1 and q * s stays inside the fp16 range.
+    const bool row_ok = g < gq;
+    const __half* qrow = reinterpret_cast<const __half*>(a.q) +
+                         (static_cast<long long>(b) * a.q_heads + h * gq + (row_ok ? g : 0)) * D;
+    float2 qv[P::KS][2];
+    float qmax = 0.0f;
+#pragma unroll
+    for (int ks = 0; ks < P::KS; ++ks)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const __half2 v = row_ok ? *reinterpret_cast<const __half2*>(qrow + 16 * ks + 8 * j + 2 * tig)
+                                 : __float2half2_rn(0.0f);
+        qv[ks][j] = __half22float2(v);
+        qmax = fmaxf(qmax, fmaxf(fabsf(qv[ks][j].x), fabsf(qv[ks][j].y)));
+      }
+    qmax = quad_max(qmax);
+    int e = 0;
+    if (qmax > 0.0f) frexpf(qmax, &e);
+    const float qscale = ldexpf(1.0f, -e);
+    uint32_t qs[P::KS][2];
+#pragma unroll
+    for (int ks = 0; ks < P::KS; ++ks)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) qs[ks][j] = pack_rn_f16x2(qv[ks][j].x * qscale, qv[ks][j].y * qscale);
+    const float p2e = ldexpf(1.0f, e) * a.scale_log2;
+    const float mult6 = kInvP6 * p2e, mult8 = kInvP8 * p2e;
+
+    int j = 0;
+    bool timed_out = false;
+    for (; j < n_mine; ++j) {
+      const int s = j % STAGES;
+      if (!mbar_wait_bounded(&bar[s], (j / STAGES) & 1)) {
+        timed_out = true;
+        break;
+      }
+      const uint8_t* sp = ring + s * P::STAGE;
+      const uint4* kcw = reinterpret_cast<const uint4*>(sp);
+      const uint4* kmr = reinterpret_cast<const uint4*>(sp + P::KC);
+      const uint4* vcw = reinterpret_cast<const uint4*>(sp + P::KC + P::KM);
+      const uint4* vmr = reinterpret_cast<const uint4*>(sp + P::KC + P::KM + P::VC);
+
+      // ---- scores: q . k_hat for 32 tokens ----
+      uint32_t kw[P::KW];
+#pragma unroll
+      for (int c = 0; c < P::KW / 4; ++c) {
+        const uint4 x = kcw[c * 32 + lane];
+        kw[4 * c] = x.x;
+        kw[4 * c + 1] = x.y;
+        kw[4 * c + 2] = x.z;
+        kw[4 * c + 3] = x.w;
+      }
+      float sacc[4][4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) sacc[i][0] = sacc[i][1] = sacc[i][2] = sacc[i][3] = 0.0f;
+      float bacc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+      for (int ks = 0; ks < P::KS; ++ks) {
+        const uint4 md = kmr[ks * 4 + tig];  // {s(d0,d0+1), s(d0+8,d0+9), z(d0,d0+1), z(d0+8,d0+9)}
+        const __half2 q0 = bits_h2(qs[ks][0]), q1 = bits_h2(qs[ks][1]);
+        const __half2 hi0 = __hmul2(q0, bits_h2(md.x));
+        const __half2 lo0 = __hfma2(q0, bits_h2(md.x), __hneg2(hi0));
+        const __half2 hi1 = __hmul2(q1, bits_h2(md.y));
+        const __half2 lo1 = __hfma2(q1, bits_h2(md.y), __hneg2(hi1));
+        const uint32_t A0 = h2_bits(hi0), A1 = h2_bits(lo0), A2 = h2_bits(hi1), A3 = h2_bits(lo1);
+        mma16816(bacc, qs[ks][0], 0u, qs[ks][1], 0u, md.z, md.w);
+        if constexpr (KB == 2) {
+          const uint32_t w = kw[ks];
+          const uint32_t l6 = w << 6, l2 = w << 2, r2 = w >> 2, r6 = w >> 6;
+          mma16816(sacc[0], A0, A1, A2, A3, l6 & kMaskP6, r2 & kMaskP6);
+          mma16816(sacc[1], A0, A1, A2, A3, l6 & kMaskP8, r2 & kMaskP8);
+          mma16816(sacc[2], A0, A1, A2, A3, l2 & kMaskP6, r6 & kMaskP6);
+          mma16816(sacc[3], A0, A1, A2, A3, l2 & kMaskP8, r6 & kMaskP8);
+        } else {
+          const uint32_t w0 = kw[2 * ks], w1 = kw[2 * ks + 1];
+          mma16816(sacc[0], A0, A1, A2, A3, (w0 << 6) & kMask4, (w1 << 6) & kMask4);
+          mma16816(sacc[1], A0, A1, A2, A3, (w0 << 2) & kMask4, (w1 << 2) & kMask4);
+          mma16816(sacc[2], A0, A1, A2, A3, (w0 >> 2) & kMask4, (w1 >> 2) & kMask4);
+          mma16816(sacc[3], A0, A1, A2, A3, (w0 >> 6) & kMask4, (w1 >> 6) & kMask4);
+        }
+      }
+      const float bias = bacc[0] * p2e;
+      float sc[8];
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        const float mult = (KB == 2 && (nt & 1)) ? mult8 : mult6;
+        sc[2 * nt] = fmaf(sacc[nt][0] + sacc[nt][2], mult, bias);
+        sc[2 * nt + 1] = fmaf(sacc[nt][1] + sacc[nt][3], mult, bias);
+      }
+
+      // ---- online softmax (log2 domain) ----
+      float mx = sc[0];
+#pragma unroll
+      for (int i = 1; i < 8; ++i) mx = fmaxf(mx, sc[i]);
+      mx = quad_max(mx);
+      const float m_new = fmaxf(m_run, mx);
+      if (m_new != m_run) {
+        const float alpha = fast_exp2(m_run - m_new);
+        l_run *= alpha;
+        vz_run *= alpha;
+#pragma unroll
+        for (int i = 0; i < P::NTV; ++i) {
+          o_acc[i][0] *= alpha;
+          o_acc[i][1] *= alpha;
+          o_acc[i][2] *= alpha;
+          o_acc[i][3] *= alpha;
+        }
+        m_run = m_new;
+      }
+      float p[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) p[i] = fast_exp2(sc[i] - m_new);
+
+      // ---- p' = p * s_t as fp16 hi + lo; the zero-point term on CUDA cores ----
+      const uint4 vs = vmr[tig], vz = vmr[4 + tig];
+      const uint32_t vsw[4] = {vs.x, vs.y, vs.z, vs.w};
+      const uint32_t vzw[4] = {vz.x, vz.y, vz.z, vz.w};
+      uint32_t phi[4], plo[4];
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        const float2 sf = __half22float2(bits_h2(vsw[nt]));
+        const float2 zf = __half22float2(bits_h2(vzw[nt]));
+        const float pp0 = p[2 * nt] * sf.x, pp1 = p[2 * nt + 1] * sf.y;
+        const __half2 hh = __floats2half2_rn(pp0, pp1);
+        const float2 hf = __half22float2(hh);
+        phi[nt] = h2_bits(hh);
+        plo[nt] = pack_rn_f16x2(pp0 - hf.x, pp1 - hf.y);
+        l_run += p[2 * nt] + p[2 * nt + 1];
+        vz_run = fmaf(p[2 * nt], zf.x, fmaf(p[2 * nt + 1], zf.y, vz_run));
+      }
+
+      // ---- o += p' . codes ----
+      uint32_t vw[P::VW];
+#pragma unroll
+      for (int c = 0; c < P::VW / 4; ++c) {
+        const uint4 x = vcw[c * 32 + lane];
+        vw[4 * c] = x.x;
+        vw[4 * c + 1] = x.y;
+        vw[4 * c + 2] = x.z;
+        vw[4 * c + 3] = x.w;
+      }
+#pragma unroll
+      for (int ks = 0; ks < 2; ++ks) {
+        const uint32_t A0 = phi[2 * ks], A1 = plo[2 * ks], A2 = phi[2 * ks + 1], A3 = plo[2 * ks + 1];
+#pragma unroll
+        for (int q = 0; q < P::NQ; ++q) {
+          if constexpr (VB == 2) {
+            const uint32_t w = vw[ks * P::NQ + q];
+            const uint32_t l6 = w << 6, l2 = w << 2, r2 = w >> 2, r6 = w >> 6;
+            mma16816(o_acc[4 * q + 0], A0, A1, A2, A3, l6 & kMaskP6, r2 & kMaskP6);
+            mma16816(o_acc[4 * q + 1], A0, A1, A2, A3, l6 & kMaskP8, r2 & kMaskP8);
+            mma16816(o_acc[4 * q + 2], A0, A1, A2, A3, l2 & kMaskP6, r6 & kMaskP6);
+            mma16816(o_acc[4 * q + 3], A0, A1, A2, A3, l2 & kMaskP8, r6 & kMaskP8);
+          } else {
+            const uint32_t w0 = vw[(2 * ks) * P::NQ + q], w1 = vw[(2 * ks + 1) * P::NQ + q];
+            mma16816(o_acc[4 * q + 0], A0, A1, A2, A3, (w0 << 6) & kMask4, (w1 << 6) & kMask4);
+            mma16816(o_acc[4 * q + 1], A0, A1, A2, A3, (w0 << 2) & kMask4, (w1 << 2) & kMask4);
+            mma16816(o_acc[4 * q + 2], A0, A1, A2, A3, (w0 >> 2) & kMask4, (w1 >> 2) & kMask4);
+            mma16816(o_acc[4 * q + 3], A0, A1, A2, A3, (w0 >> 6) & kMask4, (w1 >> 6) & kMask4);
+          }
+        }
+      }
+
+      // release the stage and refill it with the group STAGES ahead
+      __syncwarp();
+      if (lane == 0 && j + STAGES < n_mine) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        issue(j + STAGES);
+      }
+    }
+    if (timed_out) {
+      if (lane == 0) report_timeout(a.status);
+      // let the copies already in flight land before the stages are reused
+      for (int jj = j; jj < n_mine && jj < j + STAGES; ++jj) (void)mbar_wait_bounded(&bar[jj % STAGES], (jj / STAGES) & 1);
+      m_run = -INFINITY;
+      l_run = 0.0f;
+      vz_run = 0.0f;
+#pragma unroll
+      for (int i = 0; i < P::NTV; ++i) o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.0f;
+    }
+    l_run = quad_sum(l_run);
+    vz_run = quad_sum(vz_run);
+  } else {
+    // --------------------- fp16 window (CUDA cores, fp32) ---------------------
+    float* qf = reinterpret_cast<float*>(area + CombineSmem<D>::BYTES);  // [8][D]
+    for (int i = tid; i < gq * D; i += 128)
+      qf[i] = __half2float(reinterpret_cast<const __half*>(a.q)[(static_cast<long long>(b) * a.q_heads + h * gq) * D + i]);
+    __syncthreads();
+    const int t = warp * 32 + lane;
+    const bool valid = t < a.n_resid;
+    float s[kMaxGqa];
+#pragma unroll
+    for (int r = 0; r < kMaxGqa; ++r) s[r] = 0.0f;
+    if (valid) {
+      const __half* krow = reinterpret_cast<const __half*>(a.k_res) + (bh * a.res_cap + t) * D;
+      for (int c = 0; c < D; c += 8) {
+        const uint4 kv = *reinterpret_cast<const uint4*>(krow + c);
+        const uint32_t kwd[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 kf = __half22float2(bits_h2(kwd[i]));
+#pragma unroll
+          for (int r = 0; r < kMaxGqa; ++r) {
+            if (r < gq) {
+              s[r] = fmaf(qf[r * D + c + 2 * i], kf.x, s[r]);
+              s[r] = fmaf(qf[r * D + c + 2 * i + 1], kf.y, s[r]);
+            }
+          }
+        }
+      }
+    }
+    float pr[kMaxGqa];
+#pragma unroll
+    for (int r = 0; r < kMaxGqa; ++r) {
+      const float sv = valid ? s[r] * a.scale_log2 : -INFINITY;
+      rw_m[r] = warp_max(sv);
+      pr[r] = (rw_m[r] == -INFINITY) ? 0.0f : fast_exp2(sv - rw_m[r]);
+      rw_l[r] = warp_sum(pr[r]);
+#pragma unroll
+      for (int i = 0; i < D / 32; ++i) rw_o[r][i] = 0.0f;
+    }
+    const int nvalid = min(32, a.n_resid - warp * 32);
+    for (int tt = 0; tt < nvalid; ++tt) {
+      const __half* vrow = reinterpret_cast<const __half*>(a.v_res) + (bh * a.res_cap + warp * 32 + tt) * D + (D / 32) * lane;
+      float vf[D / 32];
+      if constexpr (D == 128) {
+        const uint2 vv = *reinterpret_cast<const uint2*>(vrow);
+        const float2 f0 = __half22float2(bits_h2(vv.x)), f1 = __half22float2(bits_h2(vv.y));
+        vf[0] = f0.x;
+        vf[1] = f0.y;
+        vf[2] = f1.x;
+        vf[3] = f1.y;
+      } else {
+        const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(vrow));
+        vf[0] = f0.x;
+        vf[1] = f0.y;
+      }
+#pragma unroll
+      for (int r = 0; r < kMaxGqa; ++r) {
+        const float pt = __shfl_sync(0xffffffffu, pr[r], tt);
+#pragma unroll
+        for (int i = 0; i < D / 32; ++i) rw_o[r][i] = fmaf(pt, vf[i], rw_o[r][i]);
+      }
+    }
+  }
+
+  // ------------------------------- combine the 4 warps -------------------------------
+  __syncthreads();  // every warp is done with its stages; the area is reused below
+  if (split < a.splits_g) {
+    constexpr bool kTwoFields = (VB == 2);
+#pragma unroll
+    for (int nt = 0; nt < P::NTV; ++nt) {
+      const float om = (kTwoFields && (nt & 1)) ? kInvP8 : kInvP6;
+      const int c = 8 * nt + 2 * tig;
+      o_s[(warp * 8 + g) * D + c] = fmaf(o_acc[nt][0] + o_acc[nt][2], om, vz_run);
+      o_s[(warp * 8 + g) * D + c + 1] = fmaf(o_acc[nt][1] + o_acc[nt][3], om, vz_run);
+    }
+    if (tig == 0) {
+      m_s[warp * 8 + g] = m_run;
+      l_s[warp * 8 + g] = l_run;
+    }
+  } else {
+#pragma unroll
+    for (int r = 0; r < kMaxGqa; ++r) {
+#pragma unroll
+      for (int i = 0; i < D / 32; ++i) o_s[(warp * 8 + r) * D + (D / 32) * lane + i] = rw_o[r][i];
+      if (lane == 0) {
+        m_s[warp * 8 + r] = rw_m[r];
+        l_s[warp * 8 + r] = rw_l[r];
+      }
+    }
+  }
+  __syncthreads();
+  for (int i = tid; i < gq * D; i += 128) {
+    const int r = i / D, c = i % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) M = fmaxf(M, m_s[w * 8 + r]);
+    float L = 0.0f, O = 0.0f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const float f = fast_exp2(m_s[w * 8 + r] - M);
+        L = fmaf(l_s[w * 8 + r], f, L);
+        O = fmaf(o_s[(w * 8 + r) * D + c], f, O);
+      }
+    }
+    const long long row = (static_cast<long long>(b) * a.q_heads + h * gq + r) * a.splits_total + split;
+    a.part_o[row * D + c] = O;
+    if (c == 0) {
+      a.part_ml[row * 2] = M;
+      a.part_ml[row * 2 + 1] = L;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Log-sum-exp merge of the split partials: one block per (b, query head)
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(128) merge_kernel(MergeArgs a) {
+  __shared__ float w_s[kMaxSplits];
+  __shared__ float inv_l;
+  const long long row = blockIdx.x;
+  const int S = a.splits_total;
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    float M = -INFINITY;
+    for (int s = lane; s < S; s += 32) M = fmaxf(M, a.part_ml[(row * S + s) * 2]);
+    M = warp_max(M);
+    float L = 0.0f;
+    for (int s = lane; s < S; s += 32) {
+      const float m = a.part_ml[(row * S + s) * 2];
+      const float f = (M == -INFINITY) ? 0.0f : fast_exp2(m - M);
+      w_s[s] = f;
+      L = fmaf(f, a.part_ml[(row * S + s) * 2 + 1], L);
+    }
+    L = warp_sum(L);
+    if (lane == 0) inv_l = (L > 0.0f) ? 1.0f / L : 0.0f;
+  }
+  __syncthreads();
+  for (int c = threadIdx.x; c < a.head_dim; c += blockDim.x) {
+    float O = 0.0f;
+    for (int s = 0; s < S; ++s) O = fmaf(w_s[s], a.part_o[(row * S + s) * a.head_dim + c], O);
+    O *= inv_l;
+    if (a.out_fp32)
+      reinterpret_cast<float*>(a.out)[row * a.head_dim + c] = O;
+    else
+      reinterpret_cast<__half*>(a.out)[row * a.head_dim + c] = __float2half_rn(O);
+  }
+}
+
+constexpr int kDecodeStages = 4;
+
+template <int D, int KB, int VB>
+cudaError_t quantize_dispatch(const QuantGroupsArgs& a, cudaStream_t s) {
+  dim3 grid(a.n_groups, a.kv_heads, a.batch);
+  kivi_quantize_kernel<D, KB, VB><<<grid, 128, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+template <int D, int KB, int VB>
+cudaError_t decode_dispatch(const KiviDecodeArgs& a, cudaStream_t s) {
+  constexpr int smem = DecodeSmem<D, KB, VB, kDecodeStages>::BYTES;
+  auto kern = kivi_decode_kernel<D, KB, VB, kDecodeStages>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(a.splits_total, a.kv_heads, a.batch);
+  kern<<<grid, 128, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_kivi_quantize(const QuantGroupsArgs& a, cudaStream_t s) {
+  if (a.n_groups <= 0) return cudaSuccess;
+  const int key = a.head_dim * 100 + a.k_bits * 10 + a.v_bits;
+  switch (key) {
+    case 6422: return quantize_dispatch<64, 2, 2>(a, s);
+    case 6424: return quantize_dispatch<64, 2, 4>(a, s);
+    case 6442: return quantize_dispatch<64, 4, 2>(a, s);
+    case 6444: return quantize_dispatch<64, 4, 4>(a, s);
+    case 12822: return quantize_dispatch<128, 2, 2>(a, s);
+    case 12824: return quantize_dispatch<128, 2, 4>(a, s);
+    case 12842: return quantize_dispatch<128, 4, 2>(a, s);
+    case 12844: return quantize_dispatch<128, 4, 4>(a, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_kivi_decode(const KiviDecodeArgs& a, cudaStream_t s) {
+  const int key = a.head_dim * 100 + a.k_bits * 10 + a.v_bits;
+  switch (key) {
+    case 6422: return decode_dispatch<64, 2, 2>(a, s);
+    case 6424: return decode_dispatch<64, 2, 4>(a, s);
+    case 6442: return decode_dispatch<64, 4, 2>(a, s);
+    case 6444: return decode_dispatch<64, 4, 4>(a, s);
+    case 12822: return decode_dispatch<128, 2, 2>(a, s);
+    case 12824: return decode_dispatch<128, 2, 4>(a, s);
+    case 12842: return decode_dispatch<128, 4, 2>(a, s);
+    case 12844: return decode_dispatch<128, 4, 4>(a, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_copy_tokens(const CopyTokensArgs& a, cudaStream_t s) {
+  if (a.n_tokens <= 0) return cudaSuccess;
+  const long long total = static_cast<long long>(a.n_tokens) * (a.head_dim / 8) * a.bh;
+  const int blocks = static_cast<int>((total + 255) / 256 < 4096 ? (total + 255) / 256 : 4096);
+  copy_tokens_kernel<<<blocks, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_merge(const MergeArgs& a, cudaStream_t s) {
+  merge_kernel<<<a.rows, 128, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+int device_sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+}  // namespace kvq

@@ -1,0 +1,108 @@
+// Launch interface between the C-ABI host layer (api.cu) and the kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace kvq {
+
+// Quantize n_groups groups of 32 tokens per (batch row, kv head) from an fp16
+// source into the grouped region, starting at group index dst_group0.
+struct QuantGroupsArgs {
+  const uint16_t* k_src;
+  const uint16_t* v_src;
+  long long src_bh_stride;  // fp16 elements between consecutive (b, h) rows of the source
+  int src_tok0;             // first source token
+  int n_groups;
+  int dst_group0;
+  int batch, kv_heads, head_dim, k_bits, v_bits, groups_cap;
+  uint8_t* k_codes;
+  uint8_t* k_meta;
+  uint8_t* v_codes;
+  uint8_t* v_meta;
+};
+cudaError_t launch_kivi_quantize(const QuantGroupsArgs& a, cudaStream_t s);
+
+// Copy n_tokens fp16 rows of D channels for every (b, h) (K and V together).
+struct CopyTokensArgs {
+  const uint16_t* k_src;
+  const uint16_t* v_src;
+  long long src_bh_stride;
+  int src_tok0;
+  uint16_t* k_dst;
+  uint16_t* v_dst;
+  long long dst_bh_stride;
+  int dst_tok0;
+  int n_tokens;
+  int bh;
+  int head_dim;
+};
+cudaError_t launch_copy_tokens(const CopyTokensArgs& a, cudaStream_t s);
+
+struct KiviDecodeArgs {
+  const uint8_t* k_codes;
+  const uint8_t* k_meta;
+  const uint8_t* v_codes;
+  const uint8_t* v_meta;
+  const uint16_t* k_res;
+  const uint16_t* v_res;
+  const uint16_t* q;
+  int batch, kv_heads, q_heads, head_dim, k_bits, v_bits, groups_cap, res_cap;
+  int n_groups, n_resid;
+  int splits_g;           // thread-block splits over the grouped region
+  int groups_per_split;
+  int splits_total;       // splits_g (+1 when the window is not empty)
+  float scale_log2;       // softmax scale * log2(e)
+  float* part_o;          // [B, Hq, splits_total, D]
+  float* part_ml;         // [B, Hq, splits_total, 2]
+  uint32_t* status;
+};
+cudaError_t launch_kivi_decode(const KiviDecodeArgs& a, cudaStream_t s);
+
+struct MergeArgs {
+  const float* part_o;
+  const float* part_ml;
+  int splits_total;
+  int rows;  // B * Hq
+  int head_dim;
+  void* out;
+  int out_fp32;
+};
+cudaError_t launch_merge(const MergeArgs& a, cudaStream_t s);
+
+struct Fp8QuantArgs {
+  const uint16_t* x;
+  int batch, kv_heads, seq_len, head_dim;
+  const int32_t* block_table;
+  int max_blocks;
+  int num_blocks;
+  uint8_t* pool;
+  float* scale;
+  int static_scale;
+  int value_layout;
+  uint32_t* amax_partials;
+  int amax_blocks;
+};
+cudaError_t launch_fp8_quantize(const Fp8QuantArgs& a, cudaStream_t s);
+
+struct Fp8DecodeArgs {
+  const uint16_t* q;
+  const uint8_t* k_pool;
+  const uint8_t* v_pool;
+  const float* k_scale;
+  const float* v_scale;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  int batch, q_heads, kv_heads, head_dim, max_blocks, num_blocks;
+  int splits;
+  int blocks_per_split;
+  float scale_log2;
+  float* part_o;
+  float* part_ml;
+  uint32_t* status;
+};
+cudaError_t launch_fp8_decode(const Fp8DecodeArgs& a, cudaStream_t s);
+
+int device_sm_count();
+
+}  // namespace kvq

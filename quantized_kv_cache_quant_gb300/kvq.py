@@ -1,0 +1,246 @@
+"""Python binding of libkvq (the C ABI declared in include/kvq.h).
+
+Argument marshalling only: every function here forwards to the C function of
+the same name through ctypes; all work runs in the library's CUDA kernels.
+PyTorch supplies device memory and the current CUDA stream. Importing this
+module raises ImportError when the library has not been built — there is no
+fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional, Sequence
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "libkvq.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"libkvq.so not found at {LIB_PATH}; build it with "
+        "`python -m quantized_kv_cache_quant_gb300.build` (needs nvcc)")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+c_i32, c_sz, c_vp, c_f32 = ctypes.c_int32, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_float
+
+EXPORTED = (
+    "kvq_status_string", "kivi_cache_sizes", "kivi_cache_init", "kv_quant_prefill", "kv_append_token",
+    "kv_flush_residual", "kv_decode_workspace_bytes", "kv_decode_attention", "fp8_quantize_workspace_bytes",
+    "fp8_kv_quantize", "fp8_decode_workspace_bytes", "fp8_decode_attention",
+)
+
+STATUS = {0: "KVQ_OK", 1: "KVQ_ERR_NULL", 2: "KVQ_ERR_ARG", 3: "KVQ_ERR_SHAPE", 4: "KVQ_ERR_CAPACITY",
+          5: "KVQ_ERR_WORKSPACE", 6: "KVQ_ERR_UNSUPPORTED", 7: "KVQ_ERR_CUDA", 8: "KVQ_ERR_TIMEOUT",
+          9: "KVQ_ERR_ALIGN"}
+WS_STATUS_TIMEOUT = 1
+
+
+class KvqError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        self.name = STATUS.get(code, str(code))
+        super().__init__(f"{where}: {self.name} ({_lib.kvq_status_string(code).decode()})")
+
+
+class kivi_config(ctypes.Structure):
+    _fields_ = [(n, c_i32) for n in ("batch", "kv_heads", "q_heads", "head_dim", "k_bits", "v_bits",
+                                    "group_size", "residual_len", "max_tokens")]
+
+
+class kivi_cache(ctypes.Structure):
+    _fields_ = [("cfg", kivi_config), ("k_codes", c_vp), ("k_meta", c_vp), ("v_codes", c_vp), ("v_meta", c_vp),
+                ("k_res", c_vp), ("v_res", c_vp), ("groups_cap", c_i32), ("res_cap", c_i32),
+                ("n_grouped", c_i32), ("n_resid", c_i32)]
+
+
+_P_CFG, _P_CACHE = ctypes.POINTER(kivi_config), ctypes.POINTER(kivi_cache)
+_SIG = {
+    "kvq_status_string": ([ctypes.c_int], ctypes.c_char_p),
+    "kivi_cache_sizes": ([_P_CFG, ctypes.POINTER(c_sz)], ctypes.c_int),
+    "kivi_cache_init": ([_P_CACHE, _P_CFG, ctypes.POINTER(c_vp)], ctypes.c_int),
+    "kv_quant_prefill": ([_P_CACHE, c_vp, c_vp, c_i32, c_vp], ctypes.c_int),
+    "kv_append_token": ([_P_CACHE, c_vp, c_vp, c_vp], ctypes.c_int),
+    "kv_flush_residual": ([_P_CACHE, c_vp], ctypes.c_int),
+    "kv_decode_workspace_bytes": ([_P_CFG], c_sz),
+    "kv_decode_attention": ([_P_CACHE, c_vp, c_vp, c_i32, c_f32, c_vp, c_sz, c_vp], ctypes.c_int),
+    "fp8_quantize_workspace_bytes": ([c_i32, c_i32, c_i32, c_i32], c_sz),
+    "fp8_kv_quantize": ([c_vp, c_i32, c_i32, c_i32, c_i32, c_vp, c_i32, c_i32, c_i32, c_vp, c_vp, c_i32, c_i32,
+                         c_vp, c_sz, c_vp], ctypes.c_int),
+    "fp8_decode_workspace_bytes": ([c_i32, c_i32, c_i32], c_sz),
+    "fp8_decode_attention": ([c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, c_i32, c_i32, c_i32, c_i32, c_i32,
+                              c_i32, c_i32, c_vp, c_i32, c_f32, c_vp, c_sz, c_vp], ctypes.c_int),
+}
+for _name, (_args, _res) in _SIG.items():
+    _fn = getattr(_lib, _name)
+    _fn.argtypes = _args
+    _fn.restype = _res
+
+
+def _ptr(x) -> Optional[int]:
+    """A device/host address from a torch tensor, an int or None."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(code: int, where: str) -> None:
+    if code != 0:
+        raise KvqError(code, where)
+
+
+# ---------------------------------------------------------------------------
+# thin wrappers, same names as the C ABI
+# ---------------------------------------------------------------------------
+
+def kvq_status_string(code: int) -> str:
+    return _lib.kvq_status_string(code).decode()
+
+
+def make_config(batch, kv_heads, q_heads, head_dim, k_bits=2, v_bits=2, residual_len=128, max_tokens=0,
+                group_size=32) -> kivi_config:
+    return kivi_config(batch, kv_heads, q_heads, head_dim, k_bits, v_bits, group_size, residual_len, max_tokens)
+
+
+def kivi_cache_sizes(cfg: kivi_config) -> list:
+    out = (c_sz * 6)()
+    _check(_lib.kivi_cache_sizes(ctypes.byref(cfg), out), "kivi_cache_sizes")
+    return list(out)
+
+
+def kivi_cache_init(cfg: kivi_config, bufs: Sequence) -> kivi_cache:
+    cache = kivi_cache()
+    arr = (c_vp * 6)(*[_ptr(b) for b in bufs])
+    _check(_lib.kivi_cache_init(ctypes.byref(cache), ctypes.byref(cfg), arr), "kivi_cache_init")
+    return cache
+
+
+def kv_quant_prefill(cache: kivi_cache, k, v, seq_len: int, stream=None) -> None:
+    _check(_lib.kv_quant_prefill(ctypes.byref(cache), _ptr(k), _ptr(v), seq_len, _stream(stream)), "kv_quant_prefill")
+
+
+def kv_append_token(cache: kivi_cache, k_new, v_new, stream=None) -> None:
+    _check(_lib.kv_append_token(ctypes.byref(cache), _ptr(k_new), _ptr(v_new), _stream(stream)), "kv_append_token")
+
+
+def kv_flush_residual(cache: kivi_cache, stream=None) -> None:
+    _check(_lib.kv_flush_residual(ctypes.byref(cache), _stream(stream)), "kv_flush_residual")
+
+
+def kv_decode_workspace_bytes(cfg: kivi_config) -> int:
+    return int(_lib.kv_decode_workspace_bytes(ctypes.byref(cfg)))
+
+
+def kv_decode_attention(cache: kivi_cache, q, out, out_fp32: bool, softmax_scale: float, ws, ws_bytes: int,
+                        stream=None) -> None:
+    _check(_lib.kv_decode_attention(ctypes.byref(cache), _ptr(q), _ptr(out), int(bool(out_fp32)),
+                                    float(softmax_scale), _ptr(ws), ws_bytes, _stream(stream)),
+           "kv_decode_attention")
+
+
+def fp8_quantize_workspace_bytes(batch, kv_heads, seq_len, head_dim) -> int:
+    return int(_lib.fp8_quantize_workspace_bytes(batch, kv_heads, seq_len, head_dim))
+
+
+def fp8_kv_quantize(x, batch, kv_heads, seq_len, head_dim, block_table, max_blocks, block_size, num_blocks, pool,
+                    scale, static_scale: bool, value_layout: int, ws, ws_bytes: int, stream=None) -> None:
+    _check(_lib.fp8_kv_quantize(_ptr(x), batch, kv_heads, seq_len, head_dim, _ptr(block_table), max_blocks,
+                                block_size, num_blocks, _ptr(pool), _ptr(scale), int(bool(static_scale)),
+                                value_layout, _ptr(ws), ws_bytes, _stream(stream)), "fp8_kv_quantize")
+
+
+def fp8_decode_workspace_bytes(batch, q_heads, head_dim) -> int:
+    return int(_lib.fp8_decode_workspace_bytes(batch, q_heads, head_dim))
+
+
+def fp8_decode_attention(q, k_pool, v_pool, k_scale, v_scale, block_table, seq_lens, batch, q_heads, kv_heads,
+                         head_dim, block_size, max_blocks, num_blocks, max_seq_len, out, out_fp32: bool,
+                         softmax_scale: float, ws, ws_bytes: int, stream=None) -> None:
+    _check(_lib.fp8_decode_attention(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(k_scale), _ptr(v_scale),
+                                     _ptr(block_table), _ptr(seq_lens), batch, q_heads, kv_heads, head_dim,
+                                     block_size, max_blocks, num_blocks, max_seq_len, _ptr(out),
+                                     int(bool(out_fp32)), float(softmax_scale), _ptr(ws), ws_bytes,
+                                     _stream(stream)), "fp8_decode_attention")
+
+
+# ---------------------------------------------------------------------------
+# torch-owned buffers around the descriptors (allocation only; no compute)
+# ---------------------------------------------------------------------------
+
+def _alloc_bytes(n: int, device):
+    import torch
+    # 256-byte aligned: the caching allocator hands out 512-byte aligned blocks
+    return torch.empty(max(n, 1), dtype=torch.uint8, device=device)
+
+
+class KiviCache:
+    """One layer's KIVI cache in device memory owned by PyTorch."""
+
+    NAMES = ("k_codes", "k_meta", "v_codes", "v_meta", "k_res", "v_res")
+
+    def __init__(self, batch, kv_heads, q_heads, head_dim, k_bits=2, v_bits=2, residual_len=128, max_tokens=0,
+                 device="cuda"):
+        import torch
+        self.cfg = make_config(batch, kv_heads, q_heads, head_dim, k_bits, v_bits, residual_len, max_tokens)
+        sizes = kivi_cache_sizes(self.cfg)
+        self.buffers = {n: _alloc_bytes(s, device) for n, s in zip(self.NAMES, sizes)}
+        self.desc = kivi_cache_init(self.cfg, [self.buffers[n] for n in self.NAMES])
+        self.ws_bytes = kv_decode_workspace_bytes(self.cfg)
+        self.ws = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=device)
+
+    @property
+    def n_grouped(self) -> int:
+        return self.desc.n_grouped
+
+    @property
+    def n_resid(self) -> int:
+        return self.desc.n_resid
+
+    def prefill(self, k, v, stream=None):
+        kv_quant_prefill(self.desc, k, v, k.shape[2], stream)
+
+    def append(self, k_new, v_new, stream=None):
+        kv_append_token(self.desc, k_new, v_new, stream)
+
+    def flush(self, stream=None):
+        kv_flush_residual(self.desc, stream)
+
+    def decode(self, q, out=None, out_fp32=True, softmax_scale=0.0, stream=None):
+        import torch
+        if out is None:
+            out = torch.empty(q.shape, dtype=torch.float32 if out_fp32 else torch.float16, device=q.device)
+        kv_decode_attention(self.desc, q, out, out_fp32, softmax_scale, self.ws, self.ws_bytes, stream)
+        return out
+
+    def status(self) -> int:
+        """Status word of the workspace (bit 0: a device wait timed out). Synchronizes."""
+        return int(self.ws[:4].view(__import__("torch").int32).item())
+
+    def grouped_view(self, name: str):
+        """Device bytes of one grouped record as ``[B, H, groups_cap, bytes]`` (uint8)."""
+        cfg = self.cfg
+        per = {"k_codes": 32 * cfg.head_dim * cfg.k_bits // 8, "k_meta": 4 * cfg.head_dim,
+               "v_codes": 32 * cfg.head_dim * cfg.v_bits // 8, "v_meta": 128}[name]
+        return self.buffers[name][: cfg.batch * cfg.kv_heads * self.desc.groups_cap * per].view(
+            cfg.batch, cfg.kv_heads, self.desc.groups_cap, per)
+
+    def residual_view(self, name: str):
+        cfg = self.cfg
+        n = cfg.batch * cfg.kv_heads * self.desc.res_cap * cfg.head_dim * 2
+        return self.buffers[name][:n].view(__import__("torch").float16).view(
+            cfg.batch, cfg.kv_heads, self.desc.res_cap, cfg.head_dim)
+
+
+def default_softmax_scale(head_dim: int) -> float:
+    return 1.0 / math.sqrt(head_dim)

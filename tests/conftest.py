@@ -8,7 +8,17 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 
+def _ensure_library():
+    """Build libkvq.so once if it is missing and nvcc is available."""
+    import shutil
+    lib = os.path.join(ROOT, "quantized_kv_cache_quant_gb300", "lib", "libkvq.so")
+    if not os.path.exists(lib) and (shutil.which("nvcc") or os.path.exists("/usr/local/cuda/bin/nvcc")):
+        from quantized_kv_cache_quant_gb300 import build
+        build.build()
+
+
 def pytest_configure(config):
+    _ensure_library()
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a) and the built CUDA library")
     config.addinivalue_line("markers", "slow: full-size workload (minutes)")
 

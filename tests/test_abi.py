@@ -1,0 +1,187 @@
+"""The C-ABI library: it loads, exports every declared symbol, and its host-side
+validation (no kernel launches, no GPU needed) returns the documented codes and
+leaves the cache descriptor unchanged on error."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from oracle import sizes
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kvq.h")
+
+kvq = pytest.importorskip("quantized_kv_cache_quant_gb300.kvq", reason="libkvq.so not built")
+
+ALIGNED = 1 << 20  # a fake, 256-byte aligned address: validation never dereferences it
+
+
+def declared_functions():
+    text = open(HEADER, encoding="utf-8").read()
+    return re.findall(r"KVQ_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+
+
+def test_every_declared_symbol_is_exported():
+    names = declared_functions()
+    assert len(names) == 12
+    lib = ctypes.CDLL(kvq.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(names) == sorted(kvq.EXPORTED)
+
+
+def test_status_strings():
+    for code, name in kvq.STATUS.items():
+        assert kvq.kvq_status_string(code)
+    assert kvq.kvq_status_string(0) == "ok"
+
+
+@pytest.mark.parametrize("b,h,hq,d,kb,vb,r,t", [
+    (1, 2, 2, 64, 2, 2, 128, 272),
+    (8, 32, 32, 128, 2, 2, 128, 4097),
+    (32, 8, 64, 128, 4, 4, 128, 8193),
+    (4, 8, 64, 128, 2, 2, 128, 131584),
+    (2, 3, 6, 64, 2, 4, 0, 100),
+])
+def test_cache_sizes_match_layout(b, h, hq, d, kb, vb, r, t):
+    cfg = kvq.make_config(b, h, hq, d, kb, vb, r, t)
+    got = kvq.kivi_cache_sizes(cfg)
+    want = sizes.kivi_buffer_bytes(b, h, d, kb, vb, r, t)
+    assert got == [want[n] for n in ("k_codes", "k_meta", "v_codes", "v_meta", "k_res", "v_res")]
+    ws = kvq.kv_decode_workspace_bytes(cfg)
+    assert ws == 256 + b * hq * 64 * (d + 2) * 4
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("head_dim", 96, "KVQ_ERR_UNSUPPORTED"),
+    ("k_bits", 3, "KVQ_ERR_UNSUPPORTED"),
+    ("v_bits", 8, "KVQ_ERR_UNSUPPORTED"),
+    ("group_size", 64, "KVQ_ERR_UNSUPPORTED"),
+    ("residual_len", 100, "KVQ_ERR_ARG"),
+    ("residual_len", -32, "KVQ_ERR_ARG"),
+    ("q_heads", 12, "KVQ_ERR_SHAPE"),
+    ("q_heads", 144, "KVQ_ERR_UNSUPPORTED"),
+    ("batch", 0, "KVQ_ERR_ARG"),
+    ("max_tokens", 0, "KVQ_ERR_ARG"),
+])
+def test_bad_config(field, value, code):
+    cfg = kvq.make_config(2, 8, 64, 128, 2, 2, 128, 1024)
+    setattr(cfg, field, value)
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.kivi_cache_sizes(cfg)
+    assert e.value.name == code
+    assert kvq.kv_decode_workspace_bytes(cfg) == 0
+
+
+def _fake_cache(n_grouped=0, n_resid=0, **kw):
+    args = dict(batch=2, kv_heads=2, q_heads=4, head_dim=64, k_bits=2, v_bits=2, residual_len=128, max_tokens=512)
+    args.update(kw)
+    cfg = kvq.make_config(**args)
+    cache = kvq.kivi_cache_init(cfg, [ALIGNED * (i + 1) for i in range(6)])
+    cache.n_grouped, cache.n_resid = n_grouped, n_resid
+    return cfg, cache
+
+
+def test_init_checks_pointers():
+    cfg = kvq.make_config(2, 2, 4, 64, 2, 2, 128, 512)
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.kivi_cache_init(cfg, [ALIGNED, ALIGNED, None, ALIGNED, ALIGNED, ALIGNED])
+    assert e.value.name == "KVQ_ERR_NULL"
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.kivi_cache_init(cfg, [ALIGNED, ALIGNED + 16, ALIGNED, ALIGNED, ALIGNED, ALIGNED])
+    assert e.value.name == "KVQ_ERR_ALIGN"
+    _, cache = _fake_cache()
+    assert (cache.groups_cap, cache.res_cap, cache.n_grouped, cache.n_resid) == (16, 128, 0, 0)
+    _, c0 = _fake_cache(residual_len=0)
+    assert c0.res_cap == 32
+
+
+def _snapshot(cache):
+    return (cache.n_grouped, cache.n_resid, cache.k_codes, cache.v_res)
+
+
+def test_prefill_validation_leaves_state():
+    _, cache = _fake_cache(64, 10)
+    before = _snapshot(cache)
+    for args, code in [((ALIGNED, ALIGNED, 513), "KVQ_ERR_CAPACITY"),
+                       ((ALIGNED, ALIGNED, -1), "KVQ_ERR_ARG"),
+                       ((None, ALIGNED, 10), "KVQ_ERR_NULL"),
+                       ((ALIGNED + 2, ALIGNED, 10), "KVQ_ERR_ALIGN")]:
+        with pytest.raises(kvq.KvqError) as e:
+            kvq.kv_quant_prefill(cache, *args, stream=0)
+        assert e.value.name == code
+        assert _snapshot(cache) == before
+
+
+def test_append_capacity_and_state():
+    _, cache = _fake_cache(384, 128)   # 512 tokens = max_tokens
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.kv_append_token(cache, ALIGNED, ALIGNED, stream=0)
+    assert e.value.name == "KVQ_ERR_CAPACITY"
+    assert (cache.n_grouped, cache.n_resid) == (384, 128)
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.kv_append_token(cache, None, ALIGNED, stream=0)
+    assert e.value.name == "KVQ_ERR_NULL"
+
+
+def test_corrupt_descriptor_is_rejected():
+    _, cache = _fake_cache(40, 0)       # not a multiple of 32
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.kv_flush_residual(cache, stream=0)
+    assert e.value.name == "KVQ_ERR_ARG"
+    _, cache = _fake_cache(0, 129)      # window over capacity
+    with pytest.raises(kvq.KvqError):
+        kvq.kv_append_token(cache, ALIGNED, ALIGNED, stream=0)
+
+
+def test_flush_noop_when_window_short():
+    _, cache = _fake_cache(64, 31)
+    kvq.kv_flush_residual(cache, stream=0)   # fewer than 32 tokens: nothing to do, no launch
+    assert (cache.n_grouped, cache.n_resid) == (64, 31)
+
+
+def test_decode_validation():
+    cfg, cache = _fake_cache(0, 0)
+    ws = kvq.kv_decode_workspace_bytes(cfg)
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.kv_decode_attention(cache, ALIGNED, ALIGNED, True, 0.0, ALIGNED, ws, stream=0)
+    assert e.value.name == "KVQ_ERR_ARG"                  # empty cache
+    _, cache = _fake_cache(64, 3)
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.kv_decode_attention(cache, ALIGNED, ALIGNED, True, 0.0, ALIGNED, ws - 1, stream=0)
+    assert e.value.name == "KVQ_ERR_WORKSPACE"
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.kv_decode_attention(cache, ALIGNED, ALIGNED, True, 0.0, None, ws, stream=0)
+    assert e.value.name == "KVQ_ERR_WORKSPACE"
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.kv_decode_attention(cache, ALIGNED, ALIGNED, True, float("nan"), ALIGNED, ws, stream=0)
+    assert e.value.name == "KVQ_ERR_ARG"
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.kv_decode_attention(cache, ALIGNED + 8, ALIGNED, True, 0.0, ALIGNED, ws, stream=0)
+    assert e.value.name == "KVQ_ERR_ALIGN"
+
+
+def test_fp8_validation():
+    q = dict(x=ALIGNED, batch=2, kv_heads=2, seq_len=40, head_dim=128, block_table=ALIGNED, max_blocks=3,
+             block_size=16, num_blocks=6, pool=ALIGNED, scale=ALIGNED, static_scale=False, value_layout=0,
+             ws=ALIGNED, ws_bytes=kvq.fp8_quantize_workspace_bytes(2, 2, 40, 128))
+    for change, code in [(dict(block_size=32), "KVQ_ERR_UNSUPPORTED"), (dict(head_dim=96), "KVQ_ERR_UNSUPPORTED"),
+                         (dict(max_blocks=2), "KVQ_ERR_CAPACITY"), (dict(value_layout=2), "KVQ_ERR_ARG"),
+                         (dict(ws_bytes=8), "KVQ_ERR_WORKSPACE"), (dict(pool=None), "KVQ_ERR_NULL"),
+                         (dict(scale=ALIGNED + 4), "KVQ_ERR_ALIGN"), (dict(seq_len=0), "KVQ_ERR_ARG")]:
+        args = dict(q, **change)
+        with pytest.raises(kvq.KvqError) as e:
+            kvq.fp8_kv_quantize(**args, stream=0)
+        assert e.value.name == code, change
+    d = dict(q=ALIGNED, k_pool=ALIGNED, v_pool=ALIGNED, k_scale=ALIGNED, v_scale=ALIGNED, block_table=ALIGNED,
+             seq_lens=ALIGNED, batch=2, q_heads=8, kv_heads=2, head_dim=128, block_size=16, max_blocks=3,
+             num_blocks=6, max_seq_len=40, out=ALIGNED, out_fp32=True, softmax_scale=0.0, ws=ALIGNED,
+             ws_bytes=kvq.fp8_decode_workspace_bytes(2, 8, 128))
+    for change, code in [(dict(q_heads=7), "KVQ_ERR_SHAPE"), (dict(max_seq_len=49), "KVQ_ERR_CAPACITY"),
+                         (dict(q_heads=32), "KVQ_ERR_UNSUPPORTED"), (dict(ws_bytes=100), "KVQ_ERR_WORKSPACE"),
+                         (dict(seq_lens=None), "KVQ_ERR_NULL")]:
+        args = dict(d, **change)
+        with pytest.raises(kvq.KvqError) as e:
+            kvq.fp8_decode_attention(**args, stream=0)
+        assert e.value.name == code, change

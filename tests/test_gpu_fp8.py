@@ -1,0 +1,164 @@
+"""GPU parity of the FP8 E4M3 paged path against the CPU oracle, through the C ABI.
+
+FP8 bytes and the per-tensor scale must match bit for bit; attention must stay
+within max-abs 2e-3 and relative L2 1e-3 of the float64 oracle computed on the
+same dequantized values.
+"""
+import numpy as np
+import pytest
+
+from oracle import attention, fp8, layout
+from oracle.attention import default_scale
+from quantized_kv_cache_quant_gb300 import workloads
+
+from kvq_helpers import assert_attention_close, dev, host
+
+pytestmark = pytest.mark.gpu
+
+
+def _kvq():
+    from quantized_kv_cache_quant_gb300 import kvq
+    return kvq
+
+
+def _quantize(x16, table, num_blocks, value_layout, static_scale=None):
+    import torch
+    kvq = _kvq()
+    b, h, s, d = x16.shape
+    pool = torch.full((num_blocks, h, 16 * d), 0xAB, dtype=torch.uint8, device="cuda")
+    scale = torch.tensor([static_scale if static_scale is not None else -1.0], dtype=torch.float32, device="cuda")
+    wsb = kvq.fp8_quantize_workspace_bytes(b, h, s, d)
+    ws = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
+    xt, tt = dev(x16), dev(table)
+    kvq.fp8_kv_quantize(xt, b, h, s, d, tt, table.shape[1], 16, num_blocks, pool, scale,
+                        static_scale is not None, value_layout, ws, wsb)
+    return pool, scale
+
+
+def _oracle_pool(x16, table, num_blocks, value_layout, scale):
+    byts = fp8.quantize(x16, scale)
+    nat = fp8.scatter_paged(byts, table, num_blocks, 16)
+    return layout.fp8_pack_pool(nat, value_layout)
+
+
+def test_all_fp16_values_cast_exactly():
+    """Every fp16 bit pattern (finite and not) through the GPU cast at static scale 1."""
+    allh = np.arange(65536, dtype=np.uint16).view(np.float16)
+    x = allh.reshape(1, 4, 128, 128)                     # 4 kv heads x 128 tokens x 128 channels
+    table = np.arange(8, dtype=np.int32).reshape(1, 8)
+    for vl in (0, 1):
+        pool, scale = _quantize(x, table, 8, vl, static_scale=1.0)
+        want = _oracle_pool(x, table, 8, vl, np.float32(1.0))
+        assert np.array_equal(host(pool), want)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_dynamic_scale_and_bytes(d):
+    rng = np.random.default_rng(d)
+    x = workloads.make_inputs(3, 2, 4, d, 16 * 5 + 7, 1, 21).k          # ragged last block
+    nb = 6
+    table = rng.permutation(3 * nb + 4).astype(np.int32)[: 3 * nb].reshape(3, nb)
+    pool, scale = _quantize(x, table, 3 * nb + 4, 0)
+    s_ref = fp8.dynamic_scale(x)
+    assert host(scale)[0] == s_ref
+    got = host(pool)
+    want = _oracle_pool(x, table, 3 * nb + 4, 0, s_ref)
+    used = np.unique(table)
+    assert np.array_equal(got[used], want[used])
+    unused = np.setdiff1d(np.arange(3 * nb + 4), used)
+    assert np.all(got[unused] == 0xAB)                   # untouched
+    # the ragged last block's missing rows are zero bytes
+    nat = layout.fp8_unpack_pool(got, d, 0)
+    assert np.all(nat[table[:, -1], :, 7:, :] == 0)
+
+
+def test_saturation_with_static_scale():
+    x = np.zeros((1, 1, 16, 64), np.float16)
+    x[0, 0, 0, :4] = [1000, -700, 448, -465]
+    x[0, 0, 1, :2] = [np.inf, -np.inf]
+    table = np.zeros((1, 1), np.int32)
+    pool, _ = _quantize(x, table, 1, 0, static_scale=1.0)
+    nat = layout.fp8_unpack_pool(host(pool), 64, 0)[0, 0]
+    assert list(nat[0, :4]) == [0x7E, 0xFE, 0x7E, 0xFE]
+    assert list(nat[1, :2]) == [0x7E, 0xFE]
+
+
+def _decode(q16, kpool, vpool, kscale, vscale, table, seq_lens, hkv, num_blocks, max_seq, out_fp32=True):
+    import torch
+    kvq = _kvq()
+    b, hq, d = q16.shape
+    out = torch.empty((b, hq, d), dtype=torch.float32 if out_fp32 else torch.float16, device="cuda")
+    wsb = kvq.fp8_decode_workspace_bytes(b, hq, d)
+    ws = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
+    kvq.fp8_decode_attention(dev(q16), kpool, vpool, kscale, vscale, dev(table), dev(seq_lens.astype(np.int32)),
+                             b, hq, hkv, d, 16, table.shape[1], num_blocks, max_seq, out, out_fp32, 0.0, ws, wsb)
+    return host(out).astype(np.float64), int(host(ws[:4].view(torch.int32))[0])
+
+
+def _oracle_decode(q16, k16, v16, ks, vs, seq_lens, heads=None):
+    b, hkv, s, d = k16.shape
+    kh = lambda bi, hi: fp8.e4m3_decode(fp8.quantize(k16[bi, hi, : seq_lens[bi]], ks)) * np.float64(ks)
+    vh = lambda bi, hi: fp8.e4m3_decode(fp8.quantize(v16[bi, hi, : seq_lens[bi]], vs)) * np.float64(vs)
+    return attention.decode_attention(q16, kh, vh, hkv, default_scale(d), heads)
+
+
+@pytest.mark.parametrize("d,gq", [(128, 4), (64, 1), (128, 8), (64, 2)])
+def test_decode_ragged_lengths(d, gq):
+    rng = np.random.default_rng(d + gq)
+    b, hkv, s = 3, 2, 16 * 40 + 9
+    x = workloads.make_inputs(b, hkv, hkv * gq, d, s, 1, 31 + gq)
+    nb = -(-s // 16)
+    table = rng.permutation(b * nb).astype(np.int32).reshape(b, nb)
+    kpool, kscale = _quantize(x.k, table, b * nb, 0)
+    vpool, vscale = _quantize(x.v, table, b * nb, 1)
+    seq_lens = np.array([s, 1, 16 * 17 + 3])
+    out, status = _decode(x.q[0], kpool, vpool, kscale, vscale, table, seq_lens, hkv, b * nb, s)
+    ref = _oracle_decode(x.q[0], x.k, x.v, fp8.dynamic_scale(x.k), fp8.dynamic_scale(x.v), seq_lens)
+    assert_attention_close(out, ref)
+    assert status == 0
+    out16, _ = _decode(x.q[0], kpool, vpool, kscale, vscale, table, seq_lens, hkv, b * nb, s, out_fp32=False)
+    assert_attention_close(out16, ref, fp16_out=True)
+
+
+def test_block_table_permutation_invariance():
+    rng = np.random.default_rng(5)
+    b, hkv, hq, d, s = 2, 2, 8, 128, 16 * 24
+    x = workloads.make_inputs(b, hkv, hq, d, s, 1, 41)
+    nb = s // 16
+    ident = np.arange(b * nb, dtype=np.int32).reshape(b, nb)
+    perm = rng.permutation(b * nb).astype(np.int32).reshape(b, nb)
+    outs = []
+    for table in (ident, perm):
+        kpool, ks = _quantize(x.k, table, b * nb, 0)
+        vpool, vs = _quantize(x.v, table, b * nb, 1)
+        outs.append(_decode(x.q[0], kpool, vpool, ks, vs, table, np.array([s, s]), hkv, b * nb, s)[0])
+    assert np.array_equal(outs[0], outs[1])
+
+
+def test_full_size_fp8_32k():
+    """FP8 workload at full size: B 64, 8 kv heads, 32 q heads, D 128, 32768 tokens,
+    blocks of 16 through a random permutation. Scales exact; bytes of sampled
+    blocks exact; attention on sampled heads."""
+    import torch
+    w = workloads.FP8_32K
+    k, v, q, table = workloads.fp8_inputs(w)
+    nb_total = w.batch * w.blocks_per_seq
+    kpool, kscale = _quantize(k, table, nb_total, 0)
+    vpool, vscale = _quantize(v, table, nb_total, 1)
+    ks_ref, vs_ref = fp8.dynamic_scale(k), fp8.dynamic_scale(v)
+    assert host(kscale)[0] == ks_ref and host(vscale)[0] == vs_ref
+    rng = np.random.default_rng(3)
+    for _ in range(24):
+        b, h, j = int(rng.integers(w.batch)), int(rng.integers(w.kv_heads)), int(rng.integers(w.blocks_per_seq))
+        for x16, pool, sref, vl in ((k, kpool, ks_ref, 0), (v, vpool, vs_ref, 1)):
+            blk = table[b, j]
+            want = layout.fp8_pack_pool(fp8.quantize(x16[b, h, 16 * j:16 * j + 16], sref)[None, None], vl)[0, 0]
+            assert np.array_equal(host(pool[blk, h]), want)
+    seq_lens = np.full(w.batch, w.context)
+    out, status = _decode(q, kpool, vpool, kscale, vscale, table, seq_lens, w.kv_heads, nb_total, w.context)
+    assert status == 0
+    heads = sorted({(0, 0), (w.batch - 1, w.q_heads - 1), (17, 5), (40, 30), (63, 12), (5, 20)})
+    ref = _oracle_decode(q, k, v, ks_ref, vs_ref, seq_lens, heads)
+    assert_attention_close(out, ref, heads)
+    del kpool, vpool
+    torch.cuda.empty_cache()

@@ -1,0 +1,222 @@
+"""GPU parity of the KIVI path against the CPU oracle, through the C ABI.
+
+Codes, scales and zero points must match bit for bit; attention must stay
+within max-abs 2e-3 and relative L2 1e-3 of the float64 oracle computed on
+the same dequantized values.
+"""
+import numpy as np
+import pytest
+
+from oracle.attention import default_scale
+from quantized_kv_cache_quant_gb300 import workloads
+
+from kvq_helpers import (assert_attention_close, assert_grouped_bytes_equal, assert_residual_equal, dev, host,
+                         oracle_attention, oracle_cache)
+
+pytestmark = pytest.mark.gpu
+
+
+def _kvq():
+    from quantized_kv_cache_quant_gb300 import kvq
+    return kvq
+
+
+def _run(b, hkv, hq, d, s, kb=2, vb=2, r=128, steps=0, seed=0, max_tokens=None, out_fp32=True):
+    kvq = _kvq()
+    x = workloads.make_inputs(b, hkv, hq, d, s + steps, max(steps, 1), seed)
+    k, v = x.k[:, :, :s], x.v[:, :, :s]
+    mt = max_tokens or (s + steps + 1)
+    gc = kvq.KiviCache(b, hkv, hq, d, kb, vb, r, mt)
+    gc.prefill(dev(k), dev(v))
+    oc = oracle_cache(dict(k_bits=kb, v_bits=vb, residual=r, max_tokens=mt), k, v)
+    return kvq, x, gc, oc
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("kb,vb", [(2, 2), (4, 4), (2, 4), (4, 2)])
+def test_prefill_bytes(d, kb, vb):
+    kvq, x, gc, oc = _run(2, 3, 6, d, 32 * 7 + 128 + 5, kb, vb, seed=11)
+    assert (gc.n_grouped, gc.n_resid) == (oc.n_grouped, oc.n_resid) == (256, 101)
+    assert_grouped_bytes_equal(gc, oc)
+    assert_residual_equal(gc, oc)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("gq", [1, 2, 4, 8])
+@pytest.mark.parametrize("kb,vb", [(2, 2), (4, 4)])
+def test_decode_attention(d, gq, kb, vb):
+    s = 32 * 37 + 128 - 9          # 37 groups (several splits), a ragged window
+    kvq, x, gc, oc = _run(2, 2, 2 * gq, d, s, kb, vb, seed=100 + gq)
+    q = x.q[0]
+    out = host(gc.decode(dev(q)))
+    ref = oracle_attention(oc, q, default_scale(d))
+    assert_attention_close(out, ref)
+    assert gc.status() == 0
+
+
+def test_decode_fp16_output():
+    kvq, x, gc, oc = _run(2, 2, 16, 128, 32 * 20 + 100, seed=7)
+    q = x.q[0]
+    out = host(gc.decode(dev(q), out_fp32=False)).astype(np.float64)
+    ref = oracle_attention(oc, q, default_scale(128))
+    assert_attention_close(out, ref, fp16_out=True)
+
+
+@pytest.mark.parametrize("s", [1, 17, 100, 128])
+def test_window_only(s):
+    """S <= R: nothing is quantized; attention is exact fp16 attention."""
+    kvq, x, gc, oc = _run(2, 2, 8, 64, s, seed=s)
+    assert (gc.n_grouped, gc.n_resid) == (0, s)
+    out = host(gc.decode(dev(x.q[0])))
+    assert_attention_close(out, oracle_attention(oc, x.q[0], default_scale(64)))
+
+
+def test_fully_grouped_r0():
+    """R = 0 with S a multiple of 32: every token lives in the grouped region."""
+    kvq, x, gc, oc = _run(2, 4, 8, 128, 32 * 12, r=0, seed=3)
+    assert (gc.n_grouped, gc.n_resid) == (384, 0)
+    assert_grouped_bytes_equal(gc, oc)
+    out = host(gc.decode(dev(x.q[0])))
+    assert_attention_close(out, oracle_attention(oc, x.q[0], default_scale(128)))
+
+
+def test_custom_softmax_scale():
+    kvq, x, gc, oc = _run(1, 2, 4, 64, 300, seed=5)
+    out = host(gc.decode(dev(x.q[0]), softmax_scale=0.05))
+    assert_attention_close(out, oracle_attention(oc, x.q[0], np.float32(0.05)))
+
+
+def test_tiny_workload_streaming():
+    """The tiny workload: prefill 256 tokens (128 grouped + 128 fp16), 16 decode
+    steps; the first step flushes the full window."""
+    w = workloads.TINY
+    kvq = _kvq()
+    x = workloads.kivi_inputs(w)
+    gc = kvq.KiviCache(w.batch, w.kv_heads, w.q_heads, w.head_dim, w.k_bits, w.v_bits, w.residual, w.max_tokens)
+    gc.prefill(dev(x.k), dev(x.v))
+    oc = oracle_cache(dict(k_bits=2, v_bits=2, residual=128, max_tokens=w.max_tokens), x.k, x.v)
+    assert (gc.n_grouped, gc.n_resid) == (128, 128)
+    scale = default_scale(w.head_dim)
+    for step in range(w.decode_steps):
+        gc.append(dev(x.k_new[step]), dev(x.v_new[step]))
+        oc.append(x.k_new[step], x.v_new[step])
+        assert (gc.n_grouped, gc.n_resid) == (oc.n_grouped, oc.n_resid)
+        assert_grouped_bytes_equal(gc, oc)
+        assert_residual_equal(gc, oc)
+        out = host(gc.decode(dev(x.q[step])))
+        assert_attention_close(out, oracle_attention(oc, x.q[step], scale))
+    assert (gc.n_grouped, gc.n_resid) == (256, 16)
+
+
+def test_r0_streaming_and_explicit_flush():
+    kvq = _kvq()
+    x = workloads.make_inputs(2, 2, 4, 64, 70, 40, 9)
+    gc = kvq.KiviCache(2, 2, 4, 64, 2, 2, 0, 200)
+    oc = oracle_cache(dict(k_bits=2, v_bits=2, residual=0, max_tokens=200), x.k, x.v)
+    gc.prefill(dev(x.k), dev(x.v))
+    assert (gc.n_grouped, gc.n_resid) == (64, 6)
+    for step in range(40):
+        gc.append(dev(x.k_new[step]), dev(x.v_new[step]))
+        oc.append(x.k_new[step], x.v_new[step])
+        assert (gc.n_grouped, gc.n_resid) == (oc.n_grouped, oc.n_resid)
+    assert_grouped_bytes_equal(gc, oc)
+    assert_residual_equal(gc, oc)
+    out = host(gc.decode(dev(x.q[0])))
+    assert_attention_close(out, oracle_attention(oc, x.q[0], default_scale(64)))
+
+
+def test_explicit_flush_moves_the_remainder():
+    kvq = _kvq()
+    x = workloads.make_inputs(1, 2, 2, 128, 100, 1, 12)
+    gc = kvq.KiviCache(1, 2, 2, 128, 2, 2, 128, 256)
+    oc = oracle_cache(dict(k_bits=2, v_bits=2, residual=128, max_tokens=256), x.k, x.v)
+    gc.prefill(dev(x.k), dev(x.v))
+    assert (gc.n_grouped, gc.n_resid) == (0, 100)
+    gc.flush()
+    oc.flush()
+    assert (gc.n_grouped, gc.n_resid) == (oc.n_grouped, oc.n_resid) == (96, 4)
+    assert_grouped_bytes_equal(gc, oc)
+    assert_residual_equal(gc, oc)
+    out = host(gc.decode(dev(x.q[0])))
+    assert_attention_close(out, oracle_attention(oc, x.q[0], default_scale(128)))
+
+
+def test_streaming_equals_prefill_on_device():
+    """Prefill(S0) + n appends leaves the same bytes in every shared group as prefill(S0 + n)."""
+    kvq = _kvq()
+    x = workloads.make_inputs(2, 2, 4, 128, 256 + 200, 1, 13)
+    a = kvq.KiviCache(2, 2, 4, 128, 2, 2, 128, 512)
+    a.prefill(dev(x.k[:, :, :256]), dev(x.v[:, :, :256]))
+    for t in range(256, 456):
+        a.append(dev(x.k[:, :, t].copy()), dev(x.v[:, :, t].copy()))
+    b = kvq.KiviCache(2, 2, 4, 128, 2, 2, 128, 512)
+    b.prefill(dev(x.k), dev(x.v))
+    n = min(a.n_grouped, b.n_grouped) // 32
+    for name in ("k_codes", "k_meta", "v_codes", "v_meta"):
+        assert np.array_equal(host(a.grouped_view(name))[:, :, :n], host(b.grouped_view(name))[:, :, :n]), name
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads: all bytes (or every flushed group) and sampled heads
+# ---------------------------------------------------------------------------
+
+def _sample_heads(b, hq, n, seed):
+    rng = np.random.default_rng(seed)
+    picks = {(0, 0), (b - 1, hq - 1)}
+    while len(picks) < n:
+        picks.add((int(rng.integers(b)), int(rng.integers(hq))))
+    return sorted(picks)
+
+
+@pytest.mark.parametrize("w", [workloads.MHA_4K, workloads.GQA_8K_2BIT, workloads.GQA_8K_4BIT], ids=lambda w: w.name)
+def test_full_size_decode(w):
+    kvq = _kvq()
+    x = workloads.kivi_inputs(w)
+    gc = kvq.KiviCache(w.batch, w.kv_heads, w.q_heads, w.head_dim, w.k_bits, w.v_bits, w.residual, w.max_tokens)
+    gc.prefill(dev(x.k), dev(x.v))
+    oc = oracle_cache(dict(k_bits=w.k_bits, v_bits=w.v_bits, residual=w.residual, max_tokens=w.max_tokens), x.k, x.v)
+    assert_grouped_bytes_equal(gc, oc)
+    assert_residual_equal(gc, oc)
+    heads = _sample_heads(w.batch, w.q_heads, 12, w.seed)
+    scale = default_scale(w.head_dim)
+    # attention over the prefilled cache, then one streaming decode step
+    out = host(gc.decode(dev(x.q[0])))
+    assert_attention_close(out, oracle_attention(oc, x.q[0], scale, heads), heads)
+    gc.append(dev(x.k_new[0]), dev(x.v_new[0]))
+    oc.append(x.k_new[0], x.v_new[0])
+    assert_grouped_bytes_equal(gc, oc, groups=list(range(oc.n_grouped // 32 - 4, oc.n_grouped // 32)))
+    out = host(gc.decode(dev(x.q[0])))
+    assert_attention_close(out, oracle_attention(oc, x.q[0], scale, heads), heads)
+    assert gc.status() == 0
+
+
+def test_full_size_streaming_128k():
+    """128K streaming workload: prefill 131072 tokens, 512 decode steps with a
+    flush every 128 steps; every flushed group is compared bit for bit and
+    attention is checked at steps 0, 1, 127, 128, 255, 256 and 511."""
+    w = workloads.STREAM_128K
+    kvq = _kvq()
+    x = workloads.kivi_inputs(w)
+    gc = kvq.KiviCache(w.batch, w.kv_heads, w.q_heads, w.head_dim, w.k_bits, w.v_bits, w.residual, w.max_tokens)
+    gc.prefill(dev(x.k), dev(x.v))
+    oc = oracle_cache(dict(k_bits=2, v_bits=2, residual=128, max_tokens=w.max_tokens), x.k, x.v)
+    assert (gc.n_grouped, gc.n_resid) == (130944, 128)
+    rng = np.random.default_rng(4)
+    sample_groups = sorted(set(rng.integers(0, 4092, 64).tolist()) | {0, 4091})
+    assert_grouped_bytes_equal(gc, oc, groups=sample_groups)
+    heads = _sample_heads(w.batch, w.q_heads, 6, w.seed)
+    scale = default_scale(w.head_dim)
+    check = {0, 1, 127, 128, 255, 256, 511}
+    for step in range(w.decode_steps):
+        before = gc.n_grouped
+        gc.append(dev(x.k_new[step]), dev(x.v_new[step]))
+        oc.append(x.k_new[step], x.v_new[step])
+        if gc.n_grouped != before:
+            ng = gc.n_grouped // 32
+            assert_grouped_bytes_equal(gc, oc, groups=list(range(ng - 4, ng)))
+        out = gc.decode(dev(x.q[step]))
+        if step in check:
+            assert_attention_close(host(out), oracle_attention(oc, x.q[step], scale, heads), heads)
+    assert (gc.n_grouped, gc.n_resid) == (131456, 128)
+    assert_residual_equal(gc, oc)
+    assert gc.status() == 0

@@ -138,3 +138,38 @@ def test_pack_cache_shapes():
     assert p["v_codes"].shape == (2, 3, ng, 1024)
     assert p["k_meta"].shape == (2, 3, ng, 256)
     assert p["v_meta"].shape == (2, 3, ng, 128)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_fp8_block_order_fragments(d):
+    """The FP8 in-block order against the m16n8k16 B-fragment description:
+    keys give B[k = channel][n = token] tiles, values B[k = token][n = channel]."""
+    rng = np.random.default_rng(d)
+    blk = rng.integers(0, 256, size=(1, 1, 16, d), dtype=np.uint8)
+    for vl in (0, 1):
+        perm = layout.fp8_block_order(d, vl)
+        assert sorted(perm) == list(range(16 * d))          # a permutation
+        packed = layout.fp8_pack_pool(blk, vl)[0, 0]
+        lane_bytes = lambda lane: np.array([packed[((p // 16) * 32 + lane) * 16 + p % 16] for p in range(d // 2)])
+        nat = blk[0, 0]
+        if vl == 0:
+            for nt in range(2):
+                for ks in range(d // 16):
+                    tile = np.zeros((16, 8), np.int64)
+                    for lane in range(32):
+                        g, tig = lane // 4, lane % 4
+                        lb = lane_bytes(lane)
+                        i0 = (nt * (d // 16) + ks) * 2
+                        tile[2 * tig, g], tile[2 * tig + 1, g] = lb[2 * i0], lb[2 * i0 + 1]
+                        tile[2 * tig + 8, g], tile[2 * tig + 9, g] = lb[2 * i0 + 2], lb[2 * i0 + 3]
+                    assert np.array_equal(tile, nat[8 * nt:8 * nt + 8, 16 * ks:16 * ks + 16].T)
+        else:
+            for nt in range(d // 8):
+                tile = np.zeros((16, 8), np.int64)
+                for lane in range(32):
+                    g, tig = lane // 4, lane % 4
+                    lb = lane_bytes(lane)
+                    tile[2 * tig, g], tile[2 * tig + 1, g] = lb[4 * nt], lb[4 * nt + 1]
+                    tile[2 * tig + 8, g], tile[2 * tig + 9, g] = lb[4 * nt + 2], lb[4 * nt + 3]
+                assert np.array_equal(tile, nat[:, 8 * nt:8 * nt + 8])
+        assert np.array_equal(layout.fp8_unpack_pool(layout.fp8_pack_pool(blk, vl), d, vl), blk)
