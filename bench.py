@@ -1,0 +1,407 @@
+"""Benchmark of the quantized-KV decode hot path on GB300.
+
+Workload (default): the 128K streaming KIVI 2-bit cache — batch 4, 8 kv heads,
+64 query heads (GQA 8), head_dim 128, prefill-quantize 131072 tokens, then
+decode steps that each append one fp16 K/V token (flushing the 128-token fp16
+window into 4 new groups every 128 steps) and run split-K decode attention
+over 130944+ grouped tokens plus the window.
+
+One timed step = kv_append_token (+ the flush when due) + kv_decode_attention.
+``value`` = algorithmic bytes of the timed steps / device time (GB/s), inputs
+resident in HBM. ``e2e`` repeats the steps through the same C-ABI calls with
+the step inputs (q, k_new, v_new) copied from pinned host memory and the
+output copied back inside the timed region. The prefill is timed separately
+(quantize tokens/s). ``roofline`` reports the decode kernel alone (CUDA events
+around each kv_decode_attention launch) against the measured HBM copy
+bandwidth. ``cpu_baseline`` / ``--impl reference`` time the CPU oracle on a
+bounded sample of the same workload.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-cpu-baseline]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+# the CPU-baseline leg is timed single-threaded: pin BLAS/OpenMP before numpy loads
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import numpy as np  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from quantized_kv_cache_quant_gb300 import metrics, workloads  # noqa: E402
+
+METRIC = "decode-attn KV bytes GB/s (% of GB300 HBM peak); quantize tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (weak scaling: one independent cache per GPU)
+# ---------------------------------------------------------------------------
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def run_ours(args, world, rank, local):
+    import torch
+    from quantized_kv_cache_quant_gb300 import kvq
+
+    torch.cuda.set_device(local)
+    w = workloads.WORKLOADS[args.workload]
+    assert isinstance(w, workloads.KiviWorkload), "bench.py times the KIVI streaming workloads"
+    total_steps = args.warmup + args.steps
+    if total_steps > w.decode_steps:
+        raise SystemExit(f"--warmup + --steps must be <= {w.decode_steps} for {w.name}")
+    x = workloads.kivi_inputs(w)   # same seeded data on every rank (weak scaling replicas)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    k_d, v_d = dev(x.k), dev(x.v)
+    q_d = [dev(x.q[s]) for s in range(w.decode_steps)]
+    kn_d = [dev(x.k_new[s]) for s in range(w.decode_steps)]
+    vn_d = [dev(x.v_new[s]) for s in range(w.decode_steps)]
+    cache = kvq.KiviCache(w.batch, w.kv_heads, w.q_heads, w.head_dim, w.k_bits, w.v_bits, w.residual,
+                          w.max_tokens)
+    stream = torch.cuda.current_stream()
+    out = torch.empty((w.batch, w.q_heads, w.head_dim), dtype=torch.float32, device="cuda")
+
+    # --- prefill (quantize tokens/s): warm-up then timed repetitions ---
+    for _ in range(2):
+        cache.prefill(k_d, v_d)
+    reps = 5
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(reps):
+        cache.prefill(k_d, v_d)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    prefill_s = e0.elapsed_time(e1) / 1e3 / reps
+    prefill_tokens = w.batch * w.prefill
+    prefill_bytes = metrics.kivi_prefill_bytes(w.batch, w.kv_heads, w.head_dim, w.k_bits, w.v_bits,
+                                               cache.n_grouped, cache.n_resid)
+
+    def step_bytes(before_grouped, after_grouped, n_resid):
+        b = metrics.kivi_append_bytes(w.batch, w.kv_heads, w.head_dim)
+        if after_grouped != before_grouped:
+            b += metrics.kivi_flush_bytes(w.batch, w.kv_heads, w.head_dim, w.k_bits, w.v_bits,
+                                          after_grouped - before_grouped)
+        return b + metrics.kivi_decode_bytes(w.batch, w.kv_heads, w.q_heads, w.head_dim, w.k_bits, w.v_bits,
+                                             after_grouped, n_resid)
+
+    def run_steps(first, count, timed_events=None):
+        """Enqueue `count` device-resident steps; returns (bytes, launches, decode bytes list)."""
+        nbytes, launches, dec_bytes = 0, 0, []
+        for i in range(count):
+            s = first + i
+            g0 = cache.n_grouped
+            cache.append(kn_d[s], vn_d[s])
+            launches += 1 + (1 if cache.n_grouped != g0 else 0)
+            if timed_events is not None:
+                timed_events[i][0].record(stream)
+            cache.decode(q_d[s], out=out)
+            if timed_events is not None:
+                timed_events[i][1].record(stream)
+            launches += 1
+            nbytes += step_bytes(g0, cache.n_grouped, cache.n_resid)
+            dec_bytes.append(metrics.kivi_decode_bytes(w.batch, w.kv_heads, w.q_heads, w.head_dim, w.k_bits,
+                                                       w.v_bits, cache.n_grouped, cache.n_resid))
+        return nbytes, launches, dec_bytes
+
+    # --- device-resident timed steps ---
+    cache.prefill(k_d, v_d)
+    run_steps(0, args.warmup)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local) if rank == 0 else None
+    barrier(world)
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    start.record(stream)
+    nbytes, launches, dec_bytes = run_steps(args.warmup, args.steps, ev)
+    end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop() if clocks else None
+    barrier(world)
+    t_local = start.elapsed_time(end) / 1e3
+    t = max_over_ranks(t_local, world)
+    total_bytes = sum_over_ranks(float(nbytes), world)
+    value = total_bytes / t / 1e9
+    dec_times = [a.elapsed_time(b) / 1e3 for a, b in ev]
+    achieved = statistics.mean(db / dt for db, dt in zip(dec_bytes, dec_times)) / 1e9
+    status = cache.status()
+
+    # --- end to end: host buffers, copies inside the timed region ---
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    q_h = [pin(x.q[s]) for s in range(w.decode_steps)]
+    kn_h = [pin(x.k_new[s]) for s in range(w.decode_steps)]
+    vn_h = [pin(x.v_new[s]) for s in range(w.decode_steps)]
+    out_h = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+    q_buf, kn_buf, vn_buf = torch.empty_like(q_d[0]), torch.empty_like(kn_d[0]), torch.empty_like(vn_d[0])
+    cache.prefill(k_d, v_d)
+    run_steps(0, args.warmup)
+    barrier(world)
+    torch.cuda.synchronize()
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_start.record(stream)
+    e2e_bytes = 0
+    for i in range(args.steps):
+        s = args.warmup + i
+        q_buf.copy_(q_h[s], non_blocking=True)
+        kn_buf.copy_(kn_h[s], non_blocking=True)
+        vn_buf.copy_(vn_h[s], non_blocking=True)
+        g0 = cache.n_grouped
+        cache.append(kn_buf, vn_buf)
+        cache.decode(q_buf, out=out)
+        out_h.copy_(out, non_blocking=True)
+        e2e_bytes += step_bytes(g0, cache.n_grouped, cache.n_resid)
+    e_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    te = max_over_ranks(e_start.elapsed_time(e_end) / 1e3, world)
+    e2e_value = sum_over_ranks(float(e2e_bytes), world) / te / 1e9
+    h2d = q_h[0].numel() * 2 + kn_h[0].numel() * 2 + vn_h[0].numel() * 2
+    d2h = out_h.numel() * 4
+
+    hbm, peak_kind = peaks()
+    res = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(t / args.steps * 1e3, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {
+            "workload": w.name, "batch": w.batch, "kv_heads": w.kv_heads, "q_heads": w.q_heads,
+            "head_dim": w.head_dim, "k_bits": w.k_bits, "v_bits": w.v_bits, "group": 32, "residual": w.residual,
+            "context_start": w.prefill, "steps_from": args.warmup,
+            "operands": "2-bit codes as fp16 tensor-core operands, fp32 accumulation",
+            "l2": "inputs larger than L2: each step reads ~355 MB of cache against a 129 MB L2",
+        },
+        "pct_of_hbm_peak": round(100 * value / hbm, 2),
+        "quantize_tokens_per_s": round(prefill_tokens / prefill_s, 1),
+        "quantize_gb_s": round(prefill_bytes / prefill_s / 1e9, 2),
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "traffic": None,
+                     "kernel": "kivi_decode_kernel<128,2,2,4>", "peak_source": f"{peak_kind} hbm_gbs",
+                     "decode_us": round(statistics.mean(dec_times) * 1e6, 2)},
+        "device_status": status,
+    }
+    if clk:
+        res["clocks"] = clk
+    return res
+
+
+# ---------------------------------------------------------------------------
+# the oracle on the host cores (cpu_baseline and --impl reference)
+# ---------------------------------------------------------------------------
+def oracle_sample_setup(w):
+    """One (batch row 0, kv head 0) of the workload, as a 1 x 1 oracle cache."""
+    from oracle import kivi
+    x = workloads.kivi_inputs(w)
+    gq = w.q_heads // w.kv_heads
+    c = kivi.KiviCache(1, 1, w.head_dim, w.k_bits, w.v_bits, w.residual, w.max_tokens)
+    c.prefill(x.k[:1, :1], x.v[:1, :1])
+    return x, c, gq
+
+
+def oracle_step(w, x, c, gq, s):
+    from oracle import attention
+    c.append(x.k_new[s, :1, :1], x.v_new[s, :1, :1])
+    kh, vh = c.keys_hat(0, 0), c.values_hat(0, 0)
+    scale = attention.default_scale(w.head_dim)
+    for r in range(gq):
+        attention.softmax_attend(x.q[s, 0, r], kh, vh, scale)
+    return metrics.kivi_decode_bytes(1, 1, gq, w.head_dim, w.k_bits, w.v_bits, c.n_grouped, c.n_resid)
+
+
+def cpu_baseline(w, budget_s=15.0):
+    x, c, gq = oracle_sample_setup(w)
+    t0 = time.perf_counter()
+    nbytes, steps = 0, 0
+    while time.perf_counter() - t0 < budget_s and steps < w.decode_steps:
+        nbytes += oracle_step(w, x, c, gq, steps)
+        steps += 1
+    dt = time.perf_counter() - t0
+    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{steps} decode steps of one (batch row, kv head) of {w.name}: append + flush + float64 "
+                      f"dequantize + attention for its {gq} query heads over {c.n_grouped + c.n_resid} tokens"}
+
+
+def run_reference(args, world, rank):
+    w = workloads.WORKLOADS[args.workload]
+    x, c, gq = oracle_sample_setup(w)
+    for s in range(args.warmup):
+        oracle_step(w, x, c, gq, s)
+    t0 = time.perf_counter()
+    nbytes = 0
+    for i in range(args.steps):
+        nbytes += oracle_step(w, x, c, gq, args.warmup + i)
+    dt = time.perf_counter() - t0
+    value = nbytes / dt / 1e9
+    sample = (f"per step: one (batch row, kv head) of {w.name} — append + flush + float64 dequantize + attention "
+              f"for its {gq} query heads")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=128)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=workloads.STREAM_128K.name, choices=sorted(
+        n for n, w in workloads.WORKLOADS.items() if isinstance(w, workloads.KiviWorkload)))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, world, rank)), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    res = run_ours(args, world, rank, local)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(workloads.WORKLOADS[args.workload])
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -152,10 +152,13 @@ KVQ_API kvq_status kv_append_token(kivi_cache* cache, const uint16_t* k_new, con
  * of the window. A no-op when n_resid < 32. */
 KVQ_API kvq_status kv_flush_residual(kivi_cache* cache, void* stream);
 
-/* Workspace for kv_decode_attention / fp8_decode_attention with this shape
- * (split-K partials). Its first 256 bytes hold a status word (uint32 at
- * offset 0) that kernels OR error bits into: bit 0 = a device wait timed out.
- * Zero the workspace once after allocating it; the status stays sticky. */
+/* Workspace for kv_decode_attention with this shape: a status word (uint32
+ * at offset 0; kernels OR error bits into it, bit 0 = a device wait timed
+ * out; it stays set until the caller clears it), one counter per (batch row,
+ * head) at offset 256 that the kernels return to zero after every call, and
+ * the split-K partials. Zero the whole workspace once after allocating it.
+ * One workspace serves one stream: calls that overlap on the device must not
+ * share it. */
 KVQ_API size_t kv_decode_workspace_bytes(const kivi_config* cfg);
 
 /* Decode attention [CSDN sections 2, 5] for one new token per sequence:
@@ -166,9 +169,10 @@ KVQ_API size_t kv_decode_workspace_bytes(const kivi_config* cfg);
  *   out : device [B, H_q, D], fp32 if out_fp32 != 0, else fp16
  *   softmax_scale <= 0 selects 1/sqrt(D)
  *   ws  : workspace of at least kv_decode_workspace_bytes(cfg) bytes
- * Split-K ("flash-decoding"): token chunks of each (b, kv head) go to
- * separate thread blocks, each writes (m, l, o) partials, and a log-sum-exp
- * merge kernel combines them. Dequantization happens in registers.
+ * Split-K ("flash-decoding"), one kernel launch: token chunks of each
+ * (b, kv head) go to separate thread blocks, each writes (m, l, o) partials,
+ * and the last block of that (b, kv head) to finish merges them with a
+ * log-sum-exp reduction. Dequantization happens in registers.
  * KVQ_ERR_ARG if the cache is empty. */
 KVQ_API kvq_status kv_decode_attention(const kivi_cache* cache, const uint16_t* q, void* out,
                                int32_t out_fp32, float softmax_scale, void* ws,

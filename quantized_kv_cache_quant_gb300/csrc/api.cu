@@ -109,8 +109,14 @@ kvq_status flush_groups(kivi_cache* c, int n_tokens, cudaStream_t s) {
   return KVQ_OK;
 }
 
+// Decode workspace: [status word | 256 B][split counters, one per (b, head) |
+// rounded to 256 B][partial o: B*Hq*splits*D floats][partial (m, l)].
+size_t counters_bytes(int batch, int q_heads) {
+  return (static_cast<size_t>(batch) * q_heads * sizeof(uint32_t) + 255) / 256 * 256;
+}
+
 size_t decode_ws_bytes(int batch, int q_heads, int head_dim) {
-  return static_cast<size_t>(kWsHeader) +
+  return static_cast<size_t>(kWsHeader) + counters_bytes(batch, q_heads) +
          static_cast<size_t>(batch) * q_heads * kMaxSplits * (static_cast<size_t>(head_dim) + 2) * sizeof(float);
 }
 
@@ -325,20 +331,12 @@ kvq_status kv_decode_attention(const kivi_cache* cache, const uint16_t* q, void*
   a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   uint8_t* base = static_cast<uint8_t*>(ws);
   a.status = reinterpret_cast<uint32_t*>(base);
-  a.part_o = reinterpret_cast<float*>(base + kWsHeader);
+  a.counters = reinterpret_cast<uint32_t*>(base + kWsHeader);
+  a.part_o = reinterpret_cast<float*>(base + kWsHeader + counters_bytes(cf.batch, cf.q_heads));
   a.part_ml = a.part_o + static_cast<size_t>(cf.batch) * cf.q_heads * a.splits_total * cf.head_dim;
-  const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  st = from_cuda(kvq::launch_kivi_decode(a, s));
-  if (st != KVQ_OK) return st;
-  kvq::MergeArgs mg{};
-  mg.part_o = a.part_o;
-  mg.part_ml = a.part_ml;
-  mg.splits_total = a.splits_total;
-  mg.rows = cf.batch * cf.q_heads;
-  mg.head_dim = cf.head_dim;
-  mg.out = out;
-  mg.out_fp32 = out_fp32;
-  return from_cuda(kvq::launch_merge(mg, s));
+  a.out = out;
+  a.out_fp32 = out_fp32;
+  return from_cuda(kvq::launch_kivi_decode(a, static_cast<cudaStream_t>(stream)));
 }
 
 size_t fp8_quantize_workspace_bytes(int32_t batch, int32_t kv_heads, int32_t seq_len, int32_t head_dim) {
@@ -433,20 +431,12 @@ kvq_status fp8_decode_attention(const uint16_t* q, const uint8_t* k_pool, const 
   a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   uint8_t* base = static_cast<uint8_t*>(ws);
   a.status = reinterpret_cast<uint32_t*>(base);
-  a.part_o = reinterpret_cast<float*>(base + kWsHeader);
+  a.counters = reinterpret_cast<uint32_t*>(base + kWsHeader);
+  a.part_o = reinterpret_cast<float*>(base + kWsHeader + counters_bytes(batch, q_heads));
   a.part_ml = a.part_o + static_cast<size_t>(batch) * q_heads * splits * head_dim;
-  const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  kvq_status st = from_cuda(kvq::launch_fp8_decode(a, s));
-  if (st != KVQ_OK) return st;
-  kvq::MergeArgs mg{};
-  mg.part_o = a.part_o;
-  mg.part_ml = a.part_ml;
-  mg.splits_total = splits;
-  mg.rows = batch * q_heads;
-  mg.head_dim = head_dim;
-  mg.out = out;
-  mg.out_fp32 = out_fp32;
-  return from_cuda(kvq::launch_merge(mg, s));
+  a.out = out;
+  a.out_fp32 = out_fp32;
+  return from_cuda(kvq::launch_fp8_decode(a, static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -328,27 +328,8 @@ __global__ void __launch_bounds__(128) fp8_decode_kernel(Fp8DecodeArgs a) {
     l_s[warp * 8 + g] = l_run;
   }
   __syncthreads();
-  for (int i = tid; i < gq * D; i += 128) {
-    const int r = i / D, c = i % D;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < 4; ++w) M = fmaxf(M, m_s[w * 8 + r]);
-    float L = 0.0f, O = 0.0f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        const float f = fast_exp2(m_s[w * 8 + r] - M);
-        L = fmaf(l_s[w * 8 + r], f, L);
-        O = fmaf(o_s[(w * 8 + r) * D + c], f, O);
-      }
-    }
-    const long long row = (static_cast<long long>(b) * a.q_heads + h * gq + r) * a.splits + split;
-    a.part_o[row * D + c] = O;
-    if (c == 0) {
-      a.part_ml[row * 2] = M;
-      a.part_ml[row * 2 + 1] = L;
-    }
-  }
+  finish_split<D>(o_s, m_s, l_s, gq, static_cast<long long>(b) * a.q_heads + h * gq, split, a.splits, a.part_o,
+                  a.part_ml, a.counters + static_cast<long long>(b) * a.kv_heads + h, a.out, a.out_fp32);
 }
 
 constexpr int kFp8Stages = 4;

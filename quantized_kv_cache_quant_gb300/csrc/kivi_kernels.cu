@@ -607,62 +607,8 @@ __global__ void __launch_bounds__(128) kivi_decode_kernel(KiviDecodeArgs a) {
     }
   }
   __syncthreads();
-  for (int i = tid; i < gq * D; i += 128) {
-    const int r = i / D, c = i % D;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < 4; ++w) M = fmaxf(M, m_s[w * 8 + r]);
-    float L = 0.0f, O = 0.0f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        const float f = fast_exp2(m_s[w * 8 + r] - M);
-        L = fmaf(l_s[w * 8 + r], f, L);
-        O = fmaf(o_s[(w * 8 + r) * D + c], f, O);
-      }
-    }
-    const long long row = (static_cast<long long>(b) * a.q_heads + h * gq + r) * a.splits_total + split;
-    a.part_o[row * D + c] = O;
-    if (c == 0) {
-      a.part_ml[row * 2] = M;
-      a.part_ml[row * 2 + 1] = L;
-    }
-  }
-}
-
-// ---------------------------------------------------------------------------
-// Log-sum-exp merge of the split partials: one block per (b, query head)
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(128) merge_kernel(MergeArgs a) {
-  __shared__ float w_s[kMaxSplits];
-  __shared__ float inv_l;
-  const long long row = blockIdx.x;
-  const int S = a.splits_total;
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
-    float M = -INFINITY;
-    for (int s = lane; s < S; s += 32) M = fmaxf(M, a.part_ml[(row * S + s) * 2]);
-    M = warp_max(M);
-    float L = 0.0f;
-    for (int s = lane; s < S; s += 32) {
-      const float m = a.part_ml[(row * S + s) * 2];
-      const float f = (M == -INFINITY) ? 0.0f : fast_exp2(m - M);
-      w_s[s] = f;
-      L = fmaf(f, a.part_ml[(row * S + s) * 2 + 1], L);
-    }
-    L = warp_sum(L);
-    if (lane == 0) inv_l = (L > 0.0f) ? 1.0f / L : 0.0f;
-  }
-  __syncthreads();
-  for (int c = threadIdx.x; c < a.head_dim; c += blockDim.x) {
-    float O = 0.0f;
-    for (int s = 0; s < S; ++s) O = fmaf(w_s[s], a.part_o[(row * S + s) * a.head_dim + c], O);
-    O *= inv_l;
-    if (a.out_fp32)
-      reinterpret_cast<float*>(a.out)[row * a.head_dim + c] = O;
-    else
-      reinterpret_cast<__half*>(a.out)[row * a.head_dim + c] = __float2half_rn(O);
-  }
+  finish_split<D>(o_s, m_s, l_s, gq, static_cast<long long>(b) * a.q_heads + h * gq, split, a.splits_total, a.part_o,
+                  a.part_ml, a.counters + bh, a.out, a.out_fp32);
 }
 
 constexpr int kDecodeStages = 4;
@@ -723,11 +669,6 @@ cudaError_t launch_copy_tokens(const CopyTokensArgs& a, cudaStream_t s) {
   const long long total = static_cast<long long>(a.n_tokens) * (a.head_dim / 8) * a.bh;
   const int blocks = static_cast<int>((total + 255) / 256 < 4096 ? (total + 255) / 256 : 4096);
   copy_tokens_kernel<<<blocks, 256, 0, s>>>(a);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_merge(const MergeArgs& a, cudaStream_t s) {
-  merge_kernel<<<a.rows, 128, 0, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -3,6 +3,7 @@
 // conversions, plus a bounded wait that reports a timeout instead of hanging.
 #pragma once
 
+#include <cmath>
 #include <cstdint>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -142,6 +143,83 @@ __device__ __forceinline__ float quad_sum(float v) {
 
 __device__ __forceinline__ void report_timeout(uint32_t* status) {
   if (status != nullptr) atomicOr(status, kStatusTimeout);
+}
+
+}  // namespace kvq
+
+namespace kvq {
+
+// Epilogue shared by the split-K decode kernels. The four warps of a thread
+// block have left per-warp (m, l, o) in shared memory (o_s[4][8][D],
+// m_s[4][8], l_s[4][8], log2 units). The block combines them, writes its
+// partial for each query row, and the last block of a (batch row, kv head) to
+// finish — found with an atomic counter, no waiting — merges all splits into
+// `out` and resets the counter for the next call.
+template <int D>
+__device__ __forceinline__ void finish_split(float* o_s, float* m_s, float* l_s, int gq, long long q_row0, int split,
+                                             int splits_total, float* part_o, float* part_ml, uint32_t* counter,
+                                             void* out, int out_fp32) {
+  const int tid = threadIdx.x;
+  for (int i = tid; i < gq * D; i += blockDim.x) {
+    const int r = i / D, c = i % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) M = fmaxf(M, m_s[w * 8 + r]);
+    float L = 0.0f, O = 0.0f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const float f = fast_exp2(m_s[w * 8 + r] - M);
+        L = fmaf(l_s[w * 8 + r], f, L);
+        O = fmaf(o_s[(w * 8 + r) * D + c], f, O);
+      }
+    }
+    const long long row = (q_row0 + r) * splits_total + split;
+    part_o[row * D + c] = O;
+    if (c == 0) {
+      part_ml[row * 2] = M;
+      part_ml[row * 2 + 1] = L;
+    }
+  }
+  __threadfence();
+  __syncthreads();
+  __shared__ int last;
+  if (tid == 0) last = (atomicAdd(counter, 1u) == static_cast<uint32_t>(splits_total - 1));
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  if (tid == 0) *counter = 0u;
+  // merge weights per query row into shared memory (o_s is free now)
+  float* wgt = o_s;                      // [8][kMaxSplits]
+  float* inv_l = o_s + 8 * kMaxSplits;   // [8]
+  const int warp = tid >> 5, lane = tid & 31;
+  for (int r = warp; r < gq; r += blockDim.x >> 5) {
+    const long long base = (q_row0 + r) * splits_total;
+    float M = -INFINITY;
+    for (int s = lane; s < splits_total; s += 32) M = fmaxf(M, __ldcg(part_ml + (base + s) * 2));
+    M = warp_max(M);
+    float L = 0.0f;
+    for (int s = lane; s < splits_total; s += 32) {
+      const float f = (M == -INFINITY) ? 0.0f : fast_exp2(__ldcg(part_ml + (base + s) * 2) - M);
+      wgt[r * kMaxSplits + s] = f;
+      L = fmaf(f, __ldcg(part_ml + (base + s) * 2 + 1), L);
+    }
+    L = warp_sum(L);
+    if (lane == 0) inv_l[r] = (L > 0.0f) ? 1.0f / L : 0.0f;
+  }
+  __syncthreads();
+  for (int i = tid; i < gq * D; i += blockDim.x) {
+    const int r = i / D, c = i % D;
+    const long long base = (q_row0 + r) * splits_total;
+    float O = 0.0f;
+    for (int s = 0; s < splits_total; ++s) O = fmaf(wgt[r * kMaxSplits + s], __ldcg(part_o + (base + s) * D + c), O);
+    O *= inv_l[r];
+    const long long o_idx = (q_row0 + r) * D + c;
+    if (out_fp32)
+      reinterpret_cast<float*>(out)[o_idx] = O;
+    else
+      reinterpret_cast<__half*>(out)[o_idx] = __float2half_rn(O);
+  }
 }
 
 }  // namespace kvq

@@ -55,20 +55,13 @@ struct KiviDecodeArgs {
   float scale_log2;       // softmax scale * log2(e)
   float* part_o;          // [B, Hq, splits_total, D]
   float* part_ml;         // [B, Hq, splits_total, 2]
+  uint32_t* counters;     // [B, H_kv] finished-split counters (zero between calls)
   uint32_t* status;
+  void* out;              // [B, Hq, D]
+  int out_fp32;
 };
 cudaError_t launch_kivi_decode(const KiviDecodeArgs& a, cudaStream_t s);
 
-struct MergeArgs {
-  const float* part_o;
-  const float* part_ml;
-  int splits_total;
-  int rows;  // B * Hq
-  int head_dim;
-  void* out;
-  int out_fp32;
-};
-cudaError_t launch_merge(const MergeArgs& a, cudaStream_t s);
 
 struct Fp8QuantArgs {
   const uint16_t* x;
@@ -99,7 +92,10 @@ struct Fp8DecodeArgs {
   float scale_log2;
   float* part_o;
   float* part_ml;
+  uint32_t* counters;
   uint32_t* status;
+  void* out;
+  int out_fp32;
 };
 cudaError_t launch_fp8_decode(const Fp8DecodeArgs& a, cudaStream_t s);
 

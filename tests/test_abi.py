@@ -50,7 +50,8 @@ def test_cache_sizes_match_layout(b, h, hq, d, kb, vb, r, t):
     want = sizes.kivi_buffer_bytes(b, h, d, kb, vb, r, t)
     assert got == [want[n] for n in ("k_codes", "k_meta", "v_codes", "v_meta", "k_res", "v_res")]
     ws = kvq.kv_decode_workspace_bytes(cfg)
-    assert ws == 256 + b * hq * 64 * (d + 2) * 4
+    counters = -(-b * hq * 4 // 256) * 256
+    assert ws == 256 + counters + b * hq * 64 * (d + 2) * 4
 
 
 @pytest.mark.parametrize("field,value,code", [
