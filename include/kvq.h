@@ -178,6 +178,30 @@ KVQ_API kvq_status kv_decode_attention(const kivi_cache* cache, const uint16_t* 
                                int32_t out_fp32, float softmax_scale, void* ws,
                                size_t ws_bytes, void* stream);
 
+/* Decode attention for callers that cannot allocate device memory. The pages
+ * describe nothing like it; it exists for users of this library. Some callers
+ * may not call cudaMalloc: for example a serving engine that has handed all
+ * free device memory to a fixed KV-block pool before it starts stepping, or a
+ * plugin whose host framework forbids allocation while a step runs. This call
+ * computes exactly what kv_decode_attention computes (same kernel, same
+ * arguments minus the workspace) but keeps its split-K scratch in one
+ * file-scope device array of KVQ_NOALLOC_SCRATCH_BYTES (16 MiB) that every GPU
+ * loading the library holds until the process exits; it allocates nothing.
+ *   - The scratch a call needs is 256 + 4*B*H_q (rounded up to 256) +
+ *     4*B*H_q*S*(D+2) bytes, S the number of token splits the call picks
+ *     (at most 64); a call that would need more returns KVQ_ERR_CAPACITY and
+ *     enqueues nothing.
+ *   - The first call on each device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - Every call shares the one array and clears its status word and split
+ *     counters with an asynchronous memset on `stream` first. Calls that
+ *     overlap on the GPU (other streams, other host threads) race on it:
+ *     serialize them. The device-wait timeout status of kv_decode_attention is
+ *     not reported by this call. */
+#define KVQ_NOALLOC_SCRATCH_BYTES (16u << 20)
+KVQ_API kvq_status kv_decode_attention_noalloc(const kivi_cache* cache, const uint16_t* q, void* out,
+                                               int32_t out_fp32, float softmax_scale, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* FP8 E4M3 paged cache [KIVI section 5, CSDN section 10, YUN]               */
 /* ------------------------------------------------------------------------ */

@@ -4,6 +4,7 @@
 #include <climits>
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 
 #include "kvq.h"
 #include "kvq_device.cuh"
@@ -437,6 +438,103 @@ kvq_status fp8_decode_attention(const uint16_t* q, const uint8_t* k_pool, const 
   a.out = out;
   a.out_fp32 = out_fp32;
   return from_cuda(kvq::launch_fp8_decode(a, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Decode attention for callers that cannot allocate device memory.
+// The split-K scratch (status word, split counters, partials) lives in one
+// file-scope device array instead of a caller workspace. Every GPU that loads
+// this library keeps the array until the process exits.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) uint8_t kvq_noalloc_scratch[KVQ_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+// The array's device address on the current device. In host code the array's
+// name is only a host-side stand-in, so the address is looked up once per
+// device (with that device current) and cached.
+kvq_status noalloc_scratch_address(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KVQ_ERR_CUDA;
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return KVQ_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, kvq_noalloc_scratch) != cudaSuccess || p == nullptr) return KVQ_ERR_CUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return KVQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+kvq_status kv_decode_attention_noalloc(const kivi_cache* cache, const uint16_t* q, void* out, int32_t out_fp32,
+                                       float softmax_scale, void* stream) {
+  kvq_status st = check_cache(cache);
+  if (st != KVQ_OK) return st;
+  if (q == nullptr || out == nullptr) return KVQ_ERR_NULL;
+  if (!aligned(q) || !aligned(out)) return KVQ_ERR_ALIGN;
+  if (cache->n_grouped + cache->n_resid == 0) return KVQ_ERR_ARG;
+  if (!(softmax_scale == softmax_scale) || std::isinf(softmax_scale)) return KVQ_ERR_ARG;
+  const kivi_config& cf = cache->cfg;
+  const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(cf.head_dim));
+
+  const int ng = cache->n_grouped / kGroup;
+  const int pairs = cf.batch * cf.kv_heads;
+  const int has_resid = cache->n_resid > 0 ? 1 : 0;
+  const int splits_g = choose_splits(ng, pairs, kMaxSplits - 1);
+  const int splits_total = splits_g + has_resid;
+  const size_t head = static_cast<size_t>(kWsHeader) + counters_bytes(cf.batch, cf.q_heads);
+  const size_t need = head + static_cast<size_t>(cf.batch) * cf.q_heads * splits_total *
+                                 (static_cast<size_t>(cf.head_dim) + 2) * sizeof(float);
+  if (need > static_cast<size_t>(KVQ_NOALLOC_SCRATCH_BYTES)) return KVQ_ERR_CAPACITY;
+
+  void* ws = nullptr;
+  st = noalloc_scratch_address(&ws);
+  if (st != KVQ_OK) return st;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the status word and the split counters must start at zero
+  if (cudaMemsetAsync(ws, 0, head, s) != cudaSuccess) return KVQ_ERR_CUDA;
+
+  kvq::KiviDecodeArgs a{};
+  a.k_codes = cache->k_codes;
+  a.k_meta = cache->k_meta;
+  a.v_codes = cache->v_codes;
+  a.v_meta = cache->v_meta;
+  a.k_res = cache->k_res;
+  a.v_res = cache->v_res;
+  a.q = q;
+  a.batch = cf.batch;
+  a.kv_heads = cf.kv_heads;
+  a.q_heads = cf.q_heads;
+  a.head_dim = cf.head_dim;
+  a.k_bits = cf.k_bits;
+  a.v_bits = cf.v_bits;
+  a.groups_cap = cache->groups_cap;
+  a.res_cap = cache->res_cap;
+  a.n_groups = ng;
+  a.n_resid = cache->n_resid;
+  a.splits_g = splits_g;
+  a.groups_per_split = splits_g > 0 ? ceil_div(ng, splits_g) : 0;
+  a.splits_total = splits_total;
+  a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  a.status = reinterpret_cast<uint32_t*>(base);
+  a.counters = reinterpret_cast<uint32_t*>(base + kWsHeader);
+  a.part_o = reinterpret_cast<float*>(base + head);
+  a.part_ml = a.part_o + static_cast<size_t>(cf.batch) * cf.q_heads * splits_total * cf.head_dim;
+  a.out = out;
+  a.out_fp32 = out_fp32;
+  return from_cuda(kvq::launch_kivi_decode(a, s));
 }
 
 }  // extern "C"

@@ -26,7 +26,8 @@ c_i32, c_sz, c_vp, c_f32 = ctypes.c_int32, ctypes.c_size_t, ctypes.c_void_p, cty
 
 EXPORTED = (
     "kvq_status_string", "kivi_cache_sizes", "kivi_cache_init", "kv_quant_prefill", "kv_append_token",
-    "kv_flush_residual", "kv_decode_workspace_bytes", "kv_decode_attention", "fp8_quantize_workspace_bytes",
+    "kv_flush_residual", "kv_decode_workspace_bytes", "kv_decode_attention", "kv_decode_attention_noalloc",
+    "fp8_quantize_workspace_bytes",
     "fp8_kv_quantize", "fp8_decode_workspace_bytes", "fp8_decode_attention",
 )
 
@@ -64,6 +65,7 @@ _SIG = {
     "kv_flush_residual": ([_P_CACHE, c_vp], ctypes.c_int),
     "kv_decode_workspace_bytes": ([_P_CFG], c_sz),
     "kv_decode_attention": ([_P_CACHE, c_vp, c_vp, c_i32, c_f32, c_vp, c_sz, c_vp], ctypes.c_int),
+    "kv_decode_attention_noalloc": ([_P_CACHE, c_vp, c_vp, c_i32, c_f32, c_vp], ctypes.c_int),
     "fp8_quantize_workspace_bytes": ([c_i32, c_i32, c_i32, c_i32], c_sz),
     "fp8_kv_quantize": ([c_vp, c_i32, c_i32, c_i32, c_i32, c_vp, c_i32, c_i32, c_i32, c_vp, c_vp, c_i32, c_i32,
                          c_vp, c_sz, c_vp], ctypes.c_int),
@@ -147,6 +149,14 @@ def kv_decode_attention(cache: kivi_cache, q, out, out_fp32: bool, softmax_scale
     _check(_lib.kv_decode_attention(ctypes.byref(cache), _ptr(q), _ptr(out), int(bool(out_fp32)),
                                     float(softmax_scale), _ptr(ws), ws_bytes, _stream(stream)),
            "kv_decode_attention")
+
+
+def kv_decode_attention_noalloc(cache: kivi_cache, q, out, out_fp32: bool, softmax_scale: float,
+                                stream=None) -> None:
+    """kv_decode_attention without a workspace, for callers that cannot allocate
+    device memory: the scratch is a fixed device array inside the library."""
+    _check(_lib.kv_decode_attention_noalloc(ctypes.byref(cache), _ptr(q), _ptr(out), int(bool(out_fp32)),
+                                            float(softmax_scale), _stream(stream)), "kv_decode_attention_noalloc")
 
 
 def fp8_quantize_workspace_bytes(batch, kv_heads, seq_len, head_dim) -> int:
