@@ -371,6 +371,98 @@ def run_reference(args, world, rank):
     }
 
 
+# ---------------------------------------------------------------------------
+# --table: every workload's decode call (and quantize) timed alone
+# ---------------------------------------------------------------------------
+def run_table(args):
+    """One JSON line per workload: median time of the decode-attention call over
+    the prefilled cache (L2 flushed by writing 512 MB between repetitions), its
+    algorithmic GB/s and fraction of the HBM peak, and the quantize rate."""
+    import torch
+    from quantized_kv_cache_quant_gb300 import kvq
+
+    hbm, _ = peaks()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+    def timed(fn, reps=20, warm=3):
+        ts = []
+        for r in range(reps + warm):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            if r >= warm:
+                ts.append(a.elapsed_time(b) / 1e3)
+        return statistics.median(ts)
+
+    names = args.table.split(",") if args.table != "all" else [
+        workloads.MHA_4K.name, workloads.GQA_8K_2BIT.name, workloads.GQA_8K_4BIT.name, workloads.STREAM_128K.name,
+        workloads.FP8_32K.name]
+    for name in names:
+        w = workloads.WORKLOADS[name]
+        if isinstance(w, workloads.KiviWorkload):
+            x = workloads.kivi_inputs(w, steps=1)
+            cache = kvq.KiviCache(w.batch, w.kv_heads, w.q_heads, w.head_dim, w.k_bits, w.v_bits, w.residual,
+                                  w.max_tokens)
+            k_d, v_d, q_d = dev(x.k), dev(x.v), dev(x.q[0])
+            t_pre = timed(lambda: cache.prefill(k_d, v_d), reps=5)
+            out = torch.empty((w.batch, w.q_heads, w.head_dim), dtype=torch.float32, device="cuda")
+            t_dec = timed(lambda: cache.decode(q_d, out=out))
+            nbytes = metrics.kivi_decode_bytes(w.batch, w.kv_heads, w.q_heads, w.head_dim, w.k_bits, w.v_bits,
+                                               cache.n_grouped, cache.n_resid)
+            line = {"workload": w.name, "call": "kv_decode_attention", "us": round(t_dec * 1e6, 2),
+                    "bytes": nbytes, "GB_s": round(nbytes / t_dec / 1e9, 1),
+                    "pct_of_hbm_peak": round(100 * nbytes / t_dec / 1e9 / hbm, 1),
+                    "prefill_us": round(t_pre * 1e6, 1),
+                    "quantize_tokens_per_s": round(w.batch * w.prefill / t_pre, 1),
+                    "status": cache.status()}
+            del k_d, v_d, cache
+        else:
+            k, v, q, table = workloads.fp8_inputs(w)
+            nb = w.batch * w.blocks_per_seq
+            pools, scales = [], []
+            wsb = kvq.fp8_quantize_workspace_bytes(w.batch, w.kv_heads, w.context, w.head_dim)
+            wsq = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
+            t_q = []
+            tbl = dev(table)
+            for x16, vl in ((k, 0), (v, 1)):
+                xd = dev(x16)
+                pool = torch.empty((nb, w.kv_heads, 16 * w.head_dim), dtype=torch.uint8, device="cuda")
+                sc = torch.zeros(1, dtype=torch.float32, device="cuda")
+                t_q.append(timed(lambda: kvq.fp8_kv_quantize(xd, w.batch, w.kv_heads, w.context, w.head_dim, tbl,
+                                                             w.blocks_per_seq, 16, nb, pool, sc, False, vl, wsq,
+                                                             wsb), reps=5))
+                pools.append(pool)
+                scales.append(sc)
+                del xd
+            out = torch.empty((w.batch, w.q_heads, w.head_dim), dtype=torch.float32, device="cuda")
+            wsd = kvq.fp8_decode_workspace_bytes(w.batch, w.q_heads, w.head_dim)
+            ws = torch.zeros(wsd, dtype=torch.uint8, device="cuda")
+            lens = dev(np.full(w.batch, w.context, np.int32))
+            q_d = dev(q)
+            t_dec = timed(lambda: kvq.fp8_decode_attention(q_d, pools[0], pools[1], scales[0], scales[1], tbl, lens,
+                                                           w.batch, w.q_heads, w.kv_heads, w.head_dim, 16,
+                                                           w.blocks_per_seq, nb, w.context, out, True, 0.0, ws,
+                                                           wsd))
+            nbytes = metrics.fp8_decode_bytes(w.batch, w.kv_heads, w.q_heads, w.head_dim, w.context,
+                                              w.blocks_per_seq)
+            qbytes = metrics.fp8_quantize_bytes(w.batch, w.kv_heads, w.context, w.head_dim, True)
+            line = {"workload": w.name, "call": "fp8_decode_attention", "us": round(t_dec * 1e6, 2),
+                    "bytes": nbytes, "GB_s": round(nbytes / t_dec / 1e9, 1),
+                    "pct_of_hbm_peak": round(100 * nbytes / t_dec / 1e9 / hbm, 1),
+                    "quantize_us_k_v": [round(t * 1e6, 1) for t in t_q],
+                    "quantize_GB_s": round(qbytes / statistics.mean(t_q) / 1e9, 1),
+                    "quantize_tokens_per_s": round(w.batch * w.context / statistics.mean(t_q), 1),
+                    "status": int(ws[:4].view(torch.int32).item())}
+            del pools
+        print(json.dumps(line), flush=True)
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -380,7 +472,12 @@ def main():
     ap.add_argument("--workload", default=workloads.STREAM_128K.name, choices=sorted(
         n for n, w in workloads.WORKLOADS.items() if isinstance(w, workloads.KiviWorkload)))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--table", default=None,
+                    help="'all' or comma-separated workload names: time each decode call alone instead")
     args = ap.parse_args()
+    if args.table:
+        run_table(args)
+        return
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
     world, rank, local = dist_setup()

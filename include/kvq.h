@@ -16,7 +16,7 @@
  *  [CSDN]  "大模型量化从0到1（十三）：KV Cache 量化", section 2 (attention),
  *          section 4 (cache shape [B, H_kv, S, D]), section 5 (GQA), section 10
  *          (affine and FP8 quantization formulas, per-tensor granularity),
- *          section 12 (paged cache blocks).
+ *          section 13 (paged cache blocks).
  *  [YUN]   "LLM推理加速KV Cache量化压缩实战方案" (yunthe), "自定义KV Cache量化的实现
  *          路径": per-tensor FP8 scale = max|x| / 448.
  *
@@ -212,7 +212,7 @@ KVQ_API kvq_status kv_decode_attention_noalloc(const kivi_cache* cache, const ui
  *
  * Pool layout: pool[num_blocks, H_kv, block_size * D] bytes; logical token t
  * of sequence b lives in physical block block_table[b * max_blocks + t/bs],
- * row t % bs ([CSDN] section 12). Within one (block, kv head), block_size must
+ * row t % bs ([CSDN] section 13). Within one (block, kv head), block_size must
  * be 16 and the 16*D bytes are stored in mma.sync fragment order (lane =
  * 4*g + tig, D/2 bytes per lane; byte p of lane l's stream is stored at byte
  * ((p/16)*32 + l)*16 + p%16):

@@ -17,7 +17,6 @@ using kvq::kWsHeader;
 namespace {
 
 constexpr int kAmaxBlocksMax = 4096;
-constexpr int kCtasPerSm = 4;       // resident decode blocks per SM the split count aims for
 constexpr int kMinUnitsPerSplit = 8;  // groups (or paged blocks) per split: two per warp
 
 bool aligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
@@ -121,14 +120,29 @@ size_t decode_ws_bytes(int batch, int q_heads, int head_dim) {
          static_cast<size_t>(batch) * q_heads * kMaxSplits * (static_cast<size_t>(head_dim) + 2) * sizeof(float);
 }
 
-// Number of splits for `units` work items per (b, kv head) and `pairs` pairs.
-int choose_splits(int units, int pairs, int max_splits) {
+// Token splits for `units` work items (groups or paged blocks) per
+// (batch row, kv head), `pairs` such pairs and `extra` single-block items
+// (the fp16-window blocks). Picks the split count with the smallest estimated
+// time: whole waves of resident blocks times (the items one warp processes +
+// a fixed per-block cost of about four items for the query set-up, the
+// partial write and the merge).
+int choose_splits(int units, int pairs, int max_splits, int blocks_per_sm, int extra) {
   if (units <= 0) return 0;
-  const int target = kCtasPerSm * kvq::device_sm_count();
-  int splits = ceil_div(target, pairs);
-  splits = std::min(splits, std::max(1, ceil_div(units, kMinUnitsPerSplit)));
-  splits = std::max(1, std::min(splits, max_splits));
-  const int per = ceil_div(units, splits);
+  const long long slots = static_cast<long long>(kvq::device_sm_count()) * std::max(1, blocks_per_sm);
+  const int cap = std::max(1, std::min(max_splits, ceil_div(units, kMinUnitsPerSplit)));
+  int best = 1;
+  long long best_cost = LLONG_MAX;
+  for (int s = 1; s <= cap; ++s) {
+    const int per = ceil_div(units, s);
+    const long long ctas = static_cast<long long>(pairs) * s + extra;
+    const long long waves = (ctas + slots - 1) / slots;
+    const long long cost = waves * (ceil_div(per, 4) + 4);
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  const int per = ceil_div(units, best);
   return ceil_div(units, per);
 }
 
@@ -307,7 +321,9 @@ kvq_status kv_decode_attention(const kivi_cache* cache, const uint16_t* q, void*
   const int ng = cache->n_grouped / kGroup;
   const int pairs = cf.batch * cf.kv_heads;
   const int has_resid = cache->n_resid > 0 ? 1 : 0;
-  const int splits_g = choose_splits(ng, pairs, kMaxSplits - 1);
+  const int splits_g = choose_splits(ng, pairs, kMaxSplits - 1,
+                                     kvq::kivi_decode_blocks_per_sm(cf.head_dim, cf.k_bits, cf.v_bits),
+                                     has_resid ? pairs : 0);
   kvq::KiviDecodeArgs a{};
   a.k_codes = cache->k_codes;
   a.k_meta = cache->k_meta;
@@ -412,7 +428,7 @@ kvq_status fp8_decode_attention(const uint16_t* q, const uint8_t* k_pool, const 
   if (!(softmax_scale == softmax_scale) || std::isinf(softmax_scale)) return KVQ_ERR_ARG;
   const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(head_dim));
   const int nblk = ceil_div(max_seq_len, block_size);
-  const int splits = choose_splits(nblk, batch * kv_heads, kMaxSplits);
+  const int splits = choose_splits(nblk, batch * kv_heads, kMaxSplits, kvq::fp8_decode_blocks_per_sm(head_dim), 0);
   kvq::Fp8DecodeArgs a{};
   a.q = q;
   a.k_pool = k_pool;
@@ -491,7 +507,9 @@ kvq_status kv_decode_attention_noalloc(const kivi_cache* cache, const uint16_t* 
   const int ng = cache->n_grouped / kGroup;
   const int pairs = cf.batch * cf.kv_heads;
   const int has_resid = cache->n_resid > 0 ? 1 : 0;
-  const int splits_g = choose_splits(ng, pairs, kMaxSplits - 1);
+  const int splits_g = choose_splits(ng, pairs, kMaxSplits - 1,
+                                     kvq::kivi_decode_blocks_per_sm(cf.head_dim, cf.k_bits, cf.v_bits),
+                                     has_resid ? pairs : 0);
   const int splits_total = splits_g + has_resid;
   const size_t head = static_cast<size_t>(kWsHeader) + counters_bytes(cf.batch, cf.q_heads);
   const size_t need = head + static_cast<size_t>(cf.batch) * cf.q_heads * splits_total *

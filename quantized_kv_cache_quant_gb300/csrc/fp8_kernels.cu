@@ -5,7 +5,7 @@
 // Method: "4.4 KV Cache 量化：KIVI 2-bit 与 FP8 KV Cache" (aiinfraguide), section 5
 // (E4M3 = 1 sign, 4 exponent, 3 mantissa bits); "大模型量化从0到1（十三）：KV Cache
 // 量化" (CSDN), section 10 (q = cast_fp8(x / s), x_hat = float(q) * s, per-tensor
-// scale) and section 12 (paged blocks through a block table); "LLM推理加速KV Cache
+// scale) and section 13 (paged blocks through a block table); "LLM推理加速KV Cache
 // 量化压缩实战方案" (yunthe), custom-cache section (scale = max|x| / 448).
 #include <cmath>
 
@@ -345,7 +345,26 @@ cudaError_t fp8_decode_dispatch(const Fp8DecodeArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+template <int D>
+int fp8_occupancy() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  if (cached[dev] == 0) {
+    constexpr int smem = Fp8Smem<D, kFp8Stages>::BYTES;
+    auto kern = fp8_decode_kernel<D, kFp8Stages>;
+    int n = 0;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, 128, smem) != cudaSuccess || n <= 0)
+      n = 1;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
 }  // namespace
+
+int fp8_decode_blocks_per_sm(int head_dim) { return head_dim == 64 ? fp8_occupancy<64>() : fp8_occupancy<128>(); }
 
 cudaError_t launch_fp8_quantize(const Fp8QuantArgs& a, cudaStream_t s) {
   if (!a.static_scale) {

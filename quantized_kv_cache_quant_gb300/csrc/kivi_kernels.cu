@@ -258,7 +258,8 @@ __global__ void copy_tokens_kernel(CopyTokensArgs a) {
 // {hi, lo} fp16 parts):
 //   q.k^T : A = q'_{h,d} = q_{h,d} * s_{g,d} split exactly into fp16 hi + lo
 //           (hi = fp16(q*s), lo = fma(q, s, -hi)); B = key codes (fields as
-//           fp16 subnormals); plus q . z_g from one MMA with A = q, B = z.
+//           fp16 subnormals); plus q . z_g on CUDA cores (fp16 x fp16 -> fp32
+//           fused multiply-adds, reduced over the four lanes of a quad).
 //   p.V   : A = p_t * s_t split into fp16 hi + lo; B = value codes; plus
 //           sum_t p_t z_t on CUDA cores.
 template <int D>
@@ -279,7 +280,7 @@ struct DecodeSmem {
 };
 
 template <int D, int KB, int VB, int STAGES>
-__global__ void __launch_bounds__(128) kivi_decode_kernel(KiviDecodeArgs a) {
+__global__ void __launch_bounds__(128, 4) kivi_decode_kernel(KiviDecodeArgs a) {
   using P = Kivi<D, KB, VB>;
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
@@ -293,14 +294,11 @@ __global__ void __launch_bounds__(128) kivi_decode_kernel(KiviDecodeArgs a) {
   const int gq = a.q_heads / a.kv_heads;
   const long long bh = static_cast<long long>(b) * a.kv_heads + h;
 
-  float m_run = -INFINITY, l_run = 0.0f, vz_run = 0.0f;
-  float o_acc[P::NTV][4];
-#pragma unroll
-  for (int i = 0; i < P::NTV; ++i) o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.0f;
-  // window path results (one value per query row)
-  float rw_m[kMaxGqa], rw_l[kMaxGqa], rw_o[kMaxGqa][D / 32];
-
   if (split < a.splits_g) {
+    float m_run = -INFINITY, l_run = 0.0f, vz_run = 0.0f;
+    float o_acc[P::NTV][4];
+#pragma unroll
+    for (int i = 0; i < P::NTV; ++i) o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.0f;
     // ------------------------------- grouped region -------------------------------
     const int g_begin = split * a.groups_per_split;
     const int g_end = min(a.n_groups, g_begin + a.groups_per_split);
@@ -389,7 +387,7 @@ __global__ void __launch_bounds__(128) kivi_decode_kernel(KiviDecodeArgs a) {
       float sacc[4][4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) sacc[i][0] = sacc[i][1] = sacc[i][2] = sacc[i][3] = 0.0f;
-      float bacc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      float bsum = 0.0f;  // this thread's share of q . z over its 32 channels
 #pragma unroll
       for (int ks = 0; ks < P::KS; ++ks) {
         const uint4 md = kmr[ks * 4 + tig];  // {s(d0,d0+1), s(d0+8,d0+9), z(d0,d0+1), z(d0+8,d0+9)}
@@ -399,7 +397,7 @@ __global__ void __launch_bounds__(128) kivi_decode_kernel(KiviDecodeArgs a) {
         const __half2 hi1 = __hmul2(q1, bits_h2(md.y));
         const __half2 lo1 = __hfma2(q1, bits_h2(md.y), __hneg2(hi1));
         const uint32_t A0 = h2_bits(hi0), A1 = h2_bits(lo0), A2 = h2_bits(hi1), A3 = h2_bits(lo1);
-        mma16816(bacc, qs[ks][0], 0u, qs[ks][1], 0u, md.z, md.w);
+        bsum = dot2_f16_f32(qs[ks][0], md.z, dot2_f16_f32(qs[ks][1], md.w, bsum));
         if constexpr (KB == 2) {
           const uint32_t w = kw[ks];
           const uint32_t l6 = w << 6, l2 = w << 2, r2 = w >> 2, r6 = w >> 6;
@@ -415,7 +413,7 @@ __global__ void __launch_bounds__(128) kivi_decode_kernel(KiviDecodeArgs a) {
           mma16816(sacc[3], A0, A1, A2, A3, (w0 >> 6) & kMask4, (w1 >> 6) & kMask4);
         }
       }
-      const float bias = bacc[0] * p2e;
+      const float bias = quad_sum(bsum) * p2e;
       float sc[8];
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt) {
@@ -516,7 +514,21 @@ __global__ void __launch_bounds__(128) kivi_decode_kernel(KiviDecodeArgs a) {
     }
     l_run = quad_sum(l_run);
     vz_run = quad_sum(vz_run);
+    __syncthreads();  // every warp is done with its stages; the area is reused below
+    constexpr bool kTwoFields = (VB == 2);
+#pragma unroll
+    for (int nt = 0; nt < P::NTV; ++nt) {
+      const float om = (kTwoFields && (nt & 1)) ? kInvP8 : kInvP6;
+      const int c = 8 * nt + 2 * tig;
+      o_s[(warp * 8 + g) * D + c] = fmaf(o_acc[nt][0] + o_acc[nt][2], om, vz_run);
+      o_s[(warp * 8 + g) * D + c + 1] = fmaf(o_acc[nt][1] + o_acc[nt][3], om, vz_run);
+    }
+    if (tig == 0) {
+      m_s[warp * 8 + g] = m_run;
+      l_s[warp * 8 + g] = l_run;
+    }
   } else {
+    float rw_m[kMaxGqa], rw_l[kMaxGqa], rw_o[kMaxGqa][D / 32];
     // --------------------- fp16 window (CUDA cores, fp32) ---------------------
     float* qf = reinterpret_cast<float*>(area + CombineSmem<D>::BYTES);  // [8][D]
     for (int i = tid; i < gq * D; i += 128)
@@ -578,24 +590,6 @@ __global__ void __launch_bounds__(128) kivi_decode_kernel(KiviDecodeArgs a) {
         for (int i = 0; i < D / 32; ++i) rw_o[r][i] = fmaf(pt, vf[i], rw_o[r][i]);
       }
     }
-  }
-
-  // ------------------------------- combine the 4 warps -------------------------------
-  __syncthreads();  // every warp is done with its stages; the area is reused below
-  if (split < a.splits_g) {
-    constexpr bool kTwoFields = (VB == 2);
-#pragma unroll
-    for (int nt = 0; nt < P::NTV; ++nt) {
-      const float om = (kTwoFields && (nt & 1)) ? kInvP8 : kInvP6;
-      const int c = 8 * nt + 2 * tig;
-      o_s[(warp * 8 + g) * D + c] = fmaf(o_acc[nt][0] + o_acc[nt][2], om, vz_run);
-      o_s[(warp * 8 + g) * D + c + 1] = fmaf(o_acc[nt][1] + o_acc[nt][3], om, vz_run);
-    }
-    if (tig == 0) {
-      m_s[warp * 8 + g] = m_run;
-      l_s[warp * 8 + g] = l_run;
-    }
-  } else {
 #pragma unroll
     for (int r = 0; r < kMaxGqa; ++r) {
 #pragma unroll
@@ -606,6 +600,7 @@ __global__ void __launch_bounds__(128) kivi_decode_kernel(KiviDecodeArgs a) {
       }
     }
   }
+
   __syncthreads();
   finish_split<D>(o_s, m_s, l_s, gq, static_cast<long long>(b) * a.q_heads + h * gq, split, a.splits_total, a.part_o,
                   a.part_ml, a.counters + bh, a.out, a.out_fp32);
@@ -618,6 +613,23 @@ cudaError_t quantize_dispatch(const QuantGroupsArgs& a, cudaStream_t s) {
   dim3 grid(a.n_groups, a.kv_heads, a.batch);
   kivi_quantize_kernel<D, KB, VB><<<grid, 128, 0, s>>>(a);
   return cudaGetLastError();
+}
+
+template <int D, int KB, int VB>
+int decode_occupancy() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  if (cached[dev] == 0) {
+    constexpr int smem = DecodeSmem<D, KB, VB, kDecodeStages>::BYTES;
+    auto kern = kivi_decode_kernel<D, KB, VB, kDecodeStages>;
+    int n = 0;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, 128, smem) != cudaSuccess || n <= 0)
+      n = 1;
+    cached[dev] = n;
+  }
+  return cached[dev];
 }
 
 template <int D, int KB, int VB>
@@ -661,6 +673,20 @@ cudaError_t launch_kivi_decode(const KiviDecodeArgs& a, cudaStream_t s) {
     case 12842: return decode_dispatch<128, 4, 2>(a, s);
     case 12844: return decode_dispatch<128, 4, 4>(a, s);
     default: return cudaErrorInvalidValue;
+  }
+}
+
+int kivi_decode_blocks_per_sm(int head_dim, int k_bits, int v_bits) {
+  switch (head_dim * 100 + k_bits * 10 + v_bits) {
+    case 6422: return decode_occupancy<64, 2, 2>();
+    case 6424: return decode_occupancy<64, 2, 4>();
+    case 6442: return decode_occupancy<64, 4, 2>();
+    case 6444: return decode_occupancy<64, 4, 4>();
+    case 12822: return decode_occupancy<128, 2, 2>();
+    case 12824: return decode_occupancy<128, 2, 4>();
+    case 12842: return decode_occupancy<128, 4, 2>();
+    case 12844: return decode_occupancy<128, 4, 4>();
+    default: return 1;
   }
 }
 

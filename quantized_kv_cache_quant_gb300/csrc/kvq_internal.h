@@ -100,5 +100,8 @@ struct Fp8DecodeArgs {
 cudaError_t launch_fp8_decode(const Fp8DecodeArgs& a, cudaStream_t s);
 
 int device_sm_count();
+// Resident thread blocks per SM of the decode kernels (occupancy API, cached).
+int kivi_decode_blocks_per_sm(int head_dim, int k_bits, int v_bits);
+int fp8_decode_blocks_per_sm(int head_dim);
 
 }  // namespace kvq
