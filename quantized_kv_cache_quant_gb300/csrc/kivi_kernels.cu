@@ -14,6 +14,10 @@
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
 
+#ifndef KVQ_DECODE_MIN_BLOCKS
+#define KVQ_DECODE_MIN_BLOCKS 3  // resident decode blocks per SM the register budget is sized for
+#endif
+
 namespace kvq {
 namespace {
 
@@ -258,8 +262,8 @@ __global__ void copy_tokens_kernel(CopyTokensArgs a) {
 // {hi, lo} fp16 parts):
 //   q.k^T : A = q'_{h,d} = q_{h,d} * s_{g,d} split exactly into fp16 hi + lo
 //           (hi = fp16(q*s), lo = fma(q, s, -hi)); B = key codes (fields as
-//           fp16 subnormals); plus q . z_g on CUDA cores (fp16 x fp16 -> fp32
-//           fused multiply-adds, reduced over the four lanes of a quad).
+//           fp16 subnormals); plus q . z_g from one more MMA per k-step with
+//           A = q and B = z (the tensor pipe has room; the issue slots do not).
 //   p.V   : A = p_t * s_t split into fp16 hi + lo; B = value codes; plus
 //           sum_t p_t z_t on CUDA cores.
 template <int D>
@@ -280,7 +284,7 @@ struct DecodeSmem {
 };
 
 template <int D, int KB, int VB, int STAGES>
-__global__ void __launch_bounds__(128, 4) kivi_decode_kernel(KiviDecodeArgs a) {
+__global__ void __launch_bounds__(128, KVQ_DECODE_MIN_BLOCKS) kivi_decode_kernel(KiviDecodeArgs a) {
   using P = Kivi<D, KB, VB>;
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
@@ -360,21 +364,11 @@ __global__ void __launch_bounds__(128, 4) kivi_decode_kernel(KiviDecodeArgs a) {
     const float p2e = ldexpf(1.0f, e) * a.scale_log2;
     const float mult6 = kInvP6 * p2e, mult8 = kInvP8 * p2e;
 
-    int j = 0;
-    bool timed_out = false;
-    for (; j < n_mine; ++j) {
-      const int s = j % STAGES;
-      if (!mbar_wait_bounded(&bar[s], (j / STAGES) & 1)) {
-        timed_out = true;
-        break;
-      }
-      const uint8_t* sp = ring + s * P::STAGE;
+    // q . k_hat of the 32 tokens of the group in stage `sp`: 8 scores (log2
+    // units) of this thread's row, tokens 8*nt + 2*tig + {0, 1}.
+    auto qk_scores = [&](const uint8_t* sp, float (&sc)[8]) {
       const uint4* kcw = reinterpret_cast<const uint4*>(sp);
       const uint4* kmr = reinterpret_cast<const uint4*>(sp + P::KC);
-      const uint4* vcw = reinterpret_cast<const uint4*>(sp + P::KC + P::KM);
-      const uint4* vmr = reinterpret_cast<const uint4*>(sp + P::KC + P::KM + P::VC);
-
-      // ---- scores: q . k_hat for 32 tokens ----
       uint32_t kw[P::KW];
 #pragma unroll
       for (int c = 0; c < P::KW / 4; ++c) {
@@ -387,7 +381,7 @@ __global__ void __launch_bounds__(128, 4) kivi_decode_kernel(KiviDecodeArgs a) {
       float sacc[4][4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) sacc[i][0] = sacc[i][1] = sacc[i][2] = sacc[i][3] = 0.0f;
-      float bsum = 0.0f;  // this thread's share of q . z over its 32 channels
+      float bacc[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // q . z (every column equal)
 #pragma unroll
       for (int ks = 0; ks < P::KS; ++ks) {
         const uint4 md = kmr[ks * 4 + tig];  // {s(d0,d0+1), s(d0+8,d0+9), z(d0,d0+1), z(d0+8,d0+9)}
@@ -397,7 +391,7 @@ __global__ void __launch_bounds__(128, 4) kivi_decode_kernel(KiviDecodeArgs a) {
         const __half2 hi1 = __hmul2(q1, bits_h2(md.y));
         const __half2 lo1 = __hfma2(q1, bits_h2(md.y), __hneg2(hi1));
         const uint32_t A0 = h2_bits(hi0), A1 = h2_bits(lo0), A2 = h2_bits(hi1), A3 = h2_bits(lo1);
-        bsum = dot2_f16_f32(qs[ks][0], md.z, dot2_f16_f32(qs[ks][1], md.w, bsum));
+        mma16816(bacc, qs[ks][0], 0u, qs[ks][1], 0u, md.z, md.w);
         if constexpr (KB == 2) {
           const uint32_t w = kw[ks];
           const uint32_t l6 = w << 6, l2 = w << 2, r2 = w >> 2, r6 = w >> 6;
@@ -413,16 +407,41 @@ __global__ void __launch_bounds__(128, 4) kivi_decode_kernel(KiviDecodeArgs a) {
           mma16816(sacc[3], A0, A1, A2, A3, (w0 >> 6) & kMask4, (w1 >> 6) & kMask4);
         }
       }
-      const float bias = quad_sum(bsum) * p2e;
-      float sc[8];
+      const float bias = bacc[0] * p2e;
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt) {
         const float mult = (KB == 2 && (nt & 1)) ? mult8 : mult6;
         sc[2 * nt] = fmaf(sacc[nt][0] + sacc[nt][2], mult, bias);
         sc[2 * nt + 1] = fmaf(sacc[nt][1] + sacc[nt][3], mult, bias);
       }
+    };
 
-      // ---- online softmax (log2 domain) ----
+    // Software pipeline: iteration j runs the softmax and p . V of group j
+    // and, in the same straight-line block, q . k^T of group j + 1, so that
+    // each warp keeps both the tensor pipe and the ALUs busy.
+    int j = 0;
+    bool timed_out = false;
+    float sc[8];
+    if (n_mine > 0) {
+      if (mbar_wait_bounded(&bar[0], 0))
+        qk_scores(ring, sc);
+      else
+        timed_out = true;
+    }
+    for (; !timed_out && j < n_mine; ++j) {
+      const int s = j % STAGES;
+      const uint8_t* sp = ring + s * P::STAGE;
+      // the next group's stage (this one again past the end: its scores are discarded)
+      const int jn = (j + 1 < n_mine) ? j + 1 : j;
+      if (jn != j && !mbar_wait_bounded(&bar[jn % STAGES], (jn / STAGES) & 1)) {
+        timed_out = true;
+        break;
+      }
+      const uint8_t* spn = ring + (jn % STAGES) * P::STAGE;
+      const uint4* vcw = reinterpret_cast<const uint4*>(sp + P::KC + P::KM);
+      const uint4* vmr = reinterpret_cast<const uint4*>(sp + P::KC + P::KM + P::VC);
+
+      // ---- online softmax of group j (log2 domain) ----
       float mx = sc[0];
 #pragma unroll
       for (int i = 1; i < 8; ++i) mx = fmaxf(mx, sc[i]);
@@ -463,7 +482,10 @@ __global__ void __launch_bounds__(128, 4) kivi_decode_kernel(KiviDecodeArgs a) {
         vz_run = fmaf(p[2 * nt], zf.x, fmaf(p[2 * nt + 1], zf.y, vz_run));
       }
 
-      // ---- o += p' . codes ----
+      // ---- q . k^T of group j + 1 (independent of what follows) ----
+      qk_scores(spn, sc);
+
+      // ---- o += p' . codes (group j) ----
       uint32_t vw[P::VW];
 #pragma unroll
       for (int c = 0; c < P::VW / 4; ++c) {
@@ -495,7 +517,7 @@ __global__ void __launch_bounds__(128, 4) kivi_decode_kernel(KiviDecodeArgs a) {
         }
       }
 
-      // release the stage and refill it with the group STAGES ahead
+      // release stage j and refill it with the group STAGES ahead
       __syncwarp();
       if (lane == 0 && j + STAGES < n_mine) {
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
