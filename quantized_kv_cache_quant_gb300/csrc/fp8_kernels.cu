@@ -72,37 +72,44 @@ __global__ void __launch_bounds__(256) fp8_scale_kernel(const uint32_t* __restri
 }
 
 // ---------------------------------------------------------------------------
-// Cast + scatter: one (b, h, logical block) unit at a time per thread block.
-// The 16 x D block is staged in shared memory, then each thread writes one
-// 16-byte chunk of the fragment-ordered block.
+// Cast + scatter: each warp takes one (b, h, logical block) unit at a time,
+// stages its 16 x D fp16 values in its own shared-memory slice (16-byte
+// streaming loads), then every lane writes its D/32 16-byte chunks of the
+// fragment-ordered block (chunk c of lane l at byte (c*32 + l)*16, so each
+// store instruction of the warp covers 512 contiguous bytes).
 // ---------------------------------------------------------------------------
+constexpr int kCastWarps = 8;
+
 template <int D>
-__global__ void __launch_bounds__(128) fp8_cast_kernel(Fp8QuantArgs a) {
-  __shared__ __align__(16) __half xs[kBlock * D];
+__global__ void __launch_bounds__(32 * kCastWarps) fp8_cast_kernel(Fp8QuantArgs a) {
+  constexpr int RS = D + 8;  // padded row stride (halves): rows start 4 banks apart
+  __shared__ __align__(16) __half xs_all[kCastWarps][kBlock * RS];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __half* xs = xs_all[warp];
+  const int gg = lane >> 2, tg = lane & 3;
   const int nb = (a.seq_len + kBlock - 1) / kBlock;
   const long long units = static_cast<long long>(a.batch) * a.kv_heads * nb;
   const float scale = *a.scale;
-  const int tid = threadIdx.x;
-  for (long long u = blockIdx.x; u < units; u += gridDim.x) {
+  for (long long u = static_cast<long long>(blockIdx.x) * kCastWarps + warp; u < units;
+       u += static_cast<long long>(gridDim.x) * kCastWarps) {
     const int j = static_cast<int>(u % nb);
     const long long bh = u / nb;
     const int b = static_cast<int>(bh / a.kv_heads), h = static_cast<int>(bh % a.kv_heads);
     const int t0 = j * kBlock;
     const int ntok = min(kBlock, a.seq_len - t0);
-    const uint4* src = reinterpret_cast<const uint4*>(a.x + (bh * a.seq_len + t0) * static_cast<long long>(D));
-    __syncthreads();  // the previous unit's readers are done with xs
-    for (int i = tid; i < kBlock * D / 8; i += 128) {
-      const int tok = i / (D / 8);
-      reinterpret_cast<uint4*>(xs)[i] = (tok < ntok) ? __ldcs(src + i) : make_uint4(0u, 0u, 0u, 0u);
-    }
-    __syncthreads();
     const int blk = a.block_table[static_cast<long long>(b) * a.max_blocks + j];
-    if (blk < 0 || blk >= a.num_blocks) continue;  // uniform per block: no write outside the pool
-    uint8_t* dst = a.pool + (static_cast<long long>(blk) * a.kv_heads + h) * (kBlock * D);
-    // storage chunk tid: lane l = tid % 32 holds stream bytes 16c .. 16c+15, c = tid / 32
-    for (int chunk = tid; chunk < kBlock * D / 16; chunk += 128) {
-      const int l = chunk % 32, c = chunk / 32;
-      const int gg = l >> 2, tg = l & 3;
+    if (blk < 0 || blk >= a.num_blocks) continue;  // uniform per warp: no write outside the pool
+    const uint4* src = reinterpret_cast<const uint4*>(a.x + (bh * a.seq_len + t0) * static_cast<long long>(D));
+    __syncwarp();  // the previous unit's readers are done with xs
+#pragma unroll
+    for (int i = lane; i < kBlock * D / 8; i += 32) {
+      const int tok = i / (D / 8), c8 = i % (D / 8);
+      *reinterpret_cast<uint4*>(xs + tok * RS + 8 * c8) = (tok < ntok) ? __ldcs(src + i) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    __syncwarp();
+    uint4* dst = reinterpret_cast<uint4*>(a.pool + (static_cast<long long>(blk) * a.kv_heads + h) * (kBlock * D));
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
       uint32_t out[4];
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
@@ -120,8 +127,8 @@ __global__ void __launch_bounds__(128) fp8_cast_kernel(Fp8QuantArgs a) {
           ch1 = ch0 + 1;
         }
         const bool v0 = tok0 < ntok, v1 = tok1 < ntok;
-        const float y0 = v0 ? __fdiv_rn(__half2float(xs[tok0 * D + ch0]), scale) : 0.0f;
-        const float y1 = v1 ? __fdiv_rn(__half2float(xs[tok1 * D + ch1]), scale) : 0.0f;
+        const float y0 = v0 ? __fdiv_rn(__half2float(xs[tok0 * RS + ch0]), scale) : 0.0f;
+        const float y1 = v1 ? __fdiv_rn(__half2float(xs[tok1 * RS + ch1]), scale) : 0.0f;
         uint32_t pair = f32x2_to_e4m3x2(y0, y1);
         if (!v0) pair &= 0xFF00u;
         if (!v1) pair &= 0x00FFu;
@@ -130,7 +137,7 @@ __global__ void __launch_bounds__(128) fp8_cast_kernel(Fp8QuantArgs a) {
         else
           out[k >> 1] = pair;
       }
-      reinterpret_cast<uint4*>(dst)[chunk] = make_uint4(out[0], out[1], out[2], out[3]);
+      dst[c * 32 + lane] = make_uint4(out[0], out[1], out[2], out[3]);
     }
   }
 }
@@ -378,11 +385,12 @@ cudaError_t launch_fp8_quantize(const Fp8QuantArgs& a, cudaStream_t s) {
   }
   const int nb = (a.seq_len + kBlock - 1) / kBlock;
   const long long units = static_cast<long long>(a.batch) * a.kv_heads * nb;
-  const int grid = static_cast<int>(units < 16LL * device_sm_count() ? units : 16LL * device_sm_count());
+  const long long want = (units + kCastWarps - 1) / kCastWarps;
+  const int grid = static_cast<int>(want < 8LL * device_sm_count() ? want : 8LL * device_sm_count());
   if (a.head_dim == 128)
-    fp8_cast_kernel<128><<<grid, 128, 0, s>>>(a);
+    fp8_cast_kernel<128><<<grid, 32 * kCastWarps, 0, s>>>(a);
   else if (a.head_dim == 64)
-    fp8_cast_kernel<64><<<grid, 128, 0, s>>>(a);
+    fp8_cast_kernel<64><<<grid, 32 * kCastWarps, 0, s>>>(a);
   else
     return cudaErrorInvalidValue;
   return cudaGetLastError();

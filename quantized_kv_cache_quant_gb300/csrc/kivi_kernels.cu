@@ -62,100 +62,119 @@ __device__ __forceinline__ uint32_t group_code(float x, float zf, float sf, floa
   return static_cast<uint32_t>(fminf(fmaxf(r, 0.0f), levels));
 }
 
+// The same code with the quotient taken as d * RN(1/s) when that provably
+// rounds the same way. With rcp = RN(1/s), |q - d/s| <= 2^-23 |d/s| + tiny and
+// |fl32(d/s) - d/s| <= 2^-24 |d/s|, so for |d/s| <= 16 the two quotients
+// differ by less than 2^-18: rint gives the same integer unless q lies within
+// 2^-17 of a half-integer (a tie or a near-tie), where the IEEE division
+// decides. Quotients above 16 only matter through the clamp, which the same
+// test protects at its boundary levels + 1/2.
+__device__ __forceinline__ uint32_t group_code_rcp(float x, float zf, float sf, float rcp, float levels) {
+  if (sf == 0.0f) return 0u;
+  const float d = __fsub_rn(x, zf);
+  const float q = __fmul_rn(d, rcp);
+  float r = rintf(q);
+  if (fabsf(fabsf(__fsub_rn(q, r)) - 0.5f) < 7.62939453125e-06f) r = rintf(__fdiv_rn(d, sf));
+  return static_cast<uint32_t>(fminf(fmaxf(r, 0.0f), levels));
+}
+
 template <int D, int KB, int VB>
 __global__ void __launch_bounds__(128) kivi_quantize_kernel(QuantGroupsArgs a) {
   using P = Kivi<D, KB, VB>;
-  __shared__ __align__(16) __half xk[32 * D];
-  __shared__ __align__(16) __half xv[32 * D];
-  __shared__ uint8_t ck[32 * D];
-  __shared__ uint8_t cv[32 * D];
-  __shared__ __half sk[D], zk[D], sv[32], zv[32];
+  constexpr int RS = D + 8;  // padded row stride (halves): rows start 4 banks apart
+  __shared__ __align__(16) __half xk[32 * RS];
+  __shared__ __align__(16) __half xv[32 * RS];
+  __shared__ float sk[D], zk[D], rk[D], sv[32], zv[32], rv[32];  // scale, zero, RN(1/scale)
+  __shared__ uint16_t skb[D], zkb[D], svb[32], zvb[32];           // fp16 bits of scale and zero
 
   const int grp = blockIdx.x, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
   const long long bh = static_cast<long long>(b) * a.kv_heads + h;
   const long long src_off = bh * a.src_bh_stride + static_cast<long long>(a.src_tok0 + 32 * grp) * D;
   const uint4* srck = reinterpret_cast<const uint4*>(a.k_src + src_off);
   const uint4* srcv = reinterpret_cast<const uint4*>(a.v_src + src_off);
+#pragma unroll
   for (int i = tid; i < 32 * D / 8; i += 128) {
-    reinterpret_cast<uint4*>(xk)[i] = srck[i];
-    reinterpret_cast<uint4*>(xv)[i] = srcv[i];
+    const int row = i / (D / 8), c8 = i % (D / 8);
+    *reinterpret_cast<uint4*>(xk + row * RS + 8 * c8) = __ldcs(srck + i);
+    *reinterpret_cast<uint4*>(xv + row * RS + 8 * c8) = __ldcs(srcv + i);
   }
   __syncthreads();
 
   constexpr float KL = static_cast<float>((1 << KB) - 1);
   constexpr float VL = static_cast<float>((1 << VB) - 1);
 
-  // Keys: one channel per thread, statistics over the group's 32 tokens.
-  for (int c = tid; c < D; c += 128) {
-    float mn = FLT_MAX, mx = -FLT_MAX;
+  if (tid < D / 2) {
+    // keys: one pair of channels per thread, exact fp16 min/max over the 32 tokens
+    const __half2* col = reinterpret_cast<const __half2*>(xk) + tid;
+    __half2 mn = col[0], mx = col[0];
 #pragma unroll 8
-    for (int t = 0; t < 32; ++t) {
-      const float x = __half2float(xk[t * D + c]);
-      mn = fminf(mn, x);
-      mx = fmaxf(mx, x);
+    for (int t = 1; t < 32; ++t) {
+      const __half2 v = col[t * (RS / 2)];
+      mn = __hmin2(mn, v);
+      mx = __hmax2(mx, v);
     }
-    __half s16, z16;
-    group_scale_zero(mn, mx, KL, s16, z16);
-    sk[c] = s16;
-    zk[c] = z16;
-    const float sf = __half2float(s16), zf = __half2float(z16);
-#pragma unroll 8
-    for (int t = 0; t < 32; ++t) ck[t * D + c] = static_cast<uint8_t>(group_code(__half2float(xk[t * D + c]), zf, sf, KL));
-  }
-
-  // Values: one token per warp step, channels across lanes, warp-shuffle min/max.
-  const int warp = tid >> 5, lane = tid & 31;
-  for (int t = warp; t < 32; t += 4) {
-    float xs[D / 32];
-    float mn = FLT_MAX, mx = -FLT_MAX;
+    const float2 mnf = __half22float2(mn), mxf = __half22float2(mx);
 #pragma unroll
-    for (int j = 0; j < D / 32; ++j) {
-      xs[j] = __half2float(xv[t * D + lane + 32 * j]);
-      mn = fminf(mn, xs[j]);
-      mx = fmaxf(mx, xs[j]);
+    for (int e = 0; e < 2; ++e) {
+      __half s16, z16;
+      group_scale_zero(e ? mnf.y : mnf.x, e ? mxf.y : mxf.x, KL, s16, z16);
+      const int c = 2 * tid + e;
+      sk[c] = __half2float(s16);
+      zk[c] = __half2float(z16);
+      rk[c] = __frcp_rn(__half2float(s16));
+      skb[c] = __half_as_ushort(s16);
+      zkb[c] = __half_as_ushort(z16);
     }
-    mn = warp_min(mn);
-    mx = warp_max(mx);
-    __half s16, z16;
-    group_scale_zero(mn, mx, VL, s16, z16);
-    if (lane == 0) {
-      sv[t] = s16;
-      zv[t] = z16;
-    }
-    const float sf = __half2float(s16), zf = __half2float(z16);
+  } else {
+    // values: one token per warp step over the remaining warps, warp-shuffle min/max
+    const int nw = 4 - (D / 2) / 32;         // warps left after the key channels
+    const int w = warp - (4 - nw);
+    for (int t = w; t < 32; t += nw) {
+      float mn = FLT_MAX, mx = -FLT_MAX;
 #pragma unroll
-    for (int j = 0; j < D / 32; ++j) cv[t * D + lane + 32 * j] = static_cast<uint8_t>(group_code(xs[j], zf, sf, VL));
+      for (int j = 0; j < D / 32; ++j) {
+        const float x = __half2float(xv[t * RS + lane + 32 * j]);
+        mn = fminf(mn, x);
+        mx = fmaxf(mx, x);
+      }
+      mn = warp_min(mn);
+      mx = warp_max(mx);
+      if (lane == 0) {
+        __half s16, z16;
+        group_scale_zero(mn, mx, VL, s16, z16);
+        sv[t] = __half2float(s16);
+        zv[t] = __half2float(z16);
+        rv[t] = __frcp_rn(__half2float(s16));
+        svb[t] = __half_as_ushort(s16);
+        zvb[t] = __half_as_ushort(z16);
+      }
+    }
   }
   __syncthreads();
 
   const long long grp_index = bh * a.groups_cap + a.dst_group0 + grp;
 
-  // Key code words; storage word j belongs to lane (j%128)/4, word u = 4*(j/128) + j%4.
+  // Key code words, computed straight from the staged tile. Storage word j
+  // belongs to lane (j%128)/4, word u = 4*(j/128) + j%4.
   uint32_t* kdst = reinterpret_cast<uint32_t*>(a.k_codes + grp_index * P::KC);
   for (int j = tid; j < 32 * P::KW; j += 128) {
     const int L = (j % 128) / 4, u = (j / 128) * 4 + (j % 4);
     const int gg = L >> 2, tg = L & 3;
     uint32_t w = 0;
-    if constexpr (KB == 2) {
-      const int ks = u;
 #pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int d0 = 16 * ks + 8 * r + 2 * tg;
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
-          const int tok = 8 * nt + gg, f = 4 * r + nt;
-          w |= (static_cast<uint32_t>(ck[tok * D + d0]) << (2 * f)) |
-               (static_cast<uint32_t>(ck[tok * D + d0 + 1]) << (16 + 2 * f));
-        }
-      }
-    } else {
-      const int ks = u >> 1, r = u & 1;
+    for (int rr = 0; rr < 2; ++rr) {
+      // 2 bits: word u = ks holds both r; 4 bits: word u = 2ks + r holds one r
+      if (KB == 4 && rr == 1) break;
+      const int ks = (KB == 2) ? u : (u >> 1);
+      const int r = (KB == 2) ? rr : (u & 1);
       const int d0 = 16 * ks + 8 * r + 2 * tg;
+      const float s0 = sk[d0], s1 = sk[d0 + 1], z0 = zk[d0], z1 = zk[d0 + 1], r0 = rk[d0], r1 = rk[d0 + 1];
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt) {
-        const int tok = 8 * nt + gg;
-        w |= (static_cast<uint32_t>(ck[tok * D + d0]) << (4 * nt)) |
-             (static_cast<uint32_t>(ck[tok * D + d0 + 1]) << (16 + 4 * nt));
+        const float2 x = __half22float2(reinterpret_cast<const __half2*>(xk)[(8 * nt + gg) * (RS / 2) + d0 / 2]);
+        const int f = (KB == 2) ? 4 * r + nt : nt;
+        w |= (group_code_rcp(x.x, z0, s0, r0, KL) << (KB * f)) | (group_code_rcp(x.y, z1, s1, r1, KL) << (16 + KB * f));
       }
     }
     kdst[j] = w;
@@ -167,26 +186,20 @@ __global__ void __launch_bounds__(128) kivi_quantize_kernel(QuantGroupsArgs a) {
     const int L = (j % 128) / 4, u = (j / 128) * 4 + (j % 4);
     const int gg = L >> 2, tg = L & 3;
     uint32_t w = 0;
-    if constexpr (VB == 2) {
-      const int ks = u / P::NQ, q = u % P::NQ;
 #pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int t0 = 16 * ks + 8 * r + 2 * tg;
-#pragma unroll
-        for (int n = 0; n < 4; ++n) {
-          const int ch = 8 * (4 * q + n) + gg, f = 4 * r + n;
-          w |= (static_cast<uint32_t>(cv[t0 * D + ch]) << (2 * f)) |
-               (static_cast<uint32_t>(cv[(t0 + 1) * D + ch]) << (16 + 2 * f));
-        }
-      }
-    } else {
-      const int ks = u / (2 * P::NQ), r = (u / P::NQ) % 2, q = u % P::NQ;
+    for (int rr = 0; rr < 2; ++rr) {
+      if (VB == 4 && rr == 1) break;
+      const int ks = (VB == 2) ? u / P::NQ : u / (2 * P::NQ);
+      const int r = (VB == 2) ? rr : (u / P::NQ) % 2;
+      const int q = u % P::NQ;
       const int t0 = 16 * ks + 8 * r + 2 * tg;
+      const float s0 = sv[t0], s1 = sv[t0 + 1], z0 = zv[t0], z1 = zv[t0 + 1], r0 = rv[t0], r1 = rv[t0 + 1];
 #pragma unroll
       for (int n = 0; n < 4; ++n) {
         const int ch = 8 * (4 * q + n) + gg;
-        w |= (static_cast<uint32_t>(cv[t0 * D + ch]) << (4 * n)) |
-             (static_cast<uint32_t>(cv[(t0 + 1) * D + ch]) << (16 + 4 * n));
+        const float x0 = __half2float(xv[t0 * RS + ch]), x1 = __half2float(xv[(t0 + 1) * RS + ch]);
+        const int f = (VB == 2) ? 4 * r + n : n;
+        w |= (group_code_rcp(x0, z0, s0, r0, VL) << (VB * f)) | (group_code_rcp(x1, z1, s1, r1, VL) << (16 + VB * f));
       }
     }
     vdst[j] = w;
@@ -195,36 +208,22 @@ __global__ void __launch_bounds__(128) kivi_quantize_kernel(QuantGroupsArgs a) {
   // Key meta: record ks*4 + tig = {s[d0], s[d0+1], s[d0+8], s[d0+9], z[...]}.
   if (tid < D / 4) {
     const int ks = tid >> 2, tg = tid & 3, d0 = 16 * ks + 2 * tg;
-    const int chans[4] = {d0, d0 + 1, d0 + 8, d0 + 9};
-    uint16_t v[8];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      v[i] = __half_as_ushort(sk[chans[i]]);
-      v[4 + i] = __half_as_ushort(zk[chans[i]]);
-    }
     uint4 rec;
-    rec.x = v[0] | (static_cast<uint32_t>(v[1]) << 16);
-    rec.y = v[2] | (static_cast<uint32_t>(v[3]) << 16);
-    rec.z = v[4] | (static_cast<uint32_t>(v[5]) << 16);
-    rec.w = v[6] | (static_cast<uint32_t>(v[7]) << 16);
+    rec.x = skb[d0] | (static_cast<uint32_t>(skb[d0 + 1]) << 16);
+    rec.y = skb[d0 + 8] | (static_cast<uint32_t>(skb[d0 + 9]) << 16);
+    rec.z = zkb[d0] | (static_cast<uint32_t>(zkb[d0 + 1]) << 16);
+    rec.w = zkb[d0 + 8] | (static_cast<uint32_t>(zkb[d0 + 9]) << 16);
     reinterpret_cast<uint4*>(a.k_meta + grp_index * P::KM)[tid] = rec;
-  }
-  // Value meta: 4 records of scales, then 4 of zero points.
-  if (tid < 8) {
-    const int tg = tid & 3;
-    const __half* src = (tid < 4) ? sv : zv;
-    uint16_t v[8];
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
-      v[2 * nt] = __half_as_ushort(src[8 * nt + 2 * tg]);
-      v[2 * nt + 1] = __half_as_ushort(src[8 * nt + 2 * tg + 1]);
-    }
+  } else if (tid >= 64 && tid < 72) {
+    // Value meta: 4 records of scales, then 4 of zero points.
+    const int i = tid - 64, tg = i & 3;
+    const uint16_t* src = (i < 4) ? svb : zvb;
     uint4 rec;
-    rec.x = v[0] | (static_cast<uint32_t>(v[1]) << 16);
-    rec.y = v[2] | (static_cast<uint32_t>(v[3]) << 16);
-    rec.z = v[4] | (static_cast<uint32_t>(v[5]) << 16);
-    rec.w = v[6] | (static_cast<uint32_t>(v[7]) << 16);
-    reinterpret_cast<uint4*>(a.v_meta + grp_index * P::VM)[tid] = rec;
+    rec.x = src[2 * tg] | (static_cast<uint32_t>(src[2 * tg + 1]) << 16);
+    rec.y = src[8 + 2 * tg] | (static_cast<uint32_t>(src[9 + 2 * tg]) << 16);
+    rec.z = src[16 + 2 * tg] | (static_cast<uint32_t>(src[17 + 2 * tg]) << 16);
+    rec.w = src[24 + 2 * tg] | (static_cast<uint32_t>(src[25 + 2 * tg]) << 16);
+    reinterpret_cast<uint4*>(a.v_meta + grp_index * P::VM)[i] = rec;
   }
 }
 

@@ -220,3 +220,27 @@ def test_full_size_streaming_128k():
     assert (gc.n_grouped, gc.n_resid) == (131456, 128)
     assert_residual_equal(gc, oc)
     assert gc.status() == 0
+
+
+@pytest.mark.parametrize("kb,vb", [(2, 2), (4, 4)])
+def test_prefill_exact_ties(kb, vb):
+    """Quotients that land exactly on half-integers (ties, rounded to even) and
+    just beside them: every code must match the oracle's IEEE fp32 formula."""
+    kvq = _kvq()
+    rng = np.random.default_rng(kb * 10 + vb)
+    b, h, d, s = 2, 2, 128, 32 * 8
+    levels = 2 ** kb - 1
+    k = np.empty((b, h, s, d), np.float16)
+    for g in range(s // 32):
+        step = np.float16(2.0 ** int(rng.integers(-6, 3)))
+        base = np.float16(int(rng.integers(-20, 20)) * float(step))
+        half = rng.integers(0, 2 * levels + 1, size=(b, h, 32, d))          # multiples of step / 2
+        half[:, :, 0, :], half[:, :, 1, :] = 0, 2 * levels                   # fix min and max
+        k[:, :, 32 * g:32 * g + 32] = (np.float64(base) + half * float(step) / 2).astype(np.float16)
+    nudge = rng.random(k.shape) < 0.2                                       # some values one ulp off a tie
+    k = np.where(nudge, np.nextafter(k, np.float16(np.inf)), k).astype(np.float16)
+    v = k.copy()
+    gc = kvq.KiviCache(b, h, 2 * h, d, kb, vb, 0, s)
+    gc.prefill(dev(k), dev(v))
+    oc = oracle_cache(dict(k_bits=kb, v_bits=vb, residual=0, max_tokens=s), k, v)
+    assert_grouped_bytes_equal(gc, oc)
