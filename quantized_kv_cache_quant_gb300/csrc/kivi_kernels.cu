@@ -62,20 +62,96 @@ __device__ __forceinline__ uint32_t group_code(float x, float zf, float sf, floa
   return static_cast<uint32_t>(fminf(fmaxf(r, 0.0f), levels));
 }
 
-// The same code with the quotient taken as d * RN(1/s) when that provably
-// rounds the same way. With rcp = RN(1/s), |q - d/s| <= 2^-23 |d/s| + tiny and
-// |fl32(d/s) - d/s| <= 2^-24 |d/s|, so for |d/s| <= 16 the two quotients
-// differ by less than 2^-18: rint gives the same integer unless q lies within
-// 2^-17 of a half-integer (a tie or a near-tie), where the IEEE division
-// decides. Quotients above 16 only matter through the clamp, which the same
-// test protects at its boundary levels + 1/2.
-__device__ __forceinline__ uint32_t group_code_rcp(float x, float zf, float sf, float rcp, float levels) {
-  if (sf == 0.0f) return 0u;
-  const float d = __fsub_rn(x, zf);
-  const float q = __fmul_rn(d, rcp);
-  float r = rintf(q);
-  if (fabsf(fabsf(__fsub_rn(q, r)) - 0.5f) < 7.62939453125e-06f) r = rintf(__fdiv_rn(d, sf));
+// The same code with the quotient taken as d * rcp, rcp = RN(1/s) (0 when
+// s == 0, which gives code 0 as the formula does). With rcp = RN(1/s),
+// |q - d/s| <= 2^-23 |d/s| + tiny and |fl32(d/s) - d/s| <= 2^-24 |d/s|, so for
+// |d/s| <= 16 the two quotients differ by less than 2^-18: rint gives the same
+// integer unless q lies within 2^-17 of a half-integer (a tie or a near-tie).
+// Such an element raises `near`, and the caller recomputes its word with the
+// IEEE division. Quotients above 16 only matter through the clamp, which the
+// same test protects at its boundary levels + 1/2.
+__device__ __forceinline__ uint32_t group_code_fast(float x, float zf, float rcp, float levels, bool& near) {
+  const float q = __fmul_rn(__fsub_rn(x, zf), rcp);
+  const float r = rintf(q);
+  near |= fabsf(fabsf(__fsub_rn(q, r)) - 0.5f) < 7.62939453125e-06f;
   return static_cast<uint32_t>(fminf(fmaxf(r, 0.0f), levels));
+}
+
+// One packed code word of a group. EXACT = false: reciprocal fast path (sets
+// `near`); EXACT = true: every code by the IEEE division.
+template <bool EXACT>
+struct CodeOf {
+  __device__ __forceinline__ static uint32_t get(float x, float z, float s, float rcp, float levels, bool& near) {
+    if constexpr (EXACT) {
+      (void)rcp;
+      (void)near;
+      return group_code(x, z, s, levels);
+    } else {
+      (void)s;
+      return group_code_fast(x, z, rcp, levels, near);
+    }
+  }
+};
+
+template <int D, int KB, bool EXACT>
+__device__ __forceinline__ uint32_t key_word(const __half* xk, int RS, const float* sk, const float* zk,
+                                             const float* rk, int u, int gg, int tg, bool& near) {
+  constexpr float KL = static_cast<float>((1 << KB) - 1);
+  uint32_t w = 0;
+#pragma unroll
+  for (int rr = 0; rr < (KB == 2 ? 2 : 1); ++rr) {
+    const int ks = (KB == 2) ? u : (u >> 1);
+    const int r = (KB == 2) ? rr : (u & 1);
+    const int d0 = 16 * ks + 8 * r + 2 * tg;
+    const float s0 = sk[d0], s1 = sk[d0 + 1], z0 = zk[d0], z1 = zk[d0 + 1], r0 = rk[d0], r1 = rk[d0 + 1];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      const float2 x = __half22float2(reinterpret_cast<const __half2*>(xk)[(8 * nt + gg) * (RS / 2) + d0 / 2]);
+      const int f = (KB == 2) ? 4 * r + nt : nt;
+      w |= (CodeOf<EXACT>::get(x.x, z0, s0, r0, KL, near) << (KB * f)) |
+           (CodeOf<EXACT>::get(x.y, z1, s1, r1, KL, near) << (16 + KB * f));
+    }
+  }
+  return w;
+}
+
+template <int D, int VB, bool EXACT>
+__device__ __forceinline__ uint32_t value_word(const __half* xv, int RS, const float* sv, const float* zv,
+                                               const float* rv, int u, int gg, int tg, bool& near) {
+  constexpr float VL = static_cast<float>((1 << VB) - 1);
+  constexpr int NQ = D / 32;
+  uint32_t w = 0;
+#pragma unroll
+  for (int rr = 0; rr < (VB == 2 ? 2 : 1); ++rr) {
+    const int ks = (VB == 2) ? u / NQ : u / (2 * NQ);
+    const int r = (VB == 2) ? rr : (u / NQ) % 2;
+    const int q = u % NQ;
+    const int t0 = 16 * ks + 8 * r + 2 * tg;
+    const float s0 = sv[t0], s1 = sv[t0 + 1], z0 = zv[t0], z1 = zv[t0 + 1], r0 = rv[t0], r1 = rv[t0 + 1];
+#pragma unroll
+    for (int n = 0; n < 4; ++n) {
+      const int ch = 8 * (4 * q + n) + gg;
+      const float x0 = __half2float(xv[t0 * RS + ch]), x1 = __half2float(xv[(t0 + 1) * RS + ch]);
+      const int f = (VB == 2) ? 4 * r + n : n;
+      w |= (CodeOf<EXACT>::get(x0, z0, s0, r0, VL, near) << (VB * f)) |
+           (CodeOf<EXACT>::get(x1, z1, s1, r1, VL, near) << (16 + VB * f));
+    }
+  }
+  return w;
+}
+
+template <int D, int KB>
+__device__ __noinline__ uint32_t key_word_exact(const __half* xk, int RS, const float* sk, const float* zk,
+                                                const float* rk, int u, int gg, int tg) {
+  bool unused = false;
+  return key_word<D, KB, true>(xk, RS, sk, zk, rk, u, gg, tg, unused);
+}
+
+template <int D, int VB>
+__device__ __noinline__ uint32_t value_word_exact(const __half* xv, int RS, const float* sv, const float* zv,
+                                                  const float* rv, int u, int gg, int tg) {
+  bool unused = false;
+  return value_word<D, VB, true>(xv, RS, sv, zv, rv, u, gg, tg, unused);
 }
 
 template <int D, int KB, int VB>
@@ -122,7 +198,7 @@ __global__ void __launch_bounds__(128) kivi_quantize_kernel(QuantGroupsArgs a) {
       const int c = 2 * tid + e;
       sk[c] = __half2float(s16);
       zk[c] = __half2float(z16);
-      rk[c] = __frcp_rn(__half2float(s16));
+      rk[c] = (__half2float(s16) == 0.0f) ? 0.0f : __frcp_rn(__half2float(s16));
       skb[c] = __half_as_ushort(s16);
       zkb[c] = __half_as_ushort(z16);
     }
@@ -145,7 +221,7 @@ __global__ void __launch_bounds__(128) kivi_quantize_kernel(QuantGroupsArgs a) {
         group_scale_zero(mn, mx, VL, s16, z16);
         sv[t] = __half2float(s16);
         zv[t] = __half2float(z16);
-        rv[t] = __frcp_rn(__half2float(s16));
+        rv[t] = (__half2float(s16) == 0.0f) ? 0.0f : __frcp_rn(__half2float(s16));
         svb[t] = __half_as_ushort(s16);
         zvb[t] = __half_as_ushort(z16);
       }
@@ -160,23 +236,9 @@ __global__ void __launch_bounds__(128) kivi_quantize_kernel(QuantGroupsArgs a) {
   uint32_t* kdst = reinterpret_cast<uint32_t*>(a.k_codes + grp_index * P::KC);
   for (int j = tid; j < 32 * P::KW; j += 128) {
     const int L = (j % 128) / 4, u = (j / 128) * 4 + (j % 4);
-    const int gg = L >> 2, tg = L & 3;
-    uint32_t w = 0;
-#pragma unroll
-    for (int rr = 0; rr < 2; ++rr) {
-      // 2 bits: word u = ks holds both r; 4 bits: word u = 2ks + r holds one r
-      if (KB == 4 && rr == 1) break;
-      const int ks = (KB == 2) ? u : (u >> 1);
-      const int r = (KB == 2) ? rr : (u & 1);
-      const int d0 = 16 * ks + 8 * r + 2 * tg;
-      const float s0 = sk[d0], s1 = sk[d0 + 1], z0 = zk[d0], z1 = zk[d0 + 1], r0 = rk[d0], r1 = rk[d0 + 1];
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-        const float2 x = __half22float2(reinterpret_cast<const __half2*>(xk)[(8 * nt + gg) * (RS / 2) + d0 / 2]);
-        const int f = (KB == 2) ? 4 * r + nt : nt;
-        w |= (group_code_rcp(x.x, z0, s0, r0, KL) << (KB * f)) | (group_code_rcp(x.y, z1, s1, r1, KL) << (16 + KB * f));
-      }
-    }
+    bool near = false;
+    uint32_t w = key_word<D, KB, false>(xk, RS, sk, zk, rk, u, L >> 2, L & 3, near);
+    if (near) w = key_word_exact<D, KB>(xk, RS, sk, zk, rk, u, L >> 2, L & 3);
     kdst[j] = w;
   }
 
@@ -184,24 +246,9 @@ __global__ void __launch_bounds__(128) kivi_quantize_kernel(QuantGroupsArgs a) {
   uint32_t* vdst = reinterpret_cast<uint32_t*>(a.v_codes + grp_index * P::VC);
   for (int j = tid; j < 32 * P::VW; j += 128) {
     const int L = (j % 128) / 4, u = (j / 128) * 4 + (j % 4);
-    const int gg = L >> 2, tg = L & 3;
-    uint32_t w = 0;
-#pragma unroll
-    for (int rr = 0; rr < 2; ++rr) {
-      if (VB == 4 && rr == 1) break;
-      const int ks = (VB == 2) ? u / P::NQ : u / (2 * P::NQ);
-      const int r = (VB == 2) ? rr : (u / P::NQ) % 2;
-      const int q = u % P::NQ;
-      const int t0 = 16 * ks + 8 * r + 2 * tg;
-      const float s0 = sv[t0], s1 = sv[t0 + 1], z0 = zv[t0], z1 = zv[t0 + 1], r0 = rv[t0], r1 = rv[t0 + 1];
-#pragma unroll
-      for (int n = 0; n < 4; ++n) {
-        const int ch = 8 * (4 * q + n) + gg;
-        const float x0 = __half2float(xv[t0 * RS + ch]), x1 = __half2float(xv[(t0 + 1) * RS + ch]);
-        const int f = (VB == 2) ? 4 * r + n : n;
-        w |= (group_code_rcp(x0, z0, s0, r0, VL) << (VB * f)) | (group_code_rcp(x1, z1, s1, r1, VL) << (16 + VB * f));
-      }
-    }
+    bool near = false;
+    uint32_t w = value_word<D, VB, false>(xv, RS, sv, zv, rv, u, L >> 2, L & 3, near);
+    if (near) w = value_word_exact<D, VB>(xv, RS, sv, zv, rv, u, L >> 2, L & 3);
     vdst[j] = w;
   }
 
@@ -445,9 +492,12 @@ __global__ void __launch_bounds__(128, KVQ_DECODE_MIN_BLOCKS) kivi_decode_kernel
 #pragma unroll
       for (int i = 1; i < 8; ++i) mx = fmaxf(mx, sc[i]);
       mx = quad_max(mx);
-      const float m_new = fmaxf(m_run, mx);
-      if (m_new != m_run) {
-        const float alpha = fast_exp2(m_run - m_new);
+      // The reference m_run moves only when a score exceeds it by more than
+      // 0.5 (log2 units), so weights stay <= 2^0.5 and p * s_t still fits fp16
+      // for any scale (2^0.5 * 43669 < 65504); the rescale of the 64
+      // accumulators then runs rarely instead of whenever some head's max grows.
+      if (mx > m_run + 0.5f) {
+        const float alpha = fast_exp2(m_run - mx);
         l_run *= alpha;
         vz_run *= alpha;
 #pragma unroll
@@ -457,11 +507,11 @@ __global__ void __launch_bounds__(128, KVQ_DECODE_MIN_BLOCKS) kivi_decode_kernel
           o_acc[i][2] *= alpha;
           o_acc[i][3] *= alpha;
         }
-        m_run = m_new;
+        m_run = mx;
       }
       float p[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) p[i] = fast_exp2(sc[i] - m_new);
+      for (int i = 0; i < 8; ++i) p[i] = fast_exp2(sc[i] - m_run);
 
       // ---- p' = p * s_t as fp16 hi + lo; the zero-point term on CUDA cores ----
       const uint4 vs = vmr[tig], vz = vmr[4 + tig];
