@@ -130,24 +130,30 @@ def barrier(world):
         dist.barrier()
 
 
-def max_over_ranks(x: float, world: int) -> float:
+def _reduce(x: float, world: int, op_name: str) -> float:
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=getattr(dist.ReduceOp, op_name))
     return float(t.item())
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    return _reduce(x, world, "MAX")
 
 
 def sum_over_ranks(x: float, world: int) -> float:
-    if world == 1:
-        return x
-    import torch
-    import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.SUM)
-    return float(t.item())
+    return _reduce(x, world, "SUM")
+
+
+def aggregate(bytes_local: float, seconds_local: float, world: int):
+    """Whole-job throughput under weak scaling: the bytes every rank moved over
+    the slowest rank's time. Returns (GB/s, max seconds)."""
+    t = max_over_ranks(seconds_local, world)
+    return sum_over_ranks(float(bytes_local), world) / t / 1e9, t
 
 
 # ---------------------------------------------------------------------------
@@ -234,10 +240,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     clk = clocks.stop() if clocks else None
     barrier(world)
-    t_local = start.elapsed_time(end) / 1e3
-    t = max_over_ranks(t_local, world)
-    total_bytes = sum_over_ranks(float(nbytes), world)
-    value = total_bytes / t / 1e9
+    value, t = aggregate(nbytes, start.elapsed_time(end) / 1e3, world)
     dec_times = [a.elapsed_time(b) / 1e3 for a, b in ev]
     achieved = statistics.mean(db / dt for db, dt in zip(dec_bytes, dec_times)) / 1e9
     status = cache.status()
@@ -269,8 +272,7 @@ def run_ours(args, world, rank, local):
     e_end.record(stream)
     torch.cuda.synchronize()
     barrier(world)
-    te = max_over_ranks(e_start.elapsed_time(e_end) / 1e3, world)
-    e2e_value = sum_over_ranks(float(e2e_bytes), world) / te / 1e9
+    e2e_value, _ = aggregate(e2e_bytes, e_start.elapsed_time(e_end) / 1e3, world)
     h2d = q_h[0].numel() * 2 + kn_h[0].numel() * 2 + vn_h[0].numel() * 2
     d2h = out_h.numel() * 4
 

@@ -102,7 +102,7 @@ def _oracle_decode(q16, k16, v16, ks, vs, seq_lens, heads=None):
     return attention.decode_attention(q16, kh, vh, hkv, default_scale(d), heads)
 
 
-@pytest.mark.parametrize("d,gq", [(128, 4), (64, 1), (128, 8), (64, 2)])
+@pytest.mark.parametrize("d,gq", [(128, 4), (64, 1), (128, 8), (64, 2), (128, 3), (64, 7)])
 def test_decode_ragged_lengths(d, gq):
     rng = np.random.default_rng(d + gq)
     b, hkv, s = 3, 2, 16 * 40 + 9

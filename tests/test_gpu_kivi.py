@@ -42,8 +42,8 @@ def test_prefill_bytes(d, kb, vb):
 
 
 @pytest.mark.parametrize("d", [64, 128])
-@pytest.mark.parametrize("gq", [1, 2, 4, 8])
-@pytest.mark.parametrize("kb,vb", [(2, 2), (4, 4)])
+@pytest.mark.parametrize("gq", [1, 2, 3, 4, 5, 7, 8])
+@pytest.mark.parametrize("kb,vb", [(2, 2), (4, 4), (2, 4)])
 def test_decode_attention(d, gq, kb, vb):
     s = 32 * 37 + 128 - 9          # 37 groups (several splits), a ragged window
     kvq, x, gc, oc = _run(2, 2, 2 * gq, d, s, kb, vb, seed=100 + gq)
@@ -78,6 +78,38 @@ def test_fully_grouped_r0():
     assert_grouped_bytes_equal(gc, oc)
     out = host(gc.decode(dev(x.q[0])))
     assert_attention_close(out, oracle_attention(oc, x.q[0], default_scale(128)))
+
+
+def test_zero_query_gives_mean_of_values():
+    """q = 0: every score is 0, attention is the mean of the dequantized values."""
+    kvq, x, gc, oc = _run(1, 2, 4, 128, 32 * 9 + 50, seed=17)
+    q = np.zeros_like(x.q[0])
+    out = host(gc.decode(dev(q)))
+    for h in range(4):
+        want = oc.values_hat(0, h // 2).mean(axis=0)
+        assert np.allclose(out[0, h], want, atol=2e-3, rtol=0)
+
+
+def test_fill_to_capacity_then_reject():
+    """Append until the cache holds max_tokens; the next append is refused and
+    the cache state is unchanged."""
+    kvq = _kvq()
+    x = workloads.make_inputs(1, 2, 2, 64, 100, 70, 8)
+    gc = kvq.KiviCache(1, 2, 2, 64, 2, 2, 32, 170)
+    oc = oracle_cache(dict(k_bits=2, v_bits=2, residual=32, max_tokens=170), x.k, x.v)
+    gc.prefill(dev(x.k), dev(x.v))
+    for step in range(70):
+        gc.append(dev(x.k_new[step]), dev(x.v_new[step]))
+        oc.append(x.k_new[step], x.v_new[step])
+    assert gc.n_grouped + gc.n_resid == 170
+    with pytest.raises(kvq.KvqError) as e:
+        gc.append(dev(x.k_new[0]), dev(x.v_new[0]))
+    assert e.value.name == "KVQ_ERR_CAPACITY"
+    assert gc.n_grouped + gc.n_resid == 170
+    assert_grouped_bytes_equal(gc, oc)
+    assert_residual_equal(gc, oc)
+    out = host(gc.decode(dev(x.q[0])))
+    assert_attention_close(out, oracle_attention(oc, x.q[0], default_scale(64)))
 
 
 def test_custom_softmax_scale():
