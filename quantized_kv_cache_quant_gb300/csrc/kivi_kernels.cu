@@ -427,7 +427,9 @@ __global__ void __launch_bounds__(128, KVQ_DECODE_MIN_BLOCKS) kivi_decode_kernel
       float sacc[4][4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) sacc[i][0] = sacc[i][1] = sacc[i][2] = sacc[i][3] = 0.0f;
-      float bacc[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // q . z (every column equal)
+      // q . z: this lane's four channels of head g on the FMA pipe (the tensor pipe is the
+      // busier one here); a quad sum after the loop completes the dot product.
+      float bsum = 0.0f;
 #pragma unroll
       for (int ks = 0; ks < P::KS; ++ks) {
         const uint4 md = kmr[ks * 4 + tig];  // {s(d0,d0+1), s(d0+8,d0+9), z(d0,d0+1), z(d0+8,d0+9)}
@@ -437,7 +439,7 @@ __global__ void __launch_bounds__(128, KVQ_DECODE_MIN_BLOCKS) kivi_decode_kernel
         const __half2 hi1 = __hmul2(q1, bits_h2(md.y));
         const __half2 lo1 = __hfma2(q1, bits_h2(md.y), __hneg2(hi1));
         const uint32_t A0 = h2_bits(hi0), A1 = h2_bits(lo0), A2 = h2_bits(hi1), A3 = h2_bits(lo1);
-        mma16816(bacc, qs[ks][0], 0u, qs[ks][1], 0u, md.z, md.w);
+        bsum = dot2_f16_f32(qs[ks][0], md.z, dot2_f16_f32(qs[ks][1], md.w, bsum));
         if constexpr (KB == 2) {
           const uint32_t w = kw[ks];
           const uint32_t l6 = w << 6, l2 = w << 2, r2 = w >> 2, r6 = w >> 6;
@@ -453,7 +455,7 @@ __global__ void __launch_bounds__(128, KVQ_DECODE_MIN_BLOCKS) kivi_decode_kernel
           mma16816(sacc[3], A0, A1, A2, A3, (w0 >> 6) & kMask4, (w1 >> 6) & kMask4);
         }
       }
-      const float bias = bacc[0] * p2e;
+      const float bias = quad_sum(bsum) * p2e;
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt) {
         const float mult = (KB == 2 && (nt & 1)) ? mult8 : mult6;
