@@ -146,6 +146,60 @@ int choose_splits(int units, int pairs, int max_splits, int blocks_per_sm, int e
   return ceil_div(units, per);
 }
 
+// The decode grid of a KIVI cache. The work of one (batch row, kv head) is a
+// range of units: its groups, then its fp16 window cut into 32-token chunks of
+// kChunkUnits units each (a chunk is one warp's work, about two groups' time
+// for the whole block); the range is cut evenly into `splits` blocks.
+struct DecodePlan {
+  int n_groups;
+  int splits;
+  int units_per_split;
+};
+
+DecodePlan plan_kivi_decode(const kivi_cache* cache) {
+  const kivi_config& cf = cache->cfg;
+  DecodePlan p{};
+  p.n_groups = cache->n_grouped / kGroup;
+  const int units = p.n_groups + kvq::kChunkUnits * ceil_div(cache->n_resid, kGroup);
+  p.splits = choose_splits(units, cf.batch * cf.kv_heads, kMaxSplits,
+                           kvq::kivi_decode_blocks_per_sm(cf.head_dim, cf.k_bits, cf.v_bits), 0);
+  p.units_per_split = ceil_div(units, p.splits);
+  return p;
+}
+
+kvq::KiviDecodeArgs kivi_decode_args(const kivi_cache* cache, const DecodePlan& plan, const uint16_t* q, void* out,
+                                     int32_t out_fp32, float scale, uint8_t* ws) {
+  const kivi_config& cf = cache->cfg;
+  kvq::KiviDecodeArgs a{};
+  a.k_codes = cache->k_codes;
+  a.k_meta = cache->k_meta;
+  a.v_codes = cache->v_codes;
+  a.v_meta = cache->v_meta;
+  a.k_res = cache->k_res;
+  a.v_res = cache->v_res;
+  a.q = q;
+  a.batch = cf.batch;
+  a.kv_heads = cf.kv_heads;
+  a.q_heads = cf.q_heads;
+  a.head_dim = cf.head_dim;
+  a.k_bits = cf.k_bits;
+  a.v_bits = cf.v_bits;
+  a.groups_cap = cache->groups_cap;
+  a.res_cap = cache->res_cap;
+  a.n_groups = plan.n_groups;
+  a.n_resid = cache->n_resid;
+  a.units_per_split = plan.units_per_split;
+  a.splits_total = plan.splits;
+  a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  a.status = reinterpret_cast<uint32_t*>(ws);
+  a.counters = reinterpret_cast<uint32_t*>(ws + kWsHeader);
+  a.part_o = reinterpret_cast<float*>(ws + kWsHeader + counters_bytes(cf.batch, cf.q_heads));
+  a.part_ml = a.part_o + static_cast<size_t>(cf.batch) * cf.q_heads * plan.splits * cf.head_dim;
+  a.out = out;
+  a.out_fp32 = out_fp32;
+  return a;
+}
+
 }  // namespace
 
 extern "C" {
@@ -318,41 +372,8 @@ kvq_status kv_decode_attention(const kivi_cache* cache, const uint16_t* q, void*
   if (!(softmax_scale == softmax_scale) || std::isinf(softmax_scale)) return KVQ_ERR_ARG;
   const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(cf.head_dim));
 
-  const int ng = cache->n_grouped / kGroup;
-  const int pairs = cf.batch * cf.kv_heads;
-  const int has_resid = cache->n_resid > 0 ? 1 : 0;
-  const int splits_g = choose_splits(ng, pairs, kMaxSplits - 1,
-                                     kvq::kivi_decode_blocks_per_sm(cf.head_dim, cf.k_bits, cf.v_bits),
-                                     has_resid ? pairs : 0);
-  kvq::KiviDecodeArgs a{};
-  a.k_codes = cache->k_codes;
-  a.k_meta = cache->k_meta;
-  a.v_codes = cache->v_codes;
-  a.v_meta = cache->v_meta;
-  a.k_res = cache->k_res;
-  a.v_res = cache->v_res;
-  a.q = q;
-  a.batch = cf.batch;
-  a.kv_heads = cf.kv_heads;
-  a.q_heads = cf.q_heads;
-  a.head_dim = cf.head_dim;
-  a.k_bits = cf.k_bits;
-  a.v_bits = cf.v_bits;
-  a.groups_cap = cache->groups_cap;
-  a.res_cap = cache->res_cap;
-  a.n_groups = ng;
-  a.n_resid = cache->n_resid;
-  a.splits_g = splits_g;
-  a.groups_per_split = splits_g > 0 ? ceil_div(ng, splits_g) : 0;
-  a.splits_total = splits_g + has_resid;
-  a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-  uint8_t* base = static_cast<uint8_t*>(ws);
-  a.status = reinterpret_cast<uint32_t*>(base);
-  a.counters = reinterpret_cast<uint32_t*>(base + kWsHeader);
-  a.part_o = reinterpret_cast<float*>(base + kWsHeader + counters_bytes(cf.batch, cf.q_heads));
-  a.part_ml = a.part_o + static_cast<size_t>(cf.batch) * cf.q_heads * a.splits_total * cf.head_dim;
-  a.out = out;
-  a.out_fp32 = out_fp32;
+  const DecodePlan plan = plan_kivi_decode(cache);
+  const kvq::KiviDecodeArgs a = kivi_decode_args(cache, plan, q, out, out_fp32, scale, static_cast<uint8_t*>(ws));
   return from_cuda(kvq::launch_kivi_decode(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -504,13 +525,8 @@ kvq_status kv_decode_attention_noalloc(const kivi_cache* cache, const uint16_t* 
   const kivi_config& cf = cache->cfg;
   const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(cf.head_dim));
 
-  const int ng = cache->n_grouped / kGroup;
-  const int pairs = cf.batch * cf.kv_heads;
-  const int has_resid = cache->n_resid > 0 ? 1 : 0;
-  const int splits_g = choose_splits(ng, pairs, kMaxSplits - 1,
-                                     kvq::kivi_decode_blocks_per_sm(cf.head_dim, cf.k_bits, cf.v_bits),
-                                     has_resid ? pairs : 0);
-  const int splits_total = splits_g + has_resid;
+  const DecodePlan plan = plan_kivi_decode(cache);
+  const int splits_total = plan.splits;
   const size_t head = static_cast<size_t>(kWsHeader) + counters_bytes(cf.batch, cf.q_heads);
   const size_t need = head + static_cast<size_t>(cf.batch) * cf.q_heads * splits_total *
                                  (static_cast<size_t>(cf.head_dim) + 2) * sizeof(float);
@@ -523,35 +539,7 @@ kvq_status kv_decode_attention_noalloc(const kivi_cache* cache, const uint16_t* 
   // the status word and the split counters must start at zero
   if (cudaMemsetAsync(ws, 0, head, s) != cudaSuccess) return KVQ_ERR_CUDA;
 
-  kvq::KiviDecodeArgs a{};
-  a.k_codes = cache->k_codes;
-  a.k_meta = cache->k_meta;
-  a.v_codes = cache->v_codes;
-  a.v_meta = cache->v_meta;
-  a.k_res = cache->k_res;
-  a.v_res = cache->v_res;
-  a.q = q;
-  a.batch = cf.batch;
-  a.kv_heads = cf.kv_heads;
-  a.q_heads = cf.q_heads;
-  a.head_dim = cf.head_dim;
-  a.k_bits = cf.k_bits;
-  a.v_bits = cf.v_bits;
-  a.groups_cap = cache->groups_cap;
-  a.res_cap = cache->res_cap;
-  a.n_groups = ng;
-  a.n_resid = cache->n_resid;
-  a.splits_g = splits_g;
-  a.groups_per_split = splits_g > 0 ? ceil_div(ng, splits_g) : 0;
-  a.splits_total = splits_total;
-  a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-  uint8_t* base = static_cast<uint8_t*>(ws);
-  a.status = reinterpret_cast<uint32_t*>(base);
-  a.counters = reinterpret_cast<uint32_t*>(base + kWsHeader);
-  a.part_o = reinterpret_cast<float*>(base + head);
-  a.part_ml = a.part_o + static_cast<size_t>(cf.batch) * cf.q_heads * splits_total * cf.head_dim;
-  a.out = out;
-  a.out_fp32 = out_fp32;
+  const kvq::KiviDecodeArgs a = kivi_decode_args(cache, plan, q, out, out_fp32, scale, static_cast<uint8_t*>(ws));
   return from_cuda(kvq::launch_kivi_decode(a, s));
 }
 

@@ -296,22 +296,24 @@ __global__ void copy_tokens_kernel(CopyTokensArgs a) {
 // ---------------------------------------------------------------------------
 // Split-K decode attention
 // ---------------------------------------------------------------------------
-// Grid (splits_total, H_kv, B), 4 warps. Thread blocks x < splits_g take a
-// contiguous range of groups; warp w of such a block takes groups
-// begin + w, begin + w + 4, ... through its own ring of STAGES shared-memory
-// stages filled by bulk copies (one mbarrier per stage). The last block
-// (x == splits_g) attends over the fp16 window on CUDA cores. Each block
-// writes unnormalized (m, l, o) partials per query head; m and the scores are
-// in log2 units.
+// Grid (splits, H_kv, B), 4 warps. The work of one (batch row, kv head) is a
+// range of units: its groups, then its fp16 window cut into 32-token chunks
+// worth kChunkUnits units each; split x takes units [x * U, (x + 1) * U).
+// Warp w of a block takes the block's groups begin + w, begin + w + 4, ...
+// through its own ring of STAGES shared-memory stages filled by bulk copies
+// (one mbarrier per stage), then its window chunks. Each block writes
+// unnormalized (m, l, o) partials per query head; m and the scores are in
+// log2 units.
 //
 // Tensor-core mapping per group (m16n8k16, M = 16 rows = 8 query heads x
 // {hi, lo} fp16 parts):
 //   q.k^T : A = q'_{h,d} = q_{h,d} * s_{g,d} split exactly into fp16 hi + lo
 //           (hi = fp16(q*s), lo = fma(q, s, -hi)); B = key codes (fields as
-//           fp16 subnormals); plus q . z_g from one more MMA per k-step with
-//           A = q and B = z (the tensor pipe has room; the issue slots do not).
+//           fp16 subnormals); plus q . z_g on CUDA cores.
 //   p.V   : A = p_t * s_t split into fp16 hi + lo; B = value codes; plus
 //           sum_t p_t z_t on CUDA cores.
+// Per window chunk the same tiles take fp16 operands straight from shared
+// memory (ldmatrix): A = q for q.k^T, A = p split into hi + lo, B = values.
 template <int D>
 struct CombineSmem {
   static constexpr int O_FLOATS = 4 * 8 * D;
@@ -320,21 +322,159 @@ struct CombineSmem {
 
 template <int D, int KB, int VB, int STAGES>
 struct DecodeSmem {
-  static constexpr int BAR_BYTES = 128;
+  static constexpr int BAR_BYTES = 256;
   static constexpr int STAGE_BYTES = 4 * STAGES * Kivi<D, KB, VB>::STAGE;
-  static constexpr int QF_BYTES = 8 * D * 4;
-  static constexpr int AREA = (STAGE_BYTES > CombineSmem<D>::BYTES + QF_BYTES) ? STAGE_BYTES
-                                                                               : CombineSmem<D>::BYTES + QF_BYTES;
+  static constexpr int WIN_ROW = 2 * D + 16;  // one fp16 window row, padded: ldmatrix rows hit distinct banks
+  static constexpr int AREA = (STAGE_BYTES > CombineSmem<D>::BYTES) ? STAGE_BYTES : CombineSmem<D>::BYTES;
   static constexpr int BYTES = BAR_BYTES + AREA;
-  static_assert(4 * STAGES * 8 <= BAR_BYTES, "barrier area");
+  static_assert((4 * STAGES + 4) * 8 <= BAR_BYTES, "barrier area");
+  static_assert(STAGES * Kivi<D, KB, VB>::STAGE >= 32 * WIN_ROW, "a warp's stages hold one window chunk");
 };
+
+// Online softmax over the 32 scores of one group or chunk (log2 domain): this
+// thread's 8 scores sc of row g give the weights p = 2^(sc - m_run). The
+// reference m_run moves only when a score exceeds it by more than 0.5, so
+// weights stay <= 2^0.5 and p * s_t still fits fp16 for any scale
+// (2^0.5 * 43669 < 65504); the rescale of the accumulators then runs rarely
+// instead of whenever some head's max grows.
+template <int NTV>
+__device__ __forceinline__ void online_softmax(const float (&sc)[8], float (&p)[8], float (&o_acc)[NTV][4], float& m_run,
+                                               float& l_run, float& vz_run) {
+  float mx = sc[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) mx = fmaxf(mx, sc[i]);
+  mx = quad_max(mx);
+  if (mx > m_run + 0.5f) {
+    const float alpha = fast_exp2(m_run - mx);
+    l_run *= alpha;
+    vz_run *= alpha;
+#pragma unroll
+    for (int i = 0; i < NTV; ++i) {
+      o_acc[i][0] *= alpha;
+      o_acc[i][1] *= alpha;
+      o_acc[i][2] *= alpha;
+      o_acc[i][3] *= alpha;
+    }
+    m_run = mx;
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) p[i] = fast_exp2(sc[i] - m_run);
+}
+
+// The fp16 window chunks c_first, c_first + 4, ... < c_end of one warp, after
+// its groups. The warp's stages are free by then and hold one chunk at a time
+// (rows padded to win_row bytes, one bulk copy per row, keys first, then the
+// values into the same rows). o_acc is first brought from code units to real
+// units so that p . V of the fp16 values adds straight into it. Kept out of
+// line: the main loop then keeps its own register allocation. Returns false
+// when a copy wait timed out (that copy may still be in flight on phase
+// `wphase` of `wbar`).
+template <int D, int VB>
+__device__ __noinline__ bool window_chunks(const uint16_t* k_res, const uint16_t* v_res, long long row_base,
+                                           int n_resid, int c_first, int c_end, uint8_t* buf, int win_row,
+                                           uint64_t* wbar, uint32_t& wphase, const uint32_t (&qs)[D / 16][2],
+                                           float p2e, float (&o_io)[D / 8][4], float& m_run, float& l_run,
+                                           float& vz_run) {
+  constexpr int KS = D / 16, NTV = D / 8;
+  const int lane = threadIdx.x & 31, tig = lane & 3;
+  const int mat = lane >> 3, mrow = lane & 7;  // ldmatrix row of this lane inside four 8x8 tiles
+  float o_acc[NTV][4];
+#pragma unroll
+  for (int nt = 0; nt < NTV; ++nt) {
+    const float om = (VB == 2 && (nt & 1)) ? kInvP8 : kInvP6;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o_acc[nt][i] = o_io[nt][i] * om;
+  }
+  uint32_t q[KS][2];
+#pragma unroll
+  for (int ks = 0; ks < KS; ++ks) q[ks][0] = qs[ks][0], q[ks][1] = qs[ks][1];
+  bool ok = true;
+  for (int c = c_first; c < c_end; c += 4) {
+    const int t0 = c * kGroup;
+    const int nv = min(kGroup, n_resid - t0);
+    const long long row0 = row_base + t0;
+    // keys of the chunk
+    __syncwarp();
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    if (lane == 0) mbar_arrive_expect_tx(wbar, nv * D * 2);
+    __syncwarp();
+    if (lane < nv) bulk_g2s(buf + lane * win_row, k_res + (row0 + lane) * D, D * 2, wbar);
+    if (!mbar_wait_bounded(wbar, wphase)) {
+      ok = false;
+      break;
+    }
+    wphase ^= 1u;
+    float sacc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) sacc[i][0] = sacc[i][1] = sacc[i][2] = sacc[i][3] = 0.0f;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+      for (int np = 0; np < 2; ++np) {
+        uint32_t kb[4];  // {b0, b1} of n-tiles 2np and 2np + 1
+        ldsm_x4(kb, buf + (16 * np + 8 * (mat >> 1) + mrow) * win_row + (16 * ks + 8 * (mat & 1)) * 2);
+        mma16816(sacc[2 * np], q[ks][0], 0u, q[ks][1], 0u, kb[0], kb[1]);
+        mma16816(sacc[2 * np + 1], q[ks][0], 0u, q[ks][1], 0u, kb[2], kb[3]);
+      }
+    // values of the chunk into the same rows; the rows past the window are zeroed
+    __syncwarp();
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    if (lane == 0) mbar_arrive_expect_tx(wbar, nv * D * 2);
+    __syncwarp();
+    if (lane < nv) {
+      bulk_g2s(buf + lane * win_row, v_res + (row0 + lane) * D, D * 2, wbar);
+    } else {
+      uint4* zr = reinterpret_cast<uint4*>(buf + lane * win_row);
+#pragma unroll
+      for (int i = 0; i < D / 8; ++i) zr[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    float sc[8], p[8];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int i = 0; i < 2; ++i) sc[2 * nt + i] = (8 * nt + 2 * tig + i < nv) ? sacc[nt][i] * p2e : -INFINITY;
+    online_softmax<NTV>(sc, p, o_acc, m_run, l_run, vz_run);
+    uint32_t phi[4], plo[4];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      const __half2 hh = __floats2half2_rn(p[2 * nt], p[2 * nt + 1]);
+      const float2 hf = __half22float2(hh);
+      phi[nt] = h2_bits(hh);
+      plo[nt] = pack_rn_f16x2(p[2 * nt] - hf.x, p[2 * nt + 1] - hf.y);
+      l_run += p[2 * nt] + p[2 * nt + 1];
+    }
+    if (!mbar_wait_bounded(wbar, wphase)) {
+      ok = false;
+      break;
+    }
+    wphase ^= 1u;
+    __syncwarp();  // the zeroed rows of the other lanes
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks) {
+      const uint32_t A0 = phi[2 * ks], A1 = plo[2 * ks], A2 = phi[2 * ks + 1], A3 = plo[2 * ks + 1];
+#pragma unroll
+      for (int np = 0; np < NTV / 2; ++np) {
+        uint32_t vb[4];  // {b0, b1} of channel tiles 2np and 2np + 1
+        ldsm_x4_trans(vb, buf + (16 * ks + 8 * (mat & 1) + mrow) * win_row + (16 * np + 8 * (mat >> 1)) * 2);
+        mma16816(o_acc[2 * np], A0, A1, A2, A3, vb[0], vb[1]);
+        mma16816(o_acc[2 * np + 1], A0, A1, A2, A3, vb[2], vb[3]);
+      }
+    }
+  }
+#pragma unroll
+  for (int nt = 0; nt < NTV; ++nt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o_io[nt][i] = o_acc[nt][i];
+  return ok;
+}
 
 template <int D, int KB, int VB, int STAGES>
 __global__ void __launch_bounds__(128, KVQ_DECODE_MIN_BLOCKS) kivi_decode_kernel(KiviDecodeArgs a) {
   using P = Kivi<D, KB, VB>;
+  using S = DecodeSmem<D, KB, VB, STAGES>;
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
-  uint8_t* area = smem + DecodeSmem<D, KB, VB, STAGES>::BAR_BYTES;
+  uint8_t* area = smem + S::BAR_BYTES;
   float* o_s = reinterpret_cast<float*>(area);  // [4 warps][8 rows][D]  (after the main loop)
   float* m_s = o_s + CombineSmem<D>::O_FLOATS;  // [4][8]
   float* l_s = m_s + 32;                        // [4][8]
@@ -344,334 +484,275 @@ __global__ void __launch_bounds__(128, KVQ_DECODE_MIN_BLOCKS) kivi_decode_kernel
   const int gq = a.q_heads / a.kv_heads;
   const long long bh = static_cast<long long>(b) * a.kv_heads + h;
 
-  if (split < a.splits_g) {
-    float m_run = -INFINITY, l_run = 0.0f, vz_run = 0.0f;
-    float o_acc[P::NTV][4];
+  // this split's share of the units: groups [g_begin, g_end), chunks [c_begin, c_end)
+  const int u_begin = split * a.units_per_split, u_end = u_begin + a.units_per_split;
+  const int n_chunks = (a.n_resid + kGroup - 1) / kGroup;
+  const int g_begin = min(a.n_groups, u_begin);
+  const int g_end = min(a.n_groups, u_end);
+  const int c_begin = min(n_chunks, max(0, u_begin - a.n_groups + kChunkUnits - 1) / kChunkUnits);
+  const int c_end = min(n_chunks, max(0, u_end - a.n_groups + kChunkUnits - 1) / kChunkUnits);
+
+  float m_run = -INFINITY, l_run = 0.0f, vz_run = 0.0f;
+  float o_acc[P::NTV][4];
+#pragma unroll
+  for (int i = 0; i < P::NTV; ++i) o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.0f;
+  // ------------------------------- grouped region -------------------------------
+  const int n_here = g_end - g_begin;
+  const int n_mine = (n_here > warp) ? (n_here - warp + 3) / 4 : 0;
+  uint64_t* bar = bars + warp * STAGES;
+  uint64_t* wbar = bars + 4 * STAGES + warp;  // window chunk copies
+  uint8_t* ring = area + warp * STAGES * P::STAGE;
+  const uint8_t* kc_g = a.k_codes + bh * a.groups_cap * static_cast<long long>(P::KC);
+  const uint8_t* km_g = a.k_meta + bh * a.groups_cap * static_cast<long long>(P::KM);
+  const uint8_t* vc_g = a.v_codes + bh * a.groups_cap * static_cast<long long>(P::VC);
+  const uint8_t* vm_g = a.v_meta + bh * a.groups_cap * static_cast<long long>(P::VM);
+
+  if (lane == 0) {
+#pragma unroll
+    for (int s = 0; s < STAGES; ++s) mbar_init(&bar[s], 1);
+    mbar_init(wbar, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+
+  auto issue = [&](int j) {
+    const long long grp = g_begin + warp + 4 * j;
+    uint8_t* dst = ring + (j % STAGES) * P::STAGE;
+    uint64_t* bb = &bar[j % STAGES];
+    mbar_arrive_expect_tx(bb, P::STAGE);
+    bulk_g2s(dst, kc_g + grp * P::KC, P::KC, bb);
+    bulk_g2s(dst + P::KC, km_g + grp * P::KM, P::KM, bb);
+    bulk_g2s(dst + P::KC + P::KM, vc_g + grp * P::VC, P::VC, bb);
+    bulk_g2s(dst + P::KC + P::KM + P::VC, vm_g + grp * P::VM, P::VM, bb);
+  };
+  if (lane == 0) {
+    for (int j = 0; j < STAGES && j < n_mine; ++j) issue(j);
+  }
+
+  // Query fragments of row g (query head h*gq + g), scaled by 2^-e so that
+  // |q| < 1 and q * s stays inside the fp16 range.
+  const bool row_ok = g < gq;
+  const __half* qrow = reinterpret_cast<const __half*>(a.q) +
+                       (static_cast<long long>(b) * a.q_heads + h * gq + (row_ok ? g : 0)) * D;
+  float2 qv[P::KS][2];
+  float qmax = 0.0f;
+#pragma unroll
+  for (int ks = 0; ks < P::KS; ++ks)
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const __half2 v = row_ok ? *reinterpret_cast<const __half2*>(qrow + 16 * ks + 8 * j + 2 * tig)
+                               : __float2half2_rn(0.0f);
+      qv[ks][j] = __half22float2(v);
+      qmax = fmaxf(qmax, fmaxf(fabsf(qv[ks][j].x), fabsf(qv[ks][j].y)));
+    }
+  qmax = quad_max(qmax);
+  int e = 0;
+  if (qmax > 0.0f) frexpf(qmax, &e);
+  const float qscale = ldexpf(1.0f, -e);
+  uint32_t qs[P::KS][2];
+#pragma unroll
+  for (int ks = 0; ks < P::KS; ++ks)
+#pragma unroll
+    for (int j = 0; j < 2; ++j) qs[ks][j] = pack_rn_f16x2(qv[ks][j].x * qscale, qv[ks][j].y * qscale);
+  const float p2e = ldexpf(1.0f, e) * a.scale_log2;
+  const float mult6 = kInvP6 * p2e, mult8 = kInvP8 * p2e;
+
+  // q . k_hat of the 32 tokens of the group in stage `sp`: 8 scores (log2
+  // units) of this thread's row, tokens 8*nt + 2*tig + {0, 1}.
+  auto qk_scores = [&](const uint8_t* sp, float (&sc)[8]) {
+    const uint4* kcw = reinterpret_cast<const uint4*>(sp);
+    const uint4* kmr = reinterpret_cast<const uint4*>(sp + P::KC);
+    uint32_t kw[P::KW];
+#pragma unroll
+    for (int c = 0; c < P::KW / 4; ++c) {
+      const uint4 x = kcw[c * 32 + lane];
+      kw[4 * c] = x.x;
+      kw[4 * c + 1] = x.y;
+      kw[4 * c + 2] = x.z;
+      kw[4 * c + 3] = x.w;
+    }
+    float sacc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) sacc[i][0] = sacc[i][1] = sacc[i][2] = sacc[i][3] = 0.0f;
+    // q . z: this lane's four channels of head g on the FMA pipe (the tensor pipe is the
+    // busier one here); a quad sum after the loop completes the dot product.
+    float bsum = 0.0f;
+#pragma unroll
+    for (int ks = 0; ks < P::KS; ++ks) {
+      const uint4 md = kmr[ks * 4 + tig];  // {s(d0,d0+1), s(d0+8,d0+9), z(d0,d0+1), z(d0+8,d0+9)}
+      const __half2 q0 = bits_h2(qs[ks][0]), q1 = bits_h2(qs[ks][1]);
+      const __half2 hi0 = __hmul2(q0, bits_h2(md.x));
+      const __half2 lo0 = __hfma2(q0, bits_h2(md.x), __hneg2(hi0));
+      const __half2 hi1 = __hmul2(q1, bits_h2(md.y));
+      const __half2 lo1 = __hfma2(q1, bits_h2(md.y), __hneg2(hi1));
+      const uint32_t A0 = h2_bits(hi0), A1 = h2_bits(lo0), A2 = h2_bits(hi1), A3 = h2_bits(lo1);
+      bsum = dot2_f16_f32(qs[ks][0], md.z, dot2_f16_f32(qs[ks][1], md.w, bsum));
+      if constexpr (KB == 2) {
+        const uint32_t w = kw[ks];
+        const uint32_t l6 = w << 6, l2 = w << 2, r2 = w >> 2, r6 = w >> 6;
+        mma16816(sacc[0], A0, A1, A2, A3, l6 & kMaskP6, r2 & kMaskP6);
+        mma16816(sacc[1], A0, A1, A2, A3, l6 & kMaskP8, r2 & kMaskP8);
+        mma16816(sacc[2], A0, A1, A2, A3, l2 & kMaskP6, r6 & kMaskP6);
+        mma16816(sacc[3], A0, A1, A2, A3, l2 & kMaskP8, r6 & kMaskP8);
+      } else {
+        const uint32_t w0 = kw[2 * ks], w1 = kw[2 * ks + 1];
+        mma16816(sacc[0], A0, A1, A2, A3, (w0 << 6) & kMask4, (w1 << 6) & kMask4);
+        mma16816(sacc[1], A0, A1, A2, A3, (w0 << 2) & kMask4, (w1 << 2) & kMask4);
+        mma16816(sacc[2], A0, A1, A2, A3, (w0 >> 2) & kMask4, (w1 >> 2) & kMask4);
+        mma16816(sacc[3], A0, A1, A2, A3, (w0 >> 6) & kMask4, (w1 >> 6) & kMask4);
+      }
+    }
+    const float bias = quad_sum(bsum) * p2e;
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      const float mult = (KB == 2 && (nt & 1)) ? mult8 : mult6;
+      sc[2 * nt] = fmaf(sacc[nt][0] + sacc[nt][2], mult, bias);
+      sc[2 * nt + 1] = fmaf(sacc[nt][1] + sacc[nt][3], mult, bias);
+    }
+  };
+
+  // Software pipeline: iteration j runs the softmax and p . V of group j
+  // and, in the same straight-line block, q . k^T of group j + 1, so that
+  // each warp keeps both the tensor pipe and the ALUs busy.
+  int j = 0;
+  bool timed_out = false;
+  float sc[8];
+  if (n_mine > 0) {
+    if (mbar_wait_bounded(&bar[0], 0))
+      qk_scores(ring, sc);
+    else
+      timed_out = true;
+  }
+  for (; !timed_out && j < n_mine; ++j) {
+    const int s = j % STAGES;
+    const uint8_t* sp = ring + s * P::STAGE;
+    // the next group's stage (this one again past the end: its scores are discarded)
+    const int jn = (j + 1 < n_mine) ? j + 1 : j;
+    if (jn != j && !mbar_wait_bounded(&bar[jn % STAGES], (jn / STAGES) & 1)) {
+      timed_out = true;
+      break;
+    }
+    const uint8_t* spn = ring + (jn % STAGES) * P::STAGE;
+    const uint4* vcw = reinterpret_cast<const uint4*>(sp + P::KC + P::KM);
+    const uint4* vmr = reinterpret_cast<const uint4*>(sp + P::KC + P::KM + P::VC);
+
+    float p[8];
+    online_softmax<P::NTV>(sc, p, o_acc, m_run, l_run, vz_run);
+
+    // ---- p' = p * s_t as fp16 hi + lo; the zero-point term on CUDA cores ----
+    const uint4 vs = vmr[tig], vz = vmr[4 + tig];
+    const uint32_t vsw[4] = {vs.x, vs.y, vs.z, vs.w};
+    const uint32_t vzw[4] = {vz.x, vz.y, vz.z, vz.w};
+    uint32_t phi[4], plo[4];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      const float2 sf = __half22float2(bits_h2(vsw[nt]));
+      const float2 zf = __half22float2(bits_h2(vzw[nt]));
+      const float pp0 = p[2 * nt] * sf.x, pp1 = p[2 * nt + 1] * sf.y;
+      const __half2 hh = __floats2half2_rn(pp0, pp1);
+      const float2 hf = __half22float2(hh);
+      phi[nt] = h2_bits(hh);
+      plo[nt] = pack_rn_f16x2(pp0 - hf.x, pp1 - hf.y);
+      l_run += p[2 * nt] + p[2 * nt + 1];
+      vz_run = fmaf(p[2 * nt], zf.x, fmaf(p[2 * nt + 1], zf.y, vz_run));
+    }
+
+    // ---- q . k^T of group j + 1 (independent of what follows) ----
+    qk_scores(spn, sc);
+
+    // ---- o += p' . codes (group j) ----
+    uint32_t vw[P::VW];
+#pragma unroll
+    for (int c = 0; c < P::VW / 4; ++c) {
+      const uint4 x = vcw[c * 32 + lane];
+      vw[4 * c] = x.x;
+      vw[4 * c + 1] = x.y;
+      vw[4 * c + 2] = x.z;
+      vw[4 * c + 3] = x.w;
+    }
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks) {
+      const uint32_t A0 = phi[2 * ks], A1 = plo[2 * ks], A2 = phi[2 * ks + 1], A3 = plo[2 * ks + 1];
+#pragma unroll
+      for (int q = 0; q < P::NQ; ++q) {
+        if constexpr (VB == 2) {
+          const uint32_t w = vw[ks * P::NQ + q];
+          const uint32_t l6 = w << 6, l2 = w << 2, r2 = w >> 2, r6 = w >> 6;
+          mma16816(o_acc[4 * q + 0], A0, A1, A2, A3, l6 & kMaskP6, r2 & kMaskP6);
+          mma16816(o_acc[4 * q + 1], A0, A1, A2, A3, l6 & kMaskP8, r2 & kMaskP8);
+          mma16816(o_acc[4 * q + 2], A0, A1, A2, A3, l2 & kMaskP6, r6 & kMaskP6);
+          mma16816(o_acc[4 * q + 3], A0, A1, A2, A3, l2 & kMaskP8, r6 & kMaskP8);
+        } else {
+          const uint32_t w0 = vw[(2 * ks) * P::NQ + q], w1 = vw[(2 * ks + 1) * P::NQ + q];
+          mma16816(o_acc[4 * q + 0], A0, A1, A2, A3, (w0 << 6) & kMask4, (w1 << 6) & kMask4);
+          mma16816(o_acc[4 * q + 1], A0, A1, A2, A3, (w0 << 2) & kMask4, (w1 << 2) & kMask4);
+          mma16816(o_acc[4 * q + 2], A0, A1, A2, A3, (w0 >> 2) & kMask4, (w1 >> 2) & kMask4);
+          mma16816(o_acc[4 * q + 3], A0, A1, A2, A3, (w0 >> 6) & kMask4, (w1 >> 6) & kMask4);
+        }
+      }
+    }
+
+    // release stage j and refill it with the group STAGES ahead
+    __syncwarp();
+    if (lane == 0 && j + STAGES < n_mine) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      issue(j + STAGES);
+    }
+  }
+
+  // ------------------------ fp16 window, 32-token chunks ------------------------
+  constexpr bool kTwoFields = (VB == 2);
+  bool real_units = false, win_pending = false;
+  uint32_t wphase = 0;
+  if (!timed_out && c_begin + warp < c_end) {
+    real_units = true;
+    // the call takes copies: a variable whose address escapes would live in
+    // local memory for the whole kernel, main loop included
+    float o_io[P::NTV][4], st[3] = {m_run, l_run, vz_run};
+    uint32_t q_io[P::KS][2];
+#pragma unroll
+    for (int i = 0; i < P::NTV; ++i) o_io[i][0] = o_acc[i][0], o_io[i][1] = o_acc[i][1], o_io[i][2] = o_acc[i][2], o_io[i][3] = o_acc[i][3];
+#pragma unroll
+    for (int ks = 0; ks < P::KS; ++ks) q_io[ks][0] = qs[ks][0], q_io[ks][1] = qs[ks][1];
+    uint32_t ph = 0;
+    const bool ok = window_chunks<D, VB>(a.k_res, a.v_res, bh * a.res_cap, a.n_resid, c_begin + warp, c_end, ring,
+                                         S::WIN_ROW, wbar, ph, q_io, p2e, o_io, st[0], st[1], st[2]);
+#pragma unroll
+    for (int i = 0; i < P::NTV; ++i) o_acc[i][0] = o_io[i][0], o_acc[i][1] = o_io[i][1], o_acc[i][2] = o_io[i][2], o_acc[i][3] = o_io[i][3];
+    m_run = st[0];
+    l_run = st[1];
+    vz_run = st[2];
+    wphase = ph;
+    if (!ok) {
+      timed_out = true;
+      win_pending = true;
+    }
+  }
+
+  if (timed_out) {
+    if (lane == 0) report_timeout(a.status);
+    // let the copies already in flight land before the stages are reused
+    for (int jj = j; jj < n_mine && jj < j + STAGES; ++jj) (void)mbar_wait_bounded(&bar[jj % STAGES], (jj / STAGES) & 1);
+    if (win_pending) (void)mbar_wait_bounded(wbar, wphase);
+    m_run = -INFINITY;
+    l_run = 0.0f;
+    vz_run = 0.0f;
 #pragma unroll
     for (int i = 0; i < P::NTV; ++i) o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.0f;
-    // ------------------------------- grouped region -------------------------------
-    const int g_begin = split * a.groups_per_split;
-    const int g_end = min(a.n_groups, g_begin + a.groups_per_split);
-    const int n_here = g_end - g_begin;
-    const int n_mine = (n_here > warp) ? (n_here - warp + 3) / 4 : 0;
-    uint64_t* bar = bars + warp * STAGES;
-    uint8_t* ring = area + warp * STAGES * P::STAGE;
-    const uint8_t* kc_g = a.k_codes + bh * a.groups_cap * static_cast<long long>(P::KC);
-    const uint8_t* km_g = a.k_meta + bh * a.groups_cap * static_cast<long long>(P::KM);
-    const uint8_t* vc_g = a.v_codes + bh * a.groups_cap * static_cast<long long>(P::VC);
-    const uint8_t* vm_g = a.v_meta + bh * a.groups_cap * static_cast<long long>(P::VM);
-
-    if (lane == 0) {
+  }
+  l_run = quad_sum(l_run);
+  vz_run = quad_sum(vz_run);
+  __syncthreads();  // every warp is done with its stages; the area is reused below
 #pragma unroll
-      for (int s = 0; s < STAGES; ++s) mbar_init(&bar[s], 1);
-      fence_mbar_init();
-    }
-    __syncwarp();
-
-    auto issue = [&](int j) {
-      const long long grp = g_begin + warp + 4 * j;
-      uint8_t* dst = ring + (j % STAGES) * P::STAGE;
-      uint64_t* bb = &bar[j % STAGES];
-      mbar_arrive_expect_tx(bb, P::STAGE);
-      bulk_g2s(dst, kc_g + grp * P::KC, P::KC, bb);
-      bulk_g2s(dst + P::KC, km_g + grp * P::KM, P::KM, bb);
-      bulk_g2s(dst + P::KC + P::KM, vc_g + grp * P::VC, P::VC, bb);
-      bulk_g2s(dst + P::KC + P::KM + P::VC, vm_g + grp * P::VM, P::VM, bb);
-    };
-    if (lane == 0) {
-      for (int j = 0; j < STAGES && j < n_mine; ++j) issue(j);
-    }
-
-    // Query fragments of row g (query head h*gq + g), scaled by 2^-e so that
-    // |q| < 1 and q * s stays inside the fp16 range.
-    const bool row_ok = g < gq;
-    const __half* qrow = reinterpret_cast<const __half*>(a.q) +
-                         (static_cast<long long>(b) * a.q_heads + h * gq + (row_ok ? g : 0)) * D;
-    float2 qv[P::KS][2];
-    float qmax = 0.0f;
-#pragma unroll
-    for (int ks = 0; ks < P::KS; ++ks)
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const __half2 v = row_ok ? *reinterpret_cast<const __half2*>(qrow + 16 * ks + 8 * j + 2 * tig)
-                                 : __float2half2_rn(0.0f);
-        qv[ks][j] = __half22float2(v);
-        qmax = fmaxf(qmax, fmaxf(fabsf(qv[ks][j].x), fabsf(qv[ks][j].y)));
-      }
-    qmax = quad_max(qmax);
-    int e = 0;
-    if (qmax > 0.0f) frexpf(qmax, &e);
-    const float qscale = ldexpf(1.0f, -e);
-    uint32_t qs[P::KS][2];
-#pragma unroll
-    for (int ks = 0; ks < P::KS; ++ks)
-#pragma unroll
-      for (int j = 0; j < 2; ++j) qs[ks][j] = pack_rn_f16x2(qv[ks][j].x * qscale, qv[ks][j].y * qscale);
-    const float p2e = ldexpf(1.0f, e) * a.scale_log2;
-    const float mult6 = kInvP6 * p2e, mult8 = kInvP8 * p2e;
-
-    // q . k_hat of the 32 tokens of the group in stage `sp`: 8 scores (log2
-    // units) of this thread's row, tokens 8*nt + 2*tig + {0, 1}.
-    auto qk_scores = [&](const uint8_t* sp, float (&sc)[8]) {
-      const uint4* kcw = reinterpret_cast<const uint4*>(sp);
-      const uint4* kmr = reinterpret_cast<const uint4*>(sp + P::KC);
-      uint32_t kw[P::KW];
-#pragma unroll
-      for (int c = 0; c < P::KW / 4; ++c) {
-        const uint4 x = kcw[c * 32 + lane];
-        kw[4 * c] = x.x;
-        kw[4 * c + 1] = x.y;
-        kw[4 * c + 2] = x.z;
-        kw[4 * c + 3] = x.w;
-      }
-      float sacc[4][4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) sacc[i][0] = sacc[i][1] = sacc[i][2] = sacc[i][3] = 0.0f;
-      // q . z: this lane's four channels of head g on the FMA pipe (the tensor pipe is the
-      // busier one here); a quad sum after the loop completes the dot product.
-      float bsum = 0.0f;
-#pragma unroll
-      for (int ks = 0; ks < P::KS; ++ks) {
-        const uint4 md = kmr[ks * 4 + tig];  // {s(d0,d0+1), s(d0+8,d0+9), z(d0,d0+1), z(d0+8,d0+9)}
-        const __half2 q0 = bits_h2(qs[ks][0]), q1 = bits_h2(qs[ks][1]);
-        const __half2 hi0 = __hmul2(q0, bits_h2(md.x));
-        const __half2 lo0 = __hfma2(q0, bits_h2(md.x), __hneg2(hi0));
-        const __half2 hi1 = __hmul2(q1, bits_h2(md.y));
-        const __half2 lo1 = __hfma2(q1, bits_h2(md.y), __hneg2(hi1));
-        const uint32_t A0 = h2_bits(hi0), A1 = h2_bits(lo0), A2 = h2_bits(hi1), A3 = h2_bits(lo1);
-        bsum = dot2_f16_f32(qs[ks][0], md.z, dot2_f16_f32(qs[ks][1], md.w, bsum));
-        if constexpr (KB == 2) {
-          const uint32_t w = kw[ks];
-          const uint32_t l6 = w << 6, l2 = w << 2, r2 = w >> 2, r6 = w >> 6;
-          mma16816(sacc[0], A0, A1, A2, A3, l6 & kMaskP6, r2 & kMaskP6);
-          mma16816(sacc[1], A0, A1, A2, A3, l6 & kMaskP8, r2 & kMaskP8);
-          mma16816(sacc[2], A0, A1, A2, A3, l2 & kMaskP6, r6 & kMaskP6);
-          mma16816(sacc[3], A0, A1, A2, A3, l2 & kMaskP8, r6 & kMaskP8);
-        } else {
-          const uint32_t w0 = kw[2 * ks], w1 = kw[2 * ks + 1];
-          mma16816(sacc[0], A0, A1, A2, A3, (w0 << 6) & kMask4, (w1 << 6) & kMask4);
-          mma16816(sacc[1], A0, A1, A2, A3, (w0 << 2) & kMask4, (w1 << 2) & kMask4);
-          mma16816(sacc[2], A0, A1, A2, A3, (w0 >> 2) & kMask4, (w1 >> 2) & kMask4);
-          mma16816(sacc[3], A0, A1, A2, A3, (w0 >> 6) & kMask4, (w1 >> 6) & kMask4);
-        }
-      }
-      const float bias = quad_sum(bsum) * p2e;
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-        const float mult = (KB == 2 && (nt & 1)) ? mult8 : mult6;
-        sc[2 * nt] = fmaf(sacc[nt][0] + sacc[nt][2], mult, bias);
-        sc[2 * nt + 1] = fmaf(sacc[nt][1] + sacc[nt][3], mult, bias);
-      }
-    };
-
-    // Software pipeline: iteration j runs the softmax and p . V of group j
-    // and, in the same straight-line block, q . k^T of group j + 1, so that
-    // each warp keeps both the tensor pipe and the ALUs busy.
-    int j = 0;
-    bool timed_out = false;
-    float sc[8];
-    if (n_mine > 0) {
-      if (mbar_wait_bounded(&bar[0], 0))
-        qk_scores(ring, sc);
-      else
-        timed_out = true;
-    }
-    for (; !timed_out && j < n_mine; ++j) {
-      const int s = j % STAGES;
-      const uint8_t* sp = ring + s * P::STAGE;
-      // the next group's stage (this one again past the end: its scores are discarded)
-      const int jn = (j + 1 < n_mine) ? j + 1 : j;
-      if (jn != j && !mbar_wait_bounded(&bar[jn % STAGES], (jn / STAGES) & 1)) {
-        timed_out = true;
-        break;
-      }
-      const uint8_t* spn = ring + (jn % STAGES) * P::STAGE;
-      const uint4* vcw = reinterpret_cast<const uint4*>(sp + P::KC + P::KM);
-      const uint4* vmr = reinterpret_cast<const uint4*>(sp + P::KC + P::KM + P::VC);
-
-      // ---- online softmax of group j (log2 domain) ----
-      float mx = sc[0];
-#pragma unroll
-      for (int i = 1; i < 8; ++i) mx = fmaxf(mx, sc[i]);
-      mx = quad_max(mx);
-      // The reference m_run moves only when a score exceeds it by more than
-      // 0.5 (log2 units), so weights stay <= 2^0.5 and p * s_t still fits fp16
-      // for any scale (2^0.5 * 43669 < 65504); the rescale of the 64
-      // accumulators then runs rarely instead of whenever some head's max grows.
-      if (mx > m_run + 0.5f) {
-        const float alpha = fast_exp2(m_run - mx);
-        l_run *= alpha;
-        vz_run *= alpha;
-#pragma unroll
-        for (int i = 0; i < P::NTV; ++i) {
-          o_acc[i][0] *= alpha;
-          o_acc[i][1] *= alpha;
-          o_acc[i][2] *= alpha;
-          o_acc[i][3] *= alpha;
-        }
-        m_run = mx;
-      }
-      float p[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) p[i] = fast_exp2(sc[i] - m_run);
-
-      // ---- p' = p * s_t as fp16 hi + lo; the zero-point term on CUDA cores ----
-      const uint4 vs = vmr[tig], vz = vmr[4 + tig];
-      const uint32_t vsw[4] = {vs.x, vs.y, vs.z, vs.w};
-      const uint32_t vzw[4] = {vz.x, vz.y, vz.z, vz.w};
-      uint32_t phi[4], plo[4];
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-        const float2 sf = __half22float2(bits_h2(vsw[nt]));
-        const float2 zf = __half22float2(bits_h2(vzw[nt]));
-        const float pp0 = p[2 * nt] * sf.x, pp1 = p[2 * nt + 1] * sf.y;
-        const __half2 hh = __floats2half2_rn(pp0, pp1);
-        const float2 hf = __half22float2(hh);
-        phi[nt] = h2_bits(hh);
-        plo[nt] = pack_rn_f16x2(pp0 - hf.x, pp1 - hf.y);
-        l_run += p[2 * nt] + p[2 * nt + 1];
-        vz_run = fmaf(p[2 * nt], zf.x, fmaf(p[2 * nt + 1], zf.y, vz_run));
-      }
-
-      // ---- q . k^T of group j + 1 (independent of what follows) ----
-      qk_scores(spn, sc);
-
-      // ---- o += p' . codes (group j) ----
-      uint32_t vw[P::VW];
-#pragma unroll
-      for (int c = 0; c < P::VW / 4; ++c) {
-        const uint4 x = vcw[c * 32 + lane];
-        vw[4 * c] = x.x;
-        vw[4 * c + 1] = x.y;
-        vw[4 * c + 2] = x.z;
-        vw[4 * c + 3] = x.w;
-      }
-#pragma unroll
-      for (int ks = 0; ks < 2; ++ks) {
-        const uint32_t A0 = phi[2 * ks], A1 = plo[2 * ks], A2 = phi[2 * ks + 1], A3 = plo[2 * ks + 1];
-#pragma unroll
-        for (int q = 0; q < P::NQ; ++q) {
-          if constexpr (VB == 2) {
-            const uint32_t w = vw[ks * P::NQ + q];
-            const uint32_t l6 = w << 6, l2 = w << 2, r2 = w >> 2, r6 = w >> 6;
-            mma16816(o_acc[4 * q + 0], A0, A1, A2, A3, l6 & kMaskP6, r2 & kMaskP6);
-            mma16816(o_acc[4 * q + 1], A0, A1, A2, A3, l6 & kMaskP8, r2 & kMaskP8);
-            mma16816(o_acc[4 * q + 2], A0, A1, A2, A3, l2 & kMaskP6, r6 & kMaskP6);
-            mma16816(o_acc[4 * q + 3], A0, A1, A2, A3, l2 & kMaskP8, r6 & kMaskP8);
-          } else {
-            const uint32_t w0 = vw[(2 * ks) * P::NQ + q], w1 = vw[(2 * ks + 1) * P::NQ + q];
-            mma16816(o_acc[4 * q + 0], A0, A1, A2, A3, (w0 << 6) & kMask4, (w1 << 6) & kMask4);
-            mma16816(o_acc[4 * q + 1], A0, A1, A2, A3, (w0 << 2) & kMask4, (w1 << 2) & kMask4);
-            mma16816(o_acc[4 * q + 2], A0, A1, A2, A3, (w0 >> 2) & kMask4, (w1 >> 2) & kMask4);
-            mma16816(o_acc[4 * q + 3], A0, A1, A2, A3, (w0 >> 6) & kMask4, (w1 >> 6) & kMask4);
-          }
-        }
-      }
-
-      // release stage j and refill it with the group STAGES ahead
-      __syncwarp();
-      if (lane == 0 && j + STAGES < n_mine) {
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        issue(j + STAGES);
-      }
-    }
-    if (timed_out) {
-      if (lane == 0) report_timeout(a.status);
-      // let the copies already in flight land before the stages are reused
-      for (int jj = j; jj < n_mine && jj < j + STAGES; ++jj) (void)mbar_wait_bounded(&bar[jj % STAGES], (jj / STAGES) & 1);
-      m_run = -INFINITY;
-      l_run = 0.0f;
-      vz_run = 0.0f;
-#pragma unroll
-      for (int i = 0; i < P::NTV; ++i) o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.0f;
-    }
-    l_run = quad_sum(l_run);
-    vz_run = quad_sum(vz_run);
-    __syncthreads();  // every warp is done with its stages; the area is reused below
-    constexpr bool kTwoFields = (VB == 2);
-#pragma unroll
-    for (int nt = 0; nt < P::NTV; ++nt) {
-      const float om = (kTwoFields && (nt & 1)) ? kInvP8 : kInvP6;
-      const int c = 8 * nt + 2 * tig;
-      o_s[(warp * 8 + g) * D + c] = fmaf(o_acc[nt][0] + o_acc[nt][2], om, vz_run);
-      o_s[(warp * 8 + g) * D + c + 1] = fmaf(o_acc[nt][1] + o_acc[nt][3], om, vz_run);
-    }
-    if (tig == 0) {
-      m_s[warp * 8 + g] = m_run;
-      l_s[warp * 8 + g] = l_run;
-    }
-  } else {
-    float rw_m[kMaxGqa], rw_l[kMaxGqa], rw_o[kMaxGqa][D / 32];
-    // --------------------- fp16 window (CUDA cores, fp32) ---------------------
-    float* qf = reinterpret_cast<float*>(area + CombineSmem<D>::BYTES);  // [8][D]
-    for (int i = tid; i < gq * D; i += 128)
-      qf[i] = __half2float(reinterpret_cast<const __half*>(a.q)[(static_cast<long long>(b) * a.q_heads + h * gq) * D + i]);
-    __syncthreads();
-    const int t = warp * 32 + lane;
-    const bool valid = t < a.n_resid;
-    float s[kMaxGqa];
-#pragma unroll
-    for (int r = 0; r < kMaxGqa; ++r) s[r] = 0.0f;
-    if (valid) {
-      const __half* krow = reinterpret_cast<const __half*>(a.k_res) + (bh * a.res_cap + t) * D;
-      for (int c = 0; c < D; c += 8) {
-        const uint4 kv = *reinterpret_cast<const uint4*>(krow + c);
-        const uint32_t kwd[4] = {kv.x, kv.y, kv.z, kv.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 kf = __half22float2(bits_h2(kwd[i]));
-#pragma unroll
-          for (int r = 0; r < kMaxGqa; ++r) {
-            if (r < gq) {
-              s[r] = fmaf(qf[r * D + c + 2 * i], kf.x, s[r]);
-              s[r] = fmaf(qf[r * D + c + 2 * i + 1], kf.y, s[r]);
-            }
-          }
-        }
-      }
-    }
-    float pr[kMaxGqa];
-#pragma unroll
-    for (int r = 0; r < kMaxGqa; ++r) {
-      const float sv = valid ? s[r] * a.scale_log2 : -INFINITY;
-      rw_m[r] = warp_max(sv);
-      pr[r] = (rw_m[r] == -INFINITY) ? 0.0f : fast_exp2(sv - rw_m[r]);
-      rw_l[r] = warp_sum(pr[r]);
-#pragma unroll
-      for (int i = 0; i < D / 32; ++i) rw_o[r][i] = 0.0f;
-    }
-    const int nvalid = min(32, a.n_resid - warp * 32);
-    for (int tt = 0; tt < nvalid; ++tt) {
-      const __half* vrow = reinterpret_cast<const __half*>(a.v_res) + (bh * a.res_cap + warp * 32 + tt) * D + (D / 32) * lane;
-      float vf[D / 32];
-      if constexpr (D == 128) {
-        const uint2 vv = *reinterpret_cast<const uint2*>(vrow);
-        const float2 f0 = __half22float2(bits_h2(vv.x)), f1 = __half22float2(bits_h2(vv.y));
-        vf[0] = f0.x;
-        vf[1] = f0.y;
-        vf[2] = f1.x;
-        vf[3] = f1.y;
-      } else {
-        const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(vrow));
-        vf[0] = f0.x;
-        vf[1] = f0.y;
-      }
-#pragma unroll
-      for (int r = 0; r < kMaxGqa; ++r) {
-        const float pt = __shfl_sync(0xffffffffu, pr[r], tt);
-#pragma unroll
-        for (int i = 0; i < D / 32; ++i) rw_o[r][i] = fmaf(pt, vf[i], rw_o[r][i]);
-      }
-    }
-#pragma unroll
-    for (int r = 0; r < kMaxGqa; ++r) {
-#pragma unroll
-      for (int i = 0; i < D / 32; ++i) o_s[(warp * 8 + r) * D + (D / 32) * lane + i] = rw_o[r][i];
-      if (lane == 0) {
-        m_s[warp * 8 + r] = rw_m[r];
-        l_s[warp * 8 + r] = rw_l[r];
-      }
-    }
+  for (int nt = 0; nt < P::NTV; ++nt) {
+    const float om = real_units ? 1.0f : ((kTwoFields && (nt & 1)) ? kInvP8 : kInvP6);
+    const int c = 8 * nt + 2 * tig;
+    o_s[(warp * 8 + g) * D + c] = fmaf(o_acc[nt][0] + o_acc[nt][2], om, vz_run);
+    o_s[(warp * 8 + g) * D + c + 1] = fmaf(o_acc[nt][1] + o_acc[nt][3], om, vz_run);
+  }
+  if (tig == 0) {
+    m_s[warp * 8 + g] = m_run;
+    l_s[warp * 8 + g] = l_run;
   }
 
   __syncthreads();

@@ -15,6 +15,7 @@ constexpr uint32_t kStatusTimeout = 1u;  // status bit: a device wait gave up
 constexpr int kWsHeader = 256;           // bytes reserved at the start of a decode workspace
 constexpr int kMaxSplits = 64;           // split-K partials per (batch row, query head)
 constexpr int kMaxGqa = 8;               // query heads per kv head handled by one MMA tile
+constexpr int kChunkUnits = 8;           // decode work units (groups) one 32-token window chunk is charged
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per wait
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -86,6 +87,26 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
       "{%0,%1,%2,%3};\n"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Four 8x8 fp16 tiles from shared memory into mma.sync operand registers.
+// Lane l gives the address of row l % 8 of tile l / 8 (16 contiguous bytes);
+// register i then holds tile i in fragment order: lane (g, t) receives row g,
+// columns 2t and 2t+1 (ldsm_x4), or with the tile transposed, rows 2t and
+// 2t+1 of column g (ldsm_x4_trans).
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* row) {
+  const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(row));
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(a)
+               : "memory");
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], const void* row) {
+  const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(row));
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(a)
+               : "memory");
 }
 
 // c + a.lo * b.lo + a.hi * b.hi with fp16 halves and an fp32 accumulator

@@ -49,9 +49,11 @@ struct KiviDecodeArgs {
   const uint16_t* q;
   int batch, kv_heads, q_heads, head_dim, k_bits, v_bits, groups_cap, res_cap;
   int n_groups, n_resid;
-  int splits_g;           // thread-block splits over the grouped region
-  int groups_per_split;
-  int splits_total;       // splits_g (+1 when the window is not empty)
+  // Work units of one (batch row, kv head): its n_groups groups, then its
+  // ceil(n_resid / 32) window chunks of kChunkUnits units each; split x takes
+  // units [x * units_per_split, (x + 1) * units_per_split).
+  int units_per_split;
+  int splits_total;
   float scale_log2;       // softmax scale * log2(e)
   float* part_o;          // [B, Hq, splits_total, D]
   float* part_ml;         // [B, Hq, splits_total, 2]
