@@ -146,24 +146,63 @@ int choose_splits(int units, int pairs, int max_splits, int blocks_per_sm, int e
   return ceil_div(units, per);
 }
 
-// The decode grid of a KIVI cache. The work of one (batch row, kv head) is a
-// range of units: its groups, then its fp16 window cut into 32-token chunks of
-// kChunkUnits units each (a chunk is one warp's work, about two groups' time
-// for the whole block); the range is cut evenly into `splits` blocks.
+// The decode grid of a KIVI cache. The work of one (batch row, kv head) pair
+// is a range of units: its groups, then its fp16 window cut into 32-token
+// chunks of kChunkUnits units each (a chunk is one warp's work, about two
+// groups of time for the whole block). The grid holds at most as many blocks
+// as the GPU keeps resident, all with the same number of units, in one of two
+// cuts, whichever gives the smaller block:
+//  * pair-aligned: every pair in k equal slices (no block crosses a pair), used
+//    when the pairs fill the resident slots well;
+//  * stream-K: the ranges of all pairs, one after the other, in equal slices; a
+//    block then writes one partial per pair its slice touches and pays for
+//    each extra pair about kSegmentUnits units (its pipeline drains and
+//    restarts, and it may merge the pair it leaves).
 struct DecodePlan {
   int n_groups;
-  int splits;
-  int units_per_split;
+  int units_per_pair;
+  int pair_stride;
+  int units_per_block;
+  int n_blocks;
+  int part_stride;  // the most blocks one pair can touch
 };
+
+constexpr int kSegmentUnits = 16;
 
 DecodePlan plan_kivi_decode(const kivi_cache* cache) {
   const kivi_config& cf = cache->cfg;
   DecodePlan p{};
   p.n_groups = cache->n_grouped / kGroup;
-  const int units = p.n_groups + kvq::kChunkUnits * ceil_div(cache->n_resid, kGroup);
-  p.splits = choose_splits(units, cf.batch * cf.kv_heads, kMaxSplits,
-                           kvq::kivi_decode_blocks_per_sm(cf.head_dim, cf.k_bits, cf.v_bits), 0);
-  p.units_per_split = ceil_div(units, p.splits);
+  const int U = p.n_groups + kvq::kChunkUnits * ceil_div(cache->n_resid, kGroup);
+  p.units_per_pair = U;
+  const long long pairs = static_cast<long long>(cf.batch) * cf.kv_heads;
+  const long long slots = static_cast<long long>(kvq::device_sm_count()) *
+                          std::max(1, kvq::kivi_decode_blocks_per_sm(cf.head_dim, cf.k_bits, cf.v_bits));
+  // stream-K slices
+  long long per_s = (pairs * U + slots - 1) / slots;
+  per_s = std::max<long long>(per_s, kMinUnitsPerSplit);
+  per_s = std::max<long long>(per_s, ceil_div(U, kMaxSplits - 1));  // <= kMaxSplits partials per pair
+  const long long extra_pairs = (per_s - 1) / U + 1;                 // pairs a slice can touch, minus one
+  const long long cost_s = per_s + kSegmentUnits * extra_pairs;
+  // pair-aligned slices
+  if (pairs <= slots) {
+    int k = static_cast<int>(slots / pairs);
+    k = std::min(k, std::max(1, ceil_div(U, kMinUnitsPerSplit)));
+    k = std::min(k, kMaxSplits);
+    const int per_a = ceil_div(U, k);
+    k = ceil_div(U, per_a);  // no empty slice
+    if (per_a <= cost_s) {
+      p.units_per_block = per_a;
+      p.pair_stride = k * per_a;
+      p.n_blocks = static_cast<int>(pairs * k);
+      p.part_stride = k;
+      return p;
+    }
+  }
+  p.units_per_block = static_cast<int>(per_s);
+  p.pair_stride = U;
+  p.n_blocks = static_cast<int>((pairs * U + per_s - 1) / per_s);
+  p.part_stride = std::min(kMaxSplits, ceil_div(U, p.units_per_block) + 1);
   return p;
 }
 
@@ -188,13 +227,17 @@ kvq::KiviDecodeArgs kivi_decode_args(const kivi_cache* cache, const DecodePlan& 
   a.res_cap = cache->res_cap;
   a.n_groups = plan.n_groups;
   a.n_resid = cache->n_resid;
-  a.units_per_split = plan.units_per_split;
-  a.splits_total = plan.splits;
+  a.n_pairs = cf.batch * cf.kv_heads;
+  a.units_per_pair = plan.units_per_pair;
+  a.pair_stride = plan.pair_stride;
+  a.units_per_block = plan.units_per_block;
+  a.n_blocks = plan.n_blocks;
+  a.part_stride = plan.part_stride;
   a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   a.status = reinterpret_cast<uint32_t*>(ws);
   a.counters = reinterpret_cast<uint32_t*>(ws + kWsHeader);
   a.part_o = reinterpret_cast<float*>(ws + kWsHeader + counters_bytes(cf.batch, cf.q_heads));
-  a.part_ml = a.part_o + static_cast<size_t>(cf.batch) * cf.q_heads * plan.splits * cf.head_dim;
+  a.part_ml = a.part_o + static_cast<size_t>(cf.batch) * cf.q_heads * plan.part_stride * cf.head_dim;
   a.out = out;
   a.out_fp32 = out_fp32;
   return a;
@@ -526,7 +569,7 @@ kvq_status kv_decode_attention_noalloc(const kivi_cache* cache, const uint16_t* 
   const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(cf.head_dim));
 
   const DecodePlan plan = plan_kivi_decode(cache);
-  const int splits_total = plan.splits;
+  const int splits_total = plan.part_stride;
   const size_t head = static_cast<size_t>(kWsHeader) + counters_bytes(cf.batch, cf.q_heads);
   const size_t need = head + static_cast<size_t>(cf.batch) * cf.q_heads * splits_total *
                                  (static_cast<size_t>(cf.head_dim) + 2) * sizeof(float);

@@ -335,7 +335,7 @@ __global__ void __launch_bounds__(128) fp8_decode_kernel(Fp8DecodeArgs a) {
     l_s[warp * 8 + g] = l_run;
   }
   __syncthreads();
-  finish_split<D>(o_s, m_s, l_s, gq, static_cast<long long>(b) * a.q_heads + h * gq, split, a.splits, a.part_o,
+  finish_split<D>(o_s, m_s, l_s, gq, static_cast<long long>(b) * a.q_heads + h * gq, split, a.splits, a.splits, a.part_o,
                   a.part_ml, a.counters + static_cast<long long>(b) * a.kv_heads + h, a.out, a.out_fp32);
 }
 

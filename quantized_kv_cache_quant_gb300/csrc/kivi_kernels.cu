@@ -475,38 +475,15 @@ __global__ void __launch_bounds__(128, KVQ_DECODE_MIN_BLOCKS) kivi_decode_kernel
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
   uint8_t* area = smem + S::BAR_BYTES;
-  float* o_s = reinterpret_cast<float*>(area);  // [4 warps][8 rows][D]  (after the main loop)
+  float* o_s = reinterpret_cast<float*>(area);  // [4 warps][8 rows][D]  (after a segment's loop)
   float* m_s = o_s + CombineSmem<D>::O_FLOATS;  // [4][8]
   float* l_s = m_s + 32;                        // [4][8]
 
-  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, tig = lane & 3;
   const int gq = a.q_heads / a.kv_heads;
-  const long long bh = static_cast<long long>(b) * a.kv_heads + h;
-
-  // this split's share of the units: groups [g_begin, g_end), chunks [c_begin, c_end)
-  const int u_begin = split * a.units_per_split, u_end = u_begin + a.units_per_split;
-  const int n_chunks = (a.n_resid + kGroup - 1) / kGroup;
-  const int g_begin = min(a.n_groups, u_begin);
-  const int g_end = min(a.n_groups, u_end);
-  const int c_begin = min(n_chunks, max(0, u_begin - a.n_groups + kChunkUnits - 1) / kChunkUnits);
-  const int c_end = min(n_chunks, max(0, u_end - a.n_groups + kChunkUnits - 1) / kChunkUnits);
-
-  float m_run = -INFINITY, l_run = 0.0f, vz_run = 0.0f;
-  float o_acc[P::NTV][4];
-#pragma unroll
-  for (int i = 0; i < P::NTV; ++i) o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.0f;
-  // ------------------------------- grouped region -------------------------------
-  const int n_here = g_end - g_begin;
-  const int n_mine = (n_here > warp) ? (n_here - warp + 3) / 4 : 0;
   uint64_t* bar = bars + warp * STAGES;
   uint64_t* wbar = bars + 4 * STAGES + warp;  // window chunk copies
   uint8_t* ring = area + warp * STAGES * P::STAGE;
-  const uint8_t* kc_g = a.k_codes + bh * a.groups_cap * static_cast<long long>(P::KC);
-  const uint8_t* km_g = a.k_meta + bh * a.groups_cap * static_cast<long long>(P::KM);
-  const uint8_t* vc_g = a.v_codes + bh * a.groups_cap * static_cast<long long>(P::VC);
-  const uint8_t* vm_g = a.v_meta + bh * a.groups_cap * static_cast<long long>(P::VM);
-
   if (lane == 0) {
 #pragma unroll
     for (int s = 0; s < STAGES; ++s) mbar_init(&bar[s], 1);
@@ -515,249 +492,299 @@ __global__ void __launch_bounds__(128, KVQ_DECODE_MIN_BLOCKS) kivi_decode_kernel
   }
   __syncwarp();
 
-  auto issue = [&](int j) {
-    const long long grp = g_begin + warp + 4 * j;
-    uint8_t* dst = ring + (j % STAGES) * P::STAGE;
-    uint64_t* bb = &bar[j % STAGES];
-    mbar_arrive_expect_tx(bb, P::STAGE);
-    bulk_g2s(dst, kc_g + grp * P::KC, P::KC, bb);
-    bulk_g2s(dst + P::KC, km_g + grp * P::KM, P::KM, bb);
-    bulk_g2s(dst + P::KC + P::KM, vc_g + grp * P::VC, P::VC, bb);
-    bulk_g2s(dst + P::KC + P::KM + P::VC, vm_g + grp * P::VM, P::VM, bb);
-  };
-  if (lane == 0) {
-    for (int j = 0; j < STAGES && j < n_mine; ++j) issue(j);
-  }
+  // This block's slice [u0, u1) of all units, pair after pair; one segment
+  // (and one partial) per (batch row, kv head) it touches.
+  const long long all_units = static_cast<long long>(a.n_pairs) * a.pair_stride;
+  const long long u0 = static_cast<long long>(blockIdx.x) * a.units_per_block;
+  const long long u1 = min(all_units, u0 + a.units_per_block);
+  int jg = 0;               // groups this warp has taken through its ring: stage and phase of the next
+  uint32_t wphase = 0;      // phase of the window barrier
+  bool timed_out = false;   // sticky: after a wait gives up the warp starts no more copies
+  for (long long u = u0; u < u1;) {
+    const int pair = static_cast<int>(u / a.pair_stride);
+    const long long pbase = static_cast<long long>(pair) * a.pair_stride;
+    const int lo = static_cast<int>(u - pbase);
+    const int hi = static_cast<int>(min(static_cast<long long>(a.units_per_pair), u1 - pbase));
+    u = pbase + a.pair_stride;
+    if (lo >= a.units_per_pair) continue;  // padding after the pair's units (the same for the whole block)
+    const int b = pair / a.kv_heads, h = pair % a.kv_heads;
+    const long long bh = pair;
+    const int first_block = static_cast<int>(pbase / a.units_per_block);
+    const int split = static_cast<int>(blockIdx.x) - first_block;
+    const int n_splits = static_cast<int>((pbase + a.units_per_pair - 1) / a.units_per_block) - first_block + 1;
+    // the stages and the combine area of the previous segment are reused
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncthreads();
 
-  // Query fragments of row g (query head h*gq + g), scaled by 2^-e so that
-  // |q| < 1 and q * s stays inside the fp16 range.
-  const bool row_ok = g < gq;
-  const __half* qrow = reinterpret_cast<const __half*>(a.q) +
-                       (static_cast<long long>(b) * a.q_heads + h * gq + (row_ok ? g : 0)) * D;
-  float2 qv[P::KS][2];
-  float qmax = 0.0f;
-#pragma unroll
-  for (int ks = 0; ks < P::KS; ++ks)
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const __half2 v = row_ok ? *reinterpret_cast<const __half2*>(qrow + 16 * ks + 8 * j + 2 * tig)
-                               : __float2half2_rn(0.0f);
-      qv[ks][j] = __half22float2(v);
-      qmax = fmaxf(qmax, fmaxf(fabsf(qv[ks][j].x), fabsf(qv[ks][j].y)));
-    }
-  qmax = quad_max(qmax);
-  int e = 0;
-  if (qmax > 0.0f) frexpf(qmax, &e);
-  const float qscale = ldexpf(1.0f, -e);
-  uint32_t qs[P::KS][2];
-#pragma unroll
-  for (int ks = 0; ks < P::KS; ++ks)
-#pragma unroll
-    for (int j = 0; j < 2; ++j) qs[ks][j] = pack_rn_f16x2(qv[ks][j].x * qscale, qv[ks][j].y * qscale);
-  const float p2e = ldexpf(1.0f, e) * a.scale_log2;
-  const float mult6 = kInvP6 * p2e, mult8 = kInvP8 * p2e;
+    // groups [g_begin, g_end) and window chunks [c_begin, c_end) of the segment
+    const int n_chunks = (a.n_resid + kGroup - 1) / kGroup;
+    const int g_begin = min(a.n_groups, lo);
+    const int g_end = min(a.n_groups, hi);
+    const int c_begin = min(n_chunks, max(0, lo - a.n_groups + kChunkUnits - 1) / kChunkUnits);
+    const int c_end = min(n_chunks, max(0, hi - a.n_groups + kChunkUnits - 1) / kChunkUnits);
 
-  // q . k_hat of the 32 tokens of the group in stage `sp`: 8 scores (log2
-  // units) of this thread's row, tokens 8*nt + 2*tig + {0, 1}.
-  auto qk_scores = [&](const uint8_t* sp, float (&sc)[8]) {
-    const uint4* kcw = reinterpret_cast<const uint4*>(sp);
-    const uint4* kmr = reinterpret_cast<const uint4*>(sp + P::KC);
-    uint32_t kw[P::KW];
-#pragma unroll
-    for (int c = 0; c < P::KW / 4; ++c) {
-      const uint4 x = kcw[c * 32 + lane];
-      kw[4 * c] = x.x;
-      kw[4 * c + 1] = x.y;
-      kw[4 * c + 2] = x.z;
-      kw[4 * c + 3] = x.w;
-    }
-    float sacc[4][4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) sacc[i][0] = sacc[i][1] = sacc[i][2] = sacc[i][3] = 0.0f;
-    // q . z: this lane's four channels of head g on the FMA pipe (the tensor pipe is the
-    // busier one here); a quad sum after the loop completes the dot product.
-    float bsum = 0.0f;
-#pragma unroll
-    for (int ks = 0; ks < P::KS; ++ks) {
-      const uint4 md = kmr[ks * 4 + tig];  // {s(d0,d0+1), s(d0+8,d0+9), z(d0,d0+1), z(d0+8,d0+9)}
-      const __half2 q0 = bits_h2(qs[ks][0]), q1 = bits_h2(qs[ks][1]);
-      const __half2 hi0 = __hmul2(q0, bits_h2(md.x));
-      const __half2 lo0 = __hfma2(q0, bits_h2(md.x), __hneg2(hi0));
-      const __half2 hi1 = __hmul2(q1, bits_h2(md.y));
-      const __half2 lo1 = __hfma2(q1, bits_h2(md.y), __hneg2(hi1));
-      const uint32_t A0 = h2_bits(hi0), A1 = h2_bits(lo0), A2 = h2_bits(hi1), A3 = h2_bits(lo1);
-      bsum = dot2_f16_f32(qs[ks][0], md.z, dot2_f16_f32(qs[ks][1], md.w, bsum));
-      if constexpr (KB == 2) {
-        const uint32_t w = kw[ks];
-        const uint32_t l6 = w << 6, l2 = w << 2, r2 = w >> 2, r6 = w >> 6;
-        mma16816(sacc[0], A0, A1, A2, A3, l6 & kMaskP6, r2 & kMaskP6);
-        mma16816(sacc[1], A0, A1, A2, A3, l6 & kMaskP8, r2 & kMaskP8);
-        mma16816(sacc[2], A0, A1, A2, A3, l2 & kMaskP6, r6 & kMaskP6);
-        mma16816(sacc[3], A0, A1, A2, A3, l2 & kMaskP8, r6 & kMaskP8);
-      } else {
-        const uint32_t w0 = kw[2 * ks], w1 = kw[2 * ks + 1];
-        mma16816(sacc[0], A0, A1, A2, A3, (w0 << 6) & kMask4, (w1 << 6) & kMask4);
-        mma16816(sacc[1], A0, A1, A2, A3, (w0 << 2) & kMask4, (w1 << 2) & kMask4);
-        mma16816(sacc[2], A0, A1, A2, A3, (w0 >> 2) & kMask4, (w1 >> 2) & kMask4);
-        mma16816(sacc[3], A0, A1, A2, A3, (w0 >> 6) & kMask4, (w1 >> 6) & kMask4);
-      }
-    }
-    const float bias = quad_sum(bsum) * p2e;
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
-      const float mult = (KB == 2 && (nt & 1)) ? mult8 : mult6;
-      sc[2 * nt] = fmaf(sacc[nt][0] + sacc[nt][2], mult, bias);
-      sc[2 * nt + 1] = fmaf(sacc[nt][1] + sacc[nt][3], mult, bias);
-    }
-  };
-
-  // Software pipeline: iteration j runs the softmax and p . V of group j
-  // and, in the same straight-line block, q . k^T of group j + 1, so that
-  // each warp keeps both the tensor pipe and the ALUs busy.
-  int j = 0;
-  bool timed_out = false;
-  float sc[8];
-  if (n_mine > 0) {
-    if (mbar_wait_bounded(&bar[0], 0))
-      qk_scores(ring, sc);
-    else
-      timed_out = true;
-  }
-  for (; !timed_out && j < n_mine; ++j) {
-    const int s = j % STAGES;
-    const uint8_t* sp = ring + s * P::STAGE;
-    // the next group's stage (this one again past the end: its scores are discarded)
-    const int jn = (j + 1 < n_mine) ? j + 1 : j;
-    if (jn != j && !mbar_wait_bounded(&bar[jn % STAGES], (jn / STAGES) & 1)) {
-      timed_out = true;
-      break;
-    }
-    const uint8_t* spn = ring + (jn % STAGES) * P::STAGE;
-    const uint4* vcw = reinterpret_cast<const uint4*>(sp + P::KC + P::KM);
-    const uint4* vmr = reinterpret_cast<const uint4*>(sp + P::KC + P::KM + P::VC);
-
-    float p[8];
-    online_softmax<P::NTV>(sc, p, o_acc, m_run, l_run, vz_run);
-
-    // ---- p' = p * s_t as fp16 hi + lo; the zero-point term on CUDA cores ----
-    const uint4 vs = vmr[tig], vz = vmr[4 + tig];
-    const uint32_t vsw[4] = {vs.x, vs.y, vs.z, vs.w};
-    const uint32_t vzw[4] = {vz.x, vz.y, vz.z, vz.w};
-    uint32_t phi[4], plo[4];
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
-      const float2 sf = __half22float2(bits_h2(vsw[nt]));
-      const float2 zf = __half22float2(bits_h2(vzw[nt]));
-      const float pp0 = p[2 * nt] * sf.x, pp1 = p[2 * nt + 1] * sf.y;
-      const __half2 hh = __floats2half2_rn(pp0, pp1);
-      const float2 hf = __half22float2(hh);
-      phi[nt] = h2_bits(hh);
-      plo[nt] = pack_rn_f16x2(pp0 - hf.x, pp1 - hf.y);
-      l_run += p[2 * nt] + p[2 * nt + 1];
-      vz_run = fmaf(p[2 * nt], zf.x, fmaf(p[2 * nt + 1], zf.y, vz_run));
-    }
-
-    // ---- q . k^T of group j + 1 (independent of what follows) ----
-    qk_scores(spn, sc);
-
-    // ---- o += p' . codes (group j) ----
-    uint32_t vw[P::VW];
-#pragma unroll
-    for (int c = 0; c < P::VW / 4; ++c) {
-      const uint4 x = vcw[c * 32 + lane];
-      vw[4 * c] = x.x;
-      vw[4 * c + 1] = x.y;
-      vw[4 * c + 2] = x.z;
-      vw[4 * c + 3] = x.w;
-    }
-#pragma unroll
-    for (int ks = 0; ks < 2; ++ks) {
-      const uint32_t A0 = phi[2 * ks], A1 = plo[2 * ks], A2 = phi[2 * ks + 1], A3 = plo[2 * ks + 1];
-#pragma unroll
-      for (int q = 0; q < P::NQ; ++q) {
-        if constexpr (VB == 2) {
-          const uint32_t w = vw[ks * P::NQ + q];
-          const uint32_t l6 = w << 6, l2 = w << 2, r2 = w >> 2, r6 = w >> 6;
-          mma16816(o_acc[4 * q + 0], A0, A1, A2, A3, l6 & kMaskP6, r2 & kMaskP6);
-          mma16816(o_acc[4 * q + 1], A0, A1, A2, A3, l6 & kMaskP8, r2 & kMaskP8);
-          mma16816(o_acc[4 * q + 2], A0, A1, A2, A3, l2 & kMaskP6, r6 & kMaskP6);
-          mma16816(o_acc[4 * q + 3], A0, A1, A2, A3, l2 & kMaskP8, r6 & kMaskP8);
-        } else {
-          const uint32_t w0 = vw[(2 * ks) * P::NQ + q], w1 = vw[(2 * ks + 1) * P::NQ + q];
-          mma16816(o_acc[4 * q + 0], A0, A1, A2, A3, (w0 << 6) & kMask4, (w1 << 6) & kMask4);
-          mma16816(o_acc[4 * q + 1], A0, A1, A2, A3, (w0 << 2) & kMask4, (w1 << 2) & kMask4);
-          mma16816(o_acc[4 * q + 2], A0, A1, A2, A3, (w0 >> 2) & kMask4, (w1 >> 2) & kMask4);
-          mma16816(o_acc[4 * q + 3], A0, A1, A2, A3, (w0 >> 6) & kMask4, (w1 >> 6) & kMask4);
-        }
-      }
-    }
-
-    // release stage j and refill it with the group STAGES ahead
-    __syncwarp();
-    if (lane == 0 && j + STAGES < n_mine) {
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      issue(j + STAGES);
-    }
-  }
-
-  // ------------------------ fp16 window, 32-token chunks ------------------------
-  constexpr bool kTwoFields = (VB == 2);
-  bool real_units = false, win_pending = false;
-  uint32_t wphase = 0;
-  if (!timed_out && c_begin + warp < c_end) {
-    real_units = true;
-    // the call takes copies: a variable whose address escapes would live in
-    // local memory for the whole kernel, main loop included
-    float o_io[P::NTV][4], st[3] = {m_run, l_run, vz_run};
-    uint32_t q_io[P::KS][2];
-#pragma unroll
-    for (int i = 0; i < P::NTV; ++i) o_io[i][0] = o_acc[i][0], o_io[i][1] = o_acc[i][1], o_io[i][2] = o_acc[i][2], o_io[i][3] = o_acc[i][3];
-#pragma unroll
-    for (int ks = 0; ks < P::KS; ++ks) q_io[ks][0] = qs[ks][0], q_io[ks][1] = qs[ks][1];
-    uint32_t ph = 0;
-    const bool ok = window_chunks<D, VB>(a.k_res, a.v_res, bh * a.res_cap, a.n_resid, c_begin + warp, c_end, ring,
-                                         S::WIN_ROW, wbar, ph, q_io, p2e, o_io, st[0], st[1], st[2]);
-#pragma unroll
-    for (int i = 0; i < P::NTV; ++i) o_acc[i][0] = o_io[i][0], o_acc[i][1] = o_io[i][1], o_acc[i][2] = o_io[i][2], o_acc[i][3] = o_io[i][3];
-    m_run = st[0];
-    l_run = st[1];
-    vz_run = st[2];
-    wphase = ph;
-    if (!ok) {
-      timed_out = true;
-      win_pending = true;
-    }
-  }
-
-  if (timed_out) {
-    if (lane == 0) report_timeout(a.status);
-    // let the copies already in flight land before the stages are reused
-    for (int jj = j; jj < n_mine && jj < j + STAGES; ++jj) (void)mbar_wait_bounded(&bar[jj % STAGES], (jj / STAGES) & 1);
-    if (win_pending) (void)mbar_wait_bounded(wbar, wphase);
-    m_run = -INFINITY;
-    l_run = 0.0f;
-    vz_run = 0.0f;
+    float m_run = -INFINITY, l_run = 0.0f, vz_run = 0.0f;
+    float o_acc[P::NTV][4];
 #pragma unroll
     for (int i = 0; i < P::NTV; ++i) o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.0f;
-  }
-  l_run = quad_sum(l_run);
-  vz_run = quad_sum(vz_run);
-  __syncthreads();  // every warp is done with its stages; the area is reused below
-#pragma unroll
-  for (int nt = 0; nt < P::NTV; ++nt) {
-    const float om = real_units ? 1.0f : ((kTwoFields && (nt & 1)) ? kInvP8 : kInvP6);
-    const int c = 8 * nt + 2 * tig;
-    o_s[(warp * 8 + g) * D + c] = fmaf(o_acc[nt][0] + o_acc[nt][2], om, vz_run);
-    o_s[(warp * 8 + g) * D + c + 1] = fmaf(o_acc[nt][1] + o_acc[nt][3], om, vz_run);
-  }
-  if (tig == 0) {
-    m_s[warp * 8 + g] = m_run;
-    l_s[warp * 8 + g] = l_run;
-  }
+    // ------------------------------- grouped region -------------------------------
+    const int n_here = g_end - g_begin;
+    const int n_mine = (!timed_out && n_here > warp) ? (n_here - warp + 3) / 4 : 0;
+    const uint8_t* kc_g = a.k_codes + bh * a.groups_cap * static_cast<long long>(P::KC);
+    const uint8_t* km_g = a.k_meta + bh * a.groups_cap * static_cast<long long>(P::KM);
+    const uint8_t* vc_g = a.v_codes + bh * a.groups_cap * static_cast<long long>(P::VC);
+    const uint8_t* vm_g = a.v_meta + bh * a.groups_cap * static_cast<long long>(P::VM);
 
-  __syncthreads();
-  finish_split<D>(o_s, m_s, l_s, gq, static_cast<long long>(b) * a.q_heads + h * gq, split, a.splits_total, a.part_o,
-                  a.part_ml, a.counters + bh, a.out, a.out_fp32);
+    // group j of this segment goes through ring slot (jg + j) % STAGES
+    auto issue = [&](int j) {
+      const long long grp = g_begin + warp + 4 * j;
+      uint8_t* dst = ring + ((jg + j) % STAGES) * P::STAGE;
+      uint64_t* bb = &bar[(jg + j) % STAGES];
+      mbar_arrive_expect_tx(bb, P::STAGE);
+      bulk_g2s(dst, kc_g + grp * P::KC, P::KC, bb);
+      bulk_g2s(dst + P::KC, km_g + grp * P::KM, P::KM, bb);
+      bulk_g2s(dst + P::KC + P::KM, vc_g + grp * P::VC, P::VC, bb);
+      bulk_g2s(dst + P::KC + P::KM + P::VC, vm_g + grp * P::VM, P::VM, bb);
+    };
+    auto wait_group = [&](int j) { return mbar_wait_bounded(&bar[(jg + j) % STAGES], ((jg + j) / STAGES) & 1); };
+    auto stage = [&](int j) { return ring + ((jg + j) % STAGES) * P::STAGE; };
+    if (lane == 0) {
+      for (int j = 0; j < STAGES && j < n_mine; ++j) issue(j);
+    }
+
+    // Query fragments of row g (query head h*gq + g), scaled by 2^-e so that
+    // |q| < 1 and q * s stays inside the fp16 range.
+    const bool row_ok = g < gq;
+    const __half* qrow = reinterpret_cast<const __half*>(a.q) +
+                         (static_cast<long long>(b) * a.q_heads + h * gq + (row_ok ? g : 0)) * D;
+    float2 qv[P::KS][2];
+    float qmax = 0.0f;
+#pragma unroll
+    for (int ks = 0; ks < P::KS; ++ks)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const __half2 v = row_ok ? *reinterpret_cast<const __half2*>(qrow + 16 * ks + 8 * j + 2 * tig)
+                                 : __float2half2_rn(0.0f);
+        qv[ks][j] = __half22float2(v);
+        qmax = fmaxf(qmax, fmaxf(fabsf(qv[ks][j].x), fabsf(qv[ks][j].y)));
+      }
+    qmax = quad_max(qmax);
+    int e = 0;
+    if (qmax > 0.0f) frexpf(qmax, &e);
+    const float qscale = ldexpf(1.0f, -e);
+    uint32_t qs[P::KS][2];
+#pragma unroll
+    for (int ks = 0; ks < P::KS; ++ks)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) qs[ks][j] = pack_rn_f16x2(qv[ks][j].x * qscale, qv[ks][j].y * qscale);
+    const float p2e = ldexpf(1.0f, e) * a.scale_log2;
+    const float mult6 = kInvP6 * p2e, mult8 = kInvP8 * p2e;
+
+    // q . k_hat of the 32 tokens of the group in stage `sp`: 8 scores (log2
+    // units) of this thread's row, tokens 8*nt + 2*tig + {0, 1}.
+    auto qk_scores = [&](const uint8_t* sp, float (&sc)[8]) {
+      const uint4* kcw = reinterpret_cast<const uint4*>(sp);
+      const uint4* kmr = reinterpret_cast<const uint4*>(sp + P::KC);
+      uint32_t kw[P::KW];
+#pragma unroll
+      for (int c = 0; c < P::KW / 4; ++c) {
+        const uint4 x = kcw[c * 32 + lane];
+        kw[4 * c] = x.x;
+        kw[4 * c + 1] = x.y;
+        kw[4 * c + 2] = x.z;
+        kw[4 * c + 3] = x.w;
+      }
+      float sacc[4][4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) sacc[i][0] = sacc[i][1] = sacc[i][2] = sacc[i][3] = 0.0f;
+      // q . z: this lane's four channels of head g on the FMA pipe (the tensor pipe is the
+      // busier one here); a quad sum after the loop completes the dot product.
+      float bsum = 0.0f;
+#pragma unroll
+      for (int ks = 0; ks < P::KS; ++ks) {
+        const uint4 md = kmr[ks * 4 + tig];  // {s(d0,d0+1), s(d0+8,d0+9), z(d0,d0+1), z(d0+8,d0+9)}
+        const __half2 q0 = bits_h2(qs[ks][0]), q1 = bits_h2(qs[ks][1]);
+        const __half2 hi0 = __hmul2(q0, bits_h2(md.x));
+        const __half2 lo0 = __hfma2(q0, bits_h2(md.x), __hneg2(hi0));
+        const __half2 hi1 = __hmul2(q1, bits_h2(md.y));
+        const __half2 lo1 = __hfma2(q1, bits_h2(md.y), __hneg2(hi1));
+        const uint32_t A0 = h2_bits(hi0), A1 = h2_bits(lo0), A2 = h2_bits(hi1), A3 = h2_bits(lo1);
+        bsum = dot2_f16_f32(qs[ks][0], md.z, dot2_f16_f32(qs[ks][1], md.w, bsum));
+        if constexpr (KB == 2) {
+          const uint32_t w = kw[ks];
+          const uint32_t l6 = w << 6, l2 = w << 2, r2 = w >> 2, r6 = w >> 6;
+          mma16816(sacc[0], A0, A1, A2, A3, l6 & kMaskP6, r2 & kMaskP6);
+          mma16816(sacc[1], A0, A1, A2, A3, l6 & kMaskP8, r2 & kMaskP8);
+          mma16816(sacc[2], A0, A1, A2, A3, l2 & kMaskP6, r6 & kMaskP6);
+          mma16816(sacc[3], A0, A1, A2, A3, l2 & kMaskP8, r6 & kMaskP8);
+        } else {
+          const uint32_t w0 = kw[2 * ks], w1 = kw[2 * ks + 1];
+          mma16816(sacc[0], A0, A1, A2, A3, (w0 << 6) & kMask4, (w1 << 6) & kMask4);
+          mma16816(sacc[1], A0, A1, A2, A3, (w0 << 2) & kMask4, (w1 << 2) & kMask4);
+          mma16816(sacc[2], A0, A1, A2, A3, (w0 >> 2) & kMask4, (w1 >> 2) & kMask4);
+          mma16816(sacc[3], A0, A1, A2, A3, (w0 >> 6) & kMask4, (w1 >> 6) & kMask4);
+        }
+      }
+      const float bias = quad_sum(bsum) * p2e;
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        const float mult = (KB == 2 && (nt & 1)) ? mult8 : mult6;
+        sc[2 * nt] = fmaf(sacc[nt][0] + sacc[nt][2], mult, bias);
+        sc[2 * nt + 1] = fmaf(sacc[nt][1] + sacc[nt][3], mult, bias);
+      }
+    };
+
+    // Software pipeline: iteration j runs the softmax and p . V of group j
+    // and, in the same straight-line block, q . k^T of group j + 1, so that
+    // each warp keeps both the tensor pipe and the ALUs busy.
+    int j = 0;
+    float sc[8];
+    if (n_mine > 0) {
+      if (wait_group(0))
+        qk_scores(stage(0), sc);
+      else
+        timed_out = true;
+    }
+    for (; !timed_out && j < n_mine; ++j) {
+      const uint8_t* sp = stage(j);
+      // the next group's stage (this one again past the end: its scores are discarded)
+      const int jn = (j + 1 < n_mine) ? j + 1 : j;
+      if (jn != j && !wait_group(jn)) {
+        timed_out = true;
+        break;
+      }
+      const uint8_t* spn = stage(jn);
+      const uint4* vcw = reinterpret_cast<const uint4*>(sp + P::KC + P::KM);
+      const uint4* vmr = reinterpret_cast<const uint4*>(sp + P::KC + P::KM + P::VC);
+
+      float p[8];
+      online_softmax<P::NTV>(sc, p, o_acc, m_run, l_run, vz_run);
+
+      // ---- p' = p * s_t as fp16 hi + lo; the zero-point term on CUDA cores ----
+      const uint4 vs = vmr[tig], vz = vmr[4 + tig];
+      const uint32_t vsw[4] = {vs.x, vs.y, vs.z, vs.w};
+      const uint32_t vzw[4] = {vz.x, vz.y, vz.z, vz.w};
+      uint32_t phi[4], plo[4];
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        const float2 sf = __half22float2(bits_h2(vsw[nt]));
+        const float2 zf = __half22float2(bits_h2(vzw[nt]));
+        const float pp0 = p[2 * nt] * sf.x, pp1 = p[2 * nt + 1] * sf.y;
+        const __half2 hh = __floats2half2_rn(pp0, pp1);
+        const float2 hf = __half22float2(hh);
+        phi[nt] = h2_bits(hh);
+        plo[nt] = pack_rn_f16x2(pp0 - hf.x, pp1 - hf.y);
+        l_run += p[2 * nt] + p[2 * nt + 1];
+        vz_run = fmaf(p[2 * nt], zf.x, fmaf(p[2 * nt + 1], zf.y, vz_run));
+      }
+
+      // ---- q . k^T of group j + 1 (independent of what follows) ----
+      qk_scores(spn, sc);
+
+      // ---- o += p' . codes (group j) ----
+      uint32_t vw[P::VW];
+#pragma unroll
+      for (int c = 0; c < P::VW / 4; ++c) {
+        const uint4 x = vcw[c * 32 + lane];
+        vw[4 * c] = x.x;
+        vw[4 * c + 1] = x.y;
+        vw[4 * c + 2] = x.z;
+        vw[4 * c + 3] = x.w;
+      }
+#pragma unroll
+      for (int ks = 0; ks < 2; ++ks) {
+        const uint32_t A0 = phi[2 * ks], A1 = plo[2 * ks], A2 = phi[2 * ks + 1], A3 = plo[2 * ks + 1];
+#pragma unroll
+        for (int q = 0; q < P::NQ; ++q) {
+          if constexpr (VB == 2) {
+            const uint32_t w = vw[ks * P::NQ + q];
+            const uint32_t l6 = w << 6, l2 = w << 2, r2 = w >> 2, r6 = w >> 6;
+            mma16816(o_acc[4 * q + 0], A0, A1, A2, A3, l6 & kMaskP6, r2 & kMaskP6);
+            mma16816(o_acc[4 * q + 1], A0, A1, A2, A3, l6 & kMaskP8, r2 & kMaskP8);
+            mma16816(o_acc[4 * q + 2], A0, A1, A2, A3, l2 & kMaskP6, r6 & kMaskP6);
+            mma16816(o_acc[4 * q + 3], A0, A1, A2, A3, l2 & kMaskP8, r6 & kMaskP8);
+          } else {
+            const uint32_t w0 = vw[(2 * ks) * P::NQ + q], w1 = vw[(2 * ks + 1) * P::NQ + q];
+            mma16816(o_acc[4 * q + 0], A0, A1, A2, A3, (w0 << 6) & kMask4, (w1 << 6) & kMask4);
+            mma16816(o_acc[4 * q + 1], A0, A1, A2, A3, (w0 << 2) & kMask4, (w1 << 2) & kMask4);
+            mma16816(o_acc[4 * q + 2], A0, A1, A2, A3, (w0 >> 2) & kMask4, (w1 >> 2) & kMask4);
+            mma16816(o_acc[4 * q + 3], A0, A1, A2, A3, (w0 >> 6) & kMask4, (w1 >> 6) & kMask4);
+          }
+        }
+      }
+
+      // release stage j and refill it with the group STAGES ahead
+      __syncwarp();
+      if (lane == 0 && j + STAGES < n_mine) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        issue(j + STAGES);
+      }
+    }
+
+    // ------------------------ fp16 window, 32-token chunks ------------------------
+    constexpr bool kTwoFields = (VB == 2);
+    bool real_units = false, win_pending = false, seg_timeout = timed_out && n_mine > 0;
+    if (!timed_out && c_begin + warp < c_end) {
+      real_units = true;
+      // the call takes copies: a variable whose address escapes would live in
+      // local memory for the whole kernel, main loop included
+      float o_io[P::NTV][4], st[3] = {m_run, l_run, vz_run};
+      uint32_t q_io[P::KS][2];
+#pragma unroll
+      for (int i = 0; i < P::NTV; ++i)
+        o_io[i][0] = o_acc[i][0], o_io[i][1] = o_acc[i][1], o_io[i][2] = o_acc[i][2], o_io[i][3] = o_acc[i][3];
+#pragma unroll
+      for (int ks = 0; ks < P::KS; ++ks) q_io[ks][0] = qs[ks][0], q_io[ks][1] = qs[ks][1];
+      uint32_t ph = wphase;
+      const bool ok = window_chunks<D, VB>(a.k_res, a.v_res, bh * a.res_cap, a.n_resid, c_begin + warp, c_end, ring,
+                                           S::WIN_ROW, wbar, ph, q_io, p2e, o_io, st[0], st[1], st[2]);
+#pragma unroll
+      for (int i = 0; i < P::NTV; ++i)
+        o_acc[i][0] = o_io[i][0], o_acc[i][1] = o_io[i][1], o_acc[i][2] = o_io[i][2], o_acc[i][3] = o_io[i][3];
+      m_run = st[0];
+      l_run = st[1];
+      vz_run = st[2];
+      wphase = ph;
+      if (!ok) {
+        timed_out = true;
+        seg_timeout = true;
+        win_pending = true;
+      }
+    }
+
+    if (seg_timeout) {
+      if (lane == 0) report_timeout(a.status);
+      // let the copies already in flight land before the stages are reused
+      for (int jj = j; jj < n_mine && jj < j + STAGES; ++jj) (void)wait_group(jj);
+      if (win_pending) (void)mbar_wait_bounded(wbar, wphase);
+    }
+    if (timed_out) {
+      m_run = -INFINITY;
+      l_run = 0.0f;
+      vz_run = 0.0f;
+#pragma unroll
+      for (int i = 0; i < P::NTV; ++i) o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.0f;
+    }
+    jg += n_mine;
+    l_run = quad_sum(l_run);
+    vz_run = quad_sum(vz_run);
+    __syncthreads();  // every warp is done with its stages; the area is reused below
+#pragma unroll
+    for (int nt = 0; nt < P::NTV; ++nt) {
+      const float om = real_units ? 1.0f : ((kTwoFields && (nt & 1)) ? kInvP8 : kInvP6);
+      const int c = 8 * nt + 2 * tig;
+      o_s[(warp * 8 + g) * D + c] = fmaf(o_acc[nt][0] + o_acc[nt][2], om, vz_run);
+      o_s[(warp * 8 + g) * D + c + 1] = fmaf(o_acc[nt][1] + o_acc[nt][3], om, vz_run);
+    }
+    if (tig == 0) {
+      m_s[warp * 8 + g] = m_run;
+      l_s[warp * 8 + g] = l_run;
+    }
+
+    __syncthreads();
+    finish_split<D>(o_s, m_s, l_s, gq, static_cast<long long>(b) * a.q_heads + h * gq, split, n_splits,
+                    a.part_stride, a.part_o, a.part_ml, a.counters + bh, a.out, a.out_fp32);
+  }
 }
 
 constexpr int kDecodeStages = 4;
@@ -792,8 +819,7 @@ cudaError_t decode_dispatch(const KiviDecodeArgs& a, cudaStream_t s) {
   auto kern = kivi_decode_kernel<D, KB, VB, kDecodeStages>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(a.splits_total, a.kv_heads, a.batch);
-  kern<<<grid, 128, smem, s>>>(a);
+  kern<<<a.n_blocks, 128, smem, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -185,14 +185,16 @@ namespace kvq {
 
 // Epilogue shared by the split-K decode kernels. The four warps of a thread
 // block have left per-warp (m, l, o) in shared memory (o_s[4][8][D],
-// m_s[4][8], l_s[4][8], log2 units). The block combines them, writes its
-// partial for each query row, and the last block of a (batch row, kv head) to
-// finish — found with an atomic counter, no waiting — merges all splits into
-// `out` and resets the counter for the next call.
+// m_s[4][8], l_s[4][8], log2 units). The block combines them and writes its
+// partial `split` of each query row (slot row * stride + split); the last of
+// the `splits_total` blocks of a (batch row, kv head) to finish — found with an
+// atomic counter, no waiting — merges all splits into `out` and resets the
+// counter for the next call.
+// Needs blockDim.x == 128 and D in {64, 128}.
 template <int D>
 __device__ __forceinline__ void finish_split(float* o_s, float* m_s, float* l_s, int gq, long long q_row0, int split,
-                                             int splits_total, float* part_o, float* part_ml, uint32_t* counter,
-                                             void* out, int out_fp32) {
+                                             int splits_total, int stride, float* part_o, float* part_ml,
+                                             uint32_t* counter, void* out, int out_fp32) {
   const int tid = threadIdx.x;
   for (int i = tid; i < gq * D; i += blockDim.x) {
     const int r = i / D, c = i % D;
@@ -208,7 +210,7 @@ __device__ __forceinline__ void finish_split(float* o_s, float* m_s, float* l_s,
         O = fmaf(o_s[(w * 8 + r) * D + c], f, O);
       }
     }
-    const long long row = (q_row0 + r) * splits_total + split;
+    const long long row = (q_row0 + r) * stride + split;
     part_o[row * D + c] = O;
     if (c == 0) {
       part_ml[row * 2] = M;
@@ -223,36 +225,60 @@ __device__ __forceinline__ void finish_split(float* o_s, float* m_s, float* l_s,
   if (!last) return;
   __threadfence();
   if (tid == 0) *counter = 0u;
-  // merge weights per query row into shared memory (o_s is free now)
+  // merge weights per query row into shared memory (o_s is free now); one
+  // warp per row, each lane holds splits lane and lane + 32 (kMaxSplits = 64)
+  static_assert(kMaxSplits <= 64, "two splits per lane");
   float* wgt = o_s;                      // [8][kMaxSplits]
   float* inv_l = o_s + 8 * kMaxSplits;   // [8]
   const int warp = tid >> 5, lane = tid & 31;
   for (int r = warp; r < gq; r += blockDim.x >> 5) {
-    const long long base = (q_row0 + r) * splits_total;
-    float M = -INFINITY;
-    for (int s = lane; s < splits_total; s += 32) M = fmaxf(M, __ldcg(part_ml + (base + s) * 2));
-    M = warp_max(M);
+    const long long base = (q_row0 + r) * stride;
+    float mv[2], lv[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int sp = lane + 32 * k;
+      mv[k] = (sp < splits_total) ? __ldcg(part_ml + (base + sp) * 2) : -INFINITY;
+      lv[k] = (sp < splits_total) ? __ldcg(part_ml + (base + sp) * 2 + 1) : 0.0f;
+    }
+    const float M = warp_max(fmaxf(mv[0], mv[1]));
     float L = 0.0f;
-    for (int s = lane; s < splits_total; s += 32) {
-      const float f = (M == -INFINITY) ? 0.0f : fast_exp2(__ldcg(part_ml + (base + s) * 2) - M);
-      wgt[r * kMaxSplits + s] = f;
-      L = fmaf(f, __ldcg(part_ml + (base + s) * 2 + 1), L);
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int sp = lane + 32 * k;
+      const float f = (M == -INFINITY || sp >= splits_total) ? 0.0f : fast_exp2(mv[k] - M);
+      if (sp < splits_total) wgt[r * kMaxSplits + sp] = f;
+      L = fmaf(f, lv[k], L);
     }
     L = warp_sum(L);
     if (lane == 0) inv_l[r] = (L > 0.0f) ? 1.0f / L : 0.0f;
   }
   __syncthreads();
-  for (int i = tid; i < gq * D; i += blockDim.x) {
-    const int r = i / D, c = i % D;
-    const long long base = (q_row0 + r) * splits_total;
-    float O = 0.0f;
-    for (int s = 0; s < splits_total; ++s) O = fmaf(wgt[r * kMaxSplits + s], __ldcg(part_o + (base + s) * D + c), O);
-    O *= inv_l[r];
+  // thread t sums column t % D of rows t / D, t / D + 128 / D, ...: the loads of
+  // all its rows for one split are independent and are in flight together
+  constexpr int kRowStep = 128 / D;
+  constexpr int kRowsPer = (kMaxGqa + kRowStep - 1) / kRowStep;
+  const int c = tid % D, r0 = tid / D;
+  float O[kRowsPer];
+#pragma unroll
+  for (int k = 0; k < kRowsPer; ++k) O[k] = 0.0f;
+#pragma unroll 4
+  for (int sp = 0; sp < splits_total; ++sp) {
+#pragma unroll
+    for (int k = 0; k < kRowsPer; ++k) {
+      const int r = r0 + k * kRowStep;
+      if (r < gq) O[k] = fmaf(wgt[r * kMaxSplits + sp], __ldcg(part_o + ((q_row0 + r) * stride + sp) * D + c), O[k]);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < kRowsPer; ++k) {
+    const int r = r0 + k * kRowStep;
+    if (r >= gq) continue;
     const long long o_idx = (q_row0 + r) * D + c;
+    const float v = O[k] * inv_l[r];
     if (out_fp32)
-      reinterpret_cast<float*>(out)[o_idx] = O;
+      reinterpret_cast<float*>(out)[o_idx] = v;
     else
-      reinterpret_cast<__half*>(out)[o_idx] = __float2half_rn(O);
+      reinterpret_cast<__half*>(out)[o_idx] = __float2half_rn(v);
   }
 }
 

@@ -49,14 +49,21 @@ struct KiviDecodeArgs {
   const uint16_t* q;
   int batch, kv_heads, q_heads, head_dim, k_bits, v_bits, groups_cap, res_cap;
   int n_groups, n_resid;
-  // Work units of one (batch row, kv head): its n_groups groups, then its
-  // ceil(n_resid / 32) window chunks of kChunkUnits units each; split x takes
-  // units [x * units_per_split, (x + 1) * units_per_split).
-  int units_per_split;
-  int splits_total;
+  // Work units of one (batch row, kv head) pair: its n_groups groups, then its
+  // ceil(n_resid / 32) window chunks of kChunkUnits units each. Pair p owns
+  // units [p * pair_stride, p * pair_stride + units_per_pair) of a range cut
+  // into n_blocks slices of units_per_block (pair_stride > units_per_pair pads
+  // every pair to whole slices); a block writes one partial per pair its slice
+  // touches.
+  int n_pairs;
+  int units_per_pair;
+  int pair_stride;
+  int units_per_block;
+  int n_blocks;
+  int part_stride;        // partial slots per query row (>= the blocks touching one pair)
   float scale_log2;       // softmax scale * log2(e)
-  float* part_o;          // [B, Hq, splits_total, D]
-  float* part_ml;         // [B, Hq, splits_total, 2]
+  float* part_o;          // [B, Hq, part_stride, D]
+  float* part_ml;         // [B, Hq, part_stride, 2]
   uint32_t* counters;     // [B, H_kv] finished-split counters (zero between calls)
   uint32_t* status;
   void* out;              // [B, Hq, D]
