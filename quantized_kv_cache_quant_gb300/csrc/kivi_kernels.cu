@@ -481,12 +481,17 @@ __global__ void __launch_bounds__(128, KVQ_DECODE_MIN_BLOCKS) kivi_decode_kernel
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, tig = lane & 3;
   const int gq = a.q_heads / a.kv_heads;
+  // The warp's ring: NS slots of GPS consecutive groups each, one bulk copy
+  // per record type and slot (records of consecutive groups are contiguous).
+  constexpr int GPS = 2, NS = STAGES / GPS;
+  static_assert(STAGES % GPS == 0, "whole slots");
+  constexpr int SLOT = GPS * P::STAGE;
   uint64_t* bar = bars + warp * STAGES;
   uint64_t* wbar = bars + 4 * STAGES + warp;  // window chunk copies
   uint8_t* ring = area + warp * STAGES * P::STAGE;
   if (lane == 0) {
 #pragma unroll
-    for (int s = 0; s < STAGES; ++s) mbar_init(&bar[s], 1);
+    for (int s = 0; s < NS; ++s) mbar_init(&bar[s], 1);
     mbar_init(wbar, 1);
     fence_mbar_init();
   }
@@ -497,7 +502,7 @@ __global__ void __launch_bounds__(128, KVQ_DECODE_MIN_BLOCKS) kivi_decode_kernel
   const long long all_units = static_cast<long long>(a.n_pairs) * a.pair_stride;
   const long long u0 = static_cast<long long>(blockIdx.x) * a.units_per_block;
   const long long u1 = min(all_units, u0 + a.units_per_block);
-  int jg = 0;               // groups this warp has taken through its ring: stage and phase of the next
+  int jg = 0;               // slots this warp has filled so far: ring position and phase of the next
   uint32_t wphase = 0;      // phase of the window barrier
   bool timed_out = false;   // sticky: after a wait gives up the warp starts no more copies
   for (long long u = u0; u < u1;) {
@@ -528,28 +533,42 @@ __global__ void __launch_bounds__(128, KVQ_DECODE_MIN_BLOCKS) kivi_decode_kernel
 #pragma unroll
     for (int i = 0; i < P::NTV; ++i) o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.0f;
     // ------------------------------- grouped region -------------------------------
+    // this warp's groups: pairs g_begin + GPS * (warp + 4 * k) + {0, .., GPS - 1}
     const int n_here = g_end - g_begin;
-    const int n_mine = (!timed_out && n_here > warp) ? (n_here - warp + 3) / 4 : 0;
+    int n_mine = 0;
+    if (!timed_out && n_here > GPS * warp) {
+      const int np = (n_here - GPS * warp + 4 * GPS - 1) / (4 * GPS);
+      n_mine = GPS * (np - 1) + min(GPS, n_here - GPS * (warp + 4 * (np - 1)));
+    }
+    const int n_slots = (n_mine + GPS - 1) / GPS;
     const uint8_t* kc_g = a.k_codes + bh * a.groups_cap * static_cast<long long>(P::KC);
     const uint8_t* km_g = a.k_meta + bh * a.groups_cap * static_cast<long long>(P::KM);
     const uint8_t* vc_g = a.v_codes + bh * a.groups_cap * static_cast<long long>(P::VC);
     const uint8_t* vm_g = a.v_meta + bh * a.groups_cap * static_cast<long long>(P::VM);
 
-    // group j of this segment goes through ring slot (jg + j) % STAGES
-    auto issue = [&](int j) {
-      const long long grp = g_begin + warp + 4 * j;
-      uint8_t* dst = ring + ((jg + j) % STAGES) * P::STAGE;
-      uint64_t* bb = &bar[(jg + j) % STAGES];
-      mbar_arrive_expect_tx(bb, P::STAGE);
-      bulk_g2s(dst, kc_g + grp * P::KC, P::KC, bb);
-      bulk_g2s(dst + P::KC, km_g + grp * P::KM, P::KM, bb);
-      bulk_g2s(dst + P::KC + P::KM, vc_g + grp * P::VC, P::VC, bb);
-      bulk_g2s(dst + P::KC + P::KM + P::VC, vm_g + grp * P::VM, P::VM, bb);
+    // slot k of this segment (groups GPS*k .. of the warp) goes through ring
+    // position (jg + k) % NS as [key codes x GPS | key meta x GPS | value codes
+    // x GPS | value meta x GPS]
+    auto issue = [&](int k) {
+      const int grp = g_begin + GPS * (warp + 4 * k);
+      const uint32_t cnt = static_cast<uint32_t>(min(GPS, g_end - grp));
+      uint8_t* dst = ring + ((jg + k) % NS) * SLOT;
+      uint64_t* bb = &bar[(jg + k) % NS];
+      mbar_arrive_expect_tx(bb, cnt * P::STAGE);
+      bulk_g2s(dst, kc_g + grp * static_cast<long long>(P::KC), cnt * P::KC, bb);
+      bulk_g2s(dst + GPS * P::KC, km_g + grp * static_cast<long long>(P::KM), cnt * P::KM, bb);
+      bulk_g2s(dst + GPS * (P::KC + P::KM), vc_g + grp * static_cast<long long>(P::VC), cnt * P::VC, bb);
+      bulk_g2s(dst + GPS * (P::KC + P::KM + P::VC), vm_g + grp * static_cast<long long>(P::VM), cnt * P::VM, bb);
     };
-    auto wait_group = [&](int j) { return mbar_wait_bounded(&bar[(jg + j) % STAGES], ((jg + j) / STAGES) & 1); };
-    auto stage = [&](int j) { return ring + ((jg + j) % STAGES) * P::STAGE; };
+    auto wait_slot = [&](int k) { return mbar_wait_bounded(&bar[(jg + k) % NS], ((jg + k) / NS) & 1); };
+    // the records of group j of the warp
+    auto slot_base = [&](int j) { return ring + ((jg + j / GPS) % NS) * SLOT; };
+    auto kc_of = [&](int j) { return slot_base(j) + (j % GPS) * P::KC; };
+    auto km_of = [&](int j) { return slot_base(j) + GPS * P::KC + (j % GPS) * P::KM; };
+    auto vc_of = [&](int j) { return slot_base(j) + GPS * (P::KC + P::KM) + (j % GPS) * P::VC; };
+    auto vm_of = [&](int j) { return slot_base(j) + GPS * (P::KC + P::KM + P::VC) + (j % GPS) * P::VM; };
     if (lane == 0) {
-      for (int j = 0; j < STAGES && j < n_mine; ++j) issue(j);
+      for (int k = 0; k < NS && k < n_slots; ++k) issue(k);
     }
 
     // Query fragments of row g (query head h*gq + g), scaled by 2^-e so that
@@ -580,11 +599,11 @@ __global__ void __launch_bounds__(128, KVQ_DECODE_MIN_BLOCKS) kivi_decode_kernel
     const float p2e = ldexpf(1.0f, e) * a.scale_log2;
     const float mult6 = kInvP6 * p2e, mult8 = kInvP8 * p2e;
 
-    // q . k_hat of the 32 tokens of the group in stage `sp`: 8 scores (log2
+    // q . k_hat of the 32 tokens of group j of the warp: 8 scores (log2
     // units) of this thread's row, tokens 8*nt + 2*tig + {0, 1}.
-    auto qk_scores = [&](const uint8_t* sp, float (&sc)[8]) {
-      const uint4* kcw = reinterpret_cast<const uint4*>(sp);
-      const uint4* kmr = reinterpret_cast<const uint4*>(sp + P::KC);
+    auto qk_scores = [&](int jj, float (&sc)[8]) {
+      const uint4* kcw = reinterpret_cast<const uint4*>(kc_of(jj));
+      const uint4* kmr = reinterpret_cast<const uint4*>(km_of(jj));
       uint32_t kw[P::KW];
 #pragma unroll
       for (int c = 0; c < P::KW / 4; ++c) {
@@ -640,22 +659,20 @@ __global__ void __launch_bounds__(128, KVQ_DECODE_MIN_BLOCKS) kivi_decode_kernel
     int j = 0;
     float sc[8];
     if (n_mine > 0) {
-      if (wait_group(0))
-        qk_scores(stage(0), sc);
+      if (wait_slot(0))
+        qk_scores(0, sc);
       else
         timed_out = true;
     }
     for (; !timed_out && j < n_mine; ++j) {
-      const uint8_t* sp = stage(j);
-      // the next group's stage (this one again past the end: its scores are discarded)
+      // the next group (this one again past the end: its scores are discarded)
       const int jn = (j + 1 < n_mine) ? j + 1 : j;
-      if (jn != j && !wait_group(jn)) {
+      if (jn != j && jn % GPS == 0 && !wait_slot(jn / GPS)) {
         timed_out = true;
         break;
       }
-      const uint8_t* spn = stage(jn);
-      const uint4* vcw = reinterpret_cast<const uint4*>(sp + P::KC + P::KM);
-      const uint4* vmr = reinterpret_cast<const uint4*>(sp + P::KC + P::KM + P::VC);
+      const uint4* vcw = reinterpret_cast<const uint4*>(vc_of(j));
+      const uint4* vmr = reinterpret_cast<const uint4*>(vm_of(j));
 
       float p[8];
       online_softmax<P::NTV>(sc, p, o_acc, m_run, l_run, vz_run);
@@ -679,7 +696,7 @@ __global__ void __launch_bounds__(128, KVQ_DECODE_MIN_BLOCKS) kivi_decode_kernel
       }
 
       // ---- q . k^T of group j + 1 (independent of what follows) ----
-      qk_scores(spn, sc);
+      qk_scores(jn, sc);
 
       // ---- o += p' . codes (group j) ----
       uint32_t vw[P::VW];
@@ -713,11 +730,13 @@ __global__ void __launch_bounds__(128, KVQ_DECODE_MIN_BLOCKS) kivi_decode_kernel
         }
       }
 
-      // release stage j and refill it with the group STAGES ahead
-      __syncwarp();
-      if (lane == 0 && j + STAGES < n_mine) {
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        issue(j + STAGES);
+      // after the last group of its slot: release the slot and refill it NS slots ahead
+      if (j % GPS == GPS - 1 || j + 1 == n_mine) {
+        __syncwarp();
+        if (lane == 0 && j / GPS + NS < n_slots) {
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          issue(j / GPS + NS);
+        }
       }
     }
 
@@ -755,7 +774,7 @@ __global__ void __launch_bounds__(128, KVQ_DECODE_MIN_BLOCKS) kivi_decode_kernel
     if (seg_timeout) {
       if (lane == 0) report_timeout(a.status);
       // let the copies already in flight land before the stages are reused
-      for (int jj = j; jj < n_mine && jj < j + STAGES; ++jj) (void)wait_group(jj);
+      for (int k = j / GPS; k < n_slots && k < j / GPS + NS; ++k) (void)wait_slot(k);
       if (win_pending) (void)mbar_wait_bounded(wbar, wphase);
     }
     if (timed_out) {
@@ -765,7 +784,7 @@ __global__ void __launch_bounds__(128, KVQ_DECODE_MIN_BLOCKS) kivi_decode_kernel
 #pragma unroll
       for (int i = 0; i < P::NTV; ++i) o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.0f;
     }
-    jg += n_mine;
+    jg += n_slots;
     l_run = quad_sum(l_run);
     vz_run = quad_sum(vz_run);
     __syncthreads();  // every warp is done with its stages; the area is reused below
