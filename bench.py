@@ -22,6 +22,7 @@ bounded sample of the same workload.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -42,6 +43,10 @@ sys.path.insert(0, ROOT)
 from quantized_kv_cache_quant_gb300 import metrics, workloads  # noqa: E402
 
 METRIC = "decode-attn KV bytes GB/s (% of GB300 HBM peak); quantize tokens/s"
+# ncu summary of the decode kernel on the default workload; its "traffic-record:"
+# line holds DRAM bytes of one captured launch and a hash of the sources it ran
+DECODE_PROFILE = os.path.join(ROOT, "profiles", "kivi_decode_kernel_128k_stream.md")
+DECODE_SOURCES = ("kivi_kernels.cu", "kvq_device.cuh", "kvq_internal.h", "api.cu")
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -304,7 +309,9 @@ def run_ours(args, world, rank, local):
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm, "unit": "GB/s",
-                     "frac": round(achieved / hbm, 4), "traffic": None,
+                     "frac": round(achieved / hbm, 4),
+                     "traffic": measured_traffic(w.name, statistics.mean(dec_bytes)),
+                     "traffic_unit": "DRAM bytes per launch (ncu capture, scaled to the mean launch)",
                      "kernel": "kivi_decode_kernel<128,2,2,4>", "peak_source": f"{peak_kind} hbm_gbs",
                      "decode_us": round(statistics.mean(dec_times) * 1e6, 2)},
         "device_status": status,
@@ -317,6 +324,33 @@ def run_ours(args, world, rank, local):
 # ---------------------------------------------------------------------------
 # the oracle on the host cores (cpu_baseline and --impl reference)
 # ---------------------------------------------------------------------------
+def decode_sources_sha256():
+    h = hashlib.sha256()
+    for name in DECODE_SOURCES:
+        with open(os.path.join(ROOT, "quantized_kv_cache_quant_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def measured_traffic(workload, mean_alg_bytes):
+    """DRAM read + write bytes per decode launch from the committed ncu capture,
+    scaled from the captured launch's algorithmic bytes to this run's mean. None
+    when the capture is of another workload or of decode sources that have
+    changed since it was taken."""
+    try:
+        with open(DECODE_PROFILE) as f:
+            lines = f.read().splitlines()
+    except OSError:
+        return None
+    for line in lines:
+        if line.startswith("traffic-record:"):
+            rec = json.loads(line.split(":", 1)[1])
+            if rec.get("workload") != workload or rec.get("sources_sha256") != decode_sources_sha256():
+                return None
+            return int(round(rec["dram_bytes"] * mean_alg_bytes / rec["algorithmic_bytes"]))
+    return None
+
+
 def oracle_sample_setup(w):
     """One (batch row 0, kv head 0) of the workload, as a 1 x 1 oracle cache."""
     from oracle import kivi
