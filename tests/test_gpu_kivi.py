@@ -200,6 +200,36 @@ def _sample_heads(b, hq, n, seed):
     return sorted(picks)
 
 
+def test_decode_more_pairs_than_resident_blocks():
+    """1024 (batch row, kv head) pairs, more than the GPU keeps resident: the
+    grid is the stream-K cut, whose blocks each cover two or three pairs (one
+    partial per pair) with odd group counts per segment."""
+    b, hkv, gq, d = 64, 16, 2, 64
+    s = 32 * 37 + 128 - 9                      # 37 groups + 119 window tokens per pair
+    kvq, x, gc, oc = _run(b, hkv, hkv * gq, d, s, seed=21)
+    heads = _sample_heads(b, hkv * gq, 48, 21)
+    out = host(gc.decode(dev(x.q[0])))
+    assert_attention_close(out, oracle_attention(oc, x.q[0], default_scale(d), heads), heads)
+    assert gc.status() == 0
+
+
+@pytest.mark.parametrize("n_resid", [32, 33, 64, 65, 96, 127])
+def test_decode_window_chunk_edges(n_resid):
+    """Window fills at and around the 32-token chunk boundaries, after a flush,
+    with grouped tokens in front."""
+    b, hkv, hq, d = 2, 3, 12, 128
+    s = 32 * 9 + 128                           # 9 groups + a full window
+    kvq, x, gc, oc = _run(b, hkv, hq, d, s, steps=n_resid, seed=31 + n_resid)
+    for step in range(n_resid):                # the first append flushes the full window
+        gc.append(dev(x.k_new[step]), dev(x.v_new[step]))
+        oc.append(x.k_new[step], x.v_new[step])
+    assert (gc.n_grouped, gc.n_resid) == (oc.n_grouped, oc.n_resid) == (32 * 13, n_resid)
+    q = x.q[n_resid - 1]
+    out = host(gc.decode(dev(q)))
+    assert_attention_close(out, oracle_attention(oc, q, default_scale(d)))
+    assert gc.status() == 0
+
+
 @pytest.mark.parametrize("w", [workloads.MHA_4K, workloads.GQA_8K_2BIT, workloads.GQA_8K_4BIT], ids=lambda w: w.name)
 def test_full_size_decode(w):
     kvq = _kvq()
