@@ -80,16 +80,31 @@ __global__ void __launch_bounds__(256) fp8_scale_kernel(const uint32_t* __restri
 // ---------------------------------------------------------------------------
 constexpr int kCastWarps = 8;
 
-template <int D>
-__global__ void __launch_bounds__(32 * kCastWarps) fp8_cast_kernel(Fp8QuantArgs a) {
-  constexpr int RS = D + 8;  // padded row stride (halves): rows start 4 banks apart
-  __shared__ __align__(16) __half xs_all[kCastWarps][kBlock * RS];
+// x / scale, the IEEE fp32 quotient of the formula. MODE 0: the IEEE division
+// itself. MODE 1 and 2: from y = RN(1/scale) and one correction step, which is
+// bit-identical for scales in [2^-96, 2^96]; MODE 1 also passes an infinite x
+// through (a static scale may meet infinities), MODE 2 leaves that test out: a
+// dynamic scale amax / 448 is only that finite when the tensor holds no
+// infinity or NaN (either one makes amax, hence the scale, non-finite).
+template <int MODE>
+__device__ __forceinline__ float scaled(float x, float scale, float y) {
+  if constexpr (MODE == 0) {
+    (void)y;
+    return __fdiv_rn(x, scale);
+  } else if constexpr (MODE == 1) {
+    return div_rn_by_rcp_signed(x, scale, y);
+  } else {
+    return copysignf(div_rn_by_rcp(x, scale, y), x);
+  }
+}
+
+template <int D, int MODE>
+__device__ __forceinline__ void cast_units(const Fp8QuantArgs& a, __half* xs, float scale, float y) {
+  constexpr int RS = D + 8;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __half* xs = xs_all[warp];
   const int gg = lane >> 2, tg = lane & 3;
   const int nb = (a.seq_len + kBlock - 1) / kBlock;
   const long long units = static_cast<long long>(a.batch) * a.kv_heads * nb;
-  const float scale = *a.scale;
   for (long long u = static_cast<long long>(blockIdx.x) * kCastWarps + warp; u < units;
        u += static_cast<long long>(gridDim.x) * kCastWarps) {
     const int j = static_cast<int>(u % nb);
@@ -127,8 +142,8 @@ __global__ void __launch_bounds__(32 * kCastWarps) fp8_cast_kernel(Fp8QuantArgs 
           ch1 = ch0 + 1;
         }
         const bool v0 = tok0 < ntok, v1 = tok1 < ntok;
-        const float y0 = v0 ? __fdiv_rn(__half2float(xs[tok0 * RS + ch0]), scale) : 0.0f;
-        const float y1 = v1 ? __fdiv_rn(__half2float(xs[tok1 * RS + ch1]), scale) : 0.0f;
+        const float y0 = v0 ? scaled<MODE>(__half2float(xs[tok0 * RS + ch0]), scale, y) : 0.0f;
+        const float y1 = v1 ? scaled<MODE>(__half2float(xs[tok1 * RS + ch1]), scale, y) : 0.0f;
         uint32_t pair = f32x2_to_e4m3x2(y0, y1);
         if (!v0) pair &= 0xFF00u;
         if (!v1) pair &= 0x00FFu;
@@ -140,6 +155,20 @@ __global__ void __launch_bounds__(32 * kCastWarps) fp8_cast_kernel(Fp8QuantArgs 
       dst[c * 32 + lane] = make_uint4(out[0], out[1], out[2], out[3]);
     }
   }
+}
+
+template <int D>
+__global__ void __launch_bounds__(32 * kCastWarps) fp8_cast_kernel(Fp8QuantArgs a) {
+  constexpr int RS = D + 8;  // padded row stride (halves): rows start 4 banks apart
+  __shared__ __align__(16) __half xs_all[kCastWarps][kBlock * RS];
+  __half* xs = xs_all[threadIdx.x >> 5];
+  const float scale = *a.scale;
+  if (!(scale >= 0x1p-96f && scale <= 0x1p96f))  // the same for the whole grid
+    cast_units<D, 0>(a, xs, scale, 0.0f);
+  else if (a.static_scale)
+    cast_units<D, 1>(a, xs, scale, __frcp_rn(scale));
+  else
+    cast_units<D, 2>(a, xs, scale, __frcp_rn(scale));
 }
 
 // ---------------------------------------------------------------------------

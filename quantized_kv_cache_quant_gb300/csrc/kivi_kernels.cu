@@ -56,47 +56,21 @@ __device__ __forceinline__ void group_scale_zero(float mn, float mx, float level
   z16 = __float2half_rn(__fadd_rn(mn, 0.0f));  // exact; -0 becomes +0
 }
 
-__device__ __forceinline__ uint32_t group_code(float x, float zf, float sf, float levels) {
-  if (sf == 0.0f) return 0u;
-  const float r = rintf(__fdiv_rn(__fsub_rn(x, zf), sf));
-  return static_cast<uint32_t>(fminf(fmaxf(r, 0.0f), levels));
+// The group formula's code clamp(rint(fl32((x - z) / s)), 0, levels). The
+// quotient comes from rcp = RN(1/s) and one correction step, bit-identical to
+// the IEEE division here (x, z and s are fp16 values, so nothing under- or
+// overflows; s = 0 has rcp = 0 and gives code 0 as the formula does), and
+// rint + clamp are one round-to-nearest-even conversion (x >= z: no negative
+// quotients) and a min.
+__device__ __forceinline__ uint32_t group_code(float x, float zf, float sf, float rcp, uint32_t levels) {
+  return min(__float2uint_rn(div_rn_by_rcp(__fsub_rn(x, zf), sf, rcp)), levels);
 }
 
-// The same code with the quotient taken as d * rcp, rcp = RN(1/s) (0 when
-// s == 0, which gives code 0 as the formula does). With rcp = RN(1/s),
-// |q - d/s| <= 2^-23 |d/s| + tiny and |fl32(d/s) - d/s| <= 2^-24 |d/s|, so for
-// |d/s| <= 16 the two quotients differ by less than 2^-18: rint gives the same
-// integer unless q lies within 2^-17 of a half-integer (a tie or a near-tie).
-// Such an element raises `near`, and the caller recomputes its word with the
-// IEEE division. Quotients above 16 only matter through the clamp, which the
-// same test protects at its boundary levels + 1/2.
-__device__ __forceinline__ uint32_t group_code_fast(float x, float zf, float rcp, float levels, bool& near) {
-  const float q = __fmul_rn(__fsub_rn(x, zf), rcp);
-  const float r = rintf(q);
-  near |= fabsf(fabsf(__fsub_rn(q, r)) - 0.5f) < 7.62939453125e-06f;
-  return static_cast<uint32_t>(fminf(fmaxf(r, 0.0f), levels));
-}
-
-// One packed code word of a group. EXACT = false: reciprocal fast path (sets
-// `near`); EXACT = true: every code by the IEEE division.
-template <bool EXACT>
-struct CodeOf {
-  __device__ __forceinline__ static uint32_t get(float x, float z, float s, float rcp, float levels, bool& near) {
-    if constexpr (EXACT) {
-      (void)rcp;
-      (void)near;
-      return group_code(x, z, s, levels);
-    } else {
-      (void)s;
-      return group_code_fast(x, z, rcp, levels, near);
-    }
-  }
-};
-
-template <int D, int KB, bool EXACT>
+// One packed code word of a group (storage word u of lane (gg, tg)).
+template <int D, int KB>
 __device__ __forceinline__ uint32_t key_word(const __half* xk, int RS, const float* sk, const float* zk,
-                                             const float* rk, int u, int gg, int tg, bool& near) {
-  constexpr float KL = static_cast<float>((1 << KB) - 1);
+                                             const float* rk, int u, int gg, int tg) {
+  constexpr uint32_t KL = (1u << KB) - 1u;
   uint32_t w = 0;
 #pragma unroll
   for (int rr = 0; rr < (KB == 2 ? 2 : 1); ++rr) {
@@ -108,17 +82,16 @@ __device__ __forceinline__ uint32_t key_word(const __half* xk, int RS, const flo
     for (int nt = 0; nt < 4; ++nt) {
       const float2 x = __half22float2(reinterpret_cast<const __half2*>(xk)[(8 * nt + gg) * (RS / 2) + d0 / 2]);
       const int f = (KB == 2) ? 4 * r + nt : nt;
-      w |= (CodeOf<EXACT>::get(x.x, z0, s0, r0, KL, near) << (KB * f)) |
-           (CodeOf<EXACT>::get(x.y, z1, s1, r1, KL, near) << (16 + KB * f));
+      w |= (group_code(x.x, z0, s0, r0, KL) << (KB * f)) | (group_code(x.y, z1, s1, r1, KL) << (16 + KB * f));
     }
   }
   return w;
 }
 
-template <int D, int VB, bool EXACT>
+template <int D, int VB>
 __device__ __forceinline__ uint32_t value_word(const __half* xv, int RS, const float* sv, const float* zv,
-                                               const float* rv, int u, int gg, int tg, bool& near) {
-  constexpr float VL = static_cast<float>((1 << VB) - 1);
+                                               const float* rv, int u, int gg, int tg) {
+  constexpr uint32_t VL = (1u << VB) - 1u;
   constexpr int NQ = D / 32;
   uint32_t w = 0;
 #pragma unroll
@@ -133,25 +106,10 @@ __device__ __forceinline__ uint32_t value_word(const __half* xv, int RS, const f
       const int ch = 8 * (4 * q + n) + gg;
       const float x0 = __half2float(xv[t0 * RS + ch]), x1 = __half2float(xv[(t0 + 1) * RS + ch]);
       const int f = (VB == 2) ? 4 * r + n : n;
-      w |= (CodeOf<EXACT>::get(x0, z0, s0, r0, VL, near) << (VB * f)) |
-           (CodeOf<EXACT>::get(x1, z1, s1, r1, VL, near) << (16 + VB * f));
+      w |= (group_code(x0, z0, s0, r0, VL) << (VB * f)) | (group_code(x1, z1, s1, r1, VL) << (16 + VB * f));
     }
   }
   return w;
-}
-
-template <int D, int KB>
-__device__ __noinline__ uint32_t key_word_exact(const __half* xk, int RS, const float* sk, const float* zk,
-                                                const float* rk, int u, int gg, int tg) {
-  bool unused = false;
-  return key_word<D, KB, true>(xk, RS, sk, zk, rk, u, gg, tg, unused);
-}
-
-template <int D, int VB>
-__device__ __noinline__ uint32_t value_word_exact(const __half* xv, int RS, const float* sv, const float* zv,
-                                                  const float* rv, int u, int gg, int tg) {
-  bool unused = false;
-  return value_word<D, VB, true>(xv, RS, sv, zv, rv, u, gg, tg, unused);
 }
 
 template <int D, int KB, int VB>
@@ -236,20 +194,14 @@ __global__ void __launch_bounds__(128) kivi_quantize_kernel(QuantGroupsArgs a) {
   uint32_t* kdst = reinterpret_cast<uint32_t*>(a.k_codes + grp_index * P::KC);
   for (int j = tid; j < 32 * P::KW; j += 128) {
     const int L = (j % 128) / 4, u = (j / 128) * 4 + (j % 4);
-    bool near = false;
-    uint32_t w = key_word<D, KB, false>(xk, RS, sk, zk, rk, u, L >> 2, L & 3, near);
-    if (near) w = key_word_exact<D, KB>(xk, RS, sk, zk, rk, u, L >> 2, L & 3);
-    kdst[j] = w;
+    kdst[j] = key_word<D, KB>(xk, RS, sk, zk, rk, u, L >> 2, L & 3);
   }
 
   // Value code words.
   uint32_t* vdst = reinterpret_cast<uint32_t*>(a.v_codes + grp_index * P::VC);
   for (int j = tid; j < 32 * P::VW; j += 128) {
     const int L = (j % 128) / 4, u = (j / 128) * 4 + (j % 4);
-    bool near = false;
-    uint32_t w = value_word<D, VB, false>(xv, RS, sv, zv, rv, u, L >> 2, L & 3, near);
-    if (near) w = value_word_exact<D, VB>(xv, RS, sv, zv, rv, u, L >> 2, L & 3);
-    vdst[j] = w;
+    vdst[j] = value_word<D, VB>(xv, RS, sv, zv, rv, u, L >> 2, L & 3);
   }
 
   // Key meta: record ks*4 + tig = {s[d0], s[d0+1], s[d0+8], s[d0+9], z[...]}.

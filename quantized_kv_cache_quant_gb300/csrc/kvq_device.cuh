@@ -109,6 +109,28 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], const void* row)
                : "memory");
 }
 
+// The correctly rounded fp32 quotient d / s from y = RN(1/s), by Markstein's
+// correction step (P. Markstein, "Computation of elementary functions on the
+// IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990; Handbook of
+// Floating-Point Arithmetic, the chapter on division with an FMA): q0 =
+// RN(d * y) is within an ulp of d / s, the residual r = d - s * q0 is exact
+// with an FMA, and RN(q0 + r * y) = RN(d / s) as long as d, s and the quotient
+// are normal or zero (no underflow or overflow). s = 0 with y = 0 gives 0. A
+// zero numerator gives +0: the IEEE quotient of -0 is -0, so a caller that
+// keeps the sign of zero restores it (div_rn_by_rcp_signed).
+__device__ __forceinline__ float div_rn_by_rcp(float d, float s, float y) {
+  const float q0 = __fmul_rn(d, y);
+  const float r = __fmaf_rn(-q0, s, d);
+  return __fmaf_rn(r, y, q0);
+}
+// The same for s > 0 with the IEEE results at the numerator's special values:
+// the sign of a zero numerator kept (for s > 0 the quotient has the
+// numerator's sign, so the copy changes nothing else) and an infinite
+// numerator returned as is (the correction step would turn it into a NaN).
+__device__ __forceinline__ float div_rn_by_rcp_signed(float d, float s, float y) {
+  return isinf(d) ? d : copysignf(div_rn_by_rcp(d, s, y), d);
+}
+
 // c + a.lo * b.lo + a.hi * b.hi with fp16 halves and an fp32 accumulator
 // (the fp16 products are exact in fp32; each add rounds once).
 __device__ __forceinline__ float dot2_f16_f32(uint32_t a, uint32_t b, float c) {

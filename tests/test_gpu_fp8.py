@@ -52,6 +52,21 @@ def test_all_fp16_values_cast_exactly():
         assert np.array_equal(host(pool), want)
 
 
+@pytest.mark.parametrize("special", [np.inf, -np.inf, np.nan])
+def test_dynamic_scale_with_non_finite_values(special):
+    """An infinity or NaN makes amax, hence the dynamic scale, non-finite; the
+    cast then follows the formula with that scale (finite values go to zero,
+    the special value to its saturated or NaN byte)."""
+    x = workloads.make_inputs(1, 2, 4, 128, 32, 1, 5).k.copy()
+    x[0, 1, 7, 33] = special
+    table = np.arange(2, dtype=np.int32).reshape(1, 2)
+    pool, scale = _quantize(x, table, 2, 0)
+    s_ref = fp8.dynamic_scale(x)
+    got_s = host(scale)[0]
+    assert (np.isnan(got_s) and np.isnan(s_ref)) or got_s == s_ref
+    assert np.array_equal(host(pool), _oracle_pool(x, table, 2, 0, s_ref))
+
+
 @pytest.mark.parametrize("d", [64, 128])
 def test_dynamic_scale_and_bytes(d):
     rng = np.random.default_rng(d)
