@@ -72,13 +72,24 @@ __global__ void __launch_bounds__(256) fp8_scale_kernel(const uint32_t* __restri
 }
 
 // ---------------------------------------------------------------------------
-// Cast + scatter: each warp takes one (b, h, logical block) unit at a time,
-// stages its 16 x D fp16 values in its own shared-memory slice (16-byte
-// streaming loads), then every lane writes its D/32 16-byte chunks of the
-// fragment-ordered block (chunk c of lane l at byte (c*32 + l)*16, so each
-// store instruction of the warp covers 512 contiguous bytes).
+// Cast + scatter: each warp takes (b, h, logical block) units in turn and
+// stages each unit's 16 x D fp16 values in one of its two shared-memory
+// buffers with 16-byte asynchronous copies issued one unit ahead, so the
+// loads of the next unit are in flight while this one is converted. Every
+// lane then writes its D/32 16-byte chunks of the fragment-ordered block
+// (chunk c of lane l at byte (c*32 + l)*16, so each store instruction of the
+// warp covers 512 contiguous bytes).
 // ---------------------------------------------------------------------------
-constexpr int kCastWarps = 8;
+constexpr int kCastWarps = 4;
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// wait until at most one group (the newest) of this thread's copies is in flight
+__device__ __forceinline__ void cp_async_wait_all_but_newest() {
+  asm volatile("cp.async.wait_group 1;" ::: "memory");
+}
 
 // x / scale, the IEEE fp32 quotient of the formula. MODE 0: the IEEE division
 // itself. MODE 1 and 2: from y = RN(1/scale) and one correction step, which is
@@ -99,76 +110,106 @@ __device__ __forceinline__ float scaled(float x, float scale, float y) {
 }
 
 template <int D, int MODE>
-__device__ __forceinline__ void cast_units(const Fp8QuantArgs& a, __half* xs, float scale, float y) {
-  constexpr int RS = D + 8;
+__device__ __forceinline__ void cast_units(const Fp8QuantArgs& a, __half* bufs, float scale, float y) {
+  constexpr int RS = D + 8;  // padded row stride (halves): rows start 4 banks apart
+  constexpr int BUF = kBlock * RS;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gg = lane >> 2, tg = lane & 3;
   const int nb = (a.seq_len + kBlock - 1) / kBlock;
   const long long units = static_cast<long long>(a.batch) * a.kv_heads * nb;
-  for (long long u = static_cast<long long>(blockIdx.x) * kCastWarps + warp; u < units;
-       u += static_cast<long long>(gridDim.x) * kCastWarps) {
+  const long long stride = static_cast<long long>(gridDim.x) * kCastWarps;
+
+  // Start staging unit u into buffer k (one commit group per call, empty when
+  // the unit is skipped); returns its physical block, or -1 to skip it.
+  auto stage = [&](long long u, int k) -> int {
     const int j = static_cast<int>(u % nb);
     const long long bh = u / nb;
-    const int b = static_cast<int>(bh / a.kv_heads), h = static_cast<int>(bh % a.kv_heads);
-    const int t0 = j * kBlock;
-    const int ntok = min(kBlock, a.seq_len - t0);
+    const int b = static_cast<int>(bh / a.kv_heads);
     const int blk = a.block_table[static_cast<long long>(b) * a.max_blocks + j];
-    if (blk < 0 || blk >= a.num_blocks) continue;  // uniform per warp: no write outside the pool
-    const uint4* src = reinterpret_cast<const uint4*>(a.x + (bh * a.seq_len + t0) * static_cast<long long>(D));
-    __syncwarp();  // the previous unit's readers are done with xs
+    if (blk >= 0 && blk < a.num_blocks) {  // uniform per warp: no write outside the pool
+      const int t0 = j * kBlock, ntok = min(kBlock, a.seq_len - t0);
+      const uint4* src = reinterpret_cast<const uint4*>(a.x + (bh * a.seq_len + t0) * static_cast<long long>(D));
+      __half* dst = bufs + k * BUF;
 #pragma unroll
-    for (int i = lane; i < kBlock * D / 8; i += 32) {
-      const int tok = i / (D / 8), c8 = i % (D / 8);
-      *reinterpret_cast<uint4*>(xs + tok * RS + 8 * c8) = (tok < ntok) ? __ldcs(src + i) : make_uint4(0u, 0u, 0u, 0u);
-    }
-    __syncwarp();
-    uint4* dst = reinterpret_cast<uint4*>(a.pool + (static_cast<long long>(blk) * a.kv_heads + h) * (kBlock * D));
-#pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
-      uint32_t out[4];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int i = 8 * c + k;  // byte pair index in the lane's stream
-        int tok0, ch0, tok1, ch1;
-        if (a.value_layout) {
-          const int nt = i >> 1, r = i & 1;
-          tok0 = 8 * r + 2 * tg;
-          tok1 = tok0 + 1;
-          ch0 = ch1 = 8 * nt + gg;
-        } else {
-          const int nt = i / (D / 8), rem = i % (D / 8), ks = rem >> 1, r = rem & 1;
-          tok0 = tok1 = 8 * nt + gg;
-          ch0 = 16 * ks + 8 * r + 2 * tg;
-          ch1 = ch0 + 1;
-        }
-        const bool v0 = tok0 < ntok, v1 = tok1 < ntok;
-        const float y0 = v0 ? scaled<MODE>(__half2float(xs[tok0 * RS + ch0]), scale, y) : 0.0f;
-        const float y1 = v1 ? scaled<MODE>(__half2float(xs[tok1 * RS + ch1]), scale, y) : 0.0f;
-        uint32_t pair = f32x2_to_e4m3x2(y0, y1);
-        if (!v0) pair &= 0xFF00u;
-        if (!v1) pair &= 0x00FFu;
-        if (k & 1)
-          out[k >> 1] |= pair << 16;
+      for (int i = lane; i < kBlock * D / 8; i += 32) {
+        const int tok = i / (D / 8), c8 = i % (D / 8);
+        if (tok < ntok)
+          cp_async16(dst + tok * RS + 8 * c8, src + i);
         else
-          out[k >> 1] = pair;
+          *reinterpret_cast<uint4*>(dst + tok * RS + 8 * c8) = make_uint4(0u, 0u, 0u, 0u);
       }
-      dst[c * 32 + lane] = make_uint4(out[0], out[1], out[2], out[3]);
     }
+    cp_async_commit();
+    return (blk >= 0 && blk < a.num_blocks) ? blk : -1;
+  };
+
+  long long u = static_cast<long long>(blockIdx.x) * kCastWarps + warp;
+  int k = 0;
+  int blk_of[2] = {-1, -1};
+  if (u < units) blk_of[0] = stage(u, 0);
+  for (; u < units; u += stride, k ^= 1) {
+    // the other buffer was read in the previous iteration (ended with a __syncwarp)
+    if (u + stride < units)
+      blk_of[k ^ 1] = stage(u + stride, k ^ 1);
+    else
+      cp_async_commit();
+    cp_async_wait_all_but_newest();
+    __syncwarp();  // every lane's copies of this unit have landed
+    const int blk = blk_of[k];
+    if (blk >= 0) {
+      const __half* xs = bufs + k * BUF;
+      const int j = static_cast<int>(u % nb);
+      const int h = static_cast<int>((u / nb) % a.kv_heads);
+      const int ntok = min(kBlock, a.seq_len - j * kBlock);
+      uint4* dst = reinterpret_cast<uint4*>(a.pool + (static_cast<long long>(blk) * a.kv_heads + h) * (kBlock * D));
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t out[4];
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const int i = 8 * c + kk;  // byte pair index in the lane's stream
+          int tok0, ch0, tok1, ch1;
+          if (a.value_layout) {
+            const int nt = i >> 1, r = i & 1;
+            tok0 = 8 * r + 2 * tg;
+            tok1 = tok0 + 1;
+            ch0 = ch1 = 8 * nt + gg;
+          } else {
+            const int nt = i / (D / 8), rem = i % (D / 8), ks = rem >> 1, r = rem & 1;
+            tok0 = tok1 = 8 * nt + gg;
+            ch0 = 16 * ks + 8 * r + 2 * tg;
+            ch1 = ch0 + 1;
+          }
+          const bool v0 = tok0 < ntok, v1 = tok1 < ntok;
+          const float y0 = v0 ? scaled<MODE>(__half2float(xs[tok0 * RS + ch0]), scale, y) : 0.0f;
+          const float y1 = v1 ? scaled<MODE>(__half2float(xs[tok1 * RS + ch1]), scale, y) : 0.0f;
+          uint32_t pair = f32x2_to_e4m3x2(y0, y1);
+          if (!v0) pair &= 0xFF00u;
+          if (!v1) pair &= 0x00FFu;
+          if (kk & 1)
+            out[kk >> 1] |= pair << 16;
+          else
+            out[kk >> 1] = pair;
+        }
+        dst[c * 32 + lane] = make_uint4(out[0], out[1], out[2], out[3]);
+      }
+    }
+    __syncwarp();  // this buffer is refilled next iteration
   }
+  asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 template <int D>
 __global__ void __launch_bounds__(32 * kCastWarps) fp8_cast_kernel(Fp8QuantArgs a) {
-  constexpr int RS = D + 8;  // padded row stride (halves): rows start 4 banks apart
-  __shared__ __align__(16) __half xs_all[kCastWarps][kBlock * RS];
-  __half* xs = xs_all[threadIdx.x >> 5];
+  __shared__ __align__(16) __half bufs[kCastWarps][2 * kBlock * (D + 8)];
+  __half* mine = bufs[threadIdx.x >> 5];
   const float scale = *a.scale;
   if (!(scale >= 0x1p-96f && scale <= 0x1p96f))  // the same for the whole grid
-    cast_units<D, 0>(a, xs, scale, 0.0f);
+    cast_units<D, 0>(a, mine, scale, 0.0f);
   else if (a.static_scale)
-    cast_units<D, 1>(a, xs, scale, __frcp_rn(scale));
+    cast_units<D, 1>(a, mine, scale, __frcp_rn(scale));
   else
-    cast_units<D, 2>(a, xs, scale, __frcp_rn(scale));
+    cast_units<D, 2>(a, mine, scale, __frcp_rn(scale));
 }
 
 // ---------------------------------------------------------------------------
@@ -402,6 +443,23 @@ int fp8_occupancy() {
 
 int fp8_decode_blocks_per_sm(int head_dim) { return head_dim == 64 ? fp8_occupancy<64>() : fp8_occupancy<128>(); }
 
+// Resident cast blocks per SM (the grid holds exactly that many: every warp
+// then strides over the units with its copies one unit ahead).
+int cast_blocks_per_sm(int head_dim) {
+  static int cached[64][2] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 4;
+  const int i = head_dim == 128 ? 1 : 0;
+  if (cached[dev][i] == 0) {
+    int n = 0;
+    const cudaError_t e = head_dim == 128
+                              ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fp8_cast_kernel<128>, 32 * kCastWarps, 0)
+                              : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fp8_cast_kernel<64>, 32 * kCastWarps, 0);
+    cached[dev][i] = (e == cudaSuccess && n > 0) ? n : 4;
+  }
+  return cached[dev][i];
+}
+
 cudaError_t launch_fp8_quantize(const Fp8QuantArgs& a, cudaStream_t s) {
   if (!a.static_scale) {
     const long long n_vec = static_cast<long long>(a.batch) * a.kv_heads * a.seq_len * a.head_dim / 8;
@@ -415,7 +473,8 @@ cudaError_t launch_fp8_quantize(const Fp8QuantArgs& a, cudaStream_t s) {
   const int nb = (a.seq_len + kBlock - 1) / kBlock;
   const long long units = static_cast<long long>(a.batch) * a.kv_heads * nb;
   const long long want = (units + kCastWarps - 1) / kCastWarps;
-  const int grid = static_cast<int>(want < 8LL * device_sm_count() ? want : 8LL * device_sm_count());
+  const long long full = static_cast<long long>(cast_blocks_per_sm(a.head_dim)) * device_sm_count();
+  const int grid = static_cast<int>(want < full ? want : full);
   if (a.head_dim == 128)
     fp8_cast_kernel<128><<<grid, 32 * kCastWarps, 0, s>>>(a);
   else if (a.head_dim == 64)
