@@ -160,29 +160,32 @@ __global__ void __launch_bounds__(128) kivi_quantize_kernel(QuantGroupsArgs a) {
       skb[c] = __half_as_ushort(s16);
       zkb[c] = __half_as_ushort(z16);
     }
-  } else {
-    // values: one token per warp step over the remaining warps, warp-shuffle min/max
-    const int nw = 4 - (D / 2) / 32;         // warps left after the key channels
-    const int w = warp - (4 - nw);
-    for (int t = w; t < 32; t += nw) {
-      float mn = FLT_MAX, mx = -FLT_MAX;
-#pragma unroll
-      for (int j = 0; j < D / 32; ++j) {
-        const float x = __half2float(xv[t * RS + lane + 32 * j]);
-        mn = fminf(mn, x);
-        mx = fmaxf(mx, x);
-      }
-      mn = warp_min(mn);
-      mx = warp_max(mx);
-      if (lane == 0) {
-        __half s16, z16;
-        group_scale_zero(mn, mx, VL, s16, z16);
-        sv[t] = __half2float(s16);
-        zv[t] = __half2float(z16);
-        rv[t] = (__half2float(s16) == 0.0f) ? 0.0f : __frcp_rn(__half2float(s16));
-        svb[t] = __half_as_ushort(s16);
-        zvb[t] = __half_as_ushort(z16);
-      }
+  } else if (warp >= 2) {
+    // values: warps 2 and 3, two lanes per token, each over half of the row
+    // with fp16 pair min/max; lane L reads its words in the order (c + L) mod
+    // (D / 4), which keeps every shared-memory read conflict-free at D = 128
+    constexpr int W2 = D / 4;                 // half2 words per lane
+    const int t = 16 * (warp - 2) + (lane & 15), hh = lane >> 4;
+    const __half2* row = reinterpret_cast<const __half2*>(xv) + t * (RS / 2) + hh * W2;
+    __half2 mn = row[lane & (W2 - 1)], mx = mn;
+#pragma unroll 8
+    for (int c = 1; c < W2; ++c) {
+      const __half2 v = row[(c + lane) & (W2 - 1)];
+      mn = __hmin2(mn, v);
+      mx = __hmax2(mx, v);
+    }
+    const float2 mnf2 = __half22float2(mn), mxf2 = __half22float2(mx);
+    float mnf = fminf(mnf2.x, mnf2.y), mxf = fmaxf(mxf2.x, mxf2.y);
+    mnf = fminf(mnf, __shfl_xor_sync(0xffffffffu, mnf, 16));
+    mxf = fmaxf(mxf, __shfl_xor_sync(0xffffffffu, mxf, 16));
+    if (hh == 0) {
+      __half s16, z16;
+      group_scale_zero(mnf, mxf, VL, s16, z16);
+      sv[t] = __half2float(s16);
+      zv[t] = __half2float(z16);
+      rv[t] = (__half2float(s16) == 0.0f) ? 0.0f : __frcp_rn(__half2float(s16));
+      svb[t] = __half_as_ushort(s16);
+      zvb[t] = __half_as_ushort(z16);
     }
   }
   __syncthreads();
