@@ -77,7 +77,9 @@ __device__ __forceinline__ uint32_t key_word(const __half* xk, int RS, const flo
     const int ks = (KB == 2) ? u : (u >> 1);
     const int r = (KB == 2) ? rr : (u & 1);
     const int d0 = 16 * ks + 8 * r + 2 * tg;
-    const float s0 = sk[d0], s1 = sk[d0 + 1], z0 = zk[d0], z1 = zk[d0 + 1], r0 = rk[d0], r1 = rk[d0 + 1];
+    const float2 s01 = *reinterpret_cast<const float2*>(sk + d0), z01 = *reinterpret_cast<const float2*>(zk + d0),
+                 r01 = *reinterpret_cast<const float2*>(rk + d0);
+    const float s0 = s01.x, s1 = s01.y, z0 = z01.x, z1 = z01.y, r0 = r01.x, r1 = r01.y;
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt) {
       const float2 x = __half22float2(reinterpret_cast<const __half2*>(xk)[(8 * nt + gg) * (RS / 2) + d0 / 2]);
@@ -100,7 +102,9 @@ __device__ __forceinline__ uint32_t value_word(const __half* xv, int RS, const f
     const int r = (VB == 2) ? rr : (u / NQ) % 2;
     const int q = u % NQ;
     const int t0 = 16 * ks + 8 * r + 2 * tg;
-    const float s0 = sv[t0], s1 = sv[t0 + 1], z0 = zv[t0], z1 = zv[t0 + 1], r0 = rv[t0], r1 = rv[t0 + 1];
+    const float2 s01 = *reinterpret_cast<const float2*>(sv + t0), z01 = *reinterpret_cast<const float2*>(zv + t0),
+                 r01 = *reinterpret_cast<const float2*>(rv + t0);
+    const float s0 = s01.x, s1 = s01.y, z0 = z01.x, z1 = z01.y, r0 = r01.x, r1 = r01.y;
 #pragma unroll
     for (int n = 0; n < 4; ++n) {
       const int ch = 8 * (4 * q + n) + gg;
@@ -118,7 +122,13 @@ __global__ void __launch_bounds__(128) kivi_quantize_kernel(QuantGroupsArgs a) {
   constexpr int RS = D + 8;  // padded row stride (halves): rows start 4 banks apart
   __shared__ __align__(16) __half xk[32 * RS];
   __shared__ __align__(16) __half xv[32 * RS];
-  __shared__ float sk[D], zk[D], rk[D], sv[32], zv[32], rv[32];  // scale, zero, RN(1/scale)
+  // scale, zero, RN(1/scale) per key channel and per value token (8-byte aligned: read in pairs)
+  __shared__ __align__(8) float sk[D];
+  __shared__ __align__(8) float zk[D];
+  __shared__ __align__(8) float rk[D];
+  __shared__ __align__(8) float sv[32];
+  __shared__ __align__(8) float zv[32];
+  __shared__ __align__(8) float rv[32];
   __shared__ uint16_t skb[D], zkb[D], svb[32], zvb[32];           // fp16 bits of scale and zero
 
   const int grp = blockIdx.x, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
@@ -192,19 +202,32 @@ __global__ void __launch_bounds__(128) kivi_quantize_kernel(QuantGroupsArgs a) {
 
   const long long grp_index = bh * a.groups_cap + a.dst_group0 + grp;
 
-  // Key code words, computed straight from the staged tile. Storage word j
-  // belongs to lane (j%128)/4, word u = 4*(j/128) + j%4.
-  uint32_t* kdst = reinterpret_cast<uint32_t*>(a.k_codes + grp_index * P::KC);
-  for (int j = tid; j < 32 * P::KW; j += 128) {
-    const int L = (j % 128) / 4, u = (j / 128) * 4 + (j % 4);
-    kdst[j] = key_word<D, KB>(xk, RS, sk, zk, rk, u, L >> 2, L & 3);
-  }
-
-  // Value code words.
-  uint32_t* vdst = reinterpret_cast<uint32_t*>(a.v_codes + grp_index * P::VC);
-  for (int j = tid; j < 32 * P::VW; j += 128) {
-    const int L = (j % 128) / 4, u = (j / 128) * 4 + (j % 4);
-    vdst[j] = value_word<D, VB>(xv, RS, sv, zv, rv, u, L >> 2, L & 3);
+  // Code words, computed straight from the staged tile: warps 0-1 the key
+  // words, warps 2-3 the value words. Storage words 4*ug .. 4*ug + 3 of
+  // fragment lane L are one 16-byte chunk (uint4 ug*32 + L); lane L of a warp
+  // computes that chunk, so each shared-memory load of the warp has all 32
+  // fragment lanes on the same word (conflict-free) and each store writes 512
+  // contiguous bytes.
+  if (warp < 2) {
+    uint4* kdst = reinterpret_cast<uint4*>(a.k_codes + grp_index * P::KC);
+    for (int ug = warp; ug < P::KW / 4; ug += 2) {
+      uint4 w;
+      w.x = key_word<D, KB>(xk, RS, sk, zk, rk, 4 * ug, lane >> 2, lane & 3);
+      w.y = key_word<D, KB>(xk, RS, sk, zk, rk, 4 * ug + 1, lane >> 2, lane & 3);
+      w.z = key_word<D, KB>(xk, RS, sk, zk, rk, 4 * ug + 2, lane >> 2, lane & 3);
+      w.w = key_word<D, KB>(xk, RS, sk, zk, rk, 4 * ug + 3, lane >> 2, lane & 3);
+      kdst[ug * 32 + lane] = w;
+    }
+  } else {
+    uint4* vdst = reinterpret_cast<uint4*>(a.v_codes + grp_index * P::VC);
+    for (int ug = warp - 2; ug < P::VW / 4; ug += 2) {
+      uint4 w;
+      w.x = value_word<D, VB>(xv, RS, sv, zv, rv, 4 * ug, lane >> 2, lane & 3);
+      w.y = value_word<D, VB>(xv, RS, sv, zv, rv, 4 * ug + 1, lane >> 2, lane & 3);
+      w.z = value_word<D, VB>(xv, RS, sv, zv, rv, 4 * ug + 2, lane >> 2, lane & 3);
+      w.w = value_word<D, VB>(xv, RS, sv, zv, rv, 4 * ug + 3, lane >> 2, lane & 3);
+      vdst[ug * 32 + lane] = w;
+    }
   }
 
   // Key meta: record ks*4 + tig = {s[d0], s[d0+1], s[d0+8], s[d0+9], z[...]}.
