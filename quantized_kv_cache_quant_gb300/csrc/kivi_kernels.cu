@@ -256,6 +256,9 @@ __global__ void __launch_bounds__(128) kivi_quantize_kernel(QuantGroupsArgs a) {
 // Token copies (fill the fp16 window, append a decode token, move a remainder)
 // ---------------------------------------------------------------------------
 __global__ void copy_tokens_kernel(CopyTokensArgs a) {
+  // A decode launched right after this copy may start now: it reads what this
+  // kernel writes (the fp16 window) only after its griddepcontrol.wait.
+  asm volatile("griddepcontrol.launch_dependents;");
   const int vec_per_tok = a.head_dim / 8;
   const long long per_bh = static_cast<long long>(a.n_tokens) * vec_per_tok;
   const long long total = per_bh * a.bh;
@@ -733,6 +736,7 @@ __global__ void __launch_bounds__(128, KVQ_DECODE_MIN_BLOCKS) kivi_decode_kernel
 #pragma unroll
       for (int ks = 0; ks < P::KS; ++ks) q_io[ks][0] = qs[ks][0], q_io[ks][1] = qs[ks][1];
       uint32_t ph = wphase;
+      asm volatile("griddepcontrol.wait;" ::: "memory");  // the window is complete (see decode_dispatch)
       const bool ok = window_chunks<D, VB>(a.k_res, a.v_res, bh * a.res_cap, a.n_resid, c_begin + warp, c_end, ring,
                                            S::WIN_ROW, wbar, ph, q_io, p2e, o_io, st[0], st[1], st[2]);
 #pragma unroll
@@ -778,6 +782,8 @@ __global__ void __launch_bounds__(128, KVQ_DECODE_MIN_BLOCKS) kivi_decode_kernel
       l_s[warp * 8 + g] = l_run;
     }
 
+    // the kernel before this one has finished before any workspace write (see decode_dispatch)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     __syncthreads();
     finish_split<D>(o_s, m_s, l_s, gq, static_cast<long long>(b) * a.q_heads + h * gq, split, n_splits,
                     a.part_stride, a.part_o, a.part_ml, a.counters + bh, a.out, a.out_fp32);
@@ -810,14 +816,31 @@ int decode_occupancy() {
   return cached[dev];
 }
 
+// The decode is launched as a programmatic dependent of the kernel before it
+// on the stream. Only the token copy of kv_append_token (and of the window
+// fill) lets its dependent start early; every other kernel releases it at its
+// end as usual. So the decode's grouped loop, which reads only group records
+// and q (complete before that copy started), overlaps the copy, while the
+// fp16 window and the workspace (partials, split counters, shared with the
+// previous decode) are touched only after griddepcontrol.wait, i.e. after the
+// preceding kernel has completed.
 template <int D, int KB, int VB>
 cudaError_t decode_dispatch(const KiviDecodeArgs& a, cudaStream_t s) {
   constexpr int smem = DecodeSmem<D, KB, VB, kDecodeStages>::BYTES;
   auto kern = kivi_decode_kernel<D, KB, VB, kDecodeStages>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<a.n_blocks, 128, smem, s>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(a.n_blocks));
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 }  // namespace
