@@ -115,7 +115,7 @@ typedef struct {
  *     values: tokens t0 = 16*ks + 8*r + 2*tig and t0+1 of channel 8*nt + g
  *             (nt < D/8, ks < 2).
  *   With NQ = 1 (keys) or D/32 (values):
- *     2 bits: word u = ks*NQ + nt/4, field f = 4*r + nt%4 at bits [2f, 2f+2);
+ *     2 bits: word u = ks*NQ + nt/4, field f = (4*r + nt%4 + 1) mod 8 at bits [2f, 2f+2);
  *     4 bits: word u = (2*ks + r)*NQ + nt/4, field f = nt%4 at bits [4f, 4f+4).
  *   Word u of a lane is stored at 32-bit index (u/4)*128 + lane*4 + u%4.
  *   (These are the operand fragments of the mma.sync m16n8k16 tensor-core

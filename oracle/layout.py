@@ -28,8 +28,9 @@ pair ``(ks, r, nt)``:
 
 With ``NQ`` = 1 for keys and D/32 for values:
 
-* 2 bits: word ``u = ks*NQ + nt//4``, field ``f = 4*r + nt%4`` at bits
-  ``[2f, 2f+2)`` of each half;
+* 2 bits: word ``u = ks*NQ + nt//4``, field ``f = (4*r + nt%4 + 1) mod 8`` at
+  bits ``[2f, 2f+2)`` of each half (the order in which the unshifted word,
+  its shifts by 4 either way and its per-half byte swap expose the fields);
 * 4 bits: word ``u = (2*ks + r)*NQ + nt//4``, field ``f = nt%4`` at bits
   ``[4f, 4f+4)`` of each half.
 
@@ -69,7 +70,7 @@ def pack_key_codes(codes: np.ndarray, bits: int) -> np.ndarray:
                 for nt in range(4):
                     tok = 8 * nt + g
                     if bits == 2:
-                        u, f = ks, 4 * r + nt % 4
+                        u, f = ks, (4 * r + nt % 4 + 1) % 8
                     else:
                         u, f = 2 * ks + r, nt % 4
                     _place(words, lane, u, f, bits, codes[..., tok, d0], codes[..., tok, d0 + 1])
@@ -91,7 +92,7 @@ def pack_value_codes(codes: np.ndarray, bits: int) -> np.ndarray:
                 for nt in range(d // 8):
                     ch = 8 * nt + g
                     if bits == 2:
-                        u, f = ks * nq + nt // 4, 4 * r + nt % 4
+                        u, f = ks * nq + nt // 4, (4 * r + nt % 4 + 1) % 8
                     else:
                         u, f = (2 * ks + r) * nq + nt // 4, nt % 4
                     _place(words, lane, u, f, bits, codes[..., t0, ch], codes[..., t0 + 1, ch])

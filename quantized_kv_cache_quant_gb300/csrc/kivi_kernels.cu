@@ -39,7 +39,11 @@ struct Kivi {
 // Masks that keep the code field of each fp16 half after the shift: bits 6-7
 // or 8-9 for 2-bit codes, bits 6-9 for 4-bit codes. The field then reads as
 // the fp16 subnormal code * 2^(P-24), P = 6 or 8; the top mantissa bits keep
-// the tensor-core products at full fp32-accumulation accuracy.
+// the tensor-core products at full fp32-accumulation accuracy. A 2-bit word
+// holds 8 fields per half; the word itself, its shifts by 4 either way and its
+// per-half byte swap bring two fields each to bits 6-7 and 8-9 (field order
+// f = (4r + nt + 1) mod 8 of the packed layout): three operations and eight
+// masks for 16 codes.
 constexpr uint32_t kMaskP6 = 0x00C000C0u;
 constexpr uint32_t kMaskP8 = 0x03000300u;
 constexpr uint32_t kMask4 = 0x03C003C0u;
@@ -83,7 +87,7 @@ __device__ __forceinline__ uint32_t key_word(const __half* xk, int RS, const flo
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt) {
       const float2 x = __half22float2(reinterpret_cast<const __half2*>(xk)[(8 * nt + gg) * (RS / 2) + d0 / 2]);
-      const int f = (KB == 2) ? 4 * r + nt : nt;
+      const int f = (KB == 2) ? ((4 * r + nt + 1) & 7) : nt;
       w |= (group_code(x.x, z0, s0, r0, KL) << (KB * f)) | (group_code(x.y, z1, s1, r1, KL) << (16 + KB * f));
     }
   }
@@ -109,7 +113,7 @@ __device__ __forceinline__ uint32_t value_word(const __half* xv, int RS, const f
     for (int n = 0; n < 4; ++n) {
       const int ch = 8 * (4 * q + n) + gg;
       const float x0 = __half2float(xv[t0 * RS + ch]), x1 = __half2float(xv[(t0 + 1) * RS + ch]);
-      const int f = (VB == 2) ? 4 * r + n : n;
+      const int f = (VB == 2) ? ((4 * r + n + 1) & 7) : n;
       w |= (group_code(x0, z0, s0, r0, VL) << (VB * f)) | (group_code(x1, z1, s1, r1, VL) << (16 + VB * f));
     }
   }
@@ -612,11 +616,11 @@ __global__ void __launch_bounds__(128, KVQ_DECODE_MIN_BLOCKS) kivi_decode_kernel
         bsum = dot2_f16_f32(qs[ks][0], md.z, dot2_f16_f32(qs[ks][1], md.w, bsum));
         if constexpr (KB == 2) {
           const uint32_t w = kw[ks];
-          const uint32_t l6 = w << 6, l2 = w << 2, r2 = w >> 2, r6 = w >> 6;
-          mma16816(sacc[0], A0, A1, A2, A3, l6 & kMaskP6, r2 & kMaskP6);
-          mma16816(sacc[1], A0, A1, A2, A3, l6 & kMaskP8, r2 & kMaskP8);
-          mma16816(sacc[2], A0, A1, A2, A3, l2 & kMaskP6, r6 & kMaskP6);
-          mma16816(sacc[3], A0, A1, A2, A3, l2 & kMaskP8, r6 & kMaskP8);
+          const uint32_t l4 = w << 4, r4 = w >> 4, sw = __byte_perm(w, 0u, 0x2301u);
+          mma16816(sacc[0], A0, A1, A2, A3, l4 & kMaskP6, r4 & kMaskP6);
+          mma16816(sacc[1], A0, A1, A2, A3, l4 & kMaskP8, r4 & kMaskP8);
+          mma16816(sacc[2], A0, A1, A2, A3, w & kMaskP6, sw & kMaskP6);
+          mma16816(sacc[3], A0, A1, A2, A3, w & kMaskP8, sw & kMaskP8);
         } else {
           const uint32_t w0 = kw[2 * ks], w1 = kw[2 * ks + 1];
           mma16816(sacc[0], A0, A1, A2, A3, (w0 << 6) & kMask4, (w1 << 6) & kMask4);
@@ -696,11 +700,11 @@ __global__ void __launch_bounds__(128, KVQ_DECODE_MIN_BLOCKS) kivi_decode_kernel
         for (int q = 0; q < P::NQ; ++q) {
           if constexpr (VB == 2) {
             const uint32_t w = vw[ks * P::NQ + q];
-            const uint32_t l6 = w << 6, l2 = w << 2, r2 = w >> 2, r6 = w >> 6;
-            mma16816(o_acc[4 * q + 0], A0, A1, A2, A3, l6 & kMaskP6, r2 & kMaskP6);
-            mma16816(o_acc[4 * q + 1], A0, A1, A2, A3, l6 & kMaskP8, r2 & kMaskP8);
-            mma16816(o_acc[4 * q + 2], A0, A1, A2, A3, l2 & kMaskP6, r6 & kMaskP6);
-            mma16816(o_acc[4 * q + 3], A0, A1, A2, A3, l2 & kMaskP8, r6 & kMaskP8);
+            const uint32_t l4 = w << 4, r4 = w >> 4, sw = __byte_perm(w, 0u, 0x2301u);
+            mma16816(o_acc[4 * q + 0], A0, A1, A2, A3, l4 & kMaskP6, r4 & kMaskP6);
+            mma16816(o_acc[4 * q + 1], A0, A1, A2, A3, l4 & kMaskP8, r4 & kMaskP8);
+            mma16816(o_acc[4 * q + 2], A0, A1, A2, A3, w & kMaskP6, sw & kMaskP6);
+            mma16816(o_acc[4 * q + 3], A0, A1, A2, A3, w & kMaskP8, sw & kMaskP8);
           } else {
             const uint32_t w0 = vw[(2 * ks) * P::NQ + q], w1 = vw[(2 * ks + 1) * P::NQ + q];
             mma16816(o_acc[4 * q + 0], A0, A1, A2, A3, (w0 << 6) & kMask4, (w1 << 6) & kMask4);

@@ -13,26 +13,30 @@ import pytest
 
 from oracle import kivi, layout
 
-# field extraction rule: shift applied to the 32-bit word, then a mask that
-# keeps bits [P, P + bits) of each half; returns (shift, P)
+# field extraction rule of the decode kernel: an operation on the 32-bit word
+# (a shift, or a swap of the two bytes of each 16-bit half), then a mask that
+# keeps bits [P, P + bits) of each half; returns (operation, P). For 2 bits the
+# B operand of n-tile nt%4 takes: 0 -> (w << 4, w >> 4) at P = 6, 1 -> the same
+# at P = 8, 2 -> (w, swap(w)) at P = 6, 3 -> the same at P = 8 (b0, b1 = r 0, 1).
 def _extract_rule(bits, r, nt):
     if bits == 2:
-        f = 4 * r + nt % 4
-        shift = {0: 6, 1: 6, 2: 2, 3: 2, 4: -2, 5: -2, 6: -6, 7: -6}[f]
-        p = 2 * f + shift
-        assert p in (6, 8)
+        op = [("shl", 4), ("shr", 4), ("shl", 0), ("swap", 0)][2 * ((nt % 4) // 2) + r]
+        p = 6 if nt % 2 == 0 else 8
     else:
-        f = nt % 4
-        shift = {0: 6, 1: 2, 2: -2, 3: -6}[f]
-        p = 4 * f + shift
-        assert p == 6
-    return shift, p
+        op = [("shl", 6), ("shl", 2), ("shr", 2), ("shr", 6)][nt % 4]
+        p = 6
+    return op, p
 
 
 def _extract(word, bits, r, nt):
-    shift, p = _extract_rule(bits, r, nt)
+    (kind, n), p = _extract_rule(bits, r, nt)
     w = int(word)
-    w = (w << shift) & 0xFFFFFFFF if shift >= 0 else w >> (-shift)
+    if kind == "shl":
+        w = (w << n) & 0xFFFFFFFF
+    elif kind == "shr":
+        w = w >> n
+    else:
+        w = ((w & 0x00FF00FF) << 8) | ((w >> 8) & 0x00FF00FF)
     mask = ((1 << bits) - 1) << p
     w &= mask | (mask << 16)
     lo = np.uint16(w & 0xFFFF).view(np.float16)
