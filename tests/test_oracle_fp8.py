@@ -135,3 +135,106 @@ def test_paged_scatter_gather():
     assert np.array_equal(pool2[1 * nb + 2, 1, :, :], byts[1, 1, 32:48])
     # one byte per element: half of fp16
     assert pool[:, :, :, :].size == b * nb * h * bs * d
+
+
+# ---------------------------------------------------------------- E5M2
+def _finite_e5m2_table():
+    """The finite E5M2 values from the bit layout, by exhaustive listing."""
+    vals = {}
+    for b in range(256):
+        s = -1.0 if b & 0x80 else 1.0
+        e, m = (b >> 2) & 31, b & 3
+        if e == 31:
+            continue
+        vals[b] = s * (m / 4 * 2.0 ** -14 if e == 0 else (1 + m / 4) * 2.0 ** (e - 15))
+    return vals
+
+
+def test_e5m2_format_facts():
+    table = _finite_e5m2_table()
+    assert len(table) == 248
+    assert max(table.values()) == fp8.E5M2_MAX == 57344.0
+    assert min(v for v in table.values() if v > 0) == 2.0 ** -16
+    dec = fp8.e5m2_decode(np.arange(256))
+    for b in range(256):
+        if b in table:
+            assert dec[b] == table[b]
+    assert np.isinf(dec[0x7C]) and np.isinf(dec[0xFC]) and np.isnan(dec[0x7D]) and np.isnan(dec[0xFF])
+
+
+def test_e5m2_all_fp16_inputs_against_brute_force():
+    table = _finite_e5m2_table()
+    pos = sorted((v, b) for b, v in table.items() if v >= 0 and not (b & 0x80))
+    vals = np.array([v for v, _ in pos])
+    codes = np.array([b for _, b in pos])
+    x = np.arange(65536, dtype=np.uint16).view(np.float16).astype(np.float32)
+    got = fp8.e5m2_encode(x)
+    for i, v in enumerate(x.astype(np.float64)):
+        if np.isnan(v):
+            assert got[i] == 0x7F
+            continue
+        sgn = 0x80 if np.signbit(v) else 0
+        a = min(abs(v), fp8.E5M2_MAX)
+        dist = np.abs(vals - a)
+        best = np.flatnonzero(dist == dist.min())
+        if len(best) > 1:
+            best = [j for j in best if codes[j] % 2 == 0]
+        assert got[i] == codes[best[0]] | sgn, (i, v)
+
+
+def test_e5m2_is_fp16_rounded_to_its_top_byte():
+    """E5M2 shares fp16's sign and exponent fields: below the saturation point
+    the code is the fp16 bit pattern rounded to its top byte, ties to even."""
+    bits = np.arange(65536, dtype=np.uint32)
+    x = bits.astype(np.uint16).view(np.float16)
+    ok = np.isfinite(x) & (np.abs(x.astype(np.float64)) < 57344.0)
+    mag = bits & 0x7FFF
+    rounded = (mag + 0x7F + ((mag >> 8) & 1)) >> 8            # round the low 8 bits, ties to even
+    want = (rounded | ((bits >> 8) & 0x80)).astype(np.uint8)
+    got = fp8.e5m2_encode(x.astype(np.float32))
+    assert np.array_equal(got[ok], want[ok])
+
+
+def test_e5m2_against_torch_cast():
+    torch = pytest.importorskip("torch")
+    x = np.arange(65536, dtype=np.uint16).view(np.float16).astype(np.float32)
+    x = x[np.isfinite(x) & (np.abs(x) <= 57344)]
+    ref = torch.from_numpy(x).to(torch.float8_e5m2).view(torch.uint8).numpy()
+    assert np.array_equal(fp8.e5m2_encode(x), ref)
+
+
+def test_e5m2_saturation_nan_and_signed_zero():
+    y = np.array([57344, 61439, 61440, 1e10, np.inf, -np.inf, -70000, np.nan, -0.0, 0.0], np.float32)
+    assert list(fp8.e5m2_encode(y)) == [0x7B, 0x7B, 0x7B, 0x7B, 0x7B, 0xFB, 0xFB, 0x7F, 0x80, 0x00]
+
+
+def test_e5m2_dynamic_scale():
+    rng = np.random.default_rng(3)
+    x = (rng.standard_normal((2, 3, 40, 16)) * 900).astype(np.float16)
+    s = fp8.dynamic_scale(x, "e5m2")
+    assert s == np.float32(np.float32(np.abs(x.astype(np.float32)).max()) / np.float32(57344.0))
+    q = fp8.quantize(x, s, "e5m2")
+    idx = np.unravel_index(np.abs(x.astype(np.float32)).argmax(), x.shape)
+    assert q[idx] in (0x7B, 0xFB)
+    dec = fp8.e5m2_decode(q)
+    assert np.all(np.isfinite(dec)) and np.all(np.abs(dec) <= 57344)
+
+
+# ---------------------------------------------------------------- per-head scales
+def test_per_head_scales_follow_each_head():
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal((3, 4, 33, 16)).astype(np.float32)
+    x *= np.array([0.01, 1.0, 30.0, 0.0]).reshape(1, 4, 1, 1)       # very different ranges, one all-zero head
+    x = x.astype(np.float16)
+    for fmt in fp8.FORMATS:
+        sh = fp8.dynamic_scale_per_head(x, fmt)
+        assert sh.shape == (4,) and sh.dtype == np.float32
+        for h in range(4):
+            a = np.float32(np.abs(x[:, h].astype(np.float32)).max())
+            assert sh[h] == (np.float32(1.0) if a == 0 else np.float32(a / np.float32(fp8.fmax(fmt))))
+        q = fp8.quantize(x, sh, fmt)
+        for h in range(4):                                            # per-head == per-slice scalar
+            assert np.array_equal(q[:, h], fp8.quantize(x[:, h], sh[h], fmt))
+        # each nonzero head reaches the format's largest code, which one per-tensor scale would not
+        for h in range(3):
+            assert np.max(q[:, h] & 0x7F) == (0x7E if fmt == "e4m3" else 0x7B)
