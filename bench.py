@@ -475,7 +475,7 @@ def run_table(args):
 
     names = args.table.split(",") if args.table != "all" else [
         workloads.MHA_4K.name, workloads.GQA_8K_2BIT.name, workloads.GQA_8K_4BIT.name, workloads.STREAM_128K.name,
-        workloads.FP8_32K.name]
+        workloads.FP8_32K.name, workloads.FP8_32K_E5M2_PH.name]
     for name in names:
         w = workloads.WORKLOADS[name]
         if isinstance(w, workloads.KiviWorkload):
@@ -506,10 +506,11 @@ def run_table(args):
             for x16, vl in ((k, 0), (v, 1)):
                 xd = dev(x16)
                 pool = torch.empty((nb, w.kv_heads, 16 * w.head_dim), dtype=torch.uint8, device="cuda")
-                sc = torch.zeros(1, dtype=torch.float32, device="cuda")
+                sc = torch.zeros(w.kv_heads if w.per_head else 1, dtype=torch.float32, device="cuda")
                 t_q.append(timed(lambda: kvq.fp8_kv_quantize(xd, w.batch, w.kv_heads, w.context, w.head_dim, tbl,
                                                              w.blocks_per_seq, 16, nb, pool, sc, False, vl, wsq,
-                                                             wsb), reps=5))
+                                                             wsb, per_head=w.per_head,
+                                                             fp8_format=kvq.FP8_FORMATS[w.fmt]), reps=5))
                 pools.append(pool)
                 scales.append(sc)
                 del xd
@@ -521,7 +522,8 @@ def run_table(args):
             t_dec = timed(lambda: kvq.fp8_decode_attention(q_d, pools[0], pools[1], scales[0], scales[1], tbl, lens,
                                                            w.batch, w.q_heads, w.kv_heads, w.head_dim, 16,
                                                            w.blocks_per_seq, nb, w.context, out, True, 0.0, ws,
-                                                           wsd))
+                                                           wsd, per_head=w.per_head,
+                                                           fp8_format=kvq.FP8_FORMATS[w.fmt]))
             nbytes = metrics.fp8_decode_bytes(w.batch, w.kv_heads, w.q_heads, w.head_dim, w.context,
                                               w.blocks_per_seq)
             qbytes = metrics.fp8_quantize_bytes(w.batch, w.kv_heads, w.context, w.head_dim, True)

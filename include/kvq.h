@@ -223,25 +223,32 @@ KVQ_API kvq_status kv_decode_attention_noalloc(const kivi_cache* cache, const ui
  *          t0 = 8*r + 2*tig, t0+1 of channel 8*nt + g (nt < D/8).
  * Rows of a block past the end of the sequence are written as zero bytes. */
 
-/* Workspace of fp8_kv_quantize: per-block amax partials. */
+/* Workspace of fp8_kv_quantize: per-block amax partials (4096 words, for one
+ * scale or split between the per-head scales). */
 KVQ_API size_t fp8_quantize_workspace_bytes(int32_t batch, int32_t kv_heads, int32_t seq_len, int32_t head_dim);
 
 /* Quantize one tensor (K or V) of one layer into the paged pool.
  *   x           : device fp16 [B, H_kv, seq_len, D]
  *   block_table : device int32 [B, max_blocks]; entries < num_blocks
  *   pool        : device uint8 [num_blocks, H_kv, 16*D]
- *   scale       : device float32 scalar. static_scale == 0: written with
- *                 fl32(amax/448) (amax = max|x| over the whole tensor, scale 1
- *                 if amax == 0) [YUN]; static_scale != 0: read as given
- *                 (e.g. 1.0, the no-calibration route of [KIVI] section 6.1).
+ *   scale       : device float32: one value (per_head == 0) or one per kv head
+ *                 [H_kv] (per_head == 1, [CSDN] section 10.1). static_scale == 0:
+ *                 written with fl32(amax/FMAX), amax = max|x| over the whole
+ *                 tensor (or over kv head h's slice for scale[h]), scale 1 where
+ *                 amax == 0 [YUN]; static_scale != 0: read as given (e.g. 1.0,
+ *                 the no-calibration route of [KIVI] section 6.1).
+ *   fp8_format  : 0 = E4M3 (FMAX 448), 1 = E5M2 (1 sign, 5 exponent bits with
+ *                 bias 15, 2 mantissa bits; FMAX 57344; [CSDN] section 18.4;
+ *                 round to nearest even, saturating to +-57344, NaN -> 0x7F)
  *   value_layout: 0 for keys, 1 for values (the in-block order above)
- * byte = E4M3(fl32(x / scale)). Block-table entries outside [0, num_blocks)
- * are skipped (nothing is written for that block). */
+ * byte = FP8(fl32(x / scale)). Block-table entries outside [0, num_blocks)
+ * are skipped (nothing is written for that block). per_head and fp8_format
+ * outside {0, 1} return KVQ_ERR_ARG. */
 KVQ_API kvq_status fp8_kv_quantize(const uint16_t* x, int32_t batch, int32_t kv_heads, int32_t seq_len,
                            int32_t head_dim, const int32_t* block_table, int32_t max_blocks,
                            int32_t block_size, int32_t num_blocks, uint8_t* pool, float* scale,
-                           int32_t static_scale, int32_t value_layout, void* ws, size_t ws_bytes,
-                           void* stream);
+                           int32_t static_scale, int32_t per_head, int32_t fp8_format,
+                           int32_t value_layout, void* ws, size_t ws_bytes, void* stream);
 
 /* Workspace of fp8_decode_attention (split-K partials + status word, as for
  * kv_decode_workspace_bytes). */
@@ -252,15 +259,17 @@ KVQ_API size_t fp8_decode_workspace_bytes(int32_t batch, int32_t q_heads, int32_
  * over tokens 0 .. seq_lens[b]-1 of kv head hq / (H_q/H_kv).
  *   q        : device fp16 [B, H_q, D];  out: device [B, H_q, D] (fp32 or fp16)
  *   k_pool, v_pool : pools written by fp8_kv_quantize (value_layout 0 and 1)
- *   k_scale, v_scale : device float32 scalars
+ *   k_scale, v_scale : device float32, one value each (per_head == 0) or one
+ *              per kv head [H_kv] (per_head == 1), as fp8_kv_quantize wrote them
+ *   fp8_format : the pools' format, 0 = E4M3, 1 = E5M2
  *   seq_lens : device int32 [B], each in [1, max_seq_len]
  * The host passes max_seq_len >= every seq_lens[b] (it sizes the grid) and
  * max_seq_len <= max_blocks*16. Block-table entries must lie in
  * [0, num_blocks); the kernels clamp them (and seq_lens) so that a bad table
  * gives wrong numbers but never an access outside the pool or the table. */
 KVQ_API kvq_status fp8_decode_attention(const uint16_t* q, const uint8_t* k_pool, const uint8_t* v_pool,
-                                const float* k_scale, const float* v_scale,
-                                const int32_t* block_table, const int32_t* seq_lens,
+                                const float* k_scale, const float* v_scale, int32_t per_head,
+                                int32_t fp8_format, const int32_t* block_table, const int32_t* seq_lens,
                                 int32_t batch, int32_t q_heads, int32_t kv_heads, int32_t head_dim,
                                 int32_t block_size, int32_t max_blocks, int32_t num_blocks,
                                 int32_t max_seq_len, void* out, int32_t out_fp32,

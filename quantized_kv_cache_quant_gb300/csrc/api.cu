@@ -430,13 +430,16 @@ size_t fp8_quantize_workspace_bytes(int32_t batch, int32_t kv_heads, int32_t seq
 
 kvq_status fp8_kv_quantize(const uint16_t* x, int32_t batch, int32_t kv_heads, int32_t seq_len, int32_t head_dim,
                            const int32_t* block_table, int32_t max_blocks, int32_t block_size, int32_t num_blocks,
-                           uint8_t* pool, float* scale, int32_t static_scale, int32_t value_layout, void* ws,
-                           size_t ws_bytes, void* stream) {
+                           uint8_t* pool, float* scale, int32_t static_scale, int32_t per_head, int32_t fp8_format,
+                           int32_t value_layout, void* ws, size_t ws_bytes, void* stream) {
   if (x == nullptr || block_table == nullptr || pool == nullptr || scale == nullptr) return KVQ_ERR_NULL;
   if (batch <= 0 || kv_heads <= 0 || seq_len <= 0 || num_blocks <= 0 || max_blocks <= 0) return KVQ_ERR_ARG;
   if (head_dim != 64 && head_dim != 128) return KVQ_ERR_UNSUPPORTED;
   if (block_size != 16) return KVQ_ERR_UNSUPPORTED;
   if (value_layout != 0 && value_layout != 1) return KVQ_ERR_ARG;
+  if (per_head != 0 && per_head != 1) return KVQ_ERR_ARG;
+  if (fp8_format != 0 && fp8_format != 1) return KVQ_ERR_ARG;
+  if (per_head && kv_heads > kAmaxBlocksMax) return KVQ_ERR_UNSUPPORTED;
   if (ceil_div(seq_len, block_size) > max_blocks) return KVQ_ERR_CAPACITY;
   if (!aligned(x) || !aligned(block_table) || !aligned(pool) || !aligned(scale)) return KVQ_ERR_ALIGN;
   if (!static_scale) {
@@ -456,11 +459,17 @@ kvq_status fp8_kv_quantize(const uint16_t* x, int32_t batch, int32_t kv_heads, i
   a.pool = pool;
   a.scale = scale;
   a.static_scale = static_scale;
+  a.per_head = per_head;
+  a.fmt = fp8_format;
   a.value_layout = value_layout;
   a.amax_partials = static_cast<uint32_t*>(ws);
-  const long long n_vec = static_cast<long long>(batch) * kv_heads * seq_len * head_dim / 8;
-  a.amax_blocks = static_cast<int>(std::min<long long>(
-      {static_cast<long long>(kAmaxBlocksMax), 8LL * kvq::device_sm_count(), (n_vec + 255) / 256}));
+  // amax blocks per scale: the partials of all scales fit the workspace, and
+  // about 8 blocks per SM run in all
+  const int n_scales = per_head ? kv_heads : 1;
+  const long long n_vec = static_cast<long long>(batch) * seq_len * head_dim / 8 * (per_head ? 1 : kv_heads);
+  a.amax_blocks = static_cast<int>(std::max<long long>(
+      1, std::min<long long>({static_cast<long long>(kAmaxBlocksMax / n_scales),
+                              (8LL * kvq::device_sm_count() + n_scales - 1) / n_scales, (n_vec + 255) / 256})));
   return from_cuda(kvq::launch_fp8_quantize(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -470,13 +479,16 @@ size_t fp8_decode_workspace_bytes(int32_t batch, int32_t q_heads, int32_t head_d
 }
 
 kvq_status fp8_decode_attention(const uint16_t* q, const uint8_t* k_pool, const uint8_t* v_pool, const float* k_scale,
-                                const float* v_scale, const int32_t* block_table, const int32_t* seq_lens,
+                                const float* v_scale, int32_t per_head, int32_t fp8_format,
+                                const int32_t* block_table, const int32_t* seq_lens,
                                 int32_t batch, int32_t q_heads, int32_t kv_heads, int32_t head_dim, int32_t block_size,
                                 int32_t max_blocks, int32_t num_blocks, int32_t max_seq_len, void* out,
                                 int32_t out_fp32, float softmax_scale, void* ws, size_t ws_bytes, void* stream) {
   if (!q || !k_pool || !v_pool || !k_scale || !v_scale || !block_table || !seq_lens || !out) return KVQ_ERR_NULL;
   if (batch <= 0 || q_heads <= 0 || kv_heads <= 0 || max_blocks <= 0 || num_blocks <= 0 || max_seq_len <= 0)
     return KVQ_ERR_ARG;
+  if (per_head != 0 && per_head != 1) return KVQ_ERR_ARG;
+  if (fp8_format != 0 && fp8_format != 1) return KVQ_ERR_ARG;
   if (batch > 65535 || kv_heads > 65535) return KVQ_ERR_UNSUPPORTED;
   if (head_dim != 64 && head_dim != 128) return KVQ_ERR_UNSUPPORTED;
   if (block_size != 16) return KVQ_ERR_UNSUPPORTED;
@@ -499,6 +511,8 @@ kvq_status fp8_decode_attention(const uint16_t* q, const uint8_t* k_pool, const 
   a.v_pool = v_pool;
   a.k_scale = k_scale;
   a.v_scale = v_scale;
+  a.per_head = per_head;
+  a.fmt = fp8_format;
   a.block_table = block_table;
   a.seq_lens = seq_lens;
   a.batch = batch;

@@ -1,12 +1,14 @@
-// FP8 E4M3 paged KV cache kernels for sm_103a: per-tensor amax (two passes, no
-// atomics), scale = amax / 448, cast + scatter into paged blocks, and split-K
-// decode attention over the paged cache.
+// FP8 paged KV cache kernels for sm_103a (E4M3 or E5M2, one scale per tensor
+// or per kv head): amax (two passes, no atomics), scale = amax / FMAX (448 for
+// E4M3, 57344 for E5M2), cast + scatter into paged blocks, and split-K decode
+// attention over the paged cache.
 //
 // Method: "4.4 KV Cache 量化：KIVI 2-bit 与 FP8 KV Cache" (aiinfraguide), section 5
 // (E4M3 = 1 sign, 4 exponent, 3 mantissa bits); "大模型量化从0到1（十三）：KV Cache
 // 量化" (CSDN), section 10 (q = cast_fp8(x / s), x_hat = float(q) * s, per-tensor
 // scale) and section 13 (paged blocks through a block table); "LLM推理加速KV Cache
-// 量化压缩实战方案" (yunthe), custom-cache section (scale = max|x| / 448).
+// 量化压缩实战方案" (yunthe), custom-cache section (scale = max|x| / 448); CSDN
+// section 10.1 (per-head scales) and section 18.4 (E5M2).
 #include <cmath>
 
 #include "kvq_device.cuh"
@@ -21,27 +23,46 @@ constexpr int kBlock = 16;  // tokens per paged block
 // amax: max |x| as the maximum of the fp16 magnitude bits (|x| orders like its
 // bits; a NaN's bits exceed every finite value's and infinity's).
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) fp8_amax_kernel(const uint4* __restrict__ x, long long n_vec,
-                                                       uint32_t* __restrict__ partials) {
+__device__ __forceinline__ uint32_t max_mag_bits(uint32_t m, const uint4 v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) m = max(m, max(w[k] & 0x7FFFu, (w[k] >> 16) & 0x7FFFu));
+  return m;
+}
+
+// Per tensor (gridDim.y == 1): the whole [B, H, S, D] tensor, grid-strided.
+// Per kv head (gridDim.y == H): block (x, h) strides over head h's B slices of
+// row_vecs = S * D / 8 16-byte vectors. Partial (h, x) goes to
+// partials[h * gridDim.x + x].
+__global__ void __launch_bounds__(256) fp8_amax_kernel(const uint4* __restrict__ x, long long n_vec, int batch,
+                                                       int heads, long long row_vecs, uint32_t* __restrict__ partials) {
   uint32_t m = 0;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-  long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
-  for (; i + 3 * stride < n_vec; i += 4 * stride) {
-    uint4 v[4];
+  const long long t0 = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+  if (gridDim.y == 1) {
+    long long i = t0;
+    for (; i + 3 * stride < n_vec; i += 4 * stride) {
+      uint4 v[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) v[u] = __ldcs(x + i + u * stride);
+      for (int u = 0; u < 4; ++u) v[u] = __ldcs(x + i + u * stride);
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) m = max(m, max(w[k] & 0x7FFFu, (w[k] >> 16) & 0x7FFFu));
+      for (int u = 0; u < 4; ++u) m = max_mag_bits(m, v[u]);
     }
-  }
-  for (; i < n_vec; i += stride) {
-    const uint4 v = __ldcs(x + i);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    for (; i < n_vec; i += stride) m = max_mag_bits(m, __ldcs(x + i));
+  } else {
+    const int h = blockIdx.y;
+    for (int b = 0; b < batch; ++b) {
+      const uint4* row = x + (static_cast<long long>(b) * heads + h) * row_vecs;
+      long long i = t0;
+      for (; i + 3 * stride < row_vecs; i += 4 * stride) {
+        uint4 v[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) m = max(m, max(w[k] & 0x7FFFu, (w[k] >> 16) & 0x7FFFu));
+        for (int u = 0; u < 4; ++u) v[u] = __ldcs(row + i + u * stride);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) m = max_mag_bits(m, v[u]);
+      }
+      for (; i < row_vecs; i += stride) m = max_mag_bits(m, __ldcs(row + i));
+    }
   }
   m = __reduce_max_sync(0xffffffffu, m);
   __shared__ uint32_t wm[8];
@@ -50,15 +71,16 @@ __global__ void __launch_bounds__(256) fp8_amax_kernel(const uint4* __restrict__
   if (threadIdx.x == 0) {
     uint32_t r = 0;
     for (int k = 0; k < (blockDim.x >> 5); ++k) r = max(r, wm[k]);
-    partials[blockIdx.x] = r;
+    partials[blockIdx.y * gridDim.x + blockIdx.x] = r;
   }
 }
 
-// scale = fl32(amax / 448), or 1 when the tensor is all zeros.
-__global__ void __launch_bounds__(256) fp8_scale_kernel(const uint32_t* __restrict__ partials, int n,
+// scale[h] = fl32(amax / FMAX), or 1 when the tensor (or head) is all zeros;
+// one block per scale, over its n partials.
+__global__ void __launch_bounds__(256) fp8_scale_kernel(const uint32_t* __restrict__ partials, int n, float fmax,
                                                         float* __restrict__ scale) {
   uint32_t m = 0;
-  for (int i = threadIdx.x; i < n; i += blockDim.x) m = max(m, partials[i]);
+  for (int i = threadIdx.x; i < n; i += blockDim.x) m = max(m, partials[blockIdx.x * n + i]);
   m = __reduce_max_sync(0xffffffffu, m);
   __shared__ uint32_t wm[8];
   if ((threadIdx.x & 31) == 0) wm[threadIdx.x >> 5] = m;
@@ -67,7 +89,7 @@ __global__ void __launch_bounds__(256) fp8_scale_kernel(const uint32_t* __restri
     uint32_t r = 0;
     for (int k = 0; k < (blockDim.x >> 5); ++k) r = max(r, wm[k]);
     const float amax = __half2float(__ushort_as_half(static_cast<unsigned short>(r)));
-    *scale = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
+    scale[blockIdx.x] = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, fmax);
   }
 }
 
@@ -109,8 +131,8 @@ __device__ __forceinline__ float scaled(float x, float scale, float y) {
   }
 }
 
-template <int D, int MODE>
-__device__ __forceinline__ void cast_units(const Fp8QuantArgs& a, __half* bufs, float scale, float y) {
+template <int D, int MODE, int FMT>
+__device__ __forceinline__ void cast_units(const Fp8QuantArgs& a, __half* bufs) {
   constexpr int RS = D + 8;  // padded row stride (halves): rows start 4 banks apart
   constexpr int BUF = kBlock * RS;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -161,6 +183,8 @@ __device__ __forceinline__ void cast_units(const Fp8QuantArgs& a, __half* bufs, 
       const int j = static_cast<int>(u % nb);
       const int h = static_cast<int>((u / nb) % a.kv_heads);
       const int ntok = min(kBlock, a.seq_len - j * kBlock);
+      const float scale = a.scale[a.per_head ? h : 0];
+      const float y = (MODE == 0) ? 0.0f : __frcp_rn(scale);
       uint4* dst = reinterpret_cast<uint4*>(a.pool + (static_cast<long long>(blk) * a.kv_heads + h) * (kBlock * D));
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
@@ -183,7 +207,7 @@ __device__ __forceinline__ void cast_units(const Fp8QuantArgs& a, __half* bufs, 
           const bool v0 = tok0 < ntok, v1 = tok1 < ntok;
           const float y0 = v0 ? scaled<MODE>(__half2float(xs[tok0 * RS + ch0]), scale, y) : 0.0f;
           const float y1 = v1 ? scaled<MODE>(__half2float(xs[tok1 * RS + ch1]), scale, y) : 0.0f;
-          uint32_t pair = f32x2_to_e4m3x2(y0, y1);
+          uint32_t pair = f32x2_to_fp8x2<FMT>(y0, y1);
           if (!v0) pair &= 0xFF00u;
           if (!v1) pair &= 0x00FFu;
           if (kk & 1)
@@ -199,17 +223,19 @@ __device__ __forceinline__ void cast_units(const Fp8QuantArgs& a, __half* bufs, 
   asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
-template <int D>
+template <int D, int FMT>
 __global__ void __launch_bounds__(32 * kCastWarps) fp8_cast_kernel(Fp8QuantArgs a) {
   __shared__ __align__(16) __half bufs[kCastWarps][2 * kBlock * (D + 8)];
   __half* mine = bufs[threadIdx.x >> 5];
-  const float scale = *a.scale;
-  if (!(scale >= 0x1p-96f && scale <= 0x1p96f))  // the same for the whole grid
-    cast_units<D, 0>(a, mine, scale, 0.0f);
+  // the reciprocal path when every scale is in its exact range (the same decision for the whole grid)
+  bool fast = true;
+  for (int h = 0; h < (a.per_head ? a.kv_heads : 1); ++h) fast &= (a.scale[h] >= 0x1p-96f && a.scale[h] <= 0x1p96f);
+  if (!fast)
+    cast_units<D, 0, FMT>(a, mine);
   else if (a.static_scale)
-    cast_units<D, 1>(a, mine, scale, __frcp_rn(scale));
+    cast_units<D, 1, FMT>(a, mine);
   else
-    cast_units<D, 2>(a, mine, scale, __frcp_rn(scale));
+    cast_units<D, 2, FMT>(a, mine);
 }
 
 // ---------------------------------------------------------------------------
@@ -230,7 +256,7 @@ struct Fp8Smem {
   static constexpr int BYTES = BAR_BYTES + AREA;
 };
 
-template <int D, int STAGES>
+template <int D, int STAGES, int FMT>
 __global__ void __launch_bounds__(128) fp8_decode_kernel(Fp8DecodeArgs a) {
   using S = Fp8Smem<D, STAGES>;
   constexpr int KS = D / 16, NT = D / 8, CH = D / 32;  // CH: 16-byte chunks per lane
@@ -287,8 +313,8 @@ __global__ void __launch_bounds__(128) fp8_decode_kernel(Fp8DecodeArgs a) {
 #pragma unroll
     for (int jj = 0; jj < 2; ++jj)
       qa[ks][jj] = row_ok ? *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8 * jj + 2 * tig) : 0u;
-  const float kmul = (*a.k_scale) * a.scale_log2;
-  const float vscale = *a.v_scale;
+  const float kmul = a.k_scale[a.per_head ? h : 0] * a.scale_log2;
+  const float vscale = a.v_scale[a.per_head ? h : 0];
 
   float m_run = -INFINITY, l_run = 0.0f;
   float o_acc[NT][4];
@@ -326,8 +352,8 @@ __global__ void __launch_bounds__(128) fp8_decode_kernel(Fp8DecodeArgs a) {
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
         const uint32_t w = kw[nt * KS + ks];
-        mma16816(sacc[nt], qa[ks][0], 0u, qa[ks][1], 0u, e4m3x2_to_f16x2(static_cast<uint16_t>(w & 0xFFFFu)),
-                 e4m3x2_to_f16x2(static_cast<uint16_t>(w >> 16)));
+        mma16816(sacc[nt], qa[ks][0], 0u, qa[ks][1], 0u, fp8x2_to_f16x2<FMT>(static_cast<uint16_t>(w & 0xFFFFu)),
+                 fp8x2_to_f16x2<FMT>(static_cast<uint16_t>(w >> 16)));
       }
     }
     float sc[4];
@@ -374,8 +400,8 @@ __global__ void __launch_bounds__(128) fp8_decode_kernel(Fp8DecodeArgs a) {
     }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
-      mma16816(o_acc[nt], A0, A1, A2, A3, e4m3x2_to_f16x2(static_cast<uint16_t>(vw[nt] & 0xFFFFu)),
-               e4m3x2_to_f16x2(static_cast<uint16_t>(vw[nt] >> 16)));
+      mma16816(o_acc[nt], A0, A1, A2, A3, fp8x2_to_f16x2<FMT>(static_cast<uint16_t>(vw[nt] & 0xFFFFu)),
+               fp8x2_to_f16x2<FMT>(static_cast<uint16_t>(vw[nt] >> 16)));
 
     __syncwarp();
     if (lane == 0 && j + STAGES < n_mine) {
@@ -411,10 +437,10 @@ __global__ void __launch_bounds__(128) fp8_decode_kernel(Fp8DecodeArgs a) {
 
 constexpr int kFp8Stages = 4;
 
-template <int D>
+template <int D, int FMT>
 cudaError_t fp8_decode_dispatch(const Fp8DecodeArgs& a, cudaStream_t s) {
   constexpr int smem = Fp8Smem<D, kFp8Stages>::BYTES;
-  auto kern = fp8_decode_kernel<D, kFp8Stages>;
+  auto kern = fp8_decode_kernel<D, kFp8Stages, FMT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(a.splits, a.kv_heads, a.batch);
@@ -429,7 +455,7 @@ int fp8_occupancy() {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
   if (cached[dev] == 0) {
     constexpr int smem = Fp8Smem<D, kFp8Stages>::BYTES;
-    auto kern = fp8_decode_kernel<D, kFp8Stages>;
+    auto kern = fp8_decode_kernel<D, kFp8Stages, 0>;  // both formats use the same resources
     int n = 0;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, 128, smem) != cudaSuccess || n <= 0)
@@ -453,8 +479,8 @@ int cast_blocks_per_sm(int head_dim) {
   if (cached[dev][i] == 0) {
     int n = 0;
     const cudaError_t e = head_dim == 128
-                              ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fp8_cast_kernel<128>, 32 * kCastWarps, 0)
-                              : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fp8_cast_kernel<64>, 32 * kCastWarps, 0);
+                              ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fp8_cast_kernel<128, 0>, 32 * kCastWarps, 0)
+                              : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fp8_cast_kernel<64, 0>, 32 * kCastWarps, 0);
     cached[dev][i] = (e == cudaSuccess && n > 0) ? n : 4;
   }
   return cached[dev][i];
@@ -462,11 +488,14 @@ int cast_blocks_per_sm(int head_dim) {
 
 cudaError_t launch_fp8_quantize(const Fp8QuantArgs& a, cudaStream_t s) {
   if (!a.static_scale) {
-    const long long n_vec = static_cast<long long>(a.batch) * a.kv_heads * a.seq_len * a.head_dim / 8;
-    fp8_amax_kernel<<<a.amax_blocks, 256, 0, s>>>(reinterpret_cast<const uint4*>(a.x), n_vec, a.amax_partials);
+    const long long row_vecs = static_cast<long long>(a.seq_len) * a.head_dim / 8;
+    const long long n_vec = static_cast<long long>(a.batch) * a.kv_heads * row_vecs;
+    const int n_scales = a.per_head ? a.kv_heads : 1;
+    fp8_amax_kernel<<<dim3(a.amax_blocks, n_scales), 256, 0, s>>>(reinterpret_cast<const uint4*>(a.x), n_vec,
+                                                                   a.batch, a.kv_heads, row_vecs, a.amax_partials);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    fp8_scale_kernel<<<1, 256, 0, s>>>(a.amax_partials, a.amax_blocks, a.scale);
+    fp8_scale_kernel<<<n_scales, 256, 0, s>>>(a.amax_partials, a.amax_blocks, a.fmt ? 57344.0f : 448.0f, a.scale);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -475,19 +504,24 @@ cudaError_t launch_fp8_quantize(const Fp8QuantArgs& a, cudaStream_t s) {
   const long long want = (units + kCastWarps - 1) / kCastWarps;
   const long long full = static_cast<long long>(cast_blocks_per_sm(a.head_dim)) * device_sm_count();
   const int grid = static_cast<int>(want < full ? want : full);
-  if (a.head_dim == 128)
-    fp8_cast_kernel<128><<<grid, 32 * kCastWarps, 0, s>>>(a);
-  else if (a.head_dim == 64)
-    fp8_cast_kernel<64><<<grid, 32 * kCastWarps, 0, s>>>(a);
-  else
-    return cudaErrorInvalidValue;
+  switch (a.head_dim * 10 + a.fmt) {
+    case 1280: fp8_cast_kernel<128, 0><<<grid, 32 * kCastWarps, 0, s>>>(a); break;
+    case 1281: fp8_cast_kernel<128, 1><<<grid, 32 * kCastWarps, 0, s>>>(a); break;
+    case 640: fp8_cast_kernel<64, 0><<<grid, 32 * kCastWarps, 0, s>>>(a); break;
+    case 641: fp8_cast_kernel<64, 1><<<grid, 32 * kCastWarps, 0, s>>>(a); break;
+    default: return cudaErrorInvalidValue;
+  }
   return cudaGetLastError();
 }
 
 cudaError_t launch_fp8_decode(const Fp8DecodeArgs& a, cudaStream_t s) {
-  if (a.head_dim == 128) return fp8_decode_dispatch<128>(a, s);
-  if (a.head_dim == 64) return fp8_decode_dispatch<64>(a, s);
-  return cudaErrorInvalidValue;
+  switch (a.head_dim * 10 + a.fmt) {
+    case 1280: return fp8_decode_dispatch<128, 0>(a, s);
+    case 1281: return fp8_decode_dispatch<128, 1>(a, s);
+    case 640: return fp8_decode_dispatch<64, 0>(a, s);
+    case 641: return fp8_decode_dispatch<64, 1>(a, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace kvq

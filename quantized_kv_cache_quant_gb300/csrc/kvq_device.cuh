@@ -173,6 +173,38 @@ __device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi) {
   return r;
 }
 
+// Two E5M2 bytes (low byte first) -> fp16x2 bits. E5M2 has fp16's sign and
+// exponent fields and the top two of its mantissa bits, so each byte becomes
+// the high byte of its half (exact for every code, subnormals, infinities and
+// NaNs included): one byte permute, bytes (0, b0, 0, b1).
+__device__ __forceinline__ uint32_t e5m2x2_to_f16x2(uint16_t v) {
+  return __byte_perm(static_cast<uint32_t>(v), 0u, 0x1404u);
+}
+
+// Two fp32 values -> two E5M2 bytes (round to nearest even, saturating to
+// +-57344, NaN -> 0x7F); `lo` goes to the low byte.
+__device__ __forceinline__ uint16_t f32x2_to_e5m2x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// FP8 format FMT: 0 = E4M3, 1 = E5M2.
+template <int FMT>
+__device__ __forceinline__ uint32_t fp8x2_to_f16x2(uint16_t v) {
+  if constexpr (FMT == 0)
+    return e4m3x2_to_f16x2(v);
+  else
+    return e5m2x2_to_f16x2(v);
+}
+template <int FMT>
+__device__ __forceinline__ uint16_t f32x2_to_fp8x2(float lo, float hi) {
+  if constexpr (FMT == 0)
+    return f32x2_to_e4m3x2(lo, hi);
+  else
+    return f32x2_to_e5m2x2(lo, hi);
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));

@@ -79,10 +79,12 @@ struct Fp8QuantArgs {
   int max_blocks;
   int num_blocks;
   uint8_t* pool;
-  float* scale;
+  float* scale;           // [1] or, per_head, [H_kv]
   int static_scale;
+  int per_head;
+  int fmt;                // 0 = E4M3, 1 = E5M2
   int value_layout;
-  uint32_t* amax_partials;
+  uint32_t* amax_partials;  // [per_head ? H_kv : 1][amax_blocks]
   int amax_blocks;
 };
 cudaError_t launch_fp8_quantize(const Fp8QuantArgs& a, cudaStream_t s);
@@ -91,8 +93,10 @@ struct Fp8DecodeArgs {
   const uint16_t* q;
   const uint8_t* k_pool;
   const uint8_t* v_pool;
-  const float* k_scale;
+  const float* k_scale;   // [1] or, per_head, [H_kv]
   const float* v_scale;
+  int per_head;
+  int fmt;                // 0 = E4M3, 1 = E5M2
   const int32_t* block_table;
   const int32_t* seq_lens;
   int batch, q_heads, kv_heads, head_dim, max_blocks, num_blocks;

@@ -68,10 +68,10 @@ _SIG = {
     "kv_decode_attention_noalloc": ([_P_CACHE, c_vp, c_vp, c_i32, c_f32, c_vp], ctypes.c_int),
     "fp8_quantize_workspace_bytes": ([c_i32, c_i32, c_i32, c_i32], c_sz),
     "fp8_kv_quantize": ([c_vp, c_i32, c_i32, c_i32, c_i32, c_vp, c_i32, c_i32, c_i32, c_vp, c_vp, c_i32, c_i32,
-                         c_vp, c_sz, c_vp], ctypes.c_int),
+                         c_i32, c_i32, c_vp, c_sz, c_vp], ctypes.c_int),
     "fp8_decode_workspace_bytes": ([c_i32, c_i32, c_i32], c_sz),
-    "fp8_decode_attention": ([c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, c_i32, c_i32, c_i32, c_i32, c_i32,
-                              c_i32, c_i32, c_vp, c_i32, c_f32, c_vp, c_sz, c_vp], ctypes.c_int),
+    "fp8_decode_attention": ([c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, c_i32, c_vp, c_vp, c_i32, c_i32, c_i32, c_i32,
+                              c_i32, c_i32, c_i32, c_i32, c_vp, c_i32, c_f32, c_vp, c_sz, c_vp], ctypes.c_int),
 }
 for _name, (_args, _res) in _SIG.items():
     _fn = getattr(_lib, _name)
@@ -163,11 +163,16 @@ def fp8_quantize_workspace_bytes(batch, kv_heads, seq_len, head_dim) -> int:
     return int(_lib.fp8_quantize_workspace_bytes(batch, kv_heads, seq_len, head_dim))
 
 
+FP8_FORMATS = {"e4m3": 0, "e5m2": 1}
+
+
 def fp8_kv_quantize(x, batch, kv_heads, seq_len, head_dim, block_table, max_blocks, block_size, num_blocks, pool,
-                    scale, static_scale: bool, value_layout: int, ws, ws_bytes: int, stream=None) -> None:
+                    scale, static_scale: bool, value_layout: int, ws, ws_bytes: int, stream=None,
+                    per_head: bool = False, fp8_format: int = 0) -> None:
     _check(_lib.fp8_kv_quantize(_ptr(x), batch, kv_heads, seq_len, head_dim, _ptr(block_table), max_blocks,
                                 block_size, num_blocks, _ptr(pool), _ptr(scale), int(bool(static_scale)),
-                                value_layout, _ptr(ws), ws_bytes, _stream(stream)), "fp8_kv_quantize")
+                                int(per_head), int(fp8_format), value_layout, _ptr(ws), ws_bytes, _stream(stream)),
+           "fp8_kv_quantize")
 
 
 def fp8_decode_workspace_bytes(batch, q_heads, head_dim) -> int:
@@ -176,8 +181,10 @@ def fp8_decode_workspace_bytes(batch, q_heads, head_dim) -> int:
 
 def fp8_decode_attention(q, k_pool, v_pool, k_scale, v_scale, block_table, seq_lens, batch, q_heads, kv_heads,
                          head_dim, block_size, max_blocks, num_blocks, max_seq_len, out, out_fp32: bool,
-                         softmax_scale: float, ws, ws_bytes: int, stream=None) -> None:
+                         softmax_scale: float, ws, ws_bytes: int, stream=None, per_head: bool = False,
+                         fp8_format: int = 0) -> None:
     _check(_lib.fp8_decode_attention(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(k_scale), _ptr(v_scale),
+                                     int(per_head), int(fp8_format),
                                      _ptr(block_table), _ptr(seq_lens), batch, q_heads, kv_heads, head_dim,
                                      block_size, max_blocks, num_blocks, max_seq_len, _ptr(out),
                                      int(bool(out_fp32)), float(softmax_scale), _ptr(ws), ws_bytes,

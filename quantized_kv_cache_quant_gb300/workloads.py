@@ -61,6 +61,8 @@ class Fp8Workload:
     context: int
     block_size: int = 16
     seed: int = 3
+    fmt: str = "e4m3"          # FP8 format: "e4m3" or "e5m2"
+    per_head: bool = False     # one scale per kv head instead of one per tensor
 
     @property
     def blocks_per_seq(self) -> int:
@@ -75,11 +77,15 @@ MHA_4K = KiviWorkload("kivi2_mha_b8_h32_d128_s4096", 8, 32, 32, 128, 4096, 1, se
 GQA_8K_2BIT = KiviWorkload("kivi2_gqa8_b32_h8x64_d128_s8192", 32, 8, 64, 128, 8192, 1, seed=2)
 GQA_8K_4BIT = dataclasses.replace(GQA_8K_2BIT, name="kivi4_gqa8_b32_h8x64_d128_s8192", k_bits=4, v_bits=4)
 FP8_32K = Fp8Workload("fp8_e4m3_paged_b64_h8x32_d128_s32768", 64, 8, 32, 128, 32768, 16, seed=3)
+# the same cache in E5M2 with one scale per kv head (the FP8 variants of the pages)
+FP8_32K_E5M2_PH = dataclasses.replace(FP8_32K, name="fp8_e5m2_perhead_paged_b64_h8x32_d128_s32768", fmt="e5m2",
+                                      per_head=True)
 # the same cache for 8 sequences: a size an ncu capture of the quantize kernels can hold
 FP8_32K_B8 = Fp8Workload("fp8_e4m3_paged_b8_h8x32_d128_s32768", 8, 8, 32, 128, 32768, 16, seed=3)
 STREAM_128K = KiviWorkload("kivi2_stream_b4_h8x64_d128_s131072_512steps", 4, 8, 64, 128, 131072, 512, seed=4)
 
-WORKLOADS = {w.name: w for w in (TINY, MHA_4K, GQA_8K_2BIT, GQA_8K_4BIT, FP8_32K, FP8_32K_B8, STREAM_128K)}
+WORKLOADS = {w.name: w for w in (TINY, MHA_4K, GQA_8K_2BIT, GQA_8K_4BIT, FP8_32K, FP8_32K_E5M2_PH, FP8_32K_B8,
+                                  STREAM_128K)}
 
 
 def _channel_scales(rng: np.random.Generator, kv_heads: int, head_dim: int) -> np.ndarray:

@@ -170,7 +170,9 @@ def test_fp8_validation():
     for change, code in [(dict(block_size=32), "KVQ_ERR_UNSUPPORTED"), (dict(head_dim=96), "KVQ_ERR_UNSUPPORTED"),
                          (dict(max_blocks=2), "KVQ_ERR_CAPACITY"), (dict(value_layout=2), "KVQ_ERR_ARG"),
                          (dict(ws_bytes=8), "KVQ_ERR_WORKSPACE"), (dict(pool=None), "KVQ_ERR_NULL"),
-                         (dict(scale=ALIGNED + 4), "KVQ_ERR_ALIGN"), (dict(seq_len=0), "KVQ_ERR_ARG")]:
+                         (dict(scale=ALIGNED + 4), "KVQ_ERR_ALIGN"), (dict(seq_len=0), "KVQ_ERR_ARG"),
+                         (dict(per_head=2), "KVQ_ERR_ARG"), (dict(fp8_format=2), "KVQ_ERR_ARG"),
+                         (dict(fp8_format=-1), "KVQ_ERR_ARG")]:
         args = dict(q, **change)
         with pytest.raises(kvq.KvqError) as e:
             kvq.fp8_kv_quantize(**args, stream=0)
@@ -181,7 +183,8 @@ def test_fp8_validation():
              ws_bytes=kvq.fp8_decode_workspace_bytes(2, 8, 128))
     for change, code in [(dict(q_heads=7), "KVQ_ERR_SHAPE"), (dict(max_seq_len=49), "KVQ_ERR_CAPACITY"),
                          (dict(q_heads=32), "KVQ_ERR_UNSUPPORTED"), (dict(ws_bytes=100), "KVQ_ERR_WORKSPACE"),
-                         (dict(seq_lens=None), "KVQ_ERR_NULL")]:
+                         (dict(seq_lens=None), "KVQ_ERR_NULL"), (dict(per_head=3), "KVQ_ERR_ARG"),
+                         (dict(fp8_format=2), "KVQ_ERR_ARG")]:
         args = dict(d, **change)
         with pytest.raises(kvq.KvqError) as e:
             kvq.fp8_decode_attention(**args, stream=0)

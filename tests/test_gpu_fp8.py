@@ -21,22 +21,27 @@ def _kvq():
     return kvq
 
 
-def _quantize(x16, table, num_blocks, value_layout, static_scale=None):
+def _quantize(x16, table, num_blocks, value_layout, static_scale=None, fmt="e4m3", per_head=False):
+    """static_scale: None (dynamic), a scalar, or per head an array [H]."""
     import torch
     kvq = _kvq()
     b, h, s, d = x16.shape
     pool = torch.full((num_blocks, h, 16 * d), 0xAB, dtype=torch.uint8, device="cuda")
-    scale = torch.tensor([static_scale if static_scale is not None else -1.0], dtype=torch.float32, device="cuda")
+    n = h if per_head else 1
+    init = np.full(n, -1.0, np.float32) if static_scale is None else np.broadcast_to(
+        np.asarray(static_scale, np.float32), (n,))
+    scale = torch.tensor(np.array(init), dtype=torch.float32, device="cuda")
     wsb = kvq.fp8_quantize_workspace_bytes(b, h, s, d)
     ws = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
     xt, tt = dev(x16), dev(table)
     kvq.fp8_kv_quantize(xt, b, h, s, d, tt, table.shape[1], 16, num_blocks, pool, scale,
-                        static_scale is not None, value_layout, ws, wsb)
+                        static_scale is not None, value_layout, ws, wsb, per_head=per_head,
+                        fp8_format=kvq.FP8_FORMATS[fmt])
     return pool, scale
 
 
-def _oracle_pool(x16, table, num_blocks, value_layout, scale):
-    byts = fp8.quantize(x16, scale)
+def _oracle_pool(x16, table, num_blocks, value_layout, scale, fmt="e4m3"):
+    byts = fp8.quantize(x16, scale, fmt)
     nat = fp8.scatter_paged(byts, table, num_blocks, 16)
     return layout.fp8_pack_pool(nat, value_layout)
 
@@ -98,7 +103,8 @@ def test_saturation_with_static_scale():
     assert list(nat[1, :2]) == [0x7E, 0xFE]
 
 
-def _decode(q16, kpool, vpool, kscale, vscale, table, seq_lens, hkv, num_blocks, max_seq, out_fp32=True):
+def _decode(q16, kpool, vpool, kscale, vscale, table, seq_lens, hkv, num_blocks, max_seq, out_fp32=True,
+            fmt="e4m3", per_head=False):
     import torch
     kvq = _kvq()
     b, hq, d = q16.shape
@@ -106,14 +112,18 @@ def _decode(q16, kpool, vpool, kscale, vscale, table, seq_lens, hkv, num_blocks,
     wsb = kvq.fp8_decode_workspace_bytes(b, hq, d)
     ws = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
     kvq.fp8_decode_attention(dev(q16), kpool, vpool, kscale, vscale, dev(table), dev(seq_lens.astype(np.int32)),
-                             b, hq, hkv, d, 16, table.shape[1], num_blocks, max_seq, out, out_fp32, 0.0, ws, wsb)
+                             b, hq, hkv, d, 16, table.shape[1], num_blocks, max_seq, out, out_fp32, 0.0, ws, wsb,
+                             per_head=per_head, fp8_format=kvq.FP8_FORMATS[fmt])
     return host(out).astype(np.float64), int(host(ws[:4].view(torch.int32))[0])
 
 
-def _oracle_decode(q16, k16, v16, ks, vs, seq_lens, heads=None):
+def _oracle_decode(q16, k16, v16, ks, vs, seq_lens, heads=None, fmt="e4m3"):
+    """ks, vs: scalars, or one scale per kv head."""
     b, hkv, s, d = k16.shape
-    kh = lambda bi, hi: fp8.e4m3_decode(fp8.quantize(k16[bi, hi, : seq_lens[bi]], ks)) * np.float64(ks)
-    vh = lambda bi, hi: fp8.e4m3_decode(fp8.quantize(v16[bi, hi, : seq_lens[bi]], vs)) * np.float64(vs)
+    ksh = lambda hi: np.float32(ks[hi] if np.ndim(ks) else ks)
+    vsh = lambda hi: np.float32(vs[hi] if np.ndim(vs) else vs)
+    kh = lambda bi, hi: fp8.decode(fp8.quantize(k16[bi, hi, : seq_lens[bi]], ksh(hi), fmt), fmt) * np.float64(ksh(hi))
+    vh = lambda bi, hi: fp8.decode(fp8.quantize(v16[bi, hi, : seq_lens[bi]], vsh(hi), fmt), fmt) * np.float64(vsh(hi))
     return attention.decode_attention(q16, kh, vh, hkv, default_scale(d), heads)
 
 
@@ -177,3 +187,82 @@ def test_full_size_fp8_32k():
     assert_attention_close(out, ref, heads)
     del kpool, vpool
     torch.cuda.empty_cache()
+
+
+# ------------------------------------------------------- E5M2 and per-head scales
+def test_e5m2_all_fp16_values_cast_exactly():
+    """Every fp16 bit pattern (finite and not) through the GPU E5M2 cast at static scale 1."""
+    allh = np.arange(65536, dtype=np.uint16).view(np.float16)
+    x = allh.reshape(1, 4, 128, 128)
+    table = np.arange(8, dtype=np.int32).reshape(1, 8)
+    for vl in (0, 1):
+        pool, _ = _quantize(x, table, 8, vl, static_scale=1.0, fmt="e5m2")
+        assert np.array_equal(host(pool), _oracle_pool(x, table, 8, vl, np.float32(1.0), "e5m2"))
+
+
+def _head_ranged_inputs(b, h, s, d, seed):
+    x = workloads.make_inputs(b, h, 2 * h, d, s, 1, seed).k.astype(np.float32)
+    ranges = np.array([0.002, 1.0, 40.0, 0.0, 900.0, 3.0, 0.3, 7.0][:h], np.float32)
+    return (x * ranges.reshape(1, h, 1, 1)).astype(np.float16)     # one all-zero head
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("d", [64, 128])
+def test_dynamic_per_head_scales_and_bytes(fmt, d):
+    rng = np.random.default_rng(d + len(fmt))
+    b, h, s = 3, 6, 16 * 5 + 7
+    x = _head_ranged_inputs(b, h, s, d, 17)
+    nb = 6
+    table = rng.permutation(b * nb).astype(np.int32).reshape(b, nb)
+    for vl in (0, 1):
+        pool, scale = _quantize(x, table, b * nb, vl, fmt=fmt, per_head=True)
+        s_ref = fp8.dynamic_scale_per_head(x, fmt)
+        assert np.array_equal(host(scale), s_ref)
+        assert np.array_equal(host(pool), _oracle_pool(x, table, b * nb, vl, s_ref, fmt))
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_static_per_head_scales(fmt):
+    b, h, s, d = 2, 4, 48, 128
+    x = _head_ranged_inputs(b, h, s, d, 23)
+    table = np.arange(b * 3, dtype=np.int32).reshape(b, 3)
+    given = np.array([1.0, 0.5, 0.01, 3.0e-5], np.float32)       # head 2 (|x| to ~150) saturates in E4M3
+    pool, scale = _quantize(x, table, b * 3, 0, static_scale=given, fmt=fmt, per_head=True)
+    assert np.array_equal(host(scale), given)                     # read, not written
+    assert np.array_equal(host(pool), _oracle_pool(x, table, b * 3, 0, given, fmt))
+
+
+@pytest.mark.parametrize("special", [np.inf, np.nan])
+def test_dynamic_e5m2_with_non_finite_values(special):
+    x = workloads.make_inputs(1, 2, 4, 128, 32, 1, 6).k.copy()
+    x[0, 0, 3, 9] = special
+    table = np.arange(2, dtype=np.int32).reshape(1, 2)
+    for per_head in (False, True):
+        pool, scale = _quantize(x, table, 2, 0, fmt="e5m2", per_head=per_head)
+        s_ref = np.atleast_1d(fp8.dynamic_scale_per_head(x, "e5m2") if per_head else fp8.dynamic_scale(x, "e5m2"))
+        got = host(scale)
+        assert got.shape == s_ref.shape
+        assert np.array_equal(np.isnan(got), np.isnan(s_ref)) and np.array_equal(got[~np.isnan(got)],
+                                                                               s_ref[~np.isnan(got)])
+        want = _oracle_pool(x, table, 2, 0, s_ref if per_head else s_ref[0], "e5m2")
+        assert np.array_equal(host(pool), want)
+
+
+@pytest.mark.parametrize("fmt,per_head", [("e5m2", False), ("e4m3", True), ("e5m2", True)])
+@pytest.mark.parametrize("d,gq", [(128, 4), (64, 2), (128, 8)])
+def test_decode_format_and_scale_variants(fmt, per_head, d, gq):
+    rng = np.random.default_rng(d + gq + 31 * per_head)
+    b, hkv, s = 3, 2, 16 * 30 + 9
+    x = workloads.make_inputs(b, hkv, hkv * gq, d, s, 1, 61 + gq)
+    k = (x.k.astype(np.float32) * np.array([1.0, 25.0]).reshape(1, 2, 1, 1)).astype(np.float16)
+    nb = -(-s // 16)
+    table = rng.permutation(b * nb).astype(np.int32).reshape(b, nb)
+    kpool, kscale = _quantize(k, table, b * nb, 0, fmt=fmt, per_head=per_head)
+    vpool, vscale = _quantize(x.v, table, b * nb, 1, fmt=fmt, per_head=per_head)
+    seq_lens = np.array([s, 1, 16 * 11 + 3])
+    out, status = _decode(x.q[0], kpool, vpool, kscale, vscale, table, seq_lens, hkv, b * nb, s, fmt=fmt,
+                          per_head=per_head)
+    scale_of = fp8.dynamic_scale_per_head if per_head else fp8.dynamic_scale
+    ref = _oracle_decode(x.q[0], k, x.v, scale_of(k, fmt), scale_of(x.v, fmt), seq_lens, fmt=fmt)
+    assert_attention_close(out, ref)
+    assert status == 0
