@@ -46,7 +46,7 @@ METRIC = "decode-attn KV bytes GB/s (% of GB300 HBM peak); quantize tokens/s"
 # ncu summary of the decode kernel on the default workload; its "traffic-record:"
 # line holds DRAM bytes of one captured launch and a hash of the sources it ran
 DECODE_PROFILE = os.path.join(ROOT, "profiles", "kivi_decode_kernel_128k_stream.md")
-DECODE_SOURCES = ("kivi_kernels.cu", "kvq_device.cuh", "kvq_internal.h", "api.cu")
+DECODE_SOURCES = ("kivi_kernels.cu", "kvq_device.cuh")  # the decode kernel and its device helpers
 FALLBACK_HBM_GBS = 6800.0
 
 
