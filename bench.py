@@ -475,10 +475,30 @@ def run_table(args):
 
     names = args.table.split(",") if args.table != "all" else [
         workloads.MHA_4K.name, workloads.GQA_8K_2BIT.name, workloads.GQA_8K_4BIT.name, workloads.STREAM_128K.name,
-        workloads.FP8_32K.name, workloads.FP8_32K_E5M2_PH.name]
+        workloads.FP8_32K.name, workloads.FP8_32K_E5M2_PH.name, workloads.PAGED_GQA_8K.name,
+        workloads.PAGED_VAR_16K.name]
     for name in names:
         w = workloads.WORKLOADS[name]
-        if isinstance(w, workloads.KiviWorkload):
+        if isinstance(w, workloads.PagedKiviWorkload):
+            x, lens, table = workloads.paged_inputs(w, steps=1)
+            cache = kvq.PagedKiviCache(w.batch, w.kv_heads, w.q_heads, w.head_dim, w.k_bits, w.v_bits, w.residual,
+                                       w.max_tokens, w.num_blocks)
+            cache.table.copy_(dev(table))
+            k_d, v_d, q_d = dev(x.k), dev(x.v), dev(x.q[0])
+            t_pre = timed(lambda: cache.prefill(k_d, v_d, lens.tolist()), reps=5)
+            out = torch.empty((w.batch, w.q_heads, w.head_dim), dtype=torch.float32, device="cuda")
+            t_dec = timed(lambda: cache.decode(q_d, out=out))
+            ng = [cache.n_grouped(b) for b in range(w.batch)]
+            nr = [cache.n_resid(b) for b in range(w.batch)]
+            nbytes = metrics.kivi_paged_decode_bytes(w.kv_heads, w.q_heads, w.head_dim, w.k_bits, w.v_bits, ng, nr)
+            line = {"workload": w.name, "call": "kv_paged_decode_attention", "us": round(t_dec * 1e6, 2),
+                    "bytes": nbytes, "GB_s": round(nbytes / t_dec / 1e9, 1),
+                    "pct_of_hbm_peak": round(100 * nbytes / t_dec / 1e9 / hbm, 1),
+                    "tokens": int(lens.sum()), "prefill_us": round(t_pre * 1e6, 1),
+                    "quantize_tokens_per_s": round(float(lens.sum()) / t_pre, 1),
+                    "status": cache.status()}
+            del k_d, v_d, cache
+        elif isinstance(w, workloads.KiviWorkload):
             x = workloads.kivi_inputs(w, steps=1)
             cache = kvq.KiviCache(w.batch, w.kv_heads, w.q_heads, w.head_dim, w.k_bits, w.v_bits, w.residual,
                                   w.max_tokens)

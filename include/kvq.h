@@ -203,6 +203,106 @@ KVQ_API kvq_status kv_decode_attention_noalloc(const kivi_cache* cache, const ui
                                                int32_t out_fp32, float softmax_scale, void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* Paged, variable-length KIVI cache [KIVI section 3, CSDN section 13]       */
+/* ------------------------------------------------------------------------ */
+
+/* A batch of sequences of different lengths. Each sequence is a KIVI cache of
+ * its own (the rules above: prefill split, window, flush timing, all on the
+ * sequence's own length); its groups of 32 tokens live in blocks of shared
+ * pools, reached through a block table as in [CSDN] section 13. The pages
+ * combine the two ideas without fixing a layout; this one is the library's:
+ * one pool block holds one group of one sequence for every kv head, in the
+ * four records of the contiguous cache (same byte layout per record).
+ *
+ *   pools   : k_codes [num_blocks, H_kv, 32*D*k_bits/8], k_meta [num_blocks,
+ *             H_kv, 4*D], v_codes [num_blocks, H_kv, 32*D*v_bits/8], v_meta
+ *             [num_blocks, H_kv, 128]
+ *   windows : fp16 k_res, v_res [B, H_kv, res_cap, D], one per sequence
+ *   table   : device int32 block_table [B, groups_cap], groups_cap =
+ *             ceil(max_tokens / 32); entry [b, g] is the pool block of group g
+ *             of sequence b. The caller owns and fills it (the block
+ *             allocator is the caller's): every group a call writes or reads
+ *             needs an entry in [0, num_blocks), and two groups held at the
+ *             same time need different blocks. A quantize skips a group whose
+ *             entry is outside [0, num_blocks) (nothing is written); the decode
+ *             clamps such entries into the pool (wrong numbers, no access
+ *             outside it).
+ * Sequence b's state is n_grouped[b] (a multiple of 32) and n_resid[b], kept
+ * on the host in the descriptor. Groups written by a call: prefill, groups 0
+ * .. n_grouped[b]/32 - 1 after it; append, when n_resid[b] == res_cap before
+ * it (R > 0), groups n_grouped[b]/32 .. + R/32 - 1, and with R = 0, when
+ * n_resid[b] == 31, group n_grouped[b]/32; flush, groups n_grouped[b]/32 ..
+ * + floor(n_resid[b]/32) - 1. */
+#define KVQ_PAGED_MAX_SEQS 256
+
+/* cfg.batch is the number of sequences (1 .. KVQ_PAGED_MAX_SEQS), cfg.max_tokens
+ * the capacity of one sequence; num_blocks >= 1 is the pool size in blocks. */
+typedef struct {
+  kivi_config cfg;
+  int32_t num_blocks;
+} kivi_paged_config;
+
+typedef struct {
+  kivi_paged_config pcfg;
+  uint8_t* k_codes;
+  uint8_t* k_meta;
+  uint8_t* v_codes;
+  uint8_t* v_meta;
+  uint16_t* k_res;
+  uint16_t* v_res;
+  const int32_t* block_table;
+  int32_t groups_cap;  /* block-table row length, ceil(max_tokens / 32)       */
+  int32_t res_cap;     /* R, or 32 when R = 0                                 */
+  int32_t n_grouped[KVQ_PAGED_MAX_SEQS];
+  int32_t n_resid[KVQ_PAGED_MAX_SEQS];
+} kivi_paged_cache;
+
+/* Byte sizes of the six buffers (k_codes, k_meta, v_codes, v_meta pools, then
+ * the k_res, v_res windows). */
+KVQ_API kvq_status kivi_paged_cache_sizes(const kivi_paged_config* cfg, size_t bytes_out[6]);
+
+/* Fill a descriptor for caller buffers bufs[6] and the caller's block table
+ * (device int32 [B, groups_cap]). Every sequence starts empty. No device work.
+ * KVQ_ERR_UNSUPPORTED for more than KVQ_PAGED_MAX_SEQS sequences. */
+KVQ_API kvq_status kivi_paged_cache_init(kivi_paged_cache* cache, const kivi_paged_config* cfg,
+                                         void* const bufs[6], const int32_t* block_table);
+
+/* Prefill every sequence: sequence b starts from its first seq_lens[b] tokens
+ * of k, v (device fp16 [B, H_kv, max_seq_len, D]); seq_lens is a HOST int32
+ * array of B entries in [0, max_seq_len]. Each sequence is split as
+ * kv_quant_prefill splits one cache (0 tokens leave it empty); one quantize
+ * and one copy launch serve all sequences. Previous content is discarded.
+ * KVQ_ERR_CAPACITY if some seq_lens[b] > max_tokens. */
+KVQ_API kvq_status kv_paged_prefill(kivi_paged_cache* cache, const uint16_t* k, const uint16_t* v,
+                                    int32_t max_seq_len, const int32_t* seq_lens, void* stream);
+
+/* Append one token to every sequence: k_new, v_new device fp16 [B, H_kv, D].
+ * Each sequence flushes as kv_append_token does (full windows are flushed
+ * before the copy, a full 32-slot stage right after it when R = 0), batched
+ * into one quantize launch. KVQ_ERR_CAPACITY if some sequence already holds
+ * max_tokens tokens. */
+KVQ_API kvq_status kv_paged_append(kivi_paged_cache* cache, const uint16_t* k_new, const uint16_t* v_new,
+                                   void* stream);
+
+/* Flush every sequence as kv_flush_residual flushes one cache. */
+KVQ_API kvq_status kv_paged_flush(kivi_paged_cache* cache, void* stream);
+
+/* Workspace of kv_paged_decode_attention (the layout and rules of
+ * kv_decode_workspace_bytes, B = the number of sequences). */
+KVQ_API size_t kv_paged_decode_workspace_bytes(const kivi_paged_config* cfg);
+
+/* Decode attention of one new token per sequence, as kv_decode_attention,
+ * over sequence b's own grouped tokens then window tokens. q: device fp16
+ * [B, H_q, D]; out: device [B, H_q, D] (fp32 if out_fp32). The work of all
+ * (sequence, kv head) pairs is cut into equal slices of one launch whatever
+ * the lengths (split-K across pairs, one partial per pair a slice touches,
+ * log-sum-exp merge by the last slice of each pair). KVQ_ERR_ARG if some
+ * sequence is empty. */
+KVQ_API kvq_status kv_paged_decode_attention(const kivi_paged_cache* cache, const uint16_t* q, void* out,
+                                             int32_t out_fp32, float softmax_scale, void* ws,
+                                             size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* FP8 E4M3 paged cache [KIVI section 5, CSDN section 10, YUN]               */
 /* ------------------------------------------------------------------------ */
 

@@ -243,6 +243,141 @@ kvq::KiviDecodeArgs kivi_decode_args(const kivi_cache* cache, const DecodePlan& 
   return a;
 }
 
+// ---------------------------------------------------------------------------
+// Paged, variable-length cache
+// ---------------------------------------------------------------------------
+kvq_status check_paged_config(const kivi_paged_config* c) {
+  if (c == nullptr) return KVQ_ERR_NULL;
+  const kvq_status st = check_config(&c->cfg);
+  if (st != KVQ_OK) return st;
+  if (c->cfg.batch > KVQ_PAGED_MAX_SEQS) return KVQ_ERR_UNSUPPORTED;
+  if (c->num_blocks <= 0) return KVQ_ERR_ARG;
+  return KVQ_OK;
+}
+
+void paged_record_bytes(const kivi_paged_config* pc, size_t out[6]) {
+  const kivi_config* c = &pc->cfg;
+  const size_t rows = static_cast<size_t>(pc->num_blocks) * c->kv_heads;
+  const size_t d = static_cast<size_t>(c->head_dim);
+  out[0] = rows * (32 * d * c->k_bits / 8);
+  out[1] = rows * (4 * d);
+  out[2] = rows * (32 * d * c->v_bits / 8);
+  out[3] = rows * 128;
+  out[4] = static_cast<size_t>(c->batch) * c->kv_heads * static_cast<size_t>(res_cap_of(c)) * d * 2;
+  out[5] = out[4];
+}
+
+kvq_status check_paged_cache(const kivi_paged_cache* cache) {
+  if (cache == nullptr) return KVQ_ERR_NULL;
+  const kvq_status st = check_paged_config(&cache->pcfg);
+  if (st != KVQ_OK) return st;
+  if (!cache->k_codes || !cache->k_meta || !cache->v_codes || !cache->v_meta || !cache->k_res || !cache->v_res ||
+      !cache->block_table)
+    return KVQ_ERR_NULL;
+  const kivi_config& cf = cache->pcfg.cfg;
+  if (cache->groups_cap != groups_cap_of(&cf) || cache->res_cap != res_cap_of(&cf)) return KVQ_ERR_ARG;
+  for (int b = 0; b < cf.batch; ++b) {
+    const int ng = cache->n_grouped[b], nr = cache->n_resid[b];
+    if (ng < 0 || ng % kGroup != 0 || nr < 0 || nr > cache->res_cap) return KVQ_ERR_ARG;
+    if (static_cast<long long>(ng) + nr > cf.max_tokens) return KVQ_ERR_ARG;
+    if (cf.residual_len == 0 && nr >= kGroup) return KVQ_ERR_ARG;
+  }
+  return KVQ_OK;
+}
+
+// One batched quantize: sequence b's counts[b] groups, read from source token
+// src0[b] of its rows, written to its logical groups dst0[b] on.
+kvq_status paged_quantize(const kivi_paged_cache* c, const uint16_t* k_src, const uint16_t* v_src,
+                          long long src_bh_stride, const int* counts, const int* src0, const int* dst0,
+                          cudaStream_t s) {
+  const kivi_config& cf = c->pcfg.cfg;
+  kvq::PagedQuantArgs a{};
+  long long total = 0;
+  for (int b = 0; b < cf.batch; ++b) {
+    a.r.begin[b] = static_cast<int>(total);
+    a.r.src0[b] = src0[b];
+    a.r.dst0[b] = dst0[b];
+    total += counts[b];
+    if (total > INT_MAX) return KVQ_ERR_UNSUPPORTED;
+  }
+  a.r.begin[cf.batch] = static_cast<int>(total);
+  if (total == 0) return KVQ_OK;
+  a.q.k_src = k_src;
+  a.q.v_src = v_src;
+  a.q.src_bh_stride = src_bh_stride;
+  a.q.batch = cf.batch;
+  a.q.kv_heads = cf.kv_heads;
+  a.q.head_dim = cf.head_dim;
+  a.q.k_bits = cf.k_bits;
+  a.q.v_bits = cf.v_bits;
+  a.q.groups_cap = c->groups_cap;
+  a.q.k_codes = c->k_codes;
+  a.q.k_meta = c->k_meta;
+  a.q.v_codes = c->v_codes;
+  a.q.v_meta = c->v_meta;
+  a.pools.block_table = c->block_table;
+  a.pools.groups_cap = c->groups_cap;
+  a.pools.num_blocks = c->pcfg.num_blocks;
+  a.n_seqs = cf.batch;
+  return from_cuda(kvq::launch_kivi_quantize_paged(a, s));
+}
+
+// One batched token copy into the windows: sequence b's counts[b] tokens from
+// source row src0[b] to window row dst0[b].
+kvq_status paged_copy(const kivi_paged_cache* c, const uint16_t* k_src, const uint16_t* v_src,
+                      long long src_bh_stride, const int* counts, const int* src0, const int* dst0, cudaStream_t s) {
+  const kivi_config& cf = c->pcfg.cfg;
+  kvq::PagedCopyArgs a{};
+  long long total = 0;
+  for (int b = 0; b < cf.batch; ++b) {
+    a.r.begin[b] = static_cast<int>(total);
+    a.r.src0[b] = src0[b];
+    a.r.dst0[b] = dst0[b];
+    total += counts[b];
+    if (total > INT_MAX) return KVQ_ERR_UNSUPPORTED;
+  }
+  a.r.begin[cf.batch] = static_cast<int>(total);
+  if (total == 0) return KVQ_OK;
+  a.c.k_src = k_src;
+  a.c.v_src = v_src;
+  a.c.src_bh_stride = src_bh_stride;
+  a.c.k_dst = c->k_res;
+  a.c.v_dst = c->v_res;
+  a.c.dst_bh_stride = static_cast<long long>(c->res_cap) * cf.head_dim;
+  a.c.bh = cf.batch * cf.kv_heads;
+  a.c.head_dim = cf.head_dim;
+  a.kv_heads = cf.kv_heads;
+  a.n_seqs = cf.batch;
+  return from_cuda(kvq::launch_copy_tokens_paged(a, s));
+}
+
+// Flush the window head of the sequences with counts[b] > 0 groups to flush:
+// quantize them into groups n_grouped[b]/32 on, move what is left of the
+// window (fewer than 32 tokens) to its front, and update the state.
+kvq_status paged_flush_groups(kivi_paged_cache* c, const int* counts, cudaStream_t s) {
+  const int B = c->pcfg.cfg.batch;
+  int src0[KVQ_PAGED_MAX_SEQS], dst0[KVQ_PAGED_MAX_SEQS], rest[KVQ_PAGED_MAX_SEQS], from[KVQ_PAGED_MAX_SEQS];
+  for (int b = 0; b < B; ++b) {
+    src0[b] = 0;
+    dst0[b] = c->n_grouped[b] / kGroup;
+    from[b] = kGroup * counts[b];
+    rest[b] = counts[b] > 0 ? c->n_resid[b] - from[b] : 0;  // < 32 <= from[b]: no overlap
+    if (rest[b] < 0) return KVQ_ERR_ARG;
+  }
+  const long long win_stride = static_cast<long long>(c->res_cap) * c->pcfg.cfg.head_dim;
+  kvq_status st = paged_quantize(c, c->k_res, c->v_res, win_stride, counts, src0, dst0, s);
+  if (st != KVQ_OK) return st;
+  for (int b = 0; b < B; ++b) dst0[b] = 0;
+  st = paged_copy(c, c->k_res, c->v_res, win_stride, rest, from, dst0, s);
+  if (st != KVQ_OK) return st;
+  for (int b = 0; b < B; ++b) {
+    if (counts[b] == 0) continue;
+    c->n_grouped[b] += from[b];
+    c->n_resid[b] = rest[b];
+  }
+  return KVQ_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -418,6 +553,199 @@ kvq_status kv_decode_attention(const kivi_cache* cache, const uint16_t* q, void*
   const DecodePlan plan = plan_kivi_decode(cache);
   const kvq::KiviDecodeArgs a = kivi_decode_args(cache, plan, q, out, out_fp32, scale, static_cast<uint8_t*>(ws));
   return from_cuda(kvq::launch_kivi_decode(a, static_cast<cudaStream_t>(stream)));
+}
+
+kvq_status kivi_paged_cache_sizes(const kivi_paged_config* cfg, size_t bytes_out[6]) {
+  const kvq_status st = check_paged_config(cfg);
+  if (st != KVQ_OK) return st;
+  if (bytes_out == nullptr) return KVQ_ERR_NULL;
+  paged_record_bytes(cfg, bytes_out);
+  return KVQ_OK;
+}
+
+kvq_status kivi_paged_cache_init(kivi_paged_cache* cache, const kivi_paged_config* cfg, void* const bufs[6],
+                                 const int32_t* block_table) {
+  if (cache == nullptr || bufs == nullptr || block_table == nullptr) return KVQ_ERR_NULL;
+  const kvq_status st = check_paged_config(cfg);
+  if (st != KVQ_OK) return st;
+  for (int i = 0; i < 6; ++i) {
+    if (bufs[i] == nullptr) return KVQ_ERR_NULL;
+    if (!aligned(bufs[i])) return KVQ_ERR_ALIGN;
+  }
+  if (!aligned(block_table)) return KVQ_ERR_ALIGN;
+  kivi_paged_cache c{};
+  c.pcfg = *cfg;
+  c.k_codes = static_cast<uint8_t*>(bufs[0]);
+  c.k_meta = static_cast<uint8_t*>(bufs[1]);
+  c.v_codes = static_cast<uint8_t*>(bufs[2]);
+  c.v_meta = static_cast<uint8_t*>(bufs[3]);
+  c.k_res = static_cast<uint16_t*>(bufs[4]);
+  c.v_res = static_cast<uint16_t*>(bufs[5]);
+  c.block_table = block_table;
+  c.groups_cap = groups_cap_of(&cfg->cfg);
+  c.res_cap = res_cap_of(&cfg->cfg);
+  *cache = c;
+  return KVQ_OK;
+}
+
+kvq_status kv_paged_prefill(kivi_paged_cache* cache, const uint16_t* k, const uint16_t* v, int32_t max_seq_len,
+                            const int32_t* seq_lens, void* stream) {
+  kvq_status st = check_paged_cache(cache);
+  if (st != KVQ_OK) return st;
+  if (seq_lens == nullptr) return KVQ_ERR_NULL;
+  if (max_seq_len < 0) return KVQ_ERR_ARG;
+  const kivi_config& cf = cache->pcfg.cfg;
+  const int B = cf.batch, R = cf.residual_len;
+  int groups[KVQ_PAGED_MAX_SEQS], resid[KVQ_PAGED_MAX_SEQS], zero[KVQ_PAGED_MAX_SEQS], from[KVQ_PAGED_MAX_SEQS];
+  bool any = false;
+  for (int b = 0; b < B; ++b) {
+    const int L = seq_lens[b];
+    if (L < 0 || L > max_seq_len) return KVQ_ERR_ARG;
+    if (L > cf.max_tokens) return KVQ_ERR_CAPACITY;
+    const int grouped = (R > 0) ? kGroup * ceil_div(std::max(L - R, 0), kGroup) : kGroup * (L / kGroup);
+    groups[b] = grouped / kGroup;
+    resid[b] = L - grouped;
+    from[b] = grouped;
+    zero[b] = 0;
+    any = any || L > 0;
+  }
+  if (any && (k == nullptr || v == nullptr)) return KVQ_ERR_NULL;
+  if (any && (!aligned(k) || !aligned(v))) return KVQ_ERR_ALIGN;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const long long src_stride = static_cast<long long>(max_seq_len) * cf.head_dim;
+  st = paged_quantize(cache, k, v, src_stride, groups, zero, zero, s);
+  if (st != KVQ_OK) return st;
+  st = paged_copy(cache, k, v, src_stride, resid, from, zero, s);
+  if (st != KVQ_OK) return st;
+  for (int b = 0; b < B; ++b) {
+    cache->n_grouped[b] = kGroup * groups[b];
+    cache->n_resid[b] = resid[b];
+  }
+  return KVQ_OK;
+}
+
+kvq_status kv_paged_append(kivi_paged_cache* cache, const uint16_t* k_new, const uint16_t* v_new, void* stream) {
+  kvq_status st = check_paged_cache(cache);
+  if (st != KVQ_OK) return st;
+  if (k_new == nullptr || v_new == nullptr) return KVQ_ERR_NULL;
+  if (!aligned(k_new) || !aligned(v_new)) return KVQ_ERR_ALIGN;
+  const kivi_config& cf = cache->pcfg.cfg;
+  const int B = cf.batch;
+  for (int b = 0; b < B; ++b)
+    if (cache->n_grouped[b] + cache->n_resid[b] + 1 > cf.max_tokens) return KVQ_ERR_CAPACITY;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  kivi_paged_cache c = *cache;
+  int counts[KVQ_PAGED_MAX_SEQS], one[KVQ_PAGED_MAX_SEQS], zero[KVQ_PAGED_MAX_SEQS], row[KVQ_PAGED_MAX_SEQS];
+  bool flush = false;
+  for (int b = 0; b < B; ++b) {  // full windows first (R > 0)
+    counts[b] = (c.n_resid[b] == c.res_cap) ? c.res_cap / kGroup : 0;
+    flush = flush || counts[b] > 0;
+  }
+  if (flush) {
+    st = paged_flush_groups(&c, counts, s);
+    if (st != KVQ_OK) return st;
+  }
+  for (int b = 0; b < B; ++b) {
+    one[b] = 1;
+    zero[b] = 0;
+    row[b] = c.n_resid[b];
+  }
+  st = paged_copy(&c, k_new, v_new, cf.head_dim, one, zero, row, s);
+  if (st != KVQ_OK) return st;
+  flush = false;
+  for (int b = 0; b < B; ++b) {
+    c.n_resid[b] += 1;
+    counts[b] = (cf.residual_len == 0 && c.n_resid[b] == kGroup) ? 1 : 0;  // a full 32-slot stage (R = 0)
+    flush = flush || counts[b] > 0;
+  }
+  if (flush) {
+    st = paged_flush_groups(&c, counts, s);
+    if (st != KVQ_OK) return st;
+  }
+  *cache = c;
+  return KVQ_OK;
+}
+
+kvq_status kv_paged_flush(kivi_paged_cache* cache, void* stream) {
+  kvq_status st = check_paged_cache(cache);
+  if (st != KVQ_OK) return st;
+  int counts[KVQ_PAGED_MAX_SEQS];
+  bool any = false;
+  for (int b = 0; b < cache->pcfg.cfg.batch; ++b) {
+    counts[b] = cache->n_resid[b] / kGroup;
+    any = any || counts[b] > 0;
+  }
+  if (!any) return KVQ_OK;
+  kivi_paged_cache c = *cache;
+  st = paged_flush_groups(&c, counts, static_cast<cudaStream_t>(stream));
+  if (st != KVQ_OK) return st;
+  *cache = c;
+  return KVQ_OK;
+}
+
+size_t kv_paged_decode_workspace_bytes(const kivi_paged_config* cfg) {
+  if (check_paged_config(cfg) != KVQ_OK) return 0;
+  return decode_ws_bytes(cfg->cfg.batch, cfg->cfg.q_heads, cfg->cfg.head_dim);
+}
+
+kvq_status kv_paged_decode_attention(const kivi_paged_cache* cache, const uint16_t* q, void* out, int32_t out_fp32,
+                                     float softmax_scale, void* ws, size_t ws_bytes, void* stream) {
+  kvq_status st = check_paged_cache(cache);
+  if (st != KVQ_OK) return st;
+  if (q == nullptr || out == nullptr) return KVQ_ERR_NULL;
+  if (!aligned(q) || !aligned(out)) return KVQ_ERR_ALIGN;
+  if (ws == nullptr) return KVQ_ERR_WORKSPACE;
+  if (!aligned(ws)) return KVQ_ERR_ALIGN;
+  const kivi_config& cf = cache->pcfg.cfg;
+  if (ws_bytes < decode_ws_bytes(cf.batch, cf.q_heads, cf.head_dim)) return KVQ_ERR_WORKSPACE;
+  if (!(softmax_scale == softmax_scale) || std::isinf(softmax_scale)) return KVQ_ERR_ARG;
+  const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(cf.head_dim));
+
+  // Units of every (sequence, kv head) pair, one pair after the other, cut
+  // into equal stream-K slices: about one slice per resident block, at least
+  // kMinUnitsPerSplit units, and at most kMaxSplits - 1 slices over the
+  // longest pair (its partials fit the workspace).
+  kvq::PagedSeqs seqs{};
+  seqs.pools.block_table = cache->block_table;
+  seqs.pools.groups_cap = cache->groups_cap;
+  seqs.pools.num_blocks = cache->pcfg.num_blocks;
+  seqs.n_seqs = cf.batch;
+  long long total = 0;
+  int max_u = 0;
+  for (int b = 0; b < cf.batch; ++b) {
+    const int ng = cache->n_grouped[b] / kGroup, nr = cache->n_resid[b];
+    if (ng + nr == 0) return KVQ_ERR_ARG;
+    const int U = ng + kvq::kChunkUnits * ceil_div(nr, kGroup);
+    seqs.unit0[b] = static_cast<int>(total);
+    seqs.n_groups[b] = ng;
+    seqs.n_resid[b] = nr;
+    total += static_cast<long long>(cf.kv_heads) * U;
+    if (total > INT_MAX) return KVQ_ERR_UNSUPPORTED;
+    max_u = std::max(max_u, U);
+  }
+  seqs.unit0[cf.batch] = static_cast<int>(total);
+  const long long slots = static_cast<long long>(kvq::device_sm_count()) *
+                          std::max(1, kvq::kivi_paged_decode_blocks_per_sm(cf.head_dim, cf.k_bits, cf.v_bits));
+  long long per = (total + slots - 1) / slots;
+  per = std::max<long long>(per, kMinUnitsPerSplit);
+  per = std::max<long long>(per, ceil_div(max_u, kMaxSplits - 1));
+  DecodePlan plan{};
+  plan.units_per_block = static_cast<int>(per);
+  plan.n_blocks = static_cast<int>((total + per - 1) / per);
+  plan.part_stride = std::min(kMaxSplits, ceil_div(max_u, per) + 1);
+
+  kivi_cache view{};
+  view.cfg = cf;
+  view.k_codes = cache->k_codes;
+  view.k_meta = cache->k_meta;
+  view.v_codes = cache->v_codes;
+  view.v_meta = cache->v_meta;
+  view.k_res = cache->k_res;
+  view.v_res = cache->v_res;
+  view.groups_cap = cache->groups_cap;
+  view.res_cap = cache->res_cap;
+  const kvq::KiviDecodeArgs a = kivi_decode_args(&view, plan, q, out, out_fp32, scale, static_cast<uint8_t*>(ws));
+  return from_cuda(kvq::launch_kivi_decode_paged(a, seqs, static_cast<cudaStream_t>(stream)));
 }
 
 size_t fp8_quantize_workspace_bytes(int32_t batch, int32_t kv_heads, int32_t seq_len, int32_t head_dim) {

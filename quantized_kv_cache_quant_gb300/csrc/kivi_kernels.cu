@@ -10,6 +10,7 @@
 // section 2, with grouped-query sharing (section 5).
 #include <cfloat>
 #include <cmath>
+#include <type_traits>
 
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
@@ -120,8 +121,13 @@ __device__ __forceinline__ uint32_t value_word(const __half* xv, int RS, const f
   return w;
 }
 
+// Quantize and pack one group of 32 tokens of one (batch row, kv head): the
+// fp16 rows k_src[0 .. 32*D) and v_src[...] (32 consecutive tokens of D
+// channels) become the four records at kc, km, vc and vm. Run by a whole
+// block of 128 threads.
 template <int D, int KB, int VB>
-__global__ void __launch_bounds__(128) kivi_quantize_kernel(QuantGroupsArgs a) {
+__device__ __forceinline__ void quantize_group(const uint16_t* k_src, const uint16_t* v_src, uint8_t* kc, uint8_t* km,
+                                               uint8_t* vc, uint8_t* vm) {
   using P = Kivi<D, KB, VB>;
   constexpr int RS = D + 8;  // padded row stride (halves): rows start 4 banks apart
   __shared__ __align__(16) __half xk[32 * RS];
@@ -135,12 +141,10 @@ __global__ void __launch_bounds__(128) kivi_quantize_kernel(QuantGroupsArgs a) {
   __shared__ __align__(8) float rv[32];
   __shared__ uint16_t skb[D], zkb[D], svb[32], zvb[32];           // fp16 bits of scale and zero
 
-  const int grp = blockIdx.x, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
+  const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const long long bh = static_cast<long long>(b) * a.kv_heads + h;
-  const long long src_off = bh * a.src_bh_stride + static_cast<long long>(a.src_tok0 + 32 * grp) * D;
-  const uint4* srck = reinterpret_cast<const uint4*>(a.k_src + src_off);
-  const uint4* srcv = reinterpret_cast<const uint4*>(a.v_src + src_off);
+  const uint4* srck = reinterpret_cast<const uint4*>(k_src);
+  const uint4* srcv = reinterpret_cast<const uint4*>(v_src);
 #pragma unroll
   for (int i = tid; i < 32 * D / 8; i += 128) {
     const int row = i / (D / 8), c8 = i % (D / 8);
@@ -204,8 +208,6 @@ __global__ void __launch_bounds__(128) kivi_quantize_kernel(QuantGroupsArgs a) {
   }
   __syncthreads();
 
-  const long long grp_index = bh * a.groups_cap + a.dst_group0 + grp;
-
   // Code words, computed straight from the staged tile: warps 0-1 the key
   // words, warps 2-3 the value words. Storage words 4*ug .. 4*ug + 3 of
   // fragment lane L are one 16-byte chunk (uint4 ug*32 + L); lane L of a warp
@@ -213,7 +215,7 @@ __global__ void __launch_bounds__(128) kivi_quantize_kernel(QuantGroupsArgs a) {
   // fragment lanes on the same word (conflict-free) and each store writes 512
   // contiguous bytes.
   if (warp < 2) {
-    uint4* kdst = reinterpret_cast<uint4*>(a.k_codes + grp_index * P::KC);
+    uint4* kdst = reinterpret_cast<uint4*>(kc);
     for (int ug = warp; ug < P::KW / 4; ug += 2) {
       uint4 w;
       w.x = key_word<D, KB>(xk, RS, sk, zk, rk, 4 * ug, lane >> 2, lane & 3);
@@ -223,7 +225,7 @@ __global__ void __launch_bounds__(128) kivi_quantize_kernel(QuantGroupsArgs a) {
       kdst[ug * 32 + lane] = w;
     }
   } else {
-    uint4* vdst = reinterpret_cast<uint4*>(a.v_codes + grp_index * P::VC);
+    uint4* vdst = reinterpret_cast<uint4*>(vc);
     for (int ug = warp - 2; ug < P::VW / 4; ug += 2) {
       uint4 w;
       w.x = value_word<D, VB>(xv, RS, sv, zv, rv, 4 * ug, lane >> 2, lane & 3);
@@ -242,7 +244,7 @@ __global__ void __launch_bounds__(128) kivi_quantize_kernel(QuantGroupsArgs a) {
     rec.y = skb[d0 + 8] | (static_cast<uint32_t>(skb[d0 + 9]) << 16);
     rec.z = zkb[d0] | (static_cast<uint32_t>(zkb[d0 + 1]) << 16);
     rec.w = zkb[d0 + 8] | (static_cast<uint32_t>(zkb[d0 + 9]) << 16);
-    reinterpret_cast<uint4*>(a.k_meta + grp_index * P::KM)[tid] = rec;
+    reinterpret_cast<uint4*>(km)[tid] = rec;
   } else if (tid >= 64 && tid < 72) {
     // Value meta: 4 records of scales, then 4 of zero points.
     const int i = tid - 64, tg = i & 3;
@@ -252,8 +254,55 @@ __global__ void __launch_bounds__(128) kivi_quantize_kernel(QuantGroupsArgs a) {
     rec.y = src[8 + 2 * tg] | (static_cast<uint32_t>(src[9 + 2 * tg]) << 16);
     rec.z = src[16 + 2 * tg] | (static_cast<uint32_t>(src[17 + 2 * tg]) << 16);
     rec.w = src[24 + 2 * tg] | (static_cast<uint32_t>(src[25 + 2 * tg]) << 16);
-    reinterpret_cast<uint4*>(a.v_meta + grp_index * P::VM)[i] = rec;
+    reinterpret_cast<uint4*>(vm)[i] = rec;
   }
+}
+
+// Grid (groups, H_kv, B): group blockIdx.x of the source rows from src_tok0 on
+// goes to group dst_group0 + blockIdx.x of the contiguous grouped region.
+template <int D, int KB, int VB>
+__global__ void __launch_bounds__(128) kivi_quantize_kernel(QuantGroupsArgs a) {
+  using P = Kivi<D, KB, VB>;
+  const int grp = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const long long bh = static_cast<long long>(b) * a.kv_heads + h;
+  const long long src_off = bh * a.src_bh_stride + static_cast<long long>(a.src_tok0 + 32 * grp) * D;
+  const long long gi = bh * a.groups_cap + a.dst_group0 + grp;
+  quantize_group<D, KB, VB>(a.k_src + src_off, a.v_src + src_off, a.k_codes + gi * P::KC, a.k_meta + gi * P::KM,
+                            a.v_codes + gi * P::VC, a.v_meta + gi * P::VM);
+}
+
+// The sequence that owns item x of a batched launch: the b < n with
+// begin[b] <= x < begin[b + 1] (begin is non-decreasing, begin[0] = 0 <= x <
+// begin[n]). Binary search over the parameter array.
+__device__ __forceinline__ int seq_of(const int* begin, int n, long long x) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (begin[mid] <= x)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  return lo;
+}
+
+// Grid (total groups, H_kv): item blockIdx.x is group x - begin[b] of sequence
+// b's range, read from source token src0[b] + 32 * (x - begin[b]) and written
+// to the pool block of logical group dst0[b] + (x - begin[b]). A block-table
+// entry outside [0, num_blocks) is skipped: nothing is written for it.
+template <int D, int KB, int VB>
+__global__ void __launch_bounds__(128) kivi_quantize_paged_kernel(PagedQuantArgs a) {
+  using P = Kivi<D, KB, VB>;
+  const int x = blockIdx.x, h = blockIdx.y;
+  const int b = seq_of(a.r.begin, a.n_seqs, x);
+  const int grp = x - a.r.begin[b];
+  const long long bh = static_cast<long long>(b) * a.q.kv_heads + h;
+  const long long src_off = bh * a.q.src_bh_stride + static_cast<long long>(a.r.src0[b] + 32 * grp) * D;
+  const int blk = __ldg(a.pools.block_table + static_cast<long long>(b) * a.pools.groups_cap + a.r.dst0[b] + grp);
+  if (blk < 0 || blk >= a.pools.num_blocks) return;
+  const long long ri = static_cast<long long>(blk) * a.q.kv_heads + h;
+  quantize_group<D, KB, VB>(a.q.k_src + src_off, a.q.v_src + src_off, a.q.k_codes + ri * P::KC,
+                            a.q.k_meta + ri * P::KM, a.q.v_codes + ri * P::VC, a.q.v_meta + ri * P::VM);
 }
 
 // ---------------------------------------------------------------------------
@@ -275,6 +324,30 @@ __global__ void copy_tokens_kernel(CopyTokensArgs a) {
     const long long d = (bh * a.dst_bh_stride + (a.dst_tok0 + tok) * a.head_dim) / 8 + v;
     reinterpret_cast<uint4*>(a.k_dst)[d] = reinterpret_cast<const uint4*>(a.k_src)[s];
     reinterpret_cast<uint4*>(a.v_dst)[d] = reinterpret_cast<const uint4*>(a.v_src)[s];
+  }
+}
+
+// Batched copies of a paged cache: token x of the launch (x < begin[n]) is
+// token x - begin[b] of sequence b's range; for each kv head h its D channels
+// go from source row src0[b] + (x - begin[b]) of (b, h) to window row
+// dst0[b] + (x - begin[b]). Sources and destinations of one launch do not
+// overlap.
+__global__ void copy_tokens_paged_kernel(PagedCopyArgs a) {
+  asm volatile("griddepcontrol.launch_dependents;");
+  const int vec_per_tok = a.c.head_dim / 8;
+  const long long per_tok = static_cast<long long>(a.kv_heads) * vec_per_tok;
+  const long long total = static_cast<long long>(a.r.begin[a.n_seqs]) * per_tok;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long x = i / per_tok, rem = i % per_tok;
+    const int h = static_cast<int>(rem / vec_per_tok), v = static_cast<int>(rem % vec_per_tok);
+    const int b = seq_of(a.r.begin, a.n_seqs, x);
+    const long long tok = x - a.r.begin[b];
+    const long long bh = static_cast<long long>(b) * a.kv_heads + h;
+    const long long s = (bh * a.c.src_bh_stride + (a.r.src0[b] + tok) * a.c.head_dim) / 8 + v;
+    const long long d = (bh * a.c.dst_bh_stride + (a.r.dst0[b] + tok) * a.c.head_dim) / 8 + v;
+    reinterpret_cast<uint4*>(a.c.k_dst)[d] = reinterpret_cast<const uint4*>(a.c.k_src)[s];
+    reinterpret_cast<uint4*>(a.c.v_dst)[d] = reinterpret_cast<const uint4*>(a.c.v_src)[s];
   }
 }
 
@@ -453,9 +526,14 @@ __device__ __noinline__ bool window_chunks(const uint16_t* k_res, const uint16_t
   return ok;
 }
 
-template <int D, int KB, int VB, int STAGES>
-__global__ void __launch_bounds__(128, KVQ_DECODE_MIN_BLOCKS) kivi_decode_kernel(KiviDecodeArgs a) {
+// Sequence state of the contiguous cache: every pair has a.n_groups groups and
+// a.n_resid window tokens, at unit p * pair_stride.
+struct NoSeqs {};
+
+template <int D, int KB, int VB, int STAGES, class SeqT>
+__global__ void __launch_bounds__(128, KVQ_DECODE_MIN_BLOCKS) kivi_decode_kernel(KiviDecodeArgs a, SeqT seqs) {
   using P = Kivi<D, KB, VB>;
+  constexpr bool kPaged = !std::is_same<SeqT, NoSeqs>::value;
   using S = DecodeSmem<D, KB, VB, STAGES>;
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
@@ -484,34 +562,51 @@ __global__ void __launch_bounds__(128, KVQ_DECODE_MIN_BLOCKS) kivi_decode_kernel
 
   // This block's slice [u0, u1) of all units, pair after pair; one segment
   // (and one partial) per (batch row, kv head) it touches.
-  const long long all_units = static_cast<long long>(a.n_pairs) * a.pair_stride;
+  long long all_units = static_cast<long long>(a.n_pairs) * a.pair_stride;
+  if constexpr (kPaged) all_units = seqs.unit0[seqs.n_seqs];
   const long long u0 = static_cast<long long>(blockIdx.x) * a.units_per_block;
   const long long u1 = min(all_units, u0 + a.units_per_block);
   int jg = 0;               // slots this warp has filled so far: ring position and phase of the next
   uint32_t wphase = 0;      // phase of the window barrier
   bool timed_out = false;   // sticky: after a wait gives up the warp starts no more copies
   for (long long u = u0; u < u1;) {
-    const int pair = static_cast<int>(u / a.pair_stride);
-    const long long pbase = static_cast<long long>(pair) * a.pair_stride;
-    const int lo = static_cast<int>(u - pbase);
-    const int hi = static_cast<int>(min(static_cast<long long>(a.units_per_pair), u1 - pbase));
-    u = pbase + a.pair_stride;
-    if (lo >= a.units_per_pair) continue;  // padding after the pair's units (the same for the whole block)
+    int pair, upp, n_grp, n_res;  // the pair, its units, groups and window tokens
+    long long pbase;              // its first unit
+    if constexpr (kPaged) {
+      const int sb = seq_of(seqs.unit0, seqs.n_seqs, u);
+      n_grp = seqs.n_groups[sb];
+      n_res = seqs.n_resid[sb];
+      upp = n_grp + kChunkUnits * ((n_res + kGroup - 1) / kGroup);
+      const int hh = static_cast<int>((u - seqs.unit0[sb]) / upp);
+      pair = sb * a.kv_heads + hh;
+      pbase = seqs.unit0[sb] + static_cast<long long>(hh) * upp;
+      u = pbase + upp;
+    } else {
+      pair = static_cast<int>(u / a.pair_stride);
+      pbase = static_cast<long long>(pair) * a.pair_stride;
+      upp = a.units_per_pair;
+      n_grp = a.n_groups;
+      n_res = a.n_resid;
+      u = pbase + a.pair_stride;
+    }
+    const int lo = static_cast<int>(u0 > pbase ? u0 - pbase : 0LL);
+    const int hi = static_cast<int>(min(static_cast<long long>(upp), u1 - pbase));
+    if (lo >= upp) continue;  // padding after the pair's units (the same for the whole block)
     const int b = pair / a.kv_heads, h = pair % a.kv_heads;
     const long long bh = pair;
     const int first_block = static_cast<int>(pbase / a.units_per_block);
     const int split = static_cast<int>(blockIdx.x) - first_block;
-    const int n_splits = static_cast<int>((pbase + a.units_per_pair - 1) / a.units_per_block) - first_block + 1;
+    const int n_splits = static_cast<int>((pbase + upp - 1) / a.units_per_block) - first_block + 1;
     // the stages and the combine area of the previous segment are reused
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncthreads();
 
     // groups [g_begin, g_end) and window chunks [c_begin, c_end) of the segment
-    const int n_chunks = (a.n_resid + kGroup - 1) / kGroup;
-    const int g_begin = min(a.n_groups, lo);
-    const int g_end = min(a.n_groups, hi);
-    const int c_begin = min(n_chunks, max(0, lo - a.n_groups + kChunkUnits - 1) / kChunkUnits);
-    const int c_end = min(n_chunks, max(0, hi - a.n_groups + kChunkUnits - 1) / kChunkUnits);
+    const int n_chunks = (n_res + kGroup - 1) / kGroup;
+    const int g_begin = min(n_grp, lo);
+    const int g_end = min(n_grp, hi);
+    const int c_begin = min(n_chunks, max(0, lo - n_grp + kChunkUnits - 1) / kChunkUnits);
+    const int c_end = min(n_chunks, max(0, hi - n_grp + kChunkUnits - 1) / kChunkUnits);
 
     float m_run = -INFINITY, l_run = 0.0f, vz_run = 0.0f;
     float o_acc[P::NTV][4];
@@ -526,10 +621,13 @@ __global__ void __launch_bounds__(128, KVQ_DECODE_MIN_BLOCKS) kivi_decode_kernel
       n_mine = GPS * (np - 1) + min(GPS, n_here - GPS * (warp + 4 * (np - 1)));
     }
     const int n_slots = (n_mine + GPS - 1) / GPS;
-    const uint8_t* kc_g = a.k_codes + bh * a.groups_cap * static_cast<long long>(P::KC);
-    const uint8_t* km_g = a.k_meta + bh * a.groups_cap * static_cast<long long>(P::KM);
-    const uint8_t* vc_g = a.v_codes + bh * a.groups_cap * static_cast<long long>(P::VC);
-    const uint8_t* vm_g = a.v_meta + bh * a.groups_cap * static_cast<long long>(P::VM);
+    // contiguous: the pair's records, groups one after the other; paged: the
+    // records of kv head h, block after block
+    const long long rec0 = kPaged ? h : bh * a.groups_cap;
+    const uint8_t* kc_g = a.k_codes + rec0 * P::KC;
+    const uint8_t* km_g = a.k_meta + rec0 * P::KM;
+    const uint8_t* vc_g = a.v_codes + rec0 * P::VC;
+    const uint8_t* vm_g = a.v_meta + rec0 * P::VM;
 
     // slot k of this segment (groups GPS*k .. of the warp) goes through ring
     // position (jg + k) % NS as [key codes x GPS | key meta x GPS | value codes
@@ -540,10 +638,24 @@ __global__ void __launch_bounds__(128, KVQ_DECODE_MIN_BLOCKS) kivi_decode_kernel
       uint8_t* dst = ring + ((jg + k) % NS) * SLOT;
       uint64_t* bb = &bar[(jg + k) % NS];
       mbar_arrive_expect_tx(bb, cnt * P::STAGE);
-      bulk_g2s(dst, kc_g + grp * static_cast<long long>(P::KC), cnt * P::KC, bb);
-      bulk_g2s(dst + GPS * P::KC, km_g + grp * static_cast<long long>(P::KM), cnt * P::KM, bb);
-      bulk_g2s(dst + GPS * (P::KC + P::KM), vc_g + grp * static_cast<long long>(P::VC), cnt * P::VC, bb);
-      bulk_g2s(dst + GPS * (P::KC + P::KM + P::VC), vm_g + grp * static_cast<long long>(P::VM), cnt * P::VM, bb);
+      if constexpr (kPaged) {
+        // one copy per record and group, from the group's pool block; a table
+        // entry outside [0, num_blocks) is clamped into the pool
+        const int32_t* trow = seqs.pools.block_table + static_cast<long long>(b) * a.groups_cap + grp;
+        for (uint32_t i = 0; i < cnt; ++i) {
+          const int blk = min(max(__ldg(trow + i), 0), seqs.pools.num_blocks - 1);
+          const long long r = static_cast<long long>(blk) * a.kv_heads;
+          bulk_g2s(dst + i * P::KC, kc_g + r * P::KC, P::KC, bb);
+          bulk_g2s(dst + GPS * P::KC + i * P::KM, km_g + r * P::KM, P::KM, bb);
+          bulk_g2s(dst + GPS * (P::KC + P::KM) + i * P::VC, vc_g + r * P::VC, P::VC, bb);
+          bulk_g2s(dst + GPS * (P::KC + P::KM + P::VC) + i * P::VM, vm_g + r * P::VM, P::VM, bb);
+        }
+      } else {
+        bulk_g2s(dst, kc_g + grp * static_cast<long long>(P::KC), cnt * P::KC, bb);
+        bulk_g2s(dst + GPS * P::KC, km_g + grp * static_cast<long long>(P::KM), cnt * P::KM, bb);
+        bulk_g2s(dst + GPS * (P::KC + P::KM), vc_g + grp * static_cast<long long>(P::VC), cnt * P::VC, bb);
+        bulk_g2s(dst + GPS * (P::KC + P::KM + P::VC), vm_g + grp * static_cast<long long>(P::VM), cnt * P::VM, bb);
+      }
     };
     auto wait_slot = [&](int k) { return mbar_wait_bounded(&bar[(jg + k) % NS], ((jg + k) / NS) & 1); };
     // the records of group j of the warp
@@ -741,7 +853,7 @@ __global__ void __launch_bounds__(128, KVQ_DECODE_MIN_BLOCKS) kivi_decode_kernel
       for (int ks = 0; ks < P::KS; ++ks) q_io[ks][0] = qs[ks][0], q_io[ks][1] = qs[ks][1];
       uint32_t ph = wphase;
       asm volatile("griddepcontrol.wait;" ::: "memory");  // the window is complete (see decode_dispatch)
-      const bool ok = window_chunks<D, VB>(a.k_res, a.v_res, bh * a.res_cap, a.n_resid, c_begin + warp, c_end, ring,
+      const bool ok = window_chunks<D, VB>(a.k_res, a.v_res, bh * a.res_cap, n_res, c_begin + warp, c_end, ring,
                                            S::WIN_ROW, wbar, ph, q_io, p2e, o_io, st[0], st[1], st[2]);
 #pragma unroll
       for (int i = 0; i < P::NTV; ++i)
@@ -804,13 +916,20 @@ cudaError_t quantize_dispatch(const QuantGroupsArgs& a, cudaStream_t s) {
 }
 
 template <int D, int KB, int VB>
+cudaError_t quantize_paged_dispatch(const PagedQuantArgs& a, cudaStream_t s) {
+  dim3 grid(a.r.begin[a.n_seqs], a.q.kv_heads);
+  kivi_quantize_paged_kernel<D, KB, VB><<<grid, 128, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+template <int D, int KB, int VB, class SeqT>
 int decode_occupancy() {
   static int cached[64] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
   if (cached[dev] == 0) {
     constexpr int smem = DecodeSmem<D, KB, VB, kDecodeStages>::BYTES;
-    auto kern = kivi_decode_kernel<D, KB, VB, kDecodeStages>;
+    auto kern = kivi_decode_kernel<D, KB, VB, kDecodeStages, SeqT>;
     int n = 0;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, 128, smem) != cudaSuccess || n <= 0)
@@ -828,10 +947,10 @@ int decode_occupancy() {
 // fp16 window and the workspace (partials, split counters, shared with the
 // previous decode) are touched only after griddepcontrol.wait, i.e. after the
 // preceding kernel has completed.
-template <int D, int KB, int VB>
-cudaError_t decode_dispatch(const KiviDecodeArgs& a, cudaStream_t s) {
+template <int D, int KB, int VB, class SeqT>
+cudaError_t decode_dispatch(const KiviDecodeArgs& a, const SeqT& seqs, cudaStream_t s) {
   constexpr int smem = DecodeSmem<D, KB, VB, kDecodeStages>::BYTES;
-  auto kern = kivi_decode_kernel<D, KB, VB, kDecodeStages>;
+  auto kern = kivi_decode_kernel<D, KB, VB, kDecodeStages, SeqT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -844,7 +963,7 @@ cudaError_t decode_dispatch(const KiviDecodeArgs& a, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, a);
+  return cudaLaunchKernelEx(&cfg, kern, a, seqs);
 }
 
 }  // namespace
@@ -865,33 +984,75 @@ cudaError_t launch_kivi_quantize(const QuantGroupsArgs& a, cudaStream_t s) {
   }
 }
 
-cudaError_t launch_kivi_decode(const KiviDecodeArgs& a, cudaStream_t s) {
-  const int key = a.head_dim * 100 + a.k_bits * 10 + a.v_bits;
-  switch (key) {
-    case 6422: return decode_dispatch<64, 2, 2>(a, s);
-    case 6424: return decode_dispatch<64, 2, 4>(a, s);
-    case 6442: return decode_dispatch<64, 4, 2>(a, s);
-    case 6444: return decode_dispatch<64, 4, 4>(a, s);
-    case 12822: return decode_dispatch<128, 2, 2>(a, s);
-    case 12824: return decode_dispatch<128, 2, 4>(a, s);
-    case 12842: return decode_dispatch<128, 4, 2>(a, s);
-    case 12844: return decode_dispatch<128, 4, 4>(a, s);
+namespace {
+
+template <class SeqT>
+cudaError_t decode_by_key(const KiviDecodeArgs& a, const SeqT& seqs, cudaStream_t s) {
+  switch (a.head_dim * 100 + a.k_bits * 10 + a.v_bits) {
+    case 6422: return decode_dispatch<64, 2, 2>(a, seqs, s);
+    case 6424: return decode_dispatch<64, 2, 4>(a, seqs, s);
+    case 6442: return decode_dispatch<64, 4, 2>(a, seqs, s);
+    case 6444: return decode_dispatch<64, 4, 4>(a, seqs, s);
+    case 12822: return decode_dispatch<128, 2, 2>(a, seqs, s);
+    case 12824: return decode_dispatch<128, 2, 4>(a, seqs, s);
+    case 12842: return decode_dispatch<128, 4, 2>(a, seqs, s);
+    case 12844: return decode_dispatch<128, 4, 4>(a, seqs, s);
     default: return cudaErrorInvalidValue;
   }
 }
 
-int kivi_decode_blocks_per_sm(int head_dim, int k_bits, int v_bits) {
+template <class SeqT>
+int occupancy_by_key(int head_dim, int k_bits, int v_bits) {
   switch (head_dim * 100 + k_bits * 10 + v_bits) {
-    case 6422: return decode_occupancy<64, 2, 2>();
-    case 6424: return decode_occupancy<64, 2, 4>();
-    case 6442: return decode_occupancy<64, 4, 2>();
-    case 6444: return decode_occupancy<64, 4, 4>();
-    case 12822: return decode_occupancy<128, 2, 2>();
-    case 12824: return decode_occupancy<128, 2, 4>();
-    case 12842: return decode_occupancy<128, 4, 2>();
-    case 12844: return decode_occupancy<128, 4, 4>();
+    case 6422: return decode_occupancy<64, 2, 2, SeqT>();
+    case 6424: return decode_occupancy<64, 2, 4, SeqT>();
+    case 6442: return decode_occupancy<64, 4, 2, SeqT>();
+    case 6444: return decode_occupancy<64, 4, 4, SeqT>();
+    case 12822: return decode_occupancy<128, 2, 2, SeqT>();
+    case 12824: return decode_occupancy<128, 2, 4, SeqT>();
+    case 12842: return decode_occupancy<128, 4, 2, SeqT>();
+    case 12844: return decode_occupancy<128, 4, 4, SeqT>();
     default: return 1;
   }
+}
+
+}  // namespace
+
+cudaError_t launch_kivi_decode(const KiviDecodeArgs& a, cudaStream_t s) { return decode_by_key(a, NoSeqs{}, s); }
+
+cudaError_t launch_kivi_decode_paged(const KiviDecodeArgs& a, const PagedSeqs& seqs, cudaStream_t s) {
+  return decode_by_key(a, seqs, s);
+}
+
+int kivi_decode_blocks_per_sm(int head_dim, int k_bits, int v_bits) {
+  return occupancy_by_key<NoSeqs>(head_dim, k_bits, v_bits);
+}
+
+int kivi_paged_decode_blocks_per_sm(int head_dim, int k_bits, int v_bits) {
+  return occupancy_by_key<PagedSeqs>(head_dim, k_bits, v_bits);
+}
+
+cudaError_t launch_kivi_quantize_paged(const PagedQuantArgs& a, cudaStream_t s) {
+  if (a.n_seqs <= 0 || a.r.begin[a.n_seqs] <= 0) return cudaSuccess;
+  switch (a.q.head_dim * 100 + a.q.k_bits * 10 + a.q.v_bits) {
+    case 6422: return quantize_paged_dispatch<64, 2, 2>(a, s);
+    case 6424: return quantize_paged_dispatch<64, 2, 4>(a, s);
+    case 6442: return quantize_paged_dispatch<64, 4, 2>(a, s);
+    case 6444: return quantize_paged_dispatch<64, 4, 4>(a, s);
+    case 12822: return quantize_paged_dispatch<128, 2, 2>(a, s);
+    case 12824: return quantize_paged_dispatch<128, 2, 4>(a, s);
+    case 12842: return quantize_paged_dispatch<128, 4, 2>(a, s);
+    case 12844: return quantize_paged_dispatch<128, 4, 4>(a, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_copy_tokens_paged(const PagedCopyArgs& a, cudaStream_t s) {
+  if (a.n_seqs <= 0 || a.r.begin[a.n_seqs] <= 0) return cudaSuccess;
+  const long long total = static_cast<long long>(a.r.begin[a.n_seqs]) * a.kv_heads * (a.c.head_dim / 8);
+  const int blocks = static_cast<int>((total + 255) / 256 < 4096 ? (total + 255) / 256 : 4096);
+  copy_tokens_paged_kernel<<<blocks, 256, 0, s>>>(a);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_copy_tokens(const CopyTokensArgs& a, cudaStream_t s) {

@@ -39,6 +39,45 @@ struct CopyTokensArgs {
 };
 cudaError_t launch_copy_tokens(const CopyTokensArgs& a, cudaStream_t s);
 
+// ---- paged, variable-length KIVI cache ----
+// Per-sequence state travels in the kernel parameters (at most kMaxPagedSeqs
+// sequences keep them under the 4 KB parameter limit), so a launch needs no
+// upload and captures into a CUDA graph as it is.
+constexpr int kMaxPagedSeqs = 256;
+
+// Work ranges of one batched launch: sequence b owns items [begin[b],
+// begin[b+1]) (groups for a quantize, tokens for a copy), its first source
+// token is src0[b] and its first destination (group index or window row) dst0[b].
+struct SeqRanges {
+  int begin[kMaxPagedSeqs + 1];
+  int src0[kMaxPagedSeqs];
+  int dst0[kMaxPagedSeqs];
+};
+
+// Group records of a paged cache: group g of sequence b, kv head h lives in
+// pool block block_table[b * groups_cap + g], record (block * kv_heads + h).
+struct PagedPools {
+  const int32_t* block_table;
+  int groups_cap;
+  int num_blocks;
+};
+
+struct PagedQuantArgs {
+  QuantGroupsArgs q;  // k_src/v_src, src_bh_stride, bits, shapes, pools (groups_cap, src_tok0, n_groups unused)
+  PagedPools pools;
+  int n_seqs;
+  SeqRanges r;
+};
+cudaError_t launch_kivi_quantize_paged(const PagedQuantArgs& a, cudaStream_t s);
+
+struct PagedCopyArgs {
+  CopyTokensArgs c;  // buffers, strides and head_dim (src_tok0, dst_tok0, n_tokens unused; bh = n_seqs * kv_heads)
+  int kv_heads;
+  int n_seqs;
+  SeqRanges r;
+};
+cudaError_t launch_copy_tokens_paged(const PagedCopyArgs& a, cudaStream_t s);
+
 struct KiviDecodeArgs {
   const uint8_t* k_codes;
   const uint8_t* k_meta;
@@ -70,6 +109,21 @@ struct KiviDecodeArgs {
   int out_fp32;
 };
 cudaError_t launch_kivi_decode(const KiviDecodeArgs& a, cudaStream_t s);
+
+// Decode over a paged cache: the pairs of sequence b (b * kv_heads + h) have
+// n_groups[b] groups and n_resid[b] window tokens, U_b = n_groups[b] +
+// kChunkUnits * ceil(n_resid[b] / 32) units each, and the units of all pairs
+// follow one another: pair (b, h) starts at unit0[b] + h * U_b. The fields
+// n_groups, n_resid, n_pairs, units_per_pair and pair_stride of the base
+// arguments are unused; groups_cap is the block-table row length.
+struct PagedSeqs {
+  PagedPools pools;
+  int n_seqs;
+  int unit0[kMaxPagedSeqs + 1];
+  int n_groups[kMaxPagedSeqs];
+  int n_resid[kMaxPagedSeqs];
+};
+cudaError_t launch_kivi_decode_paged(const KiviDecodeArgs& a, const PagedSeqs& seqs, cudaStream_t s);
 
 
 struct Fp8QuantArgs {
@@ -115,6 +169,7 @@ cudaError_t launch_fp8_decode(const Fp8DecodeArgs& a, cudaStream_t s);
 int device_sm_count();
 // Resident thread blocks per SM of the decode kernels (occupancy API, cached).
 int kivi_decode_blocks_per_sm(int head_dim, int k_bits, int v_bits);
+int kivi_paged_decode_blocks_per_sm(int head_dim, int k_bits, int v_bits);
 int fp8_decode_blocks_per_sm(int head_dim);
 
 }  // namespace kvq

@@ -27,6 +27,8 @@ c_i32, c_sz, c_vp, c_f32 = ctypes.c_int32, ctypes.c_size_t, ctypes.c_void_p, cty
 EXPORTED = (
     "kvq_status_string", "kivi_cache_sizes", "kivi_cache_init", "kv_quant_prefill", "kv_append_token",
     "kv_flush_residual", "kv_decode_workspace_bytes", "kv_decode_attention", "kv_decode_attention_noalloc",
+    "kivi_paged_cache_sizes", "kivi_paged_cache_init", "kv_paged_prefill", "kv_paged_append", "kv_paged_flush",
+    "kv_paged_decode_workspace_bytes", "kv_paged_decode_attention",
     "fp8_quantize_workspace_bytes",
     "fp8_kv_quantize", "fp8_decode_workspace_bytes", "fp8_decode_attention",
 )
@@ -55,7 +57,22 @@ class kivi_cache(ctypes.Structure):
                 ("n_grouped", c_i32), ("n_resid", c_i32)]
 
 
+PAGED_MAX_SEQS = 256
+
+
+class kivi_paged_config(ctypes.Structure):
+    _fields_ = [("cfg", kivi_config), ("num_blocks", c_i32)]
+
+
+class kivi_paged_cache(ctypes.Structure):
+    _fields_ = [("pcfg", kivi_paged_config), ("k_codes", c_vp), ("k_meta", c_vp), ("v_codes", c_vp),
+                ("v_meta", c_vp), ("k_res", c_vp), ("v_res", c_vp), ("block_table", c_vp),
+                ("groups_cap", c_i32), ("res_cap", c_i32),
+                ("n_grouped", c_i32 * PAGED_MAX_SEQS), ("n_resid", c_i32 * PAGED_MAX_SEQS)]
+
+
 _P_CFG, _P_CACHE = ctypes.POINTER(kivi_config), ctypes.POINTER(kivi_cache)
+_P_PCFG, _P_PCACHE = ctypes.POINTER(kivi_paged_config), ctypes.POINTER(kivi_paged_cache)
 _SIG = {
     "kvq_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "kivi_cache_sizes": ([_P_CFG, ctypes.POINTER(c_sz)], ctypes.c_int),
@@ -66,6 +83,13 @@ _SIG = {
     "kv_decode_workspace_bytes": ([_P_CFG], c_sz),
     "kv_decode_attention": ([_P_CACHE, c_vp, c_vp, c_i32, c_f32, c_vp, c_sz, c_vp], ctypes.c_int),
     "kv_decode_attention_noalloc": ([_P_CACHE, c_vp, c_vp, c_i32, c_f32, c_vp], ctypes.c_int),
+    "kivi_paged_cache_sizes": ([_P_PCFG, ctypes.POINTER(c_sz)], ctypes.c_int),
+    "kivi_paged_cache_init": ([_P_PCACHE, _P_PCFG, ctypes.POINTER(c_vp), c_vp], ctypes.c_int),
+    "kv_paged_prefill": ([_P_PCACHE, c_vp, c_vp, c_i32, ctypes.POINTER(c_i32), c_vp], ctypes.c_int),
+    "kv_paged_append": ([_P_PCACHE, c_vp, c_vp, c_vp], ctypes.c_int),
+    "kv_paged_flush": ([_P_PCACHE, c_vp], ctypes.c_int),
+    "kv_paged_decode_workspace_bytes": ([_P_PCFG], c_sz),
+    "kv_paged_decode_attention": ([_P_PCACHE, c_vp, c_vp, c_i32, c_f32, c_vp, c_sz, c_vp], ctypes.c_int),
     "fp8_quantize_workspace_bytes": ([c_i32, c_i32, c_i32, c_i32], c_sz),
     "fp8_kv_quantize": ([c_vp, c_i32, c_i32, c_i32, c_i32, c_vp, c_i32, c_i32, c_i32, c_vp, c_vp, c_i32, c_i32,
                          c_i32, c_i32, c_vp, c_sz, c_vp], ctypes.c_int),
@@ -157,6 +181,45 @@ def kv_decode_attention_noalloc(cache: kivi_cache, q, out, out_fp32: bool, softm
     device memory: the scratch is a fixed device array inside the library."""
     _check(_lib.kv_decode_attention_noalloc(ctypes.byref(cache), _ptr(q), _ptr(out), int(bool(out_fp32)),
                                             float(softmax_scale), _stream(stream)), "kv_decode_attention_noalloc")
+
+
+def kivi_paged_cache_sizes(pcfg: kivi_paged_config) -> list:
+    out = (c_sz * 6)()
+    _check(_lib.kivi_paged_cache_sizes(ctypes.byref(pcfg), out), "kivi_paged_cache_sizes")
+    return list(out)
+
+
+def kivi_paged_cache_init(pcfg: kivi_paged_config, bufs: Sequence, block_table) -> kivi_paged_cache:
+    cache = kivi_paged_cache()
+    arr = (c_vp * 6)(*[_ptr(b) for b in bufs])
+    _check(_lib.kivi_paged_cache_init(ctypes.byref(cache), ctypes.byref(pcfg), arr, _ptr(block_table)),
+           "kivi_paged_cache_init")
+    return cache
+
+
+def kv_paged_prefill(cache: kivi_paged_cache, k, v, max_seq_len: int, seq_lens: Sequence[int], stream=None) -> None:
+    lens = (c_i32 * len(seq_lens))(*[int(x) for x in seq_lens])
+    _check(_lib.kv_paged_prefill(ctypes.byref(cache), _ptr(k), _ptr(v), max_seq_len, lens, _stream(stream)),
+           "kv_paged_prefill")
+
+
+def kv_paged_append(cache: kivi_paged_cache, k_new, v_new, stream=None) -> None:
+    _check(_lib.kv_paged_append(ctypes.byref(cache), _ptr(k_new), _ptr(v_new), _stream(stream)), "kv_paged_append")
+
+
+def kv_paged_flush(cache: kivi_paged_cache, stream=None) -> None:
+    _check(_lib.kv_paged_flush(ctypes.byref(cache), _stream(stream)), "kv_paged_flush")
+
+
+def kv_paged_decode_workspace_bytes(pcfg: kivi_paged_config) -> int:
+    return int(_lib.kv_paged_decode_workspace_bytes(ctypes.byref(pcfg)))
+
+
+def kv_paged_decode_attention(cache: kivi_paged_cache, q, out, out_fp32: bool, softmax_scale: float, ws,
+                              ws_bytes: int, stream=None) -> None:
+    _check(_lib.kv_paged_decode_attention(ctypes.byref(cache), _ptr(q), _ptr(out), int(bool(out_fp32)),
+                                          float(softmax_scale), _ptr(ws), ws_bytes, _stream(stream)),
+           "kv_paged_decode_attention")
 
 
 def fp8_quantize_workspace_bytes(batch, kv_heads, seq_len, head_dim) -> int:
@@ -251,6 +314,68 @@ class KiviCache:
                "v_codes": 32 * cfg.head_dim * cfg.v_bits // 8, "v_meta": 128}[name]
         return self.buffers[name][: cfg.batch * cfg.kv_heads * self.desc.groups_cap * per].view(
             cfg.batch, cfg.kv_heads, self.desc.groups_cap, per)
+
+    def residual_view(self, name: str):
+        cfg = self.cfg
+        n = cfg.batch * cfg.kv_heads * self.desc.res_cap * cfg.head_dim * 2
+        return self.buffers[name][:n].view(__import__("torch").float16).view(
+            cfg.batch, cfg.kv_heads, self.desc.res_cap, cfg.head_dim)
+
+
+class PagedKiviCache:
+    """One layer's paged, variable-length KIVI cache: pools, windows and the
+    block table in device memory owned by PyTorch. The block table
+    (int32 ``[B, groups_cap]``) is filled by the caller (``table`` below)."""
+
+    NAMES = KiviCache.NAMES
+
+    def __init__(self, batch, kv_heads, q_heads, head_dim, k_bits=2, v_bits=2, residual_len=128, max_tokens=0,
+                 num_blocks=1, device="cuda"):
+        import torch
+        self.pcfg = kivi_paged_config(make_config(batch, kv_heads, q_heads, head_dim, k_bits, v_bits,
+                                                  residual_len, max_tokens), num_blocks)
+        self.cfg = self.pcfg.cfg
+        sizes = kivi_paged_cache_sizes(self.pcfg)
+        self.buffers = {n: _alloc_bytes(s, device) for n, s in zip(self.NAMES, sizes)}
+        groups_cap = -(-max_tokens // 32)
+        self.table = torch.zeros((batch, groups_cap), dtype=torch.int32, device=device)
+        self.desc = kivi_paged_cache_init(self.pcfg, [self.buffers[n] for n in self.NAMES], self.table)
+        self.ws_bytes = kv_paged_decode_workspace_bytes(self.pcfg)
+        self.ws = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=device)
+
+    def n_grouped(self, b: int) -> int:
+        return self.desc.n_grouped[b]
+
+    def n_resid(self, b: int) -> int:
+        return self.desc.n_resid[b]
+
+    def prefill(self, k, v, seq_lens, stream=None):
+        kv_paged_prefill(self.desc, k, v, k.shape[2], seq_lens, stream)
+
+    def append(self, k_new, v_new, stream=None):
+        kv_paged_append(self.desc, k_new, v_new, stream)
+
+    def flush(self, stream=None):
+        kv_paged_flush(self.desc, stream)
+
+    def decode(self, q, out=None, out_fp32=True, softmax_scale=0.0, stream=None):
+        import torch
+        if out is None:
+            out = torch.empty(q.shape, dtype=torch.float32 if out_fp32 else torch.float16, device=q.device)
+        kv_paged_decode_attention(self.desc, q, out, out_fp32, softmax_scale, self.ws, self.ws_bytes, stream)
+        return out
+
+    def status(self) -> int:
+        """Status word of the workspace (bit 0: a device wait timed out). Synchronizes."""
+        return int(self.ws[:4].view(__import__("torch").int32).item())
+
+    def pool_view(self, name: str):
+        """Device bytes of one record pool as ``[num_blocks, H, bytes]`` (uint8)."""
+        cfg = self.cfg
+        per = {"k_codes": 32 * cfg.head_dim * cfg.k_bits // 8, "k_meta": 4 * cfg.head_dim,
+               "v_codes": 32 * cfg.head_dim * cfg.v_bits // 8, "v_meta": 128}[name]
+        return self.buffers[name][: self.pcfg.num_blocks * cfg.kv_heads * per].view(
+            self.pcfg.num_blocks, cfg.kv_heads, per)
 
     def residual_view(self, name: str):
         cfg = self.cfg

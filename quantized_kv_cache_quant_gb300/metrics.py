@@ -26,6 +26,17 @@ def kivi_decode_bytes(batch, kv_heads, q_heads, head_dim, k_bits, v_bits, n_grou
     return grouped + window + q + out
 
 
+def kivi_paged_decode_bytes(kv_heads, q_heads, head_dim, k_bits, v_bits, n_grouped, n_resid, out_bytes=4) -> int:
+    """One kv_paged_decode_attention call over sequences holding n_grouped[b]
+    grouped and n_resid[b] window tokens: each sequence's records and window, its
+    block-table entries (int32 per group), q and out."""
+    total = 0
+    for ng, nr in zip(n_grouped, n_resid):
+        total += kivi_decode_bytes(1, kv_heads, q_heads, head_dim, k_bits, v_bits, ng, nr, out_bytes)
+        total += 4 * (ng // GROUP)
+    return total
+
+
 def kivi_append_bytes(batch, kv_heads, head_dim) -> int:
     """kv_append_token without a flush: read k_new, v_new; write them into the window."""
     return 2 * 2 * batch * kv_heads * head_dim * 2

@@ -69,6 +69,35 @@ class Fp8Workload:
         return -(-self.context // self.block_size)
 
 
+@dataclasses.dataclass(frozen=True)
+class PagedKiviWorkload:
+    """A batch of sequences of different lengths in one paged KIVI cache."""
+    name: str
+    batch: int
+    kv_heads: int
+    q_heads: int
+    head_dim: int
+    min_len: int          # prefill lengths are drawn uniformly from [min_len, max_len]
+    max_len: int
+    decode_steps: int = 1
+    k_bits: int = 2
+    v_bits: int = 2
+    residual: int = 128
+    seed: int = 5
+
+    @property
+    def max_tokens(self) -> int:
+        return self.max_len + self.decode_steps
+
+    @property
+    def groups_cap(self) -> int:
+        return -(-self.max_tokens // GROUP)
+
+    @property
+    def num_blocks(self) -> int:
+        return self.batch * self.groups_cap
+
+
 # The five workloads: a tiny correctness case, a Llama-2-7B-like MHA layer at 4K,
 # a Llama-2-70B-like GQA layer at 8K (2- and 4-bit), an FP8 paged cache at 32K,
 # and a 128K streaming cache with 512 decode steps.
@@ -83,9 +112,14 @@ FP8_32K_E5M2_PH = dataclasses.replace(FP8_32K, name="fp8_e5m2_perhead_paged_b64_
 # the same cache for 8 sequences: a size an ncu capture of the quantize kernels can hold
 FP8_32K_B8 = Fp8Workload("fp8_e4m3_paged_b8_h8x32_d128_s32768", 8, 8, 32, 128, 32768, 16, seed=3)
 STREAM_128K = KiviWorkload("kivi2_stream_b4_h8x64_d128_s131072_512steps", 4, 8, 64, 128, 131072, 512, seed=4)
+# Paged caches of the GQA 8K shape: every sequence at 8192 tokens (the cost of
+# the block table against the contiguous layout), and lengths spread over
+# 512 .. 16384 (the balance of the split across pairs of unequal length).
+PAGED_GQA_8K = PagedKiviWorkload("kivi2_paged_b32_h8x64_d128_len8192", 32, 8, 64, 128, 8192, 8192, seed=5)
+PAGED_VAR_16K = PagedKiviWorkload("kivi2_paged_b32_h8x64_d128_len512-16384", 32, 8, 64, 128, 512, 16384, seed=6)
 
 WORKLOADS = {w.name: w for w in (TINY, MHA_4K, GQA_8K_2BIT, GQA_8K_4BIT, FP8_32K, FP8_32K_E5M2_PH, FP8_32K_B8,
-                                  STREAM_128K)}
+                                  STREAM_128K, PAGED_GQA_8K, PAGED_VAR_16K)}
 
 
 def _channel_scales(rng: np.random.Generator, kv_heads: int, head_dim: int) -> np.ndarray:
@@ -161,3 +195,19 @@ def block_table(batch: int, blocks_per_seq: int, seed: int) -> np.ndarray:
     rng = np.random.Generator(np.random.PCG64(seed))
     perm = rng.permutation(batch * blocks_per_seq).astype(np.int32)
     return perm.reshape(batch, blocks_per_seq)
+
+
+def paged_lengths(batch: int, min_len: int, max_len: int, seed: int) -> np.ndarray:
+    """Prefill lengths, int32 [B], uniform on [min_len, max_len]."""
+    rng = np.random.Generator(np.random.PCG64(seed + 2000))
+    return rng.integers(min_len, max_len + 1, size=batch).astype(np.int32)
+
+
+def paged_inputs(w: PagedKiviWorkload, steps: Optional[int] = None):
+    """(inputs [B, Hkv, max_len, D] of which sequence b uses its first lengths[b]
+    tokens, the lengths, and a random permutation of every pool block as the
+    block table int32 [B, groups_cap])."""
+    x = make_inputs(w.batch, w.kv_heads, w.q_heads, w.head_dim, w.max_len,
+                    w.decode_steps if steps is None else steps, w.seed)
+    lens = paged_lengths(w.batch, w.min_len, w.max_len, w.seed)
+    return x, lens, block_table(w.batch, w.groups_cap, w.seed + 1000)

@@ -5,6 +5,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 from oracle import sizes
@@ -24,7 +25,7 @@ def declared_functions():
 
 def test_every_declared_symbol_is_exported():
     names = declared_functions()
-    assert len(names) == 13
+    assert len(names) == 20
     lib = ctypes.CDLL(kvq.LIB_PATH)
     for n in names:
         assert hasattr(lib, n), n
@@ -189,3 +190,179 @@ def test_fp8_validation():
         with pytest.raises(kvq.KvqError) as e:
             kvq.fp8_decode_attention(**args, stream=0)
         assert e.value.name == code, change
+
+
+# ---------------------------------------------------------------------------
+# paged, variable-length cache
+# ---------------------------------------------------------------------------
+
+PROBE = r"""
+#include <stddef.h>
+#include <stdio.h>
+#include "kvq.h"
+#define F(T, m) printf("%s.%s %zu\n", #T, #m, offsetof(T, m));
+int main(void) {
+  printf("kivi_config %zu\n", sizeof(kivi_config));
+  printf("kivi_cache %zu\n", sizeof(kivi_cache));
+  printf("kivi_paged_config %zu\n", sizeof(kivi_paged_config));
+  printf("kivi_paged_cache %zu\n", sizeof(kivi_paged_cache));
+  F(kivi_cache, k_codes) F(kivi_cache, v_res) F(kivi_cache, groups_cap) F(kivi_cache, n_resid)
+  F(kivi_paged_config, num_blocks)
+  F(kivi_paged_cache, k_codes) F(kivi_paged_cache, v_res) F(kivi_paged_cache, block_table)
+  F(kivi_paged_cache, groups_cap) F(kivi_paged_cache, res_cap) F(kivi_paged_cache, n_grouped)
+  F(kivi_paged_cache, n_resid)
+  printf("KVQ_PAGED_MAX_SEQS %d\n", KVQ_PAGED_MAX_SEQS);
+  return 0;
+}
+"""
+
+
+def test_struct_layouts_match_the_header(tmp_path):
+    """The ctypes descriptors have the sizes and field offsets a C compiler
+    gives the header's structs."""
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not found")
+    src, exe = tmp_path / "probe.c", tmp_path / "probe"
+    src.write_text(PROBE)
+    subprocess.run(["gcc", "-std=c99", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = dict(line.split() for line in subprocess.run([str(exe)], check=True, capture_output=True,
+                                                       text=True).stdout.splitlines())
+    want = {"kivi_config": ctypes.sizeof(kvq.kivi_config), "kivi_cache": ctypes.sizeof(kvq.kivi_cache),
+            "kivi_paged_config": ctypes.sizeof(kvq.kivi_paged_config),
+            "kivi_paged_cache": ctypes.sizeof(kvq.kivi_paged_cache), "KVQ_PAGED_MAX_SEQS": kvq.PAGED_MAX_SEQS}
+    for key, val in got.items():
+        if "." in key:
+            t, m = key.split(".")
+            want[key] = getattr(getattr(kvq, t), m).offset
+        assert int(val) == want[key], key
+
+
+def _pcfg(batch=3, num_blocks=40, **kw):
+    args = dict(batch=batch, kv_heads=2, q_heads=4, head_dim=64, k_bits=2, v_bits=2, residual_len=128,
+                max_tokens=512)
+    args.update(kw)
+    return kvq.kivi_paged_config(kvq.make_config(**args), num_blocks)
+
+
+def _fake_paged(grouped=(), resid=(), **kw):
+    pcfg = _pcfg(**kw)
+    cache = kvq.kivi_paged_cache_init(pcfg, [ALIGNED * (i + 1) for i in range(6)], ALIGNED * 8)
+    for b, n in enumerate(grouped):
+        cache.n_grouped[b] = n
+    for b, n in enumerate(resid):
+        cache.n_resid[b] = n
+    return pcfg, cache
+
+
+def _pstate(cache, n):
+    return [(cache.n_grouped[b], cache.n_resid[b]) for b in range(n)]
+
+
+@pytest.mark.parametrize("b,h,d,kb,vb,r,t,nb", [(3, 2, 64, 2, 2, 128, 512, 40), (256, 8, 128, 4, 2, 0, 100, 7),
+                                                (5, 3, 128, 2, 4, 64, 4097, 1)])
+def test_paged_sizes_match_layout(b, h, d, kb, vb, r, t, nb):
+    from oracle import paged
+    pcfg = kvq.kivi_paged_config(kvq.make_config(b, h, 2 * h, d, kb, vb, r, t), nb)
+    got = kvq.kivi_paged_cache_sizes(pcfg)
+    rec = paged.PagedKiviCache(1, h, d, kb, vb, r, nb, np.zeros((1, 1), np.int32)).record_bytes()
+    res_cap = r if r > 0 else 32
+    want = [nb * h * rec[n] for n in ("k_codes", "k_meta", "v_codes", "v_meta")] + [b * h * res_cap * d * 2] * 2
+    assert got == want
+    assert kvq.kv_paged_decode_workspace_bytes(pcfg) == kvq.kv_decode_workspace_bytes(pcfg.cfg)
+
+
+def test_paged_config_limits():
+    for pcfg, code in [(_pcfg(batch=257), "KVQ_ERR_UNSUPPORTED"), (_pcfg(num_blocks=0), "KVQ_ERR_ARG"),
+                       (_pcfg(head_dim=96), "KVQ_ERR_UNSUPPORTED"), (_pcfg(q_heads=3), "KVQ_ERR_SHAPE")]:
+        with pytest.raises(kvq.KvqError) as e:
+            kvq.kivi_paged_cache_sizes(pcfg)
+        assert e.value.name == code
+        assert kvq.kv_paged_decode_workspace_bytes(pcfg) == 0
+    kvq.kivi_paged_cache_sizes(_pcfg(batch=256))
+
+
+def test_paged_init_checks_pointers():
+    pcfg = _pcfg()
+    bufs = [ALIGNED] * 6
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.kivi_paged_cache_init(pcfg, bufs, None)
+    assert e.value.name == "KVQ_ERR_NULL"
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.kivi_paged_cache_init(pcfg, bufs, ALIGNED + 4)
+    assert e.value.name == "KVQ_ERR_ALIGN"
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.kivi_paged_cache_init(pcfg, [ALIGNED] * 5 + [None], ALIGNED)
+    assert e.value.name == "KVQ_ERR_NULL"
+    _, cache = _fake_paged()
+    assert (cache.groups_cap, cache.res_cap, cache.pcfg.num_blocks) == (16, 128, 40)
+    assert _pstate(cache, 3) == [(0, 0)] * 3
+
+
+def test_paged_prefill_validation_leaves_state():
+    _, cache = _fake_paged((64, 0, 32), (10, 5, 128))
+    before = _pstate(cache, 3)
+    for args, code in [((ALIGNED, ALIGNED, 100, [10, 101, 0]), "KVQ_ERR_ARG"),
+                       ((ALIGNED, ALIGNED, 600, [10, 513, 0]), "KVQ_ERR_CAPACITY"),
+                       ((ALIGNED, ALIGNED, 100, [10, -1, 0]), "KVQ_ERR_ARG"),
+                       ((None, ALIGNED, 100, [10, 1, 0]), "KVQ_ERR_NULL"),
+                       ((ALIGNED + 2, ALIGNED, 100, [10, 1, 0]), "KVQ_ERR_ALIGN")]:
+        with pytest.raises(kvq.KvqError) as e:
+            kvq.kv_paged_prefill(cache, *args, stream=0)
+        assert e.value.name == code
+        assert _pstate(cache, 3) == before
+
+
+def test_paged_prefill_of_empty_sequences_launches_nothing():
+    """Zero tokens everywhere: no pointer is needed, nothing is enqueued, every
+    sequence is emptied."""
+    _, cache = _fake_paged((64, 0, 32), (10, 5, 128))
+    kvq.kv_paged_prefill(cache, None, None, 0, [0, 0, 0], stream=0)
+    assert _pstate(cache, 3) == [(0, 0)] * 3
+
+
+def test_paged_append_capacity_and_state():
+    _, cache = _fake_paged((0, 384, 32), (3, 128, 0))   # sequence 1 holds max_tokens
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.kv_paged_append(cache, ALIGNED, ALIGNED, stream=0)
+    assert e.value.name == "KVQ_ERR_CAPACITY"
+    assert _pstate(cache, 3) == [(0, 3), (384, 128), (32, 0)]
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.kv_paged_append(cache, ALIGNED, None, stream=0)
+    assert e.value.name == "KVQ_ERR_NULL"
+
+
+def test_paged_corrupt_descriptor_is_rejected():
+    for grouped, resid in [((40, 0, 0), (0, 0, 0)), ((0, 0, 0), (0, 129, 0)), ((0, 0, -32), (0, 0, 0)),
+                           ((512, 0, 0), (1, 0, 0))]:
+        _, cache = _fake_paged(grouped, resid)
+        with pytest.raises(kvq.KvqError) as e:
+            kvq.kv_paged_flush(cache, stream=0)
+        assert e.value.name == "KVQ_ERR_ARG"
+    _, cache = _fake_paged((0, 0, 0), (0, 32, 0), residual_len=0)  # an R = 0 stage is never left full
+    with pytest.raises(kvq.KvqError):
+        kvq.kv_paged_flush(cache, stream=0)
+
+
+def test_paged_flush_noop_when_windows_short():
+    _, cache = _fake_paged((64, 0, 32), (31, 0, 5))
+    kvq.kv_paged_flush(cache, stream=0)
+    assert _pstate(cache, 3) == [(64, 31), (0, 0), (32, 5)]
+
+
+def test_paged_decode_validation():
+    pcfg, cache = _fake_paged((64, 0, 32), (3, 1, 0))
+    ws = kvq.kv_paged_decode_workspace_bytes(pcfg)
+    for args, code in [((ALIGNED, ALIGNED, True, 0.0, ALIGNED, ws - 1), "KVQ_ERR_WORKSPACE"),
+                       ((ALIGNED, ALIGNED, True, 0.0, None, ws), "KVQ_ERR_WORKSPACE"),
+                       ((ALIGNED, ALIGNED, True, float("inf"), ALIGNED, ws), "KVQ_ERR_ARG"),
+                       ((ALIGNED, None, True, 0.0, ALIGNED, ws), "KVQ_ERR_NULL"),
+                       ((ALIGNED + 64, ALIGNED, True, 0.0, ALIGNED, ws), "KVQ_ERR_ALIGN")]:
+        with pytest.raises(kvq.KvqError) as e:
+            kvq.kv_paged_decode_attention(cache, *args, stream=0)
+        assert e.value.name == code
+    _, cache = _fake_paged((64, 0, 32), (3, 0, 0))         # sequence 1 is empty
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.kv_paged_decode_attention(cache, ALIGNED, ALIGNED, True, 0.0, ALIGNED, ws, stream=0)
+    assert e.value.name == "KVQ_ERR_ARG"
