@@ -211,12 +211,14 @@ KVQ_API kvq_status kv_decode_attention_noalloc(const kivi_cache* cache, const ui
  * sequence's own length); its groups of 32 tokens live in blocks of shared
  * pools, reached through a block table as in [CSDN] section 13. The pages
  * combine the two ideas without fixing a layout; this one is the library's:
- * one pool block holds one group of one sequence for every kv head, in the
- * four records of the contiguous cache (same byte layout per record).
+ * one pool block holds one group of one sequence for every kv head, and for
+ * each kv head the four records of the contiguous cache (same byte layout per
+ * record) back to back, so that one group of one head is one contiguous run.
  *
- *   pools   : k_codes [num_blocks, H_kv, 32*D*k_bits/8], k_meta [num_blocks,
- *             H_kv, 4*D], v_codes [num_blocks, H_kv, 32*D*v_bits/8], v_meta
- *             [num_blocks, H_kv, 128]
+ *   pool    : [num_blocks, H_kv, E] bytes, E = KC + KM + VC + 128 with
+ *             KC = 32*D*k_bits/8 (key codes at offset 0), KM = 4*D (key meta
+ *             at KC), VC = 32*D*v_bits/8 (value codes at KC + KM), value meta
+ *             at KC + KM + VC
  *   windows : fp16 k_res, v_res [B, H_kv, res_cap, D], one per sequence
  *   table   : device int32 block_table [B, groups_cap], groups_cap =
  *             ceil(max_tokens / 32); entry [b, g] is the pool block of group g
@@ -244,10 +246,7 @@ typedef struct {
 
 typedef struct {
   kivi_paged_config pcfg;
-  uint8_t* k_codes;
-  uint8_t* k_meta;
-  uint8_t* v_codes;
-  uint8_t* v_meta;
+  uint8_t* pool;
   uint16_t* k_res;
   uint16_t* v_res;
   const int32_t* block_table;
@@ -257,15 +256,14 @@ typedef struct {
   int32_t n_resid[KVQ_PAGED_MAX_SEQS];
 } kivi_paged_cache;
 
-/* Byte sizes of the six buffers (k_codes, k_meta, v_codes, v_meta pools, then
- * the k_res, v_res windows). */
-KVQ_API kvq_status kivi_paged_cache_sizes(const kivi_paged_config* cfg, size_t bytes_out[6]);
+/* Byte sizes of the three buffers: the pool, then the k_res and v_res windows. */
+KVQ_API kvq_status kivi_paged_cache_sizes(const kivi_paged_config* cfg, size_t bytes_out[3]);
 
-/* Fill a descriptor for caller buffers bufs[6] and the caller's block table
+/* Fill a descriptor for caller buffers bufs[3] and the caller's block table
  * (device int32 [B, groups_cap]). Every sequence starts empty. No device work.
  * KVQ_ERR_UNSUPPORTED for more than KVQ_PAGED_MAX_SEQS sequences. */
 KVQ_API kvq_status kivi_paged_cache_init(kivi_paged_cache* cache, const kivi_paged_config* cfg,
-                                         void* const bufs[6], const int32_t* block_table);
+                                         void* const bufs[3], const int32_t* block_table);
 
 /* Prefill every sequence: sequence b starts from its first seq_lens[b] tokens
  * of k, v (device fp16 [B, H_kv, max_seq_len, D]); seq_lens is a HOST int32

@@ -8,8 +8,9 @@ pool and reached through a block table, as paged caches reach their blocks
 ("大模型量化从0到1（十三）：KV Cache 量化" (CSDN), section 13).
 
 Reading (the pages combine the two ideas without a layout): one block holds one
-32-token group of one sequence for every kv head, in the same four records as
-the contiguous cache (key codes, key meta, value codes, value meta);
+32-token group of one sequence for every kv head; for each kv head the four
+records of the contiguous cache (key codes, key meta, value codes, value meta)
+sit back to back, so one group of one head is one contiguous run of bytes;
 ``block_table[b, g]`` is the pool block of logical group g of sequence b; each
 sequence keeps its own fp16 window; every sequence follows the contiguous
 cache's rules (prefill split, flush timing) on its own length. Decode attention
@@ -60,6 +61,22 @@ class PagedKiviCache:
             for name, rec in packed.items():
                 for g in range(rec.shape[2]):
                     out[name][self.table[b, g]] = rec[0, :, g]
+        return out
+
+    ORDER = ("k_codes", "k_meta", "v_codes", "v_meta")
+
+    def pool(self) -> np.ndarray:
+        """The block pool, uint8 ``[num_blocks, H, sum of record bytes]``: per
+        (block, kv head) the four records in ORDER, back to back."""
+        p = self.pools()
+        return np.concatenate([p[name] for name in self.ORDER], axis=2)
+
+    def record_offsets(self) -> dict:
+        """Byte offset of each record inside one (block, kv head) entry of the pool."""
+        out, off = {}, 0
+        for name in self.ORDER:
+            out[name] = off
+            off += self.record_bytes()[name]
         return out
 
     def record_bytes(self) -> dict:

@@ -288,8 +288,9 @@ __device__ __forceinline__ int seq_of(const int* begin, int n, long long x) {
 
 // Grid (total groups, H_kv): item blockIdx.x is group x - begin[b] of sequence
 // b's range, read from source token src0[b] + 32 * (x - begin[b]) and written
-// to the pool block of logical group dst0[b] + (x - begin[b]). A block-table
-// entry outside [0, num_blocks) is skipped: nothing is written for it.
+// to the pool block of logical group dst0[b] + (x - begin[b]), its four records
+// back to back in the block's entry for kv head h. A block-table entry outside
+// [0, num_blocks) is skipped: nothing is written for it.
 template <int D, int KB, int VB>
 __global__ void __launch_bounds__(128) kivi_quantize_paged_kernel(PagedQuantArgs a) {
   using P = Kivi<D, KB, VB>;
@@ -300,9 +301,9 @@ __global__ void __launch_bounds__(128) kivi_quantize_paged_kernel(PagedQuantArgs
   const long long src_off = bh * a.q.src_bh_stride + static_cast<long long>(a.r.src0[b] + 32 * grp) * D;
   const int blk = __ldg(a.pools.block_table + static_cast<long long>(b) * a.pools.groups_cap + a.r.dst0[b] + grp);
   if (blk < 0 || blk >= a.pools.num_blocks) return;
-  const long long ri = static_cast<long long>(blk) * a.q.kv_heads + h;
-  quantize_group<D, KB, VB>(a.q.k_src + src_off, a.q.v_src + src_off, a.q.k_codes + ri * P::KC,
-                            a.q.k_meta + ri * P::KM, a.q.v_codes + ri * P::VC, a.q.v_meta + ri * P::VM);
+  uint8_t* e = a.q.k_codes + (static_cast<long long>(blk) * a.q.kv_heads + h) * P::STAGE;
+  quantize_group<D, KB, VB>(a.q.k_src + src_off, a.q.v_src + src_off, e, e + P::KC, e + P::KC + P::KM,
+                            e + P::KC + P::KM + P::VC);
 }
 
 // ---------------------------------------------------------------------------
@@ -530,6 +531,15 @@ __device__ __noinline__ bool window_chunks(const uint16_t* k_res, const uint16_t
 // a.n_resid window tokens, at unit p * pair_stride.
 struct NoSeqs {};
 
+// Block-table entries a warp of the paged decode keeps in its lanes (nothing
+// for the contiguous cache).
+template <bool kPaged>
+struct TableLanes {
+  int tbase = 0, tblk = 0;
+};
+template <>
+struct TableLanes<false> {};
+
 template <int D, int KB, int VB, int STAGES, class SeqT>
 __global__ void __launch_bounds__(128, KVQ_DECODE_MIN_BLOCKS) kivi_decode_kernel(KiviDecodeArgs a, SeqT seqs) {
   using P = Kivi<D, KB, VB>;
@@ -577,10 +587,14 @@ __global__ void __launch_bounds__(128, KVQ_DECODE_MIN_BLOCKS) kivi_decode_kernel
       n_grp = seqs.n_groups[sb];
       n_res = seqs.n_resid[sb];
       upp = n_grp + kChunkUnits * ((n_res + kGroup - 1) / kGroup);
-      const int hh = static_cast<int>((u - seqs.unit0[sb]) / upp);
+      // each pair's range opens with pair_lead units of no work (the cost of
+      // one more segment); pbase is its first unit of work
+      const int span = upp + seqs.pair_lead;
+      const int hh = static_cast<int>((u - seqs.unit0[sb]) / span);
       pair = sb * a.kv_heads + hh;
-      pbase = seqs.unit0[sb] + static_cast<long long>(hh) * upp;
-      u = pbase + upp;
+      const long long vbase = seqs.unit0[sb] + static_cast<long long>(hh) * span;
+      pbase = vbase + seqs.pair_lead;
+      u = vbase + span;
     } else {
       pair = static_cast<int>(u / a.pair_stride);
       pbase = static_cast<long long>(pair) * a.pair_stride;
@@ -592,6 +606,9 @@ __global__ void __launch_bounds__(128, KVQ_DECODE_MIN_BLOCKS) kivi_decode_kernel
     const int lo = static_cast<int>(u0 > pbase ? u0 - pbase : 0LL);
     const int hi = static_cast<int>(min(static_cast<long long>(upp), u1 - pbase));
     if (lo >= upp) continue;  // padding after the pair's units (the same for the whole block)
+    if constexpr (kPaged) {
+      if (hi <= 0) continue;  // the slice ends inside the pair's lead-in: no work here
+    }
     const int b = pair / a.kv_heads, h = pair % a.kv_heads;
     const long long bh = pair;
     const int first_block = static_cast<int>(pbase / a.units_per_block);
@@ -621,35 +638,51 @@ __global__ void __launch_bounds__(128, KVQ_DECODE_MIN_BLOCKS) kivi_decode_kernel
       n_mine = GPS * (np - 1) + min(GPS, n_here - GPS * (warp + 4 * (np - 1)));
     }
     const int n_slots = (n_mine + GPS - 1) / GPS;
-    // contiguous: the pair's records, groups one after the other; paged: the
-    // records of kv head h, block after block
-    const long long rec0 = kPaged ? h : bh * a.groups_cap;
+    // contiguous: the pair's records, groups one after the other
+    const long long rec0 = bh * a.groups_cap;
     const uint8_t* kc_g = a.k_codes + rec0 * P::KC;
     const uint8_t* km_g = a.k_meta + rec0 * P::KM;
     const uint8_t* vc_g = a.v_codes + rec0 * P::VC;
     const uint8_t* vm_g = a.v_meta + rec0 * P::VM;
+    // paged: group j's pool blocks come from the block table through the
+    // lanes (lane l holds the entry of the warp's group tbase + l)
+    TableLanes<kPaged> tl;
+    auto load_table = [&](int base) {  // warp-wide
+      if constexpr (kPaged) {
+        tl.tbase = base;
+        const int jl = base + lane;
+        if (jl < n_mine) {
+          const int grp = g_begin + GPS * (warp + 4 * (jl / GPS)) + jl % GPS;
+          tl.tblk = min(max(__ldg(seqs.pools.block_table + static_cast<long long>(b) * a.groups_cap + grp), 0),
+                        seqs.pools.num_blocks - 1);
+        }
+      }
+    };
+    // the pool blocks of slot k's groups (warp-wide)
+    auto slot_blocks = [&](int k, int& b0, int& b1) {
+      if constexpr (kPaged) {
+        if (GPS * k + GPS > tl.tbase + 32) load_table(GPS * k);
+        b0 = __shfl_sync(0xffffffffu, tl.tblk, GPS * k - tl.tbase);
+        b1 = __shfl_sync(0xffffffffu, tl.tblk, GPS * k + 1 - tl.tbase);
+      }
+    };
 
     // slot k of this segment (groups GPS*k .. of the warp) goes through ring
     // position (jg + k) % NS as [key codes x GPS | key meta x GPS | value codes
     // x GPS | value meta x GPS]
-    auto issue = [&](int k) {
+    auto issue = [&](int k, int b0 = 0, int b1 = 0) {
       const int grp = g_begin + GPS * (warp + 4 * k);
       const uint32_t cnt = static_cast<uint32_t>(min(GPS, g_end - grp));
       uint8_t* dst = ring + ((jg + k) % NS) * SLOT;
       uint64_t* bb = &bar[(jg + k) % NS];
       mbar_arrive_expect_tx(bb, cnt * P::STAGE);
       if constexpr (kPaged) {
-        // one copy per record and group, from the group's pool block; a table
-        // entry outside [0, num_blocks) is clamped into the pool
-        const int32_t* trow = seqs.pools.block_table + static_cast<long long>(b) * a.groups_cap + grp;
-        for (uint32_t i = 0; i < cnt; ++i) {
-          const int blk = min(max(__ldg(trow + i), 0), seqs.pools.num_blocks - 1);
-          const long long r = static_cast<long long>(blk) * a.kv_heads;
-          bulk_g2s(dst + i * P::KC, kc_g + r * P::KC, P::KC, bb);
-          bulk_g2s(dst + GPS * P::KC + i * P::KM, km_g + r * P::KM, P::KM, bb);
-          bulk_g2s(dst + GPS * (P::KC + P::KM) + i * P::VC, vc_g + r * P::VC, P::VC, bb);
-          bulk_g2s(dst + GPS * (P::KC + P::KM + P::VC) + i * P::VM, vm_g + r * P::VM, P::VM, bb);
-        }
+        // one copy per group: kv head h's entry of its pool block (the pool is
+        // a.k_codes; table entries outside [0, num_blocks) were clamped)
+        static_assert(GPS == 2, "two blocks per slot");
+        const uint8_t* pool_h = a.k_codes + static_cast<long long>(h) * P::STAGE;
+        bulk_g2s(dst, pool_h + static_cast<long long>(b0) * a.kv_heads * P::STAGE, P::STAGE, bb);
+        if (cnt > 1) bulk_g2s(dst + P::STAGE, pool_h + static_cast<long long>(b1) * a.kv_heads * P::STAGE, P::STAGE, bb);
       } else {
         bulk_g2s(dst, kc_g + grp * static_cast<long long>(P::KC), cnt * P::KC, bb);
         bulk_g2s(dst + GPS * P::KC, km_g + grp * static_cast<long long>(P::KM), cnt * P::KM, bb);
@@ -658,14 +691,36 @@ __global__ void __launch_bounds__(128, KVQ_DECODE_MIN_BLOCKS) kivi_decode_kernel
       }
     };
     auto wait_slot = [&](int k) { return mbar_wait_bounded(&bar[(jg + k) % NS], ((jg + k) / NS) & 1); };
-    // the records of group j of the warp
+    // the records of group j of the warp (paged: each group's four records
+    // back to back; contiguous: the GPS groups' records of one kind together)
     auto slot_base = [&](int j) { return ring + ((jg + j / GPS) % NS) * SLOT; };
-    auto kc_of = [&](int j) { return slot_base(j) + (j % GPS) * P::KC; };
-    auto km_of = [&](int j) { return slot_base(j) + GPS * P::KC + (j % GPS) * P::KM; };
-    auto vc_of = [&](int j) { return slot_base(j) + GPS * (P::KC + P::KM) + (j % GPS) * P::VC; };
-    auto vm_of = [&](int j) { return slot_base(j) + GPS * (P::KC + P::KM + P::VC) + (j % GPS) * P::VM; };
-    if (lane == 0) {
-      for (int k = 0; k < NS && k < n_slots; ++k) issue(k);
+    auto kc_of = [&](int j) {
+      if constexpr (kPaged) return slot_base(j) + (j % GPS) * P::STAGE;
+      else return slot_base(j) + (j % GPS) * P::KC;
+    };
+    auto km_of = [&](int j) {
+      if constexpr (kPaged) return slot_base(j) + (j % GPS) * P::STAGE + P::KC;
+      else return slot_base(j) + GPS * P::KC + (j % GPS) * P::KM;
+    };
+    auto vc_of = [&](int j) {
+      if constexpr (kPaged) return slot_base(j) + (j % GPS) * P::STAGE + P::KC + P::KM;
+      else return slot_base(j) + GPS * (P::KC + P::KM) + (j % GPS) * P::VC;
+    };
+    auto vm_of = [&](int j) {
+      if constexpr (kPaged) return slot_base(j) + (j % GPS) * P::STAGE + P::KC + P::KM + P::VC;
+      else return slot_base(j) + GPS * (P::KC + P::KM + P::VC) + (j % GPS) * P::VM;
+    };
+    if constexpr (kPaged) {
+      if (n_mine > 0) load_table(0);
+      for (int k = 0; k < NS && k < n_slots; ++k) {
+        int b0, b1;
+        slot_blocks(k, b0, b1);
+        if (lane == 0) issue(k, b0, b1);
+      }
+    } else {
+      if (lane == 0) {
+        for (int k = 0; k < NS && k < n_slots; ++k) issue(k);
+      }
     }
 
     // Query fragments of row g (query head h*gq + g), scaled by 2^-e so that
@@ -830,9 +885,21 @@ __global__ void __launch_bounds__(128, KVQ_DECODE_MIN_BLOCKS) kivi_decode_kernel
       // after the last group of its slot: release the slot and refill it NS slots ahead
       if (j % GPS == GPS - 1 || j + 1 == n_mine) {
         __syncwarp();
-        if (lane == 0 && j / GPS + NS < n_slots) {
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          issue(j / GPS + NS);
+        if constexpr (kPaged) {
+          const int kn = j / GPS + NS;
+          if (kn < n_slots) {
+            int b0, b1;
+            slot_blocks(kn, b0, b1);
+            if (lane == 0) {
+              asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+              issue(kn, b0, b1);
+            }
+          }
+        } else {
+          if (lane == 0 && j / GPS + NS < n_slots) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            issue(j / GPS + NS);
+          }
         }
       }
     }

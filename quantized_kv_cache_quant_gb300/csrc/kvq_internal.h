@@ -55,7 +55,9 @@ struct SeqRanges {
 };
 
 // Group records of a paged cache: group g of sequence b, kv head h lives in
-// pool block block_table[b * groups_cap + g], record (block * kv_heads + h).
+// pool block block_table[b * groups_cap + g], entry (block * kv_heads + h) of
+// the pool, its four records back to back (key codes, key meta, value codes,
+// value meta).
 struct PagedPools {
   const int32_t* block_table;
   int groups_cap;
@@ -63,7 +65,8 @@ struct PagedPools {
 };
 
 struct PagedQuantArgs {
-  QuantGroupsArgs q;  // k_src/v_src, src_bh_stride, bits, shapes, pools (groups_cap, src_tok0, n_groups unused)
+  QuantGroupsArgs q;  // sources, src_bh_stride, bits and shapes; k_codes = the pool (src_tok0, n_groups,
+                      // dst_group0 and the other record pointers unused)
   PagedPools pools;
   int n_seqs;
   SeqRanges r;
@@ -112,13 +115,17 @@ cudaError_t launch_kivi_decode(const KiviDecodeArgs& a, cudaStream_t s);
 
 // Decode over a paged cache: the pairs of sequence b (b * kv_heads + h) have
 // n_groups[b] groups and n_resid[b] window tokens, U_b = n_groups[b] +
-// kChunkUnits * ceil(n_resid[b] / 32) units each, and the units of all pairs
-// follow one another: pair (b, h) starts at unit0[b] + h * U_b. The fields
-// n_groups, n_resid, n_pairs, units_per_pair and pair_stride of the base
-// arguments are unused; groups_cap is the block-table row length.
+// kChunkUnits * ceil(n_resid[b] / 32) units of work each, and the ranges of
+// all pairs follow one another: pair (b, h) spans pair_lead + U_b units from
+// unit0[b] + h * (pair_lead + U_b), its work after the first pair_lead (a
+// slice that covers only those does nothing for the pair). k_codes of the
+// base arguments is the pool; k_meta, v_codes, v_meta, n_groups, n_resid,
+// units_per_pair and pair_stride are unused; groups_cap is the block-table
+// row length.
 struct PagedSeqs {
   PagedPools pools;
   int n_seqs;
+  int pair_lead;
   int unit0[kMaxPagedSeqs + 1];
   int n_groups[kMaxPagedSeqs];
   int n_resid[kMaxPagedSeqs];

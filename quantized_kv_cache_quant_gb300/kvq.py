@@ -65,8 +65,7 @@ class kivi_paged_config(ctypes.Structure):
 
 
 class kivi_paged_cache(ctypes.Structure):
-    _fields_ = [("pcfg", kivi_paged_config), ("k_codes", c_vp), ("k_meta", c_vp), ("v_codes", c_vp),
-                ("v_meta", c_vp), ("k_res", c_vp), ("v_res", c_vp), ("block_table", c_vp),
+    _fields_ = [("pcfg", kivi_paged_config), ("pool", c_vp), ("k_res", c_vp), ("v_res", c_vp), ("block_table", c_vp),
                 ("groups_cap", c_i32), ("res_cap", c_i32),
                 ("n_grouped", c_i32 * PAGED_MAX_SEQS), ("n_resid", c_i32 * PAGED_MAX_SEQS)]
 
@@ -184,14 +183,14 @@ def kv_decode_attention_noalloc(cache: kivi_cache, q, out, out_fp32: bool, softm
 
 
 def kivi_paged_cache_sizes(pcfg: kivi_paged_config) -> list:
-    out = (c_sz * 6)()
+    out = (c_sz * 3)()
     _check(_lib.kivi_paged_cache_sizes(ctypes.byref(pcfg), out), "kivi_paged_cache_sizes")
     return list(out)
 
 
 def kivi_paged_cache_init(pcfg: kivi_paged_config, bufs: Sequence, block_table) -> kivi_paged_cache:
     cache = kivi_paged_cache()
-    arr = (c_vp * 6)(*[_ptr(b) for b in bufs])
+    arr = (c_vp * 3)(*[_ptr(b) for b in bufs])
     _check(_lib.kivi_paged_cache_init(ctypes.byref(cache), ctypes.byref(pcfg), arr, _ptr(block_table)),
            "kivi_paged_cache_init")
     return cache
@@ -327,7 +326,8 @@ class PagedKiviCache:
     block table in device memory owned by PyTorch. The block table
     (int32 ``[B, groups_cap]``) is filled by the caller (``table`` below)."""
 
-    NAMES = KiviCache.NAMES
+    NAMES = ("pool", "k_res", "v_res")
+    RECORDS = ("k_codes", "k_meta", "v_codes", "v_meta")   # back to back in each (block, kv head) entry
 
     def __init__(self, batch, kv_heads, q_heads, head_dim, k_bits=2, v_bits=2, residual_len=128, max_tokens=0,
                  num_blocks=1, device="cuda"):
@@ -369,13 +369,26 @@ class PagedKiviCache:
         """Status word of the workspace (bit 0: a device wait timed out). Synchronizes."""
         return int(self.ws[:4].view(__import__("torch").int32).item())
 
-    def pool_view(self, name: str):
-        """Device bytes of one record pool as ``[num_blocks, H, bytes]`` (uint8)."""
+    def record_bytes(self) -> dict:
         cfg = self.cfg
-        per = {"k_codes": 32 * cfg.head_dim * cfg.k_bits // 8, "k_meta": 4 * cfg.head_dim,
-               "v_codes": 32 * cfg.head_dim * cfg.v_bits // 8, "v_meta": 128}[name]
-        return self.buffers[name][: self.pcfg.num_blocks * cfg.kv_heads * per].view(
-            self.pcfg.num_blocks, cfg.kv_heads, per)
+        return {"k_codes": 32 * cfg.head_dim * cfg.k_bits // 8, "k_meta": 4 * cfg.head_dim,
+                "v_codes": 32 * cfg.head_dim * cfg.v_bits // 8, "v_meta": 128}
+
+    def pool_view(self, name: str = None):
+        """Device bytes of the pool as ``[num_blocks, H, entry bytes]`` (uint8), or
+        of one of its records, ``[num_blocks, H, record bytes]``."""
+        cfg, rec = self.cfg, self.record_bytes()
+        entry = sum(rec.values())
+        pool = self.buffers["pool"][: self.pcfg.num_blocks * cfg.kv_heads * entry].view(
+            self.pcfg.num_blocks, cfg.kv_heads, entry)
+        if name is None:
+            return pool
+        off = 0
+        for n in self.RECORDS:
+            if n == name:
+                return pool[:, :, off:off + rec[n]]
+            off += rec[n]
+        raise KeyError(name)
 
     def residual_view(self, name: str):
         cfg = self.cfg

@@ -208,7 +208,7 @@ int main(void) {
   printf("kivi_paged_cache %zu\n", sizeof(kivi_paged_cache));
   F(kivi_cache, k_codes) F(kivi_cache, v_res) F(kivi_cache, groups_cap) F(kivi_cache, n_resid)
   F(kivi_paged_config, num_blocks)
-  F(kivi_paged_cache, k_codes) F(kivi_paged_cache, v_res) F(kivi_paged_cache, block_table)
+  F(kivi_paged_cache, pool) F(kivi_paged_cache, v_res) F(kivi_paged_cache, block_table)
   F(kivi_paged_cache, groups_cap) F(kivi_paged_cache, res_cap) F(kivi_paged_cache, n_grouped)
   F(kivi_paged_cache, n_resid)
   printf("KVQ_PAGED_MAX_SEQS %d\n", KVQ_PAGED_MAX_SEQS);
@@ -248,7 +248,7 @@ def _pcfg(batch=3, num_blocks=40, **kw):
 
 def _fake_paged(grouped=(), resid=(), **kw):
     pcfg = _pcfg(**kw)
-    cache = kvq.kivi_paged_cache_init(pcfg, [ALIGNED * (i + 1) for i in range(6)], ALIGNED * 8)
+    cache = kvq.kivi_paged_cache_init(pcfg, [ALIGNED * (i + 1) for i in range(3)], ALIGNED * 8)
     for b, n in enumerate(grouped):
         cache.n_grouped[b] = n
     for b, n in enumerate(resid):
@@ -268,7 +268,7 @@ def test_paged_sizes_match_layout(b, h, d, kb, vb, r, t, nb):
     got = kvq.kivi_paged_cache_sizes(pcfg)
     rec = paged.PagedKiviCache(1, h, d, kb, vb, r, nb, np.zeros((1, 1), np.int32)).record_bytes()
     res_cap = r if r > 0 else 32
-    want = [nb * h * rec[n] for n in ("k_codes", "k_meta", "v_codes", "v_meta")] + [b * h * res_cap * d * 2] * 2
+    want = [nb * h * sum(rec.values())] + [b * h * res_cap * d * 2] * 2
     assert got == want
     assert kvq.kv_paged_decode_workspace_bytes(pcfg) == kvq.kv_decode_workspace_bytes(pcfg.cfg)
 
@@ -285,7 +285,7 @@ def test_paged_config_limits():
 
 def test_paged_init_checks_pointers():
     pcfg = _pcfg()
-    bufs = [ALIGNED] * 6
+    bufs = [ALIGNED] * 3
     with pytest.raises(kvq.KvqError) as e:
         kvq.kivi_paged_cache_init(pcfg, bufs, None)
     assert e.value.name == "KVQ_ERR_NULL"
@@ -293,7 +293,7 @@ def test_paged_init_checks_pointers():
         kvq.kivi_paged_cache_init(pcfg, bufs, ALIGNED + 4)
     assert e.value.name == "KVQ_ERR_ALIGN"
     with pytest.raises(kvq.KvqError) as e:
-        kvq.kivi_paged_cache_init(pcfg, [ALIGNED] * 5 + [None], ALIGNED)
+        kvq.kivi_paged_cache_init(pcfg, [ALIGNED] * 2 + [None], ALIGNED)
     assert e.value.name == "KVQ_ERR_NULL"
     _, cache = _fake_paged()
     assert (cache.groups_cap, cache.res_cap, cache.pcfg.num_blocks) == (16, 128, 40)

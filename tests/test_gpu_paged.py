@@ -39,8 +39,7 @@ def _build(lens, hkv=2, hq=4, d=64, kb=2, vb=2, r=128, steps=0, seed=0, permute=
              else np.arange(nb, dtype=np.int32).reshape(b, gcap))
     gc = kvq.PagedKiviCache(b, hkv, hq, d, kb, vb, r, max_tokens, nb)
     gc.table.copy_(dev(table))
-    for name in NAMES:
-        gc.buffers[name].fill_(0xA5)      # a sentinel: blocks no group uses keep it
+    gc.buffers["pool"].fill_(0xA5)        # a sentinel: blocks no group uses keep it
     gc.prefill(dev(x.k), dev(x.v), lens)
     oc = paged.PagedKiviCache(b, hkv, d, kb, vb, r, nb, table)
     oc.prefill(x.k, x.v, lens)
@@ -53,18 +52,18 @@ def _assert_state(gc, oc):
 
 
 def _assert_pools_equal(gc, oc, table):
-    """Every block a group uses holds the oracle's records; every other block
-    still holds the sentinel."""
-    want = oc.pools()
+    """Every block a group uses holds the oracle's pool entries (the four
+    records back to back); every other block still holds the sentinel."""
+    want = oc.pool()
     used = np.zeros(oc.num_blocks, bool)
     for b in range(oc.B):
         used[table[b, :oc.n_grouped(b) // 32]] = True
-    for name in NAMES:
-        got = host(gc.pool_view(name))
-        if not np.array_equal(got[used], want[name][used]):
-            bad = np.argwhere(got[used] != want[name][used])
-            raise AssertionError(f"{name}: {len(bad)} bytes differ, first at {bad[:5].tolist()}")
-        assert np.all(got[~used] == 0xA5), name
+    got = host(gc.pool_view())
+    assert got.shape == want.shape
+    if not np.array_equal(got[used], want[used]):
+        bad = np.argwhere(got[used] != want[used])
+        raise AssertionError(f"{len(bad)} bytes differ, first at {bad[:5].tolist()}")
+    assert np.all(got[~used] == 0xA5)
 
 
 def _assert_windows_equal(gc, oc):
@@ -189,8 +188,7 @@ def test_out_of_range_table_entries():
     bad[0, 2] = -1
     bad[0, 5] = gc.pcfg.num_blocks
     gc.table.copy_(dev(bad))
-    for name in NAMES:
-        gc.buffers[name].fill_(0xA5)
+    gc.buffers["pool"].fill_(0xA5)
     gc.prefill(dev(x.k), dev(x.v), [32 * 8 + 128])
     want = oc.pools()
     for name in NAMES:

@@ -80,3 +80,19 @@ def test_staggered_flushes_during_appends():
     # a window flushes on the append that would overflow it (then refills from 1 to 64 tokens):
     # sequence 2 at once, 1 after one append, 0 after 22
     assert flushed_at == {0: [22], 1: [1, 65], 2: [0, 64]}
+
+
+def test_pool_is_the_records_back_to_back():
+    """One (block, kv head) entry of the pool is key codes, key meta, value
+    codes, value meta in that order; the sizes add up to one group's records."""
+    b, h, d = 2, 3, 64
+    x = _inputs(b, h, d, 32 * 5 + 140, 0, 9)
+    table = np.arange(b * 12, dtype=np.int32).reshape(b, 12)[:, ::-1].copy()
+    p = paged.PagedKiviCache(b, h, d, 2, 4, 128, b * 12, table)
+    p.prefill(x.k[:, :, :32 * 5 + 140], x.v[:, :, :32 * 5 + 140], [32 * 5 + 140, 40])
+    pool, recs, off = p.pool(), p.pools(), p.record_offsets()
+    nbytes = p.record_bytes()
+    assert pool.shape == (b * 12, h, 32 * d * 2 // 8 + 4 * d + 32 * d * 4 // 8 + 128)
+    assert off == {"k_codes": 0, "k_meta": 512, "v_codes": 768, "v_meta": 1792}
+    for name in p.ORDER:
+        assert np.array_equal(pool[:, :, off[name]:off[name] + nbytes[name]], recs[name])
