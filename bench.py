@@ -350,7 +350,7 @@ def run_ours(args, world, rank, local):
                      "frac": round(achieved / hbm, 4),
                      "traffic": measured_traffic(w.name, statistics.mean(dec_bytes)),
                      "traffic_unit": "DRAM bytes per launch (ncu capture, scaled to the mean launch)",
-                     "kernel": "kivi_decode_kernel<128,2,2,4>", "peak_source": f"{peak_kind} hbm_gbs",
+                     "kernel": "kivi_decode_kernel<128,2,2,4,NoSeqs>", "peak_source": f"{peak_kind} hbm_gbs",
                      "decode_us": round(statistics.mean(dec_times) * 1e6, 2)},
         "device_status": status,
     }
