@@ -27,11 +27,21 @@ a magnitude at or above 57344 (infinity included) gives +-57344 (0x7B or
 Per-head granularity (the same page, section 10.1): one K scale and one V
 scale per kv head.
 
+FP8-domain attention (the same page, section 18.7, and the aiinfraguide page's
+note on section 6: with FP8 KV and the FlashAttention-3 backend the query is
+quantized to FP8 as well, so q.k^T runs on FP8 operands and the query's scale
+matters).
+
 Readings: the scale is float32, computed from the fp16 amax as
 ``fl32(amax / FMAX)`` with FMAX the format's largest finite value (448 for
 E4M3, the pages' formula; 57344 for E5M2 by the same rule, which the pages do
 not spell out); per kv head the amax is taken over that head's slice (every
 batch row, token and channel); an all-zero tensor (or slice) takes scale 1.
+For FP8-domain attention the pages give no query scale rule: the query of one
+decode step (every batch row, query head and channel) is quantized to E4M3
+with the per-tensor rule of the cache, ``fl32(amax_q / 448)``; only q.k^T is
+in the FP8 domain (the softmax weights stay in high precision for p.V, which
+the pages do not say is quantized).
 """
 from __future__ import annotations
 
@@ -197,3 +207,16 @@ def gather_paged(pool: np.ndarray, block_table: np.ndarray, b: int, h: int, seq_
         n = min(bs, seq_len - t0)
         rows.append(pool[block_table[b, t0 // bs], h, :n, :])
     return np.concatenate(rows, axis=0) if rows else np.zeros((0, pool.shape[3]), np.uint8)
+
+
+def quantize_query(q16: np.ndarray):
+    """The query of one decode step in E4M3 for FP8-domain attention:
+    ``(codes uint8 [B, Hq, D], scale float32)`` with the per-tensor scale
+    ``fl32(amax_q / 448)`` (1 for an all-zero query)."""
+    scale = dynamic_scale(q16, "e4m3")
+    return quantize(q16, scale, "e4m3"), scale
+
+
+def query_hat(codes: np.ndarray, scale) -> np.ndarray:
+    """The query FP8-domain attention uses: ``decode(codes) * scale`` in float64."""
+    return e4m3_decode(codes).astype(np.float64) * float(scale)

@@ -150,24 +150,37 @@ def pack_cache(cache) -> dict:
 #            8nt + g (nt < D/8).
 
 def fp8_block_order(head_dim: int, value_layout: int) -> np.ndarray:
-    """perm[storage_byte] = index into the natural row-major [16, D] block."""
+    """perm[storage_byte] = index into the natural row-major [16, D] block.
+
+    value_layout 0 (keys) and 1 (values) hold byte pairs (m16n8k16 fragments
+    after an exact fp8 -> fp16 conversion); value_layout 2 (keys read by FP8
+    tensor cores) holds 4-byte words: word w = (nt * (D/32) + kk) * 2 + r of
+    lane (g, tig) is channels 32*kk + 16*r + 4*tig .. +3 of token 8*nt + g.
+    """
     d = head_dim
     perm = np.full(16 * d, -1, np.int64)
     for lane in range(32):
         g, tig = lane // 4, lane % 4
-        for i in range(d // 4):
-            if value_layout:
-                nt, r = i // 2, i % 2
-                t0 = 8 * r + 2 * tig
-                elems = [(t0, 8 * nt + g), (t0 + 1, 8 * nt + g)]
-            else:
-                nt, rem = i // (d // 8), i % (d // 8)
-                ks, r = rem // 2, rem % 2
-                d0 = 16 * ks + 8 * r + 2 * tig
-                elems = [(8 * nt + g, d0), (8 * nt + g, d0 + 1)]
-            for e, (tok, ch) in enumerate(elems):
-                p = 2 * i + e
-                perm[((p // 16) * 32 + lane) * 16 + p % 16] = tok * d + ch
+        elems = []                                   # (token, channel) of stream bytes 0, 1, 2, ...
+        if value_layout == 2:
+            for w in range(d // 8):
+                nt, rem = w // (d // 16), w % (d // 16)
+                kk, r = rem // 2, rem % 2
+                c0 = 32 * kk + 16 * r + 4 * tig
+                elems += [(8 * nt + g, c0 + e) for e in range(4)]
+        else:
+            for i in range(d // 4):
+                if value_layout == 1:
+                    nt, r = i // 2, i % 2
+                    t0 = 8 * r + 2 * tig
+                    elems += [(t0, 8 * nt + g), (t0 + 1, 8 * nt + g)]
+                else:
+                    nt, rem = i // (d // 8), i % (d // 8)
+                    ks, r = rem // 2, rem % 2
+                    d0 = 16 * ks + 8 * r + 2 * tig
+                    elems += [(8 * nt + g, d0), (8 * nt + g, d0 + 1)]
+        for p, (tok, ch) in enumerate(elems):
+            perm[((p // 16) * 32 + lane) * 16 + p % 16] = tok * d + ch
     assert np.all(perm >= 0)
     return perm
 

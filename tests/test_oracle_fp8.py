@@ -238,3 +238,33 @@ def test_per_head_scales_follow_each_head():
         # each nonzero head reaches the format's largest code, which one per-tensor scale would not
         for h in range(3):
             assert np.max(q[:, h] & 0x7F) == (0x7E if fmt == "e4m3" else 0x7B)
+
+
+def test_query_on_the_grid_is_unchanged():
+    """A query whose values are E4M3 values with amax exactly 448 has scale 1,
+    and FP8-domain attention then uses the query itself."""
+    rng = np.random.default_rng(11)
+    grid = fp8.e4m3_decode(np.arange(0x7F, dtype=np.uint8))      # every finite non-negative E4M3 value
+    q = rng.choice(grid, size=(2, 4, 64)) * rng.choice([-1.0, 1.0], size=(2, 4, 64))
+    q[0, 0, 0] = 448.0
+    q16 = q.astype(np.float16)
+    codes, scale = fp8.quantize_query(q16)
+    assert scale == np.float32(1.0)
+    assert np.array_equal(fp8.query_hat(codes, scale), q16.astype(np.float64))
+
+
+def test_query_quantization_error_bound():
+    """Every quantized query element is within half an E4M3 step of q/scale:
+    2^-4 relative in the normal range, 2^-10 absolute below it (half the
+    smallest subnormal, 2^-9); the largest magnitude lands on +-448."""
+    rng = np.random.default_rng(12)
+    q16 = (rng.standard_normal((4, 8, 128)) * rng.lognormal(0, 1, size=(4, 8, 1))).astype(np.float16)
+    codes, scale = fp8.quantize_query(q16)
+    y = q16.astype(np.float64) / float(scale)
+    yh = fp8.e4m3_decode(codes).astype(np.float64)
+    bound = np.maximum(np.abs(y) * 2.0 ** -4, 2.0 ** -10) * (1 + 2.0 ** -20)
+    assert np.all(np.abs(yh - y) <= bound)
+    i = np.unravel_index(np.argmax(np.abs(q16.astype(np.float64))), q16.shape)
+    assert codes[i] in (0x7E, 0xFE)
+    z_codes, z_scale = fp8.quantize_query(np.zeros((1, 2, 64), np.float16))
+    assert z_scale == np.float32(1.0) and not z_codes.any()

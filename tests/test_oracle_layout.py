@@ -177,3 +177,41 @@ def test_fp8_block_order_fragments(d):
                     tile[2 * tig + 8, g], tile[2 * tig + 9, g] = lb[4 * nt + 2], lb[4 * nt + 3]
                 assert np.array_equal(tile, nat[:, 8 * nt:8 * nt + 8])
         assert np.array_equal(layout.fp8_unpack_pool(layout.fp8_pack_pool(blk, vl), d, vl), blk)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_fp8_key_order_for_fp8_tensor_cores(d):
+    """value_layout 2 against the m16n8k32 8-bit operand fragments: lane (g, tig)
+    holds B[k][n] for k = 4*tig .. 4*tig + 3 (first register) and 16 + 4*tig ..
+    (second), n = g, with k = channel and n = token; a simulated m16n8k32 over
+    those fragments and row-major query bytes gives the plain product."""
+    rng = np.random.default_rng(d + 2)
+    blk = rng.integers(0, 256, size=(1, 1, 16, d), dtype=np.uint8)
+    perm = layout.fp8_block_order(d, 2)
+    assert sorted(perm) == list(range(16 * d))
+    packed = layout.fp8_pack_pool(blk, 2)[0, 0]
+    assert np.array_equal(layout.fp8_unpack_pool(layout.fp8_pack_pool(blk, 2), d, 2), blk)
+    lane_bytes = lambda lane: np.array([packed[((p // 16) * 32 + lane) * 16 + p % 16] for p in range(d // 2)])
+    nat = blk[0, 0].astype(np.int64)
+    qa = rng.integers(-8, 8, size=(16, d))            # a query tile (rows = heads), small integers
+    for nt in range(2):
+        acc = np.zeros((16, 8), np.int64)
+        for kk in range(d // 32):
+            tile = np.zeros((32, 8), np.int64)
+            for lane in range(32):
+                g, tig = lane // 4, lane % 4
+                lb = lane_bytes(lane)
+                w0 = (nt * (d // 32) + kk) * 2
+                tile[4 * tig:4 * tig + 4, g] = lb[4 * w0:4 * w0 + 4]
+                tile[16 + 4 * tig:16 + 4 * tig + 4, g] = lb[4 * w0 + 4:4 * w0 + 8]
+            assert np.array_equal(tile, nat[8 * nt:8 * nt + 8, 32 * kk:32 * kk + 32].T)
+            # A fragment of m16n8k32: rows g / g + 8, columns 4*tig.. and 16 + 4*tig.. of the tile
+            a = np.zeros((16, 32), np.int64)
+            for lane in range(32):
+                g, tig = lane // 4, lane % 4
+                for r in (g, g + 8):
+                    for half in (0, 16):
+                        cols = slice(half + 4 * tig, half + 4 * tig + 4)
+                        a[r, cols] = qa[r, 32 * kk:32 * kk + 32][cols]
+            acc += a @ tile
+        assert np.array_equal(acc, qa @ nat[8 * nt:8 * nt + 8].T)
