@@ -480,7 +480,7 @@ def run_table(args):
 
     names = args.table.split(",") if args.table != "all" else [
         workloads.MHA_4K.name, workloads.GQA_8K_2BIT.name, workloads.GQA_8K_4BIT.name, workloads.STREAM_128K.name,
-        workloads.FP8_32K.name, workloads.FP8_32K_E5M2_PH.name, workloads.PAGED_GQA_8K.name,
+        workloads.FP8_32K.name, workloads.FP8_32K_E5M2_PH.name, workloads.FP8_32K_QFP8.name, workloads.PAGED_GQA_8K.name,
         workloads.PAGED_VAR_16K.name]
     for name in names:
         w = workloads.WORKLOADS[name]
@@ -528,7 +528,7 @@ def run_table(args):
             wsq = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
             t_q = []
             tbl = dev(table)
-            for x16, vl in ((k, 0), (v, 1)):
+            for x16, vl in ((k, 2 if w.q_fp8 else 0), (v, 1)):
                 xd = dev(x16)
                 pool = torch.empty((nb, w.kv_heads, 16 * w.head_dim), dtype=torch.uint8, device="cuda")
                 sc = torch.zeros(w.kv_heads if w.per_head else 1, dtype=torch.float32, device="cuda")
@@ -548,7 +548,7 @@ def run_table(args):
                                                            w.batch, w.q_heads, w.kv_heads, w.head_dim, 16,
                                                            w.blocks_per_seq, nb, w.context, out, True, 0.0, ws,
                                                            wsd, per_head=w.per_head,
-                                                           fp8_format=kvq.FP8_FORMATS[w.fmt]))
+                                                           fp8_format=kvq.FP8_FORMATS[w.fmt], q_fp8=w.q_fp8))
             nbytes = metrics.fp8_decode_bytes(w.batch, w.kv_heads, w.q_heads, w.head_dim, w.context,
                                               w.blocks_per_seq)
             qbytes = metrics.fp8_quantize_bytes(w.batch, w.kv_heads, w.context, w.head_dim, True)

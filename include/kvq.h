@@ -338,7 +338,11 @@ KVQ_API size_t fp8_quantize_workspace_bytes(int32_t batch, int32_t kv_heads, int
  *   fp8_format  : 0 = E4M3 (FMAX 448), 1 = E5M2 (1 sign, 5 exponent bits with
  *                 bias 15, 2 mantissa bits; FMAX 57344; [CSDN] section 18.4;
  *                 round to nearest even, saturating to +-57344, NaN -> 0x7F)
- *   value_layout: 0 for keys, 1 for values (the in-block order above)
+ *   value_layout: 0 for keys, 1 for values (the in-block order above), 2 for
+ *                 keys read by FP8 tensor cores (fp8_decode_attention with
+ *                 q_fp8 = 1): 4-byte word w = (nt*(D/32) + kk)*2 + r of lane
+ *                 (g, tig) holds channels 32*kk + 16*r + 4*tig .. +3 of token
+ *                 8*nt + g (nt < 2), the B fragments of mma.sync m16n8k32
  * byte = FP8(fl32(x / scale)). Block-table entries outside [0, num_blocks)
  * are skipped (nothing is written for that block). per_head and fp8_format
  * outside {0, 1} return KVQ_ERR_ARG. */
@@ -348,8 +352,12 @@ KVQ_API kvq_status fp8_kv_quantize(const uint16_t* x, int32_t batch, int32_t kv_
                            int32_t static_scale, int32_t per_head, int32_t fp8_format,
                            int32_t value_layout, void* ws, size_t ws_bytes, void* stream);
 
-/* Workspace of fp8_decode_attention (split-K partials + status word, as for
- * kv_decode_workspace_bytes). */
+/* Workspace of fp8_decode_attention: the layout of kv_decode_workspace_bytes
+ * (status word, split counters, partials) for this batch and q_heads, then, at
+ * byte offset kv_decode_workspace_bytes of the same shape, the E4M3 query of
+ * a q_fp8 call (B*H_q*D bytes, row-major like q, the region rounded up to 256
+ * bytes), its float32 scale (one value in a 256-byte slot) and 1 KiB of amax
+ * partials. */
 KVQ_API size_t fp8_decode_workspace_bytes(int32_t batch, int32_t q_heads, int32_t head_dim);
 
 /* Decode attention over the FP8 paged cache:
@@ -360,6 +368,14 @@ KVQ_API size_t fp8_decode_workspace_bytes(int32_t batch, int32_t q_heads, int32_
  *   k_scale, v_scale : device float32, one value each (per_head == 0) or one
  *              per kv head [H_kv] (per_head == 1), as fp8_kv_quantize wrote them
  *   fp8_format : the pools' format, 0 = E4M3, 1 = E5M2
+ *   q_fp8    : 0: q stays fp16 (scores from q and the exactly converted keys);
+ *              1: FP8-domain attention ([CSDN] section 18.7: with FP8 KV and
+ *              FlashAttention-3 the query is quantized too): q is quantized to
+ *              E4M3 with the per-tensor dynamic scale q_scale = fl32(amax_q /
+ *              448) over the whole q (1 if q is all zeros), byte =
+ *              E4M3(fl32(q / q_scale)), and the scores are (E4M3 q) . (FP8 k)
+ *              * q_scale * k_scale on FP8 tensor cores; the key pool must then
+ *              hold value_layout 2. The softmax weights stay fp32 for p.V.
  *   seq_lens : device int32 [B], each in [1, max_seq_len]
  * The host passes max_seq_len >= every seq_lens[b] (it sizes the grid) and
  * max_seq_len <= max_blocks*16. Block-table entries must lie in
@@ -367,7 +383,8 @@ KVQ_API size_t fp8_decode_workspace_bytes(int32_t batch, int32_t q_heads, int32_
  * gives wrong numbers but never an access outside the pool or the table. */
 KVQ_API kvq_status fp8_decode_attention(const uint16_t* q, const uint8_t* k_pool, const uint8_t* v_pool,
                                 const float* k_scale, const float* v_scale, int32_t per_head,
-                                int32_t fp8_format, const int32_t* block_table, const int32_t* seq_lens,
+                                int32_t fp8_format, int32_t q_fp8, const int32_t* block_table,
+                                const int32_t* seq_lens,
                                 int32_t batch, int32_t q_heads, int32_t kv_heads, int32_t head_dim,
                                 int32_t block_size, int32_t max_blocks, int32_t num_blocks,
                                 int32_t max_seq_len, void* out, int32_t out_fp32,

@@ -17,6 +17,7 @@ using kvq::kWsHeader;
 namespace {
 
 constexpr int kAmaxBlocksMax = 4096;
+constexpr int kQueryAmaxBlocks = 256;  // amax blocks over a decode query (each cast block reduces them all)
 constexpr int kMinUnitsPerSplit = 8;  // groups (or paged blocks) per split: two per warp
 
 bool aligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
@@ -761,7 +762,7 @@ kvq_status fp8_kv_quantize(const uint16_t* x, int32_t batch, int32_t kv_heads, i
   if (batch <= 0 || kv_heads <= 0 || seq_len <= 0 || num_blocks <= 0 || max_blocks <= 0) return KVQ_ERR_ARG;
   if (head_dim != 64 && head_dim != 128) return KVQ_ERR_UNSUPPORTED;
   if (block_size != 16) return KVQ_ERR_UNSUPPORTED;
-  if (value_layout != 0 && value_layout != 1) return KVQ_ERR_ARG;
+  if (value_layout < 0 || value_layout > 2) return KVQ_ERR_ARG;
   if (per_head != 0 && per_head != 1) return KVQ_ERR_ARG;
   if (fp8_format != 0 && fp8_format != 1) return KVQ_ERR_ARG;
   if (per_head && kv_heads > kAmaxBlocksMax) return KVQ_ERR_UNSUPPORTED;
@@ -798,13 +799,25 @@ kvq_status fp8_kv_quantize(const uint16_t* x, int32_t batch, int32_t kv_heads, i
   return from_cuda(kvq::launch_fp8_quantize(a, static_cast<cudaStream_t>(stream)));
 }
 
+// FP8 decode workspace: the split-K layout of decode_ws_bytes, then the E4M3
+// query (B*Hq*D bytes, rounded to 256), its scale (a 256-byte slot) and the
+// amax partials of the query (kQueryAmaxBlocks words).
+size_t fp8_query_bytes(int batch, int q_heads, int head_dim) {
+  return (static_cast<size_t>(batch) * q_heads * head_dim + 255) / 256 * 256;
+}
+
+size_t fp8_decode_ws_bytes(int batch, int q_heads, int head_dim) {
+  return decode_ws_bytes(batch, q_heads, head_dim) + fp8_query_bytes(batch, q_heads, head_dim) + 256 +
+         static_cast<size_t>(kQueryAmaxBlocks) * sizeof(uint32_t);
+}
+
 size_t fp8_decode_workspace_bytes(int32_t batch, int32_t q_heads, int32_t head_dim) {
   if (batch <= 0 || q_heads <= 0 || head_dim <= 0) return 0;
-  return decode_ws_bytes(batch, q_heads, head_dim);
+  return fp8_decode_ws_bytes(batch, q_heads, head_dim);
 }
 
 kvq_status fp8_decode_attention(const uint16_t* q, const uint8_t* k_pool, const uint8_t* v_pool, const float* k_scale,
-                                const float* v_scale, int32_t per_head, int32_t fp8_format,
+                                const float* v_scale, int32_t per_head, int32_t fp8_format, int32_t q_fp8,
                                 const int32_t* block_table, const int32_t* seq_lens,
                                 int32_t batch, int32_t q_heads, int32_t kv_heads, int32_t head_dim, int32_t block_size,
                                 int32_t max_blocks, int32_t num_blocks, int32_t max_seq_len, void* out,
@@ -814,6 +827,7 @@ kvq_status fp8_decode_attention(const uint16_t* q, const uint8_t* k_pool, const 
     return KVQ_ERR_ARG;
   if (per_head != 0 && per_head != 1) return KVQ_ERR_ARG;
   if (fp8_format != 0 && fp8_format != 1) return KVQ_ERR_ARG;
+  if (q_fp8 != 0 && q_fp8 != 1) return KVQ_ERR_ARG;
   if (batch > 65535 || kv_heads > 65535) return KVQ_ERR_UNSUPPORTED;
   if (head_dim != 64 && head_dim != 128) return KVQ_ERR_UNSUPPORTED;
   if (block_size != 16) return KVQ_ERR_UNSUPPORTED;
@@ -825,10 +839,25 @@ kvq_status fp8_decode_attention(const uint16_t* q, const uint8_t* k_pool, const 
     return KVQ_ERR_ALIGN;
   if (ws == nullptr) return KVQ_ERR_WORKSPACE;
   if (!aligned(ws)) return KVQ_ERR_ALIGN;
-  if (ws_bytes < decode_ws_bytes(batch, q_heads, head_dim)) return KVQ_ERR_WORKSPACE;
+  if (ws_bytes < fp8_decode_ws_bytes(batch, q_heads, head_dim)) return KVQ_ERR_WORKSPACE;
   if (!(softmax_scale == softmax_scale) || std::isinf(softmax_scale)) return KVQ_ERR_ARG;
   const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(head_dim));
   const int nblk = ceil_div(max_seq_len, block_size);
+  uint8_t* const q_area = static_cast<uint8_t*>(ws) + decode_ws_bytes(batch, q_heads, head_dim);
+  uint8_t* const q8 = q_area;
+  float* const q_scale = reinterpret_cast<float*>(q_area + fp8_query_bytes(batch, q_heads, head_dim));
+  if (q_fp8) {
+    kvq::Fp8QueryArgs qa{};
+    qa.q = q;
+    qa.n = static_cast<long long>(batch) * q_heads * head_dim;
+    qa.q8 = q8;
+    qa.q_scale = q_scale;
+    qa.partials = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(q_scale) + 256);
+    qa.amax_blocks = static_cast<int>(std::max<long long>(
+        1, std::min<long long>(kQueryAmaxBlocks, (qa.n / 8 + 255) / 256)));
+    const kvq_status st = from_cuda(kvq::launch_fp8_quantize_query(qa, static_cast<cudaStream_t>(stream)));
+    if (st != KVQ_OK) return st;
+  }
   const int splits = choose_splits(nblk, batch * kv_heads, kMaxSplits, kvq::fp8_decode_blocks_per_sm(head_dim), 0);
   kvq::Fp8DecodeArgs a{};
   a.q = q;
@@ -838,6 +867,9 @@ kvq_status fp8_decode_attention(const uint16_t* q, const uint8_t* k_pool, const 
   a.v_scale = v_scale;
   a.per_head = per_head;
   a.fmt = fp8_format;
+  a.q_fp8 = q_fp8;
+  a.q8 = q8;
+  a.q_scale = q_scale;
   a.block_table = block_table;
   a.seq_lens = seq_lens;
   a.batch = batch;

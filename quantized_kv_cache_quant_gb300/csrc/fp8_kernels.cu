@@ -8,7 +8,9 @@
 // 量化" (CSDN), section 10 (q = cast_fp8(x / s), x_hat = float(q) * s, per-tensor
 // scale) and section 13 (paged blocks through a block table); "LLM推理加速KV Cache
 // 量化压缩实战方案" (yunthe), custom-cache section (scale = max|x| / 448); CSDN
-// section 10.1 (per-head scales) and section 18.4 (E5M2).
+// section 10.1 (per-head scales) and section 18.4 (E5M2); section 18.7
+// (FP8-domain attention: the query quantized to FP8 as well, q.k^T on FP8
+// operands).
 #include <cmath>
 
 #include "kvq_device.cuh"
@@ -193,7 +195,13 @@ __device__ __forceinline__ void cast_units(const Fp8QuantArgs& a, __half* bufs) 
         for (int kk = 0; kk < 8; ++kk) {
           const int i = 8 * c + kk;  // byte pair index in the lane's stream
           int tok0, ch0, tok1, ch1;
-          if (a.value_layout) {
+          if (a.value_layout == 2) {
+            // 4-byte word w = (nt * (D/32) + kk) * 2 + r: channels 32kk + 16r + 4tg .. +3 of token 8nt + gg
+            const int w = i >> 1, nt = w / (D / 16), rem = w % (D / 16), kk = rem >> 1, r = rem & 1;
+            tok0 = tok1 = 8 * nt + gg;
+            ch0 = 32 * kk + 16 * r + 4 * tg + 2 * (i & 1);
+            ch1 = ch0 + 1;
+          } else if (a.value_layout) {
             const int nt = i >> 1, r = i & 1;
             tok0 = 8 * r + 2 * tg;
             tok1 = tok0 + 1;
@@ -239,11 +247,68 @@ __global__ void __launch_bounds__(32 * kCastWarps) fp8_cast_kernel(Fp8QuantArgs 
 }
 
 // ---------------------------------------------------------------------------
+// The query in E4M3 (FP8-domain attention): after fp8_amax_kernel's per-block
+// partials over q, every block of the cast reduces the partials itself
+// (q_scale = fl32(amax / 448), 1 for an all-zero q; block 0 stores it), then
+// casts 8 values per thread and step by the same quotient as the cache cast,
+// row-major bytes out. Two launches: a one-block query pass (one SM reads
+// ~35 GB/s) and a separate scale kernel both cost more.
+// ---------------------------------------------------------------------------
+template <int MODE>
+__device__ __forceinline__ void cast_query(const Fp8QueryArgs& a, float scale) {
+  const float y = (MODE == 0) ? 0.0f : __frcp_rn(scale);
+  const long long n_vec = a.n / 8;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n_vec;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const uint4 v = reinterpret_cast<const uint4*>(a.q)[i];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t out[2];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 f = __half22float2(bits_h2(w[k]));
+      const uint32_t pair = f32x2_to_fp8x2<0>(scaled<MODE>(f.x, scale, y), scaled<MODE>(f.y, scale, y));
+      if (k & 1)
+        out[k >> 1] |= pair << 16;
+      else
+        out[k >> 1] = pair;
+    }
+    reinterpret_cast<uint2*>(a.q8)[i] = make_uint2(out[0], out[1]);
+  }
+}
+
+__global__ void __launch_bounds__(256) fp8_query_cast_kernel(Fp8QueryArgs a) {
+  uint32_t m = 0;
+  for (int i = threadIdx.x; i < a.amax_blocks; i += blockDim.x) m = max(m, a.partials[i]);
+  m = __reduce_max_sync(0xffffffffu, m);
+  __shared__ uint32_t wm[8];
+  __shared__ float s_scale;
+  if ((threadIdx.x & 31) == 0) wm[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t r = 0;
+    for (int k = 0; k < 8; ++k) r = max(r, wm[k]);
+    const float amax = __half2float(__ushort_as_half(static_cast<unsigned short>(r)));
+    const float scale = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
+    s_scale = scale;
+    if (blockIdx.x == 0) *a.q_scale = scale;
+  }
+  __syncthreads();
+  const float scale = s_scale;
+  if (scale >= 0x1p-96f && scale <= 0x1p96f)
+    cast_query<2>(a, scale);
+  else
+    cast_query<0>(a, scale);
+}
+
+// ---------------------------------------------------------------------------
 // Split-K decode attention over the paged FP8 cache.
 // Grid (splits, H_kv, B), 4 warps; warp w of block x takes logical blocks
 // x*bps + w, x*bps + w + 4, ... through a ring of STAGES stages (K block and
 // V block of one kv head, 16*D bytes each) filled by bulk copies.
-//   q.k^T : A = q (fp16, exact), B = E4M3 keys converted to fp16 (exact).
+//   q.k^T : A = q (fp16, exact), B = E4M3 keys converted to fp16 (exact);
+//           with QF (FP8-domain attention) A = the E4M3 query bytes and B =
+//           the key bytes as stored (value_layout 2), on the FP8 tensor path
+//           (m16n8k32), scores scaled by q_scale * k_scale.
 //   p.V   : A = p split into fp16 hi + lo rows, B = E4M3 values as fp16.
 // ---------------------------------------------------------------------------
 template <int D, int STAGES>
@@ -256,7 +321,26 @@ struct Fp8Smem {
   static constexpr int BYTES = BAR_BYTES + AREA;
 };
 
-template <int D, int STAGES, int FMT>
+// d += A (16 x 32 E4M3, rows g / g + 8) * B (32 x 8, E4M3 or E5M2 per FMT), f32.
+template <int FMT>
+__device__ __forceinline__ void mma_fp8_16832(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+  if constexpr (FMT == 0) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e5m2.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  }
+}
+
+template <int D, int STAGES, int FMT, bool QF>
 __global__ void __launch_bounds__(128) fp8_decode_kernel(Fp8DecodeArgs a) {
   using S = Fp8Smem<D, STAGES>;
   constexpr int KS = D / 16, NT = D / 8, CH = D / 32;  // CH: 16-byte chunks per lane
@@ -307,13 +391,25 @@ __global__ void __launch_bounds__(128) fp8_decode_kernel(Fp8DecodeArgs a) {
   const bool row_ok = g < gq;
   const __half* qrow = reinterpret_cast<const __half*>(a.q) +
                        (static_cast<long long>(b) * a.q_heads + h * gq + (row_ok ? g : 0)) * D;
-  uint32_t qa[KS][2];
+  // fp16 query: A fragments of m16n8k16 (rows g, channels 16ks + 8jj + 2tig, +1);
+  // E4M3 query (QF): A fragments of m16n8k32 (rows g, channels 32kk + 16jj + 4tig .. +3)
+  constexpr int QW = QF ? D / 32 : KS;
+  uint32_t qa[QW][2];
+  if constexpr (QF) {
+    const uint8_t* q8row = a.q8 + (static_cast<long long>(b) * a.q_heads + h * gq + (row_ok ? g : 0)) * D;
 #pragma unroll
-  for (int ks = 0; ks < KS; ++ks)
+    for (int kk = 0; kk < QW; ++kk)
 #pragma unroll
-    for (int jj = 0; jj < 2; ++jj)
-      qa[ks][jj] = row_ok ? *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8 * jj + 2 * tig) : 0u;
-  const float kmul = a.k_scale[a.per_head ? h : 0] * a.scale_log2;
+      for (int jj = 0; jj < 2; ++jj)
+        qa[kk][jj] = row_ok ? *reinterpret_cast<const uint32_t*>(q8row + 32 * kk + 16 * jj + 4 * tig) : 0u;
+  } else {
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj)
+        qa[ks][jj] = row_ok ? *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8 * jj + 2 * tig) : 0u;
+  }
+  const float kmul = a.k_scale[a.per_head ? h : 0] * a.scale_log2 * (QF ? *a.q_scale : 1.0f);
   const float vscale = a.v_scale[a.per_head ? h : 0];
 
   float m_run = -INFINITY, l_run = 0.0f;
@@ -349,11 +445,19 @@ __global__ void __launch_bounds__(128) fp8_decode_kernel(Fp8DecodeArgs a) {
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
       sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.0f;
+      if constexpr (QF) {
+        // value_layout 2: words (nt * (D/32) + kk) * 2 + {0, 1} are this lane's B fragment
 #pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-        const uint32_t w = kw[nt * KS + ks];
-        mma16816(sacc[nt], qa[ks][0], 0u, qa[ks][1], 0u, fp8x2_to_f16x2<FMT>(static_cast<uint16_t>(w & 0xFFFFu)),
-                 fp8x2_to_f16x2<FMT>(static_cast<uint16_t>(w >> 16)));
+        for (int kk = 0; kk < QW; ++kk)
+          mma_fp8_16832<FMT>(sacc[nt], qa[kk][0], 0u, qa[kk][1], 0u, kw[(nt * QW + kk) * 2],
+                             kw[(nt * QW + kk) * 2 + 1]);
+      } else {
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          const uint32_t w = kw[nt * KS + ks];
+          mma16816(sacc[nt], qa[ks][0], 0u, qa[ks][1], 0u, fp8x2_to_f16x2<FMT>(static_cast<uint16_t>(w & 0xFFFFu)),
+                   fp8x2_to_f16x2<FMT>(static_cast<uint16_t>(w >> 16)));
+        }
       }
     }
     float sc[4];
@@ -437,10 +541,10 @@ __global__ void __launch_bounds__(128) fp8_decode_kernel(Fp8DecodeArgs a) {
 
 constexpr int kFp8Stages = 4;
 
-template <int D, int FMT>
+template <int D, int FMT, bool QF>
 cudaError_t fp8_decode_dispatch(const Fp8DecodeArgs& a, cudaStream_t s) {
   constexpr int smem = Fp8Smem<D, kFp8Stages>::BYTES;
-  auto kern = fp8_decode_kernel<D, kFp8Stages, FMT>;
+  auto kern = fp8_decode_kernel<D, kFp8Stages, FMT, QF>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(a.splits, a.kv_heads, a.batch);
@@ -455,7 +559,7 @@ int fp8_occupancy() {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
   if (cached[dev] == 0) {
     constexpr int smem = Fp8Smem<D, kFp8Stages>::BYTES;
-    auto kern = fp8_decode_kernel<D, kFp8Stages, 0>;  // both formats use the same resources
+    auto kern = fp8_decode_kernel<D, kFp8Stages, 0, false>;  // every variant uses about the same resources
     int n = 0;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, 128, smem) != cudaSuccess || n <= 0)
@@ -515,13 +619,30 @@ cudaError_t launch_fp8_quantize(const Fp8QuantArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_fp8_decode(const Fp8DecodeArgs& a, cudaStream_t s) {
-  switch (a.head_dim * 10 + a.fmt) {
-    case 1280: return fp8_decode_dispatch<128, 0>(a, s);
-    case 1281: return fp8_decode_dispatch<128, 1>(a, s);
-    case 640: return fp8_decode_dispatch<64, 0>(a, s);
-    case 641: return fp8_decode_dispatch<64, 1>(a, s);
+  switch (a.head_dim * 100 + a.fmt * 10 + (a.q_fp8 ? 1 : 0)) {
+    case 12800: return fp8_decode_dispatch<128, 0, false>(a, s);
+    case 12810: return fp8_decode_dispatch<128, 1, false>(a, s);
+    case 6400: return fp8_decode_dispatch<64, 0, false>(a, s);
+    case 6410: return fp8_decode_dispatch<64, 1, false>(a, s);
+    case 12801: return fp8_decode_dispatch<128, 0, true>(a, s);
+    case 12811: return fp8_decode_dispatch<128, 1, true>(a, s);
+    case 6401: return fp8_decode_dispatch<64, 0, true>(a, s);
+    case 6411: return fp8_decode_dispatch<64, 1, true>(a, s);
     default: return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t launch_fp8_quantize_query(const Fp8QueryArgs& a, cudaStream_t s) {
+  if (a.n <= 0) return cudaSuccess;
+  const long long n_vec = a.n / 8;
+  fp8_amax_kernel<<<dim3(a.amax_blocks, 1), 256, 0, s>>>(reinterpret_cast<const uint4*>(a.q), n_vec, 1, 1, n_vec,
+                                                          a.partials);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const long long want = (n_vec + 255) / 256;
+  const long long full = 2LL * device_sm_count();
+  fp8_query_cast_kernel<<<static_cast<int>(want < full ? want : full), 256, 0, s>>>(a);
+  return cudaGetLastError();
 }
 
 }  // namespace kvq

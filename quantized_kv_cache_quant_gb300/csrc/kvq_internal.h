@@ -144,7 +144,7 @@ struct Fp8QuantArgs {
   int static_scale;
   int per_head;
   int fmt;                // 0 = E4M3, 1 = E5M2
-  int value_layout;
+  int value_layout;       // 0 keys, 1 values, 2 keys for FP8 tensor cores
   uint32_t* amax_partials;  // [per_head ? H_kv : 1][amax_blocks]
   int amax_blocks;
 };
@@ -160,6 +160,9 @@ struct Fp8DecodeArgs {
   int fmt;                // 0 = E4M3, 1 = E5M2
   const int32_t* block_table;
   const int32_t* seq_lens;
+  int q_fp8;              // q.k^T on FP8 tensor cores from q8 (keys in value_layout 2)
+  const uint8_t* q8;      // [B, Hq, D] E4M3 query (q_fp8)
+  const float* q_scale;   // [1] (q_fp8)
   int batch, q_heads, kv_heads, head_dim, max_blocks, num_blocks;
   int splits;
   int blocks_per_split;
@@ -172,6 +175,19 @@ struct Fp8DecodeArgs {
   int out_fp32;
 };
 cudaError_t launch_fp8_decode(const Fp8DecodeArgs& a, cudaStream_t s);
+
+// The query of one decode step in E4M3 with a per-tensor dynamic scale:
+// q_scale = fl32(amax / 448) (1 when q is all zeros), then
+// q8 = E4M3(fl32(q / q_scale)), row-major like q.
+struct Fp8QueryArgs {
+  const uint16_t* q;
+  long long n;            // elements, a multiple of 8
+  uint8_t* q8;
+  float* q_scale;
+  uint32_t* partials;     // [amax_blocks]
+  int amax_blocks;
+};
+cudaError_t launch_fp8_quantize_query(const Fp8QueryArgs& a, cudaStream_t s);
 
 int device_sm_count();
 // Resident thread blocks per SM of the decode kernels (occupancy API, cached).

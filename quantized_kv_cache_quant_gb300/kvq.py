@@ -93,8 +93,8 @@ _SIG = {
     "fp8_kv_quantize": ([c_vp, c_i32, c_i32, c_i32, c_i32, c_vp, c_i32, c_i32, c_i32, c_vp, c_vp, c_i32, c_i32,
                          c_i32, c_i32, c_vp, c_sz, c_vp], ctypes.c_int),
     "fp8_decode_workspace_bytes": ([c_i32, c_i32, c_i32], c_sz),
-    "fp8_decode_attention": ([c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, c_i32, c_vp, c_vp, c_i32, c_i32, c_i32, c_i32,
-                              c_i32, c_i32, c_i32, c_i32, c_vp, c_i32, c_f32, c_vp, c_sz, c_vp], ctypes.c_int),
+    "fp8_decode_attention": ([c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, c_i32, c_i32, c_vp, c_vp, c_i32, c_i32, c_i32,
+                              c_i32, c_i32, c_i32, c_i32, c_i32, c_vp, c_i32, c_f32, c_vp, c_sz, c_vp], ctypes.c_int),
 }
 for _name, (_args, _res) in _SIG.items():
     _fn = getattr(_lib, _name)
@@ -244,9 +244,9 @@ def fp8_decode_workspace_bytes(batch, q_heads, head_dim) -> int:
 def fp8_decode_attention(q, k_pool, v_pool, k_scale, v_scale, block_table, seq_lens, batch, q_heads, kv_heads,
                          head_dim, block_size, max_blocks, num_blocks, max_seq_len, out, out_fp32: bool,
                          softmax_scale: float, ws, ws_bytes: int, stream=None, per_head: bool = False,
-                         fp8_format: int = 0) -> None:
+                         fp8_format: int = 0, q_fp8: bool = False) -> None:
     _check(_lib.fp8_decode_attention(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(k_scale), _ptr(v_scale),
-                                     int(per_head), int(fp8_format),
+                                     int(per_head), int(fp8_format), int(q_fp8),
                                      _ptr(block_table), _ptr(seq_lens), batch, q_heads, kv_heads, head_dim,
                                      block_size, max_blocks, num_blocks, max_seq_len, _ptr(out),
                                      int(bool(out_fp32)), float(softmax_scale), _ptr(ws), ws_bytes,

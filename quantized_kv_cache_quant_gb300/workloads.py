@@ -63,6 +63,7 @@ class Fp8Workload:
     seed: int = 3
     fmt: str = "e4m3"          # FP8 format: "e4m3" or "e5m2"
     per_head: bool = False     # one scale per kv head instead of one per tensor
+    q_fp8: bool = False        # FP8-domain attention: the query quantized to E4M3 too
 
     @property
     def blocks_per_seq(self) -> int:
@@ -109,6 +110,8 @@ FP8_32K = Fp8Workload("fp8_e4m3_paged_b64_h8x32_d128_s32768", 64, 8, 32, 128, 32
 # the same cache in E5M2 with one scale per kv head (the FP8 variants of the pages)
 FP8_32K_E5M2_PH = dataclasses.replace(FP8_32K, name="fp8_e5m2_perhead_paged_b64_h8x32_d128_s32768", fmt="e5m2",
                                       per_head=True)
+# the same cache read with the query in E4M3 (FP8-domain attention on FP8 tensor cores)
+FP8_32K_QFP8 = dataclasses.replace(FP8_32K, name="fp8_e4m3_qfp8_paged_b64_h8x32_d128_s32768", q_fp8=True)
 # the same cache for 8 sequences: a size an ncu capture of the quantize kernels can hold
 FP8_32K_B8 = Fp8Workload("fp8_e4m3_paged_b8_h8x32_d128_s32768", 8, 8, 32, 128, 32768, 16, seed=3)
 STREAM_128K = KiviWorkload("kivi2_stream_b4_h8x64_d128_s131072_512steps", 4, 8, 64, 128, 131072, 512, seed=4)
@@ -118,8 +121,8 @@ STREAM_128K = KiviWorkload("kivi2_stream_b4_h8x64_d128_s131072_512steps", 4, 8, 
 PAGED_GQA_8K = PagedKiviWorkload("kivi2_paged_b32_h8x64_d128_len8192", 32, 8, 64, 128, 8192, 8192, seed=5)
 PAGED_VAR_16K = PagedKiviWorkload("kivi2_paged_b32_h8x64_d128_len512-16384", 32, 8, 64, 128, 512, 16384, seed=6)
 
-WORKLOADS = {w.name: w for w in (TINY, MHA_4K, GQA_8K_2BIT, GQA_8K_4BIT, FP8_32K, FP8_32K_E5M2_PH, FP8_32K_B8,
-                                  STREAM_128K, PAGED_GQA_8K, PAGED_VAR_16K)}
+WORKLOADS = {w.name: w for w in (TINY, MHA_4K, GQA_8K_2BIT, GQA_8K_4BIT, FP8_32K, FP8_32K_E5M2_PH, FP8_32K_QFP8,
+                                  FP8_32K_B8, STREAM_128K, PAGED_GQA_8K, PAGED_VAR_16K)}
 
 
 def _channel_scales(rng: np.random.Generator, kv_heads: int, head_dim: int) -> np.ndarray:

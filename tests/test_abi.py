@@ -169,7 +169,7 @@ def test_fp8_validation():
              block_size=16, num_blocks=6, pool=ALIGNED, scale=ALIGNED, static_scale=False, value_layout=0,
              ws=ALIGNED, ws_bytes=kvq.fp8_quantize_workspace_bytes(2, 2, 40, 128))
     for change, code in [(dict(block_size=32), "KVQ_ERR_UNSUPPORTED"), (dict(head_dim=96), "KVQ_ERR_UNSUPPORTED"),
-                         (dict(max_blocks=2), "KVQ_ERR_CAPACITY"), (dict(value_layout=2), "KVQ_ERR_ARG"),
+                         (dict(max_blocks=2), "KVQ_ERR_CAPACITY"), (dict(value_layout=3), "KVQ_ERR_ARG"),
                          (dict(ws_bytes=8), "KVQ_ERR_WORKSPACE"), (dict(pool=None), "KVQ_ERR_NULL"),
                          (dict(scale=ALIGNED + 4), "KVQ_ERR_ALIGN"), (dict(seq_len=0), "KVQ_ERR_ARG"),
                          (dict(per_head=2), "KVQ_ERR_ARG"), (dict(fp8_format=2), "KVQ_ERR_ARG"),
@@ -185,7 +185,9 @@ def test_fp8_validation():
     for change, code in [(dict(q_heads=7), "KVQ_ERR_SHAPE"), (dict(max_seq_len=49), "KVQ_ERR_CAPACITY"),
                          (dict(q_heads=32), "KVQ_ERR_UNSUPPORTED"), (dict(ws_bytes=100), "KVQ_ERR_WORKSPACE"),
                          (dict(seq_lens=None), "KVQ_ERR_NULL"), (dict(per_head=3), "KVQ_ERR_ARG"),
-                         (dict(fp8_format=2), "KVQ_ERR_ARG")]:
+                         (dict(fp8_format=2), "KVQ_ERR_ARG"), (dict(q_fp8=2), "KVQ_ERR_ARG"),
+                         (dict(ws_bytes=kvq.kv_decode_workspace_bytes(kvq.make_config(2, 8, 8, 128, 2, 2, 128, 32))),
+                          "KVQ_ERR_WORKSPACE")]:
         args = dict(d, **change)
         with pytest.raises(kvq.KvqError) as e:
             kvq.fp8_decode_attention(**args, stream=0)
@@ -366,3 +368,11 @@ def test_paged_decode_validation():
     with pytest.raises(kvq.KvqError) as e:
         kvq.kv_paged_decode_attention(cache, ALIGNED, ALIGNED, True, 0.0, ALIGNED, ws, stream=0)
     assert e.value.name == "KVQ_ERR_ARG"
+
+
+def test_fp8_decode_workspace_holds_the_query():
+    """The FP8 decode workspace is the split-K layout followed by the E4M3 query
+    (rounded to 256 bytes), its scale slot and 1 KiB of amax partials."""
+    for b, hq, d in [(2, 8, 128), (64, 32, 128), (3, 5, 64)]:
+        base = kvq.kv_decode_workspace_bytes(kvq.make_config(b, hq, hq, d, 2, 2, 128, 32))
+        assert kvq.fp8_decode_workspace_bytes(b, hq, d) == base + -(-b * hq * d // 256) * 256 + 256 + 1024

@@ -51,7 +51,7 @@ def test_all_fp16_values_cast_exactly():
     allh = np.arange(65536, dtype=np.uint16).view(np.float16)
     x = allh.reshape(1, 4, 128, 128)                     # 4 kv heads x 128 tokens x 128 channels
     table = np.arange(8, dtype=np.int32).reshape(1, 8)
-    for vl in (0, 1):
+    for vl in (0, 1, 2):
         pool, scale = _quantize(x, table, 8, vl, static_scale=1.0)
         want = _oracle_pool(x, table, 8, vl, np.float32(1.0))
         assert np.array_equal(host(pool), want)
@@ -117,9 +117,12 @@ def _decode(q16, kpool, vpool, kscale, vscale, table, seq_lens, hkv, num_blocks,
     return host(out).astype(np.float64), int(host(ws[:4].view(torch.int32))[0])
 
 
-def _oracle_decode(q16, k16, v16, ks, vs, seq_lens, heads=None, fmt="e4m3"):
-    """ks, vs: scalars, or one scale per kv head."""
+def _oracle_decode(q16, k16, v16, ks, vs, seq_lens, heads=None, fmt="e4m3", q_fp8=False):
+    """ks, vs: scalars, or one scale per kv head; q_fp8: attention from the
+    E4M3 query (FP8-domain attention)."""
     b, hkv, s, d = k16.shape
+    if q_fp8:
+        q16 = fp8.query_hat(*fp8.quantize_query(q16))
     ksh = lambda hi: np.float32(ks[hi] if np.ndim(ks) else ks)
     vsh = lambda hi: np.float32(vs[hi] if np.ndim(vs) else vs)
     kh = lambda bi, hi: fp8.decode(fp8.quantize(k16[bi, hi, : seq_lens[bi]], ksh(hi), fmt), fmt) * np.float64(ksh(hi))
@@ -266,3 +269,113 @@ def test_decode_format_and_scale_variants(fmt, per_head, d, gq):
     ref = _oracle_decode(x.q[0], k, x.v, scale_of(k, fmt), scale_of(x.v, fmt), seq_lens, fmt=fmt)
     assert_attention_close(out, ref)
     assert status == 0
+
+
+# ------------------------------------------------------- FP8-domain attention (query in E4M3)
+def _decode_qfp8(q16, kpool, vpool, kscale, vscale, table, seq_lens, hkv, num_blocks, max_seq, fmt="e4m3",
+                 per_head=False):
+    """fp8_decode_attention with q_fp8 = 1: (out, status word, E4M3 query bytes, query scale)
+    read from the workspace at the offsets the header documents."""
+    import torch
+    kvq = _kvq()
+    b, hq, d = q16.shape
+    out = torch.empty((b, hq, d), dtype=torch.float32, device="cuda")
+    wsb = kvq.fp8_decode_workspace_bytes(b, hq, d)
+    ws = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
+    kvq.fp8_decode_attention(dev(q16), kpool, vpool, kscale, vscale, dev(table), dev(seq_lens.astype(np.int32)),
+                             b, hq, hkv, d, 16, table.shape[1], num_blocks, max_seq, out, True, 0.0, ws, wsb,
+                             per_head=per_head, fp8_format=kvq.FP8_FORMATS[fmt], q_fp8=True)
+    off = kvq.kv_decode_workspace_bytes(kvq.make_config(b, hq, hq, d, 2, 2, 128, 32))
+    n = b * hq * d
+    q8 = host(ws[off:off + n]).reshape(b, hq, d)
+    qs_off = off + -(-n // 256) * 256
+    q_scale = host(ws[qs_off:qs_off + 4].view(torch.float32))[0]
+    return host(out).astype(np.float64), int(host(ws[:4].view(torch.int32))[0]), q8, q_scale
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_key_layout_for_fp8_tensor_cores(d):
+    rng = np.random.default_rng(d + 5)
+    x = workloads.make_inputs(2, 3, 6, d, 16 * 4 + 11, 1, 71).k
+    nb = 5
+    table = rng.permutation(2 * nb).astype(np.int32).reshape(2, nb)
+    pool, scale = _quantize(x, table, 2 * nb, 2)
+    s_ref = fp8.dynamic_scale(x)
+    assert host(scale)[0] == s_ref
+    assert np.array_equal(host(pool), _oracle_pool(x, table, 2 * nb, 2, s_ref))
+
+
+@pytest.mark.parametrize("fmt,per_head", [("e4m3", False), ("e5m2", False), ("e4m3", True), ("e5m2", True)])
+@pytest.mark.parametrize("d,gq", [(128, 4), (64, 1), (128, 8), (64, 3)])
+def test_fp8_domain_attention(fmt, per_head, d, gq):
+    """q.k^T from the E4M3 query on FP8 tensor cores: the query bytes and scale
+    are the oracle's bit for bit, attention is within the bars of the oracle
+    on the same quantized query, keys and values."""
+    rng = np.random.default_rng(d + gq + 7 * per_head)
+    b, hkv, s = 3, 2, 16 * 30 + 9
+    x = workloads.make_inputs(b, hkv, hkv * gq, d, s, 1, 81 + gq)
+    k = (x.k.astype(np.float32) * np.array([1.0, 25.0]).reshape(1, 2, 1, 1)).astype(np.float16)
+    q = (x.q[0].astype(np.float32) * 3.0).astype(np.float16)
+    nb = -(-s // 16)
+    table = rng.permutation(b * nb).astype(np.int32).reshape(b, nb)
+    kpool, kscale = _quantize(k, table, b * nb, 2, fmt=fmt, per_head=per_head)
+    vpool, vscale = _quantize(x.v, table, b * nb, 1, fmt=fmt, per_head=per_head)
+    seq_lens = np.array([s, 1, 16 * 11 + 3])
+    out, status, q8, q_scale = _decode_qfp8(q, kpool, vpool, kscale, vscale, table, seq_lens, hkv, b * nb, s,
+                                            fmt=fmt, per_head=per_head)
+    codes_ref, scale_ref = fp8.quantize_query(q)
+    assert q_scale == scale_ref
+    assert np.array_equal(q8, codes_ref)
+    scale_of = fp8.dynamic_scale_per_head if per_head else fp8.dynamic_scale
+    ref = _oracle_decode(q, k, x.v, scale_of(k, fmt), scale_of(x.v, fmt), seq_lens, fmt=fmt, q_fp8=True)
+    assert_attention_close(out, ref)
+    assert status == 0
+
+
+def test_fp8_domain_zero_query():
+    """q = 0: scale 1, zero bytes, every score 0 — attention is the mean of the values."""
+    b, hkv, gq, d, s = 2, 2, 4, 128, 16 * 7 + 5
+    x = workloads.make_inputs(b, hkv, hkv * gq, d, s, 1, 91)
+    nb = -(-s // 16)
+    table = np.arange(b * nb, dtype=np.int32).reshape(b, nb)
+    kpool, kscale = _quantize(x.k, table, b * nb, 2)
+    vpool, vscale = _quantize(x.v, table, b * nb, 1)
+    q = np.zeros((b, hkv * gq, d), np.float16)
+    seq_lens = np.array([s, 40])
+    out, status, q8, q_scale = _decode_qfp8(q, kpool, vpool, kscale, vscale, table, seq_lens, hkv, b * nb, s)
+    assert q_scale == 1.0 and not q8.any()
+    vs = fp8.dynamic_scale(x.v)
+    for bi in range(b):
+        for h in range(hkv):
+            vh = fp8.e4m3_decode(fp8.quantize(x.v[bi, h, :seq_lens[bi]], vs)).astype(np.float64) * float(vs)
+            for hq in range(h * gq, (h + 1) * gq):
+                assert np.allclose(out[bi, hq], vh.mean(axis=0), atol=2e-3, rtol=0)
+
+
+def test_full_size_fp8_domain_attention_32k():
+    """The 32K FP8 workload with the query in E4M3 (keys in value_layout 2):
+    scales and query bytes exact, attention on sampled heads."""
+    import torch
+    w = workloads.FP8_32K
+    k, v, q, table = workloads.fp8_inputs(w)
+    nb_total = w.batch * w.blocks_per_seq
+    kpool, kscale = _quantize(k, table, nb_total, 2)
+    vpool, vscale = _quantize(v, table, nb_total, 1)
+    ks_ref, vs_ref = fp8.dynamic_scale(k), fp8.dynamic_scale(v)
+    assert host(kscale)[0] == ks_ref and host(vscale)[0] == vs_ref
+    rng = np.random.default_rng(4)
+    for _ in range(12):
+        b, h, j = int(rng.integers(w.batch)), int(rng.integers(w.kv_heads)), int(rng.integers(w.blocks_per_seq))
+        want = layout.fp8_pack_pool(fp8.quantize(k[b, h, 16 * j:16 * j + 16], ks_ref)[None, None], 2)[0, 0]
+        assert np.array_equal(host(kpool[table[b, j], h]), want)
+    seq_lens = np.full(w.batch, w.context)
+    out, status, q8, q_scale = _decode_qfp8(q, kpool, vpool, kscale, vscale, table, seq_lens, w.kv_heads,
+                                            nb_total, w.context)
+    assert status == 0
+    codes_ref, scale_ref = fp8.quantize_query(q)
+    assert q_scale == scale_ref and np.array_equal(q8, codes_ref)
+    heads = sorted({(0, 0), (w.batch - 1, w.q_heads - 1), (17, 5), (40, 30), (63, 12), (5, 20)})
+    ref = _oracle_decode(q, k, v, ks_ref, vs_ref, seq_lens, heads, q_fp8=True)
+    assert_attention_close(out, ref, heads)
+    del kpool, vpool
+    torch.cuda.empty_cache()
