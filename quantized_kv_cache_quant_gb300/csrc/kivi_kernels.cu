@@ -89,7 +89,9 @@ __device__ __forceinline__ uint32_t key_word(const __half* xk, int RS, const flo
     for (int nt = 0; nt < 4; ++nt) {
       const float2 x = __half22float2(reinterpret_cast<const __half2*>(xk)[(8 * nt + gg) * (RS / 2) + d0 / 2]);
       const int f = (KB == 2) ? ((4 * r + nt + 1) & 7) : nt;
-      w |= (group_code(x.x, z0, s0, r0, KL) << (KB * f)) | (group_code(x.y, z1, s1, r1, KL) << (16 + KB * f));
+      // fields never overlap: adding the shifted codes sets the same bits as or-ing them, and
+      // w + (c << s) is one shift-and-add
+      w += (group_code(x.x, z0, s0, r0, KL) << (KB * f)) + (group_code(x.y, z1, s1, r1, KL) << (16 + KB * f));
     }
   }
   return w;
@@ -115,7 +117,7 @@ __device__ __forceinline__ uint32_t value_word(const __half* xv, int RS, const f
       const int ch = 8 * (4 * q + n) + gg;
       const float x0 = __half2float(xv[t0 * RS + ch]), x1 = __half2float(xv[(t0 + 1) * RS + ch]);
       const int f = (VB == 2) ? ((4 * r + n + 1) & 7) : n;
-      w |= (group_code(x0, z0, s0, r0, VL) << (VB * f)) | (group_code(x1, z1, s1, r1, VL) << (16 + VB * f));
+      w += (group_code(x0, z0, s0, r0, VL) << (VB * f)) + (group_code(x1, z1, s1, r1, VL) << (16 + VB * f));
     }
   }
   return w;
