@@ -15,7 +15,7 @@ constexpr uint32_t kStatusTimeout = 1u;  // status bit: a device wait gave up
 constexpr int kWsHeader = 256;           // bytes reserved at the start of a decode workspace
 constexpr int kMaxSplits = 64;           // split-K partials per (batch row, query head)
 constexpr int kMaxGqa = 8;               // query heads per kv head handled by one MMA tile
-constexpr int kChunkUnits = 8;           // decode work units (groups) one 32-token window chunk is charged
+constexpr int kChunkUnits = 6;           // decode work units (groups) one 32-token window chunk is charged
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per wait
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
