@@ -273,17 +273,17 @@ def test_decode_format_and_scale_variants(fmt, per_head, d, gq):
 
 # ------------------------------------------------------- FP8-domain attention (query in E4M3)
 def _decode_qfp8(q16, kpool, vpool, kscale, vscale, table, seq_lens, hkv, num_blocks, max_seq, fmt="e4m3",
-                 per_head=False):
+                 per_head=False, out_fp32=True):
     """fp8_decode_attention with q_fp8 = 1: (out, status word, E4M3 query bytes, query scale)
     read from the workspace at the offsets the header documents."""
     import torch
     kvq = _kvq()
     b, hq, d = q16.shape
-    out = torch.empty((b, hq, d), dtype=torch.float32, device="cuda")
+    out = torch.empty((b, hq, d), dtype=torch.float32 if out_fp32 else torch.float16, device="cuda")
     wsb = kvq.fp8_decode_workspace_bytes(b, hq, d)
     ws = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
     kvq.fp8_decode_attention(dev(q16), kpool, vpool, kscale, vscale, dev(table), dev(seq_lens.astype(np.int32)),
-                             b, hq, hkv, d, 16, table.shape[1], num_blocks, max_seq, out, True, 0.0, ws, wsb,
+                             b, hq, hkv, d, 16, table.shape[1], num_blocks, max_seq, out, out_fp32, 0.0, ws, wsb,
                              per_head=per_head, fp8_format=kvq.FP8_FORMATS[fmt], q_fp8=True)
     off = kvq.kv_decode_workspace_bytes(kvq.make_config(b, hq, hq, d, 2, 2, 128, 32))
     n = b * hq * d
@@ -379,3 +379,19 @@ def test_full_size_fp8_domain_attention_32k():
     assert_attention_close(out, ref, heads)
     del kpool, vpool
     torch.cuda.empty_cache()
+
+
+def test_fp8_domain_fp16_output():
+    rng = np.random.default_rng(93)
+    b, hkv, gq, d, s = 2, 2, 4, 128, 16 * 20 + 3
+    x = workloads.make_inputs(b, hkv, hkv * gq, d, s, 1, 94)
+    nb = -(-s // 16)
+    table = rng.permutation(b * nb).astype(np.int32).reshape(b, nb)
+    kpool, kscale = _quantize(x.k, table, b * nb, 2)
+    vpool, vscale = _quantize(x.v, table, b * nb, 1)
+    seq_lens = np.array([s, 100])
+    out, status, q8, q_scale = _decode_qfp8(x.q[0], kpool, vpool, kscale, vscale, table, seq_lens, hkv, b * nb, s,
+                                            out_fp32=False)
+    ref = _oracle_decode(x.q[0], x.k, x.v, fp8.dynamic_scale(x.k), fp8.dynamic_scale(x.v), seq_lens, q_fp8=True)
+    assert_attention_close(out, ref, fp16_out=True)
+    assert status == 0

@@ -259,3 +259,45 @@ def test_full_size_sampled(w):
             got = out[b, hq].astype(np.float64)
             assert np.max(np.abs(got - ref)) <= 2e-3, (b, hq)
             assert np.linalg.norm(got - ref) <= 1e-3 * np.linalg.norm(ref), (b, hq)
+
+
+def test_full_size_streaming_sampled():
+    """The mixed-length table workload streamed for 130 decode steps: every
+    sequence flushes its window once at its own step; state of all sequences,
+    records and windows of three sampled sequences against their own oracle
+    caches, and attention of their heads at the last step."""
+    kvq = _kvq()
+    w = workloads.PAGED_VAR_16K
+    steps = 130
+    x, lens, table = workloads.paged_inputs(w, steps=steps)
+    gc = kvq.PagedKiviCache(w.batch, w.kv_heads, w.q_heads, w.head_dim, w.k_bits, w.v_bits, w.residual,
+                            w.max_len + steps, w.batch * (-(-(w.max_len + steps) // 32)))
+    table = workloads.block_table(w.batch, gc.desc.groups_cap, w.seed + 1000)
+    gc.table.copy_(dev(table))
+    gc.prefill(dev(x.k), dev(x.v), lens.tolist())
+    for step in range(steps):
+        gc.append(dev(x.k_new[step]), dev(x.v_new[step]))
+    q = x.q[steps - 1]
+    out = host(gc.decode(dev(q)))
+    assert gc.status() == 0
+    gq = w.q_heads // w.kv_heads
+    rng = np.random.default_rng(w.seed + 1)
+    for b in sorted(rng.choice(w.batch, size=3, replace=False).tolist()):
+        c = _sampled_sequence_oracle(w, x, lens, b)
+        for step in range(steps):
+            c.append(x.k_new[step][b:b + 1], x.v_new[step][b:b + 1])
+        assert (gc.n_grouped(b), gc.n_resid(b)) == (c.n_grouped, c.n_resid), b
+        ng = c.n_grouped // 32
+        packed = layout.pack_cache(c)
+        for name in NAMES:
+            got = host(gc.pool_view(name))[table[b, :ng]]
+            assert np.array_equal(got.transpose(1, 0, 2), packed[name][0]), (name, b)
+        for name, want in (("k_res", c.k_res[0]), ("v_res", c.v_res[0])):
+            got = host(gc.residual_view(name))[b, :, :c.n_resid]
+            assert np.array_equal(got.view(np.uint16), want.view(np.uint16)), (name, b)
+        for hq in rng.choice(w.q_heads, size=4, replace=False):
+            h = hq // gq
+            ref = attention.softmax_attend(q[b, hq], c.keys_hat(0, h), c.values_hat(0, h), default_scale(w.head_dim))
+            got = out[b, hq].astype(np.float64)
+            assert np.max(np.abs(got - ref)) <= 2e-3, (b, hq)
+            assert np.linalg.norm(got - ref) <= 1e-3 * np.linalg.norm(ref), (b, hq)
