@@ -168,7 +168,7 @@ struct DecodePlan {
   int part_stride;  // the most blocks one pair can touch
 };
 
-constexpr int kSegmentUnits = 16;
+constexpr int kSegmentUnits = 8;
 
 // The same cost as the paged decode charges it ahead of each pair. On GB300
 // (32 sequences, GQA 8, lengths 8192 each or 512 .. 16384) 8 units measured
