@@ -321,6 +321,25 @@ struct Fp8Smem {
   static constexpr int BYTES = BAR_BYTES + AREA;
 };
 
+// The two fp16x2 operands of one word of four FP8 bytes: bytes 0-1 and bytes
+// 2-3. An E5M2 byte is the top byte of the fp16 of the same value, so each
+// half is one byte permute straight from the word (no extraction of the 16-bit
+// half first); E4M3 converts each 16-bit half with its conversion instruction.
+template <int FMT>
+__device__ __forceinline__ uint32_t fp8_lo_pair(uint32_t w) {
+  if constexpr (FMT == 1)
+    return __byte_perm(w, 0u, 0x1404u);
+  else
+    return fp8x2_to_f16x2<FMT>(static_cast<uint16_t>(w & 0xFFFFu));
+}
+template <int FMT>
+__device__ __forceinline__ uint32_t fp8_hi_pair(uint32_t w) {
+  if constexpr (FMT == 1)
+    return __byte_perm(w, 0u, 0x3424u);
+  else
+    return fp8x2_to_f16x2<FMT>(static_cast<uint16_t>(w >> 16));
+}
+
 // d += A (16 x 32 E4M3, rows g / g + 8) * B (32 x 8, E4M3 or E5M2 per FMT), f32.
 template <int FMT>
 __device__ __forceinline__ void mma_fp8_16832(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -455,8 +474,7 @@ __global__ void __launch_bounds__(128) fp8_decode_kernel(Fp8DecodeArgs a) {
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
           const uint32_t w = kw[nt * KS + ks];
-          mma16816(sacc[nt], qa[ks][0], 0u, qa[ks][1], 0u, fp8x2_to_f16x2<FMT>(static_cast<uint16_t>(w & 0xFFFFu)),
-                   fp8x2_to_f16x2<FMT>(static_cast<uint16_t>(w >> 16)));
+          mma16816(sacc[nt], qa[ks][0], 0u, qa[ks][1], 0u, fp8_lo_pair<FMT>(w), fp8_hi_pair<FMT>(w));
         }
       }
     }
@@ -504,8 +522,7 @@ __global__ void __launch_bounds__(128) fp8_decode_kernel(Fp8DecodeArgs a) {
     }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
-      mma16816(o_acc[nt], A0, A1, A2, A3, fp8x2_to_f16x2<FMT>(static_cast<uint16_t>(vw[nt] & 0xFFFFu)),
-               fp8x2_to_f16x2<FMT>(static_cast<uint16_t>(vw[nt] >> 16)));
+      mma16816(o_acc[nt], A0, A1, A2, A3, fp8_lo_pair<FMT>(vw[nt]), fp8_hi_pair<FMT>(vw[nt]));
 
     __syncwarp();
     if (lane == 0 && j + STAGES < n_mine) {
