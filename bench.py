@@ -481,7 +481,7 @@ def run_table(args):
     names = args.table.split(",") if args.table != "all" else [
         workloads.MHA_4K.name, workloads.GQA_8K_2BIT.name, workloads.GQA_8K_4BIT.name, workloads.STREAM_128K.name,
         workloads.FP8_32K.name, workloads.FP8_32K_E5M2_PH.name, workloads.FP8_32K_QFP8.name, workloads.PAGED_GQA_8K.name,
-        workloads.PAGED_VAR_16K.name]
+        workloads.PAGED_VAR_16K.name, workloads.PAGED_GQA4_VAR_16K.name]
     for name in names:
         w = workloads.WORKLOADS[name]
         if isinstance(w, workloads.PagedKiviWorkload):

@@ -734,8 +734,10 @@ kvq_status kv_paged_decode_attention(const kivi_paged_cache* cache, const uint16
     max_u = std::max(max_u, U);
   }
   seqs.unit0[cf.batch] = static_cast<int>(total);
-  const long long slots = static_cast<long long>(kvq::device_sm_count()) *
-                          std::max(1, kvq::kivi_paged_decode_blocks_per_sm(cf.head_dim, cf.k_bits, cf.v_bits));
+  const int per_sm = use_swapped_decode(cf)
+                         ? kvq::kivi_paged_decode_tr_blocks_per_sm(cf.head_dim, cf.k_bits, cf.v_bits)
+                         : kvq::kivi_paged_decode_blocks_per_sm(cf.head_dim, cf.k_bits, cf.v_bits);
+  const long long slots = static_cast<long long>(kvq::device_sm_count()) * std::max(1, per_sm);
   long long per = (total + slots - 1) / slots;
   per = std::max<long long>(per, kMinUnitsPerSplit);
   per = std::max<long long>(per, ceil_div(max_u, kMaxSplits - 1));
@@ -752,7 +754,9 @@ kvq_status kv_paged_decode_attention(const kivi_paged_cache* cache, const uint16
   view.groups_cap = cache->groups_cap;
   view.res_cap = cache->res_cap;
   const kvq::KiviDecodeArgs a = kivi_decode_args(&view, plan, q, out, out_fp32, scale, static_cast<uint8_t*>(ws));
-  return from_cuda(kvq::launch_kivi_decode_paged(a, seqs, static_cast<cudaStream_t>(stream)));
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return from_cuda(use_swapped_decode(cf) ? kvq::launch_kivi_decode_tr_paged(a, seqs, s)
+                                          : kvq::launch_kivi_decode_paged(a, seqs, s));
 }
 
 size_t fp8_quantize_workspace_bytes(int32_t batch, int32_t kv_heads, int32_t seq_len, int32_t head_dim) {

@@ -15,6 +15,7 @@
 // (CSDN), section 2, with grouped-query sharing (section 5).
 #include <cfloat>
 #include <cmath>
+#include <type_traits>
 
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
@@ -45,6 +46,31 @@ constexpr float kTrInvP6 = 262144.0f;
 constexpr float kTrInvP8 = 65536.0f;
 
 constexpr int kTrStages = 4;
+
+// Sequence state of the contiguous cache (every pair alike); the paged cache
+// passes PagedSeqs.
+struct TrNoSeqs {};
+
+// Block-table entries a warp of the paged decode keeps in its lanes.
+template <bool kPaged>
+struct TrTableLanes {
+  int tbase = 0, tblk = 0;
+};
+template <>
+struct TrTableLanes<false> {};
+
+// The sequence owning unit x: the b < n with begin[b] <= x < begin[b + 1].
+__device__ __forceinline__ int tr_seq_of(const int* begin, int n, long long x) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (begin[mid] <= x)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  return lo;
+}
 
 template <int D, int KB, int VB>
 struct TrSmem {
@@ -207,9 +233,10 @@ __device__ __noinline__ bool tr_window_chunks(const uint16_t* k_res, const uint1
   return ok;
 }
 
-template <int D, int KB, int VB>
-__global__ void __launch_bounds__(128, 4) kivi_decode_tr_kernel(KiviDecodeArgs a) {
+template <int D, int KB, int VB, class SeqT>
+__global__ void __launch_bounds__(128, 4) kivi_decode_tr_kernel(KiviDecodeArgs a, SeqT seqs) {
   using P = KiviTr<D, KB, VB>;
+  constexpr bool kPaged = !std::is_same<SeqT, TrNoSeqs>::value;
   using S = TrSmem<D, KB, VB>;
   constexpr int MT = P::MTV;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -237,20 +264,42 @@ __global__ void __launch_bounds__(128, 4) kivi_decode_tr_kernel(KiviDecodeArgs a
   }
   __syncwarp();
 
-  const long long all_units = static_cast<long long>(a.n_pairs) * a.pair_stride;
+  long long all_units = static_cast<long long>(a.n_pairs) * a.pair_stride;
+  if constexpr (kPaged) all_units = seqs.unit0[seqs.n_seqs];
   const long long u0 = static_cast<long long>(blockIdx.x) * a.units_per_block;
   const long long u1 = min(all_units, u0 + a.units_per_block);
   int jg = 0;
   uint32_t wphase = 0;
   bool timed_out = false;
   for (long long u = u0; u < u1;) {
-    const int pair = static_cast<int>(u / a.pair_stride);
-    const long long pbase = static_cast<long long>(pair) * a.pair_stride;
-    const int upp = a.units_per_pair, n_grp = a.n_groups, n_res = a.n_resid;
-    u = pbase + a.pair_stride;
+    int pair, upp, n_grp, n_res;
+    long long pbase;
+    if constexpr (kPaged) {
+      // pair (b, h) spans pair_lead units of no work, then its groups and chunks
+      const int sb = tr_seq_of(seqs.unit0, seqs.n_seqs, u);
+      n_grp = seqs.n_groups[sb];
+      n_res = seqs.n_resid[sb];
+      upp = n_grp + kChunkUnits * ((n_res + kGroup - 1) / kGroup);
+      const int span = upp + seqs.pair_lead;
+      const int hh = static_cast<int>((u - seqs.unit0[sb]) / span);
+      pair = sb * a.kv_heads + hh;
+      const long long vbase = seqs.unit0[sb] + static_cast<long long>(hh) * span;
+      pbase = vbase + seqs.pair_lead;
+      u = vbase + span;
+    } else {
+      pair = static_cast<int>(u / a.pair_stride);
+      pbase = static_cast<long long>(pair) * a.pair_stride;
+      upp = a.units_per_pair;
+      n_grp = a.n_groups;
+      n_res = a.n_resid;
+      u = pbase + a.pair_stride;
+    }
     const int lo = static_cast<int>(u0 > pbase ? u0 - pbase : 0LL);
     const int hi = static_cast<int>(min(static_cast<long long>(upp), u1 - pbase));
     if (lo >= upp) continue;  // padding after the pair's units (the same for the whole block)
+    if constexpr (kPaged) {
+      if (hi <= 0) continue;  // the slice ends inside the pair's lead-in: no work here
+    }
     const int b = pair / a.kv_heads, h = pair % a.kv_heads;
     const long long bh = pair;
     const int first_block = static_cast<int>(pbase / a.units_per_block);
@@ -277,31 +326,84 @@ __global__ void __launch_bounds__(128, 4) kivi_decode_tr_kernel(KiviDecodeArgs a
       n_mine = GPS * (np - 1) + min(GPS, n_here - GPS * (warp + 4 * (np - 1)));
     }
     const int n_slots = (n_mine + GPS - 1) / GPS;
+    // contiguous: the pair's records, groups one after the other
     const long long rec0 = bh * a.groups_cap;
     const uint8_t* kc_g = a.k_codes + rec0 * P::KC;
     const uint8_t* km_g = a.k_meta + rec0 * P::KM;
     const uint8_t* vc_g = a.v_codes + rec0 * P::VC;
     const uint8_t* vm_g = a.v_meta + rec0 * P::VM;
+    // paged: group j's pool blocks from the block table through the lanes (lane l
+    // holds the entry of the warp's group tbase + l, clamped into the pool)
+    TrTableLanes<kPaged> tl;
+    auto load_table = [&](int base) {  // warp-wide
+      if constexpr (kPaged) {
+        tl.tbase = base;
+        const int jl = base + lane;
+        if (jl < n_mine) {
+          const int grp = g_begin + GPS * (warp + 4 * (jl / GPS)) + jl % GPS;
+          tl.tblk = min(max(__ldg(seqs.pools.block_table + static_cast<long long>(b) * a.groups_cap + grp), 0),
+                        seqs.pools.num_blocks - 1);
+        }
+      }
+    };
+    auto slot_blocks = [&](int k, int& b0, int& b1) {  // warp-wide
+      if constexpr (kPaged) {
+        if (GPS * k + GPS > tl.tbase + 32) load_table(GPS * k);
+        b0 = __shfl_sync(0xffffffffu, tl.tblk, GPS * k - tl.tbase);
+        b1 = __shfl_sync(0xffffffffu, tl.tblk, GPS * k + 1 - tl.tbase);
+      }
+    };
     // slot k (groups g_begin + GPS * (warp + 4k) + {0, 1}) through ring position (jg + k) % NS
-    auto issue = [&](int k) {
+    auto issue = [&](int k, int b0 = 0, int b1 = 0) {
       const int grp = g_begin + GPS * (warp + 4 * k);
       const uint32_t cnt = static_cast<uint32_t>(min(GPS, g_end - grp));
       uint8_t* dst = ring + ((jg + k) % NS) * SLOT;
       uint64_t* bb = &bar[(jg + k) % NS];
       mbar_arrive_expect_tx(bb, cnt * P::STAGE);
-      bulk_g2s(dst, kc_g + grp * static_cast<long long>(P::KC), cnt * P::KC, bb);
-      bulk_g2s(dst + GPS * P::KC, km_g + grp * static_cast<long long>(P::KM), cnt * P::KM, bb);
-      bulk_g2s(dst + GPS * (P::KC + P::KM), vc_g + grp * static_cast<long long>(P::VC), cnt * P::VC, bb);
-      bulk_g2s(dst + GPS * (P::KC + P::KM + P::VC), vm_g + grp * static_cast<long long>(P::VM), cnt * P::VM, bb);
+      if constexpr (kPaged) {
+        // one copy per group: kv head h's entry of its pool block (the pool is a.k_codes)
+        static_assert(GPS == 2, "two blocks per slot");
+        const uint8_t* pool_h = a.k_codes + static_cast<long long>(h) * P::STAGE;
+        bulk_g2s(dst, pool_h + static_cast<long long>(b0) * a.kv_heads * P::STAGE, P::STAGE, bb);
+        if (cnt > 1) bulk_g2s(dst + P::STAGE, pool_h + static_cast<long long>(b1) * a.kv_heads * P::STAGE, P::STAGE, bb);
+      } else {
+        bulk_g2s(dst, kc_g + grp * static_cast<long long>(P::KC), cnt * P::KC, bb);
+        bulk_g2s(dst + GPS * P::KC, km_g + grp * static_cast<long long>(P::KM), cnt * P::KM, bb);
+        bulk_g2s(dst + GPS * (P::KC + P::KM), vc_g + grp * static_cast<long long>(P::VC), cnt * P::VC, bb);
+        bulk_g2s(dst + GPS * (P::KC + P::KM + P::VC), vm_g + grp * static_cast<long long>(P::VM), cnt * P::VM, bb);
+      }
     };
     auto wait_slot = [&](int k) { return mbar_wait_bounded(&bar[(jg + k) % NS], ((jg + k) / NS) & 1); };
+    // the records of group j of the warp (paged: each group's four records back
+    // to back; contiguous: the GPS groups' records of one kind together)
     auto slot_base = [&](int j) { return ring + ((jg + j / GPS) % NS) * SLOT; };
-    auto kc_of = [&](int j) { return slot_base(j) + (j % GPS) * P::KC; };
-    auto km_of = [&](int j) { return slot_base(j) + GPS * P::KC + (j % GPS) * P::KM; };
-    auto vc_of = [&](int j) { return slot_base(j) + GPS * (P::KC + P::KM) + (j % GPS) * P::VC; };
-    auto vm_of = [&](int j) { return slot_base(j) + GPS * (P::KC + P::KM + P::VC) + (j % GPS) * P::VM; };
-    if (lane == 0) {
-      for (int k = 0; k < NS && k < n_slots; ++k) issue(k);
+    auto kc_of = [&](int j) {
+      if constexpr (kPaged) return slot_base(j) + (j % GPS) * P::STAGE;
+      else return slot_base(j) + (j % GPS) * P::KC;
+    };
+    auto km_of = [&](int j) {
+      if constexpr (kPaged) return slot_base(j) + (j % GPS) * P::STAGE + P::KC;
+      else return slot_base(j) + GPS * P::KC + (j % GPS) * P::KM;
+    };
+    auto vc_of = [&](int j) {
+      if constexpr (kPaged) return slot_base(j) + (j % GPS) * P::STAGE + P::KC + P::KM;
+      else return slot_base(j) + GPS * (P::KC + P::KM) + (j % GPS) * P::VC;
+    };
+    auto vm_of = [&](int j) {
+      if constexpr (kPaged) return slot_base(j) + (j % GPS) * P::STAGE + P::KC + P::KM + P::VC;
+      else return slot_base(j) + GPS * (P::KC + P::KM + P::VC) + (j % GPS) * P::VM;
+    };
+    if constexpr (kPaged) {
+      if (n_mine > 0) load_table(0);
+      for (int k = 0; k < NS && k < n_slots; ++k) {
+        int b0 = 0, b1 = 0;
+        slot_blocks(k, b0, b1);
+        if (lane == 0) issue(k, b0, b1);
+      }
+    } else {
+      if (lane == 0) {
+        for (int k = 0; k < NS && k < n_slots; ++k) issue(k);
+      }
     }
 
     // The query of column g (head jq), channels 16ks + 2tig, +1 and 16ks + 8 + 2tig, +1,
@@ -455,9 +557,21 @@ __global__ void __launch_bounds__(128, 4) kivi_decode_tr_kernel(KiviDecodeArgs a
 
       if (j % GPS == GPS - 1 || j + 1 == n_mine) {
         __syncwarp();
-        if (lane == 0 && j / GPS + NS < n_slots) {
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          issue(j / GPS + NS);
+        if constexpr (kPaged) {
+          const int kn = j / GPS + NS;
+          if (kn < n_slots) {
+            int b0 = 0, b1 = 0;
+            slot_blocks(kn, b0, b1);
+            if (lane == 0) {
+              asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+              issue(kn, b0, b1);
+            }
+          }
+        } else {
+          if (lane == 0 && j / GPS + NS < n_slots) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            issue(j / GPS + NS);
+          }
         }
       }
     }
@@ -528,14 +642,14 @@ __global__ void __launch_bounds__(128, 4) kivi_decode_tr_kernel(KiviDecodeArgs a
   }
 }
 
-template <int D, int KB, int VB>
+template <int D, int KB, int VB, class SeqT>
 int tr_occupancy() {
   static int cached[64] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
   if (cached[dev] == 0) {
     constexpr int smem = TrSmem<D, KB, VB>::BYTES;
-    auto kern = kivi_decode_tr_kernel<D, KB, VB>;
+    auto kern = kivi_decode_tr_kernel<D, KB, VB, SeqT>;
     int n = 0;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, 128, smem) != cudaSuccess || n <= 0)
@@ -548,10 +662,10 @@ int tr_occupancy() {
 // Launched as a programmatic dependent of the kernel before it, as the decode
 // of kivi_kernels.cu is: the grouped loop reads only group records and q, the
 // fp16 window and the workspace are touched after griddepcontrol.wait.
-template <int D, int KB, int VB>
-cudaError_t tr_dispatch(const KiviDecodeArgs& a, cudaStream_t s) {
+template <int D, int KB, int VB, class SeqT>
+cudaError_t tr_dispatch(const KiviDecodeArgs& a, const SeqT& seqs, cudaStream_t s) {
   constexpr int smem = TrSmem<D, KB, VB>::BYTES;
-  auto kern = kivi_decode_tr_kernel<D, KB, VB>;
+  auto kern = kivi_decode_tr_kernel<D, KB, VB, SeqT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -564,37 +678,53 @@ cudaError_t tr_dispatch(const KiviDecodeArgs& a, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, a);
+  return cudaLaunchKernelEx(&cfg, kern, a, seqs);
 }
 
-}  // namespace
-
-cudaError_t launch_kivi_decode_tr(const KiviDecodeArgs& a, cudaStream_t s) {
+template <class SeqT>
+cudaError_t tr_by_key(const KiviDecodeArgs& a, const SeqT& seqs, cudaStream_t s) {
   switch (a.head_dim * 100 + a.k_bits * 10 + a.v_bits) {
-    case 6422: return tr_dispatch<64, 2, 2>(a, s);
-    case 6424: return tr_dispatch<64, 2, 4>(a, s);
-    case 6442: return tr_dispatch<64, 4, 2>(a, s);
-    case 6444: return tr_dispatch<64, 4, 4>(a, s);
-    case 12822: return tr_dispatch<128, 2, 2>(a, s);
-    case 12824: return tr_dispatch<128, 2, 4>(a, s);
-    case 12842: return tr_dispatch<128, 4, 2>(a, s);
-    case 12844: return tr_dispatch<128, 4, 4>(a, s);
+    case 6422: return tr_dispatch<64, 2, 2>(a, seqs, s);
+    case 6424: return tr_dispatch<64, 2, 4>(a, seqs, s);
+    case 6442: return tr_dispatch<64, 4, 2>(a, seqs, s);
+    case 6444: return tr_dispatch<64, 4, 4>(a, seqs, s);
+    case 12822: return tr_dispatch<128, 2, 2>(a, seqs, s);
+    case 12824: return tr_dispatch<128, 2, 4>(a, seqs, s);
+    case 12842: return tr_dispatch<128, 4, 2>(a, seqs, s);
+    case 12844: return tr_dispatch<128, 4, 4>(a, seqs, s);
     default: return cudaErrorInvalidValue;
   }
 }
 
-int kivi_decode_tr_blocks_per_sm(int head_dim, int k_bits, int v_bits) {
+template <class SeqT>
+int tr_occupancy_by_key(int head_dim, int k_bits, int v_bits) {
   switch (head_dim * 100 + k_bits * 10 + v_bits) {
-    case 6422: return tr_occupancy<64, 2, 2>();
-    case 6424: return tr_occupancy<64, 2, 4>();
-    case 6442: return tr_occupancy<64, 4, 2>();
-    case 6444: return tr_occupancy<64, 4, 4>();
-    case 12822: return tr_occupancy<128, 2, 2>();
-    case 12824: return tr_occupancy<128, 2, 4>();
-    case 12842: return tr_occupancy<128, 4, 2>();
-    case 12844: return tr_occupancy<128, 4, 4>();
+    case 6422: return tr_occupancy<64, 2, 2, SeqT>();
+    case 6424: return tr_occupancy<64, 2, 4, SeqT>();
+    case 6442: return tr_occupancy<64, 4, 2, SeqT>();
+    case 6444: return tr_occupancy<64, 4, 4, SeqT>();
+    case 12822: return tr_occupancy<128, 2, 2, SeqT>();
+    case 12824: return tr_occupancy<128, 2, 4, SeqT>();
+    case 12842: return tr_occupancy<128, 4, 2, SeqT>();
+    case 12844: return tr_occupancy<128, 4, 4, SeqT>();
     default: return 1;
   }
+}
+
+}  // namespace
+
+cudaError_t launch_kivi_decode_tr(const KiviDecodeArgs& a, cudaStream_t s) { return tr_by_key(a, TrNoSeqs{}, s); }
+
+cudaError_t launch_kivi_decode_tr_paged(const KiviDecodeArgs& a, const PagedSeqs& seqs, cudaStream_t s) {
+  return tr_by_key(a, seqs, s);
+}
+
+int kivi_decode_tr_blocks_per_sm(int head_dim, int k_bits, int v_bits) {
+  return tr_occupancy_by_key<TrNoSeqs>(head_dim, k_bits, v_bits);
+}
+
+int kivi_paged_decode_tr_blocks_per_sm(int head_dim, int k_bits, int v_bits) {
+  return tr_occupancy_by_key<PagedSeqs>(head_dim, k_bits, v_bits);
 }
 
 }  // namespace kvq

@@ -136,6 +136,8 @@ struct PagedSeqs {
   int n_resid[kMaxPagedSeqs];
 };
 cudaError_t launch_kivi_decode_paged(const KiviDecodeArgs& a, const PagedSeqs& seqs, cudaStream_t s);
+// The swapped-operand decode over a paged cache (H_q / H_kv <= kMaxGqaSwapped).
+cudaError_t launch_kivi_decode_tr_paged(const KiviDecodeArgs& a, const PagedSeqs& seqs, cudaStream_t s);
 
 
 struct Fp8QuantArgs {
@@ -199,6 +201,7 @@ int device_sm_count();
 int kivi_decode_blocks_per_sm(int head_dim, int k_bits, int v_bits);
 int kivi_paged_decode_blocks_per_sm(int head_dim, int k_bits, int v_bits);
 int kivi_decode_tr_blocks_per_sm(int head_dim, int k_bits, int v_bits);
+int kivi_paged_decode_tr_blocks_per_sm(int head_dim, int k_bits, int v_bits);
 int fp8_decode_blocks_per_sm(int head_dim);
 
 }  // namespace kvq

@@ -120,9 +120,11 @@ STREAM_128K = KiviWorkload("kivi2_stream_b4_h8x64_d128_s131072_512steps", 4, 8, 
 # 512 .. 16384 (the balance of the split across pairs of unequal length).
 PAGED_GQA_8K = PagedKiviWorkload("kivi2_paged_b32_h8x64_d128_len8192", 32, 8, 64, 128, 8192, 8192, seed=5)
 PAGED_VAR_16K = PagedKiviWorkload("kivi2_paged_b32_h8x64_d128_len512-16384", 32, 8, 64, 128, 512, 16384, seed=6)
+# the same lengths with four query heads per kv head (Llama-3-8B / Mistral-7B-like heads)
+PAGED_GQA4_VAR_16K = PagedKiviWorkload("kivi2_paged_b32_h8x32_d128_len512-16384", 32, 8, 32, 128, 512, 16384, seed=6)
 
 WORKLOADS = {w.name: w for w in (TINY, MHA_4K, GQA_8K_2BIT, GQA_8K_4BIT, FP8_32K, FP8_32K_E5M2_PH, FP8_32K_QFP8,
-                                  FP8_32K_B8, STREAM_128K, PAGED_GQA_8K, PAGED_VAR_16K)}
+                                  FP8_32K_B8, STREAM_128K, PAGED_GQA_8K, PAGED_VAR_16K, PAGED_GQA4_VAR_16K)}
 
 
 def _channel_scales(rng: np.random.Generator, kv_heads: int, head_dim: int) -> np.ndarray:
