@@ -208,8 +208,8 @@ KVQ_API kvq_status kv_decode_attention_noalloc(const kivi_cache* cache, const ui
 
 /* A batch of sequences of different lengths. Each sequence is a KIVI cache of
  * its own (the rules above: prefill split, window, flush timing, all on the
- * sequence's own length); its groups of 32 tokens live in blocks of shared
- * pools, reached through a block table as in [CSDN] section 13. The pages
+ * sequence's own length); its groups of 32 tokens live in blocks of one shared
+ * pool, reached through a block table as in [CSDN] section 13. The pages
  * combine the two ideas without fixing a layout; this one is the library's:
  * one pool block holds one group of one sequence for every kv head, and for
  * each kv head the four records of the contiguous cache (same byte layout per
@@ -295,7 +295,8 @@ KVQ_API size_t kv_paged_decode_workspace_bytes(const kivi_paged_config* cfg);
  * (sequence, kv head) pairs is cut into equal slices of one launch whatever
  * the lengths (split-K across pairs, one partial per pair a slice touches,
  * log-sum-exp merge by the last slice of each pair). KVQ_ERR_ARG if some
- * sequence is empty. */
+ * sequence is empty; KVQ_ERR_UNSUPPORTED if the work of all pairs exceeds
+ * 2^31 units (one unit per group, about 6 per 32 window tokens). */
 KVQ_API kvq_status kv_paged_decode_attention(const kivi_paged_cache* cache, const uint16_t* q, void* out,
                                              int32_t out_fp32, float softmax_scale, void* ws,
                                              size_t ws_bytes, void* stream);
