@@ -7,7 +7,9 @@
 // and the query heads x {hi, lo} the 8 columns, so the same packed codes serve
 // as A operands (the extracted registers of one code word are exactly the A
 // fragments of two 16-token or two 16-channel tiles) and every group takes 32
-// MMAs instead of 64, with half the accumulators.
+// MMAs instead of 64, with half the accumulators. It serves both the contiguous
+// cache and the paged one (per-sequence units, groups fetched from the pool
+// block of the block table), as the first kernel does.
 //
 // Method: "4.4 KV Cache 量化：KIVI 2-bit 与 FP8 KV Cache" (aiinfraguide), section 3
 // (keys per channel, values per token, groups of 32 tokens, fp16 window);
