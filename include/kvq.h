@@ -107,28 +107,21 @@ typedef struct {
  * Value meta (128 bytes): 4 records of fp16 scales, then 4 of zero points;
  *   record tig holds tokens {2tig, 2tig+1, 8+2tig, 9+2tig, 16+2tig, 17+2tig,
  *   24+2tig, 25+2tig}.
- * Key codes (32*D*b/8 bytes): 32 lanes x W 32-bit words (W = D/16 at 2 bits,
- *   D/8 at 4 bits); lane = 4*g + tig. Each word holds a pair of channels in
- *   its 16-bit halves (low half: first channel): channels d0 = 16*ks + 8*r +
- *   2*tig and d0+1 of token 8*nt + g (nt < 4, ks < D/16), in
- *     2 bits: word u = ks, field f = (4*r + nt + 1) mod 8 at bits [2f, 2f+2);
- *     4 bits: word u = 2*ks + r, field f = nt at bits [4f, 4f+4).
+ * Codes (32*D*b/8 bytes each for keys and values): 32 lanes x W 32-bit words
+ *   (W = D/16 at 2 bits, D/8 at 4 bits); lane = 4*g + tig. Each word holds a
+ *   pair of elements in its 16-bit halves (low half: first element):
+ *     keys  : channels d0 = 16*ks + 8*r + 2*tig and d0+1 of token 8*nt + g
+ *             (nt < 4, ks < D/16);
+ *     values: tokens t0 = 16*ks + 8*r + 2*tig and t0+1 of channel 8*nt + g
+ *             (nt < D/8, ks < 2).
+ *   With NQ = 1 (keys) or D/32 (values):
+ *     2 bits: word u = ks*NQ + nt/4, field f = (4*r + nt%4 + 1) mod 8 at bits [2f, 2f+2);
+ *     4 bits: word u = (2*ks + r)*NQ + nt/4, field f = nt%4 at bits [4f, 4f+4).
  *   Word u of a lane is stored at 32-bit index (u/4)*128 + lane*4 + u%4.
  *   (These are the operand fragments of the mma.sync m16n8k16 tensor-core
- *   instruction that computes q . k^T: the decode loads each lane's codes with
+ *   instruction, so that the decode kernel loads each lane's codes with
  *   16-byte shared-memory loads and turns them into operands with shifts and
- *   masks only.)
- * Value codes (32*D*b/8 bytes), channel-major: channel d owns the b words
- *   d*b .. d*b + b - 1; field f of word i, at bits [b*f, b*f + b) of both
- *   halves, holds a pair of consecutive tokens (low half: the first):
- *     4 bits: tokens 8*i + 2*f and +1;
- *     2 bits: tokens 16*k + 8*i + 2*j and +1 with k = 0 for odd f, 1 for even
- *             f, and j = 3, 1, 1, 0, 0, 2, 2, 3 for f = 0 .. 7.
- *   (One lane of the decode reads its channel's b words and writes the codes
- *   into tensor memory as the A operand of p . V on tcgen05.mma, one token
- *   pair per 32-bit column: the word itself, its shifts by 4 either way and
- *   its per-half byte swap expose the first 16 tokens at bits 6-7 and the
- *   last 16 at bits 8-9, pairs in order.)                                   */
+ *   masks only.)                                                            */
 
 /* Byte sizes of the six buffers in the order k_codes, k_meta, v_codes,
  * v_meta, k_res, v_res. */
@@ -179,9 +172,7 @@ KVQ_API size_t kv_decode_workspace_bytes(const kivi_config* cfg);
  * Split-K ("flash-decoding"), one kernel launch: token chunks of each
  * (b, kv head) go to separate thread blocks, each writes (m, l, o) partials,
  * and the last block of that (b, kv head) to finish merges them with a
- * log-sum-exp reduction. The codes enter the tensor cores as exact fp16
- * operands (q . k^T on mma.sync, p . V on tcgen05.mma with the accumulators
- * in tensor memory); no dequantized copy of the cache is ever written.
+ * log-sum-exp reduction. Dequantization happens in registers.
  * KVQ_ERR_ARG if the cache is empty. */
 KVQ_API kvq_status kv_decode_attention(const kivi_cache* cache, const uint16_t* q, void* out,
                                int32_t out_fp32, float softmax_scale, void* ws,

@@ -11,34 +11,30 @@ Per (batch, kv head, group of 32 tokens) there are four records:
 * key meta    : (D/16) x 4 records of 16 bytes:
                 {s[d0], s[d0+1], s[d0+8], s[d0+9], z[d0], z[d0+1], z[d0+8], z[d0+9]}
                 (fp16) with d0 = 16*ks + 2*tig, record index ks*4 + tig
-* value codes : D channels x b words (b = the bit width), u32, channel-major
+* value codes : 32 lanes x W words, u32
 * value meta  : 4 x 16 bytes of scales then 4 x 16 bytes of zeros; record tig
                 holds tokens {2tig, 2tig+1, 8+2tig, 9+2tig, 16+2tig, 17+2tig,
                 24+2tig, 25+2tig}
 
-Key code words. A lane is ``lane = 4*g + tig`` (g in 0..7, tig in 0..3). Each
-32-bit word carries codes for one pair of channels in its two 16-bit halves
-(low half: first channel of the pair, high half: second). For a pair
-``(ks, r, nt)`` the channels are ``d0 = 16*ks + 8*r + 2*tig`` and ``d0+1`` of
-token ``8*nt + g`` (nt in 0..3, ks in 0..D/16-1):
+Code words. A lane is ``lane = 4*g + tig`` (g in 0..7, tig in 0..3). Each
+32-bit word carries codes for one pair of elements in its two 16-bit halves
+(low half: first element of the pair, high half: second element). For a
+pair ``(ks, r, nt)``:
 
-* 2 bits: word ``u = ks``, field ``f = (4*r + nt + 1) mod 8`` at bits
-  ``[2f, 2f+2)`` of each half (the order in which the unshifted word, its
-  shifts by 4 either way and its per-half byte swap expose the fields);
-* 4 bits: word ``u = 2*ks + r``, field ``f = nt`` at bits ``[4f, 4f+4)``.
+* keys   : elements are channels ``d0 = 16*ks + 8*r + 2*tig`` and ``d0+1`` of
+           token ``8*nt + g`` (nt in 0..3, ks in 0..D/16-1);
+* values : elements are tokens ``t0 = 16*ks + 8*r + 2*tig`` and ``t0+1`` of
+           channel ``8*nt + g`` (nt in 0..D/8-1, ks in 0..1).
+
+With ``NQ`` = 1 for keys and D/32 for values:
+
+* 2 bits: word ``u = ks*NQ + nt//4``, field ``f = (4*r + nt%4 + 1) mod 8`` at
+  bits ``[2f, 2f+2)`` of each half (the order in which the unshifted word,
+  its shifts by 4 either way and its per-half byte swap expose the fields);
+* 4 bits: word ``u = (2*ks + r)*NQ + nt//4``, field ``f = nt%4`` at bits
+  ``[4f, 4f+4)`` of each half.
 
 Word ``u`` of lane ``lane`` is stored at u32 index ``(u//4)*128 + lane*4 + u%4``.
-
-Value code words. Channel ``d`` owns words ``d*b .. d*b + b - 1``; field ``f``
-of word ``i`` sits at bits ``[b*f, b*f + b)`` of both halves and holds a pair of
-consecutive tokens, the first in the low half:
-
-* 4 bits: tokens ``8*i + 2*f`` and ``+1``;
-* 2 bits: tokens ``16*k(f) + 8*i + 2*j(f)`` and ``+1`` with ``k(f) = 0`` for
-  odd f, 1 for even f, and ``j(f) = (3, 1, 1, 0, 0, 2, 2, 3)[f]`` (the decode
-  exposes a word's fields at bits 6-7 and 8-9 with the word itself, its shifts
-  by 4 either way and its per-half byte swap: the first 16 tokens come out at
-  bits 6-7, the last 16 at bits 8-9, pairs in order).
 """
 from __future__ import annotations
 
@@ -81,25 +77,25 @@ def pack_key_codes(codes: np.ndarray, bits: int) -> np.ndarray:
     return words.view(np.uint8).reshape(*lead, -1)
 
 
-def value_pair_token(bits: int, i: int, f: int) -> int:
-    """First token of the pair held by field f of value word i (the other is +1)."""
-    if bits == 4:
-        return 8 * i + 2 * f
-    k = 0 if f % 2 == 1 else 1
-    j = (3, 1, 1, 0, 0, 2, 2, 3)[f]
-    return 16 * k + 8 * i + 2 * j
-
-
 def pack_value_codes(codes: np.ndarray, bits: int) -> np.ndarray:
-    """codes uint8 ``[..., 32, D]`` (token, channel) -> uint8 ``[..., D*bits*4]`` (channel-major)."""
+    """codes uint8 ``[..., 32, D]`` (token, channel) -> uint8 ``[..., 32*W*4]``."""
     *lead, t, d = codes.shape
     assert t == GROUP
-    words = np.zeros((*lead, d, bits), np.uint32)
-    for i in range(bits):
-        for f in range(16 // bits):
-            t0 = value_pair_token(bits, i, f)
-            words[..., :, i] |= (codes[..., t0, :].astype(np.uint32) << (bits * f)) | (
-                codes[..., t0 + 1, :].astype(np.uint32) << (16 + bits * f))
+    w = code_words_per_lane(d, bits)
+    nq = d // 32
+    words = np.zeros((*lead, 32 * w), np.uint32)
+    for lane in range(32):
+        g, tig = lane // 4, lane % 4
+        for ks in range(2):
+            for r in range(2):
+                t0 = 16 * ks + 8 * r + 2 * tig
+                for nt in range(d // 8):
+                    ch = 8 * nt + g
+                    if bits == 2:
+                        u, f = ks * nq + nt // 4, (4 * r + nt % 4 + 1) % 8
+                    else:
+                        u, f = (2 * ks + r) * nq + nt // 4, nt % 4
+                    _place(words, lane, u, f, bits, codes[..., t0, ch], codes[..., t0 + 1, ch])
     return words.view(np.uint8).reshape(*lead, -1)
 
 

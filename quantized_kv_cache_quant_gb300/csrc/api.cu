@@ -177,6 +177,14 @@ constexpr int kSegmentUnits = 8;
 // equal lengths).
 constexpr int kPairLeadUnits = 8;
 
+// The decode kernel of a contiguous cache: the swapped-operand one when a kv
+// head serves at most kMaxGqaSwapped query heads (half the MMAs per group).
+bool use_swapped_decode(const kivi_config& cf) { return cf.q_heads / cf.kv_heads <= kvq::kMaxGqaSwapped; }
+
+cudaError_t launch_contiguous_decode(const kivi_config& cf, const kvq::KiviDecodeArgs& a, cudaStream_t s) {
+  return use_swapped_decode(cf) ? kvq::launch_kivi_decode_tr(a, s) : kvq::launch_kivi_decode(a, s);
+}
+
 DecodePlan plan_kivi_decode(const kivi_cache* cache) {
   const kivi_config& cf = cache->cfg;
   DecodePlan p{};
@@ -184,7 +192,8 @@ DecodePlan plan_kivi_decode(const kivi_cache* cache) {
   const int U = p.n_groups + kvq::kChunkUnits * ceil_div(cache->n_resid, kGroup);
   p.units_per_pair = U;
   const long long pairs = static_cast<long long>(cf.batch) * cf.kv_heads;
-  const int per_sm = kvq::kivi_decode_blocks_per_sm(cf.head_dim, cf.k_bits, cf.v_bits);
+  const int per_sm = use_swapped_decode(cf) ? kvq::kivi_decode_tr_blocks_per_sm(cf.head_dim, cf.k_bits, cf.v_bits)
+                                            : kvq::kivi_decode_blocks_per_sm(cf.head_dim, cf.k_bits, cf.v_bits);
   const long long slots = static_cast<long long>(kvq::device_sm_count()) * std::max(1, per_sm);
   // stream-K slices
   long long per_s = (pairs * U + slots - 1) / slots;
@@ -552,7 +561,7 @@ kvq_status kv_decode_attention(const kivi_cache* cache, const uint16_t* q, void*
 
   const DecodePlan plan = plan_kivi_decode(cache);
   const kvq::KiviDecodeArgs a = kivi_decode_args(cache, plan, q, out, out_fp32, scale, static_cast<uint8_t*>(ws));
-  return from_cuda(kvq::launch_kivi_decode(a, static_cast<cudaStream_t>(stream)));
+  return from_cuda(launch_contiguous_decode(cf, a, static_cast<cudaStream_t>(stream)));
 }
 
 kvq_status kivi_paged_cache_sizes(const kivi_paged_config* cfg, size_t bytes_out[3]) {
@@ -725,7 +734,9 @@ kvq_status kv_paged_decode_attention(const kivi_paged_cache* cache, const uint16
     max_u = std::max(max_u, U);
   }
   seqs.unit0[cf.batch] = static_cast<int>(total);
-  const int per_sm = kvq::kivi_paged_decode_blocks_per_sm(cf.head_dim, cf.k_bits, cf.v_bits);
+  const int per_sm = use_swapped_decode(cf)
+                         ? kvq::kivi_paged_decode_tr_blocks_per_sm(cf.head_dim, cf.k_bits, cf.v_bits)
+                         : kvq::kivi_paged_decode_blocks_per_sm(cf.head_dim, cf.k_bits, cf.v_bits);
   const long long slots = static_cast<long long>(kvq::device_sm_count()) * std::max(1, per_sm);
   long long per = (total + slots - 1) / slots;
   per = std::max<long long>(per, kMinUnitsPerSplit);
@@ -744,7 +755,8 @@ kvq_status kv_paged_decode_attention(const kivi_paged_cache* cache, const uint16
   view.res_cap = cache->res_cap;
   const kvq::KiviDecodeArgs a = kivi_decode_args(&view, plan, q, out, out_fp32, scale, static_cast<uint8_t*>(ws));
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return from_cuda(kvq::launch_kivi_decode_paged(a, seqs, s));
+  return from_cuda(use_swapped_decode(cf) ? kvq::launch_kivi_decode_tr_paged(a, seqs, s)
+                                          : kvq::launch_kivi_decode_paged(a, seqs, s));
 }
 
 size_t fp8_quantize_workspace_bytes(int32_t batch, int32_t kv_heads, int32_t seq_len, int32_t head_dim) {
@@ -955,7 +967,7 @@ kvq_status kv_decode_attention_noalloc(const kivi_cache* cache, const uint16_t* 
   if (cudaMemsetAsync(ws, 0, head, s) != cudaSuccess) return KVQ_ERR_CUDA;
 
   const kvq::KiviDecodeArgs a = kivi_decode_args(cache, plan, q, out, out_fp32, scale, static_cast<uint8_t*>(ws));
-  return from_cuda(kvq::launch_kivi_decode(a, s));
+  return from_cuda(launch_contiguous_decode(cf, a, s));
 }
 
 }  // extern "C"

@@ -1,6 +1,7 @@
 // KIVI 2/4-bit KV cache kernels for sm_103a: group quantize + pack (prefill and
-// residual flush) and token copies (window fill, append). The decode attention
-// over the packed codes is in kivi_decode_tc.cu.
+// residual flush), token copies (window fill, append), split-K decode attention
+// over the packed codes with in-register dequantization, and the log-sum-exp
+// merge of the split partials.
 //
 // Method: "4.4 KV Cache 量化：KIVI 2-bit 与 FP8 KV Cache" (aiinfraguide), section 3
 // (keys per channel, values per token, groups of 32 tokens, fp16 residual
@@ -11,12 +12,44 @@
 #include <cmath>
 #include <type_traits>
 
-#include "kivi_layout.cuh"
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
 
+#ifndef KVQ_DECODE_MIN_BLOCKS
+#define KVQ_DECODE_MIN_BLOCKS 3  // resident decode blocks per SM the register budget is sized for
+#endif
+
 namespace kvq {
 namespace {
+
+template <int D, int KB, int VB>
+struct Kivi {
+  static constexpr int KS = D / 16;                     // k-steps of q . k^T
+  static constexpr int NTV = D / 8;                     // n-tiles of p . V
+  static constexpr int NQ = D / 32;                     // value code words per (k-step[, r])
+  static constexpr int KW = (KB == 2) ? D / 16 : D / 8;  // key code words per lane
+  static constexpr int VW = (VB == 2) ? D / 16 : D / 8;  // value code words per lane
+  static constexpr int KC = 32 * D * KB / 8;            // bytes of one group's records
+  static constexpr int KM = 4 * D;
+  static constexpr int VC = 32 * D * VB / 8;
+  static constexpr int VM = 128;
+  static constexpr int STAGE = KC + KM + VC + VM;
+  static_assert(STAGE % 16 == 0, "bulk copies need 16-byte multiples");
+};
+
+// Masks that keep the code field of each fp16 half after the shift: bits 6-7
+// or 8-9 for 2-bit codes, bits 6-9 for 4-bit codes. The field then reads as
+// the fp16 subnormal code * 2^(P-24), P = 6 or 8; the top mantissa bits keep
+// the tensor-core products at full fp32-accumulation accuracy. A 2-bit word
+// holds 8 fields per half; the word itself, its shifts by 4 either way and its
+// per-half byte swap bring two fields each to bits 6-7 and 8-9 (field order
+// f = (4r + nt + 1) mod 8 of the packed layout): three operations and eight
+// masks for 16 codes.
+constexpr uint32_t kMaskP6 = 0x00C000C0u;
+constexpr uint32_t kMaskP8 = 0x03000300u;
+constexpr uint32_t kMask4 = 0x03C003C0u;
+constexpr float kInvP6 = 262144.0f;  // 2^18 = 2^(24-6)
+constexpr float kInvP8 = 65536.0f;   // 2^16 = 2^(24-8)
 
 // ---------------------------------------------------------------------------
 // Group quantization (one thread block per (group, kv head, batch row))
@@ -64,32 +97,28 @@ __device__ __forceinline__ uint32_t key_word(const __half* xk, int RS, const flo
   return w;
 }
 
-// Value code word i of channel ch (the channel-major layout of include/kvq.h):
-// field f of the word holds a pair of consecutive tokens, the first in the low
-// half at bits [VB*f, VB*f + VB), the second in the high half. 4 bits: word i,
-// field f = tokens 8i + 2f, +1. 2 bits: the decode exposes the fields of a word
-// in the order (word, shift left 4, shift right 4, byte swap) at bits 6-7
-// (tokens of the first 16, fields 3, 1, 5, 7) and 8-9 (tokens of the last 16,
-// fields 4, 2, 6, 0), so field f holds tokens 16*kstep(f) + 8i + 2*idx(f), +1.
-__device__ __forceinline__ int value_pair_token(int vb, int i, int f) {
-  if (vb == 4) return 8 * i + 2 * f;
-  const int kstep = (f & 1) ? 0 : 1;
-  const int idx = (0x32200113 >> (4 * f)) & 0xF;  // f = 0..7 -> 3, 1, 1, 0, 0, 2, 2, 3
-  return 16 * kstep + 8 * i + 2 * idx;
-}
-
 template <int D, int VB>
 __device__ __forceinline__ uint32_t value_word(const __half* xv, int RS, const float* sv, const float* zv,
-                                               const float* rv, int ch, int i) {
+                                               const float* rv, int u, int gg, int tg) {
   constexpr uint32_t VL = (1u << VB) - 1u;
+  constexpr int NQ = D / 32;
   uint32_t w = 0;
 #pragma unroll
-  for (int f = 0; f < 16 / VB; ++f) {
-    const int t0 = value_pair_token(VB, i, f);
-    const float x0 = __half2float(xv[t0 * RS + ch]), x1 = __half2float(xv[(t0 + 1) * RS + ch]);
-    // fields never overlap: adding the shifted codes sets the same bits as or-ing them
-    w += (group_code(x0, zv[t0], sv[t0], rv[t0], VL) << (VB * f)) +
-         (group_code(x1, zv[t0 + 1], sv[t0 + 1], rv[t0 + 1], VL) << (16 + VB * f));
+  for (int rr = 0; rr < (VB == 2 ? 2 : 1); ++rr) {
+    const int ks = (VB == 2) ? u / NQ : u / (2 * NQ);
+    const int r = (VB == 2) ? rr : (u / NQ) % 2;
+    const int q = u % NQ;
+    const int t0 = 16 * ks + 8 * r + 2 * tg;
+    const float2 s01 = *reinterpret_cast<const float2*>(sv + t0), z01 = *reinterpret_cast<const float2*>(zv + t0),
+                 r01 = *reinterpret_cast<const float2*>(rv + t0);
+    const float s0 = s01.x, s1 = s01.y, z0 = z01.x, z1 = z01.y, r0 = r01.x, r1 = r01.y;
+#pragma unroll
+    for (int n = 0; n < 4; ++n) {
+      const int ch = 8 * (4 * q + n) + gg;
+      const float x0 = __half2float(xv[t0 * RS + ch]), x1 = __half2float(xv[(t0 + 1) * RS + ch]);
+      const int f = (VB == 2) ? ((4 * r + n + 1) & 7) : n;
+      w += (group_code(x0, z0, s0, r0, VL) << (VB * f)) + (group_code(x1, z1, s1, r1, VL) << (16 + VB * f));
+    }
   }
   return w;
 }
@@ -182,7 +211,7 @@ __device__ __forceinline__ void quantize_group(const uint16_t* k_src, const uint
   __syncthreads();
 
   // Code words, computed straight from the staged tile: warps 0-1 the key
-  // words, warps 2-3 the value words. Key storage words 4*ug .. 4*ug + 3 of
+  // words, warps 2-3 the value words. Storage words 4*ug .. 4*ug + 3 of
   // fragment lane L are one 16-byte chunk (uint4 ug*32 + L); lane L of a warp
   // computes that chunk, so each shared-memory load of the warp has all 32
   // fragment lanes on the same word (conflict-free) and each store writes 512
@@ -198,23 +227,14 @@ __device__ __forceinline__ void quantize_group(const uint16_t* k_src, const uint
       kdst[ug * 32 + lane] = w;
     }
   } else {
-    // values, channel-major: thread c of warps 2-3 writes the VB words of channels c, c + 64, ...
-    // (each shared-memory load of a warp reads 32 consecutive channels of one token row:
-    // conflict-free; each store of a warp writes 32 * 4 * VB contiguous bytes)
-    for (int ch = tid - 64; ch < D; ch += 64) {
-      if constexpr (VB == 2) {
-        uint2 w;
-        w.x = value_word<D, VB>(xv, RS, sv, zv, rv, ch, 0);
-        w.y = value_word<D, VB>(xv, RS, sv, zv, rv, ch, 1);
-        reinterpret_cast<uint2*>(vc)[ch] = w;
-      } else {
-        uint4 w;
-        w.x = value_word<D, VB>(xv, RS, sv, zv, rv, ch, 0);
-        w.y = value_word<D, VB>(xv, RS, sv, zv, rv, ch, 1);
-        w.z = value_word<D, VB>(xv, RS, sv, zv, rv, ch, 2);
-        w.w = value_word<D, VB>(xv, RS, sv, zv, rv, ch, 3);
-        reinterpret_cast<uint4*>(vc)[ch] = w;
-      }
+    uint4* vdst = reinterpret_cast<uint4*>(vc);
+    for (int ug = warp - 2; ug < P::VW / 4; ug += 2) {
+      uint4 w;
+      w.x = value_word<D, VB>(xv, RS, sv, zv, rv, 4 * ug, lane >> 2, lane & 3);
+      w.y = value_word<D, VB>(xv, RS, sv, zv, rv, 4 * ug + 1, lane >> 2, lane & 3);
+      w.z = value_word<D, VB>(xv, RS, sv, zv, rv, 4 * ug + 2, lane >> 2, lane & 3);
+      w.w = value_word<D, VB>(xv, RS, sv, zv, rv, 4 * ug + 3, lane >> 2, lane & 3);
+      vdst[ug * 32 + lane] = w;
     }
   }
 
@@ -251,6 +271,21 @@ __global__ void __launch_bounds__(128) kivi_quantize_kernel(QuantGroupsArgs a) {
   const long long gi = bh * a.groups_cap + a.dst_group0 + grp;
   quantize_group<D, KB, VB>(a.k_src + src_off, a.v_src + src_off, a.k_codes + gi * P::KC, a.k_meta + gi * P::KM,
                             a.v_codes + gi * P::VC, a.v_meta + gi * P::VM);
+}
+
+// The sequence that owns item x of a batched launch: the b < n with
+// begin[b] <= x < begin[b + 1] (begin is non-decreasing, begin[0] = 0 <= x <
+// begin[n]). Binary search over the parameter array.
+__device__ __forceinline__ int seq_of(const int* begin, int n, long long x) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (begin[mid] <= x)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  return lo;
 }
 
 // Grid (total groups, H_kv): item blockIdx.x is group x - begin[b] of sequence
@@ -319,6 +354,628 @@ __global__ void copy_tokens_paged_kernel(PagedCopyArgs a) {
   }
 }
 
+// ---------------------------------------------------------------------------
+// Split-K decode attention
+// ---------------------------------------------------------------------------
+// Grid (splits, H_kv, B), 4 warps. The work of one (batch row, kv head) is a
+// range of units: its groups, then its fp16 window cut into 32-token chunks
+// worth kChunkUnits units each; split x takes units [x * U, (x + 1) * U).
+// Warp w of a block takes the block's groups begin + w, begin + w + 4, ...
+// through its own ring of STAGES shared-memory stages filled by bulk copies
+// (one mbarrier per stage), then its window chunks. Each block writes
+// unnormalized (m, l, o) partials per query head; m and the scores are in
+// log2 units.
+//
+// Tensor-core mapping per group (m16n8k16, M = 16 rows = 8 query heads x
+// {hi, lo} fp16 parts):
+//   q.k^T : A = q'_{h,d} = q_{h,d} * s_{g,d} split exactly into fp16 hi + lo
+//           (hi = fp16(q*s), lo = fma(q, s, -hi)); B = key codes (fields as
+//           fp16 subnormals); plus q . z_g on CUDA cores.
+//   p.V   : A = p_t * s_t split into fp16 hi + lo; B = value codes; plus
+//           sum_t p_t z_t on CUDA cores.
+// Per window chunk the same tiles take fp16 operands straight from shared
+// memory (ldmatrix): A = q for q.k^T, A = p split into hi + lo, B = values.
+template <int D>
+struct CombineSmem {
+  static constexpr int O_FLOATS = 4 * 8 * D;
+  static constexpr int BYTES = (O_FLOATS + 64) * 4;
+};
+
+template <int D, int KB, int VB, int STAGES>
+struct DecodeSmem {
+  static constexpr int BAR_BYTES = 256;
+  static constexpr int STAGE_BYTES = 4 * STAGES * Kivi<D, KB, VB>::STAGE;
+  static constexpr int WIN_ROW = 2 * D + 16;  // one fp16 window row, padded: ldmatrix rows hit distinct banks
+  static constexpr int AREA = (STAGE_BYTES > CombineSmem<D>::BYTES) ? STAGE_BYTES : CombineSmem<D>::BYTES;
+  static constexpr int BYTES = BAR_BYTES + AREA;
+  static_assert((4 * STAGES + 4) * 8 <= BAR_BYTES, "barrier area");
+  static_assert(STAGES * Kivi<D, KB, VB>::STAGE >= 32 * WIN_ROW, "a warp's stages hold one window chunk");
+};
+
+// Online softmax over the 32 scores of one group or chunk (log2 domain): this
+// thread's 8 scores sc of row g give the weights p = 2^(sc - m_run). The
+// reference m_run moves only when a score exceeds it by more than 0.5, so
+// weights stay <= 2^0.5 and p * s_t still fits fp16 for any scale
+// (2^0.5 * 43669 < 65504); the rescale of the accumulators then runs rarely
+// instead of whenever some head's max grows.
+template <int NTV>
+__device__ __forceinline__ void online_softmax(const float (&sc)[8], float (&p)[8], float (&o_acc)[NTV][4], float& m_run,
+                                               float& l_run, float& vz_run) {
+  float mx = sc[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) mx = fmaxf(mx, sc[i]);
+  mx = quad_max(mx);
+  if (mx > m_run + 0.5f) {
+    const float alpha = fast_exp2(m_run - mx);
+    l_run *= alpha;
+    vz_run *= alpha;
+#pragma unroll
+    for (int i = 0; i < NTV; ++i) {
+      o_acc[i][0] *= alpha;
+      o_acc[i][1] *= alpha;
+      o_acc[i][2] *= alpha;
+      o_acc[i][3] *= alpha;
+    }
+    m_run = mx;
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) p[i] = fast_exp2(sc[i] - m_run);
+}
+
+// The fp16 window chunks c_first, c_first + 4, ... < c_end of one warp, after
+// its groups. The warp's stages are free by then and hold one chunk at a time
+// (rows padded to win_row bytes, one bulk copy per row, keys first, then the
+// values into the same rows). o_acc is first brought from code units to real
+// units so that p . V of the fp16 values adds straight into it. Kept out of
+// line: the main loop then keeps its own register allocation. Returns false
+// when a copy wait timed out (that copy may still be in flight on phase
+// `wphase` of `wbar`).
+template <int D, int VB>
+__device__ __noinline__ bool window_chunks(const uint16_t* k_res, const uint16_t* v_res, long long row_base,
+                                           int n_resid, int c_first, int c_end, uint8_t* buf, int win_row,
+                                           uint64_t* wbar, uint32_t& wphase, const uint32_t (&qs)[D / 16][2],
+                                           float p2e, float (&o_io)[D / 8][4], float& m_run, float& l_run,
+                                           float& vz_run) {
+  constexpr int KS = D / 16, NTV = D / 8;
+  const int lane = threadIdx.x & 31, tig = lane & 3;
+  const int mat = lane >> 3, mrow = lane & 7;  // ldmatrix row of this lane inside four 8x8 tiles
+  float o_acc[NTV][4];
+#pragma unroll
+  for (int nt = 0; nt < NTV; ++nt) {
+    const float om = (VB == 2 && (nt & 1)) ? kInvP8 : kInvP6;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o_acc[nt][i] = o_io[nt][i] * om;
+  }
+  uint32_t q[KS][2];
+#pragma unroll
+  for (int ks = 0; ks < KS; ++ks) q[ks][0] = qs[ks][0], q[ks][1] = qs[ks][1];
+  bool ok = true;
+  for (int c = c_first; c < c_end; c += 4) {
+    const int t0 = c * kGroup;
+    const int nv = min(kGroup, n_resid - t0);
+    const long long row0 = row_base + t0;
+    // keys of the chunk
+    __syncwarp();
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    if (lane == 0) mbar_arrive_expect_tx(wbar, nv * D * 2);
+    __syncwarp();
+    if (lane < nv) bulk_g2s(buf + lane * win_row, k_res + (row0 + lane) * D, D * 2, wbar);
+    if (!mbar_wait_bounded(wbar, wphase)) {
+      ok = false;
+      break;
+    }
+    wphase ^= 1u;
+    float sacc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) sacc[i][0] = sacc[i][1] = sacc[i][2] = sacc[i][3] = 0.0f;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+      for (int np = 0; np < 2; ++np) {
+        uint32_t kb[4];  // {b0, b1} of n-tiles 2np and 2np + 1
+        ldsm_x4(kb, buf + (16 * np + 8 * (mat >> 1) + mrow) * win_row + (16 * ks + 8 * (mat & 1)) * 2);
+        mma16816(sacc[2 * np], q[ks][0], 0u, q[ks][1], 0u, kb[0], kb[1]);
+        mma16816(sacc[2 * np + 1], q[ks][0], 0u, q[ks][1], 0u, kb[2], kb[3]);
+      }
+    // values of the chunk into the same rows; the rows past the window are zeroed
+    __syncwarp();
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    if (lane == 0) mbar_arrive_expect_tx(wbar, nv * D * 2);
+    __syncwarp();
+    if (lane < nv) {
+      bulk_g2s(buf + lane * win_row, v_res + (row0 + lane) * D, D * 2, wbar);
+    } else {
+      uint4* zr = reinterpret_cast<uint4*>(buf + lane * win_row);
+#pragma unroll
+      for (int i = 0; i < D / 8; ++i) zr[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    float sc[8], p[8];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int i = 0; i < 2; ++i) sc[2 * nt + i] = (8 * nt + 2 * tig + i < nv) ? sacc[nt][i] * p2e : -INFINITY;
+    online_softmax<NTV>(sc, p, o_acc, m_run, l_run, vz_run);
+    uint32_t phi[4], plo[4];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      const __half2 hh = __floats2half2_rn(p[2 * nt], p[2 * nt + 1]);
+      const float2 hf = __half22float2(hh);
+      phi[nt] = h2_bits(hh);
+      plo[nt] = pack_rn_f16x2(p[2 * nt] - hf.x, p[2 * nt + 1] - hf.y);
+      l_run += p[2 * nt] + p[2 * nt + 1];
+    }
+    if (!mbar_wait_bounded(wbar, wphase)) {
+      ok = false;
+      break;
+    }
+    wphase ^= 1u;
+    __syncwarp();  // the zeroed rows of the other lanes
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks) {
+      const uint32_t A0 = phi[2 * ks], A1 = plo[2 * ks], A2 = phi[2 * ks + 1], A3 = plo[2 * ks + 1];
+#pragma unroll
+      for (int np = 0; np < NTV / 2; ++np) {
+        uint32_t vb[4];  // {b0, b1} of channel tiles 2np and 2np + 1
+        ldsm_x4_trans(vb, buf + (16 * ks + 8 * (mat & 1) + mrow) * win_row + (16 * np + 8 * (mat >> 1)) * 2);
+        mma16816(o_acc[2 * np], A0, A1, A2, A3, vb[0], vb[1]);
+        mma16816(o_acc[2 * np + 1], A0, A1, A2, A3, vb[2], vb[3]);
+      }
+    }
+  }
+#pragma unroll
+  for (int nt = 0; nt < NTV; ++nt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o_io[nt][i] = o_acc[nt][i];
+  return ok;
+}
+
+// Sequence state of the contiguous cache: every pair has a.n_groups groups and
+// a.n_resid window tokens, at unit p * pair_stride.
+struct NoSeqs {};
+
+// Block-table entries a warp of the paged decode keeps in its lanes (nothing
+// for the contiguous cache).
+template <bool kPaged>
+struct TableLanes {
+  int tbase = 0, tblk = 0;
+};
+template <>
+struct TableLanes<false> {};
+
+template <int D, int KB, int VB, int STAGES, class SeqT>
+__global__ void __launch_bounds__(128, KVQ_DECODE_MIN_BLOCKS) kivi_decode_kernel(KiviDecodeArgs a, SeqT seqs) {
+  using P = Kivi<D, KB, VB>;
+  constexpr bool kPaged = !std::is_same<SeqT, NoSeqs>::value;
+  using S = DecodeSmem<D, KB, VB, STAGES>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
+  uint8_t* area = smem + S::BAR_BYTES;
+  float* o_s = reinterpret_cast<float*>(area);  // [4 warps][8 rows][D]  (after a segment's loop)
+  float* m_s = o_s + CombineSmem<D>::O_FLOATS;  // [4][8]
+  float* l_s = m_s + 32;                        // [4][8]
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, tig = lane & 3;
+  const int gq = a.q_heads / a.kv_heads;
+  // The warp's ring: NS slots of GPS consecutive groups each, one bulk copy
+  // per record type and slot (records of consecutive groups are contiguous).
+  constexpr int GPS = 2, NS = STAGES / GPS;
+  static_assert(STAGES % GPS == 0, "whole slots");
+  constexpr int SLOT = GPS * P::STAGE;
+  uint64_t* bar = bars + warp * STAGES;
+  uint64_t* wbar = bars + 4 * STAGES + warp;  // window chunk copies
+  uint8_t* ring = area + warp * STAGES * P::STAGE;
+  if (lane == 0) {
+#pragma unroll
+    for (int s = 0; s < NS; ++s) mbar_init(&bar[s], 1);
+    mbar_init(wbar, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+
+  // This block's slice [u0, u1) of all units, pair after pair; one segment
+  // (and one partial) per (batch row, kv head) it touches.
+  long long all_units = static_cast<long long>(a.n_pairs) * a.pair_stride;
+  if constexpr (kPaged) all_units = seqs.unit0[seqs.n_seqs];
+  const long long u0 = static_cast<long long>(blockIdx.x) * a.units_per_block;
+  const long long u1 = min(all_units, u0 + a.units_per_block);
+  int jg = 0;               // slots this warp has filled so far: ring position and phase of the next
+  uint32_t wphase = 0;      // phase of the window barrier
+  bool timed_out = false;   // sticky: after a wait gives up the warp starts no more copies
+  for (long long u = u0; u < u1;) {
+    int pair, upp, n_grp, n_res;  // the pair, its units, groups and window tokens
+    long long pbase;              // its first unit
+    if constexpr (kPaged) {
+      const int sb = seq_of(seqs.unit0, seqs.n_seqs, u);
+      n_grp = seqs.n_groups[sb];
+      n_res = seqs.n_resid[sb];
+      upp = n_grp + kChunkUnits * ((n_res + kGroup - 1) / kGroup);
+      // each pair's range opens with pair_lead units of no work (the cost of
+      // one more segment); pbase is its first unit of work
+      const int span = upp + seqs.pair_lead;
+      const int hh = static_cast<int>((u - seqs.unit0[sb]) / span);
+      pair = sb * a.kv_heads + hh;
+      const long long vbase = seqs.unit0[sb] + static_cast<long long>(hh) * span;
+      pbase = vbase + seqs.pair_lead;
+      u = vbase + span;
+    } else {
+      pair = static_cast<int>(u / a.pair_stride);
+      pbase = static_cast<long long>(pair) * a.pair_stride;
+      upp = a.units_per_pair;
+      n_grp = a.n_groups;
+      n_res = a.n_resid;
+      u = pbase + a.pair_stride;
+    }
+    const int lo = static_cast<int>(u0 > pbase ? u0 - pbase : 0LL);
+    const int hi = static_cast<int>(min(static_cast<long long>(upp), u1 - pbase));
+    if (lo >= upp) continue;  // padding after the pair's units (the same for the whole block)
+    if constexpr (kPaged) {
+      if (hi <= 0) continue;  // the slice ends inside the pair's lead-in: no work here
+    }
+    const int b = pair / a.kv_heads, h = pair % a.kv_heads;
+    const long long bh = pair;
+    const int first_block = static_cast<int>(pbase / a.units_per_block);
+    const int split = static_cast<int>(blockIdx.x) - first_block;
+    const int n_splits = static_cast<int>((pbase + upp - 1) / a.units_per_block) - first_block + 1;
+    // the stages and the combine area of the previous segment are reused
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncthreads();
+
+    // groups [g_begin, g_end) and window chunks [c_begin, c_end) of the segment
+    const int n_chunks = (n_res + kGroup - 1) / kGroup;
+    const int g_begin = min(n_grp, lo);
+    const int g_end = min(n_grp, hi);
+    const int c_begin = min(n_chunks, max(0, lo - n_grp + kChunkUnits - 1) / kChunkUnits);
+    const int c_end = min(n_chunks, max(0, hi - n_grp + kChunkUnits - 1) / kChunkUnits);
+
+    float m_run = -INFINITY, l_run = 0.0f, vz_run = 0.0f;
+    float o_acc[P::NTV][4];
+#pragma unroll
+    for (int i = 0; i < P::NTV; ++i) o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.0f;
+    // ------------------------------- grouped region -------------------------------
+    // this warp's groups: pairs g_begin + GPS * (warp + 4 * k) + {0, .., GPS - 1}
+    const int n_here = g_end - g_begin;
+    int n_mine = 0;
+    if (!timed_out && n_here > GPS * warp) {
+      const int np = (n_here - GPS * warp + 4 * GPS - 1) / (4 * GPS);
+      n_mine = GPS * (np - 1) + min(GPS, n_here - GPS * (warp + 4 * (np - 1)));
+    }
+    const int n_slots = (n_mine + GPS - 1) / GPS;
+    // contiguous: the pair's records, groups one after the other
+    const long long rec0 = bh * a.groups_cap;
+    const uint8_t* kc_g = a.k_codes + rec0 * P::KC;
+    const uint8_t* km_g = a.k_meta + rec0 * P::KM;
+    const uint8_t* vc_g = a.v_codes + rec0 * P::VC;
+    const uint8_t* vm_g = a.v_meta + rec0 * P::VM;
+    // paged: group j's pool blocks come from the block table through the
+    // lanes (lane l holds the entry of the warp's group tbase + l)
+    TableLanes<kPaged> tl;
+    auto load_table = [&](int base) {  // warp-wide
+      if constexpr (kPaged) {
+        tl.tbase = base;
+        const int jl = base + lane;
+        if (jl < n_mine) {
+          const int grp = g_begin + GPS * (warp + 4 * (jl / GPS)) + jl % GPS;
+          tl.tblk = min(max(__ldg(seqs.pools.block_table + static_cast<long long>(b) * a.groups_cap + grp), 0),
+                        seqs.pools.num_blocks - 1);
+        }
+      }
+    };
+    // the pool blocks of slot k's groups (warp-wide)
+    auto slot_blocks = [&](int k, int& b0, int& b1) {
+      if constexpr (kPaged) {
+        if (GPS * k + GPS > tl.tbase + 32) load_table(GPS * k);
+        b0 = __shfl_sync(0xffffffffu, tl.tblk, GPS * k - tl.tbase);
+        b1 = __shfl_sync(0xffffffffu, tl.tblk, GPS * k + 1 - tl.tbase);
+      }
+    };
+
+    // slot k of this segment (groups GPS*k .. of the warp) goes through ring
+    // position (jg + k) % NS as [key codes x GPS | key meta x GPS | value codes
+    // x GPS | value meta x GPS]
+    auto issue = [&](int k, int b0 = 0, int b1 = 0) {
+      const int grp = g_begin + GPS * (warp + 4 * k);
+      const uint32_t cnt = static_cast<uint32_t>(min(GPS, g_end - grp));
+      uint8_t* dst = ring + ((jg + k) % NS) * SLOT;
+      uint64_t* bb = &bar[(jg + k) % NS];
+      mbar_arrive_expect_tx(bb, cnt * P::STAGE);
+      if constexpr (kPaged) {
+        // one copy per group: kv head h's entry of its pool block (the pool is
+        // a.k_codes; table entries outside [0, num_blocks) were clamped)
+        static_assert(GPS == 2, "two blocks per slot");
+        const uint8_t* pool_h = a.k_codes + static_cast<long long>(h) * P::STAGE;
+        bulk_g2s(dst, pool_h + static_cast<long long>(b0) * a.kv_heads * P::STAGE, P::STAGE, bb);
+        if (cnt > 1) bulk_g2s(dst + P::STAGE, pool_h + static_cast<long long>(b1) * a.kv_heads * P::STAGE, P::STAGE, bb);
+      } else {
+        bulk_g2s(dst, kc_g + grp * static_cast<long long>(P::KC), cnt * P::KC, bb);
+        bulk_g2s(dst + GPS * P::KC, km_g + grp * static_cast<long long>(P::KM), cnt * P::KM, bb);
+        bulk_g2s(dst + GPS * (P::KC + P::KM), vc_g + grp * static_cast<long long>(P::VC), cnt * P::VC, bb);
+        bulk_g2s(dst + GPS * (P::KC + P::KM + P::VC), vm_g + grp * static_cast<long long>(P::VM), cnt * P::VM, bb);
+      }
+    };
+    auto wait_slot = [&](int k) { return mbar_wait_bounded(&bar[(jg + k) % NS], ((jg + k) / NS) & 1); };
+    // the records of group j of the warp (paged: each group's four records
+    // back to back; contiguous: the GPS groups' records of one kind together)
+    auto slot_base = [&](int j) { return ring + ((jg + j / GPS) % NS) * SLOT; };
+    auto kc_of = [&](int j) {
+      if constexpr (kPaged) return slot_base(j) + (j % GPS) * P::STAGE;
+      else return slot_base(j) + (j % GPS) * P::KC;
+    };
+    auto km_of = [&](int j) {
+      if constexpr (kPaged) return slot_base(j) + (j % GPS) * P::STAGE + P::KC;
+      else return slot_base(j) + GPS * P::KC + (j % GPS) * P::KM;
+    };
+    auto vc_of = [&](int j) {
+      if constexpr (kPaged) return slot_base(j) + (j % GPS) * P::STAGE + P::KC + P::KM;
+      else return slot_base(j) + GPS * (P::KC + P::KM) + (j % GPS) * P::VC;
+    };
+    auto vm_of = [&](int j) {
+      if constexpr (kPaged) return slot_base(j) + (j % GPS) * P::STAGE + P::KC + P::KM + P::VC;
+      else return slot_base(j) + GPS * (P::KC + P::KM + P::VC) + (j % GPS) * P::VM;
+    };
+    if constexpr (kPaged) {
+      if (n_mine > 0) load_table(0);
+      for (int k = 0; k < NS && k < n_slots; ++k) {
+        int b0, b1;
+        slot_blocks(k, b0, b1);
+        if (lane == 0) issue(k, b0, b1);
+      }
+    } else {
+      if (lane == 0) {
+        for (int k = 0; k < NS && k < n_slots; ++k) issue(k);
+      }
+    }
+
+    // Query fragments of row g (query head h*gq + g), scaled by 2^-e so that
+    // |q| < 1 and q * s stays inside the fp16 range.
+    const bool row_ok = g < gq;
+    const __half* qrow = reinterpret_cast<const __half*>(a.q) +
+                         (static_cast<long long>(b) * a.q_heads + h * gq + (row_ok ? g : 0)) * D;
+    float2 qv[P::KS][2];
+    float qmax = 0.0f;
+#pragma unroll
+    for (int ks = 0; ks < P::KS; ++ks)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const __half2 v = row_ok ? *reinterpret_cast<const __half2*>(qrow + 16 * ks + 8 * j + 2 * tig)
+                                 : __float2half2_rn(0.0f);
+        qv[ks][j] = __half22float2(v);
+        qmax = fmaxf(qmax, fmaxf(fabsf(qv[ks][j].x), fabsf(qv[ks][j].y)));
+      }
+    qmax = quad_max(qmax);
+    int e = 0;
+    if (qmax > 0.0f) frexpf(qmax, &e);
+    const float qscale = ldexpf(1.0f, -e);
+    uint32_t qs[P::KS][2];
+#pragma unroll
+    for (int ks = 0; ks < P::KS; ++ks)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) qs[ks][j] = pack_rn_f16x2(qv[ks][j].x * qscale, qv[ks][j].y * qscale);
+    const float p2e = ldexpf(1.0f, e) * a.scale_log2;
+    const float mult6 = kInvP6 * p2e, mult8 = kInvP8 * p2e;
+
+    // q . k_hat of the 32 tokens of group j of the warp: 8 scores (log2
+    // units) of this thread's row, tokens 8*nt + 2*tig + {0, 1}.
+    auto qk_scores = [&](int jj, float (&sc)[8]) {
+      const uint4* kcw = reinterpret_cast<const uint4*>(kc_of(jj));
+      const uint4* kmr = reinterpret_cast<const uint4*>(km_of(jj));
+      uint32_t kw[P::KW];
+#pragma unroll
+      for (int c = 0; c < P::KW / 4; ++c) {
+        const uint4 x = kcw[c * 32 + lane];
+        kw[4 * c] = x.x;
+        kw[4 * c + 1] = x.y;
+        kw[4 * c + 2] = x.z;
+        kw[4 * c + 3] = x.w;
+      }
+      float sacc[4][4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) sacc[i][0] = sacc[i][1] = sacc[i][2] = sacc[i][3] = 0.0f;
+      // q . z: this lane's four channels of head g on the FMA pipe (the tensor pipe is the
+      // busier one here); a quad sum after the loop completes the dot product.
+      float bsum = 0.0f;
+#pragma unroll
+      for (int ks = 0; ks < P::KS; ++ks) {
+        const uint4 md = kmr[ks * 4 + tig];  // {s(d0,d0+1), s(d0+8,d0+9), z(d0,d0+1), z(d0+8,d0+9)}
+        const __half2 q0 = bits_h2(qs[ks][0]), q1 = bits_h2(qs[ks][1]);
+        const __half2 hi0 = __hmul2(q0, bits_h2(md.x));
+        const __half2 lo0 = __hfma2(q0, bits_h2(md.x), __hneg2(hi0));
+        const __half2 hi1 = __hmul2(q1, bits_h2(md.y));
+        const __half2 lo1 = __hfma2(q1, bits_h2(md.y), __hneg2(hi1));
+        const uint32_t A0 = h2_bits(hi0), A1 = h2_bits(lo0), A2 = h2_bits(hi1), A3 = h2_bits(lo1);
+        bsum = dot2_f16_f32(qs[ks][0], md.z, dot2_f16_f32(qs[ks][1], md.w, bsum));
+        if constexpr (KB == 2) {
+          const uint32_t w = kw[ks];
+          const uint32_t l4 = w << 4, r4 = w >> 4, sw = __byte_perm(w, 0u, 0x2301u);
+          mma16816(sacc[0], A0, A1, A2, A3, l4 & kMaskP6, r4 & kMaskP6);
+          mma16816(sacc[1], A0, A1, A2, A3, l4 & kMaskP8, r4 & kMaskP8);
+          mma16816(sacc[2], A0, A1, A2, A3, w & kMaskP6, sw & kMaskP6);
+          mma16816(sacc[3], A0, A1, A2, A3, w & kMaskP8, sw & kMaskP8);
+        } else {
+          const uint32_t w0 = kw[2 * ks], w1 = kw[2 * ks + 1];
+          mma16816(sacc[0], A0, A1, A2, A3, (w0 << 6) & kMask4, (w1 << 6) & kMask4);
+          mma16816(sacc[1], A0, A1, A2, A3, (w0 << 2) & kMask4, (w1 << 2) & kMask4);
+          mma16816(sacc[2], A0, A1, A2, A3, (w0 >> 2) & kMask4, (w1 >> 2) & kMask4);
+          mma16816(sacc[3], A0, A1, A2, A3, (w0 >> 6) & kMask4, (w1 >> 6) & kMask4);
+        }
+      }
+      const float bias = quad_sum(bsum) * p2e;
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        const float mult = (KB == 2 && (nt & 1)) ? mult8 : mult6;
+        sc[2 * nt] = fmaf(sacc[nt][0] + sacc[nt][2], mult, bias);
+        sc[2 * nt + 1] = fmaf(sacc[nt][1] + sacc[nt][3], mult, bias);
+      }
+    };
+
+    // Software pipeline: iteration j runs the softmax and p . V of group j
+    // and, in the same straight-line block, q . k^T of group j + 1, so that
+    // each warp keeps both the tensor pipe and the ALUs busy.
+    int j = 0;
+    float sc[8];
+    if (n_mine > 0) {
+      if (wait_slot(0))
+        qk_scores(0, sc);
+      else
+        timed_out = true;
+    }
+    for (; !timed_out && j < n_mine; ++j) {
+      // the next group (this one again past the end: its scores are discarded)
+      const int jn = (j + 1 < n_mine) ? j + 1 : j;
+      if (jn != j && jn % GPS == 0 && !wait_slot(jn / GPS)) {
+        timed_out = true;
+        break;
+      }
+      const uint4* vcw = reinterpret_cast<const uint4*>(vc_of(j));
+      const uint4* vmr = reinterpret_cast<const uint4*>(vm_of(j));
+
+      float p[8];
+      online_softmax<P::NTV>(sc, p, o_acc, m_run, l_run, vz_run);
+
+      // ---- p' = p * s_t as fp16 hi + lo; the zero-point term on CUDA cores ----
+      const uint4 vs = vmr[tig], vz = vmr[4 + tig];
+      const uint32_t vsw[4] = {vs.x, vs.y, vs.z, vs.w};
+      const uint32_t vzw[4] = {vz.x, vz.y, vz.z, vz.w};
+      uint32_t phi[4], plo[4];
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        const float2 sf = __half22float2(bits_h2(vsw[nt]));
+        const float2 zf = __half22float2(bits_h2(vzw[nt]));
+        const float pp0 = p[2 * nt] * sf.x, pp1 = p[2 * nt + 1] * sf.y;
+        const __half2 hh = __floats2half2_rn(pp0, pp1);
+        const float2 hf = __half22float2(hh);
+        phi[nt] = h2_bits(hh);
+        plo[nt] = pack_rn_f16x2(pp0 - hf.x, pp1 - hf.y);
+        l_run += p[2 * nt] + p[2 * nt + 1];
+        vz_run = fmaf(p[2 * nt], zf.x, fmaf(p[2 * nt + 1], zf.y, vz_run));
+      }
+
+      // ---- q . k^T of group j + 1 (independent of what follows) ----
+      qk_scores(jn, sc);
+
+      // ---- o += p' . codes (group j) ----
+      uint32_t vw[P::VW];
+#pragma unroll
+      for (int c = 0; c < P::VW / 4; ++c) {
+        const uint4 x = vcw[c * 32 + lane];
+        vw[4 * c] = x.x;
+        vw[4 * c + 1] = x.y;
+        vw[4 * c + 2] = x.z;
+        vw[4 * c + 3] = x.w;
+      }
+#pragma unroll
+      for (int ks = 0; ks < 2; ++ks) {
+        const uint32_t A0 = phi[2 * ks], A1 = plo[2 * ks], A2 = phi[2 * ks + 1], A3 = plo[2 * ks + 1];
+#pragma unroll
+        for (int q = 0; q < P::NQ; ++q) {
+          if constexpr (VB == 2) {
+            const uint32_t w = vw[ks * P::NQ + q];
+            const uint32_t l4 = w << 4, r4 = w >> 4, sw = __byte_perm(w, 0u, 0x2301u);
+            mma16816(o_acc[4 * q + 0], A0, A1, A2, A3, l4 & kMaskP6, r4 & kMaskP6);
+            mma16816(o_acc[4 * q + 1], A0, A1, A2, A3, l4 & kMaskP8, r4 & kMaskP8);
+            mma16816(o_acc[4 * q + 2], A0, A1, A2, A3, w & kMaskP6, sw & kMaskP6);
+            mma16816(o_acc[4 * q + 3], A0, A1, A2, A3, w & kMaskP8, sw & kMaskP8);
+          } else {
+            const uint32_t w0 = vw[(2 * ks) * P::NQ + q], w1 = vw[(2 * ks + 1) * P::NQ + q];
+            mma16816(o_acc[4 * q + 0], A0, A1, A2, A3, (w0 << 6) & kMask4, (w1 << 6) & kMask4);
+            mma16816(o_acc[4 * q + 1], A0, A1, A2, A3, (w0 << 2) & kMask4, (w1 << 2) & kMask4);
+            mma16816(o_acc[4 * q + 2], A0, A1, A2, A3, (w0 >> 2) & kMask4, (w1 >> 2) & kMask4);
+            mma16816(o_acc[4 * q + 3], A0, A1, A2, A3, (w0 >> 6) & kMask4, (w1 >> 6) & kMask4);
+          }
+        }
+      }
+
+      // after the last group of its slot: release the slot and refill it NS slots ahead
+      if (j % GPS == GPS - 1 || j + 1 == n_mine) {
+        __syncwarp();
+        if constexpr (kPaged) {
+          const int kn = j / GPS + NS;
+          if (kn < n_slots) {
+            int b0, b1;
+            slot_blocks(kn, b0, b1);
+            if (lane == 0) {
+              asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+              issue(kn, b0, b1);
+            }
+          }
+        } else {
+          if (lane == 0 && j / GPS + NS < n_slots) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            issue(j / GPS + NS);
+          }
+        }
+      }
+    }
+
+    // ------------------------ fp16 window, 32-token chunks ------------------------
+    constexpr bool kTwoFields = (VB == 2);
+    bool real_units = false, win_pending = false, seg_timeout = timed_out && n_mine > 0;
+    if (!timed_out && c_begin + warp < c_end) {
+      real_units = true;
+      // the call takes copies: a variable whose address escapes would live in
+      // local memory for the whole kernel, main loop included
+      float o_io[P::NTV][4], st[3] = {m_run, l_run, vz_run};
+      uint32_t q_io[P::KS][2];
+#pragma unroll
+      for (int i = 0; i < P::NTV; ++i)
+        o_io[i][0] = o_acc[i][0], o_io[i][1] = o_acc[i][1], o_io[i][2] = o_acc[i][2], o_io[i][3] = o_acc[i][3];
+#pragma unroll
+      for (int ks = 0; ks < P::KS; ++ks) q_io[ks][0] = qs[ks][0], q_io[ks][1] = qs[ks][1];
+      uint32_t ph = wphase;
+      asm volatile("griddepcontrol.wait;" ::: "memory");  // the window is complete (see decode_dispatch)
+      const bool ok = window_chunks<D, VB>(a.k_res, a.v_res, bh * a.res_cap, n_res, c_begin + warp, c_end, ring,
+                                           S::WIN_ROW, wbar, ph, q_io, p2e, o_io, st[0], st[1], st[2]);
+#pragma unroll
+      for (int i = 0; i < P::NTV; ++i)
+        o_acc[i][0] = o_io[i][0], o_acc[i][1] = o_io[i][1], o_acc[i][2] = o_io[i][2], o_acc[i][3] = o_io[i][3];
+      m_run = st[0];
+      l_run = st[1];
+      vz_run = st[2];
+      wphase = ph;
+      if (!ok) {
+        timed_out = true;
+        seg_timeout = true;
+        win_pending = true;
+      }
+    }
+
+    if (seg_timeout) {
+      if (lane == 0) report_timeout(a.status);
+      // let the copies already in flight land before the stages are reused
+      for (int k = j / GPS; k < n_slots && k < j / GPS + NS; ++k) (void)wait_slot(k);
+      if (win_pending) (void)mbar_wait_bounded(wbar, wphase);
+    }
+    if (timed_out) {
+      m_run = -INFINITY;
+      l_run = 0.0f;
+      vz_run = 0.0f;
+#pragma unroll
+      for (int i = 0; i < P::NTV; ++i) o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.0f;
+    }
+    jg += n_slots;
+    l_run = quad_sum(l_run);
+    vz_run = quad_sum(vz_run);
+    __syncthreads();  // every warp is done with its stages; the area is reused below
+#pragma unroll
+    for (int nt = 0; nt < P::NTV; ++nt) {
+      const float om = real_units ? 1.0f : ((kTwoFields && (nt & 1)) ? kInvP8 : kInvP6);
+      const int c = 8 * nt + 2 * tig;
+      o_s[(warp * 8 + g) * D + c] = fmaf(o_acc[nt][0] + o_acc[nt][2], om, vz_run);
+      o_s[(warp * 8 + g) * D + c + 1] = fmaf(o_acc[nt][1] + o_acc[nt][3], om, vz_run);
+    }
+    if (tig == 0) {
+      m_s[warp * 8 + g] = m_run;
+      l_s[warp * 8 + g] = l_run;
+    }
+
+    // the kernel before this one has finished before any workspace write (see decode_dispatch)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    __syncthreads();
+    finish_split<D>(o_s, m_s, l_s, gq, static_cast<long long>(b) * a.q_heads + h * gq, split, n_splits,
+                    a.part_stride, a.part_o, a.part_ml, a.counters + bh, a.out, a.out_fp32);
+  }
+}
+
+constexpr int kDecodeStages = 4;
 
 template <int D, int KB, int VB>
 cudaError_t quantize_dispatch(const QuantGroupsArgs& a, cudaStream_t s) {
@@ -332,6 +989,50 @@ cudaError_t quantize_paged_dispatch(const PagedQuantArgs& a, cudaStream_t s) {
   dim3 grid(a.r.begin[a.n_seqs], a.q.kv_heads);
   kivi_quantize_paged_kernel<D, KB, VB><<<grid, 128, 0, s>>>(a);
   return cudaGetLastError();
+}
+
+template <int D, int KB, int VB, class SeqT>
+int decode_occupancy() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  if (cached[dev] == 0) {
+    constexpr int smem = DecodeSmem<D, KB, VB, kDecodeStages>::BYTES;
+    auto kern = kivi_decode_kernel<D, KB, VB, kDecodeStages, SeqT>;
+    int n = 0;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, 128, smem) != cudaSuccess || n <= 0)
+      n = 1;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+// The decode is launched as a programmatic dependent of the kernel before it
+// on the stream. Only the token copy of kv_append_token (and of the window
+// fill) lets its dependent start early; every other kernel releases it at its
+// end as usual. So the decode's grouped loop, which reads only group records
+// and q (complete before that copy started), overlaps the copy, while the
+// fp16 window and the workspace (partials, split counters, shared with the
+// previous decode) are touched only after griddepcontrol.wait, i.e. after the
+// preceding kernel has completed.
+template <int D, int KB, int VB, class SeqT>
+cudaError_t decode_dispatch(const KiviDecodeArgs& a, const SeqT& seqs, cudaStream_t s) {
+  constexpr int smem = DecodeSmem<D, KB, VB, kDecodeStages>::BYTES;
+  auto kern = kivi_decode_kernel<D, KB, VB, kDecodeStages, SeqT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(a.n_blocks));
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a, seqs);
 }
 
 }  // namespace
@@ -350,6 +1051,54 @@ cudaError_t launch_kivi_quantize(const QuantGroupsArgs& a, cudaStream_t s) {
     case 12844: return quantize_dispatch<128, 4, 4>(a, s);
     default: return cudaErrorInvalidValue;
   }
+}
+
+namespace {
+
+template <class SeqT>
+cudaError_t decode_by_key(const KiviDecodeArgs& a, const SeqT& seqs, cudaStream_t s) {
+  switch (a.head_dim * 100 + a.k_bits * 10 + a.v_bits) {
+    case 6422: return decode_dispatch<64, 2, 2>(a, seqs, s);
+    case 6424: return decode_dispatch<64, 2, 4>(a, seqs, s);
+    case 6442: return decode_dispatch<64, 4, 2>(a, seqs, s);
+    case 6444: return decode_dispatch<64, 4, 4>(a, seqs, s);
+    case 12822: return decode_dispatch<128, 2, 2>(a, seqs, s);
+    case 12824: return decode_dispatch<128, 2, 4>(a, seqs, s);
+    case 12842: return decode_dispatch<128, 4, 2>(a, seqs, s);
+    case 12844: return decode_dispatch<128, 4, 4>(a, seqs, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <class SeqT>
+int occupancy_by_key(int head_dim, int k_bits, int v_bits) {
+  switch (head_dim * 100 + k_bits * 10 + v_bits) {
+    case 6422: return decode_occupancy<64, 2, 2, SeqT>();
+    case 6424: return decode_occupancy<64, 2, 4, SeqT>();
+    case 6442: return decode_occupancy<64, 4, 2, SeqT>();
+    case 6444: return decode_occupancy<64, 4, 4, SeqT>();
+    case 12822: return decode_occupancy<128, 2, 2, SeqT>();
+    case 12824: return decode_occupancy<128, 2, 4, SeqT>();
+    case 12842: return decode_occupancy<128, 4, 2, SeqT>();
+    case 12844: return decode_occupancy<128, 4, 4, SeqT>();
+    default: return 1;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_kivi_decode(const KiviDecodeArgs& a, cudaStream_t s) { return decode_by_key(a, NoSeqs{}, s); }
+
+cudaError_t launch_kivi_decode_paged(const KiviDecodeArgs& a, const PagedSeqs& seqs, cudaStream_t s) {
+  return decode_by_key(a, seqs, s);
+}
+
+int kivi_decode_blocks_per_sm(int head_dim, int k_bits, int v_bits) {
+  return occupancy_by_key<NoSeqs>(head_dim, k_bits, v_bits);
+}
+
+int kivi_paged_decode_blocks_per_sm(int head_dim, int k_bits, int v_bits) {
+  return occupancy_by_key<PagedSeqs>(head_dim, k_bits, v_bits);
 }
 
 cudaError_t launch_kivi_quantize_paged(const PagedQuantArgs& a, cudaStream_t s) {

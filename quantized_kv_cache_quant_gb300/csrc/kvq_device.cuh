@@ -89,16 +89,6 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// D += A * B, m16n8k8, fp16 inputs, fp32 accumulators: a0 = (row g, cols 2t,
-// 2t+1), a1 = (row g+8, same cols); b0 = (rows 2t, 2t+1 of col g); C/D as
-// for m16n8k16.
-__device__ __forceinline__ void mma1688(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t b0) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k8.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, {%0,%1,%2,%3};\n"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a0), "r"(a1), "r"(b0));
-}
-
 // Four 8x8 fp16 tiles from shared memory into mma.sync operand registers.
 // Lane l gives the address of row l % 8 of tile l / 8 (16 contiguous bytes);
 // register i then holds tile i in fragment order: lane (g, t) receives row g,
@@ -239,116 +229,6 @@ __device__ __forceinline__ float quad_sum(float v) {
   return v + __shfl_xor_sync(0xffffffffu, v, 2);
 }
 
-// Shared-memory accesses by 32-bit shared-window address (volatile: they keep
-// their order against the barrier and mbarrier waits around them).
-__device__ __forceinline__ uint4 lds128(uint32_t a) {
-  uint4 v;
-  asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
-  return v;
-}
-__device__ __forceinline__ uint2 lds64(uint32_t a) {
-  uint2 v;
-  asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
-  return v;
-}
-__device__ __forceinline__ void sts32(uint32_t a, uint32_t v) {
-  asm volatile("st.shared.b32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
-}
-
-// ---- tcgen05: the fifth-generation tensor cores and their tensor memory ----
-// Tensor memory (TMEM) is 128 lanes x 512 columns of 32-bit cells per SM; a
-// thread block allocates a power-of-two number of columns and addresses a cell
-// as (lane << 16) | column. Warp w of a block reaches lanes 32*(w%4) .. +31.
-
-// Allocate ncols columns; the base address is written to *dst (shared memory).
-// Executed by one whole warp.
-__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(dst)),
-               "r"(ncols)
-               : "memory");
-}
-// This block makes no further allocation (lets other blocks allocate). Whole warp.
-__device__ __forceinline__ void tmem_relinquish() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-// Free what tmem_alloc returned. Whole warp.
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-// Order tensor-core and tensor-memory operations around a thread barrier.
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// Lane i of the warp writes r[0..15] to columns taddr.col .. +15 of lane
-// taddr.lane + i (taddr.lane = 32 * (warp % 4)). Whole warp.
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
-      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-      : "memory");
-}
-// Eight columns: r[0..7] to columns taddr.col .. +7. Whole warp.
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3,
-                                         uint32_t r4, uint32_t r5, uint32_t r6, uint32_t r7) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r0),
-               "r"(r1), "r"(r2), "r"(r3), "r"(r4), "r"(r5), "r"(r6), "r"(r7)
-               : "memory");
-}
-// The reverse: columns taddr.col .. +15 of lane taddr.lane + i into r. Whole warp.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr)
-      : "memory");
-}
-__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
-// Shared-memory operand descriptor, K-major, no swizzle: the operand is cut
-// into core matrices of 8 rows x 16 bytes (each 128 contiguous bytes, rows 16
-// bytes apart); lbo = bytes between core matrices adjacent along K, sbo =
-// bytes between core matrices adjacent along M or N. Bits 46-47 hold the
-// descriptor version 1.
-__device__ __forceinline__ uint64_t smem_desc_kmajor(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
-         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
-}
-
-// Instruction descriptor of kind::f16 with fp16 A and B, fp32 D, both operands
-// K-major: bits 4-5 D format (1 = f32), 7-9 / 10-12 A / B format (0 = f16),
-// 17-22 N / 8, 24-28 M / 16.
-template <int M, int N>
-constexpr uint32_t tc_idesc_f16_f32() {
-  static_assert(M == 128 && N % 16 == 0 && N >= 16 && N <= 256, "shape of one cta_group::1 MMA");
-  return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
-}
-
-// D[tmem] (+)= A[tmem] * B[smem]: one tcgen05.mma of kind::f16, A read from
-// tensor memory (row m = lane m, column j = K elements 2j, 2j+1), accumulate
-// when `accum` != 0. Issued by one thread.
-__device__ __forceinline__ void tc_mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                                  uint32_t accum) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accum)
-      : "memory");
-}
-// One arrival on `bar` once every tcgen05.mma this thread issued before has completed.
-__device__ __forceinline__ void tc_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
-               : "memory");
-}
-
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 __device__ __forceinline__ void report_timeout(uint32_t* status) {
   if (status != nullptr) atomicOr(status, kStatusTimeout);
 }
@@ -357,16 +237,15 @@ __device__ __forceinline__ void report_timeout(uint32_t* status) {
 
 namespace kvq {
 
-// Epilogue shared by the split-K decode kernels. The block has left NW
-// partial (m, l, o) triples per query row in shared memory (o_s[NW][8][D],
-// m_s[NW][8], l_s[NW][8], log2 units; one per warp, or NW = 1 when the
-// block's warps share one accumulator). The block combines them and writes its
+// Epilogue shared by the split-K decode kernels. The four warps of a thread
+// block have left per-warp (m, l, o) in shared memory (o_s[4][8][D],
+// m_s[4][8], l_s[4][8], log2 units). The block combines them and writes its
 // partial `split` of each query row (slot row * stride + split); the last of
 // the `splits_total` blocks of a (batch row, kv head) to finish — found with an
 // atomic counter, no waiting — merges all splits into `out` and resets the
 // counter for the next call.
 // Needs blockDim.x == 128 and D in {64, 128}.
-template <int D, int NW = 4>
+template <int D>
 __device__ __forceinline__ void finish_split(float* o_s, float* m_s, float* l_s, int gq, long long q_row0, int split,
                                              int splits_total, int stride, float* part_o, float* part_ml,
                                              uint32_t* counter, void* out, int out_fp32) {
@@ -375,11 +254,11 @@ __device__ __forceinline__ void finish_split(float* o_s, float* m_s, float* l_s,
     const int r = i / D, c = i % D;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < NW; ++w) M = fmaxf(M, m_s[w * 8 + r]);
+    for (int w = 0; w < 4; ++w) M = fmaxf(M, m_s[w * 8 + r]);
     float L = 0.0f, O = 0.0f;
     if (M != -INFINITY) {
 #pragma unroll
-      for (int w = 0; w < NW; ++w) {
+      for (int w = 0; w < 4; ++w) {
         const float f = fast_exp2(m_s[w * 8 + r] - M);
         L = fmaf(l_s[w * 8 + r], f, L);
         O = fmaf(o_s[(w * 8 + r) * D + c], f, O);

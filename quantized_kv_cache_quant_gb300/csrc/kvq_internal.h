@@ -112,6 +112,12 @@ struct KiviDecodeArgs {
   int out_fp32;
 };
 cudaError_t launch_kivi_decode(const KiviDecodeArgs& a, cudaStream_t s);
+// The same decode with the tensor-core operands swapped (tokens and channels
+// on the tile rows, query heads x {hi, lo} on its 8 columns), for caches whose
+// kv heads serve at most kMaxGqaSwapped query heads.
+constexpr int kMaxGqaSwapped = 4;
+cudaError_t launch_kivi_decode_tr(const KiviDecodeArgs& a, cudaStream_t s);
+
 // Decode over a paged cache: the pairs of sequence b (b * kv_heads + h) have
 // n_groups[b] groups and n_resid[b] window tokens, U_b = n_groups[b] +
 // kChunkUnits * ceil(n_resid[b] / 32) units of work each, and the ranges of
@@ -130,6 +136,8 @@ struct PagedSeqs {
   int n_resid[kMaxPagedSeqs];
 };
 cudaError_t launch_kivi_decode_paged(const KiviDecodeArgs& a, const PagedSeqs& seqs, cudaStream_t s);
+// The swapped-operand decode over a paged cache (H_q / H_kv <= kMaxGqaSwapped).
+cudaError_t launch_kivi_decode_tr_paged(const KiviDecodeArgs& a, const PagedSeqs& seqs, cudaStream_t s);
 
 
 struct Fp8QuantArgs {
@@ -192,6 +200,8 @@ int device_sm_count();
 // Resident thread blocks per SM of the decode kernels (occupancy API, cached).
 int kivi_decode_blocks_per_sm(int head_dim, int k_bits, int v_bits);
 int kivi_paged_decode_blocks_per_sm(int head_dim, int k_bits, int v_bits);
+int kivi_decode_tr_blocks_per_sm(int head_dim, int k_bits, int v_bits);
+int kivi_paged_decode_tr_blocks_per_sm(int head_dim, int k_bits, int v_bits);
 int fp8_decode_blocks_per_sm(int head_dim);
 
 }  // namespace kvq

@@ -1,15 +1,12 @@
 """Pins of the packed-cache layout.
 
-The key packer in ``oracle.layout`` is checked against the mma.sync m16n8k16
+The packer in ``oracle.layout`` is checked against the mma.sync m16n8k16
 operand-fragment semantics of the PTX ISA (B operand, ``.col``: register b0
 holds rows ``k = 2*tig + {0,1}`` and b1 rows ``k = 2*tig + 8 + {0,1}`` of
-column ``n = lane // 4``); the value packer against the tensor-memory A
-operand of tcgen05.mma kind::f16 (lane = row = channel, 32-bit column j = K
-elements 2j and 2j + 1, here tokens). Both are combined with the documented
-field-extraction rule: each 16-bit half of an extracted register is an fp16
-subnormal whose value is ``code * 2^(P - 24)``. This is a different route to
-the same bytes than the packer's own loops, so an index slip in either shows
-up here.
+column ``n = lane // 4``), combined with the documented field-extraction rule:
+each 16-bit half of an extracted register is an fp16 subnormal whose value is
+``code * 2^(P - 24)``. This is a different route to the same bytes than the
+packer's own loops, so an index slip in either shows up here.
 """
 import numpy as np
 import pytest
@@ -74,60 +71,26 @@ def test_key_fragments(bits, d):
             assert np.array_equal(tile, want), (ks, nt)
 
 
-# value columns: for 2 bits, column c of a channel's 16 comes from word (c % 8) // 4
-# by operation [w, w << 4, w >> 4, swap(w)][c % 4], read at P = 6 for c < 8 and
-# P = 8 for c >= 8; for 4 bits from word c // 4 by [w << 6, w << 2, w >> 2,
-# w >> 6][c % 4] at P = 6.
-def _value_column(words_of_channel, bits, c):
-    if bits == 2:
-        w = int(words_of_channel[(c % 8) // 4])
-        kind, n = [("shl", 0), ("shl", 4), ("shr", 4), ("swap", 0)][c % 4]
-        p = 6 if c < 8 else 8
-    else:
-        w = int(words_of_channel[c // 4])
-        kind, n = [("shl", 6), ("shl", 2), ("shr", 2), ("shr", 6)][c % 4]
-        p = 6
-    if kind == "shl":
-        w = (w << n) & 0xFFFFFFFF
-    elif kind == "shr":
-        w = w >> n
-    else:
-        w = ((w & 0x00FF00FF) << 8) | ((w >> 8) & 0x00FF00FF)
-    mask = ((1 << bits) - 1) << p
-    w &= mask | (mask << 16)
-    scale = 2.0 ** (24 - p)
-    return (float(np.uint16(w & 0xFFFF).view(np.float16)) * scale,
-            float(np.uint16(w >> 16).view(np.float16)) * scale)
-
-
 @pytest.mark.parametrize("bits", [2, 4])
 @pytest.mark.parametrize("d", [64, 128])
-def test_value_tensor_memory_columns(bits, d):
+def test_value_fragments(bits, d):
     rng = np.random.default_rng(bits * 7 + d)
     codes = rng.integers(0, 2 ** bits, size=(32, d), dtype=np.uint8)
-    words = layout.pack_value_codes(codes, bits).view(np.uint32).reshape(d, bits)
-    assert words.size * 4 == 32 * d * bits // 8
-    # A of p . V: row = channel, K = the 32 tokens, column c = tokens 2c, 2c + 1
-    a = np.full((d, 32), -1.0)
-    for ch in range(d):
-        for c in range(16):
-            a[ch, 2 * c], a[ch, 2 * c + 1] = _value_column(words[ch], bits, c)
-    assert np.array_equal(a, codes.T.astype(np.float64))
-
-
-def test_simulated_pv_matches_plain_product():
-    """p' . codes through the tensor-memory columns equals the plain product."""
-    rng = np.random.default_rng(13)
-    d = 128
-    codes = rng.integers(0, 4, size=(32, d), dtype=np.uint8)
-    words = layout.pack_value_codes(codes, 2).view(np.uint32).reshape(d, 2)
-    pp = rng.standard_normal(32)
-    out = np.zeros(d)
-    for ch in range(d):
-        for c in range(16):
-            lo, hi = _value_column(words[ch], 2, c)
-            out[ch] += pp[2 * c] * lo + pp[2 * c + 1] * hi
-    assert np.allclose(out, pp @ codes.astype(np.float64), rtol=1e-12, atol=1e-12)
+    words = layout.pack_value_codes(codes, bits).view(np.uint32)
+    nq = d // 32
+    # B tiles of p . V: K = 16 tokens of k-step ks, N = 8 channels of n-tile nt
+    for ks in range(2):
+        for nt in range(d // 8):
+            tile = np.full((16, 8), -1.0)
+            for lane in range(32):
+                g, tig = lane // 4, lane % 4
+                for r in range(2):
+                    u = ks * nq + nt // 4 if bits == 2 else (2 * ks + r) * nq + nt // 4
+                    lo, hi = _extract(_word(words, lane, u), bits, r, nt)
+                    tile[2 * tig + 8 * r, g] = lo
+                    tile[2 * tig + 8 * r + 1, g] = hi
+            want = codes[16 * ks:16 * ks + 16, 8 * nt:8 * nt + 8].astype(np.float64)
+            assert np.array_equal(tile, want), (ks, nt)
 
 
 def test_simulated_scores_match_plain_product():
