@@ -200,3 +200,69 @@ def fp8_unpack_pool(packed_pool: np.ndarray, head_dim: int, value_layout: int) -
     out = np.empty_like(packed_pool)
     out[:, :, perm] = packed_pool
     return out.reshape(nb, h, 16, head_dim)
+
+
+# ---------------------------------------------------------------------------
+# NVFP4 paged blocks: one (block, kv head) record of 16 tokens x D holds
+# 8*D bytes of 4-bit codes, then D bytes of E4M3 block scales
+# (specification in ``include/kvq.h``, section "NVFP4 paged cache").
+#   keys   : lane = 4g + tig owns 4*KS code bytes (KS = D/16); its byte
+#            i = (nt*KS + ks)*2 + r holds channels c0 = 16ks + 8r + 2tig (low
+#            nibble) and c0 + 1 (high nibble) of token 8nt + g (nt < 2);
+#            scale byte g*2*KS + nt*KS + ks is the scale of token 8nt + g,
+#            channels 16ks .. 16ks + 15.
+#   values : lane owns D/4 code bytes; its byte i = nt*2 + r holds tokens
+#            t0 = 8r + 2tig (low nibble) and t0 + 1 (high nibble) of channel
+#            8nt + g (nt < D/8); scale byte ((tig*2 + r)*(D/16) + j)*2 + e is
+#            the scale of token 8r + 2tig + e, channels 16j .. 16j + 15.
+# Byte p of a lane's code stream is stored at ((p//16)*32 + lane)*16 + p%16.
+# ---------------------------------------------------------------------------
+
+def nvfp4_pack_record(codes: np.ndarray, scales: np.ndarray, role: int) -> np.ndarray:
+    """One block: codes uint8 ``[16, D]`` (0..15), scales uint8 ``[16, D/16]`` -> uint8 ``[9*D]``."""
+    t, d = codes.shape
+    assert t == 16
+    ks_n = d // 16
+    out = np.zeros(9 * d, np.uint8)
+    for lane in range(32):
+        g, tig = lane // 4, lane % 4
+        stream = []
+        if role == 0:
+            for nt in range(2):
+                for ks in range(ks_n):
+                    for r in range(2):
+                        c0 = 16 * ks + 8 * r + 2 * tig
+                        tok = 8 * nt + g
+                        stream.append(int(codes[tok, c0]) | (int(codes[tok, c0 + 1]) << 4))
+        else:
+            for nt in range(d // 8):
+                for r in range(2):
+                    t0 = 8 * r + 2 * tig
+                    ch = 8 * nt + g
+                    stream.append(int(codes[t0, ch]) | (int(codes[t0 + 1, ch]) << 4))
+        for p, byte in enumerate(stream):
+            out[((p // 16) * 32 + lane) * 16 + p % 16] = byte
+    sc = out[8 * d:]
+    if role == 0:
+        for g in range(8):
+            for nt in range(2):
+                for ks in range(ks_n):
+                    sc[g * 2 * ks_n + nt * ks_n + ks] = scales[8 * nt + g, ks]
+    else:
+        for tig in range(4):
+            for r in range(2):
+                for j in range(ks_n):
+                    for e in range(2):
+                        sc[((tig * 2 + r) * ks_n + j) * 2 + e] = scales[8 * r + 2 * tig + e, j]
+    return out
+
+
+def nvfp4_pack_pool(codes_pool: np.ndarray, scales_pool: np.ndarray, role: int) -> np.ndarray:
+    """Natural blocks codes ``[nb, H, 16, D]``, scales ``[nb, H, 16, D/16]`` -> ``[nb, H, 9*D]``."""
+    nb, h, _, d = codes_pool.shape
+    out = np.zeros((nb, h, 9 * d), np.uint8)
+    for b in range(nb):
+        for hh in range(h):
+            if codes_pool[b, hh].any() or scales_pool[b, hh].any():
+                out[b, hh] = nvfp4_pack_record(codes_pool[b, hh], scales_pool[b, hh], role)
+    return out
