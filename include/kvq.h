@@ -391,6 +391,102 @@ KVQ_API kvq_status fp8_decode_attention(const uint16_t* q, const uint8_t* k_pool
                                 int32_t max_seq_len, void* out, int32_t out_fp32,
                                 float softmax_scale, void* ws, size_t ws_bytes, void* stream);
 
+/* ------------------------------------------------------------------------ */
+/* NVFP4 paged cache [CSDN sections 21.2, 21.3, 13]                          */
+/* ------------------------------------------------------------------------ */
+
+/* [CSDN] section 21.2 names NVFP4 KV as the more aggressive 4-bit
+ * floating-point cache path of Blackwell-class GPUs (about 1/4 of the BF16
+ * bytes, section 21.3) without giving its format. This library follows
+ * NVIDIA's public NVFP4 definition, with the tensor scale from the pages'
+ * per-tensor amax rule:
+ *   element : E2M1 (1 sign, 2 exponent bits with bias 1, 1 mantissa bit;
+ *             magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6), round to nearest even,
+ *             saturating to +-6. Inputs must be finite.
+ *   block   : 16 consecutive channels of one token share one E4M3 scale byte
+ *             b = E4M3(fl32(fl32(amax_b / 6) / s_t)), S_b = e4m3(b).
+ *   tensor  : one float32 scale s_t per tensor (K or V of a layer):
+ *             dynamic s_t = fl32(amax / 2688) (2688 = 448 * 6; 1 for an
+ *             all-zero tensor), or a static (calibrated) value.
+ *   code    = E2M1(fl32(x / fl32(S_b * s_t))), 0 for the whole block when
+ *             S_b = 0; dequantized value = e2m1(code) * S_b * s_t.
+ *
+ * Pool: [num_blocks, kv_heads, 9*D] bytes; one (block, kv head) record holds
+ * 16 tokens: 8*D bytes of codes, then D scale bytes. Logical token t of
+ * sequence b lives in block block_table[b * max_blocks + t/16], row t % 16.
+ * Within a record (lane = 4*g + tig; byte p of a lane's code stream at byte
+ * ((p/16)*32 + lane)*16 + p%16 of the record):
+ *   KVQ_ROLE_KEY   : code byte i = (nt*(D/16) + ks)*2 + r of a lane holds
+ *                    channels c0 = 16*ks + 8*r + 2*tig (low nibble) and c0+1
+ *                    (high nibble) of token 8*nt + g (nt < 2); scale byte
+ *                    g*(D/8) + nt*(D/16) + ks is the scale of token 8*nt + g,
+ *                    channels 16*ks .. 16*ks + 15;
+ *   KVQ_ROLE_VALUE : code byte i = nt*2 + r holds tokens t0 = 8*r + 2*tig (low
+ *                    nibble) and t0+1 (high nibble) of channel 8*nt + g
+ *                    (nt < D/8); scale byte ((tig*2 + r)*(D/16) + j)*2 + e is
+ *                    the scale of token 8*r + 2*tig + e, channels 16*j .. +15.
+ * (These are the m16n8k16 operand fragments of q.k^T and p.V, with each
+ * lane's block scales next to each other.) Rows past the end of a sequence
+ * hold zero codes and zero scales. */
+#define KVQ_ROLE_KEY 0
+#define KVQ_ROLE_VALUE 1
+
+/* Host-side descriptor of one pool (device memory owned by the caller). */
+typedef struct {
+  int32_t role;        /* KVQ_ROLE_KEY or KVQ_ROLE_VALUE: fixes the in-block order */
+  int32_t num_blocks;
+  int32_t kv_heads;
+  int32_t head_dim;    /* 64 or 128 */
+  uint8_t* pool;       /* device [num_blocks, kv_heads, 9 * head_dim] */
+  float* tensor_scale; /* device float32 [1] */
+} nvfp4_pool;
+
+/* Bytes of the pool buffer for this shape (0 if the shape is invalid). */
+KVQ_API size_t nvfp4_pool_bytes(int32_t num_blocks, int32_t kv_heads, int32_t head_dim);
+
+/* Fill a descriptor; no device work. KVQ_ERR_ARG for a role other than
+ * KVQ_ROLE_KEY / KVQ_ROLE_VALUE or num_blocks, kv_heads <= 0;
+ * KVQ_ERR_UNSUPPORTED for head_dim other than 64, 128. */
+KVQ_API kvq_status nvfp4_pool_init(nvfp4_pool* pool, int32_t role, int32_t num_blocks, int32_t kv_heads,
+                                   int32_t head_dim, void* buf, float* tensor_scale);
+
+/* Workspace of nvfp4_kv_quantize with a dynamic scale (amax partials). */
+KVQ_API size_t nvfp4_quantize_workspace_bytes(void);
+
+/* Quantize one tensor (K or V, as the pool's role says) into the pool.
+ *   x           : device fp16 [B, kv_heads, seq_len, D]
+ *   block_table : device int32 [B, max_blocks]; blocks whose entry lies
+ *                 outside [0, num_blocks) are skipped (nothing written)
+ *   static_scale: 0 = write the dynamic s_t to *tensor_scale first; 1 = read
+ *                 *tensor_scale as given (a calibrated scale, > 0)
+ *   ws          : nvfp4_quantize_workspace_bytes() bytes when static_scale == 0
+ * KVQ_ERR_CAPACITY if ceil(seq_len/16) > max_blocks. */
+KVQ_API kvq_status nvfp4_kv_quantize(const nvfp4_pool* pool, const uint16_t* x, int32_t batch, int32_t seq_len,
+                                     const int32_t* block_table, int32_t max_blocks, int32_t static_scale, void* ws,
+                                     size_t ws_bytes, void* stream);
+
+/* Workspace of nvfp4_decode_attention (the layout of kv_decode_workspace_bytes). */
+KVQ_API size_t nvfp4_decode_workspace_bytes(int32_t batch, int32_t q_heads, int32_t head_dim);
+
+/* Decode attention over the NVFP4 paged cache:
+ *   out[b, hq] = softmax(q . K_hat^T * softmax_scale) V_hat
+ * over tokens 0 .. seq_lens[b]-1 of kv head hq / (H_q/H_kv), with K_hat and
+ * V_hat the dequantized values of the two pools.
+ *   k, v     : descriptors of a KVQ_ROLE_KEY and a KVQ_ROLE_VALUE pool of the
+ *              same shape (KVQ_ERR_ARG otherwise)
+ *   q        : device fp16 [B, H_q, D];  out: device [B, H_q, D] (fp32 or fp16)
+ *   seq_lens : device int32 [B], each in [1, max_seq_len]; max_seq_len <=
+ *              max_blocks*16 (the host sizes the grid from it)
+ * Split-K over the blocks of each sequence, merged by the last block of each
+ * (b, kv head) as in fp8_decode_attention. Table entries and seq_lens are
+ * clamped on the device: a bad table gives wrong numbers, never an access
+ * outside the pool. */
+KVQ_API kvq_status nvfp4_decode_attention(const uint16_t* q, const nvfp4_pool* k, const nvfp4_pool* v,
+                                          const int32_t* block_table, const int32_t* seq_lens, int32_t batch,
+                                          int32_t q_heads, int32_t max_blocks, int32_t max_seq_len, void* out,
+                                          int32_t out_fp32, float softmax_scale, void* ws, size_t ws_bytes,
+                                          void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -71,7 +71,8 @@ def e2m1_encode(y: np.ndarray) -> np.ndarray:
     E = np.where(a >= 4.0, 3, E)
     step = np.where(E == 0, 0.5, np.exp2((E - 2).astype(np.float64)))
     base = np.where(E == 0, 0.0, np.exp2((E - 1).astype(np.float64)))
-    m = np.rint((a - base) / step).astype(np.int64)      # 0, 1 or 2 (2 = carry)
+    with np.errstate(invalid="ignore"):                 # non-finite quotients (S_b = 0) are replaced by the caller
+        m = np.rint((a - base) / step).astype(np.int64)  # 0, 1 or 2 (2 = carry)
     code = np.where(E == 0, m, (E << 1) + m)             # a carry (m = 2) moves to the next binade: (E + 1) << 1
     code = np.where((code > 7) | (a > E2M1_MAX), 7, code)
     return (code | sign).astype(np.uint8)

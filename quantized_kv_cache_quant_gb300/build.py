@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libkvq.so")
-SOURCES = ["api.cu", "kivi_kernels.cu", "kivi_decode_tr.cu", "fp8_kernels.cu"]
+SOURCES = ["api.cu", "kivi_kernels.cu", "kivi_decode_tr.cu", "fp8_kernels.cu", "nvfp4_kernels.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

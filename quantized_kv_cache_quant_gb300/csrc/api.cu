@@ -904,6 +904,137 @@ kvq_status fp8_decode_attention(const uint16_t* q, const uint8_t* k_pool, const 
   return from_cuda(kvq::launch_fp8_decode(a, static_cast<cudaStream_t>(stream)));
 }
 
+// ---------------------------------------------------------------------------
+// NVFP4 paged cache
+// ---------------------------------------------------------------------------
+size_t nvfp4_pool_bytes(int32_t num_blocks, int32_t kv_heads, int32_t head_dim) {
+  if (num_blocks <= 0 || kv_heads <= 0 || (head_dim != 64 && head_dim != 128)) return 0;
+  return static_cast<size_t>(num_blocks) * kv_heads * 9 * head_dim;
+}
+
+kvq_status nvfp4_pool_init(nvfp4_pool* pool, int32_t role, int32_t num_blocks, int32_t kv_heads, int32_t head_dim,
+                           void* buf, float* tensor_scale) {
+  if (pool == nullptr || buf == nullptr || tensor_scale == nullptr) return KVQ_ERR_NULL;
+  if (role != KVQ_ROLE_KEY && role != KVQ_ROLE_VALUE) return KVQ_ERR_ARG;
+  if (num_blocks <= 0 || kv_heads <= 0) return KVQ_ERR_ARG;
+  if (head_dim != 64 && head_dim != 128) return KVQ_ERR_UNSUPPORTED;
+  if (!aligned(buf) || !aligned(tensor_scale)) return KVQ_ERR_ALIGN;
+  nvfp4_pool p{};
+  p.role = role;
+  p.num_blocks = num_blocks;
+  p.kv_heads = kv_heads;
+  p.head_dim = head_dim;
+  p.pool = static_cast<uint8_t*>(buf);
+  p.tensor_scale = tensor_scale;
+  *pool = p;
+  return KVQ_OK;
+}
+
+namespace {
+kvq_status check_nvfp4_pool(const nvfp4_pool* p) {
+  if (p == nullptr || p->pool == nullptr || p->tensor_scale == nullptr) return KVQ_ERR_NULL;
+  if (p->role != KVQ_ROLE_KEY && p->role != KVQ_ROLE_VALUE) return KVQ_ERR_ARG;
+  if (p->num_blocks <= 0 || p->kv_heads <= 0) return KVQ_ERR_ARG;
+  if (p->head_dim != 64 && p->head_dim != 128) return KVQ_ERR_UNSUPPORTED;
+  if (!aligned(p->pool) || !aligned(p->tensor_scale)) return KVQ_ERR_ALIGN;
+  return KVQ_OK;
+}
+}  // namespace
+
+size_t nvfp4_quantize_workspace_bytes(void) { return static_cast<size_t>(kAmaxBlocksMax) * sizeof(uint32_t); }
+
+kvq_status nvfp4_kv_quantize(const nvfp4_pool* pool, const uint16_t* x, int32_t batch, int32_t seq_len,
+                             const int32_t* block_table, int32_t max_blocks, int32_t static_scale, void* ws,
+                             size_t ws_bytes, void* stream) {
+  const kvq_status st = check_nvfp4_pool(pool);
+  if (st != KVQ_OK) return st;
+  if (x == nullptr || block_table == nullptr) return KVQ_ERR_NULL;
+  if (batch <= 0 || seq_len <= 0 || max_blocks <= 0) return KVQ_ERR_ARG;
+  if (static_scale != 0 && static_scale != 1) return KVQ_ERR_ARG;
+  if (ceil_div(seq_len, 16) > max_blocks) return KVQ_ERR_CAPACITY;
+  if (!aligned(x) || !aligned(block_table)) return KVQ_ERR_ALIGN;
+  if (!static_scale) {
+    if (ws == nullptr) return KVQ_ERR_WORKSPACE;
+    if (!aligned(ws)) return KVQ_ERR_ALIGN;
+    if (ws_bytes < nvfp4_quantize_workspace_bytes()) return KVQ_ERR_WORKSPACE;
+  }
+  kvq::Nvfp4QuantArgs a{};
+  a.x = x;
+  a.batch = batch;
+  a.kv_heads = pool->kv_heads;
+  a.seq_len = seq_len;
+  a.head_dim = pool->head_dim;
+  a.role = pool->role;
+  a.block_table = block_table;
+  a.max_blocks = max_blocks;
+  a.num_blocks = pool->num_blocks;
+  a.pool = pool->pool;
+  a.scale = pool->tensor_scale;
+  a.static_scale = static_scale;
+  a.amax_partials = static_cast<uint32_t*>(ws);
+  const long long n_vec = static_cast<long long>(batch) * pool->kv_heads * seq_len * pool->head_dim / 8;
+  a.amax_blocks = static_cast<int>(std::max<long long>(
+      1, std::min<long long>({static_cast<long long>(kAmaxBlocksMax), 8LL * kvq::device_sm_count(), (n_vec + 255) / 256})));
+  return from_cuda(kvq::launch_nvfp4_quantize(a, static_cast<cudaStream_t>(stream)));
+}
+
+size_t nvfp4_decode_workspace_bytes(int32_t batch, int32_t q_heads, int32_t head_dim) {
+  if (batch <= 0 || q_heads <= 0 || head_dim <= 0) return 0;
+  return decode_ws_bytes(batch, q_heads, head_dim);
+}
+
+kvq_status nvfp4_decode_attention(const uint16_t* q, const nvfp4_pool* k, const nvfp4_pool* v,
+                                  const int32_t* block_table, const int32_t* seq_lens, int32_t batch, int32_t q_heads,
+                                  int32_t max_blocks, int32_t max_seq_len, void* out, int32_t out_fp32,
+                                  float softmax_scale, void* ws, size_t ws_bytes, void* stream) {
+  kvq_status st = check_nvfp4_pool(k);
+  if (st != KVQ_OK) return st;
+  st = check_nvfp4_pool(v);
+  if (st != KVQ_OK) return st;
+  if (k->role != KVQ_ROLE_KEY || v->role != KVQ_ROLE_VALUE) return KVQ_ERR_ARG;
+  if (k->num_blocks != v->num_blocks || k->kv_heads != v->kv_heads || k->head_dim != v->head_dim) return KVQ_ERR_SHAPE;
+  if (!q || !block_table || !seq_lens || !out) return KVQ_ERR_NULL;
+  if (batch <= 0 || q_heads <= 0 || max_blocks <= 0 || max_seq_len <= 0) return KVQ_ERR_ARG;
+  const int kv_heads = k->kv_heads, head_dim = k->head_dim;
+  if (batch > 65535 || kv_heads > 65535) return KVQ_ERR_UNSUPPORTED;
+  if (q_heads % kv_heads != 0) return KVQ_ERR_SHAPE;
+  if (q_heads / kv_heads > kvq::kMaxGqa) return KVQ_ERR_UNSUPPORTED;
+  if (max_seq_len > max_blocks * 16) return KVQ_ERR_CAPACITY;
+  if (!aligned(q) || !aligned(block_table) || !aligned(seq_lens) || !aligned(out)) return KVQ_ERR_ALIGN;
+  if (ws == nullptr) return KVQ_ERR_WORKSPACE;
+  if (!aligned(ws)) return KVQ_ERR_ALIGN;
+  if (ws_bytes < decode_ws_bytes(batch, q_heads, head_dim)) return KVQ_ERR_WORKSPACE;
+  if (!(softmax_scale == softmax_scale) || std::isinf(softmax_scale)) return KVQ_ERR_ARG;
+  const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(head_dim));
+  const int nblk = ceil_div(max_seq_len, 16);
+  const int splits = choose_splits(nblk, batch * kv_heads, kMaxSplits, kvq::nvfp4_decode_blocks_per_sm(head_dim), 0);
+  kvq::Nvfp4DecodeArgs a{};
+  a.q = q;
+  a.k_pool = k->pool;
+  a.v_pool = v->pool;
+  a.k_scale = k->tensor_scale;
+  a.v_scale = v->tensor_scale;
+  a.block_table = block_table;
+  a.seq_lens = seq_lens;
+  a.batch = batch;
+  a.q_heads = q_heads;
+  a.kv_heads = kv_heads;
+  a.head_dim = head_dim;
+  a.max_blocks = max_blocks;
+  a.num_blocks = k->num_blocks;
+  a.splits = splits;
+  a.blocks_per_split = ceil_div(nblk, splits);
+  a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  a.status = reinterpret_cast<uint32_t*>(base);
+  a.counters = reinterpret_cast<uint32_t*>(base + kWsHeader);
+  a.part_o = reinterpret_cast<float*>(base + kWsHeader + counters_bytes(batch, q_heads));
+  a.part_ml = a.part_o + static_cast<size_t>(batch) * q_heads * splits * head_dim;
+  a.out = out;
+  a.out_fp32 = out_fp32;
+  return from_cuda(kvq::launch_nvfp4_decode(a, static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"
 
 // ---------------------------------------------------------------------------

@@ -635,6 +635,15 @@ cudaError_t launch_fp8_quantize(const Fp8QuantArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+cudaError_t launch_tensor_scale(const uint16_t* x, long long n_vec, float fmax, uint32_t* partials, int blocks,
+                                float* scale, cudaStream_t s) {
+  fp8_amax_kernel<<<dim3(blocks, 1), 256, 0, s>>>(reinterpret_cast<const uint4*>(x), n_vec, 1, 1, n_vec, partials);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  fp8_scale_kernel<<<1, 256, 0, s>>>(partials, blocks, fmax, scale);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_fp8_decode(const Fp8DecodeArgs& a, cudaStream_t s) {
   switch (a.head_dim * 100 + a.fmt * 10 + (a.q_fp8 ? 1 : 0)) {
     case 12800: return fp8_decode_dispatch<128, 0, false>(a, s);

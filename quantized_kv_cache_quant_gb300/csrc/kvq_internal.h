@@ -196,6 +196,49 @@ struct Fp8QueryArgs {
 };
 cudaError_t launch_fp8_quantize_query(const Fp8QueryArgs& a, cudaStream_t s);
 
+// ---- NVFP4 paged cache ----
+struct Nvfp4QuantArgs {
+  const uint16_t* x;      // fp16 [B, H_kv, seq_len, D]
+  int batch, kv_heads, seq_len, head_dim;
+  int role;               // 0 keys, 1 values: the in-block order of the records
+  const int32_t* block_table;
+  int max_blocks;
+  int num_blocks;
+  uint8_t* pool;          // [num_blocks, H_kv, 9 * D]
+  float* scale;           // [1] tensor scale
+  int static_scale;
+  uint32_t* amax_partials;
+  int amax_blocks;
+};
+cudaError_t launch_nvfp4_quantize(const Nvfp4QuantArgs& a, cudaStream_t s);
+
+struct Nvfp4DecodeArgs {
+  const uint16_t* q;
+  const uint8_t* k_pool;
+  const uint8_t* v_pool;
+  const float* k_scale;   // [1]
+  const float* v_scale;   // [1]
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  int batch, q_heads, kv_heads, head_dim, max_blocks, num_blocks;
+  int splits;
+  int blocks_per_split;
+  float scale_log2;
+  float* part_o;
+  float* part_ml;
+  uint32_t* counters;
+  uint32_t* status;
+  void* out;
+  int out_fp32;
+};
+cudaError_t launch_nvfp4_decode(const Nvfp4DecodeArgs& a, cudaStream_t s);
+int nvfp4_decode_blocks_per_sm(int head_dim);
+
+// scale[0] = fl32(amax / fmax) over n_vec 16-byte vectors of fp16 at x (1 when
+// all are zero): per-block amax partials, then one reducing block.
+cudaError_t launch_tensor_scale(const uint16_t* x, long long n_vec, float fmax, uint32_t* partials, int blocks,
+                                float* scale, cudaStream_t s);
+
 int device_sm_count();
 // Resident thread blocks per SM of the decode kernels (occupancy API, cached).
 int kivi_decode_blocks_per_sm(int head_dim, int k_bits, int v_bits);

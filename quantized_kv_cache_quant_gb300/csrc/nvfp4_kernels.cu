@@ -1,0 +1,496 @@
+// NVFP4 paged KV cache kernels for sm_103a: 4-bit E2M1 values with one E4M3
+// scale per 16 channels of a token and one fp32 scale per tensor; cast +
+// scatter into paged blocks, and split-K decode attention over the paged cache.
+//
+// Method: "大模型量化从0到1（十三）：KV Cache 量化" (CSDN), section 21.2 (NVFP4 KV
+// cache: the more aggressive 4-bit floating-point path, scales calibrated
+// offline, for Blackwell-class GPUs) and section 21.3 (about 1/4 of the BF16
+// bytes); section 13 (paged blocks through a block table). The format is
+// NVIDIA's public NVFP4; the tensor scale follows the pages' per-tensor rule
+// scale = amax / FMAX with FMAX = 448 * 6 (the largest E4M3 block scale times
+// the largest E2M1 value).
+//   block scale byte b = E4M3(fl32(fl32(amax_b / 6) / s_t)),  S_b = e4m3(b)
+//   code              = E2M1(fl32(x / fl32(S_b * s_t)))   (0 when S_b = 0)
+//   dequantized value = e2m1(code) * S_b * s_t
+#include <cmath>
+
+#include "kvq_device.cuh"
+#include "kvq_internal.h"
+
+namespace kvq {
+namespace {
+
+constexpr int kBlock = 16;    // tokens per paged block
+constexpr int kCastWarps = 4;
+
+// Two fp32 values -> one byte of two E2M1 codes (round to nearest even,
+// saturating to +-6); `lo` goes to the low nibble.
+__device__ __forceinline__ uint32_t f32x2_to_e2m1x2(float lo, float hi) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\t.reg .b16 u;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\t"
+      "mov.b16 u, {t, 0};\n\t"
+      "cvt.u32.u16 %0, u;\n\t}"
+      : "=r"(r)
+      : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Byte k of w (two E2M1 codes, low nibble first) -> fp16x2 (exact).
+template <int K>
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t w) {
+  uint32_t r;
+  if constexpr (K == 0)
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b0;\n\t}"
+        : "=r"(r)
+        : "r"(w));
+  else if constexpr (K == 1)
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b1;\n\t}"
+        : "=r"(r)
+        : "r"(w));
+  else if constexpr (K == 2)
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b2;\n\t}"
+        : "=r"(r)
+        : "r"(w));
+  else
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b3;\n\t}"
+        : "=r"(r)
+        : "r"(w));
+  return r;
+}
+
+// The two E4M3 scale bytes of half h of w -> fp16x2 (exact).
+__device__ __forceinline__ uint32_t e4m3_pair(uint32_t w, int h) {
+  return e4m3x2_to_f16x2(static_cast<uint16_t>(h ? (w >> 16) : (w & 0xFFFFu)));
+}
+
+// ---------------------------------------------------------------------------
+// Cast + scatter: one warp per (b, h, logical block) unit. The warp stages the
+// unit's 16 x D fp16 values (rows past the sequence zero), computes the
+// scale of each (token, 16-channel block), then writes the record: every lane
+// its D/4 code bytes in 16-byte chunks (chunk c of lane l at byte (c*32 +
+// l)*16), then the D scale bytes, in the in-block order of the role.
+// ---------------------------------------------------------------------------
+template <int D, int ROLE>
+__global__ void __launch_bounds__(32 * kCastWarps) nvfp4_cast_kernel(Nvfp4QuantArgs a) {
+  constexpr int KS = D / 16;
+  constexpr int RS = D + 8;  // padded row stride (halves)
+  __shared__ __align__(16) __half tile[kCastWarps][kBlock * RS];
+  __shared__ float dn[kCastWarps][kBlock * KS];   // fl32(S_b * s_t) per (token, channel block)
+  __shared__ float rc[kCastWarps][kBlock * KS];   // RN(1 / that)
+  __shared__ uint8_t sbyte[kCastWarps][kBlock * KS];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, tig = lane & 3;
+  __half* xs = tile[warp];
+  const float s_t = *a.scale;
+  const int nb = (a.seq_len + kBlock - 1) / kBlock;
+  const long long units = static_cast<long long>(a.batch) * a.kv_heads * nb;
+  for (long long u = blockIdx.x * static_cast<long long>(kCastWarps) + warp; u < units;
+       u += static_cast<long long>(gridDim.x) * kCastWarps) {
+    const int j = static_cast<int>(u % nb);
+    const long long bh = u / nb;
+    const int b = static_cast<int>(bh / a.kv_heads), h = static_cast<int>(bh % a.kv_heads);
+    const int blk = a.block_table[static_cast<long long>(b) * a.max_blocks + j];
+    if (blk < 0 || blk >= a.num_blocks) continue;  // uniform per warp: no write outside the pool
+    const int t0 = j * kBlock, ntok = min(kBlock, a.seq_len - t0);
+    const uint4* src = reinterpret_cast<const uint4*>(a.x + (bh * a.seq_len + t0) * static_cast<long long>(D));
+#pragma unroll
+    for (int i = lane; i < kBlock * D / 8; i += 32) {
+      const int tok = i / (D / 8), c8 = i % (D / 8);
+      *reinterpret_cast<uint4*>(xs + tok * RS + 8 * c8) = (tok < ntok) ? __ldcs(src + i) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    __syncwarp();
+    // block scales
+#pragma unroll
+    for (int p = lane; p < kBlock * KS; p += 32) {
+      const int tok = p / KS, ks = p % KS;
+      const uint4* row = reinterpret_cast<const uint4*>(xs + tok * RS + 16 * ks);
+      const uint4 v0 = row[0], v1 = row[1];
+      const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+      uint32_t m = 0;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) m = max(m, max(w[k] & 0x7FFFu, (w[k] >> 16) & 0x7FFFu));
+      const float amax = __half2float(__ushort_as_half(static_cast<unsigned short>(m)));
+      const float v = __fdiv_rn(__fdiv_rn(amax, 6.0f), s_t);
+      const uint32_t byte = f32x2_to_e4m3x2(v, 0.0f) & 0xFFu;
+      const float S = __half2float(__ushort_as_half(static_cast<unsigned short>(e4m3x2_to_f16x2(
+          static_cast<uint16_t>(byte)) & 0xFFFFu)));
+      const float d = __fmul_rn(S, s_t);
+      sbyte[warp][p] = static_cast<uint8_t>(byte);
+      dn[warp][p] = d;
+      rc[warp][p] = (d > 0.0f) ? __frcp_rn(d) : 0.0f;
+    }
+    __syncwarp();
+    // fl32(x / d) (the IEEE quotient, sign of zero kept), 0 when the block scale is 0
+    auto q = [&](float x, float d, float y) -> float {
+      if (d == 0.0f) return 0.0f;
+      return (d >= 0x1p-96f && d <= 0x1p96f) ? div_rn_by_rcp_signed(x, d, y) : __fdiv_rn(x, d);
+    };
+    uint8_t* dst = a.pool + (static_cast<long long>(blk) * a.kv_heads + h) * (9 * D);
+#pragma unroll
+    for (int c = 0; c < D / 64; ++c) {
+      uint32_t out[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+      for (int kk = 0; kk < 16; ++kk) {
+        const int p = 16 * c + kk;  // byte of the lane's code stream
+        int ta, ca, tb, cb, ia, ib;
+        if constexpr (ROLE == 0) {
+          const int nt = p / (2 * KS), ks = (p % (2 * KS)) >> 1, r = p & 1;
+          ta = tb = 8 * nt + g;
+          ca = 16 * ks + 8 * r + 2 * tig;
+          cb = ca + 1;
+          ia = ib = ta * KS + ks;
+        } else {
+          const int nt = p >> 1, r = p & 1;
+          ta = 8 * r + 2 * tig;
+          tb = ta + 1;
+          ca = cb = 8 * nt + g;
+          ia = ta * KS + (ca >> 4);
+          ib = tb * KS + (ca >> 4);
+        }
+        const float xa = __half2float(xs[ta * RS + ca]), xb = __half2float(xs[tb * RS + cb]);
+        const uint32_t byte = f32x2_to_e2m1x2(q(xa, dn[warp][ia], rc[warp][ia]), q(xb, dn[warp][ib], rc[warp][ib]));
+        out[kk >> 2] |= byte << (8 * (kk & 3));
+      }
+      reinterpret_cast<uint4*>(dst)[c * 32 + lane] = make_uint4(out[0], out[1], out[2], out[3]);
+    }
+    // the D scale bytes: lane l writes bytes 4l .. 4l + 3 (D = 128) or 2l .. 2l + 1 (D = 64)
+    constexpr int PER = D / 32;
+    uint32_t sw = 0;
+#pragma unroll
+    for (int e = 0; e < PER; ++e) {
+      const int s = PER * lane + e;  // scale byte index in the record
+      int tok, blkc;
+      if constexpr (ROLE == 0) {
+        const int gg = s / (2 * KS), rem = s % (2 * KS), nt = rem / KS, ks = rem % KS;
+        tok = 8 * nt + gg;
+        blkc = ks;
+      } else {
+        const int ee = s & 1, jj = (s >> 1) % KS, tr = (s >> 1) / KS, r = tr & 1, tg = tr >> 1;
+        tok = 8 * r + 2 * tg + ee;
+        blkc = jj;
+      }
+      sw |= static_cast<uint32_t>(sbyte[warp][tok * KS + blkc]) << (8 * e);
+    }
+    if constexpr (PER == 4)
+      reinterpret_cast<uint32_t*>(dst + 8 * D)[lane] = sw;
+    else
+      reinterpret_cast<uint16_t*>(dst + 8 * D)[lane] = static_cast<uint16_t>(sw);
+    __syncwarp();  // the staging buffers are refilled by the next unit
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Split-K decode attention over the paged NVFP4 cache. Grid (splits, H_kv, B),
+// 4 warps; warp w of block x takes logical blocks x*bps + w, x*bps + w + 4,
+// ... through a ring of STAGES stages (the key record and the value record of
+// one kv head, 9*D bytes each) filled by bulk copies. Per m16n8k16 k-step the
+// 16 key channels are one scale block, so every operand is fp16(e2m1 * S_b),
+// exact (at most 6 significant bits, inside the fp16 range):
+//   q.k^T : A = q (fp16), B = E2M1 keys converted to fp16, times the block
+//           scale of their token (one half broadcast to both halves);
+//           scores * s_t(K) * softmax scale.
+//   p.V   : A = p split into fp16 hi + lo rows, B = E2M1 values as fp16 times
+//           the scales of their two tokens (one E4M3 pair); outputs * s_t(V).
+// ---------------------------------------------------------------------------
+template <int D, int STAGES>
+struct Nvfp4Smem {
+  static constexpr int BAR_BYTES = 128;
+  static constexpr int REC = 9 * D;
+  static constexpr int STAGE = 2 * REC;
+  static constexpr int RING = 4 * STAGES * STAGE;
+  static constexpr int COMBINE = (4 * 8 * D + 64) * 4;
+  static constexpr int AREA = RING > COMBINE ? RING : COMBINE;
+  static constexpr int BYTES = BAR_BYTES + AREA;
+};
+
+template <int D, int STAGES>
+__global__ void __launch_bounds__(128) nvfp4_decode_kernel(Nvfp4DecodeArgs a) {
+  using S = Nvfp4Smem<D, STAGES>;
+  constexpr int KS = D / 16, NT = D / 8, CH = D / 64;  // CH: 16-byte code chunks per lane
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
+  uint8_t* area = smem + S::BAR_BYTES;
+  float* o_s = reinterpret_cast<float*>(area);
+  float* m_s = o_s + 4 * 8 * D;
+  float* l_s = m_s + 32;
+
+  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, tig = lane & 3;
+  const int gq = a.q_heads / a.kv_heads;
+  const int len = min(max(a.seq_lens[b], 0), a.max_blocks * kBlock);
+  const int nblk = (len + kBlock - 1) / kBlock;
+  const int j_begin = split * a.blocks_per_split;
+  const int j_end = min(nblk, j_begin + a.blocks_per_split);
+  const int n_here = j_end - j_begin;
+  const int n_mine = (n_here > warp) ? (n_here - warp + 3) / 4 : 0;
+  uint64_t* bar = bars + warp * STAGES;
+  uint8_t* ring = area + warp * STAGES * S::STAGE;
+  const int32_t* table = a.block_table + static_cast<long long>(b) * a.max_blocks;
+
+  if (lane == 0) {
+#pragma unroll
+    for (int s = 0; s < STAGES; ++s) mbar_init(&bar[s], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  // physical block of the warp's j-th logical block, clamped into the pool
+  auto phys = [&](int j) -> long long {
+    const int blk = table[j_begin + warp + 4 * j];
+    return static_cast<long long>(min(max(blk, 0), a.num_blocks - 1));
+  };
+  auto issue = [&](int j, long long blk) {
+    const long long off = (blk * a.kv_heads + h) * S::REC;
+    uint8_t* dst = ring + (j % STAGES) * S::STAGE;
+    uint64_t* bb = &bar[j % STAGES];
+    mbar_arrive_expect_tx(bb, S::STAGE);
+    bulk_g2s(dst, a.k_pool + off, S::REC, bb);
+    bulk_g2s(dst + S::REC, a.v_pool + off, S::REC, bb);
+  };
+  if (lane == 0) {
+    for (int j = 0; j < STAGES && j < n_mine; ++j) issue(j, phys(j));
+  }
+
+  const bool row_ok = g < gq;
+  const __half* qrow = reinterpret_cast<const __half*>(a.q) +
+                       (static_cast<long long>(b) * a.q_heads + h * gq + (row_ok ? g : 0)) * D;
+  uint32_t qa[KS][2];
+#pragma unroll
+  for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj)
+      qa[ks][jj] = row_ok ? *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8 * jj + 2 * tig) : 0u;
+  const float kmul = *a.k_scale * a.scale_log2;
+  const float vscale = *a.v_scale;
+
+  float m_run = -INFINITY, l_run = 0.0f;
+  float o_acc[NT][4];
+#pragma unroll
+  for (int i = 0; i < NT; ++i) o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.0f;
+
+  int j = 0;
+  bool timed_out = false;
+  for (; j < n_mine; ++j) {
+    const int s = j % STAGES;
+    const long long next_blk = (lane == 0 && j + STAGES < n_mine) ? phys(j + STAGES) : 0;
+    if (!mbar_wait_bounded(&bar[s], (j / STAGES) & 1)) {
+      timed_out = true;
+      break;
+    }
+    const uint8_t* kr = ring + s * S::STAGE;
+    const uint8_t* vr = kr + S::REC;
+    const int tok_base = (j_begin + warp + 4 * j) * kBlock;
+
+    // keys: stream byte (nt*KS + ks)*2 + r, scales of tokens g (nt = 0) and 8 + g (nt = 1)
+    uint32_t kw[D / 16];
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      const uint4 x = reinterpret_cast<const uint4*>(kr)[c * 32 + lane];
+      kw[4 * c] = x.x;
+      kw[4 * c + 1] = x.y;
+      kw[4 * c + 2] = x.z;
+      kw[4 * c + 3] = x.w;
+    }
+    uint32_t ksw[KS / 2];  // scale bytes nt*KS + ks of row g, four to a word
+    if constexpr (D == 128) {
+      const uint4 x = *reinterpret_cast<const uint4*>(kr + 8 * D + g * 2 * KS);
+      ksw[0] = x.x;
+      ksw[1] = x.y;
+      ksw[2] = x.z;
+      ksw[3] = x.w;
+    } else {
+      const uint2 x = *reinterpret_cast<const uint2*>(kr + 8 * D + g * 2 * KS);
+      ksw[0] = x.x;
+      ksw[1] = x.y;
+    }
+    float sacc[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.0f;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        const int i = nt * KS + ks;                        // (r = 0, 1) bytes 2i, 2i + 1
+        const uint32_t w = kw[i >> 1];
+        const uint32_t sp = e4m3_pair(ksw[i >> 2], (i >> 1) & 1);  // scales i & ~1, i | 1
+        const __half2 sc2 = (i & 1) ? __high2half2(bits_h2(sp)) : __low2half2(bits_h2(sp));
+        uint32_t b0, b1;
+        if (i & 1) {
+          b0 = e2m1x2_to_f16x2<2>(w);
+          b1 = e2m1x2_to_f16x2<3>(w);
+        } else {
+          b0 = e2m1x2_to_f16x2<0>(w);
+          b1 = e2m1x2_to_f16x2<1>(w);
+        }
+        mma16816(sacc[nt], qa[ks][0], 0u, qa[ks][1], 0u, h2_bits(__hmul2(bits_h2(b0), sc2)),
+                 h2_bits(__hmul2(bits_h2(b1), sc2)));
+      }
+    }
+    float sc[4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int tok = tok_base + 8 * nt + 2 * tig + e;
+        sc[2 * nt + e] = (tok < len) ? sacc[nt][e] * kmul : -INFINITY;
+      }
+    float mx = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+    mx = quad_max(mx);
+    const float m_new = fmaxf(m_run, mx);
+    if (m_new != m_run) {
+      const float alpha = fast_exp2(m_run - m_new);
+      l_run *= alpha;
+#pragma unroll
+      for (int i = 0; i < NT; ++i) {
+        o_acc[i][0] *= alpha;
+        o_acc[i][1] *= alpha;
+        o_acc[i][2] *= alpha;
+        o_acc[i][3] *= alpha;
+      }
+      m_run = m_new;
+    }
+    float p[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) p[i] = fast_exp2(sc[i] - m_new);
+    l_run += (p[0] + p[1]) + (p[2] + p[3]);
+    const __half2 h0 = __floats2half2_rn(p[0], p[1]), h1 = __floats2half2_rn(p[2], p[3]);
+    const float2 f0 = __half22float2(h0), f1 = __half22float2(h1);
+    const uint32_t A0 = h2_bits(h0), A1 = pack_rn_f16x2(p[0] - f0.x, p[1] - f0.y);
+    const uint32_t A2 = h2_bits(h1), A3 = pack_rn_f16x2(p[2] - f1.x, p[3] - f1.y);
+
+    // values: stream byte nt*2 + r (tokens 8r + 2tig, +1 of channel 8nt + g);
+    // scale pairs ((tig*2 + r)*KS + blk)*2 + {0, 1}, read as this lane's 4*KS bytes
+    uint32_t vw[D / 16];
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      const uint4 x = reinterpret_cast<const uint4*>(vr)[c * 32 + lane];
+      vw[4 * c] = x.x;
+      vw[4 * c + 1] = x.y;
+      vw[4 * c + 2] = x.z;
+      vw[4 * c + 3] = x.w;
+    }
+    uint32_t vsw[KS];  // pair (r, blk) is half (r*KS + blk) of this array
+    {
+      const uint4* sp = reinterpret_cast<const uint4*>(vr + 8 * D + tig * 4 * KS);
+#pragma unroll
+      for (int c = 0; c < KS / 4; ++c) {
+        const uint4 x = sp[c];
+        vsw[4 * c] = x.x;
+        vsw[4 * c + 1] = x.y;
+        vsw[4 * c + 2] = x.z;
+        vsw[4 * c + 3] = x.w;
+      }
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const uint32_t w = vw[nt >> 1];
+      const int blk = nt >> 1, pr0 = blk, pr1 = KS + blk;  // pair indices of r = 0 and r = 1
+      const uint32_t s0 = e4m3_pair(vsw[pr0 >> 1], pr0 & 1), s1 = e4m3_pair(vsw[pr1 >> 1], pr1 & 1);
+      uint32_t c0, c1;
+      if (nt & 1) {
+        c0 = e2m1x2_to_f16x2<2>(w);
+        c1 = e2m1x2_to_f16x2<3>(w);
+      } else {
+        c0 = e2m1x2_to_f16x2<0>(w);
+        c1 = e2m1x2_to_f16x2<1>(w);
+      }
+      mma16816(o_acc[nt], A0, A1, A2, A3, h2_bits(__hmul2(bits_h2(c0), bits_h2(s0))),
+               h2_bits(__hmul2(bits_h2(c1), bits_h2(s1))));
+    }
+
+    __syncwarp();
+    if (lane == 0 && j + STAGES < n_mine) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      issue(j + STAGES, next_blk);
+    }
+  }
+  if (timed_out) {
+    if (lane == 0) report_timeout(a.status);
+    for (int jj = j; jj < n_mine && jj < j + STAGES; ++jj) (void)mbar_wait_bounded(&bar[jj % STAGES], (jj / STAGES) & 1);
+    m_run = -INFINITY;
+    l_run = 0.0f;
+#pragma unroll
+    for (int i = 0; i < NT; ++i) o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.0f;
+  }
+  l_run = quad_sum(l_run);
+
+  __syncthreads();
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int c = 8 * nt + 2 * tig;
+    o_s[(warp * 8 + g) * D + c] = (o_acc[nt][0] + o_acc[nt][2]) * vscale;
+    o_s[(warp * 8 + g) * D + c + 1] = (o_acc[nt][1] + o_acc[nt][3]) * vscale;
+  }
+  if (tig == 0) {
+    m_s[warp * 8 + g] = m_run;
+    l_s[warp * 8 + g] = l_run;
+  }
+  __syncthreads();
+  finish_split<D>(o_s, m_s, l_s, gq, static_cast<long long>(b) * a.q_heads + h * gq, split, a.splits, a.splits, a.part_o,
+                  a.part_ml, a.counters + static_cast<long long>(b) * a.kv_heads + h, a.out, a.out_fp32);
+}
+
+constexpr int kNvfp4Stages = 4;
+
+template <int D>
+cudaError_t nvfp4_decode_dispatch(const Nvfp4DecodeArgs& a, cudaStream_t s) {
+  constexpr int smem = Nvfp4Smem<D, kNvfp4Stages>::BYTES;
+  auto kern = nvfp4_decode_kernel<D, kNvfp4Stages>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(a.splits, a.kv_heads, a.batch);
+  kern<<<grid, 128, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+template <int D>
+int nvfp4_occupancy() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  if (cached[dev] == 0) {
+    constexpr int smem = Nvfp4Smem<D, kNvfp4Stages>::BYTES;
+    auto kern = nvfp4_decode_kernel<D, kNvfp4Stages>;
+    int n = 0;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, 128, smem) != cudaSuccess || n <= 0)
+      n = 1;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+}  // namespace
+
+int nvfp4_decode_blocks_per_sm(int head_dim) {
+  return head_dim == 64 ? nvfp4_occupancy<64>() : nvfp4_occupancy<128>();
+}
+
+cudaError_t launch_nvfp4_quantize(const Nvfp4QuantArgs& a, cudaStream_t s) {
+  if (!a.static_scale) {
+    const long long n_vec = static_cast<long long>(a.batch) * a.kv_heads * a.seq_len * a.head_dim / 8;
+    const cudaError_t e = launch_tensor_scale(a.x, n_vec, 448.0f * 6.0f, a.amax_partials, a.amax_blocks, a.scale, s);
+    if (e != cudaSuccess) return e;
+  }
+  const int nb = (a.seq_len + kBlock - 1) / kBlock;
+  const long long units = static_cast<long long>(a.batch) * a.kv_heads * nb;
+  const long long want = (units + kCastWarps - 1) / kCastWarps;
+  const long long full = 8LL * device_sm_count();
+  const int grid = static_cast<int>(want < full ? want : full);
+  switch (a.head_dim * 10 + a.role) {
+    case 1280: nvfp4_cast_kernel<128, 0><<<grid, 32 * kCastWarps, 0, s>>>(a); break;
+    case 1281: nvfp4_cast_kernel<128, 1><<<grid, 32 * kCastWarps, 0, s>>>(a); break;
+    case 640: nvfp4_cast_kernel<64, 0><<<grid, 32 * kCastWarps, 0, s>>>(a); break;
+    case 641: nvfp4_cast_kernel<64, 1><<<grid, 32 * kCastWarps, 0, s>>>(a); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_nvfp4_decode(const Nvfp4DecodeArgs& a, cudaStream_t s) {
+  switch (a.head_dim) {
+    case 128: return nvfp4_decode_dispatch<128>(a, s);
+    case 64: return nvfp4_decode_dispatch<64>(a, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace kvq

@@ -31,6 +31,8 @@ EXPORTED = (
     "kv_paged_decode_workspace_bytes", "kv_paged_decode_attention",
     "fp8_quantize_workspace_bytes",
     "fp8_kv_quantize", "fp8_decode_workspace_bytes", "fp8_decode_attention",
+    "nvfp4_pool_bytes", "nvfp4_pool_init", "nvfp4_quantize_workspace_bytes", "nvfp4_kv_quantize",
+    "nvfp4_decode_workspace_bytes", "nvfp4_decode_attention",
 )
 
 STATUS = {0: "KVQ_OK", 1: "KVQ_ERR_NULL", 2: "KVQ_ERR_ARG", 3: "KVQ_ERR_SHAPE", 4: "KVQ_ERR_CAPACITY",
@@ -70,6 +72,15 @@ class kivi_paged_cache(ctypes.Structure):
                 ("n_grouped", c_i32 * PAGED_MAX_SEQS), ("n_resid", c_i32 * PAGED_MAX_SEQS)]
 
 
+ROLE_KEY, ROLE_VALUE = 0, 1
+
+
+class nvfp4_pool(ctypes.Structure):
+    _fields_ = [("role", c_i32), ("num_blocks", c_i32), ("kv_heads", c_i32), ("head_dim", c_i32), ("pool", c_vp),
+                ("tensor_scale", c_vp)]
+
+
+_P_NV = ctypes.POINTER(nvfp4_pool)
 _P_CFG, _P_CACHE = ctypes.POINTER(kivi_config), ctypes.POINTER(kivi_cache)
 _P_PCFG, _P_PCACHE = ctypes.POINTER(kivi_paged_config), ctypes.POINTER(kivi_paged_cache)
 _SIG = {
@@ -95,6 +106,13 @@ _SIG = {
     "fp8_decode_workspace_bytes": ([c_i32, c_i32, c_i32], c_sz),
     "fp8_decode_attention": ([c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, c_i32, c_i32, c_vp, c_vp, c_i32, c_i32, c_i32,
                               c_i32, c_i32, c_i32, c_i32, c_i32, c_vp, c_i32, c_f32, c_vp, c_sz, c_vp], ctypes.c_int),
+    "nvfp4_pool_bytes": ([c_i32, c_i32, c_i32], c_sz),
+    "nvfp4_pool_init": ([_P_NV, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp], ctypes.c_int),
+    "nvfp4_quantize_workspace_bytes": ([], c_sz),
+    "nvfp4_kv_quantize": ([_P_NV, c_vp, c_i32, c_i32, c_vp, c_i32, c_i32, c_vp, c_sz, c_vp], ctypes.c_int),
+    "nvfp4_decode_workspace_bytes": ([c_i32, c_i32, c_i32], c_sz),
+    "nvfp4_decode_attention": ([c_vp, _P_NV, _P_NV, c_vp, c_vp, c_i32, c_i32, c_i32, c_i32, c_vp, c_i32, c_f32, c_vp,
+                                c_sz, c_vp], ctypes.c_int),
 }
 for _name, (_args, _res) in _SIG.items():
     _fn = getattr(_lib, _name)
@@ -253,6 +271,40 @@ def fp8_decode_attention(q, k_pool, v_pool, k_scale, v_scale, block_table, seq_l
                                      _stream(stream)), "fp8_decode_attention")
 
 
+def nvfp4_pool_bytes(num_blocks, kv_heads, head_dim) -> int:
+    return int(_lib.nvfp4_pool_bytes(num_blocks, kv_heads, head_dim))
+
+
+def nvfp4_pool_init(role: int, num_blocks: int, kv_heads: int, head_dim: int, buf, tensor_scale) -> nvfp4_pool:
+    desc = nvfp4_pool()
+    _check(_lib.nvfp4_pool_init(ctypes.byref(desc), role, num_blocks, kv_heads, head_dim, _ptr(buf),
+                                _ptr(tensor_scale)), "nvfp4_pool_init")
+    return desc
+
+
+def nvfp4_quantize_workspace_bytes() -> int:
+    return int(_lib.nvfp4_quantize_workspace_bytes())
+
+
+def nvfp4_kv_quantize(pool: nvfp4_pool, x, batch, seq_len, block_table, max_blocks, static_scale: bool, ws,
+                      ws_bytes: int, stream=None) -> None:
+    _check(_lib.nvfp4_kv_quantize(ctypes.byref(pool), _ptr(x), batch, seq_len, _ptr(block_table), max_blocks,
+                                  int(bool(static_scale)), _ptr(ws), ws_bytes, _stream(stream)), "nvfp4_kv_quantize")
+
+
+def nvfp4_decode_workspace_bytes(batch, q_heads, head_dim) -> int:
+    return int(_lib.nvfp4_decode_workspace_bytes(batch, q_heads, head_dim))
+
+
+def nvfp4_decode_attention(q, k: nvfp4_pool, v: nvfp4_pool, block_table, seq_lens, batch, q_heads, max_blocks,
+                           max_seq_len, out, out_fp32: bool, softmax_scale: float, ws, ws_bytes: int,
+                           stream=None) -> None:
+    _check(_lib.nvfp4_decode_attention(_ptr(q), ctypes.byref(k), ctypes.byref(v), _ptr(block_table), _ptr(seq_lens),
+                                       batch, q_heads, max_blocks, max_seq_len, _ptr(out), int(bool(out_fp32)),
+                                       float(softmax_scale), _ptr(ws), ws_bytes, _stream(stream)),
+           "nvfp4_decode_attention")
+
+
 # ---------------------------------------------------------------------------
 # torch-owned buffers around the descriptors (allocation only; no compute)
 # ---------------------------------------------------------------------------
@@ -399,3 +451,25 @@ class PagedKiviCache:
 
 def default_softmax_scale(head_dim: int) -> float:
     return 1.0 / math.sqrt(head_dim)
+
+
+class Nvfp4Pool:
+    """One NVFP4 pool (keys or values) with its tensor scale, in device memory
+    owned by PyTorch."""
+
+    def __init__(self, role: int, num_blocks: int, kv_heads: int, head_dim: int, device="cuda"):
+        import torch
+        self.buf = _alloc_bytes(nvfp4_pool_bytes(num_blocks, kv_heads, head_dim), device)
+        self.scale = torch.ones(64, dtype=torch.float32, device=device)  # [0] is the tensor scale (256-byte slot)
+        self.desc = nvfp4_pool_init(role, num_blocks, kv_heads, head_dim, self.buf, self.scale)
+        self.ws_bytes = nvfp4_quantize_workspace_bytes()
+        self.ws = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=device)
+
+    def quantize(self, x, block_table, max_blocks, static_scale=False, stream=None):
+        nvfp4_kv_quantize(self.desc, x, x.shape[0], x.shape[2], block_table, max_blocks, static_scale, self.ws,
+                          self.ws_bytes, stream)
+
+    def view(self):
+        """Device bytes as ``[num_blocks, H, 9 * D]`` (uint8)."""
+        d = self.desc
+        return self.buf[: d.num_blocks * d.kv_heads * 9 * d.head_dim].view(d.num_blocks, d.kv_heads, 9 * d.head_dim)

@@ -68,3 +68,20 @@ def fp8_quantize_bytes(batch, kv_heads, seq_len, head_dim, dynamic: bool) -> int
     """One fp8_kv_quantize call: (amax pass +) cast pass over fp16 x, FP8 bytes written."""
     n = batch * kv_heads * seq_len * head_dim
     return n * 2 * (2 if dynamic else 1) + n
+
+
+def nvfp4_record_bytes_per_token(head_dim) -> int:
+    """NVFP4 bytes of one token of one kv head: D/2 code bytes and D/16 scale bytes."""
+    return head_dim // 2 + head_dim // 16
+
+
+def nvfp4_decode_bytes(batch, kv_heads, q_heads, head_dim, seq_len, blocks_per_seq, out_bytes=4) -> int:
+    """One nvfp4_decode_attention call: K and V records, the block table, q and out."""
+    kv = 2 * batch * kv_heads * seq_len * nvfp4_record_bytes_per_token(head_dim)
+    return kv + batch * blocks_per_seq * 4 + batch * q_heads * head_dim * (2 + out_bytes)
+
+
+def nvfp4_quantize_bytes(batch, kv_heads, seq_len, head_dim, dynamic: bool) -> int:
+    """One nvfp4_kv_quantize call: (amax pass +) cast pass over fp16 x, records written."""
+    n = batch * kv_heads * seq_len
+    return n * head_dim * 2 * (2 if dynamic else 1) + n * nvfp4_record_bytes_per_token(head_dim)

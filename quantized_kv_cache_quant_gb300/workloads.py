@@ -71,6 +71,23 @@ class Fp8Workload:
 
 
 @dataclasses.dataclass(frozen=True)
+class Nvfp4Workload:
+    """An NVFP4 paged cache (4-bit E2M1 values, E4M3 scale per 16 channels, fp32 tensor scale)."""
+    name: str
+    batch: int
+    kv_heads: int
+    q_heads: int
+    head_dim: int
+    context: int
+    block_size: int = 16
+    seed: int = 3
+
+    @property
+    def blocks_per_seq(self) -> int:
+        return -(-self.context // self.block_size)
+
+
+@dataclasses.dataclass(frozen=True)
 class PagedKiviWorkload:
     """A batch of sequences of different lengths in one paged KIVI cache."""
     name: str
@@ -114,6 +131,9 @@ FP8_32K_E5M2_PH = dataclasses.replace(FP8_32K, name="fp8_e5m2_perhead_paged_b64_
 FP8_32K_QFP8 = dataclasses.replace(FP8_32K, name="fp8_e4m3_qfp8_paged_b64_h8x32_d128_s32768", q_fp8=True)
 # the same cache for 8 sequences: a size an ncu capture of the quantize kernels can hold
 FP8_32K_B8 = Fp8Workload("fp8_e4m3_paged_b8_h8x32_d128_s32768", 8, 8, 32, 128, 32768, 16, seed=3)
+# the FP8 32K cache's inputs in NVFP4 (the 4-bit floating-point KV of Blackwell-class GPUs)
+NVFP4_32K = Nvfp4Workload("nvfp4_paged_b64_h8x32_d128_s32768", 64, 8, 32, 128, 32768, 16, seed=3)
+NVFP4_32K_B8 = Nvfp4Workload("nvfp4_paged_b8_h8x32_d128_s32768", 8, 8, 32, 128, 32768, 16, seed=3)
 STREAM_128K = KiviWorkload("kivi2_stream_b4_h8x64_d128_s131072_512steps", 4, 8, 64, 128, 131072, 512, seed=4)
 # Paged caches of the GQA 8K shape: every sequence at 8192 tokens (the cost of
 # the block table against the contiguous layout), and lengths spread over
@@ -124,7 +144,8 @@ PAGED_VAR_16K = PagedKiviWorkload("kivi2_paged_b32_h8x64_d128_len512-16384", 32,
 PAGED_GQA4_VAR_16K = PagedKiviWorkload("kivi2_paged_b32_h8x32_d128_len512-16384", 32, 8, 32, 128, 512, 16384, seed=6)
 
 WORKLOADS = {w.name: w for w in (TINY, MHA_4K, GQA_8K_2BIT, GQA_8K_4BIT, FP8_32K, FP8_32K_E5M2_PH, FP8_32K_QFP8,
-                                  FP8_32K_B8, STREAM_128K, PAGED_GQA_8K, PAGED_VAR_16K, PAGED_GQA4_VAR_16K)}
+                                  FP8_32K_B8, NVFP4_32K, NVFP4_32K_B8, STREAM_128K, PAGED_GQA_8K, PAGED_VAR_16K,
+                                  PAGED_GQA4_VAR_16K)}
 
 
 def _channel_scales(rng: np.random.Generator, kv_heads: int, head_dim: int) -> np.ndarray:
@@ -186,7 +207,7 @@ def kivi_inputs(w: KiviWorkload, seq: Optional[int] = None, steps: Optional[int]
                        w.decode_steps if steps is None else steps, w.seed)
 
 
-def fp8_inputs(w: Fp8Workload, context: Optional[int] = None):
+def fp8_inputs(w, context: Optional[int] = None):
     """K, V fp16 [B, Hkv, S, D], q fp16 [B, Hq, D] and a randomly permuted block table."""
     s = w.context if context is None else context
     x = make_inputs(w.batch, w.kv_heads, w.q_heads, w.head_dim, s, 1, w.seed)

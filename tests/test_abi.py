@@ -25,7 +25,7 @@ def declared_functions():
 
 def test_every_declared_symbol_is_exported():
     names = declared_functions()
-    assert len(names) == 20
+    assert len(names) == 26
     lib = ctypes.CDLL(kvq.LIB_PATH)
     for n in names:
         assert hasattr(lib, n), n
@@ -208,6 +208,10 @@ int main(void) {
   printf("kivi_cache %zu\n", sizeof(kivi_cache));
   printf("kivi_paged_config %zu\n", sizeof(kivi_paged_config));
   printf("kivi_paged_cache %zu\n", sizeof(kivi_paged_cache));
+  printf("nvfp4_pool %zu\n", sizeof(nvfp4_pool));
+  F(nvfp4_pool, role) F(nvfp4_pool, head_dim) F(nvfp4_pool, pool) F(nvfp4_pool, tensor_scale)
+  printf("KVQ_ROLE_KEY %d\n", KVQ_ROLE_KEY);
+  printf("KVQ_ROLE_VALUE %d\n", KVQ_ROLE_VALUE);
   F(kivi_cache, k_codes) F(kivi_cache, v_res) F(kivi_cache, groups_cap) F(kivi_cache, n_resid)
   F(kivi_paged_config, num_blocks)
   F(kivi_paged_cache, pool) F(kivi_paged_cache, v_res) F(kivi_paged_cache, block_table)
@@ -233,7 +237,9 @@ def test_struct_layouts_match_the_header(tmp_path):
                                                        text=True).stdout.splitlines())
     want = {"kivi_config": ctypes.sizeof(kvq.kivi_config), "kivi_cache": ctypes.sizeof(kvq.kivi_cache),
             "kivi_paged_config": ctypes.sizeof(kvq.kivi_paged_config),
-            "kivi_paged_cache": ctypes.sizeof(kvq.kivi_paged_cache), "KVQ_PAGED_MAX_SEQS": kvq.PAGED_MAX_SEQS}
+            "kivi_paged_cache": ctypes.sizeof(kvq.kivi_paged_cache), "KVQ_PAGED_MAX_SEQS": kvq.PAGED_MAX_SEQS,
+            "nvfp4_pool": ctypes.sizeof(kvq.nvfp4_pool), "KVQ_ROLE_KEY": kvq.ROLE_KEY,
+            "KVQ_ROLE_VALUE": kvq.ROLE_VALUE}
     for key, val in got.items():
         if "." in key:
             t, m = key.split(".")
@@ -376,3 +382,57 @@ def test_fp8_decode_workspace_holds_the_query():
     for b, hq, d in [(2, 8, 128), (64, 32, 128), (3, 5, 64)]:
         base = kvq.kv_decode_workspace_bytes(kvq.make_config(b, hq, hq, d, 2, 2, 128, 32))
         assert kvq.fp8_decode_workspace_bytes(b, hq, d) == base + -(-b * hq * d // 256) * 256 + 256 + 1024
+
+
+def test_nvfp4_validation():
+    """Host-side checks of the NVFP4 calls: roles, shapes, alignment, workspace;
+    the decode refuses a value pool given as keys (and the reverse)."""
+    assert kvq.nvfp4_pool_bytes(10, 8, 128) == 10 * 8 * 9 * 128
+    assert kvq.nvfp4_pool_bytes(10, 8, 96) == 0
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.nvfp4_pool_init(2, 4, 2, 128, ALIGNED, ALIGNED * 2)
+    assert e.value.name == "KVQ_ERR_ARG"
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.nvfp4_pool_init(kvq.ROLE_KEY, 4, 2, 96, ALIGNED, ALIGNED * 2)
+    assert e.value.name == "KVQ_ERR_UNSUPPORTED"
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.nvfp4_pool_init(kvq.ROLE_KEY, 4, 2, 128, ALIGNED + 16, ALIGNED * 2)
+    assert e.value.name == "KVQ_ERR_ALIGN"
+    k = kvq.nvfp4_pool_init(kvq.ROLE_KEY, 4, 2, 128, ALIGNED, ALIGNED * 2)
+    v = kvq.nvfp4_pool_init(kvq.ROLE_VALUE, 4, 2, 128, ALIGNED * 3, ALIGNED * 4)
+    wsb = kvq.nvfp4_decode_workspace_bytes(2, 4, 128)
+
+    def dec(kk, vv, **kw):
+        args = dict(q=ALIGNED * 5, block_table=ALIGNED * 6, seq_lens=ALIGNED * 7, batch=2, q_heads=4, max_blocks=2,
+                    max_seq_len=32, out=ALIGNED * 8, out_fp32=True, softmax_scale=0.0, ws=ALIGNED * 9, ws_bytes=wsb)
+        args.update(kw)
+        with pytest.raises(kvq.KvqError) as e:
+            kvq.nvfp4_decode_attention(args["q"], kk, vv, args["block_table"], args["seq_lens"], args["batch"],
+                                       args["q_heads"], args["max_blocks"], args["max_seq_len"], args["out"],
+                                       args["out_fp32"], args["softmax_scale"], args["ws"], args["ws_bytes"], stream=0)
+        return e.value.name
+
+    assert dec(v, k) == "KVQ_ERR_ARG"          # roles swapped
+    assert dec(k, k) == "KVQ_ERR_ARG"
+    v2 = kvq.nvfp4_pool_init(kvq.ROLE_VALUE, 5, 2, 128, ALIGNED * 3, ALIGNED * 4)
+    assert dec(k, v2) == "KVQ_ERR_SHAPE"
+    assert dec(k, v, q_heads=3) == "KVQ_ERR_SHAPE"
+    assert dec(k, v, q_heads=18) == "KVQ_ERR_UNSUPPORTED"
+    assert dec(k, v, max_seq_len=33) == "KVQ_ERR_CAPACITY"
+    assert dec(k, v, ws_bytes=wsb - 1) == "KVQ_ERR_WORKSPACE"
+    assert dec(k, v, out=ALIGNED + 4) == "KVQ_ERR_ALIGN"
+
+    def quant(pool, **kw):
+        args = dict(x=ALIGNED * 5, batch=2, seq_len=40, block_table=ALIGNED * 6, max_blocks=3, static_scale=False,
+                    ws=ALIGNED * 7, ws_bytes=kvq.nvfp4_quantize_workspace_bytes())
+        args.update(kw)
+        with pytest.raises(kvq.KvqError) as e:
+            kvq.nvfp4_kv_quantize(pool, args["x"], args["batch"], args["seq_len"], args["block_table"],
+                                  args["max_blocks"], args["static_scale"], args["ws"], args["ws_bytes"], stream=0)
+        return e.value.name
+
+    assert quant(k, max_blocks=2) == "KVQ_ERR_CAPACITY"
+    assert quant(k, ws=None) == "KVQ_ERR_WORKSPACE"
+    assert quant(k, ws_bytes=16) == "KVQ_ERR_WORKSPACE"
+    assert quant(k, x=None) == "KVQ_ERR_NULL"
+    assert quant(k, seq_len=0) == "KVQ_ERR_ARG"
