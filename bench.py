@@ -161,6 +161,22 @@ def aggregate(bytes_local: float, seconds_local: float, world: int):
     return sum_over_ranks(float(bytes_local), world) / t / 1e9, t
 
 
+def timed_window_start(w, warmup: int, steps: int) -> int:
+    """First timed step: after at least `warmup` untimed steps, and early enough
+    that the timed steps cover a residual flush (the appends that find a full
+    window: steps residual, 2 * residual, ... after a prefill that fills it)."""
+    if w.residual <= 0:
+        return warmup
+    flush_steps = range(w.residual, w.decode_steps, w.residual)
+    if any(warmup <= f < warmup + steps for f in flush_steps):
+        return warmup
+    for f in flush_steps:
+        start = max(warmup, f - steps // 2)
+        if start <= f < start + steps and start + steps <= w.decode_steps:
+            return start
+    return warmup
+
+
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
@@ -171,8 +187,8 @@ def run_ours(args, world, rank, local):
     torch.cuda.set_device(local)
     w = workloads.WORKLOADS[args.workload]
     assert isinstance(w, workloads.KiviWorkload), "bench.py times the KIVI streaming workloads"
-    total_steps = args.warmup + args.steps
-    if total_steps > w.decode_steps:
+    first = timed_window_start(w, args.warmup, args.steps)
+    if first + args.steps > w.decode_steps:
         raise SystemExit(f"--warmup + --steps must be <= {w.decode_steps} for {w.name}")
     x = workloads.kivi_inputs(w)   # same seeded data on every rank (weak scaling replicas)
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
@@ -230,9 +246,9 @@ def run_ours(args, world, rank, local):
 
     # --- the decode kernel alone: events around each decode of the same steps ---
     cache.prefill(k_d, v_d)
-    run_steps(0, args.warmup)
+    run_steps(0, first)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    _, _, dec_bytes = run_steps(args.warmup, args.steps, ev)
+    _, _, dec_bytes = run_steps(first, args.steps, ev)
     torch.cuda.synchronize()
     dec_times = [a.elapsed_time(b) / 1e3 for a, b in ev]
     achieved = statistics.mean(db / dt for db, dt in zip(dec_bytes, dec_times)) / 1e9
@@ -240,7 +256,7 @@ def run_ours(args, world, rank, local):
     # --- device-resident timed steps (nothing between the kernels of a step, as a
     # caller runs them: the decode may start while the append's copy finishes) ---
     cache.prefill(k_d, v_d)
-    run_steps(0, args.warmup)
+    run_steps(0, first)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local) if rank == 0 else None
     barrier(world)
@@ -249,8 +265,10 @@ def run_ours(args, world, rank, local):
         clocks.start()
         time.sleep(0.3)
     start.record(stream)
-    nbytes, launches, _ = run_steps(args.warmup, args.steps)
+    g_before = cache.n_grouped
+    nbytes, launches, _ = run_steps(first, args.steps)
     end.record(stream)
+    timed_flushes = (cache.n_grouped - g_before) // w.residual
     torch.cuda.synchronize()
     clk = clocks.stop() if clocks else None
     barrier(world)
@@ -278,7 +296,7 @@ def run_ours(args, world, rank, local):
     ev = lambda: torch.cuda.Event()
     h2d_done, used, d2h_done = ([ev() for _ in range(args.steps)] for _ in range(3))
     cache.prefill(k_d, v_d)
-    run_steps(0, args.warmup)
+    run_steps(0, first)
     barrier(world)
     torch.cuda.synchronize()
     e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -290,7 +308,7 @@ def run_ours(args, world, rank, local):
         if i >= 2:
             up.wait_event(used[i - 2])  # step i - 2 is done with this buffer
         with torch.cuda.stream(up):
-            bufs[i % 2].copy_(step_h[args.warmup + i], non_blocking=True)
+            bufs[i % 2].copy_(step_h[first + i], non_blocking=True)
         h2d_done[i].record(up)
 
     e2e_bytes = 0
@@ -331,12 +349,14 @@ def run_ours(args, world, rank, local):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f32",
+        "dtype": "fp16",
         "data": "synthetic",
         "config": {
             "workload": w.name, "batch": w.batch, "kv_heads": w.kv_heads, "q_heads": w.q_heads,
             "head_dim": w.head_dim, "k_bits": w.k_bits, "v_bits": w.v_bits, "group": 32, "residual": w.residual,
-            "context_start": w.prefill, "steps_from": args.warmup,
+            "context_start": w.prefill, "steps_from": first, "timed_flushes": timed_flushes,
+            "dtypes": {"cache": f"int{w.k_bits}/int{w.v_bits} codes, fp16 scales, zero points and window",
+                       "q": "fp16", "tensor_core_operands": "fp16", "accumulate": "fp32", "out": "fp32"},
             "operands": "2-bit codes as fp16 tensor-core operands, fp32 accumulation",
             "l2": "inputs larger than L2: each step reads ~355 MB of cache against a 129 MB L2",
         },
@@ -409,38 +429,135 @@ def oracle_step(w, x, c, gq, s):
     return metrics.kivi_decode_bytes(1, 1, gq, w.head_dim, w.k_bits, w.v_bits, c.n_grouped, c.n_resid)
 
 
-def cpu_baseline(w, budget_s=15.0):
+def _oracle_worker(conn, w, pair, k, v, q, k_new, v_new):
+    """One host process: the oracle cache of one (batch row, kv head) pair of the
+    workload; runs decode steps on request and answers with their bytes."""
+    from oracle import attention, kivi
+    gq = w.q_heads // w.kv_heads
+    c = kivi.KiviCache(1, 1, w.head_dim, w.k_bits, w.v_bits, w.residual, w.max_tokens)
+    c.prefill(k, v)
+    scale = attention.default_scale(w.head_dim)
+    conn.send("ready")
+    while True:
+        s = conn.recv()
+        if s is None:
+            break
+        if isinstance(s, tuple):  # ("advance", step): the cache state only, no attention (untimed steps)
+            c.append(k_new[s[1]], v_new[s[1]])
+            conn.send(0)
+            continue
+        c.append(k_new[s], v_new[s])
+        kh, vh = c.keys_hat(0, 0), c.values_hat(0, 0)
+        for r in range(gq):
+            attention.softmax_attend(q[s, r], kh, vh, scale)
+        conn.send(metrics.kivi_decode_bytes(1, 1, gq, w.head_dim, w.k_bits, w.v_bits, c.n_grouped, c.n_resid))
+
+
+class OraclePool:
+    """One spawned process per host core (at most one per (batch row, kv head)
+    pair), each holding the oracle cache of its own pair; a step runs the same
+    decode step on every pair at once. Spawned, not forked: the parent may hold
+    a CUDA context."""
+
+    def __init__(self, w, n_proc):
+        import multiprocessing as mp
+        x = workloads.kivi_inputs(w)
+        pairs = [(b, h) for b in range(w.batch) for h in range(w.kv_heads)][:max(1, n_proc)]
+        gq = w.q_heads // w.kv_heads
+        ctx = mp.get_context("spawn")
+        self.conns, self.procs = [], []
+        for b, h in pairs:
+            a, bconn = ctx.Pipe()
+            args = (bconn, w, (b, h), x.k[b:b + 1, h:h + 1].copy(), x.v[b:b + 1, h:h + 1].copy(),
+                    x.q[:, b, h * gq:(h + 1) * gq].copy(), x.k_new[:, b:b + 1, h:h + 1].copy(),
+                    x.v_new[:, b:b + 1, h:h + 1].copy())
+            p = ctx.Process(target=_oracle_worker, args=args, daemon=True)
+            p.start()
+            self.conns.append(a)
+            self.procs.append(p)
+        for cn in self.conns:
+            assert cn.recv() == "ready"
+        self.n = len(self.conns)
+        self.gq = gq
+
+    def step(self, s) -> int:
+        for cn in self.conns:
+            cn.send(s)
+        return sum(cn.recv() for cn in self.conns)
+
+    def advance(self, s) -> None:
+        """Append step s's token on every pair without the attention (untimed steps)."""
+        for cn in self.conns:
+            cn.send(("advance", s))
+        for cn in self.conns:
+            cn.recv()
+
+    def close(self):
+        for cn in self.conns:
+            cn.send(None)
+        for p in self.procs:
+            p.join(timeout=10)
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(w, budget_s=12.0):
+    """The oracle on the host cores: single-threaded on one (batch row, kv head)
+    pair, and one process per core over as many pairs, each for about budget_s."""
     x, c, gq = oracle_sample_setup(w)
     t0 = time.perf_counter()
     nbytes, steps = 0, 0
     while time.perf_counter() - t0 < budget_s and steps < w.decode_steps:
         nbytes += oracle_step(w, x, c, gq, steps)
         steps += 1
+    single = nbytes / (time.perf_counter() - t0) / 1e9
+    del x, c
+    cores = min(host_cores(), w.batch * w.kv_heads)
+    pool = OraclePool(w, cores)
+    t0 = time.perf_counter()
+    nbytes, asteps = 0, 0
+    while time.perf_counter() - t0 < budget_s and asteps < w.decode_steps:
+        nbytes += pool.step(asteps)
+        asteps += 1
     dt = time.perf_counter() - t0
-    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{steps} decode steps of one (batch row, kv head) of {w.name}: append + flush + float64 "
-                      f"dequantize + attention for its {gq} query heads over {c.n_grouped + c.n_resid} tokens"}
+    pool.close()
+    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": pool.n, "kind": "oracle",
+            "sample": f"{asteps} decode steps of {pool.n} (batch row, kv head) pairs of {w.name}, one process per "
+                      f"core: append + flush + float64 dequantize + attention for each pair's {gq} query heads",
+            "single_core": {"value": round(single, 4), "cores": 1,
+                            "sample": f"{steps} decode steps of one pair, single-threaded"}}
 
 
 def run_reference(args, world, rank):
     w = workloads.WORKLOADS[args.workload]
-    x, c, gq = oracle_sample_setup(w)
-    for s in range(args.warmup):
-        oracle_step(w, x, c, gq, s)
+    cores = min(host_cores(), w.batch * w.kv_heads)
+    pool = OraclePool(w, cores)
+    first = timed_window_start(w, args.warmup, args.steps)
+    for s in range(first - args.warmup):
+        pool.advance(s)            # the cache state of the steps before the warm-up window
+    for s in range(first - args.warmup, first):
+        pool.step(s)
     t0 = time.perf_counter()
     nbytes = 0
     for i in range(args.steps):
-        nbytes += oracle_step(w, x, c, gq, args.warmup + i)
+        nbytes += pool.step(first + i)
     dt = time.perf_counter() - t0
+    pool.close()
     value = nbytes / dt / 1e9
-    sample = (f"per step: one (batch row, kv head) of {w.name} — append + flush + float64 dequantize + attention "
-              f"for its {gq} query heads")
+    sample = (f"per step: {pool.n} (batch row, kv head) pairs of {w.name}, one process per core — append + flush + "
+              f"float64 dequantize + attention for each pair's {pool.gq} query heads")
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name},
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": pool.n, "kind": "oracle",
+                         "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -448,8 +565,14 @@ def run_reference(args, world, rank):
 # ---------------------------------------------------------------------------
 # --table: every workload's decode call (and quantize) timed alone
 # ---------------------------------------------------------------------------
-def run_table(args):
-    """One JSON line per workload: trimmed mean time of the decode-attention call over
+TABLE_ALL = (workloads.MHA_4K.name, workloads.GQA_8K_2BIT.name, workloads.GQA_8K_4BIT.name,
+             workloads.STREAM_128K.name, workloads.FP8_32K.name, workloads.FP8_32K_E5M2_PH.name,
+             workloads.FP8_32K_QFP8.name, workloads.NVFP4_32K.name, workloads.PAGED_GQA_8K.name,
+             workloads.PAGED_VAR_16K.name, workloads.PAGED_GQA4_VAR_16K.name)
+
+
+def table_rows(names):
+    """One dict per workload: trimmed mean time of the decode-attention call over
     the prefilled cache (L2 flushed by writing 512 MB between repetitions), its
     algorithmic GB/s and fraction of the HBM peak, and the quantize rate."""
     import torch
@@ -478,10 +601,13 @@ def run_table(args):
         cut = len(ts) // 10
         return statistics.mean(ts[cut:len(ts) - cut])
 
-    names = args.table.split(",") if args.table != "all" else [
-        workloads.MHA_4K.name, workloads.GQA_8K_2BIT.name, workloads.GQA_8K_4BIT.name, workloads.STREAM_128K.name,
-        workloads.FP8_32K.name, workloads.FP8_32K_E5M2_PH.name, workloads.FP8_32K_QFP8.name, workloads.PAGED_GQA_8K.name,
-        workloads.PAGED_VAR_16K.name, workloads.PAGED_GQA4_VAR_16K.name]
+    def row(w, call, t_dec, nbytes, **extra):
+        line = {"workload": w.name, "call": call, "us": round(t_dec * 1e6, 2), "bytes": nbytes,
+                "GB_s": round(nbytes / t_dec / 1e9, 1), "frac": round(nbytes / t_dec / 1e9 / hbm, 4)}
+        line.update(extra)
+        return line
+
+    rows = []
     for name in names:
         w = workloads.WORKLOADS[name]
         if isinstance(w, workloads.PagedKiviWorkload):
@@ -496,12 +622,9 @@ def run_table(args):
             ng = [cache.n_grouped(b) for b in range(w.batch)]
             nr = [cache.n_resid(b) for b in range(w.batch)]
             nbytes = metrics.kivi_paged_decode_bytes(w.kv_heads, w.q_heads, w.head_dim, w.k_bits, w.v_bits, ng, nr)
-            line = {"workload": w.name, "call": "kv_paged_decode_attention", "us": round(t_dec * 1e6, 2),
-                    "bytes": nbytes, "GB_s": round(nbytes / t_dec / 1e9, 1),
-                    "pct_of_hbm_peak": round(100 * nbytes / t_dec / 1e9 / hbm, 1),
-                    "tokens": int(lens.sum()), "prefill_us": round(t_pre * 1e6, 1),
-                    "quantize_tokens_per_s": round(float(lens.sum()) / t_pre, 1),
-                    "status": cache.status()}
+            rows.append(row(w, "kv_paged_decode_attention", t_dec, nbytes, tokens=int(lens.sum()),
+                            prefill_us=round(t_pre * 1e6, 1),
+                            quantize_tokens_per_s=round(float(lens.sum()) / t_pre, 1), status=cache.status()))
             del k_d, v_d, cache
         elif isinstance(w, workloads.KiviWorkload):
             x = workloads.kivi_inputs(w, steps=1)
@@ -513,13 +636,39 @@ def run_table(args):
             t_dec = timed(lambda: cache.decode(q_d, out=out))
             nbytes = metrics.kivi_decode_bytes(w.batch, w.kv_heads, w.q_heads, w.head_dim, w.k_bits, w.v_bits,
                                                cache.n_grouped, cache.n_resid)
-            line = {"workload": w.name, "call": "kv_decode_attention", "us": round(t_dec * 1e6, 2),
-                    "bytes": nbytes, "GB_s": round(nbytes / t_dec / 1e9, 1),
-                    "pct_of_hbm_peak": round(100 * nbytes / t_dec / 1e9 / hbm, 1),
-                    "prefill_us": round(t_pre * 1e6, 1),
-                    "quantize_tokens_per_s": round(w.batch * w.prefill / t_pre, 1),
-                    "status": cache.status()}
+            pre_bytes = metrics.kivi_prefill_bytes(w.batch, w.kv_heads, w.head_dim, w.k_bits, w.v_bits,
+                                                   cache.n_grouped, cache.n_resid)
+            rows.append(row(w, "kv_decode_attention", t_dec, nbytes, prefill_us=round(t_pre * 1e6, 1),
+                            prefill_GB_s=round(pre_bytes / t_pre / 1e9, 1),
+                            prefill_frac=round(pre_bytes / t_pre / 1e9 / hbm, 4),
+                            quantize_tokens_per_s=round(w.batch * w.prefill / t_pre, 1), status=cache.status()))
             del k_d, v_d, cache
+        elif isinstance(w, workloads.Nvfp4Workload):
+            k, v, q, table = workloads.fp8_inputs(w)
+            nb = w.blocks_per_seq
+            tbl = dev(table)
+            pools, t_q = [], []
+            for x16, role in ((k, kvq.ROLE_KEY), (v, kvq.ROLE_VALUE)):
+                xd = dev(x16)
+                p = kvq.Nvfp4Pool(role, w.batch * nb, w.kv_heads, w.head_dim)
+                t_q.append(timed(lambda: p.quantize(xd, tbl, nb), reps=5))
+                pools.append(p)
+                del xd
+            out = torch.empty((w.batch, w.q_heads, w.head_dim), dtype=torch.float32, device="cuda")
+            wsd = kvq.nvfp4_decode_workspace_bytes(w.batch, w.q_heads, w.head_dim)
+            ws = torch.zeros(wsd, dtype=torch.uint8, device="cuda")
+            lens = dev(np.full(w.batch, w.context, np.int32))
+            q_d = dev(q)
+            t_dec = timed(lambda: kvq.nvfp4_decode_attention(q_d, pools[0].desc, pools[1].desc, tbl, lens, w.batch,
+                                                             w.q_heads, nb, w.context, out, True, 0.0, ws, wsd))
+            nbytes = metrics.nvfp4_decode_bytes(w.batch, w.kv_heads, w.q_heads, w.head_dim, w.context, nb)
+            qbytes = metrics.nvfp4_quantize_bytes(w.batch, w.kv_heads, w.context, w.head_dim, True)
+            rows.append(row(w, "nvfp4_decode_attention", t_dec, nbytes,
+                            quantize_us_k_v=[round(t * 1e6, 1) for t in t_q],
+                            quantize_GB_s=round(qbytes / statistics.mean(t_q) / 1e9, 1),
+                            quantize_tokens_per_s=round(w.batch * w.context / statistics.mean(t_q), 1),
+                            status=int(ws[:4].view(torch.int32).item())))
+            del pools
         else:
             k, v, q, table = workloads.fp8_inputs(w)
             nb = w.batch * w.blocks_per_seq
@@ -552,19 +701,38 @@ def run_table(args):
             nbytes = metrics.fp8_decode_bytes(w.batch, w.kv_heads, w.q_heads, w.head_dim, w.context,
                                               w.blocks_per_seq)
             qbytes = metrics.fp8_quantize_bytes(w.batch, w.kv_heads, w.context, w.head_dim, True)
-            line = {"workload": w.name, "call": "fp8_decode_attention", "us": round(t_dec * 1e6, 2),
-                    "bytes": nbytes, "GB_s": round(nbytes / t_dec / 1e9, 1),
-                    "pct_of_hbm_peak": round(100 * nbytes / t_dec / 1e9 / hbm, 1),
-                    "quantize_us_k_v": [round(t * 1e6, 1) for t in t_q],
-                    "quantize_GB_s": round(qbytes / statistics.mean(t_q) / 1e9, 1),
-                    "quantize_tokens_per_s": round(w.batch * w.context / statistics.mean(t_q), 1),
-                    "status": int(ws[:4].view(torch.int32).item())}
+            rows.append(row(w, "fp8_decode_attention", t_dec, nbytes,
+                            quantize_us_k_v=[round(t * 1e6, 1) for t in t_q],
+                            quantize_GB_s=round(qbytes / statistics.mean(t_q) / 1e9, 1),
+                            quantize_tokens_per_s=round(w.batch * w.context / statistics.mean(t_q), 1),
+                            status=int(ws[:4].view(torch.int32).item())))
             del pools
-        print(json.dumps(line), flush=True)
         torch.cuda.empty_cache()
+    del flush
+    torch.cuda.empty_cache()
+    return rows
 
 
-def main():
+def run_table(args):
+    names = TABLE_ALL if args.table == "all" else args.table.split(",")
+    for r in table_rows(names):
+        print(json.dumps(r), flush=True)
+
+
+def launcher_cmd(n_gpus: int, argv, port: int):
+    """The command that runs this script as n_gpus ranks on one node."""
+    return [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n_gpus}",
+            "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__), *argv]
+
+
+def free_port() -> int:
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=128)
@@ -573,25 +741,35 @@ def main():
     ap.add_argument("--workload", default=workloads.STREAM_128K.name, choices=sorted(
         n for n, w in workloads.WORKLOADS.items() if isinstance(w, workloads.KiviWorkload)))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-table", action="store_true", help="leave the per-workload decode table out of the line")
     ap.add_argument("--table", default=None,
                     help="'all' or comma-separated workload names: time each decode call alone instead")
-    args = ap.parse_args()
+    args = ap.parse_args(argv)
     if args.table:
         run_table(args)
-        return
+        return 0
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
+    if args.gpus < 1:
+        raise SystemExit("--gpus must be >= 1")
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        # started without a launcher: run the N ranks under torch.distributed.run
+        return subprocess.call(launcher_cmd(args.gpus, sys.argv[1:] if argv is None else argv, free_port()))
     world, rank, local = dist_setup()
+    if world != args.gpus:
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={world}: launch one rank per GPU")
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(run_reference(args, world, rank)), flush=True)
-        return
+        return 0
     if world > 1:
         import torch
         import torch.distributed as dist
         torch.cuda.set_device(local)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     res = run_ours(args, world, rank, local)
+    if rank == 0 and world == 1 and not args.no_table:
+        res["table"] = {r.pop("workload"): r for r in table_rows(TABLE_ALL)}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(workloads.WORKLOADS[args.workload])
     if rank == 0:
@@ -599,7 +777,8 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+    return 0
 
 
 if __name__ == "__main__":
-    main()
+    sys.exit(main())

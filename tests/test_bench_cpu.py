@@ -62,3 +62,31 @@ def test_paged_decode_bytes_are_the_sequences_sum():
     total = metrics.kivi_paged_decode_bytes(8, 32, 128, 2, 2, ng, nr)
     want = sum(metrics.kivi_decode_bytes(1, 8, 32, 128, 2, 2, g, r) + 4 * (g // 32) for g, r in zip(ng, nr))
     assert total == want
+
+
+def test_gpus_that_disagree_with_the_launcher_are_refused():
+    env = dict(os.environ, WORLD_SIZE="1", RANK="0", LOCAL_RANK="0")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2", "--steps", "3"], cwd=ROOT,
+                       capture_output=True, text=True, timeout=120, env=env)
+    assert r.returncode != 0
+    assert "--gpus 2 but WORLD_SIZE=1" in r.stderr
+
+
+def test_gpus_without_a_launcher_runs_one_rank_per_gpu():
+    sys.path.insert(0, ROOT)
+    import bench
+    cmd = bench.launcher_cmd(4, ["--gpus", "4", "--steps", "7"], 29511)
+    assert cmd[1:3] == ["-m", "torch.distributed.run"]
+    assert "--nproc-per-node=4" in cmd and "--nnodes=1" in cmd
+    assert cmd[cmd.index("--master-addr") + 1] == "127.0.0.1" and cmd[cmd.index("--master-port") + 1] == "29511"
+    assert cmd[-4:] == ["--gpus", "4", "--steps", "7"] and cmd[-5].endswith("bench.py")
+
+
+@pytest.mark.parametrize("warmup,steps", [(3, 128), (5, 20), (3, 3), (200, 10), (3, 300)])
+def test_timed_steps_cover_a_residual_flush(warmup, steps):
+    sys.path.insert(0, ROOT)
+    import bench
+    w = workloads.STREAM_128K
+    first = bench.timed_window_start(w, warmup, steps)
+    assert first >= warmup and first + steps <= w.decode_steps
+    assert any(first <= f < first + steps for f in range(w.residual, w.decode_steps, w.residual))
