@@ -671,35 +671,25 @@ def table_rows(names):
             del pools
         else:
             k, v, q, table = workloads.fp8_inputs(w)
-            nb = w.batch * w.blocks_per_seq
-            pools, scales = [], []
-            wsb = kvq.fp8_quantize_workspace_bytes(w.batch, w.kv_heads, w.context, w.head_dim)
-            wsq = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
-            t_q = []
+            nb = w.blocks_per_seq
             tbl = dev(table)
-            for x16, vl in ((k, 2 if w.q_fp8 else 0), (v, 1)):
+            pools, t_q = [], []
+            for x16, role in ((k, kvq.ROLE_KEY), (v, kvq.ROLE_VALUE)):
                 xd = dev(x16)
-                pool = torch.empty((nb, w.kv_heads, 16 * w.head_dim), dtype=torch.uint8, device="cuda")
-                sc = torch.zeros(w.kv_heads if w.per_head else 1, dtype=torch.float32, device="cuda")
-                t_q.append(timed(lambda: kvq.fp8_kv_quantize(xd, w.batch, w.kv_heads, w.context, w.head_dim, tbl,
-                                                             w.blocks_per_seq, 16, nb, pool, sc, False, vl, wsq,
-                                                             wsb, per_head=w.per_head,
-                                                             fp8_format=kvq.FP8_FORMATS[w.fmt]), reps=5))
-                pools.append(pool)
-                scales.append(sc)
+                p = kvq.Fp8Pool(role, w.batch * nb, w.kv_heads, w.head_dim, fp8_format=kvq.FP8_FORMATS[w.fmt],
+                                per_head=w.per_head)
+                t_q.append(timed(lambda: p.quantize(xd, tbl, nb), reps=5))
+                pools.append(p)
                 del xd
             out = torch.empty((w.batch, w.q_heads, w.head_dim), dtype=torch.float32, device="cuda")
             wsd = kvq.fp8_decode_workspace_bytes(w.batch, w.q_heads, w.head_dim)
             ws = torch.zeros(wsd, dtype=torch.uint8, device="cuda")
             lens = dev(np.full(w.batch, w.context, np.int32))
             q_d = dev(q)
-            t_dec = timed(lambda: kvq.fp8_decode_attention(q_d, pools[0], pools[1], scales[0], scales[1], tbl, lens,
-                                                           w.batch, w.q_heads, w.kv_heads, w.head_dim, 16,
-                                                           w.blocks_per_seq, nb, w.context, out, True, 0.0, ws,
-                                                           wsd, per_head=w.per_head,
-                                                           fp8_format=kvq.FP8_FORMATS[w.fmt], q_fp8=w.q_fp8))
-            nbytes = metrics.fp8_decode_bytes(w.batch, w.kv_heads, w.q_heads, w.head_dim, w.context,
-                                              w.blocks_per_seq)
+            t_dec = timed(lambda: kvq.fp8_decode_attention(q_d, pools[0].desc, pools[1].desc, tbl, lens, w.batch,
+                                                           w.q_heads, nb, w.context, out, True, 0.0, ws, wsd,
+                                                           q_fp8=w.q_fp8))
+            nbytes = metrics.fp8_decode_bytes(w.batch, w.kv_heads, w.q_heads, w.head_dim, w.context, nb)
             qbytes = metrics.fp8_quantize_bytes(w.batch, w.kv_heads, w.context, w.head_dim, True)
             rows.append(row(w, "fp8_decode_attention", t_dec, nbytes,
                             quantize_us_k_v=[round(t * 1e6, 1) for t in t_q],

@@ -305,53 +305,69 @@ KVQ_API kvq_status kv_paged_decode_attention(const kivi_paged_cache* cache, cons
 /* FP8 E4M3 paged cache [KIVI section 5, CSDN section 10, YUN]               */
 /* ------------------------------------------------------------------------ */
 
+/* Roles of a paged pool: the library fixes each role's in-block byte order;
+ * the decode calls take one pool of each and refuse them swapped. */
+#define KVQ_ROLE_KEY 0
+#define KVQ_ROLE_VALUE 1
+
 /* E4M3: 1 sign, 4 exponent (bias 7), 3 mantissa bits; largest finite 448.
  * Encoding rounds to nearest even; magnitudes >= 448 (and infinities)
- * saturate to +-448; NaN encodes as 0x7F.
+ * saturate to +-448; NaN encodes as 0x7F. E5M2 ([CSDN] section 18.4): 1 sign,
+ * 5 exponent bits (bias 15), 2 mantissa bits; largest finite 57344; round to
+ * nearest even, saturating to +-57344, NaN -> 0x7F.
  *
- * Pool layout: pool[num_blocks, H_kv, block_size * D] bytes; logical token t
- * of sequence b lives in physical block block_table[b * max_blocks + t/bs],
- * row t % bs ([CSDN] section 13). Within one (block, kv head), block_size must
- * be 16 and the 16*D bytes are stored in mma.sync fragment order (lane =
- * 4*g + tig, D/2 bytes per lane; byte p of lane l's stream is stored at byte
- * ((p/16)*32 + l)*16 + p%16):
- *   keys   (value_layout = 0): byte pair i = (nt*(D/16) + ks)*2 + r of a lane
- *          holds channels d0 = 16*ks + 8*r + 2*tig, d0+1 of token 8*nt + g
- *          (nt < 2);
- *   values (value_layout = 1): byte pair i = nt*2 + r holds tokens
- *          t0 = 8*r + 2*tig, t0+1 of channel 8*nt + g (nt < D/8).
+ * Pool layout: pool[num_blocks, H_kv, 16 * D] bytes; logical token t of
+ * sequence b lives in physical block block_table[b * max_blocks + t/16], row
+ * t % 16 ([CSDN] section 13). Within one (block, kv head) the 16*D bytes are
+ * stored in tensor-core fragment order (lane = 4*g + tig, D/2 bytes per lane;
+ * byte p of lane l's stream is stored at byte ((p/16)*32 + l)*16 + p%16):
+ *   KVQ_ROLE_KEY   : 4-byte word w = (nt*(D/32) + kk)*2 + r of a lane holds
+ *                    channels 32*kk + 16*r + 4*tig .. +3 of token 8*nt + g
+ *                    (nt < 2): the B fragments of mma.sync m16n8k32 (FP8
+ *                    operands), and, with the query's channels permuted
+ *                    alike, those of m16n8k16 after an exact fp16 conversion;
+ *   KVQ_ROLE_VALUE : byte pair i = nt*2 + r of a lane holds tokens
+ *                    t0 = 8*r + 2*tig, t0+1 of channel 8*nt + g (nt < D/8).
  * Rows of a block past the end of the sequence are written as zero bytes. */
+
+/* Host-side descriptor of one FP8 pool (device memory owned by the caller). */
+typedef struct {
+  int32_t role;        /* KVQ_ROLE_KEY or KVQ_ROLE_VALUE: fixes the in-block order */
+  int32_t fp8_format;  /* 0 = E4M3 (FMAX 448), 1 = E5M2 (FMAX 57344)                */
+  int32_t per_head;    /* 0: one scale for the tensor; 1: one per kv head [CSDN 10.1] */
+  int32_t num_blocks;
+  int32_t kv_heads;
+  int32_t head_dim;    /* 64 or 128 */
+  uint8_t* pool;       /* device [num_blocks, kv_heads, 16 * head_dim]              */
+  float* scale;        /* device float32 [1] (per_head == 0) or [kv_heads]           */
+} fp8_pool;
+
+/* Bytes of the pool buffer for this shape (0 if the shape is invalid). */
+KVQ_API size_t fp8_pool_bytes(int32_t num_blocks, int32_t kv_heads, int32_t head_dim);
+
+/* Fill a descriptor; no device work. KVQ_ERR_ARG for a role, fp8_format or
+ * per_head out of range or num_blocks, kv_heads <= 0; KVQ_ERR_UNSUPPORTED for
+ * head_dim other than 64, 128. */
+KVQ_API kvq_status fp8_pool_init(fp8_pool* pool, int32_t role, int32_t fp8_format, int32_t per_head,
+                                 int32_t num_blocks, int32_t kv_heads, int32_t head_dim, void* buf, float* scale);
 
 /* Workspace of fp8_kv_quantize: per-block amax partials (4096 words, for one
  * scale or split between the per-head scales). */
 KVQ_API size_t fp8_quantize_workspace_bytes(int32_t batch, int32_t kv_heads, int32_t seq_len, int32_t head_dim);
 
-/* Quantize one tensor (K or V) of one layer into the paged pool.
- *   x           : device fp16 [B, H_kv, seq_len, D]
- *   block_table : device int32 [B, max_blocks]; entries < num_blocks
- *   pool        : device uint8 [num_blocks, H_kv, 16*D]
- *   scale       : device float32: one value (per_head == 0) or one per kv head
- *                 [H_kv] (per_head == 1, [CSDN] section 10.1). static_scale == 0:
- *                 written with fl32(amax/FMAX), amax = max|x| over the whole
- *                 tensor (or over kv head h's slice for scale[h]), scale 1 where
- *                 amax == 0 [YUN]; static_scale != 0: read as given (e.g. 1.0,
- *                 the no-calibration route of [KIVI] section 6.1).
- *   fp8_format  : 0 = E4M3 (FMAX 448), 1 = E5M2 (1 sign, 5 exponent bits with
- *                 bias 15, 2 mantissa bits; FMAX 57344; [CSDN] section 18.4;
- *                 round to nearest even, saturating to +-57344, NaN -> 0x7F)
- *   value_layout: 0 for keys, 1 for values (the in-block order above), 2 for
- *                 keys read by FP8 tensor cores (fp8_decode_attention with
- *                 q_fp8 = 1): 4-byte word w = (nt*(D/32) + kk)*2 + r of lane
- *                 (g, tig) holds channels 32*kk + 16*r + 4*tig .. +3 of token
- *                 8*nt + g (nt < 2), the B fragments of mma.sync m16n8k32
- * byte = FP8(fl32(x / scale)). Block-table entries outside [0, num_blocks)
- * are skipped (nothing is written for that block). per_head and fp8_format
- * outside {0, 1} return KVQ_ERR_ARG. */
-KVQ_API kvq_status fp8_kv_quantize(const uint16_t* x, int32_t batch, int32_t kv_heads, int32_t seq_len,
-                           int32_t head_dim, const int32_t* block_table, int32_t max_blocks,
-                           int32_t block_size, int32_t num_blocks, uint8_t* pool, float* scale,
-                           int32_t static_scale, int32_t per_head, int32_t fp8_format,
-                           int32_t value_layout, void* ws, size_t ws_bytes, void* stream);
+/* Quantize one tensor (K or V, as the pool's role says) of one layer into the pool.
+ *   x           : device fp16 [B, kv_heads, seq_len, D]
+ *   block_table : device int32 [B, max_blocks]; blocks whose entry lies
+ *                 outside [0, num_blocks) are skipped (nothing written)
+ *   static_scale: 0: the pool's scale is written with fl32(amax/FMAX), amax =
+ *                 max|x| over the whole tensor (or over kv head h's slice for
+ *                 scale[h]), scale 1 where amax == 0 [YUN]; 1: the scale is
+ *                 read as given (e.g. 1.0, the no-calibration route of [KIVI]
+ *                 section 6.1).
+ * byte = FP8(fl32(x / scale)). KVQ_ERR_CAPACITY if ceil(seq_len/16) > max_blocks. */
+KVQ_API kvq_status fp8_kv_quantize(const fp8_pool* pool, const uint16_t* x, int32_t batch, int32_t seq_len,
+                                   const int32_t* block_table, int32_t max_blocks, int32_t static_scale, void* ws,
+                                   size_t ws_bytes, void* stream);
 
 /* Workspace of fp8_decode_attention: the layout of kv_decode_workspace_bytes
  * (status word, split counters, partials) for this batch and q_heads, then, at
@@ -364,32 +380,28 @@ KVQ_API size_t fp8_decode_workspace_bytes(int32_t batch, int32_t q_heads, int32_
 /* Decode attention over the FP8 paged cache:
  *   out[b, hq] = softmax(q . (k_scale * K)^T * softmax_scale) (v_scale * V)
  * over tokens 0 .. seq_lens[b]-1 of kv head hq / (H_q/H_kv).
+ *   k, v     : a KVQ_ROLE_KEY and a KVQ_ROLE_VALUE pool of the same shape,
+ *              format and scale granularity (KVQ_ERR_ARG for swapped roles or
+ *              different formats or granularities, KVQ_ERR_SHAPE for shapes)
  *   q        : device fp16 [B, H_q, D];  out: device [B, H_q, D] (fp32 or fp16)
- *   k_pool, v_pool : pools written by fp8_kv_quantize (value_layout 0 and 1)
- *   k_scale, v_scale : device float32, one value each (per_head == 0) or one
- *              per kv head [H_kv] (per_head == 1), as fp8_kv_quantize wrote them
- *   fp8_format : the pools' format, 0 = E4M3, 1 = E5M2
  *   q_fp8    : 0: q stays fp16 (scores from q and the exactly converted keys);
  *              1: FP8-domain attention ([CSDN] section 18.7: with FP8 KV and
  *              FlashAttention-3 the query is quantized too): q is quantized to
  *              E4M3 with the per-tensor dynamic scale q_scale = fl32(amax_q /
  *              448) over the whole q (1 if q is all zeros), byte =
  *              E4M3(fl32(q / q_scale)), and the scores are (E4M3 q) . (FP8 k)
- *              * q_scale * k_scale on FP8 tensor cores; the key pool must then
- *              hold value_layout 2. The softmax weights stay fp32 for p.V.
+ *              * q_scale * k_scale on FP8 tensor cores. The softmax weights
+ *              stay fp32 for p.V.
  *   seq_lens : device int32 [B], each in [1, max_seq_len]
  * The host passes max_seq_len >= every seq_lens[b] (it sizes the grid) and
  * max_seq_len <= max_blocks*16. Block-table entries must lie in
  * [0, num_blocks); the kernels clamp them (and seq_lens) so that a bad table
  * gives wrong numbers but never an access outside the pool or the table. */
-KVQ_API kvq_status fp8_decode_attention(const uint16_t* q, const uint8_t* k_pool, const uint8_t* v_pool,
-                                const float* k_scale, const float* v_scale, int32_t per_head,
-                                int32_t fp8_format, int32_t q_fp8, const int32_t* block_table,
-                                const int32_t* seq_lens,
-                                int32_t batch, int32_t q_heads, int32_t kv_heads, int32_t head_dim,
-                                int32_t block_size, int32_t max_blocks, int32_t num_blocks,
-                                int32_t max_seq_len, void* out, int32_t out_fp32,
-                                float softmax_scale, void* ws, size_t ws_bytes, void* stream);
+KVQ_API kvq_status fp8_decode_attention(const uint16_t* q, const fp8_pool* k, const fp8_pool* v, int32_t q_fp8,
+                                        const int32_t* block_table, const int32_t* seq_lens, int32_t batch,
+                                        int32_t q_heads, int32_t max_blocks, int32_t max_seq_len, void* out,
+                                        int32_t out_fp32, float softmax_scale, void* ws, size_t ws_bytes,
+                                        void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* NVFP4 paged cache [CSDN sections 21.2, 21.3, 13]                          */
@@ -428,10 +440,7 @@ KVQ_API kvq_status fp8_decode_attention(const uint16_t* q, const uint8_t* k_pool
  * (These are the m16n8k16 operand fragments of q.k^T and p.V, with each
  * lane's block scales next to each other.) Rows past the end of a sequence
  * hold zero codes and zero scales. */
-#define KVQ_ROLE_KEY 0
-#define KVQ_ROLE_VALUE 1
-
-/* Host-side descriptor of one pool (device memory owned by the caller). */
+/* Host-side descriptor of one NVFP4 pool (device memory owned by the caller). */
 typedef struct {
   int32_t role;        /* KVQ_ROLE_KEY or KVQ_ROLE_VALUE: fixes the in-block order */
   int32_t num_blocks;

@@ -767,20 +767,58 @@ size_t fp8_quantize_workspace_bytes(int32_t batch, int32_t kv_heads, int32_t seq
   return static_cast<size_t>(kAmaxBlocksMax) * sizeof(uint32_t);
 }
 
-kvq_status fp8_kv_quantize(const uint16_t* x, int32_t batch, int32_t kv_heads, int32_t seq_len, int32_t head_dim,
-                           const int32_t* block_table, int32_t max_blocks, int32_t block_size, int32_t num_blocks,
-                           uint8_t* pool, float* scale, int32_t static_scale, int32_t per_head, int32_t fp8_format,
-                           int32_t value_layout, void* ws, size_t ws_bytes, void* stream) {
-  if (x == nullptr || block_table == nullptr || pool == nullptr || scale == nullptr) return KVQ_ERR_NULL;
-  if (batch <= 0 || kv_heads <= 0 || seq_len <= 0 || num_blocks <= 0 || max_blocks <= 0) return KVQ_ERR_ARG;
-  if (head_dim != 64 && head_dim != 128) return KVQ_ERR_UNSUPPORTED;
-  if (block_size != 16) return KVQ_ERR_UNSUPPORTED;
-  if (value_layout < 0 || value_layout > 2) return KVQ_ERR_ARG;
-  if (per_head != 0 && per_head != 1) return KVQ_ERR_ARG;
+size_t fp8_pool_bytes(int32_t num_blocks, int32_t kv_heads, int32_t head_dim) {
+  if (num_blocks <= 0 || kv_heads <= 0 || (head_dim != 64 && head_dim != 128)) return 0;
+  return static_cast<size_t>(num_blocks) * kv_heads * 16 * head_dim;
+}
+
+kvq_status fp8_pool_init(fp8_pool* pool, int32_t role, int32_t fp8_format, int32_t per_head, int32_t num_blocks,
+                         int32_t kv_heads, int32_t head_dim, void* buf, float* scale) {
+  if (pool == nullptr || buf == nullptr || scale == nullptr) return KVQ_ERR_NULL;
+  if (role != KVQ_ROLE_KEY && role != KVQ_ROLE_VALUE) return KVQ_ERR_ARG;
   if (fp8_format != 0 && fp8_format != 1) return KVQ_ERR_ARG;
-  if (per_head && kv_heads > kAmaxBlocksMax) return KVQ_ERR_UNSUPPORTED;
-  if (ceil_div(seq_len, block_size) > max_blocks) return KVQ_ERR_CAPACITY;
-  if (!aligned(x) || !aligned(block_table) || !aligned(pool) || !aligned(scale)) return KVQ_ERR_ALIGN;
+  if (per_head != 0 && per_head != 1) return KVQ_ERR_ARG;
+  if (num_blocks <= 0 || kv_heads <= 0) return KVQ_ERR_ARG;
+  if (head_dim != 64 && head_dim != 128) return KVQ_ERR_UNSUPPORTED;
+  if (!aligned(buf) || !aligned(scale)) return KVQ_ERR_ALIGN;
+  fp8_pool p{};
+  p.role = role;
+  p.fp8_format = fp8_format;
+  p.per_head = per_head;
+  p.num_blocks = num_blocks;
+  p.kv_heads = kv_heads;
+  p.head_dim = head_dim;
+  p.pool = static_cast<uint8_t*>(buf);
+  p.scale = scale;
+  *pool = p;
+  return KVQ_OK;
+}
+
+namespace {
+kvq_status check_fp8_pool(const fp8_pool* p) {
+  if (p == nullptr || p->pool == nullptr || p->scale == nullptr) return KVQ_ERR_NULL;
+  if (p->role != KVQ_ROLE_KEY && p->role != KVQ_ROLE_VALUE) return KVQ_ERR_ARG;
+  if (p->fp8_format != 0 && p->fp8_format != 1) return KVQ_ERR_ARG;
+  if (p->per_head != 0 && p->per_head != 1) return KVQ_ERR_ARG;
+  if (p->num_blocks <= 0 || p->kv_heads <= 0) return KVQ_ERR_ARG;
+  if (p->head_dim != 64 && p->head_dim != 128) return KVQ_ERR_UNSUPPORTED;
+  if (!aligned(p->pool) || !aligned(p->scale)) return KVQ_ERR_ALIGN;
+  return KVQ_OK;
+}
+}  // namespace
+
+kvq_status fp8_kv_quantize(const fp8_pool* pool, const uint16_t* x, int32_t batch, int32_t seq_len,
+                           const int32_t* block_table, int32_t max_blocks, int32_t static_scale, void* ws,
+                           size_t ws_bytes, void* stream) {
+  const kvq_status st = check_fp8_pool(pool);
+  if (st != KVQ_OK) return st;
+  if (x == nullptr || block_table == nullptr) return KVQ_ERR_NULL;
+  if (batch <= 0 || seq_len <= 0 || max_blocks <= 0) return KVQ_ERR_ARG;
+  if (static_scale != 0 && static_scale != 1) return KVQ_ERR_ARG;
+  const int kv_heads = pool->kv_heads, head_dim = pool->head_dim;
+  if (pool->per_head && kv_heads > kAmaxBlocksMax) return KVQ_ERR_UNSUPPORTED;
+  if (ceil_div(seq_len, 16) > max_blocks) return KVQ_ERR_CAPACITY;
+  if (!aligned(x) || !aligned(block_table)) return KVQ_ERR_ALIGN;
   if (!static_scale) {
     if (ws == nullptr) return KVQ_ERR_WORKSPACE;
     if (!aligned(ws)) return KVQ_ERR_ALIGN;
@@ -794,18 +832,19 @@ kvq_status fp8_kv_quantize(const uint16_t* x, int32_t batch, int32_t kv_heads, i
   a.head_dim = head_dim;
   a.block_table = block_table;
   a.max_blocks = max_blocks;
-  a.num_blocks = num_blocks;
-  a.pool = pool;
-  a.scale = scale;
+  a.num_blocks = pool->num_blocks;
+  a.pool = pool->pool;
+  a.scale = pool->scale;
   a.static_scale = static_scale;
-  a.per_head = per_head;
-  a.fmt = fp8_format;
-  a.value_layout = value_layout;
+  a.per_head = pool->per_head;
+  a.fmt = pool->fp8_format;
+  // keys in the m16n8k32 order (read by both decode paths), values in p.V's
+  a.value_layout = (pool->role == KVQ_ROLE_KEY) ? 2 : 1;
   a.amax_partials = static_cast<uint32_t*>(ws);
   // amax blocks per scale: the partials of all scales fit the workspace, and
   // about 8 blocks per SM run in all
-  const int n_scales = per_head ? kv_heads : 1;
-  const long long n_vec = static_cast<long long>(batch) * seq_len * head_dim / 8 * (per_head ? 1 : kv_heads);
+  const int n_scales = pool->per_head ? kv_heads : 1;
+  const long long n_vec = static_cast<long long>(batch) * seq_len * head_dim / 8 * (pool->per_head ? 1 : kv_heads);
   a.amax_blocks = static_cast<int>(std::max<long long>(
       1, std::min<long long>({static_cast<long long>(kAmaxBlocksMax / n_scales),
                               (8LL * kvq::device_sm_count() + n_scales - 1) / n_scales, (n_vec + 255) / 256})));
@@ -829,32 +868,36 @@ size_t fp8_decode_workspace_bytes(int32_t batch, int32_t q_heads, int32_t head_d
   return fp8_decode_ws_bytes(batch, q_heads, head_dim);
 }
 
-kvq_status fp8_decode_attention(const uint16_t* q, const uint8_t* k_pool, const uint8_t* v_pool, const float* k_scale,
-                                const float* v_scale, int32_t per_head, int32_t fp8_format, int32_t q_fp8,
-                                const int32_t* block_table, const int32_t* seq_lens,
-                                int32_t batch, int32_t q_heads, int32_t kv_heads, int32_t head_dim, int32_t block_size,
-                                int32_t max_blocks, int32_t num_blocks, int32_t max_seq_len, void* out,
-                                int32_t out_fp32, float softmax_scale, void* ws, size_t ws_bytes, void* stream) {
-  if (!q || !k_pool || !v_pool || !k_scale || !v_scale || !block_table || !seq_lens || !out) return KVQ_ERR_NULL;
-  if (batch <= 0 || q_heads <= 0 || kv_heads <= 0 || max_blocks <= 0 || num_blocks <= 0 || max_seq_len <= 0)
-    return KVQ_ERR_ARG;
-  if (per_head != 0 && per_head != 1) return KVQ_ERR_ARG;
-  if (fp8_format != 0 && fp8_format != 1) return KVQ_ERR_ARG;
+kvq_status fp8_decode_attention(const uint16_t* q, const fp8_pool* k, const fp8_pool* v, int32_t q_fp8,
+                                const int32_t* block_table, const int32_t* seq_lens, int32_t batch, int32_t q_heads,
+                                int32_t max_blocks, int32_t max_seq_len, void* out, int32_t out_fp32,
+                                float softmax_scale, void* ws, size_t ws_bytes, void* stream) {
+  kvq_status st = check_fp8_pool(k);
+  if (st != KVQ_OK) return st;
+  st = check_fp8_pool(v);
+  if (st != KVQ_OK) return st;
+  if (k->role != KVQ_ROLE_KEY || v->role != KVQ_ROLE_VALUE) return KVQ_ERR_ARG;
+  if (k->fp8_format != v->fp8_format || k->per_head != v->per_head) return KVQ_ERR_ARG;
+  if (k->num_blocks != v->num_blocks || k->kv_heads != v->kv_heads || k->head_dim != v->head_dim) return KVQ_ERR_SHAPE;
+  if (!q || !block_table || !seq_lens || !out) return KVQ_ERR_NULL;
+  if (batch <= 0 || q_heads <= 0 || max_blocks <= 0 || max_seq_len <= 0) return KVQ_ERR_ARG;
   if (q_fp8 != 0 && q_fp8 != 1) return KVQ_ERR_ARG;
+  const int kv_heads = k->kv_heads, head_dim = k->head_dim, block_size = 16;
   if (batch > 65535 || kv_heads > 65535) return KVQ_ERR_UNSUPPORTED;
-  if (head_dim != 64 && head_dim != 128) return KVQ_ERR_UNSUPPORTED;
-  if (block_size != 16) return KVQ_ERR_UNSUPPORTED;
   if (q_heads % kv_heads != 0) return KVQ_ERR_SHAPE;
   if (q_heads / kv_heads > kvq::kMaxGqa) return KVQ_ERR_UNSUPPORTED;
   if (max_seq_len > max_blocks * block_size) return KVQ_ERR_CAPACITY;
-  if (!aligned(q) || !aligned(k_pool) || !aligned(v_pool) || !aligned(k_scale) || !aligned(v_scale) ||
-      !aligned(block_table) || !aligned(seq_lens) || !aligned(out))
-    return KVQ_ERR_ALIGN;
+  if (!aligned(q) || !aligned(block_table) || !aligned(seq_lens) || !aligned(out)) return KVQ_ERR_ALIGN;
   if (ws == nullptr) return KVQ_ERR_WORKSPACE;
   if (!aligned(ws)) return KVQ_ERR_ALIGN;
   if (ws_bytes < fp8_decode_ws_bytes(batch, q_heads, head_dim)) return KVQ_ERR_WORKSPACE;
   if (!(softmax_scale == softmax_scale) || std::isinf(softmax_scale)) return KVQ_ERR_ARG;
   const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(head_dim));
+  const int num_blocks = k->num_blocks, per_head = k->per_head, fp8_format = k->fp8_format;
+  const uint8_t* const k_pool = k->pool;
+  const uint8_t* const v_pool = v->pool;
+  const float* const k_scale = k->scale;
+  const float* const v_scale = v->scale;
   const int nblk = ceil_div(max_seq_len, block_size);
   uint8_t* const q_area = static_cast<uint8_t*>(ws) + decode_ws_bytes(batch, q_heads, head_dim);
   uint8_t* const q8 = q_area;

@@ -305,9 +305,10 @@ __global__ void __launch_bounds__(256) fp8_query_cast_kernel(Fp8QueryArgs a) {
 // Grid (splits, H_kv, B), 4 warps; warp w of block x takes logical blocks
 // x*bps + w, x*bps + w + 4, ... through a ring of STAGES stages (K block and
 // V block of one kv head, 16*D bytes each) filled by bulk copies.
-//   q.k^T : A = q (fp16, exact), B = E4M3 keys converted to fp16 (exact);
+//   q.k^T : A = q (fp16, exact, channels permuted as the keys' order), B =
+//           FP8 keys converted to fp16 (exact);
 //           with QF (FP8-domain attention) A = the E4M3 query bytes and B =
-//           the key bytes as stored (value_layout 2), on the FP8 tensor path
+//           the key bytes as stored (the keys' order is the m16n8k32 one), on the FP8 tensor path
 //           (m16n8k32), scores scaled by q_scale * k_scale.
 //   p.V   : A = p split into fp16 hi + lo rows, B = E4M3 values as fp16.
 // ---------------------------------------------------------------------------
@@ -422,11 +423,17 @@ __global__ void __launch_bounds__(128) fp8_decode_kernel(Fp8DecodeArgs a) {
       for (int jj = 0; jj < 2; ++jj)
         qa[kk][jj] = row_ok ? *reinterpret_cast<const uint32_t*>(q8row + 32 * kk + 16 * jj + 4 * tig) : 0u;
   } else {
+    // The keys are stored in the m16n8k32 order (4 consecutive channels
+    // 16ks + 4tig .. +3 per word). A dot product does not depend on the order
+    // of its terms, so k-step ks pairs its K rows with channels permuted
+    // alike on both sides: rows 2tig, 2tig + 1 <-> channels 16ks + 4tig, +1
+    // (b0 = bytes 0-1 of the word, a0), rows 2tig + 8, + 9 <-> channels
+    // 16ks + 4tig + 2, + 3 (b1 = bytes 2-3, a2).
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks)
 #pragma unroll
       for (int jj = 0; jj < 2; ++jj)
-        qa[ks][jj] = row_ok ? *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8 * jj + 2 * tig) : 0u;
+        qa[ks][jj] = row_ok ? *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 4 * tig + 2 * jj) : 0u;
   }
   const float kmul = a.k_scale[a.per_head ? h : 0] * a.scale_log2 * (QF ? *a.q_scale : 1.0f);
   const float vscale = a.v_scale[a.per_head ? h : 0];
@@ -450,7 +457,7 @@ __global__ void __launch_bounds__(128) fp8_decode_kernel(Fp8DecodeArgs a) {
     const uint4* vb = reinterpret_cast<const uint4*>(ring + s * S::STAGE + kBlock * D);
     const int tok_base = (j_begin + warp + 4 * j) * kBlock;
 
-    // keys: lane's stream word wi = nt*KS + ks holds (r = 0, r = 1) byte pairs
+    // keys: lane stream word nt*KS + ks holds channels 16ks + 4tig .. +3 of token 8nt + g
     uint32_t kw[2 * KS];
 #pragma unroll
     for (int c = 0; c < CH; ++c) {
@@ -465,7 +472,7 @@ __global__ void __launch_bounds__(128) fp8_decode_kernel(Fp8DecodeArgs a) {
     for (int nt = 0; nt < 2; ++nt) {
       sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.0f;
       if constexpr (QF) {
-        // value_layout 2: words (nt * (D/32) + kk) * 2 + {0, 1} are this lane's B fragment
+        // words (nt * (D/32) + kk) * 2 + {0, 1} are this lane's m16n8k32 B fragment
 #pragma unroll
         for (int kk = 0; kk < QW; ++kk)
           mma_fp8_16832<FMT>(sacc[nt], qa[kk][0], 0u, qa[kk][1], 0u, kw[(nt * QW + kk) * 2],

@@ -29,7 +29,7 @@ EXPORTED = (
     "kv_flush_residual", "kv_decode_workspace_bytes", "kv_decode_attention", "kv_decode_attention_noalloc",
     "kivi_paged_cache_sizes", "kivi_paged_cache_init", "kv_paged_prefill", "kv_paged_append", "kv_paged_flush",
     "kv_paged_decode_workspace_bytes", "kv_paged_decode_attention",
-    "fp8_quantize_workspace_bytes",
+    "fp8_pool_bytes", "fp8_pool_init", "fp8_quantize_workspace_bytes",
     "fp8_kv_quantize", "fp8_decode_workspace_bytes", "fp8_decode_attention",
     "nvfp4_pool_bytes", "nvfp4_pool_init", "nvfp4_quantize_workspace_bytes", "nvfp4_kv_quantize",
     "nvfp4_decode_workspace_bytes", "nvfp4_decode_attention",
@@ -80,7 +80,13 @@ class nvfp4_pool(ctypes.Structure):
                 ("tensor_scale", c_vp)]
 
 
+class fp8_pool(ctypes.Structure):
+    _fields_ = [("role", c_i32), ("fp8_format", c_i32), ("per_head", c_i32), ("num_blocks", c_i32),
+                ("kv_heads", c_i32), ("head_dim", c_i32), ("pool", c_vp), ("scale", c_vp)]
+
+
 _P_NV = ctypes.POINTER(nvfp4_pool)
+_P_F8 = ctypes.POINTER(fp8_pool)
 _P_CFG, _P_CACHE = ctypes.POINTER(kivi_config), ctypes.POINTER(kivi_cache)
 _P_PCFG, _P_PCACHE = ctypes.POINTER(kivi_paged_config), ctypes.POINTER(kivi_paged_cache)
 _SIG = {
@@ -100,12 +106,13 @@ _SIG = {
     "kv_paged_flush": ([_P_PCACHE, c_vp], ctypes.c_int),
     "kv_paged_decode_workspace_bytes": ([_P_PCFG], c_sz),
     "kv_paged_decode_attention": ([_P_PCACHE, c_vp, c_vp, c_i32, c_f32, c_vp, c_sz, c_vp], ctypes.c_int),
+    "fp8_pool_bytes": ([c_i32, c_i32, c_i32], c_sz),
+    "fp8_pool_init": ([_P_F8, c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp], ctypes.c_int),
     "fp8_quantize_workspace_bytes": ([c_i32, c_i32, c_i32, c_i32], c_sz),
-    "fp8_kv_quantize": ([c_vp, c_i32, c_i32, c_i32, c_i32, c_vp, c_i32, c_i32, c_i32, c_vp, c_vp, c_i32, c_i32,
-                         c_i32, c_i32, c_vp, c_sz, c_vp], ctypes.c_int),
+    "fp8_kv_quantize": ([_P_F8, c_vp, c_i32, c_i32, c_vp, c_i32, c_i32, c_vp, c_sz, c_vp], ctypes.c_int),
     "fp8_decode_workspace_bytes": ([c_i32, c_i32, c_i32], c_sz),
-    "fp8_decode_attention": ([c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, c_i32, c_i32, c_vp, c_vp, c_i32, c_i32, c_i32,
-                              c_i32, c_i32, c_i32, c_i32, c_i32, c_vp, c_i32, c_f32, c_vp, c_sz, c_vp], ctypes.c_int),
+    "fp8_decode_attention": ([c_vp, _P_F8, _P_F8, c_i32, c_vp, c_vp, c_i32, c_i32, c_i32, c_i32, c_vp, c_i32, c_f32,
+                              c_vp, c_sz, c_vp], ctypes.c_int),
     "nvfp4_pool_bytes": ([c_i32, c_i32, c_i32], c_sz),
     "nvfp4_pool_init": ([_P_NV, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp], ctypes.c_int),
     "nvfp4_quantize_workspace_bytes": ([], c_sz),
@@ -239,36 +246,42 @@ def kv_paged_decode_attention(cache: kivi_paged_cache, q, out, out_fp32: bool, s
            "kv_paged_decode_attention")
 
 
-def fp8_quantize_workspace_bytes(batch, kv_heads, seq_len, head_dim) -> int:
-    return int(_lib.fp8_quantize_workspace_bytes(batch, kv_heads, seq_len, head_dim))
+def fp8_pool_bytes(num_blocks, kv_heads, head_dim) -> int:
+    return int(_lib.fp8_pool_bytes(num_blocks, kv_heads, head_dim))
 
 
 FP8_FORMATS = {"e4m3": 0, "e5m2": 1}
 
 
-def fp8_kv_quantize(x, batch, kv_heads, seq_len, head_dim, block_table, max_blocks, block_size, num_blocks, pool,
-                    scale, static_scale: bool, value_layout: int, ws, ws_bytes: int, stream=None,
-                    per_head: bool = False, fp8_format: int = 0) -> None:
-    _check(_lib.fp8_kv_quantize(_ptr(x), batch, kv_heads, seq_len, head_dim, _ptr(block_table), max_blocks,
-                                block_size, num_blocks, _ptr(pool), _ptr(scale), int(bool(static_scale)),
-                                int(per_head), int(fp8_format), value_layout, _ptr(ws), ws_bytes, _stream(stream)),
-           "fp8_kv_quantize")
+def fp8_pool_init(role: int, fp8_format: int, per_head: bool, num_blocks: int, kv_heads: int, head_dim: int, buf,
+                  scale) -> fp8_pool:
+    desc = fp8_pool()
+    _check(_lib.fp8_pool_init(ctypes.byref(desc), role, int(fp8_format), int(per_head), num_blocks, kv_heads,
+                              head_dim, _ptr(buf), _ptr(scale)), "fp8_pool_init")
+    return desc
+
+
+def fp8_quantize_workspace_bytes(batch, kv_heads, seq_len, head_dim) -> int:
+    return int(_lib.fp8_quantize_workspace_bytes(batch, kv_heads, seq_len, head_dim))
+
+
+def fp8_kv_quantize(pool: fp8_pool, x, batch, seq_len, block_table, max_blocks, static_scale: bool, ws,
+                    ws_bytes: int, stream=None) -> None:
+    _check(_lib.fp8_kv_quantize(ctypes.byref(pool), _ptr(x), batch, seq_len, _ptr(block_table), max_blocks,
+                                int(bool(static_scale)), _ptr(ws), ws_bytes, _stream(stream)), "fp8_kv_quantize")
 
 
 def fp8_decode_workspace_bytes(batch, q_heads, head_dim) -> int:
     return int(_lib.fp8_decode_workspace_bytes(batch, q_heads, head_dim))
 
 
-def fp8_decode_attention(q, k_pool, v_pool, k_scale, v_scale, block_table, seq_lens, batch, q_heads, kv_heads,
-                         head_dim, block_size, max_blocks, num_blocks, max_seq_len, out, out_fp32: bool,
-                         softmax_scale: float, ws, ws_bytes: int, stream=None, per_head: bool = False,
-                         fp8_format: int = 0, q_fp8: bool = False) -> None:
-    _check(_lib.fp8_decode_attention(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(k_scale), _ptr(v_scale),
-                                     int(per_head), int(fp8_format), int(q_fp8),
-                                     _ptr(block_table), _ptr(seq_lens), batch, q_heads, kv_heads, head_dim,
-                                     block_size, max_blocks, num_blocks, max_seq_len, _ptr(out),
-                                     int(bool(out_fp32)), float(softmax_scale), _ptr(ws), ws_bytes,
-                                     _stream(stream)), "fp8_decode_attention")
+def fp8_decode_attention(q, k: fp8_pool, v: fp8_pool, block_table, seq_lens, batch, q_heads, max_blocks,
+                         max_seq_len, out, out_fp32: bool, softmax_scale: float, ws, ws_bytes: int, stream=None,
+                         q_fp8: bool = False) -> None:
+    _check(_lib.fp8_decode_attention(_ptr(q), ctypes.byref(k), ctypes.byref(v), int(q_fp8), _ptr(block_table),
+                                     _ptr(seq_lens), batch, q_heads, max_blocks, max_seq_len, _ptr(out),
+                                     int(bool(out_fp32)), float(softmax_scale), _ptr(ws), ws_bytes, _stream(stream)),
+           "fp8_decode_attention")
 
 
 def nvfp4_pool_bytes(num_blocks, kv_heads, head_dim) -> int:
@@ -473,3 +486,31 @@ class Nvfp4Pool:
         """Device bytes as ``[num_blocks, H, 9 * D]`` (uint8)."""
         d = self.desc
         return self.buf[: d.num_blocks * d.kv_heads * 9 * d.head_dim].view(d.num_blocks, d.kv_heads, 9 * d.head_dim)
+
+
+class Fp8Pool:
+    """One FP8 pool (keys or values) with its scale(s), in device memory owned by PyTorch."""
+
+    def __init__(self, role: int, num_blocks: int, kv_heads: int, head_dim: int, fp8_format: int = 0,
+                 per_head: bool = False, device="cuda"):
+        import torch
+        self.buf = _alloc_bytes(fp8_pool_bytes(num_blocks, kv_heads, head_dim), device)
+        n = kv_heads if per_head else 1
+        self.scale_buf = torch.ones(max(64, -(-n // 64) * 64), dtype=torch.float32, device=device)
+        self.scale = self.scale_buf[:n]
+        self.desc = fp8_pool_init(role, fp8_format, per_head, num_blocks, kv_heads, head_dim, self.buf, self.scale_buf)
+        self.ws = None
+
+    def quantize(self, x, block_table, max_blocks, static_scale=False, stream=None):
+        import torch
+        b, h, s, d = x.shape
+        wsb = fp8_quantize_workspace_bytes(b, h, s, d)
+        if self.ws is None or self.ws.numel() < wsb:
+            self.ws = torch.zeros(wsb, dtype=torch.uint8, device=x.device)
+        fp8_kv_quantize(self.desc, x, b, s, block_table, max_blocks, static_scale, self.ws, wsb, stream)
+
+    def view(self):
+        """Device bytes as ``[num_blocks, H, 16 * D]`` (uint8)."""
+        d = self.desc
+        return self.buf[: d.num_blocks * d.kv_heads * 16 * d.head_dim].view(d.num_blocks, d.kv_heads,
+                                                                             16 * d.head_dim)

@@ -25,7 +25,7 @@ def declared_functions():
 
 def test_every_declared_symbol_is_exported():
     names = declared_functions()
-    assert len(names) == 26
+    assert len(names) == 28
     lib = ctypes.CDLL(kvq.LIB_PATH)
     for n in names:
         assert hasattr(lib, n), n
@@ -165,33 +165,54 @@ def test_decode_validation():
 
 
 def test_fp8_validation():
-    q = dict(x=ALIGNED, batch=2, kv_heads=2, seq_len=40, head_dim=128, block_table=ALIGNED, max_blocks=3,
-             block_size=16, num_blocks=6, pool=ALIGNED, scale=ALIGNED, static_scale=False, value_layout=0,
-             ws=ALIGNED, ws_bytes=kvq.fp8_quantize_workspace_bytes(2, 2, 40, 128))
-    for change, code in [(dict(block_size=32), "KVQ_ERR_UNSUPPORTED"), (dict(head_dim=96), "KVQ_ERR_UNSUPPORTED"),
-                         (dict(max_blocks=2), "KVQ_ERR_CAPACITY"), (dict(value_layout=3), "KVQ_ERR_ARG"),
-                         (dict(ws_bytes=8), "KVQ_ERR_WORKSPACE"), (dict(pool=None), "KVQ_ERR_NULL"),
-                         (dict(scale=ALIGNED + 4), "KVQ_ERR_ALIGN"), (dict(seq_len=0), "KVQ_ERR_ARG"),
-                         (dict(per_head=2), "KVQ_ERR_ARG"), (dict(fp8_format=2), "KVQ_ERR_ARG"),
-                         (dict(fp8_format=-1), "KVQ_ERR_ARG")]:
+    """Host-side checks of the FP8 calls: pool descriptors (role, format, scale
+    granularity, shape), capacity, workspace, alignment; the decode refuses
+    swapped or mismatched pools with KVQ_ERR_ARG."""
+    assert kvq.fp8_pool_bytes(6, 2, 128) == 6 * 2 * 16 * 128 and kvq.fp8_pool_bytes(6, 2, 96) == 0
+    for args, code in [((2, 0, 0, 6, 2, 128), "KVQ_ERR_ARG"), ((0, 2, 0, 6, 2, 128), "KVQ_ERR_ARG"),
+                       ((0, 0, 2, 6, 2, 128), "KVQ_ERR_ARG"), ((0, 0, 0, 0, 2, 128), "KVQ_ERR_ARG"),
+                       ((0, 0, 0, 6, 2, 96), "KVQ_ERR_UNSUPPORTED")]:
+        with pytest.raises(kvq.KvqError) as e:
+            kvq.fp8_pool_init(*args, ALIGNED, ALIGNED * 2)
+        assert e.value.name == code, args
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.fp8_pool_init(kvq.ROLE_KEY, 0, 0, 6, 2, 128, ALIGNED, ALIGNED + 4)
+    assert e.value.name == "KVQ_ERR_ALIGN"
+    k = kvq.fp8_pool_init(kvq.ROLE_KEY, 0, 0, 6, 2, 128, ALIGNED, ALIGNED * 2)
+    v = kvq.fp8_pool_init(kvq.ROLE_VALUE, 0, 0, 6, 2, 128, ALIGNED * 3, ALIGNED * 4)
+    q = dict(x=ALIGNED, batch=2, seq_len=40, block_table=ALIGNED, max_blocks=3, static_scale=False, ws=ALIGNED,
+             ws_bytes=kvq.fp8_quantize_workspace_bytes(2, 2, 40, 128))
+    for change, code in [(dict(max_blocks=2), "KVQ_ERR_CAPACITY"), (dict(ws_bytes=8), "KVQ_ERR_WORKSPACE"),
+                         (dict(x=None), "KVQ_ERR_NULL"), (dict(block_table=ALIGNED + 4), "KVQ_ERR_ALIGN"),
+                         (dict(seq_len=0), "KVQ_ERR_ARG")]:
         args = dict(q, **change)
         with pytest.raises(kvq.KvqError) as e:
-            kvq.fp8_kv_quantize(**args, stream=0)
+            kvq.fp8_kv_quantize(k, **args, stream=0)
         assert e.value.name == code, change
-    d = dict(q=ALIGNED, k_pool=ALIGNED, v_pool=ALIGNED, k_scale=ALIGNED, v_scale=ALIGNED, block_table=ALIGNED,
-             seq_lens=ALIGNED, batch=2, q_heads=8, kv_heads=2, head_dim=128, block_size=16, max_blocks=3,
-             num_blocks=6, max_seq_len=40, out=ALIGNED, out_fp32=True, softmax_scale=0.0, ws=ALIGNED,
-             ws_bytes=kvq.fp8_decode_workspace_bytes(2, 8, 128))
+    d = dict(q=ALIGNED, block_table=ALIGNED, seq_lens=ALIGNED, batch=2, q_heads=8, max_blocks=3, max_seq_len=40,
+             out=ALIGNED, out_fp32=True, softmax_scale=0.0, ws=ALIGNED, ws_bytes=kvq.fp8_decode_workspace_bytes(2, 8, 128))
+
+    def dec(kk, vv, **change):
+        args = dict(d, **change)
+        qq = args.pop("q")
+        with pytest.raises(kvq.KvqError) as e:
+            kvq.fp8_decode_attention(qq, kk, vv, **args, stream=0)
+        return e.value.name
+
     for change, code in [(dict(q_heads=7), "KVQ_ERR_SHAPE"), (dict(max_seq_len=49), "KVQ_ERR_CAPACITY"),
                          (dict(q_heads=32), "KVQ_ERR_UNSUPPORTED"), (dict(ws_bytes=100), "KVQ_ERR_WORKSPACE"),
-                         (dict(seq_lens=None), "KVQ_ERR_NULL"), (dict(per_head=3), "KVQ_ERR_ARG"),
-                         (dict(fp8_format=2), "KVQ_ERR_ARG"), (dict(q_fp8=2), "KVQ_ERR_ARG"),
+                         (dict(seq_lens=None), "KVQ_ERR_NULL"), (dict(q_fp8=2), "KVQ_ERR_ARG"),
                          (dict(ws_bytes=kvq.kv_decode_workspace_bytes(kvq.make_config(2, 8, 8, 128, 2, 2, 128, 32))),
                           "KVQ_ERR_WORKSPACE")]:
-        args = dict(d, **change)
-        with pytest.raises(kvq.KvqError) as e:
-            kvq.fp8_decode_attention(**args, stream=0)
-        assert e.value.name == code, change
+        assert dec(k, v, **change) == code, change
+    assert dec(v, k) == "KVQ_ERR_ARG"                        # roles swapped
+    assert dec(k, k) == "KVQ_ERR_ARG"
+    v5 = kvq.fp8_pool_init(kvq.ROLE_VALUE, 1, 0, 6, 2, 128, ALIGNED * 3, ALIGNED * 4)
+    assert dec(k, v5) == "KVQ_ERR_ARG"                       # formats differ
+    vph = kvq.fp8_pool_init(kvq.ROLE_VALUE, 0, 1, 6, 2, 128, ALIGNED * 3, ALIGNED * 4)
+    assert dec(k, vph) == "KVQ_ERR_ARG"                      # scale granularities differ
+    v7 = kvq.fp8_pool_init(kvq.ROLE_VALUE, 0, 0, 7, 2, 128, ALIGNED * 3, ALIGNED * 4)
+    assert dec(k, v7) == "KVQ_ERR_SHAPE"
 
 
 # ---------------------------------------------------------------------------
@@ -209,6 +230,9 @@ int main(void) {
   printf("kivi_paged_config %zu\n", sizeof(kivi_paged_config));
   printf("kivi_paged_cache %zu\n", sizeof(kivi_paged_cache));
   printf("nvfp4_pool %zu\n", sizeof(nvfp4_pool));
+  printf("fp8_pool %zu\n", sizeof(fp8_pool));
+  F(fp8_pool, role) F(fp8_pool, fp8_format) F(fp8_pool, per_head) F(fp8_pool, head_dim) F(fp8_pool, pool)
+  F(fp8_pool, scale)
   F(nvfp4_pool, role) F(nvfp4_pool, head_dim) F(nvfp4_pool, pool) F(nvfp4_pool, tensor_scale)
   printf("KVQ_ROLE_KEY %d\n", KVQ_ROLE_KEY);
   printf("KVQ_ROLE_VALUE %d\n", KVQ_ROLE_VALUE);
@@ -238,7 +262,8 @@ def test_struct_layouts_match_the_header(tmp_path):
     want = {"kivi_config": ctypes.sizeof(kvq.kivi_config), "kivi_cache": ctypes.sizeof(kvq.kivi_cache),
             "kivi_paged_config": ctypes.sizeof(kvq.kivi_paged_config),
             "kivi_paged_cache": ctypes.sizeof(kvq.kivi_paged_cache), "KVQ_PAGED_MAX_SEQS": kvq.PAGED_MAX_SEQS,
-            "nvfp4_pool": ctypes.sizeof(kvq.nvfp4_pool), "KVQ_ROLE_KEY": kvq.ROLE_KEY,
+            "nvfp4_pool": ctypes.sizeof(kvq.nvfp4_pool), "fp8_pool": ctypes.sizeof(kvq.fp8_pool),
+            "KVQ_ROLE_KEY": kvq.ROLE_KEY,
             "KVQ_ROLE_VALUE": kvq.ROLE_VALUE}
     for key, val in got.items():
         if "." in key:

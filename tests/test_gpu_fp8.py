@@ -21,23 +21,25 @@ def _kvq():
     return kvq
 
 
-def _quantize(x16, table, num_blocks, value_layout, static_scale=None, fmt="e4m3", per_head=False):
-    """static_scale: None (dynamic), a scalar, or per head an array [H]."""
+# the oracle's in-block order of each role: keys in the m16n8k32 order (layout id 2), values 1
+KEY, VALUE = 2, 1
+
+
+def _quantize(x16, table, num_blocks, vl, static_scale=None, fmt="e4m3", per_head=False):
+    """A key (vl = KEY) or value (vl = VALUE) pool; static_scale: None (dynamic), a
+    scalar, or per head an array [H]. Returns (pool, its scale tensor)."""
     import torch
     kvq = _kvq()
     b, h, s, d = x16.shape
-    pool = torch.full((num_blocks, h, 16 * d), 0xAB, dtype=torch.uint8, device="cuda")
+    p = kvq.Fp8Pool(kvq.ROLE_KEY if vl == KEY else kvq.ROLE_VALUE, num_blocks, h, d,
+                    fp8_format=kvq.FP8_FORMATS[fmt], per_head=per_head)
+    p.buf.fill_(0xAB)
     n = h if per_head else 1
     init = np.full(n, -1.0, np.float32) if static_scale is None else np.broadcast_to(
         np.asarray(static_scale, np.float32), (n,))
-    scale = torch.tensor(np.array(init), dtype=torch.float32, device="cuda")
-    wsb = kvq.fp8_quantize_workspace_bytes(b, h, s, d)
-    ws = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
-    xt, tt = dev(x16), dev(table)
-    kvq.fp8_kv_quantize(xt, b, h, s, d, tt, table.shape[1], 16, num_blocks, pool, scale,
-                        static_scale is not None, value_layout, ws, wsb, per_head=per_head,
-                        fp8_format=kvq.FP8_FORMATS[fmt])
-    return pool, scale
+    p.scale.copy_(torch.tensor(np.array(init), dtype=torch.float32))
+    p.quantize(dev(x16), dev(table), table.shape[1], static_scale=static_scale is not None)
+    return p, p.scale
 
 
 def _oracle_pool(x16, table, num_blocks, value_layout, scale, fmt="e4m3"):
@@ -51,10 +53,10 @@ def test_all_fp16_values_cast_exactly():
     allh = np.arange(65536, dtype=np.uint16).view(np.float16)
     x = allh.reshape(1, 4, 128, 128)                     # 4 kv heads x 128 tokens x 128 channels
     table = np.arange(8, dtype=np.int32).reshape(1, 8)
-    for vl in (0, 1, 2):
+    for vl in (KEY, VALUE):
         pool, scale = _quantize(x, table, 8, vl, static_scale=1.0)
         want = _oracle_pool(x, table, 8, vl, np.float32(1.0))
-        assert np.array_equal(host(pool), want)
+        assert np.array_equal(host(pool.view()), want)
 
 
 @pytest.mark.parametrize("special", [np.inf, -np.inf, np.nan])
@@ -65,11 +67,11 @@ def test_dynamic_scale_with_non_finite_values(special):
     x = workloads.make_inputs(1, 2, 4, 128, 32, 1, 5).k.copy()
     x[0, 1, 7, 33] = special
     table = np.arange(2, dtype=np.int32).reshape(1, 2)
-    pool, scale = _quantize(x, table, 2, 0)
+    pool, scale = _quantize(x, table, 2, KEY)
     s_ref = fp8.dynamic_scale(x)
     got_s = host(scale)[0]
     assert (np.isnan(got_s) and np.isnan(s_ref)) or got_s == s_ref
-    assert np.array_equal(host(pool), _oracle_pool(x, table, 2, 0, s_ref))
+    assert np.array_equal(host(pool.view()), _oracle_pool(x, table, 2, KEY, s_ref))
 
 
 @pytest.mark.parametrize("d", [64, 128])
@@ -78,17 +80,17 @@ def test_dynamic_scale_and_bytes(d):
     x = workloads.make_inputs(3, 2, 4, d, 16 * 5 + 7, 1, 21).k          # ragged last block
     nb = 6
     table = rng.permutation(3 * nb + 4).astype(np.int32)[: 3 * nb].reshape(3, nb)
-    pool, scale = _quantize(x, table, 3 * nb + 4, 0)
+    pool, scale = _quantize(x, table, 3 * nb + 4, KEY)
     s_ref = fp8.dynamic_scale(x)
     assert host(scale)[0] == s_ref
-    got = host(pool)
-    want = _oracle_pool(x, table, 3 * nb + 4, 0, s_ref)
+    got = host(pool.view())
+    want = _oracle_pool(x, table, 3 * nb + 4, KEY, s_ref)
     used = np.unique(table)
     assert np.array_equal(got[used], want[used])
     unused = np.setdiff1d(np.arange(3 * nb + 4), used)
     assert np.all(got[unused] == 0xAB)                   # untouched
     # the ragged last block's missing rows are zero bytes
-    nat = layout.fp8_unpack_pool(got, d, 0)
+    nat = layout.fp8_unpack_pool(got, d, KEY)
     assert np.all(nat[table[:, -1], :, 7:, :] == 0)
 
 
@@ -97,8 +99,8 @@ def test_saturation_with_static_scale():
     x[0, 0, 0, :4] = [1000, -700, 448, -465]
     x[0, 0, 1, :2] = [np.inf, -np.inf]
     table = np.zeros((1, 1), np.int32)
-    pool, _ = _quantize(x, table, 1, 0, static_scale=1.0)
-    nat = layout.fp8_unpack_pool(host(pool), 64, 0)[0, 0]
+    pool, _ = _quantize(x, table, 1, KEY, static_scale=1.0)
+    nat = layout.fp8_unpack_pool(host(pool.view()), 64, KEY)[0, 0]
     assert list(nat[0, :4]) == [0x7E, 0xFE, 0x7E, 0xFE]
     assert list(nat[1, :2]) == [0x7E, 0xFE]
 
@@ -111,9 +113,8 @@ def _decode(q16, kpool, vpool, kscale, vscale, table, seq_lens, hkv, num_blocks,
     out = torch.empty((b, hq, d), dtype=torch.float32 if out_fp32 else torch.float16, device="cuda")
     wsb = kvq.fp8_decode_workspace_bytes(b, hq, d)
     ws = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
-    kvq.fp8_decode_attention(dev(q16), kpool, vpool, kscale, vscale, dev(table), dev(seq_lens.astype(np.int32)),
-                             b, hq, hkv, d, 16, table.shape[1], num_blocks, max_seq, out, out_fp32, 0.0, ws, wsb,
-                             per_head=per_head, fp8_format=kvq.FP8_FORMATS[fmt])
+    kvq.fp8_decode_attention(dev(q16), kpool.desc, vpool.desc, dev(table), dev(seq_lens.astype(np.int32)),
+                             b, hq, table.shape[1], max_seq, out, out_fp32, 0.0, ws, wsb)
     return host(out).astype(np.float64), int(host(ws[:4].view(torch.int32))[0])
 
 
@@ -137,8 +138,8 @@ def test_decode_ragged_lengths(d, gq):
     x = workloads.make_inputs(b, hkv, hkv * gq, d, s, 1, 31 + gq)
     nb = -(-s // 16)
     table = rng.permutation(b * nb).astype(np.int32).reshape(b, nb)
-    kpool, kscale = _quantize(x.k, table, b * nb, 0)
-    vpool, vscale = _quantize(x.v, table, b * nb, 1)
+    kpool, kscale = _quantize(x.k, table, b * nb, KEY)
+    vpool, vscale = _quantize(x.v, table, b * nb, VALUE)
     seq_lens = np.array([s, 1, 16 * 17 + 3])
     out, status = _decode(x.q[0], kpool, vpool, kscale, vscale, table, seq_lens, hkv, b * nb, s)
     ref = _oracle_decode(x.q[0], x.k, x.v, fp8.dynamic_scale(x.k), fp8.dynamic_scale(x.v), seq_lens)
@@ -157,8 +158,8 @@ def test_block_table_permutation_invariance():
     perm = rng.permutation(b * nb).astype(np.int32).reshape(b, nb)
     outs = []
     for table in (ident, perm):
-        kpool, ks = _quantize(x.k, table, b * nb, 0)
-        vpool, vs = _quantize(x.v, table, b * nb, 1)
+        kpool, ks = _quantize(x.k, table, b * nb, KEY)
+        vpool, vs = _quantize(x.v, table, b * nb, VALUE)
         outs.append(_decode(x.q[0], kpool, vpool, ks, vs, table, np.array([s, s]), hkv, b * nb, s)[0])
     assert np.array_equal(outs[0], outs[1])
 
@@ -171,17 +172,17 @@ def test_full_size_fp8_32k():
     w = workloads.FP8_32K
     k, v, q, table = workloads.fp8_inputs(w)
     nb_total = w.batch * w.blocks_per_seq
-    kpool, kscale = _quantize(k, table, nb_total, 0)
-    vpool, vscale = _quantize(v, table, nb_total, 1)
+    kpool, kscale = _quantize(k, table, nb_total, KEY)
+    vpool, vscale = _quantize(v, table, nb_total, VALUE)
     ks_ref, vs_ref = fp8.dynamic_scale(k), fp8.dynamic_scale(v)
     assert host(kscale)[0] == ks_ref and host(vscale)[0] == vs_ref
     rng = np.random.default_rng(3)
     for _ in range(24):
         b, h, j = int(rng.integers(w.batch)), int(rng.integers(w.kv_heads)), int(rng.integers(w.blocks_per_seq))
-        for x16, pool, sref, vl in ((k, kpool, ks_ref, 0), (v, vpool, vs_ref, 1)):
+        for x16, pool, sref, vl in ((k, kpool, ks_ref, KEY), (v, vpool, vs_ref, VALUE)):
             blk = table[b, j]
             want = layout.fp8_pack_pool(fp8.quantize(x16[b, h, 16 * j:16 * j + 16], sref)[None, None], vl)[0, 0]
-            assert np.array_equal(host(pool[blk, h]), want)
+            assert np.array_equal(host(pool.view()[blk, h]), want)
     seq_lens = np.full(w.batch, w.context)
     out, status = _decode(q, kpool, vpool, kscale, vscale, table, seq_lens, w.kv_heads, nb_total, w.context)
     assert status == 0
@@ -198,9 +199,9 @@ def test_e5m2_all_fp16_values_cast_exactly():
     allh = np.arange(65536, dtype=np.uint16).view(np.float16)
     x = allh.reshape(1, 4, 128, 128)
     table = np.arange(8, dtype=np.int32).reshape(1, 8)
-    for vl in (0, 1):
+    for vl in (KEY, VALUE):
         pool, _ = _quantize(x, table, 8, vl, static_scale=1.0, fmt="e5m2")
-        assert np.array_equal(host(pool), _oracle_pool(x, table, 8, vl, np.float32(1.0), "e5m2"))
+        assert np.array_equal(host(pool.view()), _oracle_pool(x, table, 8, vl, np.float32(1.0), "e5m2"))
 
 
 def _head_ranged_inputs(b, h, s, d, seed):
@@ -217,11 +218,11 @@ def test_dynamic_per_head_scales_and_bytes(fmt, d):
     x = _head_ranged_inputs(b, h, s, d, 17)
     nb = 6
     table = rng.permutation(b * nb).astype(np.int32).reshape(b, nb)
-    for vl in (0, 1):
+    for vl in (KEY, VALUE):
         pool, scale = _quantize(x, table, b * nb, vl, fmt=fmt, per_head=True)
         s_ref = fp8.dynamic_scale_per_head(x, fmt)
         assert np.array_equal(host(scale), s_ref)
-        assert np.array_equal(host(pool), _oracle_pool(x, table, b * nb, vl, s_ref, fmt))
+        assert np.array_equal(host(pool.view()), _oracle_pool(x, table, b * nb, vl, s_ref, fmt))
 
 
 @pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
@@ -230,9 +231,9 @@ def test_static_per_head_scales(fmt):
     x = _head_ranged_inputs(b, h, s, d, 23)
     table = np.arange(b * 3, dtype=np.int32).reshape(b, 3)
     given = np.array([1.0, 0.5, 0.01, 3.0e-5], np.float32)       # head 2 (|x| to ~150) saturates in E4M3
-    pool, scale = _quantize(x, table, b * 3, 0, static_scale=given, fmt=fmt, per_head=True)
+    pool, scale = _quantize(x, table, b * 3, KEY, static_scale=given, fmt=fmt, per_head=True)
     assert np.array_equal(host(scale), given)                     # read, not written
-    assert np.array_equal(host(pool), _oracle_pool(x, table, b * 3, 0, given, fmt))
+    assert np.array_equal(host(pool.view()), _oracle_pool(x, table, b * 3, KEY, given, fmt))
 
 
 @pytest.mark.parametrize("special", [np.inf, np.nan])
@@ -241,14 +242,14 @@ def test_dynamic_e5m2_with_non_finite_values(special):
     x[0, 0, 3, 9] = special
     table = np.arange(2, dtype=np.int32).reshape(1, 2)
     for per_head in (False, True):
-        pool, scale = _quantize(x, table, 2, 0, fmt="e5m2", per_head=per_head)
+        pool, scale = _quantize(x, table, 2, KEY, fmt="e5m2", per_head=per_head)
         s_ref = np.atleast_1d(fp8.dynamic_scale_per_head(x, "e5m2") if per_head else fp8.dynamic_scale(x, "e5m2"))
         got = host(scale)
         assert got.shape == s_ref.shape
         assert np.array_equal(np.isnan(got), np.isnan(s_ref)) and np.array_equal(got[~np.isnan(got)],
                                                                                s_ref[~np.isnan(got)])
-        want = _oracle_pool(x, table, 2, 0, s_ref if per_head else s_ref[0], "e5m2")
-        assert np.array_equal(host(pool), want)
+        want = _oracle_pool(x, table, 2, KEY, s_ref if per_head else s_ref[0], "e5m2")
+        assert np.array_equal(host(pool.view()), want)
 
 
 @pytest.mark.parametrize("fmt,per_head", [("e5m2", False), ("e4m3", True), ("e5m2", True)])
@@ -260,8 +261,8 @@ def test_decode_format_and_scale_variants(fmt, per_head, d, gq):
     k = (x.k.astype(np.float32) * np.array([1.0, 25.0]).reshape(1, 2, 1, 1)).astype(np.float16)
     nb = -(-s // 16)
     table = rng.permutation(b * nb).astype(np.int32).reshape(b, nb)
-    kpool, kscale = _quantize(k, table, b * nb, 0, fmt=fmt, per_head=per_head)
-    vpool, vscale = _quantize(x.v, table, b * nb, 1, fmt=fmt, per_head=per_head)
+    kpool, kscale = _quantize(k, table, b * nb, KEY, fmt=fmt, per_head=per_head)
+    vpool, vscale = _quantize(x.v, table, b * nb, VALUE, fmt=fmt, per_head=per_head)
     seq_lens = np.array([s, 1, 16 * 11 + 3])
     out, status = _decode(x.q[0], kpool, vpool, kscale, vscale, table, seq_lens, hkv, b * nb, s, fmt=fmt,
                           per_head=per_head)
@@ -282,9 +283,8 @@ def _decode_qfp8(q16, kpool, vpool, kscale, vscale, table, seq_lens, hkv, num_bl
     out = torch.empty((b, hq, d), dtype=torch.float32 if out_fp32 else torch.float16, device="cuda")
     wsb = kvq.fp8_decode_workspace_bytes(b, hq, d)
     ws = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
-    kvq.fp8_decode_attention(dev(q16), kpool, vpool, kscale, vscale, dev(table), dev(seq_lens.astype(np.int32)),
-                             b, hq, hkv, d, 16, table.shape[1], num_blocks, max_seq, out, out_fp32, 0.0, ws, wsb,
-                             per_head=per_head, fp8_format=kvq.FP8_FORMATS[fmt], q_fp8=True)
+    kvq.fp8_decode_attention(dev(q16), kpool.desc, vpool.desc, dev(table), dev(seq_lens.astype(np.int32)),
+                             b, hq, table.shape[1], max_seq, out, out_fp32, 0.0, ws, wsb, q_fp8=True)
     off = kvq.kv_decode_workspace_bytes(kvq.make_config(b, hq, hq, d, 2, 2, 128, 32))
     n = b * hq * d
     q8 = host(ws[off:off + n]).reshape(b, hq, d)
@@ -294,15 +294,15 @@ def _decode_qfp8(q16, kpool, vpool, kscale, vscale, table, seq_lens, hkv, num_bl
 
 
 @pytest.mark.parametrize("d", [64, 128])
-def test_key_layout_for_fp8_tensor_cores(d):
+def test_key_pool_in_the_fp8_tensor_core_order(d):
     rng = np.random.default_rng(d + 5)
     x = workloads.make_inputs(2, 3, 6, d, 16 * 4 + 11, 1, 71).k
     nb = 5
     table = rng.permutation(2 * nb).astype(np.int32).reshape(2, nb)
-    pool, scale = _quantize(x, table, 2 * nb, 2)
+    pool, scale = _quantize(x, table, 2 * nb, KEY)
     s_ref = fp8.dynamic_scale(x)
     assert host(scale)[0] == s_ref
-    assert np.array_equal(host(pool), _oracle_pool(x, table, 2 * nb, 2, s_ref))
+    assert np.array_equal(host(pool.view()), _oracle_pool(x, table, 2 * nb, KEY, s_ref))
 
 
 @pytest.mark.parametrize("fmt,per_head", [("e4m3", False), ("e5m2", False), ("e4m3", True), ("e5m2", True)])
@@ -318,8 +318,8 @@ def test_fp8_domain_attention(fmt, per_head, d, gq):
     q = (x.q[0].astype(np.float32) * 3.0).astype(np.float16)
     nb = -(-s // 16)
     table = rng.permutation(b * nb).astype(np.int32).reshape(b, nb)
-    kpool, kscale = _quantize(k, table, b * nb, 2, fmt=fmt, per_head=per_head)
-    vpool, vscale = _quantize(x.v, table, b * nb, 1, fmt=fmt, per_head=per_head)
+    kpool, kscale = _quantize(k, table, b * nb, KEY, fmt=fmt, per_head=per_head)
+    vpool, vscale = _quantize(x.v, table, b * nb, VALUE, fmt=fmt, per_head=per_head)
     seq_lens = np.array([s, 1, 16 * 11 + 3])
     out, status, q8, q_scale = _decode_qfp8(q, kpool, vpool, kscale, vscale, table, seq_lens, hkv, b * nb, s,
                                             fmt=fmt, per_head=per_head)
@@ -338,8 +338,8 @@ def test_fp8_domain_zero_query():
     x = workloads.make_inputs(b, hkv, hkv * gq, d, s, 1, 91)
     nb = -(-s // 16)
     table = np.arange(b * nb, dtype=np.int32).reshape(b, nb)
-    kpool, kscale = _quantize(x.k, table, b * nb, 2)
-    vpool, vscale = _quantize(x.v, table, b * nb, 1)
+    kpool, kscale = _quantize(x.k, table, b * nb, KEY)
+    vpool, vscale = _quantize(x.v, table, b * nb, VALUE)
     q = np.zeros((b, hkv * gq, d), np.float16)
     seq_lens = np.array([s, 40])
     out, status, q8, q_scale = _decode_qfp8(q, kpool, vpool, kscale, vscale, table, seq_lens, hkv, b * nb, s)
@@ -353,21 +353,21 @@ def test_fp8_domain_zero_query():
 
 
 def test_full_size_fp8_domain_attention_32k():
-    """The 32K FP8 workload with the query in E4M3 (keys in value_layout 2):
+    """The 32K FP8 workload with the query in E4M3:
     scales and query bytes exact, attention on sampled heads."""
     import torch
     w = workloads.FP8_32K
     k, v, q, table = workloads.fp8_inputs(w)
     nb_total = w.batch * w.blocks_per_seq
-    kpool, kscale = _quantize(k, table, nb_total, 2)
-    vpool, vscale = _quantize(v, table, nb_total, 1)
+    kpool, kscale = _quantize(k, table, nb_total, KEY)
+    vpool, vscale = _quantize(v, table, nb_total, VALUE)
     ks_ref, vs_ref = fp8.dynamic_scale(k), fp8.dynamic_scale(v)
     assert host(kscale)[0] == ks_ref and host(vscale)[0] == vs_ref
     rng = np.random.default_rng(4)
     for _ in range(12):
         b, h, j = int(rng.integers(w.batch)), int(rng.integers(w.kv_heads)), int(rng.integers(w.blocks_per_seq))
-        want = layout.fp8_pack_pool(fp8.quantize(k[b, h, 16 * j:16 * j + 16], ks_ref)[None, None], 2)[0, 0]
-        assert np.array_equal(host(kpool[table[b, j], h]), want)
+        want = layout.fp8_pack_pool(fp8.quantize(k[b, h, 16 * j:16 * j + 16], ks_ref)[None, None], KEY)[0, 0]
+        assert np.array_equal(host(kpool.view()[table[b, j], h]), want)
     seq_lens = np.full(w.batch, w.context)
     out, status, q8, q_scale = _decode_qfp8(q, kpool, vpool, kscale, vscale, table, seq_lens, w.kv_heads,
                                             nb_total, w.context)
@@ -387,11 +387,28 @@ def test_fp8_domain_fp16_output():
     x = workloads.make_inputs(b, hkv, hkv * gq, d, s, 1, 94)
     nb = -(-s // 16)
     table = rng.permutation(b * nb).astype(np.int32).reshape(b, nb)
-    kpool, kscale = _quantize(x.k, table, b * nb, 2)
-    vpool, vscale = _quantize(x.v, table, b * nb, 1)
+    kpool, kscale = _quantize(x.k, table, b * nb, KEY)
+    vpool, vscale = _quantize(x.v, table, b * nb, VALUE)
     seq_lens = np.array([s, 100])
     out, status, q8, q_scale = _decode_qfp8(x.q[0], kpool, vpool, kscale, vscale, table, seq_lens, hkv, b * nb, s,
                                             out_fp32=False)
     ref = _oracle_decode(x.q[0], x.k, x.v, fp8.dynamic_scale(x.k), fp8.dynamic_scale(x.v), seq_lens, q_fp8=True)
     assert_attention_close(out, ref, fp16_out=True)
     assert status == 0
+
+
+def test_decode_refuses_swapped_or_mismatched_pools():
+    """The pools record their role, format and scale granularity; the decode
+    refuses a value pool given as keys (and the reverse) and pools that disagree."""
+    kvq = _kvq()
+    b, hkv, gq, d, s = 1, 2, 2, 64, 32
+    x = workloads.make_inputs(b, hkv, hkv * gq, d, s, 1, 97)
+    table = np.arange(2, dtype=np.int32).reshape(1, 2)
+    kpool, _ = _quantize(x.k, table, 2, KEY)
+    vpool, _ = _quantize(x.v, table, 2, VALUE)
+    v5, _ = _quantize(x.v, table, 2, VALUE, fmt="e5m2")
+    vph, _ = _quantize(x.v, table, 2, VALUE, per_head=True)
+    for kp, vp in ((vpool, kpool), (kpool, kpool), (kpool, v5), (kpool, vph)):
+        with pytest.raises(kvq.KvqError) as e:
+            _decode(x.q[0], kp, vp, None, None, table, np.array([s]), hkv, 2, s)
+        assert e.value.name == "KVQ_ERR_ARG"
