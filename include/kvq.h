@@ -192,15 +192,27 @@ KVQ_API kvq_status kv_decode_attention(const kivi_cache* cache, const uint16_t* 
  *     (at most 64); a call that would need more returns KVQ_ERR_CAPACITY and
  *     enqueues nothing.
  *   - The first call on each device looks up the array's device address (with
- *     that device current); make that first call before any stream capture.
- *   - Every call shares the one array and clears its status word and split
- *     counters with an asynchronous memset on `stream` first. Calls that
- *     overlap on the GPU (other streams, other host threads) race on it:
- *     serialize them. The device-wait timeout status of kv_decode_attention is
- *     not reported by this call. */
+ *     that device current) and zeroes the array's status word; make that
+ *     first call before any stream capture. The address is kept for the life
+ *     of the process: calling this after cudaDeviceReset in the same process
+ *     is not supported (the reset unloads the array).
+ *   - Every call shares the one array and clears its split counters with an
+ *     asynchronous memset on `stream` first. Calls that overlap on the GPU
+ *     (other streams, other host threads) race on it: serialize them.
+ *   - Like the workspace status word of kv_decode_attention, the array's
+ *     status word collects the error bits of every call (bit 0 = a device
+ *     wait timed out) until kv_decode_noalloc_status clears it. */
 #define KVQ_NOALLOC_SCRATCH_BYTES (16u << 20)
 KVQ_API kvq_status kv_decode_attention_noalloc(const kivi_cache* cache, const uint16_t* q, void* out,
                                                int32_t out_fp32, float softmax_scale, void* stream);
+
+/* Reads the status word of kv_decode_attention_noalloc's scratch array on the
+ * current device into *status (host memory): it enqueues the copy on `stream`
+ * and waits for that stream, so the word covers every call enqueued on it
+ * before. With clear != 0 the word is then zeroed (enqueued on `stream`).
+ * Returns KVQ_ERR_TIMEOUT when bit 0 is set, else KVQ_OK. Not for use during
+ * stream capture. */
+KVQ_API kvq_status kv_decode_noalloc_status(uint32_t* status, int32_t clear, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* Paged, variable-length KIVI cache [KIVI section 3, CSDN section 13]       */

@@ -1096,8 +1096,10 @@ void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
 
 // The array's device address on the current device. In host code the array's
 // name is only a host-side stand-in, so the address is looked up once per
-// device (with that device current) and cached.
-kvq_status noalloc_scratch_address(void** out) {
+// device (with that device current) and cached. The first lookup on a device
+// also zeroes the array's header (status word and split counters) on
+// `stream`, so the status word starts clear; later calls leave it alone.
+kvq_status noalloc_scratch_address(void** out, cudaStream_t stream) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KVQ_ERR_CUDA;
   if (dev < 0 || dev >= kNoAllocMaxDevices) return KVQ_ERR_UNSUPPORTED;
@@ -1105,6 +1107,7 @@ kvq_status noalloc_scratch_address(void** out) {
   if (g_noalloc_ptr[dev] == nullptr) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, kvq_noalloc_scratch) != cudaSuccess || p == nullptr) return KVQ_ERR_CUDA;
+    if (cudaMemsetAsync(p, 0, kWsHeader, stream) != cudaSuccess) return KVQ_ERR_CUDA;
     g_noalloc_ptr[dev] = p;
   }
   *out = g_noalloc_ptr[dev];
@@ -1134,14 +1137,28 @@ kvq_status kv_decode_attention_noalloc(const kivi_cache* cache, const uint16_t* 
   if (need > static_cast<size_t>(KVQ_NOALLOC_SCRATCH_BYTES)) return KVQ_ERR_CAPACITY;
 
   void* ws = nullptr;
-  st = noalloc_scratch_address(&ws);
-  if (st != KVQ_OK) return st;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // the status word and the split counters must start at zero
-  if (cudaMemsetAsync(ws, 0, head, s) != cudaSuccess) return KVQ_ERR_CUDA;
+  st = noalloc_scratch_address(&ws, s);
+  if (st != KVQ_OK) return st;
+  // the split counters must start at zero (a call that timed out may have left
+  // some set); the status word keeps the error bits of earlier calls
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  if (cudaMemsetAsync(base + kWsHeader, 0, head - kWsHeader, s) != cudaSuccess) return KVQ_ERR_CUDA;
 
-  const kvq::KiviDecodeArgs a = kivi_decode_args(cache, plan, q, out, out_fp32, scale, static_cast<uint8_t*>(ws));
+  const kvq::KiviDecodeArgs a = kivi_decode_args(cache, plan, q, out, out_fp32, scale, base);
   return from_cuda(launch_contiguous_decode(cf, a, s));
+}
+
+kvq_status kv_decode_noalloc_status(uint32_t* status, int32_t clear, void* stream) {
+  if (status == nullptr) return KVQ_ERR_NULL;
+  void* ws = nullptr;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const kvq_status st = noalloc_scratch_address(&ws, s);
+  if (st != KVQ_OK) return st;
+  if (cudaMemcpyAsync(status, ws, sizeof(uint32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess) return KVQ_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return KVQ_ERR_CUDA;
+  if (clear != 0 && cudaMemsetAsync(ws, 0, sizeof(uint32_t), s) != cudaSuccess) return KVQ_ERR_CUDA;
+  return (*status & kvq::kStatusTimeout) != 0 ? KVQ_ERR_TIMEOUT : KVQ_OK;
 }
 
 }  // extern "C"

@@ -27,7 +27,7 @@ c_i32, c_sz, c_vp, c_f32 = ctypes.c_int32, ctypes.c_size_t, ctypes.c_void_p, cty
 EXPORTED = (
     "kvq_status_string", "kivi_cache_sizes", "kivi_cache_init", "kv_quant_prefill", "kv_append_token",
     "kv_flush_residual", "kv_decode_workspace_bytes", "kv_decode_attention", "kv_decode_attention_noalloc",
-    "kivi_paged_cache_sizes", "kivi_paged_cache_init", "kv_paged_prefill", "kv_paged_append", "kv_paged_flush",
+    "kv_decode_noalloc_status", "kivi_paged_cache_sizes", "kivi_paged_cache_init", "kv_paged_prefill", "kv_paged_append", "kv_paged_flush",
     "kv_paged_decode_workspace_bytes", "kv_paged_decode_attention",
     "fp8_pool_bytes", "fp8_pool_init", "fp8_quantize_workspace_bytes",
     "fp8_kv_quantize", "fp8_decode_workspace_bytes", "fp8_decode_attention",
@@ -99,6 +99,7 @@ _SIG = {
     "kv_decode_workspace_bytes": ([_P_CFG], c_sz),
     "kv_decode_attention": ([_P_CACHE, c_vp, c_vp, c_i32, c_f32, c_vp, c_sz, c_vp], ctypes.c_int),
     "kv_decode_attention_noalloc": ([_P_CACHE, c_vp, c_vp, c_i32, c_f32, c_vp], ctypes.c_int),
+    "kv_decode_noalloc_status": ([ctypes.POINTER(ctypes.c_uint32), c_i32, c_vp], ctypes.c_int),
     "kivi_paged_cache_sizes": ([_P_PCFG, ctypes.POINTER(c_sz)], ctypes.c_int),
     "kivi_paged_cache_init": ([_P_PCACHE, _P_PCFG, ctypes.POINTER(c_vp), c_vp], ctypes.c_int),
     "kv_paged_prefill": ([_P_PCACHE, c_vp, c_vp, c_i32, ctypes.POINTER(c_i32), c_vp], ctypes.c_int),
@@ -205,6 +206,17 @@ def kv_decode_attention_noalloc(cache: kivi_cache, q, out, out_fp32: bool, softm
     device memory: the scratch is a fixed device array inside the library."""
     _check(_lib.kv_decode_attention_noalloc(ctypes.byref(cache), _ptr(q), _ptr(out), int(bool(out_fp32)),
                                             float(softmax_scale), _stream(stream)), "kv_decode_attention_noalloc")
+
+
+def kv_decode_noalloc_status(clear: bool = False, stream=None) -> int:
+    """The status word of kv_decode_attention_noalloc's scratch array on the
+    current device (bit 0: a device wait timed out); waits for `stream`.
+    Returns the word; KVQ_ERR_TIMEOUT is reported through the word, not raised."""
+    word = ctypes.c_uint32(0)
+    code = _lib.kv_decode_noalloc_status(ctypes.byref(word), int(bool(clear)), _stream(stream))
+    if code not in (0, 8):
+        raise KvqError(code, "kv_decode_noalloc_status")
+    return int(word.value)
 
 
 def kivi_paged_cache_sizes(pcfg: kivi_paged_config) -> list:

@@ -25,7 +25,7 @@ def declared_functions():
 
 def test_every_declared_symbol_is_exported():
     names = declared_functions()
-    assert len(names) == 28
+    assert len(names) == 29
     lib = ctypes.CDLL(kvq.LIB_PATH)
     for n in names:
         assert hasattr(lib, n), n
@@ -461,3 +461,8 @@ def test_nvfp4_validation():
     assert quant(k, ws_bytes=16) == "KVQ_ERR_WORKSPACE"
     assert quant(k, x=None) == "KVQ_ERR_NULL"
     assert quant(k, seq_len=0) == "KVQ_ERR_ARG"
+
+
+def test_noalloc_status_needs_a_host_word():
+    # the pointer check comes before any device access
+    assert kvq._lib.kv_decode_noalloc_status(None, 0, None) == 1
