@@ -208,7 +208,7 @@ __device__ __noinline__ bool tr_window_chunks(const uint16_t* k_res, const uint1
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const __half hi = __float2half_rn(p[k]);
-      const __half lo = __float2half_rn(p[k] - __half2float(hi));
+      const __half lo = __float2half_rn((p[k] - __half2float(hi)) * kLoGain);
       bt[k] = movm_trans(h2_bits(__halves2half2(hi, lo)));
       l_run += p[k];
     }
@@ -505,7 +505,7 @@ __global__ void __launch_bounds__(128, 4) kivi_decode_tr_kernel(KiviDecodeArgs a
       float p[4];
       tr_softmax<MT>(sc, p, o_acc, m_run, l_run, vz_run);
 
-      // p' = p * s_t split into fp16 hi + lo (columns 2 tig, 2 tig + 1 of the
+      // p' = p * s_t split into fp16 hi + lo * kLoGain (columns 2 tig, 2 tig + 1 of the
       // token row), transposed into the B fragments of p . V; the scales and
       // zero points of tokens g + 8k are halves 2k + (g & 1) of records g / 2 and 4 + g / 2
       const uint4 vs = vmr[g >> 1], vz = vmr[4 + (g >> 1)];
@@ -519,7 +519,7 @@ __global__ void __launch_bounds__(128, 4) kivi_decode_tr_kernel(KiviDecodeArgs a
         const float s_t = (g & 1) ? sf.y : sf.x, z_t = (g & 1) ? zf.y : zf.x;
         const float pp = p[k] * s_t;
         const __half hi = __float2half_rn(pp);
-        const __half lo = __float2half_rn(pp - __half2float(hi));
+        const __half lo = __float2half_rn((pp - __half2float(hi)) * kLoGain);
         bt[k] = movm_trans(h2_bits(__halves2half2(hi, lo)));
         l_run += p[k];
         vz_run = fmaf(p[k], z_t, vz_run);
@@ -630,8 +630,8 @@ __global__ void __launch_bounds__(128, 4) kivi_decode_tr_kernel(KiviDecodeArgs a
     float* orow = o_s + (warp * 8 + tig) * D;
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
-      orow[16 * mt + g] = fmaf(o_acc[mt][0] + o_acc[mt][1], om_lo, vz_run);
-      orow[16 * mt + 8 + g] = fmaf(o_acc[mt][2] + o_acc[mt][3], om_hi, vz_run);
+      orow[16 * mt + g] = fmaf(fmaf(o_acc[mt][1], kLoGainInv, o_acc[mt][0]), om_lo, vz_run);
+      orow[16 * mt + 8 + g] = fmaf(fmaf(o_acc[mt][3], kLoGainInv, o_acc[mt][2]), om_hi, vz_run);
     }
     if (g == 0) {
       m_s[warp * 8 + tig] = m_run;

@@ -371,8 +371,8 @@ __global__ void copy_tokens_paged_kernel(PagedCopyArgs a) {
 //   q.k^T : A = q'_{h,d} = q_{h,d} * s_{g,d} split exactly into fp16 hi + lo
 //           (hi = fp16(q*s), lo = fma(q, s, -hi)); B = key codes (fields as
 //           fp16 subnormals); plus q . z_g on CUDA cores.
-//   p.V   : A = p_t * s_t split into fp16 hi + lo; B = value codes; plus
-//           sum_t p_t z_t on CUDA cores.
+//   p.V   : A = p_t * s_t split into fp16 hi + lo (lo carried times
+//           kLoGain); B = value codes; plus sum_t p_t z_t on CUDA cores.
 // Per window chunk the same tiles take fp16 operands straight from shared
 // memory (ldmatrix): A = q for q.k^T, A = p split into hi + lo, B = values.
 template <int D>
@@ -501,7 +501,7 @@ __device__ __noinline__ bool window_chunks(const uint16_t* k_res, const uint16_t
       const __half2 hh = __floats2half2_rn(p[2 * nt], p[2 * nt + 1]);
       const float2 hf = __half22float2(hh);
       phi[nt] = h2_bits(hh);
-      plo[nt] = pack_rn_f16x2(p[2 * nt] - hf.x, p[2 * nt + 1] - hf.y);
+      plo[nt] = pack_rn_f16x2((p[2 * nt] - hf.x) * kLoGain, (p[2 * nt + 1] - hf.y) * kLoGain);
       l_run += p[2 * nt] + p[2 * nt + 1];
     }
     if (!mbar_wait_bounded(wbar, wphase)) {
@@ -844,7 +844,7 @@ __global__ void __launch_bounds__(128, KVQ_DECODE_MIN_BLOCKS) kivi_decode_kernel
         const __half2 hh = __floats2half2_rn(pp0, pp1);
         const float2 hf = __half22float2(hh);
         phi[nt] = h2_bits(hh);
-        plo[nt] = pack_rn_f16x2(pp0 - hf.x, pp1 - hf.y);
+        plo[nt] = pack_rn_f16x2((pp0 - hf.x) * kLoGain, (pp1 - hf.y) * kLoGain);
         l_run += p[2 * nt] + p[2 * nt + 1];
         vz_run = fmaf(p[2 * nt], zf.x, fmaf(p[2 * nt + 1], zf.y, vz_run));
       }
@@ -959,8 +959,8 @@ __global__ void __launch_bounds__(128, KVQ_DECODE_MIN_BLOCKS) kivi_decode_kernel
     for (int nt = 0; nt < P::NTV; ++nt) {
       const float om = real_units ? 1.0f : ((kTwoFields && (nt & 1)) ? kInvP8 : kInvP6);
       const int c = 8 * nt + 2 * tig;
-      o_s[(warp * 8 + g) * D + c] = fmaf(o_acc[nt][0] + o_acc[nt][2], om, vz_run);
-      o_s[(warp * 8 + g) * D + c + 1] = fmaf(o_acc[nt][1] + o_acc[nt][3], om, vz_run);
+      o_s[(warp * 8 + g) * D + c] = fmaf(fmaf(o_acc[nt][2], kLoGainInv, o_acc[nt][0]), om, vz_run);
+      o_s[(warp * 8 + g) * D + c + 1] = fmaf(fmaf(o_acc[nt][3], kLoGainInv, o_acc[nt][1]), om, vz_run);
     }
     if (tig == 0) {
       m_s[warp * 8 + g] = m_run;

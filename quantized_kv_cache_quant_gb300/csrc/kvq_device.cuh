@@ -17,6 +17,15 @@ constexpr int kMaxSplits = 64;           // split-K partials per (batch row, que
 constexpr int kMaxGqa = 8;               // query heads per kv head handled by one MMA tile
 constexpr int kChunkUnits = 6;           // decode work units (groups) one 32-token window chunk is charged
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per wait
+// The decode splits each p * s_t (and each softmax weight p of a window
+// token) into fp16 hi + lo tensor-core operands on separate accumulator rows
+// or columns. The lo part is carried times kLoGain and its accumulator scaled
+// back once at the end: a product below fp16's normal range (a token whose
+// value scale is an fp16 subnormal) then keeps 11 more bits than the
+// subnormal grid 2^-24 gives. |lo| <= half an ulp of hi <= 16, so
+// |lo| * kLoGain <= 2^15 stays finite.
+constexpr float kLoGain = 2048.0f;
+constexpr float kLoGainInv = 1.0f / 2048.0f;
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -38,6 +38,28 @@ def assert_grouped_bytes_equal(gpu_cache, ocache, groups=None):
             raise AssertionError(f"{name}: {len(bad)} bytes differ, first at {bad[:5].tolist()}")
 
 
+def assert_all_grouped_bytes_equal(gpu_cache, ocache, rows_per_chunk=1):
+    """Bit-exact comparison of every group of every (batch row, kv head), the
+    oracle packed a few batch rows at a time (bounded host memory)."""
+    ng = ocache.n_grouped // 32
+    assert gpu_cache.n_grouped == ocache.n_grouped
+    got = {name: host(gpu_cache.grouped_view(name))[:, :, :ng] for name in
+           ("k_codes", "k_meta", "v_codes", "v_meta")}
+    for b0 in range(0, ocache.B, rows_per_chunk):
+        rows = slice(b0, b0 + rows_per_chunk)
+        want = {
+            "k_codes": layout.pack_key_codes(ocache.k_codes[rows], ocache.k_bits),
+            "k_meta": layout.pack_key_meta(ocache.k_scale[rows], ocache.k_zero[rows]),
+            "v_codes": layout.pack_value_codes(ocache.v_codes[rows], ocache.v_bits),
+            "v_meta": layout.pack_value_meta(ocache.v_scale[rows], ocache.v_zero[rows]),
+        }
+        for name, w in want.items():
+            g = got[name][rows]
+            if not np.array_equal(g, w):
+                bad = np.argwhere(g != w)
+                raise AssertionError(f"{name} rows {b0}+: {len(bad)} bytes differ, first at {bad[:5].tolist()}")
+
+
 def _pack_groups(ocache, groups):
     g = np.asarray(groups)
     return {

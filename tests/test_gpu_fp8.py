@@ -42,6 +42,55 @@ def _quantize(x16, table, num_blocks, vl, static_scale=None, fmt="e4m3", per_hea
     return p, p.scale
 
 
+def _code_table(scale, fmt="e4m3"):
+    """The oracle's byte for every fp16 bit pattern at this scale. The cast is
+    elementwise, so table[bits(x)] is the oracle's quantize of x: full-size
+    tensors are looked up instead of re-running the oracle on every element."""
+    allh = np.arange(65536, dtype=np.uint32).astype(np.uint16).view(np.float16)
+    with np.errstate(invalid="ignore"):          # the NaN and infinity patterns
+        return fp8.quantize(allh, scale, fmt)
+
+
+def _assert_every_record(pool, x16, table, scale, vl):
+    """Every (block, kv head) record of a full-size pool against the oracle
+    bytes, one batch row at a time (its blocks gathered on the device)."""
+    import torch
+    tab = _code_table(scale)
+    b, h, s, d = x16.shape
+    nbs = s // 16
+    view = pool.view()
+    for bi in range(b):
+        nat = tab[x16[bi].view(np.uint16)].reshape(h, nbs, 16, d).transpose(1, 0, 2, 3)
+        want = layout.fp8_pack_pool(nat, vl)
+        got = host(view.index_select(0, torch.from_numpy(table[bi].astype(np.int64)).cuda()))
+        if not np.array_equal(got, want):
+            bad = np.argwhere(got != want)
+            raise AssertionError(f"row {bi}: {len(bad)} bytes differ, first at {bad[:5].tolist()}")
+
+
+def _oracle_decode_tab(q16, k16, v16, ks, vs, heads, q_fp8=False):
+    """_oracle_decode for a per-tensor E4M3 scale with the keys and values
+    quantized through the oracle's code tables (the same bytes, faster)."""
+    b, hkv, s, d = k16.shape
+    if q_fp8:
+        q16 = fp8.query_hat(*fp8.quantize_query(q16))
+    dec = fp8.decode(np.arange(256, dtype=np.uint8), "e4m3")
+    ktab, vtab = _code_table(ks), _code_table(vs)
+    kh = lambda bi, hi: dec[ktab[k16[bi, hi].view(np.uint16)]] * np.float64(ks)
+    vh = lambda bi, hi: dec[vtab[v16[bi, hi].view(np.uint16)]] * np.float64(vs)
+    return attention.decode_attention(q16, kh, vh, hkv, default_scale(d), heads)
+
+
+def _wide_heads(w):
+    """Two kv heads of every batch row, with all their query heads."""
+    gq = w.q_heads // w.kv_heads
+    out = []
+    for bi in range(w.batch):
+        for h in sorted({(3 * bi) % w.kv_heads, (3 * bi + 5) % w.kv_heads}):
+            out += [(bi, h * gq + j) for j in range(gq)]
+    return out
+
+
 def _oracle_pool(x16, table, num_blocks, value_layout, scale, fmt="e4m3"):
     byts = fp8.quantize(x16, scale, fmt)
     nat = fp8.scatter_paged(byts, table, num_blocks, 16)
@@ -166,8 +215,8 @@ def test_block_table_permutation_invariance():
 
 def test_full_size_fp8_32k():
     """FP8 workload at full size: B 64, 8 kv heads, 32 q heads, D 128, 32768 tokens,
-    blocks of 16 through a random permutation. Scales exact; bytes of sampled
-    blocks exact; attention on sampled heads."""
+    blocks of 16 through a random permutation. Scales exact; every record of
+    both pools exact; attention on 512 of the 2048 query heads."""
     import torch
     w = workloads.FP8_32K
     k, v, q, table = workloads.fp8_inputs(w)
@@ -176,19 +225,18 @@ def test_full_size_fp8_32k():
     vpool, vscale = _quantize(v, table, nb_total, VALUE)
     ks_ref, vs_ref = fp8.dynamic_scale(k), fp8.dynamic_scale(v)
     assert host(kscale)[0] == ks_ref and host(vscale)[0] == vs_ref
-    rng = np.random.default_rng(3)
-    for _ in range(24):
-        b, h, j = int(rng.integers(w.batch)), int(rng.integers(w.kv_heads)), int(rng.integers(w.blocks_per_seq))
-        for x16, pool, sref, vl in ((k, kpool, ks_ref, KEY), (v, vpool, vs_ref, VALUE)):
-            blk = table[b, j]
-            want = layout.fp8_pack_pool(fp8.quantize(x16[b, h, 16 * j:16 * j + 16], sref)[None, None], vl)[0, 0]
-            assert np.array_equal(host(pool.view()[blk, h]), want)
+    _assert_every_record(kpool, k, table, ks_ref, KEY)
+    _assert_every_record(vpool, v, table, vs_ref, VALUE)
     seq_lens = np.full(w.batch, w.context)
     out, status = _decode(q, kpool, vpool, kscale, vscale, table, seq_lens, w.kv_heads, nb_total, w.context)
     assert status == 0
-    heads = sorted({(0, 0), (w.batch - 1, w.q_heads - 1), (17, 5), (40, 30), (63, 12), (5, 20)})
-    ref = _oracle_decode(q, k, v, ks_ref, vs_ref, seq_lens, heads)
+    heads = _wide_heads(w)
+    ref = _oracle_decode_tab(q, k, v, ks_ref, vs_ref, heads)
     assert_attention_close(out, ref, heads)
+    # the table route is the oracle's own arithmetic: one pair through the plain oracle agrees exactly
+    one = heads[:4]
+    assert np.array_equal(_oracle_decode(q, k, v, ks_ref, vs_ref, seq_lens, one)[tuple(np.array(one).T)],
+                          ref[tuple(np.array(one).T)])
     del kpool, vpool
     torch.cuda.empty_cache()
 
@@ -354,7 +402,7 @@ def test_fp8_domain_zero_query():
 
 def test_full_size_fp8_domain_attention_32k():
     """The 32K FP8 workload with the query in E4M3:
-    scales and query bytes exact, attention on sampled heads."""
+    scales and query bytes exact, attention on 512 of the 2048 query heads."""
     import torch
     w = workloads.FP8_32K
     k, v, q, table = workloads.fp8_inputs(w)
@@ -374,8 +422,8 @@ def test_full_size_fp8_domain_attention_32k():
     assert status == 0
     codes_ref, scale_ref = fp8.quantize_query(q)
     assert q_scale == scale_ref and np.array_equal(q8, codes_ref)
-    heads = sorted({(0, 0), (w.batch - 1, w.q_heads - 1), (17, 5), (40, 30), (63, 12), (5, 20)})
-    ref = _oracle_decode(q, k, v, ks_ref, vs_ref, seq_lens, heads, q_fp8=True)
+    heads = _wide_heads(w)
+    ref = _oracle_decode_tab(q, k, v, ks_ref, vs_ref, heads, q_fp8=True)
     assert_attention_close(out, ref, heads)
     del kpool, vpool
     torch.cuda.empty_cache()

@@ -10,8 +10,8 @@ import pytest
 from oracle.attention import default_scale
 from quantized_kv_cache_quant_gb300 import workloads
 
-from kvq_helpers import (assert_attention_close, assert_grouped_bytes_equal, assert_residual_equal, dev, host,
-                         oracle_attention, oracle_cache)
+from kvq_helpers import (assert_all_grouped_bytes_equal, assert_attention_close, assert_grouped_bytes_equal,
+                         assert_residual_equal, dev, host, oracle_attention, oracle_cache)
 
 pytestmark = pytest.mark.gpu
 
@@ -237,25 +237,26 @@ def test_full_size_decode(w):
     gc = kvq.KiviCache(w.batch, w.kv_heads, w.q_heads, w.head_dim, w.k_bits, w.v_bits, w.residual, w.max_tokens)
     gc.prefill(dev(x.k), dev(x.v))
     oc = oracle_cache(dict(k_bits=w.k_bits, v_bits=w.v_bits, residual=w.residual, max_tokens=w.max_tokens), x.k, x.v)
-    assert_grouped_bytes_equal(gc, oc)
+    assert_all_grouped_bytes_equal(gc, oc, rows_per_chunk=4)
     assert_residual_equal(gc, oc)
-    heads = _sample_heads(w.batch, w.q_heads, 12, w.seed)
     scale = default_scale(w.head_dim)
-    # attention over the prefilled cache, then one streaming decode step
+    # attention on every query head over the prefilled cache, then one streaming decode step
     out = host(gc.decode(dev(x.q[0])))
-    assert_attention_close(out, oracle_attention(oc, x.q[0], scale, heads), heads)
+    assert_attention_close(out, oracle_attention(oc, x.q[0], scale))
     gc.append(dev(x.k_new[0]), dev(x.v_new[0]))
     oc.append(x.k_new[0], x.v_new[0])
     assert_grouped_bytes_equal(gc, oc, groups=list(range(oc.n_grouped // 32 - 4, oc.n_grouped // 32)))
     out = host(gc.decode(dev(x.q[0])))
-    assert_attention_close(out, oracle_attention(oc, x.q[0], scale, heads), heads)
+    assert_attention_close(out, oracle_attention(oc, x.q[0], scale))
     assert gc.status() == 0
 
 
 def test_full_size_streaming_128k():
-    """128K streaming workload: prefill 131072 tokens, 512 decode steps with a
-    flush every 128 steps; every flushed group is compared bit for bit and
-    attention is checked at steps 0, 1, 127, 128, 255, 256 and 511."""
+    """128K streaming workload: prefill 131072 tokens (every byte of all 4092
+    groups x 32 pairs compared), 512 decode steps with a flush every 128
+    steps; every flushed group is compared bit for bit, attention is checked
+    on every query head at steps 0 and 511 and on sampled heads at steps 1,
+    127, 128, 255 and 256."""
     w = workloads.STREAM_128K
     kvq = _kvq()
     x = workloads.kivi_inputs(w)
@@ -263,10 +264,9 @@ def test_full_size_streaming_128k():
     gc.prefill(dev(x.k), dev(x.v))
     oc = oracle_cache(dict(k_bits=2, v_bits=2, residual=128, max_tokens=w.max_tokens), x.k, x.v)
     assert (gc.n_grouped, gc.n_resid) == (130944, 128)
-    rng = np.random.default_rng(4)
-    sample_groups = sorted(set(rng.integers(0, 4092, 64).tolist()) | {0, 4091})
-    assert_grouped_bytes_equal(gc, oc, groups=sample_groups)
-    heads = _sample_heads(w.batch, w.q_heads, 6, w.seed)
+    assert_all_grouped_bytes_equal(gc, oc)
+    heads = _sample_heads(w.batch, w.q_heads, 24, w.seed)
+    every = {0, w.decode_steps - 1}
     scale = default_scale(w.head_dim)
     check = {0, 1, 127, 128, 255, 256, 511}
     for step in range(w.decode_steps):
@@ -277,7 +277,9 @@ def test_full_size_streaming_128k():
             ng = gc.n_grouped // 32
             assert_grouped_bytes_equal(gc, oc, groups=list(range(ng - 4, ng)))
         out = gc.decode(dev(x.q[step]))
-        if step in check:
+        if step in every:
+            assert_attention_close(host(out), oracle_attention(oc, x.q[step], scale))
+        elif step in check:
             assert_attention_close(host(out), oracle_attention(oc, x.q[step], scale, heads), heads)
     assert (gc.n_grouped, gc.n_resid) == (131456, 128)
     assert_residual_equal(gc, oc)
