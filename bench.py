@@ -616,7 +616,7 @@ def table_rows(names):
                                        w.max_tokens, w.num_blocks)
             cache.table.copy_(dev(table))
             k_d, v_d, q_d = dev(x.k), dev(x.v), dev(x.q[0])
-            t_pre = timed(lambda: cache.prefill(k_d, v_d, lens.tolist()), reps=5)
+            t_pre = timed(lambda: cache.prefill(k_d, v_d, lens.tolist()), reps=20)
             out = torch.empty((w.batch, w.q_heads, w.head_dim), dtype=torch.float32, device="cuda")
             t_dec = timed(lambda: cache.decode(q_d, out=out))
             ng = [cache.n_grouped(b) for b in range(w.batch)]
@@ -631,7 +631,7 @@ def table_rows(names):
             cache = kvq.KiviCache(w.batch, w.kv_heads, w.q_heads, w.head_dim, w.k_bits, w.v_bits, w.residual,
                                   w.max_tokens)
             k_d, v_d, q_d = dev(x.k), dev(x.v), dev(x.q[0])
-            t_pre = timed(lambda: cache.prefill(k_d, v_d), reps=5)
+            t_pre = timed(lambda: cache.prefill(k_d, v_d), reps=20)
             out = torch.empty((w.batch, w.q_heads, w.head_dim), dtype=torch.float32, device="cuda")
             t_dec = timed(lambda: cache.decode(q_d, out=out))
             nbytes = metrics.kivi_decode_bytes(w.batch, w.kv_heads, w.q_heads, w.head_dim, w.k_bits, w.v_bits,

@@ -106,14 +106,6 @@ __global__ void __launch_bounds__(256) fp8_scale_kernel(const uint32_t* __restri
 // ---------------------------------------------------------------------------
 constexpr int kCastWarps = 4;
 
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-// wait until at most one group (the newest) of this thread's copies is in flight
-__device__ __forceinline__ void cp_async_wait_all_but_newest() {
-  asm volatile("cp.async.wait_group 1;" ::: "memory");
-}
 
 // x / scale, the IEEE fp32 quotient of the formula. MODE 0: the IEEE division
 // itself. MODE 1 and 2: from y = RN(1/scale) and one correction step, which is

@@ -71,69 +71,199 @@ __device__ __forceinline__ uint32_t group_code(float x, float zf, float sf, floa
   return min(__float2uint_rn(div_rn_by_rcp(__fsub_rn(x, zf), sf, rcp)), levels);
 }
 
-// One packed code word of a group (storage word u of lane (gg, tg)).
+// ---- 2-bit codes by thresholds -------------------------------------------
+// The group formula's code is a non-decreasing function of x (every step of it
+// is monotone), so for 2-bit codes code(x) = #{k = 1..3 : x >= theta_k} with
+// theta_k the smallest fp16 value whose code is at least k. The thresholds are
+// exact, from the rounding rules of the formula's two fp32 steps:
+//  * rint(q) >= k  <=>  q >= k - 1/2 (even k: the tie rounds to k) or
+//    q > k - 1/2 (odd k); q = fl32(d / s) reaches m = k - 1/2 from the
+//    midpoint between m and its fp32 neighbour (m's significand is even, so a
+//    tie there rounds to m). Hence code >= k  <=>  d >= D_k with the fp32
+//    threshold D_k = RU(s (1.5 - 2^-24)) for k = 2, and for k = 1, 3 the
+//    smallest fp32 above s (m + h), h = 2^-25, 2^-23 (one fused multiply-add
+//    rounded up, and one rounded down to see whether it was exact);
+//  * d = fl32(x - z) is monotone in x, so theta_k is the smallest fp16 x with
+//    fl32(x - z) >= D_k: RU16(z + D_k) when the subtraction is exact near it
+//    (checked at that value and the fp16 value below it), else found by a
+//    bisection over the fp16 order keys (x close to 0 while |z| is large).
+// Every element then costs three fp16 comparisons and no division.
+
+// Order keys of fp16 bit patterns: a pattern maps to an int in the order of
+// the values (both zeros to 0, +inf to 0x7C00), and back.
+__device__ __forceinline__ int f16_key(uint32_t b) {
+  return (b & 0x8000u) ? -static_cast<int>(b & 0x7FFFu) : static_cast<int>(b & 0x7FFFu);
+}
+__device__ __forceinline__ uint32_t f16_from_key(int key) {
+  return key >= 0 ? static_cast<uint32_t>(key) : (0x8000u | static_cast<uint32_t>(-key));
+}
+
+// D_k above (s > 0, k = 1, 2, 3).
+__device__ __forceinline__ float code_step(float s, int k) {
+  if (k == 2) return __fmaf_ru(-0x1p-24f, s, __fmul_rn(1.5f, s));
+  const float ms = __fmul_rn(k == 1 ? 0.5f : 2.5f, s);  // exact
+  const float h = (k == 1) ? 0x1p-25f : 0x1p-23f;
+  const float up = __fmaf_ru(h, s, ms), dn = __fmaf_rd(h, s, ms);
+  return (up == dn) ? __uint_as_float(__float_as_uint(up) + 1u) : up;  // exact: the next fp32 above
+}
+
+// fl32(x - z) >= d for the fp16 value with bits xb.
+__device__ __forceinline__ bool reaches(uint32_t xb, float zf, float d) {
+  return __fsub_rn(__half2float(__ushort_as_half(static_cast<unsigned short>(xb))), zf) >= d;
+}
+
+// theta_k as fp16 bits (+inf, 0x7C00, when no fp16 value reaches code k;
+// every code is 0 when s = 0).
+__device__ __forceinline__ uint32_t code_threshold(uint32_t zb, float zf, float sf, int k) {
+  if (sf == 0.0f) return 0x7C00u;
+  const float d = code_step(sf, k);
+  const uint32_t x0 = __half_as_ushort(__float2half_ru(__fadd_ru(zf, d)));
+  const int k0 = f16_key(x0), kz = f16_key(zb);
+  const bool r0 = reaches(x0, zf, d);
+  const bool r1 = (k0 - 1 > kz) && reaches(f16_from_key(k0 - 1), zf, d);
+  if (r0 && !r1) return x0;
+  // rare: bisection with reaches(lo) false and reaches(hi) true (z never reaches d > 0; +inf always does)
+  int lo = r0 ? kz : k0, hi = r0 ? k0 - 1 : 0x7C00;
+  for (int it = 0; it < 17 && hi - lo > 1; ++it) {
+    const int mid = lo + (hi - lo) / 2;
+    if (reaches(f16_from_key(mid), zf, d))
+      hi = mid;
+    else
+      lo = mid;
+  }
+  return f16_from_key(hi);
+}
+
+// One 2-bit code pair from thresholds (t1 <= t2 <= t3), per fp16 half: the
+// high code bit is [x >= t2] (as a mask m); the low bit compares x with t3 or
+// t1 as m selects, read as 1024 + bit (exact) whose bits are 0x6400 + bit; m
+// adds the high bit. A word adds eight such pairs, each shifted to its field;
+// the 0x6400 parts sum to a constant (kThresholdBase) that is subtracted once
+// per word.
+__device__ __forceinline__ uint32_t threshold_pair(__half2 x, uint32_t t1, uint32_t t2, uint32_t t3) {
+  const uint32_t m = __hge2_mask(x, bits_h2(t2));
+  const uint32_t tl = (m & t3) | (~m & t1);
+  const uint32_t lo = h2_bits(__hadd2(__hge2(x, bits_h2(tl)), __float2half2_rn(1024.0f)));
+  return lo | (m & 0x00020002u);
+}
+constexpr uint32_t threshold_base() {
+  uint32_t s = 0;
+  for (int f = 0; f < 8; ++f) s += 0x64006400u << (2 * f);
+  return s;
+}
+constexpr uint32_t kThresholdBase = threshold_base();
+
+// One packed code word of a group (storage word u of lane l = 4 gg + tg),
+// from the row-major tiles xk and xv (RS halves per token). The elements a
+// word packs come as fp16 pairs from one ldmatrix of four 8 x 8 tiles: keys
+// {x[8 nt + gg][d0], x[8 nt + gg][d0 + 1]} (tiles nt = 0..3 of tokens 8 nt ..,
+// channels d0 - 2 tg ..), values {x[t0][ch], x[t0 + 1][ch]} (the transposed
+// tiles of tokens t0 - 2 tg .., channels ch - gg ..).
 template <int D, int KB>
 __device__ __forceinline__ uint32_t key_word(const __half* xk, int RS, const float* sk, const float* zk,
-                                             const float* rk, int u, int gg, int tg) {
+                                             const float* rk, const uint4* thk, int u, int lane) {
   constexpr uint32_t KL = (1u << KB) - 1u;
+  const int tg = lane & 3;
   uint32_t w = 0;
 #pragma unroll
   for (int rr = 0; rr < (KB == 2 ? 2 : 1); ++rr) {
     const int ks = (KB == 2) ? u : (u >> 1);
     const int r = (KB == 2) ? rr : (u & 1);
     const int d0 = 16 * ks + 8 * r + 2 * tg;
-    const float2 s01 = *reinterpret_cast<const float2*>(sk + d0), z01 = *reinterpret_cast<const float2*>(zk + d0),
-                 r01 = *reinterpret_cast<const float2*>(rk + d0);
-    const float s0 = s01.x, s1 = s01.y, z0 = z01.x, z1 = z01.y, r0 = r01.x, r1 = r01.y;
+    uint32_t xr[4];
+    ldsm_x4(xr, xk + lane * RS + 16 * ks + 8 * r);  // lane l addresses row l of tile l / 8
+    if constexpr (KB == 2) {
+      const uint4 th = thk[d0 / 2];
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
-      const float2 x = __half22float2(reinterpret_cast<const __half2*>(xk)[(8 * nt + gg) * (RS / 2) + d0 / 2]);
-      const int f = (KB == 2) ? ((4 * r + nt + 1) & 7) : nt;
-      // fields never overlap: adding the shifted codes sets the same bits as or-ing them, and
-      // w + (c << s) is one shift-and-add
-      w += (group_code(x.x, z0, s0, r0, KL) << (KB * f)) + (group_code(x.y, z1, s1, r1, KL) << (16 + KB * f));
+      for (int nt = 0; nt < 4; ++nt) {
+        const int f = (4 * r + nt + 1) & 7;
+        w += threshold_pair(bits_h2(xr[nt]), th.x, th.y, th.z) << (2 * f);
+      }
+    } else {
+      const float2 s01 = *reinterpret_cast<const float2*>(sk + d0), z01 = *reinterpret_cast<const float2*>(zk + d0),
+                   r01 = *reinterpret_cast<const float2*>(rk + d0);
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        const float2 x = __half22float2(bits_h2(xr[nt]));
+        // fields never overlap: adding the shifted codes sets the same bits as or-ing them, and
+        // w + (c << s) is one shift-and-add
+        w += (group_code(x.x, z01.x, s01.x, r01.x, KL) << (KB * nt)) +
+             (group_code(x.y, z01.y, s01.y, r01.y, KL) << (16 + KB * nt));
+      }
     }
   }
-  return w;
+  return (KB == 2) ? w - kThresholdBase : w;
 }
 
 template <int D, int VB>
 __device__ __forceinline__ uint32_t value_word(const __half* xv, int RS, const float* sv, const float* zv,
-                                               const float* rv, int u, int gg, int tg) {
+                                               const float* rv, const uint4* thv, int u, int lane) {
   constexpr uint32_t VL = (1u << VB) - 1u;
   constexpr int NQ = D / 32;
+  const int tg = lane & 3;
   uint32_t w = 0;
 #pragma unroll
   for (int rr = 0; rr < (VB == 2 ? 2 : 1); ++rr) {
     const int ks = (VB == 2) ? u / NQ : u / (2 * NQ);
     const int r = (VB == 2) ? rr : (u / NQ) % 2;
     const int q = u % NQ;
-    const int t0 = 16 * ks + 8 * r + 2 * tg;
-    const float2 s01 = *reinterpret_cast<const float2*>(sv + t0), z01 = *reinterpret_cast<const float2*>(zv + t0),
-                 r01 = *reinterpret_cast<const float2*>(rv + t0);
-    const float s0 = s01.x, s1 = s01.y, z0 = z01.x, z1 = z01.y, r0 = r01.x, r1 = r01.y;
+    const int t0 = 16 * ks + 8 * r + 2 * tg;  // tokens t0, t0 + 1
+    uint32_t xr[4];
+    ldsm_x4_trans(xr, xv + (16 * ks + 8 * r + (lane & 7)) * RS + 8 * (4 * q + (lane >> 3)));
+    if constexpr (VB == 2) {
+      const uint4 th = thv[t0 / 2];
 #pragma unroll
-    for (int n = 0; n < 4; ++n) {
-      const int ch = 8 * (4 * q + n) + gg;
-      const float x0 = __half2float(xv[t0 * RS + ch]), x1 = __half2float(xv[(t0 + 1) * RS + ch]);
-      const int f = (VB == 2) ? ((4 * r + n + 1) & 7) : n;
-      w += (group_code(x0, z0, s0, r0, VL) << (VB * f)) + (group_code(x1, z1, s1, r1, VL) << (16 + VB * f));
+      for (int n = 0; n < 4; ++n) {
+        const int f = (4 * r + n + 1) & 7;
+        w += threshold_pair(bits_h2(xr[n]), th.x, th.y, th.z) << (2 * f);
+      }
+    } else {
+      const float2 s01 = *reinterpret_cast<const float2*>(sv + t0), z01 = *reinterpret_cast<const float2*>(zv + t0),
+                   r01 = *reinterpret_cast<const float2*>(rv + t0);
+#pragma unroll
+      for (int n = 0; n < 4; ++n) {
+        const float2 x = __half22float2(bits_h2(xr[n]));
+        w += (group_code(x.x, z01.x, s01.x, r01.x, VL) << (VB * n)) +
+             (group_code(x.y, z01.y, s01.y, r01.y, VL) << (16 + VB * n));
+      }
     }
   }
-  return w;
+  return (VB == 2) ? w - kThresholdBase : w;
 }
 
-// Quantize and pack one group of 32 tokens of one (batch row, kv head): the
-// fp16 rows k_src[0 .. 32*D) and v_src[...] (32 consecutive tokens of D
-// channels) become the four records at kc, km, vc and vm. Run by a whole
-// block of 128 threads.
+// Row stride of a staged 32-token tile (halves): the 8 rows of an ldmatrix
+// tile hit distinct banks.
+template <int D>
+struct Tile {
+  static constexpr int RS = D + 8;
+};
+
+// Start the 16-byte asynchronous copies of one group's fp16 rows k_src[0 ..
+// 32*D) and v_src[...] (32 consecutive tokens of D channels) into the tiles xk
+// and xv; the caller commits and waits. Run by a whole block of 128 threads.
+template <int D>
+__device__ __forceinline__ void load_group_async(const uint16_t* k_src, const uint16_t* v_src, __half* xk, __half* xv) {
+  constexpr int RS = Tile<D>::RS;
+  const uint4* srck = reinterpret_cast<const uint4*>(k_src);
+  const uint4* srcv = reinterpret_cast<const uint4*>(v_src);
+#pragma unroll
+  for (int i = threadIdx.x; i < 32 * D / 8; i += 128) {
+    const int row = i / (D / 8), c8 = i % (D / 8);
+    cp_async16(xk + row * RS + 8 * c8, srck + i);
+    cp_async16(xv + row * RS + 8 * c8, srcv + i);
+  }
+}
+
+// Quantize and pack one staged group of 32 tokens of one (batch row, kv head)
+// into the four records at kc, km, vc and vm (nothing is written when write is
+// false; the block still takes part in every barrier). Run by a whole block of
+// 128 threads after a barrier that makes the tiles visible; it leaves the
+// tiles unread behind a final barrier of its own.
 template <int D, int KB, int VB>
-__device__ __forceinline__ void quantize_group(const uint16_t* k_src, const uint16_t* v_src, uint8_t* kc, uint8_t* km,
-                                               uint8_t* vc, uint8_t* vm) {
+__device__ __forceinline__ void quantize_tiles(const __half* xk, const __half* xv, uint8_t* kc, uint8_t* km,
+                                               uint8_t* vc, uint8_t* vm, bool write) {
   using P = Kivi<D, KB, VB>;
-  constexpr int RS = D + 8;  // padded row stride (halves): rows start 4 banks apart
-  __shared__ __align__(16) __half xk[32 * RS];
-  __shared__ __align__(16) __half xv[32 * RS];
+  constexpr int RS = Tile<D>::RS;
   // scale, zero, RN(1/scale) per key channel and per value token (8-byte aligned: read in pairs)
   __shared__ __align__(8) float sk[D];
   __shared__ __align__(8) float zk[D];
@@ -141,19 +271,13 @@ __device__ __forceinline__ void quantize_group(const uint16_t* k_src, const uint
   __shared__ __align__(8) float sv[32];
   __shared__ __align__(8) float zv[32];
   __shared__ __align__(8) float rv[32];
-  __shared__ uint16_t skb[D], zkb[D], svb[32], zvb[32];           // fp16 bits of scale and zero
+  __shared__ uint16_t skb[D], zkb[D], svb[32], zvb[32];  // fp16 bits of scale and zero
+  // 2-bit thresholds: entry j = {t1, t2, t3} of channels (keys) or tokens (values) 2j and 2j + 1
+  __shared__ __align__(16) uint4 thk[D / 2];
+  __shared__ __align__(16) uint4 thv[16];
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const uint4* srck = reinterpret_cast<const uint4*>(k_src);
-  const uint4* srcv = reinterpret_cast<const uint4*>(v_src);
-#pragma unroll
-  for (int i = tid; i < 32 * D / 8; i += 128) {
-    const int row = i / (D / 8), c8 = i % (D / 8);
-    *reinterpret_cast<uint4*>(xk + row * RS + 8 * c8) = __ldcs(srck + i);
-    *reinterpret_cast<uint4*>(xv + row * RS + 8 * c8) = __ldcs(srcv + i);
-  }
-  __syncthreads();
 
   constexpr float KL = static_cast<float>((1 << KB) - 1);
   constexpr float VL = static_cast<float>((1 << VB) - 1);
@@ -169,6 +293,7 @@ __device__ __forceinline__ void quantize_group(const uint16_t* k_src, const uint
       mx = __hmax2(mx, v);
     }
     const float2 mnf = __half22float2(mn), mxf = __half22float2(mx);
+    uint32_t th[3] = {0u, 0u, 0u};  // KB == 2: thresholds of channels 2 tid (low half) and 2 tid + 1
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       __half s16, z16;
@@ -179,7 +304,13 @@ __device__ __forceinline__ void quantize_group(const uint16_t* k_src, const uint
       rk[c] = (__half2float(s16) == 0.0f) ? 0.0f : __frcp_rn(__half2float(s16));
       skb[c] = __half_as_ushort(s16);
       zkb[c] = __half_as_ushort(z16);
+      if constexpr (KB == 2) {
+#pragma unroll
+        for (int k = 1; k <= 3; ++k)
+          th[k - 1] |= code_threshold(__half_as_ushort(z16), __half2float(z16), __half2float(s16), k) << (16 * e);
+      }
     }
+    if constexpr (KB == 2) thk[tid] = make_uint4(th[0], th[1], th[2], 0u);
   } else if (warp >= 2) {
     // values: warps 2 and 3, two lanes per token, each over half of the row
     // with fp16 pair min/max; lane L reads its words in the order (c + L) mod
@@ -198,48 +329,61 @@ __device__ __forceinline__ void quantize_group(const uint16_t* k_src, const uint
     float mnf = fminf(mnf2.x, mnf2.y), mxf = fmaxf(mxf2.x, mxf2.y);
     mnf = fminf(mnf, __shfl_xor_sync(0xffffffffu, mnf, 16));
     mxf = fmaxf(mxf, __shfl_xor_sync(0xffffffffu, mxf, 16));
+    __half s16, z16;
+    group_scale_zero(mnf, mxf, VL, s16, z16);
     if (hh == 0) {
-      __half s16, z16;
-      group_scale_zero(mnf, mxf, VL, s16, z16);
       sv[t] = __half2float(s16);
       zv[t] = __half2float(z16);
       rv[t] = (__half2float(s16) == 0.0f) ? 0.0f : __frcp_rn(__half2float(s16));
       svb[t] = __half_as_ushort(s16);
       zvb[t] = __half_as_ushort(z16);
     }
+    if constexpr (VB == 2) {
+      // both lanes of the token share its three thresholds: t1 on lane hh = 0, t2 and t3 on hh = 1
+      uint16_t* th16 = reinterpret_cast<uint16_t*>(thv + (t >> 1)) + (t & 1);
+#pragma unroll
+      for (int k = 1; k <= 2; ++k) {
+        const int kk = hh ? k + 1 : 1;
+        if (hh || k == 1)
+          th16[2 * (kk - 1)] = static_cast<uint16_t>(
+              code_threshold(__half_as_ushort(z16), __half2float(z16), __half2float(s16), kk));
+      }
+    }
   }
   __syncthreads();
 
-  // Code words, computed straight from the staged tile: warps 0-1 the key
+  // Code words, computed straight from the staged tiles: warps 0-1 the key
   // words, warps 2-3 the value words. Storage words 4*ug .. 4*ug + 3 of
   // fragment lane L are one 16-byte chunk (uint4 ug*32 + L); lane L of a warp
-  // computes that chunk, so each shared-memory load of the warp has all 32
-  // fragment lanes on the same word (conflict-free) and each store writes 512
-  // contiguous bytes.
-  if (warp < 2) {
+  // computes that chunk (its elements from conflict-free ldmatrix loads), and
+  // each store of the warp writes 512 contiguous bytes.
+  if (!write) {
+    // a skipped pool block: nothing to compute or store
+  } else if (warp < 2) {
     uint4* kdst = reinterpret_cast<uint4*>(kc);
     for (int ug = warp; ug < P::KW / 4; ug += 2) {
       uint4 w;
-      w.x = key_word<D, KB>(xk, RS, sk, zk, rk, 4 * ug, lane >> 2, lane & 3);
-      w.y = key_word<D, KB>(xk, RS, sk, zk, rk, 4 * ug + 1, lane >> 2, lane & 3);
-      w.z = key_word<D, KB>(xk, RS, sk, zk, rk, 4 * ug + 2, lane >> 2, lane & 3);
-      w.w = key_word<D, KB>(xk, RS, sk, zk, rk, 4 * ug + 3, lane >> 2, lane & 3);
+      w.x = key_word<D, KB>(xk, RS, sk, zk, rk, thk, 4 * ug, lane);
+      w.y = key_word<D, KB>(xk, RS, sk, zk, rk, thk, 4 * ug + 1, lane);
+      w.z = key_word<D, KB>(xk, RS, sk, zk, rk, thk, 4 * ug + 2, lane);
+      w.w = key_word<D, KB>(xk, RS, sk, zk, rk, thk, 4 * ug + 3, lane);
       kdst[ug * 32 + lane] = w;
     }
   } else {
     uint4* vdst = reinterpret_cast<uint4*>(vc);
     for (int ug = warp - 2; ug < P::VW / 4; ug += 2) {
       uint4 w;
-      w.x = value_word<D, VB>(xv, RS, sv, zv, rv, 4 * ug, lane >> 2, lane & 3);
-      w.y = value_word<D, VB>(xv, RS, sv, zv, rv, 4 * ug + 1, lane >> 2, lane & 3);
-      w.z = value_word<D, VB>(xv, RS, sv, zv, rv, 4 * ug + 2, lane >> 2, lane & 3);
-      w.w = value_word<D, VB>(xv, RS, sv, zv, rv, 4 * ug + 3, lane >> 2, lane & 3);
+      w.x = value_word<D, VB>(xv, RS, sv, zv, rv, thv, 4 * ug, lane);
+      w.y = value_word<D, VB>(xv, RS, sv, zv, rv, thv, 4 * ug + 1, lane);
+      w.z = value_word<D, VB>(xv, RS, sv, zv, rv, thv, 4 * ug + 2, lane);
+      w.w = value_word<D, VB>(xv, RS, sv, zv, rv, thv, 4 * ug + 3, lane);
       vdst[ug * 32 + lane] = w;
     }
   }
 
   // Key meta: record ks*4 + tig = {s[d0], s[d0+1], s[d0+8], s[d0+9], z[...]}.
-  if (tid < D / 4) {
+  if (!write) {
+  } else if (tid < D / 4) {
     const int ks = tid >> 2, tg = tid & 3, d0 = 16 * ks + 2 * tg;
     uint4 rec;
     rec.x = skb[d0] | (static_cast<uint32_t>(skb[d0 + 1]) << 16);
@@ -258,19 +402,48 @@ __device__ __forceinline__ void quantize_group(const uint16_t* k_src, const uint
     rec.w = src[24 + 2 * tg] | (static_cast<uint32_t>(src[25 + 2 * tg]) << 16);
     reinterpret_cast<uint4*>(vm)[i] = rec;
   }
+  __syncthreads();  // the tiles and the block's statistics are free again
 }
 
-// Grid (groups, H_kv, B): group blockIdx.x of the source rows from src_tok0 on
-// goes to group dst_group0 + blockIdx.x of the contiguous grouped region.
+// Persistent blocks over the items (group, kv head, batch row), group index
+// fastest: item i goes to group dst_group0 + grp of the contiguous grouped
+// region, read from source token src_tok0 + 32 * grp. Each block stages the
+// next item's tiles with asynchronous copies into its second buffer while it
+// quantizes the current one.
 template <int D, int KB, int VB>
 __global__ void __launch_bounds__(128) kivi_quantize_kernel(QuantGroupsArgs a) {
   using P = Kivi<D, KB, VB>;
-  const int grp = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const long long bh = static_cast<long long>(b) * a.kv_heads + h;
-  const long long src_off = bh * a.src_bh_stride + static_cast<long long>(a.src_tok0 + 32 * grp) * D;
-  const long long gi = bh * a.groups_cap + a.dst_group0 + grp;
-  quantize_group<D, KB, VB>(a.k_src + src_off, a.v_src + src_off, a.k_codes + gi * P::KC, a.k_meta + gi * P::KM,
-                            a.v_codes + gi * P::VC, a.v_meta + gi * P::VM);
+  constexpr int TILE = 32 * Tile<D>::RS;
+  __shared__ __align__(16) __half tiles[2][2][TILE];  // [buffer][keys, values]
+  const int n_bh = a.kv_heads * a.batch;
+  // item = bh * n_groups + grp, advanced by gridDim.x = step_bh * n_groups + step_grp per turn
+  const int step_bh = static_cast<int>(gridDim.x) / a.n_groups, step_grp = static_cast<int>(gridDim.x) % a.n_groups;
+  int bh = static_cast<int>(blockIdx.x) / a.n_groups, grp = static_cast<int>(blockIdx.x) % a.n_groups;
+  if (bh >= n_bh) return;
+  auto src_off = [&](int pbh, int pgrp) {
+    return static_cast<long long>(pbh) * a.src_bh_stride + static_cast<long long>(a.src_tok0 + 32 * pgrp) * D;
+  };
+  {
+    const long long off = src_off(bh, grp);
+    load_group_async<D>(a.k_src + off, a.v_src + off, tiles[0][0], tiles[0][1]);
+  }
+  cp_async_commit();
+  for (int buf = 0; bh < n_bh; buf ^= 1) {
+    int nbh = bh + step_bh, ngrp = grp + step_grp;
+    if (ngrp >= a.n_groups) ngrp -= a.n_groups, ++nbh;
+    if (nbh < n_bh) {
+      const long long off = src_off(nbh, ngrp);
+      load_group_async<D>(a.k_src + off, a.v_src + off, tiles[buf ^ 1][0], tiles[buf ^ 1][1]);
+    }
+    cp_async_commit();
+    cp_async_wait_all_but_newest();  // this item's copies have landed
+    __syncthreads();
+    const long long gi = static_cast<long long>(bh) * a.groups_cap + a.dst_group0 + grp;
+    quantize_tiles<D, KB, VB>(tiles[buf][0], tiles[buf][1], a.k_codes + gi * P::KC, a.k_meta + gi * P::KM,
+                              a.v_codes + gi * P::VC, a.v_meta + gi * P::VM, true);
+    bh = nbh;
+    grp = ngrp;
+  }
 }
 
 // The sequence that owns item x of a batched launch: the b < n with
@@ -288,24 +461,59 @@ __device__ __forceinline__ int seq_of(const int* begin, int n, long long x) {
   return lo;
 }
 
-// Grid (total groups, H_kv): item blockIdx.x is group x - begin[b] of sequence
-// b's range, read from source token src0[b] + 32 * (x - begin[b]) and written
-// to the pool block of logical group dst0[b] + (x - begin[b]), its four records
-// back to back in the block's entry for kv head h. A block-table entry outside
-// [0, num_blocks) is skipped: nothing is written for it.
+// Persistent blocks over the items (x, kv head h), x fastest: x is group
+// x - begin[b] of sequence b's range, read from source token src0[b] + 32 *
+// (x - begin[b]) and written to the pool block of logical group dst0[b] + (x -
+// begin[b]), its four records back to back in the block's entry for kv head
+// h. A block-table entry outside [0, num_blocks) is skipped: nothing is
+// written for it. The next item's tiles are staged while this one is
+// quantized, as in the contiguous kernel.
 template <int D, int KB, int VB>
 __global__ void __launch_bounds__(128) kivi_quantize_paged_kernel(PagedQuantArgs a) {
   using P = Kivi<D, KB, VB>;
-  const int x = blockIdx.x, h = blockIdx.y;
-  const int b = seq_of(a.r.begin, a.n_seqs, x);
-  const int grp = x - a.r.begin[b];
-  const long long bh = static_cast<long long>(b) * a.q.kv_heads + h;
-  const long long src_off = bh * a.q.src_bh_stride + static_cast<long long>(a.r.src0[b] + 32 * grp) * D;
-  const int blk = __ldg(a.pools.block_table + static_cast<long long>(b) * a.pools.groups_cap + a.r.dst0[b] + grp);
-  if (blk < 0 || blk >= a.pools.num_blocks) return;
-  uint8_t* e = a.q.k_codes + (static_cast<long long>(blk) * a.q.kv_heads + h) * P::STAGE;
-  quantize_group<D, KB, VB>(a.q.k_src + src_off, a.q.v_src + src_off, e, e + P::KC, e + P::KC + P::KM,
-                            e + P::KC + P::KM + P::VC);
+  constexpr int TILE = 32 * Tile<D>::RS;
+  __shared__ __align__(16) __half tiles[2][2][TILE];
+  const int total_x = a.r.begin[a.n_seqs];
+  // item = h * total_x + x, advanced by gridDim.x = step_h * total_x + step_x per turn; the
+  // sequence b of x only moves forward while h stays, and restarts its search when h moves
+  const int step_h = static_cast<int>(gridDim.x) / total_x, step_x = static_cast<int>(gridDim.x) % total_x;
+  int h = static_cast<int>(blockIdx.x) / total_x, x = static_cast<int>(blockIdx.x) % total_x;
+  if (h >= a.q.kv_heads) return;
+  int b = seq_of(a.r.begin, a.n_seqs, x);
+  auto src_off = [&](int pb, int px, int ph) {
+    const long long bh = static_cast<long long>(pb) * a.q.kv_heads + ph;
+    return bh * a.q.src_bh_stride + static_cast<long long>(a.r.src0[pb] + 32 * (px - a.r.begin[pb])) * D;
+  };
+  {
+    const long long off = src_off(b, x, h);
+    load_group_async<D>(a.q.k_src + off, a.q.v_src + off, tiles[0][0], tiles[0][1]);
+  }
+  cp_async_commit();
+  for (int buf = 0; h < a.q.kv_heads; buf ^= 1) {
+    int nh = h + step_h, nx = x + step_x, nb = b;
+    if (nx >= total_x) nx -= total_x, ++nh;
+    if (nh != h || nx < x) {
+      nb = seq_of(a.r.begin, a.n_seqs, nx);
+    } else {
+      while (a.r.begin[nb + 1] <= nx) ++nb;  // nb < n_seqs: nx < total_x = begin[n_seqs]
+    }
+    if (nh < a.q.kv_heads) {
+      const long long off = src_off(nb, nx, nh);
+      load_group_async<D>(a.q.k_src + off, a.q.v_src + off, tiles[buf ^ 1][0], tiles[buf ^ 1][1]);
+    }
+    cp_async_commit();
+    cp_async_wait_all_but_newest();
+    __syncthreads();
+    const int grp = x - a.r.begin[b];
+    const int blk = __ldg(a.pools.block_table + static_cast<long long>(b) * a.pools.groups_cap + a.r.dst0[b] + grp);
+    const bool ok = blk >= 0 && blk < a.pools.num_blocks;
+    uint8_t* e = a.q.k_codes + (static_cast<long long>(ok ? blk : 0) * a.q.kv_heads + h) * P::STAGE;
+    quantize_tiles<D, KB, VB>(tiles[buf][0], tiles[buf][1], e, e + P::KC, e + P::KC + P::KM,
+                              e + P::KC + P::KM + P::VC, ok);
+    h = nh;
+    x = nx;
+    b = nb;
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -977,17 +1185,36 @@ __global__ void __launch_bounds__(128, KVQ_DECODE_MIN_BLOCKS) kivi_decode_kernel
 
 constexpr int kDecodeStages = 4;
 
+// Persistent quantize grid: every resident block slot of the GPU (occupancy
+// queried once per kernel and device), at most one block per item.
+template <class Kern>
+int quantize_grid(Kern kern, long long items, int (&cached)[64]) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  if (cached[dev] == 0) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 128, 0) != cudaSuccess || per_sm < 1) per_sm = 1;
+    cached[dev] = per_sm;
+  }
+  const long long slots = static_cast<long long>(cached[dev]) * device_sm_count();
+  return static_cast<int>(items < slots ? items : slots);
+}
+
 template <int D, int KB, int VB>
 cudaError_t quantize_dispatch(const QuantGroupsArgs& a, cudaStream_t s) {
-  dim3 grid(a.n_groups, a.kv_heads, a.batch);
-  kivi_quantize_kernel<D, KB, VB><<<grid, 128, 0, s>>>(a);
+  const long long total = static_cast<long long>(a.n_groups) * a.kv_heads * a.batch;
+  static int cached[64] = {0};
+  const int blocks = quantize_grid(kivi_quantize_kernel<D, KB, VB>, total, cached);
+  kivi_quantize_kernel<D, KB, VB><<<blocks, 128, 0, s>>>(a);
   return cudaGetLastError();
 }
 
 template <int D, int KB, int VB>
 cudaError_t quantize_paged_dispatch(const PagedQuantArgs& a, cudaStream_t s) {
-  dim3 grid(a.r.begin[a.n_seqs], a.q.kv_heads);
-  kivi_quantize_paged_kernel<D, KB, VB><<<grid, 128, 0, s>>>(a);
+  const long long total = static_cast<long long>(a.r.begin[a.n_seqs]) * a.q.kv_heads;
+  static int cached[64] = {0};
+  const int blocks = quantize_grid(kivi_quantize_paged_kernel<D, KB, VB>, total, cached);
+  kivi_quantize_paged_kernel<D, KB, VB><<<blocks, 128, 0, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -118,6 +118,16 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], const void* row)
                : "memory");
 }
 
+// 16-byte asynchronous global -> shared copies (L2 only), committed in groups.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// wait until at most one group (the newest) of this thread's copies is in flight
+__device__ __forceinline__ void cp_async_wait_all_but_newest() {
+  asm volatile("cp.async.wait_group 1;" ::: "memory");
+}
+
 // The correctly rounded fp32 quotient d / s from y = RN(1/s), by Markstein's
 // correction step (P. Markstein, "Computation of elementary functions on the
 // IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990; Handbook of

@@ -7,6 +7,7 @@ the same dequantized values.
 import numpy as np
 import pytest
 
+from oracle import kivi
 from oracle.attention import default_scale
 from quantized_kv_cache_quant_gb300 import workloads
 
@@ -304,6 +305,72 @@ def test_prefill_exact_ties(kb, vb):
     nudge = rng.random(k.shape) < 0.2                                       # some values one ulp off a tie
     k = np.where(nudge, np.nextafter(k, np.float16(np.inf)), k).astype(np.float16)
     v = k.copy()
+    gc = kvq.KiviCache(b, h, 2 * h, d, kb, vb, 0, s)
+    gc.prefill(dev(k), dev(v))
+    oc = oracle_cache(dict(k_bits=kb, v_bits=vb, residual=0, max_tokens=s), k, v)
+    assert_grouped_bytes_equal(gc, oc)
+
+
+def _f16_range(mn, mx):
+    """Every fp16 value in [mn, mx] in increasing order (-0 left out)."""
+    def key(h):
+        b = int(np.array([h], np.float16).view(np.uint16)[0])
+        return -(b & 0x7FFF) if b & 0x8000 else b
+    ks = np.arange(key(mn), key(mx) + 1)
+    bits = np.where(ks >= 0, ks, 0x8000 | (-ks)).astype(np.uint16)
+    return bits.view(np.float16)
+
+
+def _code_steps(mn, mx, bits):
+    """The fp16 values where the oracle's code changes for a group of min mn and
+    max mx, and the values just below them: rows [mn, mx, x] keep the group's
+    min and max, so their third code is code(x)."""
+    xs = _f16_range(mn, mx)
+    rows = np.stack([np.full(xs.size, mn, np.float16), np.full(xs.size, mx, np.float16), xs], axis=-1)
+    codes = kivi.quantize_groups(rows, bits)[0][:, 2].astype(int)
+    up = np.nonzero(np.diff(codes) > 0)[0]
+    return np.unique(np.concatenate([xs[up], xs[up + 1]]))
+
+
+@pytest.mark.parametrize("kb,vb", [(2, 2), (4, 4), (2, 4)])
+def test_prefill_at_every_code_step(kb, vb):
+    """Groups whose elements sit on both sides of every step of the code
+    function (found by the oracle over all fp16 values of the group's range),
+    for ranges that are symmetric about 0 (a step near 0, where fp32 rounding of
+    x - min moves it), tiny (subnormal scales), up to +-65504, one-signed,
+    constant and zero: every byte must match."""
+    kvq = _kvq()
+    rng = np.random.default_rng(kb * 10 + vb + 7)
+    ranges = [(-3.0, 3.0), (-1000.0, 1000.0), (-65504.0, 65504.0), (-1e-6, 1e-6), (-6e-8, 6e-8), (0.0, 2.0),
+              (-2.0, 0.0), (1.0, 1.0), (0.0, 0.0), (-5e4, 3e-5), (-3e-5, 5e4), (-1000.0, 1e-3), (100.0, 100.5),
+              (-60000.0, 2.0), (-0.75, 0.25), (5e-5, 7e-5)]
+    for _ in range(16):
+        a, c = sorted(rng.standard_normal(2) * 10.0 ** rng.uniform(-6, 4.5))
+        ranges.append((a, c))
+    groups = []
+    for a, c in ranges:
+        mn, mx = np.float16(a), np.float16(c)
+        steps = _code_steps(mn, mx, max(kb, vb))
+        steps = steps if kb == vb else np.unique(np.concatenate([steps, _code_steps(mn, mx, min(kb, vb))]))
+        groups.append((mn, mx, steps))
+    b, h, d, ng = 2, 2, 128, 4
+    s = 32 * ng
+    k = np.empty((b, h, s, d), np.float16)
+    v = np.empty((b, h, s, d), np.float16)
+    for bi in range(b):
+        for hi in range(h):
+            for g in range(ng):
+                for ch in range(d):                    # key group: channel ch over 32 tokens
+                    mn, mx, steps = groups[int(rng.integers(len(groups)))]
+                    col = rng.choice(_f16_range(mn, mx), 30)
+                    take = steps[:30] if steps.size <= 30 else rng.choice(steps, 30, replace=False)
+                    col[:take.size] = take
+                    k[bi, hi, 32 * g:32 * g + 32, ch] = rng.permutation(np.concatenate([[mn, mx], col]))
+                for t in range(32 * g, 32 * g + 32):   # value group: token t over 128 channels
+                    mn, mx, steps = groups[int(rng.integers(len(groups)))]
+                    row = rng.choice(_f16_range(mn, mx), d - 2)
+                    row[:steps.size] = steps[:d - 2]
+                    v[bi, hi, t] = rng.permutation(np.concatenate([[mn, mx], row]))
     gc = kvq.KiviCache(b, h, 2 * h, d, kb, vb, 0, s)
     gc.prefill(dev(k), dev(v))
     oc = oracle_cache(dict(k_bits=kb, v_bits=vb, residual=0, max_tokens=s), k, v)
