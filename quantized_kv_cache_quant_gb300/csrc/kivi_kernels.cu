@@ -61,14 +61,24 @@ __device__ __forceinline__ void group_scale_zero(float mn, float mx, float level
   z16 = __float2half_rn(__fadd_rn(mn, 0.0f));  // exact; -0 becomes +0
 }
 
-// The group formula's code clamp(rint(fl32((x - z) / s)), 0, levels). The
-// quotient comes from rcp = RN(1/s) and one correction step, bit-identical to
-// the IEEE division here (x, z and s are fp16 values, so nothing under- or
-// overflows; s = 0 has rcp = 0 and gives code 0 as the formula does), and
-// rint + clamp are one round-to-nearest-even conversion (x >= z: no negative
-// quotients) and a min.
-__device__ __forceinline__ uint32_t group_code(float x, float zf, float sf, float rcp, uint32_t levels) {
-  return min(__float2uint_rn(div_rn_by_rcp(__fsub_rn(x, zf), sf, rcp)), levels);
+// The group formula's codes clamp(rint(fl32((x - z) / s)), 0, levels) of two
+// fp16 values x (one group each: zero points z, scales s, reciprocals
+// rcp = RN(1/s)) in packed fp32 operations, as {code0, code1} in the two
+// 16-bit halves. The quotient comes from rcp and one correction step (q0 =
+// d rcp, r = d - q0 s by fused multiply-add, q = q0 + r rcp), bit-identical
+// to the IEEE division here (x, z and s are fp16 values, so nothing under- or
+// overflows; s = 0 has rcp = 0 and gives code 0 as the formula does). x >= z
+// leaves no negative quotient, so q + 2^23 rounds q to an integer to nearest
+// even in its low bits (q < 2^22); the two low halves are merged and clamped
+// to the top code with one 16-bit SIMD min.
+__device__ __forceinline__ uint32_t group_code_pair(__half2 x, float2 zf, float2 sf, float2 rcp, uint32_t levels) {
+  const float2 d = __fadd2_rn(__half22float2(x), make_float2(-zf.x, -zf.y));
+  const float2 q0 = __fmul2_rn(d, rcp);
+  const float2 r = __ffma2_rn(q0, make_float2(-sf.x, -sf.y), d);
+  const float2 q = __ffma2_rn(r, rcp, q0);
+  const float2 t = __fadd2_rn(q, make_float2(0x1p23f, 0x1p23f));
+  const uint32_t pair = __byte_perm(__float_as_uint(t.x), __float_as_uint(t.y), 0x5410);
+  return __vminu2(pair, levels * 0x00010001u);
 }
 
 // ---- 2-bit codes by thresholds -------------------------------------------
@@ -183,13 +193,8 @@ __device__ __forceinline__ uint32_t key_word(const __half* xk, int RS, const flo
       const float2 s01 = *reinterpret_cast<const float2*>(sk + d0), z01 = *reinterpret_cast<const float2*>(zk + d0),
                    r01 = *reinterpret_cast<const float2*>(rk + d0);
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-        const float2 x = __half22float2(bits_h2(xr[nt]));
-        // fields never overlap: adding the shifted codes sets the same bits as or-ing them, and
-        // w + (c << s) is one shift-and-add
-        w += (group_code(x.x, z01.x, s01.x, r01.x, KL) << (KB * nt)) +
-             (group_code(x.y, z01.y, s01.y, r01.y, KL) << (16 + KB * nt));
-      }
+      for (int nt = 0; nt < 4; ++nt)  // fields never overlap: adding the shifted pair sets the same bits as or-ing
+        w += group_code_pair(bits_h2(xr[nt]), z01, s01, r01, KL) << (KB * nt);
     }
   }
   return (KB == 2) ? w - kThresholdBase : w;
@@ -221,11 +226,7 @@ __device__ __forceinline__ uint32_t value_word(const __half* xv, int RS, const f
       const float2 s01 = *reinterpret_cast<const float2*>(sv + t0), z01 = *reinterpret_cast<const float2*>(zv + t0),
                    r01 = *reinterpret_cast<const float2*>(rv + t0);
 #pragma unroll
-      for (int n = 0; n < 4; ++n) {
-        const float2 x = __half22float2(bits_h2(xr[n]));
-        w += (group_code(x.x, z01.x, s01.x, r01.x, VL) << (VB * n)) +
-             (group_code(x.y, z01.y, s01.y, r01.y, VL) << (16 + VB * n));
-      }
+      for (int n = 0; n < 4; ++n) w += group_code_pair(bits_h2(xr[n]), z01, s01, r01, VL) << (VB * n);
     }
   }
   return (VB == 2) ? w - kThresholdBase : w;
