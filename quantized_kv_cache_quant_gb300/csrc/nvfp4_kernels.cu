@@ -23,16 +23,18 @@ namespace {
 constexpr int kBlock = 16;    // tokens per paged block
 constexpr int kCastWarps = 4;
 
-// Two fp32 values -> one byte of two E2M1 codes (round to nearest even,
-// saturating to +-6); `lo` goes to the low nibble.
-__device__ __forceinline__ uint32_t f32x2_to_e2m1x2(float lo, float hi) {
+// Four fp32 pairs -> four bytes of E2M1 codes in one word (byte i from pair
+// (lo[i], hi[i]), lo in the low nibble; round to nearest even, saturating).
+__device__ __forceinline__ uint32_t f32x8_to_e2m1x8(const float2 (&q)[4]) {
   uint32_t r;
-  asm("{\n\t.reg .b8 t;\n\t.reg .b16 u;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\t"
-      "mov.b16 u, {t, 0};\n\t"
-      "cvt.u32.u16 %0, u;\n\t}"
+  asm("{\n\t.reg .b8 t0, t1, t2, t3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t3, %8, %7;\n\t"
+      "mov.b32 %0, {t0, t1, t2, t3};\n\t}"
       : "=r"(r)
-      : "f"(hi), "f"(lo));
+      : "f"(q[0].x), "f"(q[0].y), "f"(q[1].x), "f"(q[1].y), "f"(q[2].x), "f"(q[2].y), "f"(q[3].x), "f"(q[3].y));
   return r;
 }
 
@@ -65,117 +67,194 @@ __device__ __forceinline__ uint32_t e4m3_pair(uint32_t w, int h) {
 }
 
 // ---------------------------------------------------------------------------
-// Cast + scatter: one warp per (b, h, logical block) unit. The warp stages the
-// unit's 16 x D fp16 values (rows past the sequence zero), computes the
-// scale of each (token, 16-channel block), then writes the record: every lane
-// its D/4 code bytes in 16-byte chunks (chunk c of lane l at byte (c*32 +
-// l)*16), then the D scale bytes, in the in-block order of the role.
+// Cast + scatter: one warp per (b, h, logical block) unit, the units of a warp
+// a grid-stride walk. Each warp stages the next unit's 16 x D fp16 values in
+// its second shared-memory buffer with asynchronous copies (rows past the
+// sequence zero-filled) while it casts the current one: the scale of each
+// (token, 16-channel block), then the record, every lane its D/4 code bytes in
+// 16-byte chunks (chunk c of lane l at byte (c*32 + l)*16), then the D scale
+// bytes, in the in-block order of the role.
+//
+// Per element pair the quotient fl32(x / d), d = fl32(S_b * s_t), comes from
+// y = RN(1/d) and one correction step in packed fp32 operations (exact for
+// 2^-96 <= d <= 2^96; a unit with another nonzero d takes the IEEE division
+// per element), the sign of a zero x is restored, and a block whose scale is
+// 0 has its x masked to +0 first, so that all its codes are 0.
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ void cp_async16_zfill(void* dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src), "r"(valid ? 16 : 0)
+               : "memory");
+}
+
+// fl32(x / d) for each half of the fp16 pair xm (already masked), from the
+// reciprocals y, with the sign of a zero x kept.
+__device__ __forceinline__ float2 quot_pair(uint32_t xm, float2 d, float2 y) {
+  const float2 x = __half22float2(bits_h2(xm));
+  const float2 q0 = __fmul2_rn(x, y);
+  const float2 r = __ffma2_rn(q0, make_float2(-d.x, -d.y), x);
+  const float2 q = __ffma2_rn(r, y, q0);
+  return make_float2(copysignf(q.x, x.x), copysignf(q.y, x.y));
+}
+
 template <int D, int ROLE>
 __global__ void __launch_bounds__(32 * kCastWarps) nvfp4_cast_kernel(Nvfp4QuantArgs a) {
   constexpr int KS = D / 16;
-  constexpr int RS = D + 8;  // padded row stride (halves)
-  __shared__ __align__(16) __half tile[kCastWarps][kBlock * RS];
-  __shared__ float dn[kCastWarps][kBlock * KS];   // fl32(S_b * s_t) per (token, channel block)
-  __shared__ float rc[kCastWarps][kBlock * KS];   // RN(1 / that)
-  __shared__ uint8_t sbyte[kCastWarps][kBlock * KS];
+  constexpr int RS = D + 8;  // padded row stride (halves): ldmatrix rows on distinct banks
+  __shared__ __align__(16) __half tile[kCastWarps][2][kBlock * RS];
+  // per (channel block, token) of the unit: d = fl32(S_b * s_t), y = RN(1/d) (0 when d = 0) and an
+  // fp16 mask (all ones when d > 0, else 0), in the order the role's element pairs read them:
+  // keys {d, y, mask, -} per token; values {d, d', y, y'} and {mask, mask'} per token pair
+  constexpr int NPAR = (ROLE == 0) ? KS * kBlock : KS * kBlock / 2;
+  __shared__ __align__(16) float4 par[kCastWarps][NPAR];
+  __shared__ __align__(4) uint16_t msk[kCastWarps][KS * kBlock];  // values: [block][token]
+  __shared__ uint8_t sbyte[kCastWarps][kBlock * KS];               // [token][block]: the E4M3 scale byte
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, tig = lane & 3;
-  __half* xs = tile[warp];
   const float s_t = *a.scale;
+  const bool st_fast = s_t >= 0x1p-96f && s_t <= 0x1p96f;
+  const float y_t = st_fast ? __frcp_rn(s_t) : 0.0f;
+  const float y_6 = __frcp_rn(6.0f);
   const int nb = (a.seq_len + kBlock - 1) / kBlock;
   const long long units = static_cast<long long>(a.batch) * a.kv_heads * nb;
-  for (long long u = blockIdx.x * static_cast<long long>(kCastWarps) + warp; u < units;
-       u += static_cast<long long>(gridDim.x) * kCastWarps) {
+  const long long stride = static_cast<long long>(gridDim.x) * kCastWarps;
+
+  auto stage = [&](long long u, __half* xs) {
     const int j = static_cast<int>(u % nb);
     const long long bh = u / nb;
-    const int b = static_cast<int>(bh / a.kv_heads), h = static_cast<int>(bh % a.kv_heads);
-    const int blk = a.block_table[static_cast<long long>(b) * a.max_blocks + j];
-    if (blk < 0 || blk >= a.num_blocks) continue;  // uniform per warp: no write outside the pool
     const int t0 = j * kBlock, ntok = min(kBlock, a.seq_len - t0);
     const uint4* src = reinterpret_cast<const uint4*>(a.x + (bh * a.seq_len + t0) * static_cast<long long>(D));
 #pragma unroll
     for (int i = lane; i < kBlock * D / 8; i += 32) {
       const int tok = i / (D / 8), c8 = i % (D / 8);
-      *reinterpret_cast<uint4*>(xs + tok * RS + 8 * c8) = (tok < ntok) ? __ldcs(src + i) : make_uint4(0u, 0u, 0u, 0u);
+      cp_async16_zfill(xs + tok * RS + 8 * c8, (tok < ntok) ? src + i : src, tok < ntok);
     }
+  };
+
+  long long u = blockIdx.x * static_cast<long long>(kCastWarps) + warp;
+  if (u < units) stage(u, tile[warp][0]);
+  cp_async_commit();
+  for (int buf = 0; u < units; u += stride, buf ^= 1) {
+    if (u + stride < units) stage(u + stride, tile[warp][buf ^ 1]);
+    cp_async_commit();
+    cp_async_wait_all_but_newest();
     __syncwarp();
-    // block scales
+    const __half* xs = tile[warp][buf];
+    const int j = static_cast<int>(u % nb);
+    const long long bh = u / nb;
+    const int b = static_cast<int>(bh / a.kv_heads), h = static_cast<int>(bh % a.kv_heads);
+    const int blk = a.block_table[static_cast<long long>(b) * a.max_blocks + j];
+    if (blk >= 0 && blk < a.num_blocks) {  // uniform per warp: no write outside the pool
+      // block scales
+      bool slow = false;
 #pragma unroll
-    for (int p = lane; p < kBlock * KS; p += 32) {
-      const int tok = p / KS, ks = p % KS;
-      const uint4* row = reinterpret_cast<const uint4*>(xs + tok * RS + 16 * ks);
-      const uint4 v0 = row[0], v1 = row[1];
-      const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-      uint32_t m = 0;
+      for (int p = lane; p < kBlock * KS; p += 32) {
+        const int tok = p / KS, ks = p % KS;
+        const uint4* row = reinterpret_cast<const uint4*>(xs + tok * RS + 16 * ks);
+        const uint4 v0 = row[0], v1 = row[1];
+        const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+        uint32_t m = 0;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) m = max(m, max(w[k] & 0x7FFFu, (w[k] >> 16) & 0x7FFFu));
-      const float amax = __half2float(__ushort_as_half(static_cast<unsigned short>(m)));
-      const float v = __fdiv_rn(__fdiv_rn(amax, 6.0f), s_t);
-      const uint32_t byte = f32x2_to_e4m3x2(v, 0.0f) & 0xFFu;
-      const float S = __half2float(__ushort_as_half(static_cast<unsigned short>(e4m3x2_to_f16x2(
-          static_cast<uint16_t>(byte)) & 0xFFFFu)));
-      const float d = __fmul_rn(S, s_t);
-      sbyte[warp][p] = static_cast<uint8_t>(byte);
-      dn[warp][p] = d;
-      rc[warp][p] = (d > 0.0f) ? __frcp_rn(d) : 0.0f;
-    }
-    __syncwarp();
-    // fl32(x / d) (the IEEE quotient, sign of zero kept), 0 when the block scale is 0
-    auto q = [&](float x, float d, float y) -> float {
-      if (d == 0.0f) return 0.0f;
-      return (d >= 0x1p-96f && d <= 0x1p96f) ? div_rn_by_rcp_signed(x, d, y) : __fdiv_rn(x, d);
-    };
-    uint8_t* dst = a.pool + (static_cast<long long>(blk) * a.kv_heads + h) * (9 * D);
-#pragma unroll
-    for (int c = 0; c < D / 64; ++c) {
-      uint32_t out[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-      for (int kk = 0; kk < 16; ++kk) {
-        const int p = 16 * c + kk;  // byte of the lane's code stream
-        int ta, ca, tb, cb, ia, ib;
+        for (int k = 0; k < 8; ++k) m = max(m, max(w[k] & 0x7FFFu, (w[k] >> 16) & 0x7FFFu));
+        const float amax = __half2float(__ushort_as_half(static_cast<unsigned short>(m)));
+        const float a6 = div_rn_by_rcp(amax, 6.0f, y_6);  // amax is a finite fp16 value: exact
+        const float v = st_fast ? div_rn_by_rcp(a6, s_t, y_t) : __fdiv_rn(a6, s_t);
+        const uint32_t byte = f32x2_to_e4m3x2(v, 0.0f) & 0xFFu;
+        const float S = __half2float(__ushort_as_half(static_cast<unsigned short>(e4m3x2_to_f16x2(
+            static_cast<uint16_t>(byte)) & 0xFFFFu)));
+        const float d = __fmul_rn(S, s_t);
+        const float y = (d > 0.0f) ? __frcp_rn(d) : 0.0f;
+        sbyte[warp][p] = static_cast<uint8_t>(byte);
         if constexpr (ROLE == 0) {
-          const int nt = p / (2 * KS), ks = (p % (2 * KS)) >> 1, r = p & 1;
-          ta = tb = 8 * nt + g;
-          ca = 16 * ks + 8 * r + 2 * tig;
-          cb = ca + 1;
-          ia = ib = ta * KS + ks;
+          par[warp][ks * kBlock + tok] = make_float4(d, y, __uint_as_float(d > 0.0f ? 0xFFFFFFFFu : 0u), 0.0f);
         } else {
-          const int nt = p >> 1, r = p & 1;
-          ta = 8 * r + 2 * tig;
-          tb = ta + 1;
-          ca = cb = 8 * nt + g;
-          ia = ta * KS + (ca >> 4);
-          ib = tb * KS + (ca >> 4);
+          float* pv = reinterpret_cast<float*>(&par[warp][ks * (kBlock / 2) + (tok >> 1)]);
+          pv[tok & 1] = d;
+          pv[2 + (tok & 1)] = y;
+          msk[warp][ks * kBlock + tok] = (d > 0.0f) ? 0xFFFFu : 0u;
         }
-        const float xa = __half2float(xs[ta * RS + ca]), xb = __half2float(xs[tb * RS + cb]);
-        const uint32_t byte = f32x2_to_e2m1x2(q(xa, dn[warp][ia], rc[warp][ia]), q(xb, dn[warp][ib], rc[warp][ib]));
-        out[kk >> 2] |= byte << (8 * (kk & 3));
+        slow |= d > 0.0f && (d < 0x1p-96f || d > 0x1p96f);
       }
-      reinterpret_cast<uint4*>(dst)[c * 32 + lane] = make_uint4(out[0], out[1], out[2], out[3]);
-    }
-    // the D scale bytes: lane l writes bytes 4l .. 4l + 3 (D = 128) or 2l .. 2l + 1 (D = 64)
-    constexpr int PER = D / 32;
-    uint32_t sw = 0;
+      slow = __any_sync(0xffffffffu, slow);
+      __syncwarp();
+      uint8_t* dst = a.pool + (static_cast<long long>(blk) * a.kv_heads + h) * (9 * D);
+      const float4* pw = par[warp];
+      const uint16_t* mw = msk[warp];
+      // fl32(x / d) of one fp16 pair of elements: the reciprocal path, or (a unit with a block scale
+      // outside its range) the IEEE division
+      auto quot = [&](bool ieee, uint32_t xm, float2 d, float2 y) -> float2 {
+        if (!ieee) return quot_pair(xm, d, y);
+        const float2 x = __half22float2(bits_h2(xm));
+        return make_float2(d.x == 0.0f ? 0.0f : __fdiv_rn(x.x, d.x), d.y == 0.0f ? 0.0f : __fdiv_rn(x.y, d.y));
+      };
+      // the lane's 16-byte chunks of codes; byte kk of chunk c = the codes of one fp16 pair of elements
+      auto write_codes = [&](bool ieee) {
 #pragma unroll
-    for (int e = 0; e < PER; ++e) {
-      const int s = PER * lane + e;  // scale byte index in the record
-      int tok, blkc;
-      if constexpr (ROLE == 0) {
-        const int gg = s / (2 * KS), rem = s % (2 * KS), nt = rem / KS, ks = rem % KS;
-        tok = 8 * nt + gg;
-        blkc = ks;
-      } else {
-        const int ee = s & 1, jj = (s >> 1) % KS, tr = (s >> 1) / KS, r = tr & 1, tg = tr >> 1;
-        tok = 8 * r + 2 * tg + ee;
-        blkc = jj;
+        for (int c = 0; c < D / 64; ++c) {
+          float2 q[16];
+          if constexpr (ROLE == 0) {
+            // keys: byte p = (nt * KS + ks) * 2 + r holds channels 16 ks + 8 r + 2 tig, +1 of token 8 nt + g
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk) {
+              const int p = 16 * c + kk, nt = p / (2 * KS), ks = (p % (2 * KS)) >> 1, r = p & 1;
+              const int tok = 8 * nt + g, ch = 16 * ks + 8 * r + 2 * tig;
+              const uint32_t xp = *reinterpret_cast<const uint32_t*>(xs + tok * RS + ch);
+              const float4 pr = pw[ks * kBlock + tok];
+              q[kk] = quot(ieee, xp & __float_as_uint(pr.z), make_float2(pr.x, pr.x), make_float2(pr.y, pr.y));
+            }
+          } else {
+            // values: byte p = nt * 2 + r holds tokens 8 r + 2 tig, +1 of channel 8 nt + g, from the
+            // transposed 8 x 8 tiles of tokens 8 r .., channels 8 nt .. (four tiles per ldmatrix)
+#pragma unroll
+            for (int r = 0; r < 2; ++r)
+#pragma unroll
+              for (int q4 = 0; q4 < 2; ++q4) {
+                uint32_t t4[4];
+                const int nt0 = 8 * c + 4 * q4;
+                ldsm_x4_trans(t4, xs + (8 * r + (lane & 7)) * RS + 8 * (nt0 + (lane >> 3)));
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const int ta = 8 * r + 2 * tig, blkc = (8 * (nt0 + e) + g) >> 4;
+                  const float4 pr = pw[blkc * (kBlock / 2) + (ta >> 1)];
+                  const uint32_t mk = *reinterpret_cast<const uint32_t*>(mw + blkc * kBlock + ta);
+                  q[(4 * q4 + e) * 2 + r] = quot(ieee, t4[e] & mk, make_float2(pr.x, pr.y), make_float2(pr.z, pr.w));
+                }
+              }
+          }
+          uint4 w;
+          w.x = f32x8_to_e2m1x8({q[0], q[1], q[2], q[3]});
+          w.y = f32x8_to_e2m1x8({q[4], q[5], q[6], q[7]});
+          w.z = f32x8_to_e2m1x8({q[8], q[9], q[10], q[11]});
+          w.w = f32x8_to_e2m1x8({q[12], q[13], q[14], q[15]});
+          reinterpret_cast<uint4*>(dst)[c * 32 + lane] = w;
+        }
+      };
+      if (!slow)
+        write_codes(false);
+      else
+        write_codes(true);
+      // the D scale bytes: lane l writes bytes 4l .. 4l + 3 (D = 128) or 2l .. 2l + 1 (D = 64)
+      constexpr int PER = D / 32;
+      uint32_t sw = 0;
+#pragma unroll
+      for (int e = 0; e < PER; ++e) {
+        const int s = PER * lane + e;  // scale byte index in the record
+        int tok, blkc;
+        if constexpr (ROLE == 0) {
+          const int gg = s / (2 * KS), rem = s % (2 * KS), nt = rem / KS, ks = rem % KS;
+          tok = 8 * nt + gg;
+          blkc = ks;
+        } else {
+          const int ee = s & 1, jj = (s >> 1) % KS, tr = (s >> 1) / KS, r = tr & 1, tg = tr >> 1;
+          tok = 8 * r + 2 * tg + ee;
+          blkc = jj;
+        }
+        sw |= static_cast<uint32_t>(sbyte[warp][tok * KS + blkc]) << (8 * e);
       }
-      sw |= static_cast<uint32_t>(sbyte[warp][tok * KS + blkc]) << (8 * e);
+      if constexpr (PER == 4)
+        reinterpret_cast<uint32_t*>(dst + 8 * D)[lane] = sw;
+      else
+        reinterpret_cast<uint16_t*>(dst + 8 * D)[lane] = static_cast<uint16_t>(sw);
     }
-    if constexpr (PER == 4)
-      reinterpret_cast<uint32_t*>(dst + 8 * D)[lane] = sw;
-    else
-      reinterpret_cast<uint16_t*>(dst + 8 * D)[lane] = static_cast<uint16_t>(sw);
-    __syncwarp();  // the staging buffers are refilled by the next unit
+    __syncwarp();  // this buffer and the scale arrays are refilled by the next unit
   }
 }
 
@@ -464,6 +543,26 @@ int nvfp4_decode_blocks_per_sm(int head_dim) {
   return head_dim == 64 ? nvfp4_occupancy<64>() : nvfp4_occupancy<128>();
 }
 
+// Resident cast blocks per SM (occupancy API, once per device and variant).
+int nvfp4_cast_blocks_per_sm(int head_dim, int role) {
+  static int cached[64][4] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  const int v = (head_dim == 128 ? 2 : 0) + (role ? 1 : 0);
+  if (cached[dev][v] == 0) {
+    int n = 0;
+    cudaError_t e;
+    switch (v) {
+      case 3: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, nvfp4_cast_kernel<128, 1>, 32 * kCastWarps, 0); break;
+      case 2: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, nvfp4_cast_kernel<128, 0>, 32 * kCastWarps, 0); break;
+      case 1: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, nvfp4_cast_kernel<64, 1>, 32 * kCastWarps, 0); break;
+      default: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, nvfp4_cast_kernel<64, 0>, 32 * kCastWarps, 0); break;
+    }
+    cached[dev][v] = (e == cudaSuccess && n > 0) ? n : 1;
+  }
+  return cached[dev][v];
+}
+
 cudaError_t launch_nvfp4_quantize(const Nvfp4QuantArgs& a, cudaStream_t s) {
   if (!a.static_scale) {
     const long long n_vec = static_cast<long long>(a.batch) * a.kv_heads * a.seq_len * a.head_dim / 8;
@@ -473,7 +572,7 @@ cudaError_t launch_nvfp4_quantize(const Nvfp4QuantArgs& a, cudaStream_t s) {
   const int nb = (a.seq_len + kBlock - 1) / kBlock;
   const long long units = static_cast<long long>(a.batch) * a.kv_heads * nb;
   const long long want = (units + kCastWarps - 1) / kCastWarps;
-  const long long full = 8LL * device_sm_count();
+  const long long full = static_cast<long long>(nvfp4_cast_blocks_per_sm(a.head_dim, a.role)) * device_sm_count();
   const int grid = static_cast<int>(want < full ? want : full);
   switch (a.head_dim * 10 + a.role) {
     case 1280: nvfp4_cast_kernel<128, 0><<<grid, 32 * kCastWarps, 0, s>>>(a); break;
