@@ -88,6 +88,30 @@ def test_static_scale_saturation():
     _assert_pool(p, _oracle_pool(kvq.ROLE_KEY, x, table, 3, s_t), np.arange(3))
 
 
+@pytest.mark.parametrize("s_t", [2.0 ** -110, 1.0 / 64])
+@pytest.mark.parametrize("role", [0, 1])
+def test_zero_blocks_negative_zeros_and_the_division_path(role, s_t):
+    """A static tensor scale of 2^-110 puts every nonzero block divisor
+    fl32(S_b * s_t) below 2^-96, where the cast takes the IEEE division (the
+    whole unit); 1/64 keeps the reciprocal path. All-zero and negative-zero
+    blocks give codes 0 either way, and a negative zero in a nonzero block keeps
+    its sign (code 8)."""
+    x = workloads.make_inputs(1, 2, 2, 128, 48, 1, 41).v.astype(np.float16)
+    x[0, 0, 5] = 0.0                             # a zero token: every block of it 0
+    x[0, 1, 7] = np.float16(-0.0)                # a negative-zero token
+    x[0, 1, 20, :16] = np.float16(-0.0)          # one negative-zero block in a token
+    x[0, 1, 21, 3] = np.float16(-0.0)            # a negative zero in a nonzero block: code 8
+    table = np.arange(3, dtype=np.int32).reshape(1, 3)
+    s_t = np.float32(s_t)
+    p = _pool(role, x, table, 3, static_scale=s_t)
+    want = _oracle_pool(role, x, table, 3, s_t)
+    _assert_pool(p, want, np.arange(3))
+    codes, sb = nvfp4.quantize(x, s_t)
+    divisors = fp8.e4m3_decode(sb[sb != 0]) * float(s_t)
+    assert np.any(codes == 8)
+    assert np.all(divisors < 2.0 ** -96) if s_t < 2.0 ** -100 else np.all(divisors >= 2.0 ** -96)
+
+
 def test_table_entries_outside_the_pool_are_skipped():
     kvq = _kvq()
     x = workloads.make_inputs(1, 2, 2, 64, 48, 1, 41).v
