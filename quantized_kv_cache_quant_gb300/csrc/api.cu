@@ -189,7 +189,8 @@ DecodePlan plan_kivi_decode(const kivi_cache* cache) {
   const kivi_config& cf = cache->cfg;
   DecodePlan p{};
   p.n_groups = cache->n_grouped / kGroup;
-  const int U = p.n_groups + kvq::kChunkUnits * ceil_div(cache->n_resid, kGroup);
+  const int chunk_units = use_swapped_decode(cf) ? kvq::kTrChunkUnits : kvq::kChunkUnits;
+  const int U = p.n_groups + chunk_units * ceil_div(cache->n_resid, kGroup);
   p.units_per_pair = U;
   const long long pairs = static_cast<long long>(cf.batch) * cf.kv_heads;
   const int per_sm = use_swapped_decode(cf) ? kvq::kivi_decode_tr_blocks_per_sm(cf.head_dim, cf.k_bits, cf.v_bits)
@@ -725,7 +726,7 @@ kvq_status kv_paged_decode_attention(const kivi_paged_cache* cache, const uint16
   for (int b = 0; b < cf.batch; ++b) {
     const int ng = cache->n_grouped[b] / kGroup, nr = cache->n_resid[b];
     if (ng + nr == 0) return KVQ_ERR_ARG;
-    const int U = ng + kvq::kChunkUnits * ceil_div(nr, kGroup);
+    const int U = ng + (use_swapped_decode(cf) ? kvq::kTrChunkUnits : kvq::kChunkUnits) * ceil_div(nr, kGroup);
     seqs.unit0[b] = static_cast<int>(total);
     seqs.n_groups[b] = ng;
     seqs.n_resid[b] = nr;

@@ -281,7 +281,7 @@ __global__ void __launch_bounds__(128, 4) kivi_decode_tr_kernel(KiviDecodeArgs a
       const int sb = tr_seq_of(seqs.unit0, seqs.n_seqs, u);
       n_grp = seqs.n_groups[sb];
       n_res = seqs.n_resid[sb];
-      upp = n_grp + kChunkUnits * ((n_res + kGroup - 1) / kGroup);
+      upp = n_grp + kTrChunkUnits * ((n_res + kGroup - 1) / kGroup);
       const int span = upp + seqs.pair_lead;
       const int hh = static_cast<int>((u - seqs.unit0[sb]) / span);
       pair = sb * a.kv_heads + hh;
@@ -313,8 +313,8 @@ __global__ void __launch_bounds__(128, 4) kivi_decode_tr_kernel(KiviDecodeArgs a
     const int n_chunks = (n_res + kGroup - 1) / kGroup;
     const int g_begin = min(n_grp, lo);
     const int g_end = min(n_grp, hi);
-    const int c_begin = min(n_chunks, max(0, lo - n_grp + kChunkUnits - 1) / kChunkUnits);
-    const int c_end = min(n_chunks, max(0, hi - n_grp + kChunkUnits - 1) / kChunkUnits);
+    const int c_begin = min(n_chunks, max(0, lo - n_grp + kTrChunkUnits - 1) / kTrChunkUnits);
+    const int c_end = min(n_chunks, max(0, hi - n_grp + kTrChunkUnits - 1) / kTrChunkUnits);
 
     float m_run = -INFINITY, l_run = 0.0f, vz_run = 0.0f;
     float o_acc[MT][4];

@@ -116,6 +116,12 @@ cudaError_t launch_kivi_decode(const KiviDecodeArgs& a, cudaStream_t s);
 // on the tile rows, query heads x {hi, lo} on its 8 columns), for caches whose
 // kv heads serve at most kMaxGqaSwapped query heads.
 constexpr int kMaxGqaSwapped = 4;
+// Units one 32-token window chunk is charged in the swapped-operand decode
+// (its groups cost about half the MMAs of the other kernel's, its window
+// chunks about as much). Swept 6, 8, 10, 12, 16 on GB300: 8 is best (MHA 4K
+// 43.3 -> 42.4 us; paged GQA-4 70.2 -> 69.9 us), 10 and above change the cut
+// and cost 2-9 %.
+constexpr int kTrChunkUnits = 8;
 cudaError_t launch_kivi_decode_tr(const KiviDecodeArgs& a, cudaStream_t s);
 
 // Decode over a paged cache: the pairs of sequence b (b * kv_heads + h) have
