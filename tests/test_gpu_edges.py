@@ -13,6 +13,8 @@ swapped-operand kernel) and for the contiguous and the paged cache:
   (an attention-sink-like token); it lies in the grouped region for some
   pairs and in the fp16 window for the others.
 
+The FP8 and NVFP4 paged decodes take the first two at the same magnitudes.
+
 Attention is linear in the values, so outputs are compared after dividing by
 the values' magnitude M (the same bars as the other parity tests: max-abs
 2e-3 and relative L2 1e-3 of the float64 oracle on the same dequantized
@@ -146,3 +148,52 @@ def test_paged_edges(kind, gq, kb, vb):
     ref = attention.decode_attention(q, oc.keys_hat, oc.values_hat, oc.H, default_scale(d))
     out = host(gc.decode(dev(q)))
     assert_attention_close(out / m, ref / m)
+
+
+# ---------------------------------------------------------------------------
+# The FP8 and NVFP4 paged decodes at the same magnitudes: keys and values
+# scaled by 2^-16 (the tensor scales shrink with them) and up to +-65000.
+# ---------------------------------------------------------------------------
+def _scaled(kind, x):
+    k, v, q = x.k.astype(np.float64), x.v.astype(np.float64), x.q[0].astype(np.float64)
+    if kind == "tiny":
+        k, v, q, m = k * TINY, v * TINY, q * 64.0, TINY
+    else:
+        k = k / np.abs(k).max() * BIG
+        v = v / np.abs(v).max() * BIG
+        q, m = q * 2.0 ** -12, BIG
+    return k.astype(np.float16), v.astype(np.float16), q.astype(np.float16), m
+
+
+@pytest.mark.parametrize("kind", ["tiny", "fp16_max"])
+@pytest.mark.parametrize("gq", [4, 1])
+def test_fp8_decode_edges(kind, gq):
+    from oracle import fp8
+    from test_gpu_fp8 import KEY, VALUE, _decode, _oracle_decode, _quantize
+    b, hkv, d, s = 2, 2, 128, 16 * 40 + 5
+    x = workloads.make_inputs(b, hkv, hkv * gq, d, s, 1, 300 + gq)
+    k, v, q, m = _scaled(kind, x)
+    nb = -(-s // 16)
+    table = workloads.block_table(b, nb, 7)
+    kp, ks = _quantize(k, table, b * nb, KEY)
+    vp, vs = _quantize(v, table, b * nb, VALUE)
+    lens = np.array([s, 16 * 9 + 3])
+    out, status = _decode(q, kp, vp, ks, vs, table, lens, hkv, b * nb, s)
+    assert status == 0
+    ref = _oracle_decode(q, k, v, fp8.dynamic_scale(k), fp8.dynamic_scale(v), lens)
+    assert_attention_close(out / m, ref / m)
+
+
+@pytest.mark.parametrize("kind", ["tiny", "fp16_max"])
+@pytest.mark.parametrize("gq", [4, 1])
+def test_nvfp4_decode_edges(kind, gq):
+    from test_gpu_nvfp4 import _decode, _oracle_decode
+    b, hkv, d, s = 2, 2, 128, 16 * 40 + 5
+    x = workloads.make_inputs(b, hkv, hkv * gq, d, s, 1, 400 + gq)
+    k, v, q, m = _scaled(kind, x)
+    xs = workloads.KVInputs(k, v, q[None], x.k_new, x.v_new)
+    nb = -(-s // 16)
+    table = workloads.block_table(b, nb, 9)
+    lens = np.array([s, 16 * 9 + 3], np.int32)
+    got = _decode(xs, table, nb, lens, hkv * gq)
+    assert_attention_close(got / m, _oracle_decode(xs, lens) / m)
