@@ -125,7 +125,32 @@ __device__ __forceinline__ float scaled(float x, float scale, float y) {
   }
 }
 
-template <int D, int MODE, int FMT>
+// scaled<MODE> of both halves of an fp16 pair, the reciprocal path in packed
+// fp32 operations (the same steps, so the same quotients).
+template <int MODE>
+__device__ __forceinline__ float2 scaled_pair(uint32_t xh2, float scale, float y) {
+  const float2 x = __half22float2(bits_h2(xh2));
+  if constexpr (MODE == 0) {
+    (void)y;
+    return make_float2(__fdiv_rn(x.x, scale), __fdiv_rn(x.y, scale));
+  } else {
+    const float2 q0 = __fmul2_rn(x, make_float2(y, y));
+    const float2 r = __ffma2_rn(q0, make_float2(-scale, -scale), x);
+    const float2 q = __ffma2_rn(r, make_float2(y, y), q0);
+    float2 o = make_float2(copysignf(q.x, x.x), copysignf(q.y, x.y));
+    if constexpr (MODE == 1) {
+      if (isinf(x.x)) o.x = x.x;
+      if (isinf(x.y)) o.y = x.y;
+    }
+    return o;
+  }
+}
+
+// ROLE 2: keys (4-byte words = m16n8k32 B fragments), ROLE 1: values (token
+// pairs per channel). Byte pairs of the lane's stream come as fp16 pairs:
+// keys two adjacent channels of a token (one 32-bit load), values two tokens of
+// a channel (a transposed ldmatrix gives four of them).
+template <int D, int MODE, int FMT, int ROLE>
 __device__ __forceinline__ void cast_units(const Fp8QuantArgs& a, __half* bufs) {
   constexpr int RS = D + 8;  // padded row stride (halves): rows start 4 banks apart
   constexpr int BUF = kBlock * RS;
@@ -180,42 +205,38 @@ __device__ __forceinline__ void cast_units(const Fp8QuantArgs& a, __half* bufs) 
       const float scale = a.scale[a.per_head ? h : 0];
       const float y = (MODE == 0) ? 0.0f : __frcp_rn(scale);
       uint4* dst = reinterpret_cast<uint4*>(a.pool + (static_cast<long long>(blk) * a.kv_heads + h) * (kBlock * D));
+      const bool full = ntok == kBlock;  // else rows past the sequence are zeroed bytes
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
-        uint32_t out[4];
+        uint32_t pr[8];  // byte pair kk of the lane's 16-byte chunk c (pair index 8c + kk of its stream)
+        if constexpr (ROLE == 2) {
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const int i = 8 * c + kk;  // byte pair index in the lane's stream
-          int tok0, ch0, tok1, ch1;
-          if (a.value_layout == 2) {
-            // 4-byte word w = (nt * (D/32) + kk) * 2 + r: channels 32kk + 16r + 4tg .. +3 of token 8nt + gg
-            const int w = i >> 1, nt = w / (D / 16), rem = w % (D / 16), kk = rem >> 1, r = rem & 1;
-            tok0 = tok1 = 8 * nt + gg;
-            ch0 = 32 * kk + 16 * r + 4 * tg + 2 * (i & 1);
-            ch1 = ch0 + 1;
-          } else if (a.value_layout) {
-            const int nt = i >> 1, r = i & 1;
-            tok0 = 8 * r + 2 * tg;
-            tok1 = tok0 + 1;
-            ch0 = ch1 = 8 * nt + gg;
-          } else {
-            const int nt = i / (D / 8), rem = i % (D / 8), ks = rem >> 1, r = rem & 1;
-            tok0 = tok1 = 8 * nt + gg;
-            ch0 = 16 * ks + 8 * r + 2 * tg;
-            ch1 = ch0 + 1;
+          for (int kk = 0; kk < 8; ++kk) {
+            // 4-byte word w = (nt * (D/32) + k2) * 2 + r: channels 32k2 + 16r + 4tg .. +3 of token 8nt + gg
+            const int i = 8 * c + kk, w = i >> 1, nt = w / (D / 16), rem = w % (D / 16), k2 = rem >> 1, r = rem & 1;
+            const int tok = 8 * nt + gg, ch = 32 * k2 + 16 * r + 4 * tg + 2 * (i & 1);
+            const float2 q = scaled_pair<MODE>(*reinterpret_cast<const uint32_t*>(xs + tok * RS + ch), scale, y);
+            pr[kk] = f32x2_to_fp8x2<FMT>(q.x, q.y);
+            if (!full && tok >= ntok) pr[kk] = 0u;
           }
-          const bool v0 = tok0 < ntok, v1 = tok1 < ntok;
-          const float y0 = v0 ? scaled<MODE>(__half2float(xs[tok0 * RS + ch0]), scale, y) : 0.0f;
-          const float y1 = v1 ? scaled<MODE>(__half2float(xs[tok1 * RS + ch1]), scale, y) : 0.0f;
-          uint32_t pair = f32x2_to_fp8x2<FMT>(y0, y1);
-          if (!v0) pair &= 0xFF00u;
-          if (!v1) pair &= 0x00FFu;
-          if (kk & 1)
-            out[kk >> 1] |= pair << 16;
-          else
-            out[kk >> 1] = pair;
+        } else {
+          // pair i = 2nt + r: tokens 8r + 2tg, +1 of channel 8nt + gg (nt = 4c + e for tile e)
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            uint32_t t4[4];
+            ldsm_x4_trans(t4, xs + (8 * r + (lane & 7)) * RS + 8 * (4 * c + (lane >> 3)));
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 q = scaled_pair<MODE>(t4[e], scale, y);
+              uint32_t v = f32x2_to_fp8x2<FMT>(q.x, q.y);
+              const int t0 = 8 * r + 2 * tg;
+              if (!full) v &= (t0 < ntok ? 0x00FFu : 0u) | (t0 + 1 < ntok ? 0xFF00u : 0u);
+              pr[2 * e + r] = v;
+            }
+          }
         }
-        dst[c * 32 + lane] = make_uint4(out[0], out[1], out[2], out[3]);
+        dst[c * 32 + lane] = make_uint4(pr[0] | (pr[1] << 16), pr[2] | (pr[3] << 16), pr[4] | (pr[5] << 16),
+                                        pr[6] | (pr[7] << 16));
       }
     }
     __syncwarp();  // this buffer is refilled next iteration
@@ -230,12 +251,16 @@ __global__ void __launch_bounds__(32 * kCastWarps) fp8_cast_kernel(Fp8QuantArgs 
   // the reciprocal path when every scale is in its exact range (the same decision for the whole grid)
   bool fast = true;
   for (int h = 0; h < (a.per_head ? a.kv_heads : 1); ++h) fast &= (a.scale[h] >= 0x1p-96f && a.scale[h] <= 0x1p96f);
-  if (!fast)
-    cast_units<D, 0, FMT>(a, mine);
-  else if (a.static_scale)
-    cast_units<D, 1, FMT>(a, mine);
-  else
-    cast_units<D, 2, FMT>(a, mine);
+  const int mode = !fast ? 0 : (a.static_scale ? 1 : 2);
+  if (a.value_layout == 2) {
+    if (mode == 0) cast_units<D, 0, FMT, 2>(a, mine);
+    else if (mode == 1) cast_units<D, 1, FMT, 2>(a, mine);
+    else cast_units<D, 2, FMT, 2>(a, mine);
+  } else {
+    if (mode == 0) cast_units<D, 0, FMT, 1>(a, mine);
+    else if (mode == 1) cast_units<D, 1, FMT, 1>(a, mine);
+    else cast_units<D, 2, FMT, 1>(a, mine);
+  }
 }
 
 // ---------------------------------------------------------------------------

@@ -157,7 +157,7 @@ struct Fp8QuantArgs {
   int static_scale;
   int per_head;
   int fmt;                // 0 = E4M3, 1 = E5M2
-  int value_layout;       // 0 keys, 1 values, 2 keys for FP8 tensor cores
+  int value_layout;       // the in-block order: 2 keys (m16n8k32 B fragments), 1 values
   uint32_t* amax_partials;  // [per_head ? H_kv : 1][amax_blocks]
   int amax_blocks;
 };
