@@ -144,12 +144,15 @@ __global__ void __launch_bounds__(32 * kCastWarps) nvfp4_cast_kernel(Nvfp4QuantA
     const int blk = a.block_table[static_cast<long long>(b) * a.max_blocks + j];
     if (blk >= 0 && blk < a.num_blocks) {  // uniform per warp: no write outside the pool
       // block scales
-      bool slow = false;
+      bool slow = false, zero = false;  // a divisor outside the reciprocal range; a block whose scale is 0
 #pragma unroll
       for (int p = lane; p < kBlock * KS; p += 32) {
         const int tok = p / KS, ks = p % KS;
+        // the block's two 16-byte halves, the upper one first for odd ks / 4: the 8 lanes of a load
+        // phase then cover all 32 banks (the blocks of a token are 32 bytes apart)
         const uint4* row = reinterpret_cast<const uint4*>(xs + tok * RS + 16 * ks);
-        const uint4 v0 = row[0], v1 = row[1];
+        const int sw = (ks >> 2) & 1;
+        const uint4 v0 = row[sw], v1 = row[sw ^ 1];
         const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
         uint32_t m = 0;
 #pragma unroll
@@ -172,8 +175,10 @@ __global__ void __launch_bounds__(32 * kCastWarps) nvfp4_cast_kernel(Nvfp4QuantA
           msk[warp][ks * kBlock + tok] = (d > 0.0f) ? 0xFFFFu : 0u;
         }
         slow |= d > 0.0f && (d < 0x1p-96f || d > 0x1p96f);
+        zero |= d == 0.0f;
       }
       slow = __any_sync(0xffffffffu, slow);
+      zero = __any_sync(0xffffffffu, zero);
       __syncwarp();
       uint8_t* dst = a.pool + (static_cast<long long>(blk) * a.kv_heads + h) * (9 * D);
       const float4* pw = par[warp];
@@ -186,7 +191,7 @@ __global__ void __launch_bounds__(32 * kCastWarps) nvfp4_cast_kernel(Nvfp4QuantA
         return make_float2(d.x == 0.0f ? 0.0f : __fdiv_rn(x.x, d.x), d.y == 0.0f ? 0.0f : __fdiv_rn(x.y, d.y));
       };
       // the lane's 16-byte chunks of codes; byte kk of chunk c = the codes of one fp16 pair of elements
-      auto write_codes = [&](bool ieee) {
+      auto write_codes = [&](bool ieee, bool masked) {
 #pragma unroll
         for (int c = 0; c < D / 64; ++c) {
           float2 q[16];
@@ -198,7 +203,8 @@ __global__ void __launch_bounds__(32 * kCastWarps) nvfp4_cast_kernel(Nvfp4QuantA
               const int tok = 8 * nt + g, ch = 16 * ks + 8 * r + 2 * tig;
               const uint32_t xp = *reinterpret_cast<const uint32_t*>(xs + tok * RS + ch);
               const float4 pr = pw[ks * kBlock + tok];
-              q[kk] = quot(ieee, xp & __float_as_uint(pr.z), make_float2(pr.x, pr.x), make_float2(pr.y, pr.y));
+              q[kk] = quot(ieee, masked ? xp & __float_as_uint(pr.z) : xp, make_float2(pr.x, pr.x),
+                           make_float2(pr.y, pr.y));
             }
           } else {
             // values: byte p = nt * 2 + r holds tokens 8 r + 2 tig, +1 of channel 8 nt + g, from the
@@ -214,8 +220,8 @@ __global__ void __launch_bounds__(32 * kCastWarps) nvfp4_cast_kernel(Nvfp4QuantA
                 for (int e = 0; e < 4; ++e) {
                   const int ta = 8 * r + 2 * tig, blkc = (8 * (nt0 + e) + g) >> 4;
                   const float4 pr = pw[blkc * (kBlock / 2) + (ta >> 1)];
-                  const uint32_t mk = *reinterpret_cast<const uint32_t*>(mw + blkc * kBlock + ta);
-                  q[(4 * q4 + e) * 2 + r] = quot(ieee, t4[e] & mk, make_float2(pr.x, pr.y), make_float2(pr.z, pr.w));
+                  const uint32_t xm = masked ? t4[e] & *reinterpret_cast<const uint32_t*>(mw + blkc * kBlock + ta) : t4[e];
+                  q[(4 * q4 + e) * 2 + r] = quot(ieee, xm, make_float2(pr.x, pr.y), make_float2(pr.z, pr.w));
                 }
               }
           }
@@ -227,10 +233,13 @@ __global__ void __launch_bounds__(32 * kCastWarps) nvfp4_cast_kernel(Nvfp4QuantA
           reinterpret_cast<uint4*>(dst)[c * 32 + lane] = w;
         }
       };
-      if (!slow)
-        write_codes(false);
+      // (warp-uniform) the usual unit: every divisor in the reciprocal range and none zero
+      if (!slow && !zero)
+        write_codes(false, false);
+      else if (!slow)
+        write_codes(false, true);
       else
-        write_codes(true);
+        write_codes(true, true);
       // the D scale bytes: lane l writes bytes 4l .. 4l + 3 (D = 128) or 2l .. 2l + 1 (D = 64)
       constexpr int PER = D / 32;
       uint32_t sw = 0;
