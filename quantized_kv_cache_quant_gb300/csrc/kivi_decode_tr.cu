@@ -485,20 +485,17 @@ __global__ void __launch_bounds__(128, 4) kivi_decode_tr_kernel(KiviDecodeArgs a
       sc[3] = fmaf(sacc[1][2] + sacc[1][3], mult8, bias);
     };
 
+    // One group at a time: q . k^T, softmax and p . V of group j (issuing
+    // q . k^T of group j + 1 inside group j's p . V, as the other kernel does,
+    // measured 2-3 % slower here: MHA 4K 41.6 against 43.0 us).
     int j = 0;
     float sc[4];
-    if (n_mine > 0) {
-      if (wait_slot(0))
-        qk_scores(0, sc);
-      else
-        timed_out = true;
-    }
     for (; !timed_out && j < n_mine; ++j) {
-      const int jn = (j + 1 < n_mine) ? j + 1 : j;
-      if (jn != j && jn % GPS == 0 && !wait_slot(jn / GPS)) {
+      if (j % GPS == 0 && !wait_slot(j / GPS)) {
         timed_out = true;
         break;
       }
+      qk_scores(j, sc);
       const uint4* vcw = reinterpret_cast<const uint4*>(vc_of(j));
       const uint4* vmr = reinterpret_cast<const uint4*>(vm_of(j));
 
@@ -525,7 +522,6 @@ __global__ void __launch_bounds__(128, 4) kivi_decode_tr_kernel(KiviDecodeArgs a
         vz_run = fmaf(p[k], z_t, vz_run);
       }
 
-      qk_scores(jn, sc);
 
       // ---- o^T += codes^T . p' (group j): rows = channels 16 mt + .., columns = heads x {hi, lo} ----
       uint32_t vw[P::VW];
