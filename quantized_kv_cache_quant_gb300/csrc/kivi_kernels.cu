@@ -18,14 +18,6 @@
 #ifndef KVQ_DECODE_MIN_BLOCKS
 #define KVQ_DECODE_MIN_BLOCKS 3  // resident decode blocks per SM the register budget is sized for
 #endif
-// Contiguous cache: q.k^T of group j + 1 is issued inside group j's p.V (software pipeline);
-// paged cache: one group at a time (measured on GB300: paged 32 x 8K 84.7 -> 81.9 us and 512-16384
-// tokens 88.5 -> 84.6 us one group at a time, the contiguous decodes equal or 1 % slower that way).
-template <bool kPaged>
-struct DecodePipelined {
-  static constexpr bool value = !kPaged;
-};
-
 namespace kvq {
 namespace {
 
@@ -1023,34 +1015,18 @@ __global__ void __launch_bounds__(128, KVQ_DECODE_MIN_BLOCKS) kivi_decode_kernel
       }
     };
 
-    // Software pipeline (contiguous cache): iteration j runs the softmax and
-    // p . V of group j and, in the same straight-line block, q . k^T of group
-    // j + 1, so that each warp keeps both the tensor pipe and the ALUs busy;
-    // the paged cache takes one group at a time.
-    int j = 0;
-    float sc[8];
-    constexpr bool kPipe = DecodePipelined<kPaged>::value;
-    if (kPipe && n_mine > 0) {
-      if (wait_slot(0))
-        qk_scores(0, sc);
-      else
-        timed_out = true;
-    }
+    // One group at a time: q . k^T, the softmax and p . V of group j. (Issuing
+    // q . k^T of group j + 1 inside group j's p . V, a software pipeline, was
+    // measured on GB300 against this: 2-bit D 128 equal, the other bit widths
+    // and D 64 1.5-4.5 % slower, GQA-8 4-bit at 8K 95.0 against 90.8 us.)
+    int j = 0;  // after the loop: the group a timed-out wait stopped at
     for (; !timed_out && j < n_mine; ++j) {
-      // the next group (this one again past the end: its scores are discarded)
-      const int jn = (j + 1 < n_mine) ? j + 1 : j;
-      if constexpr (kPipe) {
-        if (jn != j && jn % GPS == 0 && !wait_slot(jn / GPS)) {
-          timed_out = true;
-          break;
-        }
-      } else {
-        if (j % GPS == 0 && !wait_slot(j / GPS)) {
-          timed_out = true;
-          break;
-        }
-        qk_scores(j, sc);
+      if (j % GPS == 0 && !wait_slot(j / GPS)) {
+        timed_out = true;
+        break;
       }
+      float sc[8];
+      qk_scores(j, sc);
       const uint4* vcw = reinterpret_cast<const uint4*>(vc_of(j));
       const uint4* vmr = reinterpret_cast<const uint4*>(vm_of(j));
 
@@ -1074,9 +1050,6 @@ __global__ void __launch_bounds__(128, KVQ_DECODE_MIN_BLOCKS) kivi_decode_kernel
         l_run += p[2 * nt] + p[2 * nt + 1];
         vz_run = fmaf(p[2 * nt], zf.x, fmaf(p[2 * nt + 1], zf.y, vz_run));
       }
-
-      // ---- q . k^T of group j + 1 (independent of what follows) ----
-      if constexpr (kPipe) qk_scores(jn, sc);
 
       // ---- o += p' . codes (group j) ----
       uint32_t vw[P::VW];
