@@ -1051,7 +1051,8 @@ kvq_status nvfp4_decode_attention(const uint16_t* q, const nvfp4_pool* k, const 
   if (!(softmax_scale == softmax_scale) || std::isinf(softmax_scale)) return KVQ_ERR_ARG;
   const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(head_dim));
   const int nblk = ceil_div(max_seq_len, 16);
-  const int splits = choose_splits(nblk, batch * kv_heads, kMaxSplits, kvq::nvfp4_decode_blocks_per_sm(head_dim), 0);
+  const int per_sm = kvq::nvfp4_decode_blocks_per_sm(head_dim, q_heads / kv_heads);
+  const int splits = choose_splits(nblk, batch * kv_heads, kMaxSplits, per_sm, 0);
   kvq::Nvfp4DecodeArgs a{};
   a.q = q;
   a.k_pool = k->pool;

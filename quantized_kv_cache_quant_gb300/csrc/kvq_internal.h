@@ -238,7 +238,7 @@ struct Nvfp4DecodeArgs {
   int out_fp32;
 };
 cudaError_t launch_nvfp4_decode(const Nvfp4DecodeArgs& a, cudaStream_t s);
-int nvfp4_decode_blocks_per_sm(int head_dim);
+int nvfp4_decode_blocks_per_sm(int head_dim, int gq);  // gq: query heads per kv head
 
 // scale[0] = fl32(amax / fmax) over n_vec 16-byte vectors of fp16 at x (1 when
 // all are zero): per-block amax partials, then one reducing block.

@@ -279,6 +279,13 @@ __global__ void __launch_bounds__(32 * kCastWarps) nvfp4_cast_kernel(Nvfp4QuantA
 //           scores * s_t(K) * softmax scale.
 //   p.V   : A = p split into fp16 hi + lo rows, B = E2M1 values as fp16 times
 //           the scales of their two tokens (one E4M3 pair); outputs * s_t(V).
+// kSwap (kv heads that serve at most 4 query heads): the operands change
+// sides. The 16 tokens of a block (q.k^T) or 16 channels (p.V) are the tile
+// rows and the query heads its 8 columns: column n of q.k^T carries head n/2
+// (both columns of a head the same query, so lane (g, t) holds head t's scores
+// of tokens g and g + 8), column n of p.V head n/2, part n%2 of p = hi + lo.
+// The A fragments are the same record words the other arrangement reads as B
+// fragments, regrouped (no layout change); half the MMAs and accumulators.
 // ---------------------------------------------------------------------------
 template <int D, int STAGES>
 struct Nvfp4Smem {
@@ -291,10 +298,54 @@ struct Nvfp4Smem {
   static constexpr int BYTES = BAR_BYTES + AREA;
 };
 
-template <int D, int STAGES>
-__global__ void __launch_bounds__(128) nvfp4_decode_kernel(Nvfp4DecodeArgs a) {
+// The reference max m_run moves only when a score exceeds it by more than this
+// (log2 units), so the accumulators are rescaled rarely; the weights
+// p <= 2^kNvfp4MaxSlack keep their fp16 hi + lo split exact to 2^-22 and the
+// fp32 sums far from overflow.
+constexpr float kNvfp4MaxSlack = 8.0f;
+#ifndef KVQ_NVFP4_SWAP_MIN_BLOCKS
+#define KVQ_NVFP4_SWAP_MIN_BLOCKS 4  // resident swapped-operand decode blocks per SM the registers are sized for
+#endif
+
+// Transpose of an 8 x 8 fp16 tile held in mma fragment order across the warp:
+// lane (g, t) holds row g, columns 2t and 2t + 1 before and after.
+__device__ __forceinline__ uint32_t tile_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+// Max and sum over the eight lanes that share t = lane % 4.
+__device__ __forceinline__ float column_max(float v) {
+  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+  return fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+}
+__device__ __forceinline__ float column_sum(float v) {
+  v += __shfl_xor_sync(0xffffffffu, v, 4);
+  v += __shfl_xor_sync(0xffffffffu, v, 8);
+  return v + __shfl_xor_sync(0xffffffffu, v, 16);
+}
+
+// Byte k (0..3, a compile-time value after unrolling) of w -> fp16x2.
+__device__ __forceinline__ uint32_t e2m1_byte(uint32_t w, int k) {
+  switch (k) {
+    case 0: return e2m1x2_to_f16x2<0>(w);
+    case 1: return e2m1x2_to_f16x2<1>(w);
+    case 2: return e2m1x2_to_f16x2<2>(w);
+    default: return e2m1x2_to_f16x2<3>(w);
+  }
+}
+
+__device__ __forceinline__ uint32_t hmul2_bits(uint32_t x, uint32_t y) {
+  return h2_bits(__hmul2(bits_h2(x), bits_h2(y)));
+}
+
+template <int D, int STAGES, bool kSwap>
+__global__ void __launch_bounds__(128, kSwap ? KVQ_NVFP4_SWAP_MIN_BLOCKS : 1) nvfp4_decode_kernel(Nvfp4DecodeArgs a) {
   using S = Nvfp4Smem<D, STAGES>;
   constexpr int KS = D / 16, NT = D / 8, CH = D / 64;  // CH: 16-byte code chunks per lane
+  constexpr int NACC = kSwap ? D / 16 : D / 8;         // p.V accumulator tiles
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
   uint8_t* area = smem + S::BAR_BYTES;
@@ -338,22 +389,38 @@ __global__ void __launch_bounds__(128) nvfp4_decode_kernel(Nvfp4DecodeArgs a) {
     for (int j = 0; j < STAGES && j < n_mine; ++j) issue(j, phys(j));
   }
 
-  const bool row_ok = g < gq;
+  // The query head of this lane's q fragments: row g (A), or column g (B, swapped).
+  const int qh = kSwap ? (g >> 1) : g;
+  const bool q_ok = qh < gq;
   const __half* qrow = reinterpret_cast<const __half*>(a.q) +
-                       (static_cast<long long>(b) * a.q_heads + h * gq + (row_ok ? g : 0)) * D;
+                       (static_cast<long long>(b) * a.q_heads + h * gq + (q_ok ? qh : 0)) * D;
   uint32_t qa[KS][2];
 #pragma unroll
   for (int ks = 0; ks < KS; ++ks)
 #pragma unroll
     for (int jj = 0; jj < 2; ++jj)
-      qa[ks][jj] = row_ok ? *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8 * jj + 2 * tig) : 0u;
+      qa[ks][jj] = q_ok ? *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8 * jj + 2 * tig) : 0u;
   const float kmul = *a.k_scale * a.scale_log2;
   const float vscale = *a.v_scale;
 
   float m_run = -INFINITY, l_run = 0.0f;
-  float o_acc[NT][4];
+  float o_acc[NACC][4];
 #pragma unroll
-  for (int i = 0; i < NT; ++i) o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.0f;
+  for (int i = 0; i < NACC; ++i) o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.0f;
+  auto rescale = [&](float mx) {
+    if (mx > m_run + kNvfp4MaxSlack) {
+      const float alpha = fast_exp2(m_run - mx);
+      l_run *= alpha;
+#pragma unroll
+      for (int i = 0; i < NACC; ++i) {
+        o_acc[i][0] *= alpha;
+        o_acc[i][1] *= alpha;
+        o_acc[i][2] *= alpha;
+        o_acc[i][3] *= alpha;
+      }
+      m_run = mx;
+    }
+  };
 
   int j = 0;
   bool timed_out = false;
@@ -367,8 +434,10 @@ __global__ void __launch_bounds__(128) nvfp4_decode_kernel(Nvfp4DecodeArgs a) {
     const uint8_t* kr = ring + s * S::STAGE;
     const uint8_t* vr = kr + S::REC;
     const int tok_base = (j_begin + warp + 4 * j) * kBlock;
+    const bool ragged = tok_base + kBlock > len;  // the sequence's last block (warp-uniform)
 
-    // keys: stream byte (nt*KS + ks)*2 + r, scales of tokens g (nt = 0) and 8 + g (nt = 1)
+    // keys: stream byte (nt*KS + ks)*2 + r holds channels 16ks + 8r + 2tig, +1 of
+    // token 8nt + g; scale bytes nt*KS + ks of token 8nt + g, four to a word
     uint32_t kw[D / 16];
 #pragma unroll
     for (int c = 0; c < CH; ++c) {
@@ -378,7 +447,7 @@ __global__ void __launch_bounds__(128) nvfp4_decode_kernel(Nvfp4DecodeArgs a) {
       kw[4 * c + 2] = x.z;
       kw[4 * c + 3] = x.w;
     }
-    uint32_t ksw[KS / 2];  // scale bytes nt*KS + ks of row g, four to a word
+    uint32_t ksw[KS / 2];
     if constexpr (D == 128) {
       const uint4 x = *reinterpret_cast<const uint4*>(kr + 8 * D + g * 2 * KS);
       ksw[0] = x.x;
@@ -390,61 +459,14 @@ __global__ void __launch_bounds__(128) nvfp4_decode_kernel(Nvfp4DecodeArgs a) {
       ksw[0] = x.x;
       ksw[1] = x.y;
     }
-    float sacc[2][4];
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.0f;
-#pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-        const int i = nt * KS + ks;                        // (r = 0, 1) bytes 2i, 2i + 1
-        const uint32_t w = kw[i >> 1];
-        const uint32_t sp = e4m3_pair(ksw[i >> 2], (i >> 1) & 1);  // scales i & ~1, i | 1
-        const __half2 sc2 = (i & 1) ? __high2half2(bits_h2(sp)) : __low2half2(bits_h2(sp));
-        uint32_t b0, b1;
-        if (i & 1) {
-          b0 = e2m1x2_to_f16x2<2>(w);
-          b1 = e2m1x2_to_f16x2<3>(w);
-        } else {
-          b0 = e2m1x2_to_f16x2<0>(w);
-          b1 = e2m1x2_to_f16x2<1>(w);
-        }
-        mma16816(sacc[nt], qa[ks][0], 0u, qa[ks][1], 0u, h2_bits(__hmul2(bits_h2(b0), sc2)),
-                 h2_bits(__hmul2(bits_h2(b1), sc2)));
-      }
-    }
-    float sc[4];
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int tok = tok_base + 8 * nt + 2 * tig + e;
-        sc[2 * nt + e] = (tok < len) ? sacc[nt][e] * kmul : -INFINITY;
-      }
-    float mx = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
-    mx = quad_max(mx);
-    const float m_new = fmaxf(m_run, mx);
-    if (m_new != m_run) {
-      const float alpha = fast_exp2(m_run - m_new);
-      l_run *= alpha;
-#pragma unroll
-      for (int i = 0; i < NT; ++i) {
-        o_acc[i][0] *= alpha;
-        o_acc[i][1] *= alpha;
-        o_acc[i][2] *= alpha;
-        o_acc[i][3] *= alpha;
-      }
-      m_run = m_new;
-    }
-    float p[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) p[i] = fast_exp2(sc[i] - m_new);
-    l_run += (p[0] + p[1]) + (p[2] + p[3]);
-    const __half2 h0 = __floats2half2_rn(p[0], p[1]), h1 = __floats2half2_rn(p[2], p[3]);
-    const float2 f0 = __half22float2(h0), f1 = __half22float2(h1);
-    const uint32_t A0 = h2_bits(h0), A1 = pack_rn_f16x2(p[0] - f0.x, p[1] - f0.y);
-    const uint32_t A2 = h2_bits(h1), A3 = pack_rn_f16x2(p[2] - f1.x, p[3] - f1.y);
+    // the fp16 codes of byte pair (i, r) times the scale of stream index i
+    auto key_scale = [&](int i) {
+      const uint32_t sp = e4m3_pair(ksw[i >> 2], (i >> 1) & 1);  // scales i & ~1, i | 1
+      return h2_bits((i & 1) ? __high2half2(bits_h2(sp)) : __low2half2(bits_h2(sp)));
+    };
+    auto key_operand = [&](int i, int r) { return e2m1_byte(kw[i >> 1], 2 * (i & 1) + r); };
 
-    // values: stream byte nt*2 + r (tokens 8r + 2tig, +1 of channel 8nt + g);
+    // values: stream byte nt*2 + r holds tokens 8r + 2tig, +1 of channel 8nt + g;
     // scale pairs ((tig*2 + r)*KS + blk)*2 + {0, 1}, read as this lane's 4*KS bytes
     uint32_t vw[D / 16];
 #pragma unroll
@@ -467,21 +489,83 @@ __global__ void __launch_bounds__(128) nvfp4_decode_kernel(Nvfp4DecodeArgs a) {
         vsw[4 * c + 3] = x.w;
       }
     }
+    auto value_scale = [&](int r, int blk) {
+      const int pr = r * KS + blk;
+      return e4m3_pair(vsw[pr >> 1], pr & 1);
+    };
+
+    if constexpr (!kSwap) {
+      float sacc[2][4];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const uint32_t w = vw[nt >> 1];
-      const int blk = nt >> 1, pr0 = blk, pr1 = KS + blk;  // pair indices of r = 0 and r = 1
-      const uint32_t s0 = e4m3_pair(vsw[pr0 >> 1], pr0 & 1), s1 = e4m3_pair(vsw[pr1 >> 1], pr1 & 1);
-      uint32_t c0, c1;
-      if (nt & 1) {
-        c0 = e2m1x2_to_f16x2<2>(w);
-        c1 = e2m1x2_to_f16x2<3>(w);
-      } else {
-        c0 = e2m1x2_to_f16x2<0>(w);
-        c1 = e2m1x2_to_f16x2<1>(w);
+      for (int nt = 0; nt < 2; ++nt) {
+        sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.0f;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          const int i = nt * KS + ks;
+          const uint32_t sc2 = key_scale(i);
+          mma16816(sacc[nt], qa[ks][0], 0u, qa[ks][1], 0u, hmul2_bits(key_operand(i, 0), sc2),
+                   hmul2_bits(key_operand(i, 1), sc2));
+        }
       }
-      mma16816(o_acc[nt], A0, A1, A2, A3, h2_bits(__hmul2(bits_h2(c0), bits_h2(s0))),
-               h2_bits(__hmul2(bits_h2(c1), bits_h2(s1))));
+      float sc[4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) sc[2 * nt + e] = sacc[nt][e] * kmul;
+      if (ragged) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if (tok_base + 8 * (i >> 1) + 2 * tig + (i & 1) >= len) sc[i] = -INFINITY;
+      }
+      rescale(quad_max(fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]))));
+      float p[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) p[i] = fast_exp2(sc[i] - m_run);
+      l_run += (p[0] + p[1]) + (p[2] + p[3]);
+      const __half2 h0 = __floats2half2_rn(p[0], p[1]), h1 = __floats2half2_rn(p[2], p[3]);
+      const float2 f0 = __half22float2(h0), f1 = __half22float2(h1);
+      const uint32_t A0 = h2_bits(h0), A1 = pack_rn_f16x2(p[0] - f0.x, p[1] - f0.y);
+      const uint32_t A2 = h2_bits(h1), A3 = pack_rn_f16x2(p[2] - f1.x, p[3] - f1.y);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const uint32_t w = vw[nt >> 1];
+        const uint32_t s0 = value_scale(0, nt >> 1), s1 = value_scale(1, nt >> 1);
+        mma16816(o_acc[nt], A0, A1, A2, A3, hmul2_bits(e2m1_byte(w, 2 * (nt & 1)), s0),
+                 hmul2_bits(e2m1_byte(w, 2 * (nt & 1) + 1), s1));
+      }
+    } else {
+      // q.k^T: rows = tokens g, g + 8 (stream indices ks and KS + ks), k = channels of block ks
+      float sacc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        const uint32_t s_g = key_scale(ks), s_g8 = key_scale(KS + ks);
+        mma16816(sacc, hmul2_bits(key_operand(ks, 0), s_g), hmul2_bits(key_operand(KS + ks, 0), s_g8),
+                 hmul2_bits(key_operand(ks, 1), s_g), hmul2_bits(key_operand(KS + ks, 1), s_g8), qa[ks][0],
+                 qa[ks][1]);
+      }
+      // head tig's scores of tokens g and g + 8 (columns 2tig + 1 repeat them)
+      float sc0 = sacc[0] * kmul, sc1 = sacc[2] * kmul;
+      if (ragged) {
+        if (tok_base + g >= len) sc0 = -INFINITY;
+        if (tok_base + 8 + g >= len) sc1 = -INFINITY;
+      }
+      rescale(column_max(fmaxf(sc0, sc1)));
+      const float p0 = fast_exp2(sc0 - m_run), p1 = fast_exp2(sc1 - m_run);
+      l_run += p0 + p1;
+      // p = hi + lo in columns 2tig, 2tig + 1 of token rows g and g + 8, transposed
+      // into the B fragments (k = tokens 2tig, +1 and 2tig + 8, +9; column g)
+      const __half hi0 = __float2half_rn(p0), hi1 = __float2half_rn(p1);
+      const __half lo0 = __float2half_rn(p0 - __half2float(hi0)), lo1 = __float2half_rn(p1 - __half2float(hi1));
+      const uint32_t B0 = tile_trans(h2_bits(__halves2half2(hi0, lo0)));
+      const uint32_t B1 = tile_trans(h2_bits(__halves2half2(hi1, lo1)));
+      // p.V: rows = channels 16mt + g, + 8 (stream bytes 0, 2 / 1, 3 of word mt), k = tokens
+#pragma unroll
+      for (int mt = 0; mt < NACC; ++mt) {
+        const uint32_t w = vw[mt];
+        const uint32_t s0 = value_scale(0, mt), s1 = value_scale(1, mt);
+        mma16816(o_acc[mt], hmul2_bits(e2m1_byte(w, 0), s0), hmul2_bits(e2m1_byte(w, 2), s0),
+                 hmul2_bits(e2m1_byte(w, 1), s1), hmul2_bits(e2m1_byte(w, 3), s1), B0, B1);
+      }
     }
 
     __syncwarp();
@@ -496,20 +580,34 @@ __global__ void __launch_bounds__(128) nvfp4_decode_kernel(Nvfp4DecodeArgs a) {
     m_run = -INFINITY;
     l_run = 0.0f;
 #pragma unroll
-    for (int i = 0; i < NT; ++i) o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.0f;
+    for (int i = 0; i < NACC; ++i) o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.0f;
   }
-  l_run = quad_sum(l_run);
 
   __syncthreads();
+  if constexpr (!kSwap) {
+    l_run = quad_sum(l_run);
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const int c = 8 * nt + 2 * tig;
-    o_s[(warp * 8 + g) * D + c] = (o_acc[nt][0] + o_acc[nt][2]) * vscale;
-    o_s[(warp * 8 + g) * D + c + 1] = (o_acc[nt][1] + o_acc[nt][3]) * vscale;
-  }
-  if (tig == 0) {
-    m_s[warp * 8 + g] = m_run;
-    l_s[warp * 8 + g] = l_run;
+    for (int nt = 0; nt < NT; ++nt) {
+      const int c = 8 * nt + 2 * tig;
+      o_s[(warp * 8 + g) * D + c] = (o_acc[nt][0] + o_acc[nt][2]) * vscale;
+      o_s[(warp * 8 + g) * D + c + 1] = (o_acc[nt][1] + o_acc[nt][3]) * vscale;
+    }
+    if (tig == 0) {
+      m_s[warp * 8 + g] = m_run;
+      l_s[warp * 8 + g] = l_run;
+    }
+  } else {
+    // head tig: channels 16mt + g (columns hi, lo) and 16mt + 8 + g; rows gq.. of the warp's 8 are unused
+    l_run = column_sum(l_run);
+#pragma unroll
+    for (int mt = 0; mt < NACC; ++mt) {
+      o_s[(warp * 8 + tig) * D + 16 * mt + g] = (o_acc[mt][0] + o_acc[mt][1]) * vscale;
+      o_s[(warp * 8 + tig) * D + 16 * mt + 8 + g] = (o_acc[mt][2] + o_acc[mt][3]) * vscale;
+    }
+    if (g == 0) {
+      m_s[warp * 8 + tig] = m_run;
+      l_s[warp * 8 + tig] = l_run;
+    }
   }
   __syncthreads();
   finish_split<D>(o_s, m_s, l_s, gq, static_cast<long long>(b) * a.q_heads + h * gq, split, a.splits, a.splits, a.part_o,
@@ -518,10 +616,13 @@ __global__ void __launch_bounds__(128) nvfp4_decode_kernel(Nvfp4DecodeArgs a) {
 
 constexpr int kNvfp4Stages = 4;
 
-template <int D>
+// The swapped-operand arrangement serves kv heads with at most 4 query heads.
+inline bool nvfp4_swapped(int gq) { return gq <= 4; }
+
+template <int D, bool kSwap>
 cudaError_t nvfp4_decode_dispatch(const Nvfp4DecodeArgs& a, cudaStream_t s) {
   constexpr int smem = Nvfp4Smem<D, kNvfp4Stages>::BYTES;
-  auto kern = nvfp4_decode_kernel<D, kNvfp4Stages>;
+  auto kern = nvfp4_decode_kernel<D, kNvfp4Stages, kSwap>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(a.splits, a.kv_heads, a.batch);
@@ -529,14 +630,14 @@ cudaError_t nvfp4_decode_dispatch(const Nvfp4DecodeArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-template <int D>
+template <int D, bool kSwap>
 int nvfp4_occupancy() {
   static int cached[64] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
   if (cached[dev] == 0) {
     constexpr int smem = Nvfp4Smem<D, kNvfp4Stages>::BYTES;
-    auto kern = nvfp4_decode_kernel<D, kNvfp4Stages>;
+    auto kern = nvfp4_decode_kernel<D, kNvfp4Stages, kSwap>;
     int n = 0;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, 128, smem) != cudaSuccess || n <= 0)
@@ -548,8 +649,9 @@ int nvfp4_occupancy() {
 
 }  // namespace
 
-int nvfp4_decode_blocks_per_sm(int head_dim) {
-  return head_dim == 64 ? nvfp4_occupancy<64>() : nvfp4_occupancy<128>();
+int nvfp4_decode_blocks_per_sm(int head_dim, int gq) {
+  if (nvfp4_swapped(gq)) return head_dim == 64 ? nvfp4_occupancy<64, true>() : nvfp4_occupancy<128, true>();
+  return head_dim == 64 ? nvfp4_occupancy<64, false>() : nvfp4_occupancy<128, false>();
 }
 
 // Resident cast blocks per SM (occupancy API, once per device and variant).
@@ -594,9 +696,11 @@ cudaError_t launch_nvfp4_quantize(const Nvfp4QuantArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_nvfp4_decode(const Nvfp4DecodeArgs& a, cudaStream_t s) {
+  if (a.kv_heads <= 0) return cudaErrorInvalidValue;
+  const bool swapped = nvfp4_swapped(a.q_heads / a.kv_heads);
   switch (a.head_dim) {
-    case 128: return nvfp4_decode_dispatch<128>(a, s);
-    case 64: return nvfp4_decode_dispatch<64>(a, s);
+    case 128: return swapped ? nvfp4_decode_dispatch<128, true>(a, s) : nvfp4_decode_dispatch<128, false>(a, s);
+    case 64: return swapped ? nvfp4_decode_dispatch<64, true>(a, s) : nvfp4_decode_dispatch<64, false>(a, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -185,7 +185,7 @@ def test_fp8_decode_edges(kind, gq):
 
 
 @pytest.mark.parametrize("kind", ["tiny", "fp16_max"])
-@pytest.mark.parametrize("gq", [4, 1])
+@pytest.mark.parametrize("gq", [8, 4, 1])
 def test_nvfp4_decode_edges(kind, gq):
     from test_gpu_nvfp4 import _decode, _oracle_decode
     b, hkv, d, s = 2, 2, 128, 16 * 40 + 5

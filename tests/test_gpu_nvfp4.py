@@ -150,7 +150,7 @@ def _oracle_decode(x, lens, heads=None, scale=None):
 
 
 @pytest.mark.parametrize("d", [64, 128])
-@pytest.mark.parametrize("gq", [1, 4, 8])
+@pytest.mark.parametrize("gq", [1, 2, 3, 4, 8])
 def test_decode_attention(d, gq):
     b, h, s = 3, 2, 300
     x = workloads.make_inputs(b, h, h * gq, d, s, 1, 50 + d + gq)
@@ -159,6 +159,30 @@ def test_decode_attention(d, gq):
     lens = np.array([300, 17, 161], np.int32)
     got = _decode(x, table, nb, lens, h * gq)
     assert_attention_close(got, _oracle_decode(x, lens))
+
+
+@pytest.mark.parametrize("gq", [4, 8])
+def test_decode_rising_logits(gq):
+    """Keys that drift along the query heads' mean direction, so each head's
+    logits rise through the sequence (by 6 to 25 in log2 units over a spread
+    of about 4.5 between tokens): the running maximum of the decode moves many
+    times, in steps below and above its slack, in both operand arrangements (at most 4 query heads per kv
+    head: tokens on the tile rows; more: heads on the rows)."""
+    b, h, s, d = 2, 2, 16 * 37 + 9, 128
+    x = workloads.make_inputs(b, h, h * gq, d, s, 1, 70 + gq)
+    k = x.k.astype(np.float64)
+    q = x.q[0].astype(np.float64)
+    for bi in range(b):
+        for hi in range(h):
+            u = q[bi, hi * gq:(hi + 1) * gq].sum(axis=0)
+            u /= np.linalg.norm(u)
+            k[bi, hi] += np.linspace(0.0, 24.0, s)[:, None] * u
+    xs = workloads.KVInputs(k.astype(np.float16), x.v, x.q, x.k_new, x.v_new)
+    nb = -(-s // 16)
+    table = workloads.block_table(b, nb, 71)
+    lens = np.array([s, 16 * 20 + 3], np.int32)
+    got = _decode(xs, table, nb, lens, h * gq)
+    assert_attention_close(got, _oracle_decode(xs, lens))
 
 
 def test_decode_fp16_output_and_custom_scale():
