@@ -45,7 +45,7 @@ def build(verbose_ptxas: bool = False) -> str:
     objdir = os.path.join(LIBDIR, "obj")
     os.makedirs(objdir, exist_ok=True)
     extra = ["-Xptxas", "-v"] if verbose_ptxas else []
-    # extra nvcc flags for tuning builds, e.g. KVQ_NVCC_FLAGS=-DKVQ_DECODE_MIN_BLOCKS=3
+    # extra nvcc flags for tuning builds, e.g. KVQ_NVCC_FLAGS=-DKVQ_NVFP4_SWAP_MIN_BLOCKS=5
     extra += os.environ.get("KVQ_NVCC_FLAGS", "").split()
     objs = [os.path.join(objdir, s.replace(".cu", ".o")) for s in SOURCES]
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:

@@ -235,6 +235,10 @@ __device__ __noinline__ bool tr_window_chunks(const uint16_t* k_res, const uint1
   return ok;
 }
 
+// 4 resident blocks per SM (113-126 registers). 6 at D = 64 (79 registers) and
+// 5 for the paged cache with 2-bit keys at D = 128 (95) also fit without
+// spills, but measured slower on GB300: MHA D 64 47.8 -> 52.0 us, paged GQA-4
+// 68.5 -> 70.5 us.
 template <int D, int KB, int VB, class SeqT>
 __global__ void __launch_bounds__(128, 4) kivi_decode_tr_kernel(KiviDecodeArgs a, SeqT seqs) {
   using P = KiviTr<D, KB, VB>;

@@ -15,9 +15,15 @@
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
 
-#ifndef KVQ_DECODE_MIN_BLOCKS
-#define KVQ_DECODE_MIN_BLOCKS 3  // resident decode blocks per SM the register budget is sized for
-#endif
+// Resident decode blocks per SM the register budget is sized for: 3 at D = 128
+// (168 registers; a 128-register bound spills 112-204 bytes), 4 at D = 64
+// (118-128 registers, no spills; 5 blocks spill). D = 64 against 3 blocks,
+// GB300: GQA-8 8K 2-bit 97.0 -> 95.7 us, 4-bit 103.1 -> 100.7 us, paged
+// 512-16384 tokens 62.1 -> 59.3 us.
+template <int D>
+struct DecodeMinBlocks {
+  static constexpr int value = (D == 64) ? 4 : 3;
+};
 namespace kvq {
 namespace {
 
@@ -751,7 +757,7 @@ template <>
 struct TableLanes<false> {};
 
 template <int D, int KB, int VB, int STAGES, class SeqT>
-__global__ void __launch_bounds__(128, KVQ_DECODE_MIN_BLOCKS) kivi_decode_kernel(KiviDecodeArgs a, SeqT seqs) {
+__global__ void __launch_bounds__(128, DecodeMinBlocks<D>::value) kivi_decode_kernel(KiviDecodeArgs a, SeqT seqs) {
   using P = Kivi<D, KB, VB>;
   constexpr bool kPaged = !std::is_same<SeqT, NoSeqs>::value;
   using S = DecodeSmem<D, KB, VB, STAGES>;
