@@ -573,8 +573,11 @@ TABLE_ALL = (workloads.MHA_4K.name, workloads.GQA_8K_2BIT.name, workloads.GQA_8K
 
 def table_rows(names):
     """One dict per workload: trimmed mean time of the decode-attention call over
-    the prefilled cache (L2 flushed by writing 512 MB between repetitions), its
-    algorithmic GB/s and fraction of the HBM peak, and the quantize rate."""
+    the prefilled cache, its algorithmic GB/s and fraction of the HBM peak, and
+    the quantize rate. Before each repetition L2 is flushed by writing 512 MB
+    and reading them back: the timed call finds none of its data in L2 and no
+    dirty lines of the flush to write back (after the write alone, the 129 MB
+    of dirty lines cost a 128K prefill ~20 us of write-back)."""
     import torch
     from quantized_kv_cache_quant_gb300 import kvq
 
@@ -590,6 +593,7 @@ def table_rows(names):
         ts = []
         for r in range(reps + warm):
             flush.zero_()
+            flush_sum = torch.sum(flush, dtype=torch.int64)  # reads the 512 MB back: L2 clean
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             fn()
@@ -597,6 +601,7 @@ def table_rows(names):
             torch.cuda.synchronize()
             if r >= warm:
                 ts.append(a.elapsed_time(b) / 1e3)
+        del flush_sum
         ts.sort()
         cut = len(ts) // 10
         return statistics.mean(ts[cut:len(ts) - cut])

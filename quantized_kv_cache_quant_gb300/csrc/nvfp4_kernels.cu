@@ -78,8 +78,8 @@ __device__ __forceinline__ uint32_t e4m3_pair(uint32_t w, int h) {
 // Per element pair the quotient fl32(x / d), d = fl32(S_b * s_t), comes from
 // y = RN(1/d) and one correction step in packed fp32 operations (exact for
 // 2^-96 <= d <= 2^96; a unit with another nonzero d takes the IEEE division
-// per element), the sign of a zero x is restored, and a block whose scale is
-// 0 has its x masked to +0 first, so that all its codes are 0.
+// per element), and a block whose scale is 0 has its x masked to +0 first, so
+// that all its codes are 0.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void cp_async16_zfill(void* dst, const void* src, bool valid) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src), "r"(valid ? 16 : 0)
@@ -87,13 +87,15 @@ __device__ __forceinline__ void cp_async16_zfill(void* dst, const void* src, boo
 }
 
 // fl32(x / d) for each half of the fp16 pair xm (already masked), from the
-// reciprocals y, with the sign of a zero x kept.
-__device__ __forceinline__ float2 quot_pair(uint32_t xm, float2 d, float2 y) {
-  const float2 x = __half22float2(bits_h2(xm));
-  const float2 q0 = __fmul2_rn(x, y);
-  const float2 r = __ffma2_rn(q0, make_float2(-d.x, -d.y), x);
-  const float2 q = __ffma2_rn(r, y, q0);
-  return make_float2(copysignf(q.x, x.x), copysignf(q.y, x.y));
+// negated reciprocals ny = -RN(1/d): q0 = (-x)(-y) = fl32(x y), the residual
+// r = fl32(d q0 - x) (the exact negation of the usual x - d q0, so the same
+// value up to sign) and q = fl32(q0 - r y). Written with -x and -y the signed
+// zeros come out right on their own: x = -0 gives -0, x = +0 gives +0.
+__device__ __forceinline__ float2 quot_pair(uint32_t xm, float2 d, float2 ny) {
+  const float2 nx = __half22float2(__hneg2(bits_h2(xm)));
+  const float2 q0 = __fmul2_rn(nx, ny);
+  const float2 r = __ffma2_rn(d, q0, nx);
+  return __ffma2_rn(r, ny, q0);
 }
 
 template <int D, int ROLE>
@@ -101,9 +103,9 @@ __global__ void __launch_bounds__(32 * kCastWarps) nvfp4_cast_kernel(Nvfp4QuantA
   constexpr int KS = D / 16;
   constexpr int RS = D + 8;  // padded row stride (halves): ldmatrix rows on distinct banks
   __shared__ __align__(16) __half tile[kCastWarps][2][kBlock * RS];
-  // per (channel block, token) of the unit: d = fl32(S_b * s_t), y = RN(1/d) (0 when d = 0) and an
-  // fp16 mask (all ones when d > 0, else 0), in the order the role's element pairs read them:
-  // keys {d, y, mask, -} per token; values {d, d', y, y'} and {mask, mask'} per token pair
+  // per (channel block, token) of the unit: d = fl32(S_b * s_t), ny = -RN(1/d) (-0 when d = 0) and
+  // an fp16 mask (all ones when d > 0, else 0), in the order the role's element pairs read them:
+  // keys {d, ny, mask, -} per token; values {d, d', ny, ny'} and {mask, mask'} per token pair
   constexpr int NPAR = (ROLE == 0) ? KS * kBlock : KS * kBlock / 2;
   __shared__ __align__(16) float4 par[kCastWarps][NPAR];
   __shared__ __align__(4) uint16_t msk[kCastWarps][KS * kBlock];  // values: [block][token]
@@ -164,14 +166,14 @@ __global__ void __launch_bounds__(32 * kCastWarps) nvfp4_cast_kernel(Nvfp4QuantA
         const float S = __half2float(__ushort_as_half(static_cast<unsigned short>(e4m3x2_to_f16x2(
             static_cast<uint16_t>(byte)) & 0xFFFFu)));
         const float d = __fmul_rn(S, s_t);
-        const float y = (d > 0.0f) ? __frcp_rn(d) : 0.0f;
+        const float ny = -((d > 0.0f) ? __frcp_rn(d) : 0.0f);
         sbyte[warp][p] = static_cast<uint8_t>(byte);
         if constexpr (ROLE == 0) {
-          par[warp][ks * kBlock + tok] = make_float4(d, y, __uint_as_float(d > 0.0f ? 0xFFFFFFFFu : 0u), 0.0f);
+          par[warp][ks * kBlock + tok] = make_float4(d, ny, __uint_as_float(d > 0.0f ? 0xFFFFFFFFu : 0u), 0.0f);
         } else {
           float* pv = reinterpret_cast<float*>(&par[warp][ks * (kBlock / 2) + (tok >> 1)]);
           pv[tok & 1] = d;
-          pv[2 + (tok & 1)] = y;
+          pv[2 + (tok & 1)] = ny;
           msk[warp][ks * kBlock + tok] = (d > 0.0f) ? 0xFFFFu : 0u;
         }
         slow |= d > 0.0f && (d < 0x1p-96f || d > 0x1p96f);
@@ -185,8 +187,8 @@ __global__ void __launch_bounds__(32 * kCastWarps) nvfp4_cast_kernel(Nvfp4QuantA
       const uint16_t* mw = msk[warp];
       // fl32(x / d) of one fp16 pair of elements: the reciprocal path, or (a unit with a block scale
       // outside its range) the IEEE division
-      auto quot = [&](bool ieee, uint32_t xm, float2 d, float2 y) -> float2 {
-        if (!ieee) return quot_pair(xm, d, y);
+      auto quot = [&](bool ieee, uint32_t xm, float2 d, float2 ny) -> float2 {
+        if (!ieee) return quot_pair(xm, d, ny);
         const float2 x = __half22float2(bits_h2(xm));
         return make_float2(d.x == 0.0f ? 0.0f : __fdiv_rn(x.x, d.x), d.y == 0.0f ? 0.0f : __fdiv_rn(x.y, d.y));
       };
