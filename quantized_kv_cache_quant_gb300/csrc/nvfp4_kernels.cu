@@ -156,9 +156,13 @@ __global__ void __launch_bounds__(32 * kCastWarps) nvfp4_cast_kernel(Nvfp4QuantA
         const int sw = (ks >> 2) & 1;
         const uint4 v0 = row[sw], v1 = row[sw ^ 1];
         const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-        uint32_t m = 0;
+        // |x| as 15-bit patterns (ordered like the values), maxima of both halves at once
+        uint32_t a[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) m = max(m, max(w[k] & 0x7FFFu, (w[k] >> 16) & 0x7FFFu));
+        for (int k = 0; k < 8; ++k) a[k] = w[k] & 0x7FFF7FFFu;
+        const uint32_t m2 = __vimax3_u16x2(__vimax3_u16x2(a[0], a[1], a[2]), __vimax3_u16x2(a[3], a[4], a[5]),
+                                           __vmaxu2(a[6], a[7]));
+        const uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
         const float amax = __half2float(__ushort_as_half(static_cast<unsigned short>(m)));
         const float a6 = div_rn_by_rcp(amax, 6.0f, y_6);  // amax is a finite fp16 value: exact
         const float v = st_fast ? div_rn_by_rcp(a6, s_t, y_t) : __fdiv_rn(a6, s_t);
@@ -198,15 +202,21 @@ __global__ void __launch_bounds__(32 * kCastWarps) nvfp4_cast_kernel(Nvfp4QuantA
         for (int c = 0; c < D / 64; ++c) {
           float2 q[16];
           if constexpr (ROLE == 0) {
-            // keys: byte p = (nt * KS + ks) * 2 + r holds channels 16 ks + 8 r + 2 tig, +1 of token 8 nt + g
+            // keys: byte p = (nt * KS + ks) * 2 + r holds channels 16 ks + 8 r + 2 tig, +1 of token 8 nt + g:
+            // the (g, tig) element pair of the 8 x 8 tile of tokens 8 nt .., channels 8 (p % 2KS) .., four
+            // tiles (consecutive p) per ldmatrix
 #pragma unroll
-            for (int kk = 0; kk < 16; ++kk) {
-              const int p = 16 * c + kk, nt = p / (2 * KS), ks = (p % (2 * KS)) >> 1, r = p & 1;
-              const int tok = 8 * nt + g, ch = 16 * ks + 8 * r + 2 * tig;
-              const uint32_t xp = *reinterpret_cast<const uint32_t*>(xs + tok * RS + ch);
-              const float4 pr = pw[ks * kBlock + tok];
-              q[kk] = quot(ieee, masked ? xp & __float_as_uint(pr.z) : xp, make_float2(pr.x, pr.x),
-                           make_float2(pr.y, pr.y));
+            for (int q4 = 0; q4 < 4; ++q4) {
+              uint32_t t4[4];
+              const int pl = 16 * c + 4 * q4 + (lane >> 3);  // the tile whose row this lane addresses
+              ldsm_x4(t4, xs + (8 * (pl / (2 * KS)) + (lane & 7)) * RS + 8 * (pl % (2 * KS)));
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int kk = 4 * q4 + e, p = 16 * c + kk, nt = p / (2 * KS), ks = (p % (2 * KS)) >> 1;
+                const float4 pr = pw[ks * kBlock + 8 * nt + g];
+                q[kk] = quot(ieee, masked ? t4[e] & __float_as_uint(pr.z) : t4[e], make_float2(pr.x, pr.x),
+                             make_float2(pr.y, pr.y));
+              }
             }
           } else {
             // values: byte p = nt * 2 + r holds tokens 8 r + 2 tig, +1 of channel 8 nt + g, from the
