@@ -66,8 +66,23 @@ __device__ __forceinline__ void group_scale_zero(float mn, float mx, float level
   z16 = __float2half_rn(__fadd_rn(mn, 0.0f));  // exact; -0 becomes +0
 }
 
+// fl32(x - z) of both halves of the fp16 pair x (nz = -z): one mixed-precision
+// fused multiply-add x * 1 + nz per element, the widening to fp32 included
+// (the product is exact, the sum rounds once).
+__device__ __forceinline__ float2 sub_f16_f32(uint32_t x, float2 nz) {
+  float2 d;
+  asm("{\n\t.reg .b16 xl, xh, one;\n\t"
+      "mov.b32 {xl, xh}, %2;\n\t"
+      "mov.b16 one, 0x3C00;\n\t"
+      "fma.rn.f32.f16 %0, xl, one, %3;\n\t"
+      "fma.rn.f32.f16 %1, xh, one, %4;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "r"(x), "f"(nz.x), "f"(nz.y));
+  return d;
+}
+
 // The group formula's codes clamp(rint(fl32((x - z) / s)), 0, levels) of two
-// fp16 values x (one group each: zero points z, scales s, reciprocals
+// fp16 values x (one group each: nz = -z, and sr = {-s, -s', rcp, rcp'} with
 // rcp = RN(1/s)) in packed fp32 operations, as {code0, code1} in the two
 // 16-bit halves. The quotient comes from rcp and one correction step (q0 =
 // d rcp, r = d - q0 s by fused multiply-add, q = q0 + r rcp), bit-identical
@@ -76,10 +91,11 @@ __device__ __forceinline__ void group_scale_zero(float mn, float mx, float level
 // leaves no negative quotient, so q + 2^23 rounds q to an integer to nearest
 // even in its low bits (q < 2^22); the two low halves are merged and clamped
 // to the top code with one 16-bit SIMD min.
-__device__ __forceinline__ uint32_t group_code_pair(__half2 x, float2 zf, float2 sf, float2 rcp, uint32_t levels) {
-  const float2 d = __fadd2_rn(__half22float2(x), make_float2(-zf.x, -zf.y));
+__device__ __forceinline__ uint32_t group_code_pair(uint32_t x, float2 nz, float4 sr, uint32_t levels) {
+  const float2 d = sub_f16_f32(x, nz);
+  const float2 rcp = make_float2(sr.z, sr.w);
   const float2 q0 = __fmul2_rn(d, rcp);
-  const float2 r = __ffma2_rn(q0, make_float2(-sf.x, -sf.y), d);
+  const float2 r = __ffma2_rn(q0, make_float2(sr.x, sr.y), d);
   const float2 q = __ffma2_rn(r, rcp, q0);
   const float2 t = __fadd2_rn(q, make_float2(0x1p23f, 0x1p23f));
   const uint32_t pair = __byte_perm(__float_as_uint(t.x), __float_as_uint(t.y), 0x5410);
@@ -175,8 +191,8 @@ constexpr uint32_t kThresholdBase = threshold_base();
 // channels d0 - 2 tg ..), values {x[t0][ch], x[t0 + 1][ch]} (the transposed
 // tiles of tokens t0 - 2 tg .., channels ch - gg ..).
 template <int D, int KB>
-__device__ __forceinline__ uint32_t key_word(const __half* xk, int RS, const float* sk, const float* zk,
-                                             const float* rk, const uint4* thk, int u, int lane) {
+__device__ __forceinline__ uint32_t key_word(const __half* xk, int RS, const float4* srk, const float2* nzk,
+                                             const uint4* thk, int u, int lane) {
   constexpr uint32_t KL = (1u << KB) - 1u;
   const int tg = lane & 3;
   uint32_t w = 0;
@@ -195,19 +211,19 @@ __device__ __forceinline__ uint32_t key_word(const __half* xk, int RS, const flo
         w += threshold_pair(bits_h2(xr[nt]), th.x, th.y, th.z) << (2 * f);
       }
     } else {
-      const float2 s01 = *reinterpret_cast<const float2*>(sk + d0), z01 = *reinterpret_cast<const float2*>(zk + d0),
-                   r01 = *reinterpret_cast<const float2*>(rk + d0);
+      const float4 sr = srk[d0 / 2];
+      const float2 nz = nzk[d0 / 2];
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt)  // fields never overlap: adding the shifted pair sets the same bits as or-ing
-        w += group_code_pair(bits_h2(xr[nt]), z01, s01, r01, KL) << (KB * nt);
+        w += group_code_pair(xr[nt], nz, sr, KL) << (KB * nt);
     }
   }
   return (KB == 2) ? w - kThresholdBase : w;
 }
 
 template <int D, int VB>
-__device__ __forceinline__ uint32_t value_word(const __half* xv, int RS, const float* sv, const float* zv,
-                                               const float* rv, const uint4* thv, int u, int lane) {
+__device__ __forceinline__ uint32_t value_word(const __half* xv, int RS, const float4* srv, const float2* nzv,
+                                               const uint4* thv, int u, int lane) {
   constexpr uint32_t VL = (1u << VB) - 1u;
   constexpr int NQ = D / 32;
   const int tg = lane & 3;
@@ -228,10 +244,10 @@ __device__ __forceinline__ uint32_t value_word(const __half* xv, int RS, const f
         w += threshold_pair(bits_h2(xr[n]), th.x, th.y, th.z) << (2 * f);
       }
     } else {
-      const float2 s01 = *reinterpret_cast<const float2*>(sv + t0), z01 = *reinterpret_cast<const float2*>(zv + t0),
-                   r01 = *reinterpret_cast<const float2*>(rv + t0);
+      const float4 sr = srv[t0 / 2];
+      const float2 nz = nzv[t0 / 2];
 #pragma unroll
-      for (int n = 0; n < 4; ++n) w += group_code_pair(bits_h2(xr[n]), z01, s01, r01, VL) << (VB * n);
+      for (int n = 0; n < 4; ++n) w += group_code_pair(xr[n], nz, sr, VL) << (VB * n);
     }
   }
   return (VB == 2) ? w - kThresholdBase : w;
@@ -270,13 +286,11 @@ __device__ __forceinline__ void quantize_tiles(const __half* xk, const __half* x
                                                uint8_t* vc, uint8_t* vm, bool write) {
   using P = Kivi<D, KB, VB>;
   constexpr int RS = Tile<D>::RS;
-  // scale, zero, RN(1/scale) per key channel and per value token (8-byte aligned: read in pairs)
-  __shared__ __align__(8) float sk[D];
-  __shared__ __align__(8) float zk[D];
-  __shared__ __align__(8) float rk[D];
-  __shared__ __align__(8) float sv[32];
-  __shared__ __align__(8) float zv[32];
-  __shared__ __align__(8) float rv[32];
+  // 4-bit codes: per pair of key channels (value tokens) {-s, -s', RN(1/s), RN(1/s')} and {-z, -z'}
+  __shared__ float4 srk[D / 2];
+  __shared__ float2 nzk[D / 2];
+  __shared__ float4 srv[16];
+  __shared__ float2 nzv[16];
   __shared__ uint16_t skb[D], zkb[D], svb[32], zvb[32];  // fp16 bits of scale and zero
   // 2-bit thresholds: entry j = {t1, t2, t3} of channels (keys) or tokens (values) 2j and 2j + 1
   __shared__ __align__(16) uint4 thk[D / 2];
@@ -300,14 +314,15 @@ __device__ __forceinline__ void quantize_tiles(const __half* xk, const __half* x
     }
     const float2 mnf = __half22float2(mn), mxf = __half22float2(mx);
     uint32_t th[3] = {0u, 0u, 0u};  // KB == 2: thresholds of channels 2 tid (low half) and 2 tid + 1
+    float sr[4], nz[2];
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       __half s16, z16;
       group_scale_zero(e ? mnf.y : mnf.x, e ? mxf.y : mxf.x, KL, s16, z16);
       const int c = 2 * tid + e;
-      sk[c] = __half2float(s16);
-      zk[c] = __half2float(z16);
-      rk[c] = (__half2float(s16) == 0.0f) ? 0.0f : __frcp_rn(__half2float(s16));
+      sr[e] = -__half2float(s16);
+      sr[2 + e] = (__half2float(s16) == 0.0f) ? 0.0f : __frcp_rn(__half2float(s16));
+      nz[e] = -__half2float(z16);
       skb[c] = __half_as_ushort(s16);
       zkb[c] = __half_as_ushort(z16);
       if constexpr (KB == 2) {
@@ -316,7 +331,12 @@ __device__ __forceinline__ void quantize_tiles(const __half* xk, const __half* x
           th[k - 1] |= code_threshold(__half_as_ushort(z16), __half2float(z16), __half2float(s16), k) << (16 * e);
       }
     }
-    if constexpr (KB == 2) thk[tid] = make_uint4(th[0], th[1], th[2], 0u);
+    if constexpr (KB == 2) {
+      thk[tid] = make_uint4(th[0], th[1], th[2], 0u);
+    } else {
+      srk[tid] = make_float4(sr[0], sr[1], sr[2], sr[3]);
+      nzk[tid] = make_float2(nz[0], nz[1]);
+    }
   } else if (warp >= 2) {
     // values: warps 2 and 3, two lanes per token, each over half of the row
     // with fp16 pair min/max; lane L reads its words in the order (c + L) mod
@@ -338,9 +358,12 @@ __device__ __forceinline__ void quantize_tiles(const __half* xk, const __half* x
     __half s16, z16;
     group_scale_zero(mnf, mxf, VL, s16, z16);
     if (hh == 0) {
-      sv[t] = __half2float(s16);
-      zv[t] = __half2float(z16);
-      rv[t] = (__half2float(s16) == 0.0f) ? 0.0f : __frcp_rn(__half2float(s16));
+      if constexpr (VB != 2) {
+        float* sr = reinterpret_cast<float*>(srv + (t >> 1));
+        sr[t & 1] = -__half2float(s16);
+        sr[2 + (t & 1)] = (__half2float(s16) == 0.0f) ? 0.0f : __frcp_rn(__half2float(s16));
+        reinterpret_cast<float*>(nzv + (t >> 1))[t & 1] = -__half2float(z16);
+      }
       svb[t] = __half_as_ushort(s16);
       zvb[t] = __half_as_ushort(z16);
     }
@@ -369,20 +392,20 @@ __device__ __forceinline__ void quantize_tiles(const __half* xk, const __half* x
     uint4* kdst = reinterpret_cast<uint4*>(kc);
     for (int ug = warp; ug < P::KW / 4; ug += 2) {
       uint4 w;
-      w.x = key_word<D, KB>(xk, RS, sk, zk, rk, thk, 4 * ug, lane);
-      w.y = key_word<D, KB>(xk, RS, sk, zk, rk, thk, 4 * ug + 1, lane);
-      w.z = key_word<D, KB>(xk, RS, sk, zk, rk, thk, 4 * ug + 2, lane);
-      w.w = key_word<D, KB>(xk, RS, sk, zk, rk, thk, 4 * ug + 3, lane);
+      w.x = key_word<D, KB>(xk, RS, srk, nzk, thk, 4 * ug, lane);
+      w.y = key_word<D, KB>(xk, RS, srk, nzk, thk, 4 * ug + 1, lane);
+      w.z = key_word<D, KB>(xk, RS, srk, nzk, thk, 4 * ug + 2, lane);
+      w.w = key_word<D, KB>(xk, RS, srk, nzk, thk, 4 * ug + 3, lane);
       kdst[ug * 32 + lane] = w;
     }
   } else {
     uint4* vdst = reinterpret_cast<uint4*>(vc);
     for (int ug = warp - 2; ug < P::VW / 4; ug += 2) {
       uint4 w;
-      w.x = value_word<D, VB>(xv, RS, sv, zv, rv, thv, 4 * ug, lane);
-      w.y = value_word<D, VB>(xv, RS, sv, zv, rv, thv, 4 * ug + 1, lane);
-      w.z = value_word<D, VB>(xv, RS, sv, zv, rv, thv, 4 * ug + 2, lane);
-      w.w = value_word<D, VB>(xv, RS, sv, zv, rv, thv, 4 * ug + 3, lane);
+      w.x = value_word<D, VB>(xv, RS, srv, nzv, thv, 4 * ug, lane);
+      w.y = value_word<D, VB>(xv, RS, srv, nzv, thv, 4 * ug + 1, lane);
+      w.z = value_word<D, VB>(xv, RS, srv, nzv, thv, 4 * ug + 2, lane);
+      w.w = value_word<D, VB>(xv, RS, srv, nzv, thv, 4 * ug + 3, lane);
       vdst[ug * 32 + lane] = w;
     }
   }
