@@ -656,7 +656,7 @@ def table_rows(names):
             for x16, role in ((k, kvq.ROLE_KEY), (v, kvq.ROLE_VALUE)):
                 xd = dev(x16)
                 p = kvq.Nvfp4Pool(role, w.batch * nb, w.kv_heads, w.head_dim)
-                t_q.append(timed(lambda: p.quantize(xd, tbl, nb), reps=5))
+                t_q.append(timed(lambda: p.quantize(xd, tbl, nb), reps=10))
                 pools.append(p)
                 del xd
             out = torch.empty((w.batch, w.q_heads, w.head_dim), dtype=torch.float32, device="cuda")
@@ -683,7 +683,7 @@ def table_rows(names):
                 xd = dev(x16)
                 p = kvq.Fp8Pool(role, w.batch * nb, w.kv_heads, w.head_dim, fp8_format=kvq.FP8_FORMATS[w.fmt],
                                 per_head=w.per_head)
-                t_q.append(timed(lambda: p.quantize(xd, tbl, nb), reps=5))
+                t_q.append(timed(lambda: p.quantize(xd, tbl, nb), reps=10))
                 pools.append(p)
                 del xd
             out = torch.empty((w.batch, w.q_heads, w.head_dim), dtype=torch.float32, device="cuda")
