@@ -513,6 +513,13 @@ __global__ void __launch_bounds__(128) kivi_quantize_paged_kernel(PagedQuantArgs
     const long long bh = static_cast<long long>(pb) * a.q.kv_heads + ph;
     return bh * a.q.src_bh_stride + static_cast<long long>(a.r.src0[pb] + 32 * (px - a.r.begin[pb])) * D;
   };
+  // the pool block of item x of sequence pb (its block-table entry), loaded one item ahead
+  // together with that item's tiles, so that the load is not waited for
+  auto table_entry = [&](int pb, int px) {
+    return __ldg(a.pools.block_table + static_cast<long long>(pb) * a.pools.groups_cap + a.r.dst0[pb] +
+                 (px - a.r.begin[pb]));
+  };
+  int blk = table_entry(b, x);
   {
     const long long off = src_off(b, x, h);
     load_group_async<D>(a.q.k_src + off, a.q.v_src + off, tiles[0][0], tiles[0][1]);
@@ -526,15 +533,15 @@ __global__ void __launch_bounds__(128) kivi_quantize_paged_kernel(PagedQuantArgs
     } else {
       while (a.r.begin[nb + 1] <= nx) ++nb;  // nb < n_seqs: nx < total_x = begin[n_seqs]
     }
+    int nblk = -1;
     if (nh < a.q.kv_heads) {
+      nblk = table_entry(nb, nx);
       const long long off = src_off(nb, nx, nh);
       load_group_async<D>(a.q.k_src + off, a.q.v_src + off, tiles[buf ^ 1][0], tiles[buf ^ 1][1]);
     }
     cp_async_commit();
     cp_async_wait_all_but_newest();
     __syncthreads();
-    const int grp = x - a.r.begin[b];
-    const int blk = __ldg(a.pools.block_table + static_cast<long long>(b) * a.pools.groups_cap + a.r.dst0[b] + grp);
     const bool ok = blk >= 0 && blk < a.pools.num_blocks;
     uint8_t* e = a.q.k_codes + (static_cast<long long>(ok ? blk : 0) * a.q.kv_heads + h) * P::STAGE;
     quantize_tiles<D, KB, VB>(tiles[buf][0], tiles[buf][1], e, e + P::KC, e + P::KC + P::KM,
@@ -542,6 +549,7 @@ __global__ void __launch_bounds__(128) kivi_quantize_paged_kernel(PagedQuantArgs
     h = nh;
     x = nx;
     b = nb;
+    blk = nblk;
   }
 }
 
