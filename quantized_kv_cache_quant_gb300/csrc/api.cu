@@ -452,7 +452,23 @@ kvq_status kv_quant_prefill(kivi_cache* cache, const uint16_t* k, const uint16_t
   const int grouped = (R > 0) ? kGroup * ceil_div(std::max(seq_len - R, 0), kGroup) : kGroup * (seq_len / kGroup);
   const int resid = seq_len - grouped;
   kivi_cache c = *cache;
-  if (grouped > 0) {
+  // the window fill: tokens [grouped, seq_len) of every (b, h) to rows 0.. of the window
+  kvq::CopyTokensArgs m{};
+  if (resid > 0) {
+    m.k_src = k;
+    m.v_src = v;
+    m.src_bh_stride = static_cast<long long>(seq_len) * c.cfg.head_dim;
+    m.src_tok0 = grouped;
+    m.k_dst = c.k_res;
+    m.v_dst = c.v_res;
+    m.dst_bh_stride = static_cast<long long>(c.res_cap) * c.cfg.head_dim;
+    m.dst_tok0 = 0;
+    m.n_tokens = resid;
+    m.bh = c.cfg.batch * c.cfg.kv_heads;
+    m.head_dim = c.cfg.head_dim;
+  }
+  {
+    // one launch: the groups, then (same grid, as blocks run out of groups) the window fill
     kvq::QuantGroupsArgs q{};
     q.k_src = k;
     q.v_src = v;
@@ -470,23 +486,7 @@ kvq_status kv_quant_prefill(kivi_cache* cache, const uint16_t* k, const uint16_t
     q.k_meta = c.k_meta;
     q.v_codes = c.v_codes;
     q.v_meta = c.v_meta;
-    st = from_cuda(kvq::launch_kivi_quantize(q, s));
-    if (st != KVQ_OK) return st;
-  }
-  if (resid > 0) {
-    kvq::CopyTokensArgs m{};
-    m.k_src = k;
-    m.v_src = v;
-    m.src_bh_stride = static_cast<long long>(seq_len) * c.cfg.head_dim;
-    m.src_tok0 = grouped;
-    m.k_dst = c.k_res;
-    m.v_dst = c.v_res;
-    m.dst_bh_stride = static_cast<long long>(c.res_cap) * c.cfg.head_dim;
-    m.dst_tok0 = 0;
-    m.n_tokens = resid;
-    m.bh = c.cfg.batch * c.cfg.kv_heads;
-    m.head_dim = c.cfg.head_dim;
-    st = from_cuda(kvq::launch_copy_tokens(m, s));
+    st = from_cuda(kvq::launch_kivi_quantize(q, s, &m));
     if (st != KVQ_OK) return st;
   }
   cache->n_grouped = grouped;

@@ -434,13 +434,32 @@ __device__ __forceinline__ void quantize_tiles(const __half* xk, const __half* x
   __syncthreads();  // the tiles and the block's statistics are free again
 }
 
+// The 16-byte vectors first, first + stride, ... of a token copy (vector i: (b, h)
+// row i / (n_tokens * D/8), token and vector within it), K and V together.
+__device__ __forceinline__ void copy_token_vectors(const CopyTokensArgs& a, long long first, long long stride) {
+  const int vec_per_tok = a.head_dim / 8;
+  const long long per_bh = static_cast<long long>(a.n_tokens) * vec_per_tok;
+  const long long total = per_bh * a.bh;
+  for (long long i = first; i < total; i += stride) {
+    const long long bh = i / per_bh;
+    const long long rem = i % per_bh;
+    const long long tok = rem / vec_per_tok, v = rem % vec_per_tok;
+    const long long s = (bh * a.src_bh_stride + (a.src_tok0 + tok) * a.head_dim) / 8 + v;
+    const long long d = (bh * a.dst_bh_stride + (a.dst_tok0 + tok) * a.head_dim) / 8 + v;
+    reinterpret_cast<uint4*>(a.k_dst)[d] = reinterpret_cast<const uint4*>(a.k_src)[s];
+    reinterpret_cast<uint4*>(a.v_dst)[d] = reinterpret_cast<const uint4*>(a.v_src)[s];
+  }
+}
+
 // Persistent blocks over the items (group, kv head, batch row), group index
 // fastest: item i goes to group dst_group0 + grp of the contiguous grouped
 // region, read from source token src_tok0 + 32 * grp. Each block stages the
 // next item's tiles with asynchronous copies into its second buffer while it
-// quantizes the current one.
+// quantizes the current one. Then the grid copies the fp16 tokens of w (a
+// prefill's window fill; n_tokens = 0: none) in a grid-stride loop, so that
+// blocks that run out of groups early copy while the others finish.
 template <int D, int KB, int VB>
-__global__ void __launch_bounds__(128) kivi_quantize_kernel(QuantGroupsArgs a) {
+__global__ void __launch_bounds__(128) kivi_quantize_kernel(QuantGroupsArgs a, CopyTokensArgs w) {
   using P = Kivi<D, KB, VB>;
   constexpr int TILE = 32 * Tile<D>::RS;
   __shared__ __align__(16) __half tiles[2][2][TILE];  // [buffer][keys, values]
@@ -448,11 +467,10 @@ __global__ void __launch_bounds__(128) kivi_quantize_kernel(QuantGroupsArgs a) {
   // item = bh * n_groups + grp, advanced by gridDim.x = step_bh * n_groups + step_grp per turn
   const int step_bh = static_cast<int>(gridDim.x) / a.n_groups, step_grp = static_cast<int>(gridDim.x) % a.n_groups;
   int bh = static_cast<int>(blockIdx.x) / a.n_groups, grp = static_cast<int>(blockIdx.x) % a.n_groups;
-  if (bh >= n_bh) return;
   auto src_off = [&](int pbh, int pgrp) {
     return static_cast<long long>(pbh) * a.src_bh_stride + static_cast<long long>(a.src_tok0 + 32 * pgrp) * D;
   };
-  {
+  if (bh < n_bh) {
     const long long off = src_off(bh, grp);
     load_group_async<D>(a.k_src + off, a.v_src + off, tiles[0][0], tiles[0][1]);
   }
@@ -473,6 +491,9 @@ __global__ void __launch_bounds__(128) kivi_quantize_kernel(QuantGroupsArgs a) {
     bh = nbh;
     grp = ngrp;
   }
+  if (w.n_tokens > 0)
+    copy_token_vectors(w, blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x,
+                       static_cast<long long>(gridDim.x) * blockDim.x);
 }
 
 // The sequence that owns item x of a batched launch: the b < n with
@@ -560,19 +581,8 @@ __global__ void copy_tokens_kernel(CopyTokensArgs a) {
   // A decode launched right after this copy may start now: it reads what this
   // kernel writes (the fp16 window) only after its griddepcontrol.wait.
   asm volatile("griddepcontrol.launch_dependents;");
-  const int vec_per_tok = a.head_dim / 8;
-  const long long per_bh = static_cast<long long>(a.n_tokens) * vec_per_tok;
-  const long long total = per_bh * a.bh;
-  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const long long bh = i / per_bh;
-    const long long rem = i % per_bh;
-    const long long tok = rem / vec_per_tok, v = rem % vec_per_tok;
-    const long long s = (bh * a.src_bh_stride + (a.src_tok0 + tok) * a.head_dim) / 8 + v;
-    const long long d = (bh * a.dst_bh_stride + (a.dst_tok0 + tok) * a.head_dim) / 8 + v;
-    reinterpret_cast<uint4*>(a.k_dst)[d] = reinterpret_cast<const uint4*>(a.k_src)[s];
-    reinterpret_cast<uint4*>(a.v_dst)[d] = reinterpret_cast<const uint4*>(a.v_src)[s];
-  }
+  copy_token_vectors(a, blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x,
+                     static_cast<long long>(gridDim.x) * blockDim.x);
 }
 
 // Batched copies of a paged cache: token x of the launch (x < begin[n]) is
@@ -1229,11 +1239,11 @@ int quantize_grid(Kern kern, long long items, int (&cached)[64]) {
 }
 
 template <int D, int KB, int VB>
-cudaError_t quantize_dispatch(const QuantGroupsArgs& a, cudaStream_t s) {
+cudaError_t quantize_dispatch(const QuantGroupsArgs& a, const CopyTokensArgs& w, cudaStream_t s) {
   const long long total = static_cast<long long>(a.n_groups) * a.kv_heads * a.batch;
   static int cached[64] = {0};
   const int blocks = quantize_grid(kivi_quantize_kernel<D, KB, VB>, total, cached);
-  kivi_quantize_kernel<D, KB, VB><<<blocks, 128, 0, s>>>(a);
+  kivi_quantize_kernel<D, KB, VB><<<blocks, 128, 0, s>>>(a, w);
   return cudaGetLastError();
 }
 
@@ -1292,18 +1302,20 @@ cudaError_t decode_dispatch(const KiviDecodeArgs& a, const SeqT& seqs, cudaStrea
 
 }  // namespace
 
-cudaError_t launch_kivi_quantize(const QuantGroupsArgs& a, cudaStream_t s) {
-  if (a.n_groups <= 0) return cudaSuccess;
+cudaError_t launch_kivi_quantize(const QuantGroupsArgs& a, cudaStream_t s, const CopyTokensArgs* window) {
+  CopyTokensArgs w{};
+  if (window != nullptr && window->n_tokens > 0) w = *window;
+  if (a.n_groups <= 0) return launch_copy_tokens(w, s);  // nothing to quantize: the copy alone (if any)
   const int key = a.head_dim * 100 + a.k_bits * 10 + a.v_bits;
   switch (key) {
-    case 6422: return quantize_dispatch<64, 2, 2>(a, s);
-    case 6424: return quantize_dispatch<64, 2, 4>(a, s);
-    case 6442: return quantize_dispatch<64, 4, 2>(a, s);
-    case 6444: return quantize_dispatch<64, 4, 4>(a, s);
-    case 12822: return quantize_dispatch<128, 2, 2>(a, s);
-    case 12824: return quantize_dispatch<128, 2, 4>(a, s);
-    case 12842: return quantize_dispatch<128, 4, 2>(a, s);
-    case 12844: return quantize_dispatch<128, 4, 4>(a, s);
+    case 6422: return quantize_dispatch<64, 2, 2>(a, w, s);
+    case 6424: return quantize_dispatch<64, 2, 4>(a, w, s);
+    case 6442: return quantize_dispatch<64, 4, 2>(a, w, s);
+    case 6444: return quantize_dispatch<64, 4, 4>(a, w, s);
+    case 12822: return quantize_dispatch<128, 2, 2>(a, w, s);
+    case 12824: return quantize_dispatch<128, 2, 4>(a, w, s);
+    case 12842: return quantize_dispatch<128, 4, 2>(a, w, s);
+    case 12844: return quantize_dispatch<128, 4, 4>(a, w, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -21,7 +21,6 @@ struct QuantGroupsArgs {
   uint8_t* v_codes;
   uint8_t* v_meta;
 };
-cudaError_t launch_kivi_quantize(const QuantGroupsArgs& a, cudaStream_t s);
 
 // Copy n_tokens fp16 rows of D channels for every (b, h) (K and V together).
 struct CopyTokensArgs {
@@ -38,6 +37,11 @@ struct CopyTokensArgs {
   int head_dim;
 };
 cudaError_t launch_copy_tokens(const CopyTokensArgs& a, cudaStream_t s);
+
+// Quantize a's groups; window (optional, n_tokens > 0) is a token copy that the
+// same launch makes after its groups (a prefill's window fill), or alone when
+// a has no groups.
+cudaError_t launch_kivi_quantize(const QuantGroupsArgs& a, cudaStream_t s, const CopyTokensArgs* window = nullptr);
 
 // ---- paged, variable-length KIVI cache ----
 // Per-sequence state travels in the kernel parameters (at most kMaxPagedSeqs
