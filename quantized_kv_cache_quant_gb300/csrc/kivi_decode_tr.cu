@@ -86,26 +86,6 @@ struct TrSmem {
   static_assert(kTrStages * KiviTr<D, KB, VB>::STAGE >= 32 * WIN_ROW, "a warp's stages hold one window chunk");
 };
 
-// Transpose of an 8 x 8 fp16 tile held in mma fragment order across the warp:
-// lane (g, t) holds row g, columns 2t and 2t + 1 before and after.
-__device__ __forceinline__ uint32_t movm_trans(uint32_t x) {
-  uint32_t y;
-  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
-  return y;
-}
-
-// Reductions over the eight lanes that share t = lane % 4 (one query head's tokens).
-__device__ __forceinline__ float col_max(float v) {
-  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
-  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
-  return fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
-}
-__device__ __forceinline__ float col_sum(float v) {
-  v += __shfl_xor_sync(0xffffffffu, v, 4);
-  v += __shfl_xor_sync(0xffffffffu, v, 8);
-  return v + __shfl_xor_sync(0xffffffffu, v, 16);
-}
-
 // The online softmax step for query head t = lane % 4 over this thread's four
 // scores (tokens g, g + 8, g + 16, g + 24 of the group or chunk), log2 units,
 // with the lazy rescale of the decode kernel (the reference maximum moves only

@@ -248,6 +248,27 @@ __device__ __forceinline__ float quad_sum(float v) {
   return v + __shfl_xor_sync(0xffffffffu, v, 2);
 }
 
+// Max and sum over the eight lanes that share t = lane % 4 (one column of an
+// mma fragment: in the swapped-operand decodes, one query head's tokens).
+__device__ __forceinline__ float col_max(float v) {
+  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+  return fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+}
+__device__ __forceinline__ float col_sum(float v) {
+  v += __shfl_xor_sync(0xffffffffu, v, 4);
+  v += __shfl_xor_sync(0xffffffffu, v, 8);
+  return v + __shfl_xor_sync(0xffffffffu, v, 16);
+}
+
+// Transpose of an 8 x 8 fp16 tile held in mma fragment order across the warp:
+// lane (g, t) holds row g, columns 2t and 2t + 1 before and after.
+__device__ __forceinline__ uint32_t movm_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
 __device__ __forceinline__ void report_timeout(uint32_t* status) {
   if (status != nullptr) atomicOr(status, kStatusTimeout);
 }

@@ -319,26 +319,6 @@ constexpr float kNvfp4MaxSlack = 8.0f;
 #define KVQ_NVFP4_SWAP_MIN_BLOCKS 4  // resident swapped-operand decode blocks per SM the registers are sized for
 #endif
 
-// Transpose of an 8 x 8 fp16 tile held in mma fragment order across the warp:
-// lane (g, t) holds row g, columns 2t and 2t + 1 before and after.
-__device__ __forceinline__ uint32_t tile_trans(uint32_t x) {
-  uint32_t y;
-  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
-  return y;
-}
-
-// Max and sum over the eight lanes that share t = lane % 4.
-__device__ __forceinline__ float column_max(float v) {
-  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
-  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
-  return fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
-}
-__device__ __forceinline__ float column_sum(float v) {
-  v += __shfl_xor_sync(0xffffffffu, v, 4);
-  v += __shfl_xor_sync(0xffffffffu, v, 8);
-  return v + __shfl_xor_sync(0xffffffffu, v, 16);
-}
-
 // Byte k (0..3, a compile-time value after unrolling) of w -> fp16x2.
 __device__ __forceinline__ uint32_t e2m1_byte(uint32_t w, int k) {
   switch (k) {
@@ -561,15 +541,15 @@ __global__ void __launch_bounds__(128, kSwap ? KVQ_NVFP4_SWAP_MIN_BLOCKS : 1) nv
         if (tok_base + g >= len) sc0 = -INFINITY;
         if (tok_base + 8 + g >= len) sc1 = -INFINITY;
       }
-      rescale(column_max(fmaxf(sc0, sc1)));
+      rescale(col_max(fmaxf(sc0, sc1)));
       const float p0 = fast_exp2(sc0 - m_run), p1 = fast_exp2(sc1 - m_run);
       l_run += p0 + p1;
       // p = hi + lo in columns 2tig, 2tig + 1 of token rows g and g + 8, transposed
       // into the B fragments (k = tokens 2tig, +1 and 2tig + 8, +9; column g)
       const __half hi0 = __float2half_rn(p0), hi1 = __float2half_rn(p1);
       const __half lo0 = __float2half_rn(p0 - __half2float(hi0)), lo1 = __float2half_rn(p1 - __half2float(hi1));
-      const uint32_t B0 = tile_trans(h2_bits(__halves2half2(hi0, lo0)));
-      const uint32_t B1 = tile_trans(h2_bits(__halves2half2(hi1, lo1)));
+      const uint32_t B0 = movm_trans(h2_bits(__halves2half2(hi0, lo0)));
+      const uint32_t B1 = movm_trans(h2_bits(__halves2half2(hi1, lo1)));
       // p.V: rows = channels 16mt + g, + 8 (stream bytes 0, 2 / 1, 3 of word mt), k = tokens
 #pragma unroll
       for (int mt = 0; mt < NACC; ++mt) {
@@ -610,7 +590,7 @@ __global__ void __launch_bounds__(128, kSwap ? KVQ_NVFP4_SWAP_MIN_BLOCKS : 1) nv
     }
   } else {
     // head tig: channels 16mt + g (columns hi, lo) and 16mt + 8 + g; rows gq.. of the warp's 8 are unused
-    l_run = column_sum(l_run);
+    l_run = col_sum(l_run);
 #pragma unroll
     for (int mt = 0; mt < NACC; ++mt) {
       o_s[(warp * 8 + tig) * D + 16 * mt + g] = (o_acc[mt][0] + o_acc[mt][1]) * vscale;
